@@ -1,0 +1,292 @@
+"""Plain fp64 CPU oracle for fused linear cross-entropy and the standalone row-wise CE kernel.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import or call this module: only the
+tests, the smoke check and the benchmark's CPU-baseline leg use it.  It shares no code with the CUDA
+library and imports nothing from the package.
+
+Every function here is the textbook definition written out in float64, in the notation of
+"Fused Linear Cross-Entropy: The Math, the Memory Wall, and Two Ways Around It" (p1) and
+"Greyhound -- Cross-Entropy" (p3).  Inputs are bf16 bit patterns (uint16) or float arrays; they are
+widened exactly to float64 before any arithmetic.
+
+Definitions followed (page, section):
+  * logits z = W . hidden[t] (+ b), p = softmax(z), l_t = -z_y + LSE(z)       p1 "The setting"
+  * L = (1/n_valid) sum_t l_t [y_t != -100] (mean); the plain sum for "sum"   p1 "The setting";
+                                                                              p2 "Forward pass" (mean, sum)
+  * dl_t/dz = softmax(z) - onehot(y_t)  (boxed identity)                      p1 "The identity that makes
+                                                                                 fused fwbw possible"
+  * LSE = max z + log sum exp(z - max z)                                      same section, consequence 3
+  * dlogits[t,:] = (1/n_valid) [y_t != -100] (softmax(z_t) - onehot(y_t));
+    grad_input = dlogits . W;  grad_W = dlogits^T . hidden;
+    grad_b = sum_t dlogits[t,:]                                               p1 "From dlogits to
+                                                                                 grad_input and grad_W"
+  * z_i = LSE_i^2 (z-loss), its gradient scales the softmax term before the
+    target column is adjusted                                                 p3 formulas, "Loss and
+                                                                                 gradient together"
+  * loss = ce_sum / max(n_valid, 1)                                           p3 "Usage" (raw helper)
+
+Readings where the pages are silent (each also listed in the design notes):
+  * with z-loss in the fused loss, l_t = LSE_t - z_y + z_loss * LSE_t^2, so the gradient row is
+    p * (1 + 2 z_loss LSE_t) - onehot(y_t);
+  * n_valid = 0 gives loss 0 and all-zero gradients (the clamp of p3 "Usage");
+  * a target outside [0, V) that is not ignore_index is treated as ignored;
+  * z_sum of the standalone CE is the unscaled sum of LSE^2 over valid rows.
+
+Rows are processed in blocks only to bound memory: the loss is a sum over tokens and both gradients
+are sums of per-token terms, and p1 ("The identity ...", consequence 2) states that this sum commutes
+with chunking over tokens.  No other blocking, fusion or reordering is done.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "widen", "logits", "lse", "flce_reference", "flce_lse", "flce_sampled", "flce_reference_loops",
+    "ce_reference", "ce_reference_loops",
+]
+
+
+def widen(x) -> np.ndarray:
+    """bf16 bit patterns (uint16) or any float array -> float64, exactly."""
+    a = np.asarray(x)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def logits(hidden, W, bias=None) -> np.ndarray:
+    """z = hidden . W^T (+ b) in float64 (p1 "The setting": z = W . hidden[t])."""
+    z = widen(hidden) @ widen(W).T
+    if bias is not None:
+        z = z + widen(bias)[None, :]
+    return z
+
+
+def lse(z: np.ndarray) -> np.ndarray:
+    """Row-wise log-sum-exp, LSE = max z + log sum exp(z - max z) (p1, consequence 3)."""
+    m = np.max(z, axis=-1)
+    return m + np.log(np.sum(np.exp(z - m[..., None]), axis=-1))
+
+
+def _valid_mask(target: np.ndarray, V: int, ignore_index: int) -> np.ndarray:
+    t = np.asarray(target, dtype=np.int64)
+    return (t != ignore_index) & (t >= 0) & (t < V)
+
+
+def _scale(n_valid: int, reduction: str) -> float:
+    if reduction == "mean":
+        return 1.0 / max(n_valid, 1)
+    if reduction == "sum":
+        return 1.0
+    raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
+
+
+def flce_reference(hidden, W, target, bias=None, ignore_index: int = -100, reduction: str = "mean",
+                   z_loss: float = 0.0, want_grads: bool = True, row_block: int = 512) -> dict:
+    """Loss and gradients of fused linear cross-entropy, straight from the definitions.
+
+    Returns a dict with ``loss`` (float), ``n_valid`` (int), ``lse`` [BT], and when ``want_grads``
+    ``grad_input`` [BT, H], ``grad_W`` [V, H], ``grad_bias`` [V] (None without a bias), all float64.
+    """
+    h = widen(hidden)
+    w = widen(W)
+    b = None if bias is None else widen(bias)
+    t = np.asarray(target, dtype=np.int64)
+    BT, H = h.shape
+    V = w.shape[0]
+    valid = _valid_mask(t, V, ignore_index)
+    n_valid = int(valid.sum())
+    s = _scale(n_valid, reduction)
+
+    loss_terms = []
+    lse_all = np.empty(BT)
+    if want_grads:
+        grad_input = np.zeros((BT, H))
+        grad_W = np.zeros((V, H))
+        grad_b = np.zeros(V) if b is not None else None
+    for r0 in range(0, BT, row_block):
+        r1 = min(BT, r0 + row_block)
+        rows = np.arange(r1 - r0)
+        z = h[r0:r1] @ w.T
+        if b is not None:
+            z += b[None, :]
+        m = z.max(axis=1)
+        e = np.exp(z - m[:, None])
+        denom = e.sum(axis=1)
+        L = m + np.log(denom)
+        lse_all[r0:r1] = L
+        v = valid[r0:r1]
+        y = np.where(v, t[r0:r1], 0)
+        z_y = z[rows, y]
+        loss_terms.append(np.where(v, (L - z_y) + z_loss * L * L, 0.0))
+        if want_grads:
+            p = e / denom[:, None]
+            d = p * (1.0 + 2.0 * z_loss * L)[:, None]
+            d[rows, y] -= 1.0
+            d *= (s * v)[:, None]
+            grad_input[r0:r1] = d @ w
+            grad_W += d.T @ h[r0:r1]
+            if grad_b is not None:
+                grad_b += d.sum(axis=0)
+    loss = s * math.fsum(np.concatenate(loss_terms).tolist()) if loss_terms else 0.0
+    out = dict(loss=loss, n_valid=n_valid, lse=lse_all)
+    if want_grads:
+        out.update(grad_input=grad_input, grad_W=grad_W, grad_bias=grad_b)
+    return out
+
+
+def flce_lse(hidden, W, bias=None, row_block: int = 512) -> np.ndarray:
+    """LSE of every row of z = hidden . W^T (+ b), float64, without gradients."""
+    h = widen(hidden)
+    w = widen(W)
+    b = None if bias is None else widen(bias)
+    out = np.empty(h.shape[0])
+    for r0 in range(0, h.shape[0], row_block):
+        z = h[r0:r0 + row_block] @ w.T
+        if b is not None:
+            z += b[None, :]
+        out[r0:r0 + row_block] = lse(z)
+    return out
+
+
+def flce_sampled(hidden, W, target, lse_all, rows, vocab_rows, bias=None, ignore_index: int = -100,
+                 reduction: str = "mean", z_loss: float = 0.0) -> dict:
+    """Selected outputs of the fused path, given the float64 LSE of every row (from ``flce_lse``).
+
+    * ``loss`` over all rows (needs only LSE and z_y),
+    * ``grad_input[rows]``: dlogits rows times W,
+    * ``grad_W[vocab_rows]`` and ``grad_bias[vocab_rows]``: the dlogits columns of those vocabulary
+      entries (over every token) times hidden.
+    All from the same definitions as ``flce_reference``.
+    """
+    h = widen(hidden)
+    w = widen(W)
+    b = None if bias is None else widen(bias)
+    t = np.asarray(target, dtype=np.int64)
+    BT, H = h.shape
+    V = w.shape[0]
+    L = np.asarray(lse_all, dtype=np.float64)
+    valid = _valid_mask(t, V, ignore_index)
+    n_valid = int(valid.sum())
+    s = _scale(n_valid, reduction)
+    y = np.where(valid, t, 0)
+
+    # z_y for every row: hidden[t] . W[y_t] (+ b[y_t])
+    z_y = np.einsum("ij,ij->i", h, w[y])
+    if b is not None:
+        z_y += b[y]
+    loss = s * math.fsum(np.where(valid, (L - z_y) + z_loss * L * L, 0.0).tolist())
+
+    rows = np.asarray(rows, dtype=np.int64)
+    z = h[rows] @ w.T
+    if b is not None:
+        z += b[None, :]
+    d = np.exp(z - L[rows][:, None]) * (1.0 + 2.0 * z_loss * L[rows])[:, None]
+    d[np.arange(len(rows)), y[rows]] -= 1.0
+    d *= (s * valid[rows])[:, None]
+    gi = d @ w
+
+    vr = np.asarray(vocab_rows, dtype=np.int64)
+    zc = h @ w[vr].T                       # [BT, len(vr)] logits columns of the chosen entries
+    if b is not None:
+        zc += b[vr][None, :]
+    dc = np.exp(zc - L[:, None]) * (1.0 + 2.0 * z_loss * L)[:, None]
+    dc -= ((y[:, None] == vr[None, :]) & valid[:, None]).astype(np.float64)
+    dc *= (s * valid)[:, None]
+    gw = dc.T @ h
+    gb = dc.sum(axis=0) if b is not None else None
+    return dict(loss=loss, n_valid=n_valid, grad_input_rows=gi, grad_W_rows=gw, grad_bias_rows=gb)
+
+
+def flce_reference_loops(hidden, W, target, bias=None, ignore_index: int = -100,
+                         reduction: str = "mean", z_loss: float = 0.0) -> dict:
+    """The same definitions with explicit Python loops and ``math`` scalars (tiny shapes only).
+
+    Materialises the full logits, softmax and dlogits matrices element by element, as the naive path
+    of p1 "The engineering wall" does, so it can check the vectorised oracle by brute force.
+    """
+    h = widen(hidden)
+    w = widen(W)
+    b = None if bias is None else widen(bias)
+    t = [int(x) for x in np.asarray(target)]
+    BT, H = h.shape
+    V = w.shape[0]
+    valid = [(y != ignore_index) and (0 <= y < V) for y in t]
+    n_valid = sum(valid)
+    s = _scale(n_valid, reduction)
+    Z = [[math.fsum(float(h[i, k]) * float(w[j, k]) for k in range(H)) + (float(b[j]) if b is not None else 0.0)
+          for j in range(V)] for i in range(BT)]
+    loss_terms = []
+    D = [[0.0] * V for _ in range(BT)]
+    lse_rows = []
+    for i in range(BT):
+        m = max(Z[i])
+        L = m + math.log(math.fsum(math.exp(zj - m) for zj in Z[i]))
+        lse_rows.append(L)
+        if not valid[i]:
+            continue
+        loss_terms.append(L - Z[i][t[i]] + z_loss * L * L)
+        for j in range(V):
+            pj = math.exp(Z[i][j] - L)
+            D[i][j] = s * (pj * (1.0 + 2.0 * z_loss * L) - (1.0 if j == t[i] else 0.0))
+    gi = np.array([[math.fsum(D[i][j] * float(w[j, k]) for j in range(V)) for k in range(H)] for i in range(BT)])
+    gw = np.array([[math.fsum(D[i][j] * float(h[i, k]) for i in range(BT)) for k in range(H)] for j in range(V)])
+    gb = np.array([math.fsum(D[i][j] for i in range(BT)) for j in range(V)]) if b is not None else None
+    return dict(loss=s * math.fsum(loss_terms), n_valid=n_valid, lse=np.array(lse_rows), grad_input=gi,
+                grad_W=gw, grad_bias=gb, dlogits=np.array(D))
+
+
+def ce_reference(logits_, labels, ignore_index: int = -100, z_loss: float = 0.0,
+                 row_block: int = 256) -> dict:
+    """Standalone row-wise cross-entropy with its logits gradient (p3 "Cross-Entropy").
+
+    Per row: loss_i = LSE(logits_i) - logits_{i, y_i}; z_i = LSE_i^2.  Returns ``ce_sum`` and
+    ``z_sum`` over valid rows, ``n_valid``, ``lse`` and ``dlogits`` = p * (1 + 2 z_loss LSE) - onehot(y)
+    on valid rows and 0 on ignored rows (the gradient of ce_sum + z_loss * z_sum).
+    """
+    x = np.asarray(logits_)
+    lab = np.asarray(labels, dtype=np.int64)
+    B, V = x.shape
+    valid = _valid_mask(lab, V, ignore_index)
+    y = np.where(valid, lab, 0)
+    ce_terms, z_terms = [], []
+    dl = np.zeros((B, V))
+    lse_all = np.empty(B)
+    for r0 in range(0, B, row_block):
+        r1 = min(B, r0 + row_block)
+        rows = np.arange(r1 - r0)
+        z = widen(x[r0:r1])
+        L = lse(z)
+        lse_all[r0:r1] = L
+        v = valid[r0:r1]
+        ce_terms.append(np.where(v, L - z[rows, y[r0:r1]], 0.0))
+        z_terms.append(np.where(v, L * L, 0.0))
+        d = np.exp(z - L[:, None]) * (1.0 + 2.0 * z_loss * L)[:, None]
+        d[rows, y[r0:r1]] -= 1.0
+        dl[r0:r1] = d * v[:, None]
+    ce_sum = math.fsum(np.concatenate(ce_terms).tolist()) if ce_terms else 0.0
+    z_sum = math.fsum(np.concatenate(z_terms).tolist()) if z_terms else 0.0
+    return dict(ce_sum=ce_sum, z_sum=z_sum, n_valid=int(valid.sum()), lse=lse_all, dlogits=dl)
+
+
+def ce_reference_loops(logits_, labels, ignore_index: int = -100, z_loss: float = 0.0) -> dict:
+    """Element-by-element version of ``ce_reference`` for tiny inputs."""
+    x = widen(logits_)
+    B, V = x.shape
+    ce_sum, z_sum, n_valid = [], [], 0
+    D = np.zeros((B, V))
+    for i in range(B):
+        y = int(labels[i])
+        if y == ignore_index or not (0 <= y < V):
+            continue
+        n_valid += 1
+        row = [float(v) for v in x[i]]
+        m = max(row)
+        L = m + math.log(math.fsum(math.exp(v - m) for v in row))
+        ce_sum.append(L - row[y])
+        z_sum.append(L * L)
+        for j in range(V):
+            D[i, j] = math.exp(row[j] - L) * (1.0 + 2.0 * z_loss * L) - (1.0 if j == y else 0.0)
+    return dict(ce_sum=math.fsum(ce_sum), z_sum=math.fsum(z_sum), n_valid=n_valid, dlogits=D)

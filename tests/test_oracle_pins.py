@@ -1,0 +1,277 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+  * brute force: the element-by-element loop version of the same definitions;
+  * calculus: central finite differences of the loss against the analytic gradients
+    (the boxed identity dl/dz = softmax - onehot of "Fused Linear Cross-Entropy", "The identity ...");
+  * an independent library: torch.nn.functional.cross_entropy in float64 on the CPU, with autograd;
+  * closed forms: W = 0, V = 1, and the hand-evaluated values in tests/golden/ce_closed_forms.txt;
+  * invariants: LSE shift, dlogits row sums, ignored rows, n_valid = 0, vocabulary permutation.
+
+The same checks run against deliberately broken copies of the oracle (test_planted_mistakes) to show
+that a dropped term, a wrong sign, a wrong index or a wrong scale fails at least one of them.
+"""
+from __future__ import annotations
+
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.flce_oracle as ORACLE
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rel(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    scale = max(float(np.max(np.abs(b))) if b.size else 0.0, 1e-300)
+    return float(np.max(np.abs(a - b))) / scale if b.size else 0.0
+
+
+def _tiny_case(seed=1, BT=6, H=5, V=7, bias=True, ignore_rows=(2,), logit_scale=1.0):
+    rng = np.random.default_rng(seed)
+    hidden = rng.standard_normal((BT, H)) * logit_scale
+    W = rng.standard_normal((V, H))
+    b = rng.standard_normal(V) if bias else None
+    t = rng.integers(0, V, BT)
+    for r in ignore_rows:
+        t[r] = -100
+    return hidden, W, b, t
+
+
+# ----------------------------------------------------------------------------- pins (parameterised
+# by the oracle module so that planted-mistake copies can be run through them)
+
+def pin_loops_vs_vectorised(orc):
+    for reduction in ("mean", "sum"):
+        for zl in (0.0, 1e-2):
+            hidden, W, b, t = _tiny_case()
+            ref = orc.flce_reference_loops(hidden, W, t, bias=b, reduction=reduction, z_loss=zl)
+            got = orc.flce_reference(hidden, W, t, bias=b, reduction=reduction, z_loss=zl, row_block=4)
+            assert abs(got["loss"] - ref["loss"]) <= 1e-12 * abs(ref["loss"])
+            assert got["n_valid"] == ref["n_valid"]
+            for k in ("grad_input", "grad_W", "grad_bias", "lse"):
+                assert _rel(got[k], ref[k]) < 1e-12, k
+
+
+def pin_finite_differences(orc):
+    h_step = 1e-6
+    for reduction, zl in (("mean", 1e-2), ("sum", 0.0), ("mean", 0.0)):
+        hidden, W, b, t = _tiny_case(seed=3)
+        t[4] = 11  # out of range: read as ignored
+        g = orc.flce_reference(hidden, W, t, bias=b, reduction=reduction, z_loss=zl, row_block=4)
+
+        def loss_at(hh, ww, bb):
+            return orc.flce_reference(hh, ww, t, bias=bb, reduction=reduction, z_loss=zl,
+                                      want_grads=False, row_block=4)["loss"]
+
+        for name, arr, grad in (("hidden", hidden, g["grad_input"]), ("W", W, g["grad_W"]),
+                                ("bias", b, g["grad_bias"])):
+            fd = np.zeros_like(arr)
+            for idx in np.ndindex(arr.shape):
+                plus = arr.copy()
+                minus = arr.copy()
+                plus[idx] += h_step
+                minus[idx] -= h_step
+                args_p = {"hidden": (plus, W, b), "W": (hidden, plus, b), "bias": (hidden, W, plus)}[name]
+                args_m = {"hidden": (minus, W, b), "W": (hidden, minus, b), "bias": (hidden, W, minus)}[name]
+                fd[idx] = (loss_at(*args_p) - loss_at(*args_m)) / (2 * h_step)
+            assert _rel(grad, fd) < 1e-6, (name, reduction, zl)
+
+
+def pin_torch_fp64(orc):
+    for reduction in ("mean", "sum"):
+        for zl in (0.0, 1e-3):
+            hidden, W, b, t = _tiny_case(seed=5, BT=37, H=16, V=50, ignore_rows=(0, 9, 30))
+            got = orc.flce_reference(hidden, W, t, bias=b, reduction=reduction, z_loss=zl, row_block=8)
+            th = torch.tensor(hidden, requires_grad=True)
+            tw = torch.tensor(W, requires_grad=True)
+            tb = torch.tensor(b, requires_grad=True)
+            tt = torch.tensor(t)
+            z = th @ tw.T + tb
+            ce = torch.nn.functional.cross_entropy(z, tt, ignore_index=-100, reduction=reduction)
+            valid = (tt != -100).double()
+            scale = 1.0 / valid.sum() if reduction == "mean" else 1.0
+            loss = ce + zl * scale * (torch.logsumexp(z, dim=1) ** 2 * valid).sum()
+            loss.backward()
+            assert abs(got["loss"] - loss.item()) <= 1e-12 * abs(loss.item())
+            assert _rel(got["grad_input"], th.grad.numpy()) < 1e-10
+            assert _rel(got["grad_W"], tw.grad.numpy()) < 1e-10
+            assert _rel(got["grad_bias"], tb.grad.numpy()) < 1e-10
+            assert _rel(got["lse"], torch.logsumexp(z, dim=1).detach().numpy()) < 1e-13
+
+
+def pin_closed_forms(orc):
+    # W = 0, no bias: z = 0, LSE = log V, grad_input = 0,
+    # grad_W[n] = s * sum_valid ((1 + 2 zl log V)/V - [y_t = n]) hidden[t]
+    rng = np.random.default_rng(7)
+    BT, H, V, zl = 9, 4, 7, 1e-2
+    hidden = rng.standard_normal((BT, H))
+    t = rng.integers(0, V, BT)
+    t[3] = -100
+    g = orc.flce_reference(hidden, np.zeros((V, H)), t, z_loss=zl, row_block=4)
+    valid = t != -100
+    n = int(valid.sum())
+    lv = math.log(V)
+    assert abs(g["loss"] - (lv + zl * lv * lv)) < 1e-13
+    assert np.all(g["grad_input"] == 0.0)
+    expect = np.zeros((V, H))
+    for i in range(BT):
+        if valid[i]:
+            for j in range(V):
+                expect[j] += ((1 + 2 * zl * lv) / V - (1.0 if j == t[i] else 0.0)) * hidden[i] / n
+    assert _rel(g["grad_W"], expect) < 1e-12
+    # V = 1: the CE part vanishes; loss = s * sum_valid zl z^2; grad row = s * 2 zl z * W[0]
+    W1 = rng.standard_normal((1, H))
+    t1 = np.zeros(BT, dtype=np.int64)
+    t1[5] = -100
+    g1 = orc.flce_reference(hidden, W1, t1, z_loss=zl, reduction="sum", row_block=4)
+    z = hidden @ W1[0]
+    v1 = t1 != -100
+    assert abs(g1["loss"] - zl * float(np.sum(z[v1] ** 2))) < 1e-12
+    assert _rel(g1["grad_input"], (2 * zl * z * v1)[:, None] * W1[0][None, :]) < 1e-12
+    # golden closed-form CE values
+    with open(os.path.join(GOLDEN, "ce_closed_forms.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            name, logit_s, tgt, lse_s, loss_s = [x.strip() for x in line.split("|")]
+            if "*" in logit_s:
+                val, cnt = logit_s.split("*")
+                row = [float(val)] * int(cnt)
+            else:
+                row = [float(x) for x in logit_s.split(",")]
+            r = orc.ce_reference(np.array([row]), np.array([int(tgt)]))
+            assert abs(r["lse"][0] - float(lse_s)) < 1e-14 * max(1.0, float(lse_s)), name
+            assert abs(r["ce_sum"] - float(loss_s)) < 1e-14 * max(1.0, float(loss_s)), name
+
+
+def pin_invariants(orc):
+    hidden, W, b, t = _tiny_case(seed=11, BT=10, H=6, V=9, ignore_rows=(1, 7))
+    # LSE shift: a constant added to every bias entry shifts LSE and leaves loss / grads (zl = 0)
+    g0 = orc.flce_reference(hidden, W, t, bias=b, row_block=3)
+    g1 = orc.flce_reference(hidden, W, t, bias=b + 3.25, row_block=3)
+    assert _rel(g1["lse"] - 3.25, g0["lse"]) < 1e-13
+    assert abs(g1["loss"] - g0["loss"]) < 1e-12
+    for k in ("grad_input", "grad_W", "grad_bias"):
+        assert _rel(g1[k], g0[k]) < 1e-11, k
+    # dlogits row sums: 0 with zl = 0, s * 2 zl LSE on valid rows with zl > 0 (summed: grad_bias)
+    zl = 0.05
+    for reduction in ("mean", "sum"):
+        g = orc.flce_reference(hidden, W, t, bias=b, z_loss=zl, reduction=reduction, row_block=3)
+        valid = t != -100
+        s = 1.0 / valid.sum() if reduction == "mean" else 1.0
+        assert abs(g["grad_bias"].sum() - s * 2 * zl * g["lse"][valid].sum()) < 1e-12
+    assert abs(g0["grad_bias"].sum()) < 1e-13
+    # ignored rows: zero grad_input rows; changing them changes nothing else
+    assert np.all(g0["grad_input"][[1, 7]] == 0.0)
+    h2 = hidden.copy()
+    h2[[1, 7]] += 5.0
+    g2 = orc.flce_reference(h2, W, t, bias=b, row_block=3)
+    assert abs(g2["loss"] - g0["loss"]) < 1e-13
+    assert _rel(g2["grad_W"], g0["grad_W"]) < 1e-13
+    assert _rel(g2["grad_bias"], g0["grad_bias"]) < 1e-13
+    # n_valid = 0: loss 0, all gradients 0
+    gz = orc.flce_reference(hidden, W, np.full_like(t, -100), bias=b, z_loss=zl, row_block=3)
+    assert gz["n_valid"] == 0 and gz["loss"] == 0.0
+    for k in ("grad_input", "grad_W", "grad_bias"):
+        assert np.all(gz[k] == 0.0)
+    # vocabulary permutation: permute W rows, bias and relabel targets
+    perm = np.random.default_rng(0).permutation(W.shape[0])
+    inv = np.argsort(perm)
+    tp = np.where(t == -100, -100, inv[np.where(t == -100, 0, t)])
+    gp = orc.flce_reference(hidden, W[perm], tp, bias=b[perm], row_block=3)
+    assert abs(gp["loss"] - g0["loss"]) < 1e-12
+    assert _rel(gp["grad_W"], g0["grad_W"][perm]) < 1e-12
+    assert _rel(gp["grad_bias"], g0["grad_bias"][perm]) < 1e-12
+    assert _rel(gp["grad_input"], g0["grad_input"]) < 1e-12
+
+
+def pin_ce(orc):
+    rng = np.random.default_rng(13)
+    B, V, zl = 11, 23, 1e-2
+    x = rng.standard_normal((B, V)) * 2
+    lab = rng.integers(0, V, B)
+    lab[[2, 8]] = -100
+    got = orc.ce_reference(x, lab, z_loss=zl, row_block=4)
+    loops = orc.ce_reference_loops(x, lab, z_loss=zl)
+    assert abs(got["ce_sum"] - loops["ce_sum"]) < 1e-12 * abs(loops["ce_sum"])
+    assert abs(got["z_sum"] - loops["z_sum"]) < 1e-12 * abs(loops["z_sum"])
+    assert got["n_valid"] == loops["n_valid"] == B - 2
+    assert _rel(got["dlogits"], loops["dlogits"]) < 1e-12
+    tx = torch.tensor(x, requires_grad=True)
+    tl = torch.tensor(lab)
+    ce = torch.nn.functional.cross_entropy(tx, tl, ignore_index=-100, reduction="sum")
+    valid = (tl != -100).double()
+    zs = (torch.logsumexp(tx, dim=1) ** 2 * valid).sum()
+    (ce + zl * zs).backward()
+    assert abs(got["ce_sum"] - ce.item()) < 1e-12 * abs(ce.item())
+    assert abs(got["z_sum"] - zs.item()) < 1e-12 * abs(zs.item())
+    assert _rel(got["dlogits"], tx.grad.numpy()) < 1e-12
+    assert np.all(got["dlogits"][[2, 8]] == 0.0)
+
+
+def pin_sampled_matches_full(orc):
+    hidden, W, b, t = _tiny_case(seed=17, BT=40, H=12, V=33, ignore_rows=(3, 4, 20))
+    zl = 1e-3
+    full = orc.flce_reference(hidden, W, t, bias=b, z_loss=zl, row_block=7)
+    L = orc.flce_lse(hidden, W, bias=b, row_block=6)
+    assert _rel(L, full["lse"]) < 1e-14
+    rows = [0, 3, 17, 39]
+    vrows = [0, 5, 32]
+    smp = orc.flce_sampled(hidden, W, t, L, rows, vrows, bias=b, z_loss=zl)
+    assert abs(smp["loss"] - full["loss"]) < 1e-12 * abs(full["loss"])
+    assert _rel(smp["grad_input_rows"], full["grad_input"][rows]) < 1e-12
+    assert _rel(smp["grad_W_rows"], full["grad_W"][vrows]) < 1e-12
+    assert _rel(smp["grad_bias_rows"], full["grad_bias"][vrows]) < 1e-12
+
+
+PINS = [pin_loops_vs_vectorised, pin_finite_differences, pin_torch_fp64, pin_closed_forms,
+        pin_invariants, pin_ce, pin_sampled_matches_full]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_oracle_pin(pin):
+    pin(ORACLE)
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+
+MUTATIONS = {
+    "z-loss factor dropped from gradient": ("d = p * (1.0 + 2.0 * z_loss * L)[:, None]", "d = p * (1.0 + z_loss * L)[:, None]"),
+    "onehot sign flipped": ("            d[rows, y] -= 1.0\n            d *= (s * v)", "            d[rows, y] += 1.0\n            d *= (s * v)"),
+    "grad_W accumulation dropped": ("grad_W += d.T @ h[r0:r1]", "grad_W = d.T @ h[r0:r1]"),
+    "max term dropped from LSE": ("L = m + np.log(denom)", "L = np.log(denom)"),
+    "z-loss term not squared": ("(L - z_y) + z_loss * L * L, 0.0))\n        if want_grads", "(L - z_y) + z_loss * L, 0.0))\n        if want_grads"),
+    "target index shifted": ("y = np.where(v, t[r0:r1], 0)", "y = np.where(v, t[r0:r1], 0)[::-1]"),
+    "mean over all rows": ("    n_valid = int(valid.sum())\n    s = _scale(n_valid, reduction)\n\n    loss_terms", "    n_valid = int(valid.sum())\n    s = _scale(BT, reduction)\n\n    loss_terms"),
+    "bias sign flipped": ("        z = h[r0:r1] @ w.T\n        if b is not None:\n            z += b[None, :]\n        m = z.max", "        z = h[r0:r1] @ w.T\n        if b is not None:\n            z -= b[None, :]\n        m = z.max"),
+    "ignored CE rows not zeroed": ("dl[r0:r1] = d * v[:, None]", "dl[r0:r1] = d"),
+    "CE target column not adjusted": ("        d[rows, y[r0:r1]] -= 1.0\n        dl[r0:r1]", "        dl[r0:r1]"),
+    "grad_input uses transposed product": ("grad_input[r0:r1] = d @ w", "grad_input[r0:r1] = (w.T @ d.T).T * 0 + d @ w[::-1]"),
+}
+
+
+def _mutated_oracle(src: str, old: str, new: str):
+    assert src.count(old) == 1, f"mutation anchor must be unique: {old!r}"
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src.replace(old, new), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistakes(name):
+    with open(ORACLE.__file__) as f:
+        src = f.read()
+    mutant = _mutated_oracle(src, *MUTATIONS[name])
+    failures = 0
+    for pin in PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError, IndexError):
+            failures += 1
+    assert failures > 0, f"no pin caught the planted mistake: {name}"
