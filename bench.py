@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Benchmark of the fused linear cross-entropy library on one GB300 (or N independent replicas).
+
+One step = one flce_fwd_bwd call (every pass: LSE tiles, merge, loss reduction, grad_input pass,
+grad_W pass) over one batch of the long-batch LM-head workload (BT=65535, H=1024, V=176245, bf16,
+seeded synthetic inputs, mean reduction).  Prints ONE JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Timing: W untimed steps, then K steps bracketed by a barrier and torch.cuda.synchronize() on both
+sides, measured with CUDA events on the launching stream; the maximum over ranks is reported.
+The inputs (hidden 128 MiB + W 344 MiB) are larger than the 126 MB L2, so no explicit flush is done.
+Per-kernel times come from CUDA events the library records at its pass boundaries inside the same
+timed region (flce_fwd_bwd_timed).  ``--impl reference`` times the fp64 CPU oracle instead, on
+bounded row samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_cross_entropy_tma_gb300 import workloads as wl  # noqa: E402
+
+# verl _Split_Dlogits_N, tuned: 356 ms fwd+bwd at BT=65535, H=1024, V=176245 on an H100 ("Fused Linear
+# Cross-Entropy", "Putting numbers on it") -> 65535 / 0.356 s tokens/s.  Another machine: context only.
+PAGES_TOKENS_PER_S = {"long": 65535 / 0.356}
+KERNELS_PER_STEP = 5  # lse_partial, lse_merge, loss_reduce, dgrad(grad_input), dgrad(grad_W)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "linear_cross_entropy_tma_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str, workload: str, src_digest: str):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if the kernel source has not
+    changed since the counters were taken; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_digest") != src_digest:
+        return None
+    return e["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling (200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        with open(self.out.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.out.name)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def to_device_bf16(bits, device):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+# ----------------------------------------------------------------------------------- our arm
+def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local: int, peaks: dict):
+    import torch
+    import linear_cross_entropy_tma_gb300 as flce
+
+    dev = torch.device("cuda", local)
+    d = wl.make_fused_inputs(w)
+    hidden = to_device_bf16(d["hidden"], dev)
+    W = to_device_bf16(d["W"], dev)
+    target = torch.from_numpy(d["target"]).to(dev)
+    bias = torch.from_numpy(d["bias"]).to(dev) if d["bias"] is not None else None
+    out = {"loss": torch.empty(1, device=dev), "n_valid": torch.empty(1, dtype=torch.int64, device=dev),
+           "grad_input": torch.empty((w.BT, w.H), dtype=torch.bfloat16, device=dev),
+           "grad_W": torch.empty((w.V, w.H), dtype=torch.float32, device=dev)}
+    if bias is not None:
+        out["grad_bias"] = torch.empty(w.V, device=dev)
+    ws = torch.empty(flce.workspace_size(w.BT, w.H, w.V), dtype=torch.uint8, device=dev)
+    kw = dict(bias=bias, reduction=w.reduction, z_loss=w.z_loss, workspace=ws, out=out)
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+
+    pass_ev = [[ev() for _ in range(5)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(warmup):
+        flce.flce_fwd_bwd(hidden, W, target, **kw)
+    torch.cuda.synchronize()
+    assert flce.read_device_status(ws) == 0, "device status word non-zero after warm-up"
+
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for k in range(steps):
+        flce.flce_fwd_bwd(hidden, W, target, pass_events=pass_ev[k], **kw)
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    peak_mem = torch.cuda.max_memory_allocated(dev)
+    passes = {name: statistics.mean(pass_ev[k][i].elapsed_time(pass_ev[k][i + 1]) for k in range(steps))
+              for i, name in enumerate(("lse_partial", "lse_merge+loss_reduce", "dgrad_grad_input", "dgrad_grad_W"))}
+    loss = out["loss"].item()
+
+    # end to end through the same public call from pinned host buffers: H2D of the inputs, the call,
+    # D2H of the loss and both gradients, every step
+    h_hidden = torch.from_numpy(d["hidden"].view("int16")).pin_memory()
+    h_W = torch.from_numpy(d["W"].view("int16")).pin_memory()
+    h_target = torch.from_numpy(d["target"]).pin_memory()
+    h_bias = torch.from_numpy(d["bias"]).pin_memory() if bias is not None else None
+    r_loss = torch.empty(1).pin_memory()
+    r_gi = torch.empty((w.BT, w.H), dtype=torch.int16).pin_memory()
+    r_gw = torch.empty((w.V, w.H), dtype=torch.float32).pin_memory()
+    r_gb = torch.empty(w.V).pin_memory() if bias is not None else None
+    h2d = h_hidden.numel() * 2 + h_W.numel() * 2 + h_target.numel() * 8 + (h_bias.numel() * 4 if h_bias is not None else 0)
+    d2h = 4 + r_gi.numel() * 2 + r_gw.numel() * 4 + (r_gb.numel() * 4 if r_gb is not None else 0)
+
+    def e2e_step():
+        hidden.view(torch.int16).copy_(h_hidden, non_blocking=True)
+        W.view(torch.int16).copy_(h_W, non_blocking=True)
+        target.copy_(h_target, non_blocking=True)
+        if bias is not None:
+            bias.copy_(h_bias, non_blocking=True)
+        flce.flce_fwd_bwd(hidden, W, target, **kw)
+        r_loss.copy_(out["loss"], non_blocking=True)
+        r_gi.copy_(out["grad_input"].view(torch.int16), non_blocking=True)
+        r_gw.copy_(out["grad_W"], non_blocking=True)
+        if r_gb is not None:
+            r_gb.copy_(out["grad_bias"], non_blocking=True)
+
+    e2e_steps = max(3, min(steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world) / e2e_steps
+    del h_hidden, h_W, r_gi, r_gw
+    return dict(elapsed_ms=elapsed_ms, passes=passes, clocks=clocks, peak_mem=peak_mem, loss=loss, e2e_ms=e2e_ms,
+                h2d=h2d, d2h=d2h, workspace_bytes=ws.numel())
+
+
+def bench_ce(steps: int, warmup: int, local: int, peaks: dict):
+    import torch
+    import linear_cross_entropy_tma_gb300 as flce
+    w = wl.CE_LOGITS
+    dev = torch.device("cuda", local)
+    c = wl.make_ce_inputs(w)
+    logits = to_device_bf16(c["logits"], dev)
+    labels = torch.from_numpy(c["labels"]).to(dev)
+    ws = torch.empty(flce.ce_workspace_size(w.B, w.V), dtype=torch.uint8, device=dev)
+    out = {"ce_sum": torch.empty(1, device=dev), "z_sum": torch.empty(1, device=dev),
+           "n_valid": torch.empty(1, dtype=torch.int64, device=dev)}
+    # every call rewrites the buffer in place (logits -> dlogits); the work per call is the same
+    for _ in range(warmup):
+        flce.ce_with_grad(logits, labels, z_loss=w.z_loss, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        flce.ce_with_grad(logits, labels, z_loss=w.z_loss, workspace=ws, out=out)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    gbs = w.bytes_moved() / (ms * 1e-3) / 1e9
+    src = kernel_source_digest(["ce_kernel.cu"])
+    return {"workload": w.name, "value": gbs, "unit": "GB/s", "ms_per_call": ms,
+            "rows_per_s": w.B / (ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": dram_traffic("ce_rows_kernel", "ce", src),
+                         "peak_source": peaks["source"], "algorithmic_bytes": w.bytes_moved()}}
+
+
+# ----------------------------------------------------------------------------------- oracle timing
+def time_oracle_tokens(w: wl.FusedWorkload, d: dict, n_rows: int, offset: int = 0):
+    import oracle
+    rows = slice(offset, offset + n_rows)
+    t = time.perf_counter()
+    oracle.flce_reference(d["hidden"][rows], d["W"], d["target"][rows], bias=d["bias"], reduction=w.reduction,
+                          z_loss=w.z_loss, row_block=min(n_rows, 256))
+    return time.perf_counter() - t
+
+
+def cpu_cores():
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            n = min(n, int(os.environ[var]))
+    return n
+
+
+def cpu_baseline(w: wl.FusedWorkload, target_s: float = 12.0):
+    d = wl.make_fused_inputs(w)
+    t64 = time_oracle_tokens(w, d, 64)
+    n = int(max(64, min(w.BT, 64 * target_s / max(t64, 1e-3))))
+    n = min(n, 2048)
+    t = time_oracle_tokens(w, d, n, offset=64)
+    return {"value": n / t, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 oracle, full loss + grad_input + grad_W work for {n} of the {w.BT} tokens "
+                      f"(rows 64..{64 + n - 1}), full V={w.V} and H={w.H}; {t:.1f} s"}
+
+
+def run_reference(args, w):
+    rank, world, local = dist_info()
+    if rank != 0:
+        return 0
+    d = wl.make_fused_inputs(w)
+    per_step = 64
+    for k in range(args.warmup):
+        time_oracle_tokens(w, d, per_step, offset=(k * per_step) % max(1, w.BT - per_step))
+    times = []
+    for k in range(args.steps):
+        times.append(time_oracle_tokens(w, d, per_step, offset=((args.warmup + k) * per_step) % max(1, w.BT - per_step)))
+    total = sum(times)
+    value = per_step * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle", "cores": cpu_cores(),
+                             "sample": f"each step: the fp64 oracle's full per-token work for {per_step} tokens of the "
+                                       f"workload (rows advance each step), full V and H"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "fused LM-head CE fwd+bwd tokens/s & % bf16 tensor peak; CE-only GB/s % HBM"
+
+
+def config_of(w):
+    return {"workload": w.name, "BT": w.BT, "H": w.H, "V": w.V, "reduction": w.reduction, "z_loss": w.z_loss,
+            "bias": w.bias_std is not None, "targets": w.targets,
+            "l2": "no flush: hidden + W (472 MiB at this shape) exceed the 126 MB L2",
+            "parallelism": "independent replica per GPU"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(wl.FUSED_WORKLOADS), default="long")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ce", action="store_true")
+    args = ap.parse_args()
+    w = wl.FUSED_WORKLOADS[args.workload]
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(local)
+    import linear_cross_entropy_tma_gb300 as flce
+    flce.load()
+    peaks = load_peaks()
+
+    r = bench_fused(w, args.steps, args.warmup, world, local, peaks)
+    ms = r["elapsed_ms"] / args.steps
+    value = world * w.BT / (ms * 1e-3)
+    passes = r["passes"]
+    dominant = max(("lse_partial", "dgrad_grad_input", "dgrad_grad_W"), key=lambda k: passes[k])
+    # algorithmic work per launch of each tensor-core kernel: logits 2*BT*V*H; each gradient pass
+    # recomputes the logits (2*BT*V*H) and runs its GEMM (2*BT*V*H)
+    alg = {"lse_partial": 2 * w.BT * w.V * w.H, "dgrad_grad_input": 4 * w.BT * w.V * w.H,
+           "dgrad_grad_W": 4 * w.BT * w.V * w.H}
+    kname = {"lse_partial": "lse_partial_kernel", "dgrad_grad_input": "dgrad_kernel<false>",
+             "dgrad_grad_W": "dgrad_kernel<true>"}
+    src = kernel_source_digest(["flce_fwd.cu", "flce_bwd.cu", "sm100.cuh"])
+    peak_tf = peaks["bf16_tflops_sustained"]
+    achieved = alg[dominant] / (passes[dominant] * 1e-3) / 1e12
+    step_tflops = w.flops() / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / world) / PAGES_TOKENS_PER_S[args.workload] if args.workload in PAGES_TOKENS_PER_S else None,
+        "vs_baseline_note": "value per GPU / verl tuned _Split_Dlogits_N on an H100 (356 ms, pages' table); context only",
+        "dtype": "bf16", "data": "synthetic (seeded; hidden N(0,1), W N(0,0.02), uniform targets, 10% ignored)",
+        "config": config_of(w),
+        "roofline": {"bound": "tensor", "kernel": kname[dominant], "achieved": achieved, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": dram_traffic(kname[dominant], args.workload, src),
+                     "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)",
+                     "algorithmic_flops_per_launch": alg[dominant], "ms_per_launch": passes[dominant]},
+        "step_roofline": {"flops_per_step": w.flops(), "achieved_tflops": step_tflops,
+                          "frac_of_sustained": step_tflops / peak_tf, "frac_of_burst": step_tflops / peaks["bf16_tflops"],
+                          "convention": "8*BT*V*H per fused forward+backward"},
+        "pass_ms": passes,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": r["clocks"],
+        "e2e": {"value": world * w.BT / (r["e2e_ms"] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},
+        "memory": {"peak_allocated_bytes": r["peak_mem"], "workspace_bytes": r["workspace_bytes"],
+                   "avoided_fp32_logits_bytes": 4 * w.BT * w.V},
+        "loss": r["loss"],
+    }
+    if not args.no_ce and world == 1:
+        line["ce_standalone"] = bench_ce(args.steps, args.warmup, local, peaks)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,161 @@
+/*
+ * flce.h -- C ABI of the GB300 (sm_103a) fused linear cross-entropy library, libflce.so.
+ *
+ * Two operations:
+ *
+ *   flce_fwd_bwd   Fused LM-head cross-entropy.  With logits z = hidden . W^T (+ bias) it returns
+ *                  the loss and the gradients grad_input = dlogits . W, grad_W = dlogits^T . hidden
+ *                  and grad_bias = sum_t dlogits[t, :], where
+ *                      dlogits[t, :] = s * [y_t valid] * (softmax(z_t) * (1 + 2 z_loss LSE_t) - onehot(y_t))
+ *                  and s = 1 / max(n_valid, 1) for the mean reduction, 1 for the sum reduction.
+ *                  The (BT, V) logits are never written to device memory: each logits tile lives
+ *                  only in tensor memory and registers of the CTA that computes it.
+ *                  Definitions: "Fused Linear Cross-Entropy: The Math, the Memory Wall, and Two Ways
+ *                  Around It", sections "The setting" (loss), "The identity that makes fused fwbw
+ *                  possible" (softmax - onehot, two-scalar LSE) and "From dlogits to grad_input and
+ *                  grad_W" (the two boxed GEMMs and the bias column sum).  The z-loss term
+ *                  z_loss * LSE^2 per valid token follows "Greyhound -- Cross-Entropy", formulas and
+ *                  "Loss and gradient together".
+ *
+ *   ce_with_grad   Row-wise cross-entropy over logits that already exist, in place: the logits buffer
+ *                  is overwritten with dlogits = [y valid] * (softmax * (1 + 2 z_loss LSE) - onehot),
+ *                  and the sums ce_sum = sum_valid (LSE - z_y), z_sum = sum_valid LSE^2 and the count
+ *                  n_valid are returned ("Greyhound -- Cross-Entropy", "Kernel design", "Shape and
+ *                  dtype constraints" and the raw helper under "Usage").
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device, row-major and contiguous.
+ *     bf16 tensors are passed as uint16_t (raw bfloat16 bit patterns).
+ *   - The caller owns and allocates every buffer, including the workspace.  The library keeps no
+ *     state between calls and touches no memory other than the buffers it is given.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and the call
+ *     returns without synchronising.  Only flce_read_device_status synchronises the stream.
+ *   - Outputs are overwritten, never accumulated into.
+ *   - Argument errors are reported synchronously by the return code before anything is enqueued.
+ *     Data errors (a target outside [0, V) that is not ignore_index) are found on the device: the
+ *     row is treated as ignored and bit FLCE_STATUS_BAD_TARGET is set in the workspace status word.
+ *   - Every wait inside a kernel is bounded; a wait that gives up sets FLCE_STATUS_TIMEOUT in the
+ *     status word and the kernel returns instead of hanging.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum flce_status {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARG = 1,          /* null required pointer, negative size, bad reduction, bias /
+                                        grad_bias mismatch, aliasing outputs */
+  FLCE_ERR_MISALIGNED = 2,           /* a pointer is not 16-byte aligned (workspace: 256-byte) */
+  FLCE_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the matching *_workspace_size() */
+  FLCE_ERR_UNSUPPORTED = 4,          /* a size outside what the kernels handle (see each call) */
+  FLCE_ERR_CUDA = 5,                 /* a CUDA runtime call or a kernel launch failed */
+  FLCE_ERR_NO_DEVICE = 6             /* the current device is not a compute capability 10.3 GPU */
+} flce_status;
+
+/* reduction argument of flce_fwd_bwd */
+#define FLCE_REDUCTION_MEAN 0
+#define FLCE_REDUCTION_SUM 1
+
+/* bits of the device status word (first 4 bytes of either workspace) */
+#define FLCE_STATUS_BAD_TARGET 0x1u
+#define FLCE_STATUS_TIMEOUT 0x2u
+
+/*
+ * Bytes of workspace flce_fwd_bwd needs for these sizes (O(BT) floats: per-row LSE statistics,
+ * per-row loss terms, the status word and the valid count).  Returns 0 for negative sizes.
+ */
+size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V);
+
+/*
+ * Fused linear cross-entropy, forward and backward in one call.
+ *
+ *   hidden      [BT, H] bf16, device.                      (p1 "The setting": hidden[t] in R^H)
+ *   W           [V, H]  bf16, device.                      (LM-head weight, V x H)
+ *   bias        [V] fp32, device, or NULL for no bias.
+ *   target      [BT] int64, device: class index in [0, V), or ignore_index.
+ *   BT, H, V    sizes.  BT >= 0; H >= 8 with H % 8 == 0 (16-byte rows for the tensor-memory-access
+ *               copies); V >= 1.  BT, V < 2^31.  Otherwise FLCE_ERR_UNSUPPORTED / INVALID_ARG.
+ *   ignore_index  rows whose target equals it contribute nothing (PyTorch's -100 by default).
+ *   reduction   FLCE_REDUCTION_MEAN (divide by max(n_valid, 1)) or FLCE_REDUCTION_SUM.
+ *   z_loss      multiplier of the per-token LSE^2 term (0 disables it).
+ *   loss        [1] fp32, device: the reduced loss.
+ *   grad_input  [BT, H] bf16, device, or NULL to skip the grad_input pass.
+ *   grad_W      [V, H] fp32, device, or NULL.
+ *   grad_bias   [V] fp32, device, or NULL; must be NULL when bias is NULL.
+ *               When both grad_W and grad_bias are NULL the grad_W pass is skipped.
+ *   n_valid     [1] int64, device, or NULL: number of rows whose target is in [0, V).
+ *   workspace   device scratch of at least flce_workspace_size(BT, H, V) bytes, 256-byte aligned.
+ *               Its contents on entry do not matter.  Overlapping calls must use separate
+ *               workspaces.
+ *   stream      cudaStream_t.
+ *
+ * hidden, W, grad_input: 16-byte aligned.  bias, target, grad_W, grad_bias, loss: 4/8-byte aligned
+ * (natural alignment).
+ */
+flce_status flce_fwd_bwd(const uint16_t* hidden, const uint16_t* W, const float* bias,
+                         const int64_t* target, int64_t BT, int64_t H, int64_t V,
+                         int64_t ignore_index, int reduction, float z_loss, float* loss,
+                         uint16_t* grad_input, float* grad_W, float* grad_bias, int64_t* n_valid,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * flce_fwd_bwd with timing hooks: identical work and results, plus cudaEventRecord of caller-created
+ * CUDA events at the pass boundaries on `stream`, so a caller can time each kernel inside a longer
+ * timed region without any synchronisation:
+ *   events[0] before the LSE pass        events[1] after the LSE tile kernel
+ *   events[2] after the merge + loss reduction
+ *   events[3] after the grad_input pass  events[4] after the grad_W pass
+ * (a skipped pass records its two events back to back).  n_events must be 0 or 5; events may be
+ * NULL when n_events is 0.  The events are owned by the caller (cudaEvent_t handles).
+ */
+flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const float* bias,
+                               const int64_t* target, int64_t BT, int64_t H, int64_t V,
+                               int64_t ignore_index, int reduction, float z_loss, float* loss,
+                               uint16_t* grad_input, float* grad_W, float* grad_bias,
+                               int64_t* n_valid, void* workspace, size_t workspace_bytes,
+                               void* stream, void* const* events, int n_events);
+
+/* Bytes of workspace ce_with_grad needs for B rows (per-row partial sums and the status word). */
+size_t ce_workspace_size(int64_t B, int64_t V);
+
+/*
+ * Standalone cross-entropy with the logits gradient written in place.
+ *
+ *   logits      [B, V] bf16, device, 16-byte aligned.  In: logits.  Out: dlogits (bf16).
+ *   labels      [B] int64, device.
+ *   B, V        B >= 0, 1 <= V < 2^31.
+ *   ignore_index  rows with this label: no loss, not counted, gradient row written as zeros.
+ *   z_loss      multiplier used in the gradient; z_sum itself is returned unscaled.
+ *   ce_sum      [1] fp32, device: sum over valid rows of LSE - z_y.
+ *   z_sum       [1] fp32, device: sum over valid rows of LSE^2.
+ *   n_valid     [1] int64, device: number of valid rows.
+ *               The mean loss of p3 "Usage" is ce_sum / max(n_valid, 1).
+ *   workspace   at least ce_workspace_size(B, V) bytes, 256-byte aligned.
+ */
+flce_status ce_with_grad(uint16_t* logits, const int64_t* labels, int64_t B, int64_t V,
+                         int64_t ignore_index, float z_loss, float* ce_sum, float* z_sum,
+                         int64_t* n_valid, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Copy the device status word of a workspace used by a previous call to *host_status, after
+ * synchronising `stream`.  0 means no data error and no timeout.
+ */
+flce_status flce_read_device_status(const void* workspace, uint32_t* host_status, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* flce_status_string(flce_status status);
+
+/* Description of the last FLCE_ERR_CUDA / FLCE_ERR_UNSUPPORTED on this host thread (static buffer). */
+const char* flce_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H_ */

@@ -1,0 +1,170 @@
+"""ctypes binding of libflce.so (argument marshalling only; every step runs in the CUDA kernels).
+
+The functions below take torch CUDA tensors, check dtypes/shapes/devices, allocate the outputs and the
+workspace with torch (PyTorch is only the memory and stream provider), and call the C ABI declared
+in include/flce.h.  There is no fallback: if the library is missing, or the call returns an error,
+a RuntimeError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libflce.so")
+
+FLCE_OK = 0
+STATUS_BAD_TARGET = 0x1
+STATUS_TIMEOUT = 0x2
+EXPORTED = ("flce_workspace_size", "flce_fwd_bwd", "flce_fwd_bwd_timed", "ce_workspace_size", "ce_with_grad",
+            "flce_read_device_status", "flce_status_string", "flce_last_error")
+
+_lib = None
+
+c_p = ctypes.c_void_p
+c_i64 = ctypes.c_int64
+c_sz = ctypes.c_size_t
+
+
+def load() -> ctypes.CDLL:
+    """Load libflce.so once; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m linear_cross_entropy_tma_gb300.build` "
+                           "(needs nvcc from CUDA 13)")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.flce_workspace_size.restype = c_sz
+    lib.flce_workspace_size.argtypes = [c_i64, c_i64, c_i64]
+    lib.flce_fwd_bwd.restype = ctypes.c_int
+    lib.flce_fwd_bwd.argtypes = [c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i64, ctypes.c_int, ctypes.c_float,
+                                 c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]
+    lib.flce_fwd_bwd_timed.restype = ctypes.c_int
+    lib.flce_fwd_bwd_timed.argtypes = lib.flce_fwd_bwd.argtypes + [ctypes.POINTER(c_p), ctypes.c_int]
+    lib.ce_workspace_size.restype = c_sz
+    lib.ce_workspace_size.argtypes = [c_i64, c_i64]
+    lib.ce_with_grad.restype = ctypes.c_int
+    lib.ce_with_grad.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, ctypes.c_float, c_p, c_p, c_p, c_p, c_sz, c_p]
+    lib.flce_read_device_status.restype = ctypes.c_int
+    lib.flce_read_device_status.argtypes = [c_p, ctypes.POINTER(ctypes.c_uint32), c_p]
+    lib.flce_status_string.restype = ctypes.c_char_p
+    lib.flce_status_string.argtypes = [ctypes.c_int]
+    lib.flce_last_error.restype = ctypes.c_char_p
+    lib.flce_last_error.argtypes = []
+    _lib = lib
+    return lib
+
+
+def check(status: int) -> None:
+    if status != FLCE_OK:
+        lib = load()
+        raise RuntimeError(f"{lib.flce_status_string(status).decode()}: {lib.flce_last_error().decode()}")
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream) -> int | None:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def workspace_size(BT: int, H: int, V: int) -> int:
+    return int(load().flce_workspace_size(BT, H, V))
+
+
+def ce_workspace_size(B: int, V: int) -> int:
+    return int(load().ce_workspace_size(B, V))
+
+
+def _bf16_ptr_ok(t, name):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+
+
+def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reduction: str = "mean",
+                 z_loss: float = 0.0, need_grad_input: bool = True, need_grad_W: bool = True, workspace=None,
+                 out=None, stream=None, pass_events=None) -> dict:
+    """Fused linear cross-entropy forward + backward on the current CUDA device.
+
+    hidden [BT, H] bf16, W [V, H] bf16, target [BT] int64, bias [V] fp32 or None.  Returns a dict with
+    ``loss`` (fp32 [1]), ``n_valid`` (int64 [1]), ``grad_input`` (bf16 [BT, H] or None), ``grad_W``
+    (fp32 [V, H] or None), ``grad_bias`` (fp32 [V] or None).  ``out`` may supply preallocated outputs
+    with the same keys; ``workspace`` a uint8 CUDA tensor of at least ``workspace_size`` bytes.
+    ``pass_events``: five recorded ``torch.cuda.Event(enable_timing=True)`` objects; the library
+    re-records them at the pass boundaries (flce_fwd_bwd_timed) for per-kernel timing.
+    """
+    import torch
+    _bf16_ptr_ok(hidden, "hidden")
+    _bf16_ptr_ok(W, "W")
+    BT, H = hidden.shape
+    V, H2 = W.shape
+    if H2 != H or target.shape != (BT,) or target.dtype != torch.int64 or not target.is_cuda:
+        raise ValueError("shapes must be hidden [BT, H], W [V, H], target [BT] int64 on the GPU")
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (V,) or not bias.is_cuda):
+        raise ValueError("bias must be a CUDA float32 tensor of shape [V]")
+    red = {"mean": 0, "sum": 1}[reduction]
+    dev = hidden.device
+    o = dict(out or {})
+    if "loss" not in o:
+        o["loss"] = torch.empty(1, dtype=torch.float32, device=dev)
+    if "n_valid" not in o:
+        o["n_valid"] = torch.empty(1, dtype=torch.int64, device=dev)
+    if need_grad_input and o.get("grad_input") is None:
+        o["grad_input"] = torch.empty((BT, H), dtype=torch.bfloat16, device=dev)
+    if need_grad_W and o.get("grad_W") is None:
+        o["grad_W"] = torch.empty((V, H), dtype=torch.float32, device=dev)
+    if need_grad_W and bias is not None and o.get("grad_bias") is None:
+        o["grad_bias"] = torch.empty(V, dtype=torch.float32, device=dev)
+    gi = o.get("grad_input") if need_grad_input else None
+    gw = o.get("grad_W") if need_grad_W else None
+    gb = o.get("grad_bias") if (need_grad_W and bias is not None) else None
+    need = workspace_size(BT, H, V)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    args = (_ptr(hidden), _ptr(W), _ptr(bias), _ptr(target), BT, H, V, ignore_index, red, float(z_loss),
+            _ptr(o["loss"]), _ptr(gi), _ptr(gw), _ptr(gb), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel(),
+            _stream_ptr(stream))
+    if pass_events is None:
+        check(load().flce_fwd_bwd(*args))
+    else:
+        if len(pass_events) != 5:
+            raise ValueError("pass_events needs exactly 5 events")
+        handles = (c_p * 5)(*[ev.cuda_event for ev in pass_events])
+        check(load().flce_fwd_bwd_timed(*args, handles, 5))
+    return dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, workspace=workspace)
+
+
+def ce_with_grad(logits, labels, ignore_index: int = -100, z_loss: float = 0.0, workspace=None, out=None,
+                 stream=None) -> dict:
+    """Row-wise CE over bf16 logits [B, V]; overwrites ``logits`` with dlogits in place.
+
+    Returns ``ce_sum`` (fp32 [1]), ``z_sum`` (fp32 [1]) and ``n_valid`` (int64 [1]).
+    """
+    import torch
+    _bf16_ptr_ok(logits, "logits")
+    B, V = logits.shape
+    if labels.shape != (B,) or labels.dtype != torch.int64 or not labels.is_cuda:
+        raise ValueError("labels must be a CUDA int64 tensor of shape [B]")
+    dev = logits.device
+    o = dict(out or {})
+    for k, dt in (("ce_sum", torch.float32), ("z_sum", torch.float32), ("n_valid", torch.int64)):
+        if k not in o:
+            o[k] = torch.empty(1, dtype=dt, device=dev)
+    if workspace is None:
+        workspace = torch.empty(ce_workspace_size(B, V), dtype=torch.uint8, device=dev)
+    check(load().ce_with_grad(_ptr(logits), _ptr(labels), B, V, ignore_index, float(z_loss), _ptr(o["ce_sum"]),
+                              _ptr(o["z_sum"]), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel(),
+                              _stream_ptr(stream)))
+    return dict(ce_sum=o["ce_sum"], z_sum=o["z_sum"], n_valid=o["n_valid"], workspace=workspace)
+
+
+def read_device_status(workspace, stream=None) -> int:
+    """Status word of a workspace after the call that used it (synchronises the stream)."""
+    v = ctypes.c_uint32(0)
+    check(load().flce_read_device_status(_ptr(workspace), ctypes.byref(v), _stream_ptr(stream)))
+    return int(v.value)

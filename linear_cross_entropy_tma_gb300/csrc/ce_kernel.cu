@@ -1,0 +1,273 @@
+// ce_kernel.cu -- standalone row-wise cross-entropy over materialised bf16 logits, with the logits
+// gradient written back in place ("Greyhound -- Cross-Entropy", "Kernel design": one block per row,
+// fp32 online max/sum across the row, warp reductions to the row LSE, a second pass that overwrites
+// the logits with dlogits; z-loss scales the softmax term before the target column is adjusted).
+//
+// GB300 shape of it: a persistent grid of two 512-thread CTAs per SM walks the rows.  Pass 1 streams
+// the row with 16-byte loads tagged to stay in L2, pass 2 re-reads it (an L2 hit: at most
+// 2 x 152 rows x 250 KB = 76 MB are in flight, well under the 126 MB L2) and writes dlogits with
+// 16-byte stores tagged evict-first.  HBM therefore sees one read and one write of the logits.
+// Per-row (ce, LSE^2, valid) land in the workspace; the last CTA to finish sums them in a fixed
+// order (float64), so the three outputs are deterministic.
+#include "ce_kernel.cuh"
+#include "sm100.cuh"
+
+namespace flce {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 4;  // 16-byte vectors per thread in flight per step
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld16_hint(const void* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st16_hint(void* ptr, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+               ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+// Merge two (max, sum) pairs of the online softmax; max values are in the log2 domain.
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  const float a = (m == mn) ? s : s * ex2_approx(m - mn);
+  const float b = (m2 == mn) ? s2 : s2 * ex2_approx(m2 - mn);
+  m = mn;
+  s = a + b;
+}
+
+__device__ __forceinline__ void accumulate8(const uint4 v, float& m, float& s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16_lo(w[i]) * kLog2e;
+    x[2 * i + 1] = bf16_hi(w[i]) * kLog2e;
+  }
+  float cm = x[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) cm = fmaxf(cm, x[i]);
+  const float mn = fmaxf(m, cm);
+  float acc = s * ex2_approx(m - mn);  // m = -inf on the first call gives 0 * 0
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc += ex2_approx(x[i] - mn);
+  m = mn;
+  s = acc;
+}
+
+// dlogits of 8 consecutive columns starting at column c0 (softmax * zf - onehot).
+__device__ __forceinline__ uint4 grad8(const uint4 v, int64_t c0, int64_t y, float lse2, float zf) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float a = ex2_approx(fmaf(bf16_lo(w[i]), kLog2e, -lse2)) * zf;
+    float b = ex2_approx(fmaf(bf16_hi(w[i]), kLog2e, -lse2)) * zf;
+    if (c0 + 2 * i == y) a -= 1.0f;
+    if (c0 + 2 * i + 1 == y) b -= 1.0f;
+    o[i] = pack_bf16x2(a, b);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float grad1(uint16_t raw, int64_t c, int64_t y, float lse2, float zf) {
+  float g = ex2_approx(fmaf(__uint_as_float(static_cast<uint32_t>(raw) << 16), kLog2e, -lse2)) * zf;
+  return (c == y) ? g - 1.0f : g;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return static_cast<uint16_t>(pack_bf16x2(f, 0.0f) & 0xFFFFu);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels, int64_t B, int64_t V,
+               int64_t ignore_index, float z_loss, float4* __restrict__ row_out, uint32_t* __restrict__ status,
+               uint32_t* __restrict__ done_counter, float* __restrict__ ce_sum, float* __restrict__ z_sum,
+               int64_t* __restrict__ n_valid) {
+  __shared__ float s_m[kWarps], s_s[kWarps];
+  __shared__ float s_lse2;
+  __shared__ float s_zy;
+  __shared__ double s_red[2][kWarps];
+  __shared__ long long s_cnt[kWarps];
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const uint64_t keep = policy_evict_last();
+  const uint64_t drop = policy_evict_first();
+
+  for (int64_t r = blockIdx.x; r < B; r += gridDim.x) {
+    const int64_t y = labels[r];
+    const bool valid = (y != ignore_index) && (y >= 0) && (y < V);
+    uint16_t* row = logits + r * V;
+    // 16-byte aligned middle part of the row; scalar head and tail around it
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+    const int64_t head_raw = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) >> 1);
+    const int64_t head = head_raw < V ? head_raw : V;
+    const int64_t nvec = (V - head) >> 3;
+    const int64_t tail0 = head + nvec * 8;
+    uint4* vrow = reinterpret_cast<uint4*>(row + head);
+
+    if (!valid) {
+      if (tid == 0) {
+        if (y != ignore_index) atomicOr(status, kStatusBadTarget);
+        row_out[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int64_t i = tid; i < nvec; i += kThreads) st16_hint(vrow + i, make_uint4(0, 0, 0, 0), drop);
+      for (int64_t c = tid; c < head; c += kThreads) row[c] = 0;
+      for (int64_t c = tail0 + tid; c < V; c += kThreads) row[c] = 0;
+      continue;
+    }
+
+    if (tid == 0) s_zy = __uint_as_float(static_cast<uint32_t>(row[y]) << 16);
+
+    // ---- pass 1: online (max, sum) in the log2 domain
+    float m = -INFINITY, s = 0.f;
+    for (int64_t c = tid; c < head; c += kThreads) {
+      const float x = __uint_as_float(static_cast<uint32_t>(row[c]) << 16) * kLog2e;
+      merge_ms(m, s, x, 1.0f);
+    }
+    for (int64_t c = tail0 + tid; c < V; c += kThreads) {
+      const float x = __uint_as_float(static_cast<uint32_t>(row[c]) << 16) * kLog2e;
+      merge_ms(m, s, x, 1.0f);
+    }
+    int64_t i = tid;
+    for (; i + (kUnroll - 1) * kThreads < nvec; i += kUnroll * kThreads) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) v[u] = ld16_hint(vrow + i + u * kThreads, keep);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) accumulate8(v[u], m, s);
+    }
+    for (; i < nvec; i += kThreads) accumulate8(ld16_hint(vrow + i, keep), m, s);
+
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+      merge_ms(m, s, m2, s2);
+    }
+    if ((tid & 31) == 0) {
+      s_m[warp] = m;
+      s_s[warp] = s;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      m = (tid < kWarps) ? s_m[tid] : -INFINITY;
+      s = (tid < kWarps) ? s_s[tid] : 0.f;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+        merge_ms(m, s, m2, s2);
+      }
+      if (tid == 0) {
+        const float lse2 = m + __log2f(s);
+        s_lse2 = lse2;
+        const float lse = lse2 * kLn2;
+        row_out[r] = make_float4(lse - s_zy, lse * lse, 1.f, 0.f);
+      }
+    }
+    __syncthreads();
+    const float lse2 = s_lse2;
+    const float zf = 1.0f + 2.0f * z_loss * (lse2 * kLn2);
+
+    // ---- pass 2: overwrite with dlogits
+    for (int64_t c = tid; c < head; c += kThreads) row[c] = f32_to_bf16_bits(grad1(row[c], c, y, lse2, zf));
+    for (int64_t c = tail0 + tid; c < V; c += kThreads) row[c] = f32_to_bf16_bits(grad1(row[c], c, y, lse2, zf));
+    i = tid;
+    for (; i + (kUnroll - 1) * kThreads < nvec; i += kUnroll * kThreads) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) v[u] = ld16_hint(vrow + i + u * kThreads, drop);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        st16_hint(vrow + i + u * kThreads, grad8(v[u], head + (i + u * kThreads) * 8, y, lse2, zf), drop);
+    }
+    for (; i < nvec; i += kThreads) st16_hint(vrow + i, grad8(ld16_hint(vrow + i, drop), head + i * 8, y, lse2, zf), drop);
+    __syncthreads();  // s_m / s_s / s_lse2 / s_zy are reused by the next row
+  }
+
+  // ---- the last CTA to finish reduces the per-row terms in row order
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(done_counter, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  double ce = 0.0, zz = 0.0;
+  long long cnt = 0;
+  for (int64_t k = tid; k < B; k += kThreads) {
+    const float4 v = __ldcg(row_out + k);
+    ce += v.x;
+    zz += v.y;
+    cnt += (v.z != 0.f) ? 1 : 0;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    ce += __shfl_xor_sync(0xffffffffu, ce, off);
+    zz += __shfl_xor_sync(0xffffffffu, zz, off);
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+  }
+  if ((tid & 31) == 0) {
+    s_red[0][warp] = ce;
+    s_red[1][warp] = zz;
+    s_cnt[warp] = cnt;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double a = 0.0, b = 0.0;
+    long long n = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      a += s_red[0][w];
+      b += s_red[1][w];
+      n += s_cnt[w];
+    }
+    *ce_sum = static_cast<float>(a);
+    *z_sum = static_cast<float>(b);
+    *n_valid = n;
+    *done_counter = 0u;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ce_rows(uint16_t* logits, const int64_t* labels, int64_t B, int64_t V, int64_t ignore_index,
+                           float z_loss, float* ce_sum, float* z_sum, int64_t* n_valid, void* workspace,
+                           int num_sms, cudaStream_t stream) {
+  auto* ws = static_cast<unsigned char*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  uint32_t* counter = reinterpret_cast<uint32_t*>(ws + 4);
+  float4* row_out = reinterpret_cast<float4*>(ws + kCeHeaderBytes);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kCeHeaderBytes, stream);
+  if (e != cudaSuccess) return e;
+  if (B == 0) {
+    if ((e = cudaMemsetAsync(ce_sum, 0, sizeof(float), stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(z_sum, 0, sizeof(float), stream)) != cudaSuccess) return e;
+    return cudaMemsetAsync(n_valid, 0, sizeof(int64_t), stream);
+  }
+  const int64_t cap = static_cast<int64_t>(num_sms) * 2;
+  const int64_t grid = B < cap ? B : cap;
+  ce_rows_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(logits, labels, B, V, ignore_index, z_loss,
+                                                                        row_out, status, counter, ce_sum, z_sum,
+                                                                        n_valid);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

@@ -1,0 +1,382 @@
+// flce_fwd.cu -- forward passes of fused linear cross-entropy: per-row LSE without logits in HBM.
+//
+// lse_partial: one CTA per (128-token tile, vocabulary split).  A TMA producer warp streams
+// hidden[m-tile, k-block] and W[n-tile, k-block] (128-byte swizzled, 64-wide k-blocks) through a
+// 4-stage mbarrier ring; one thread of the MMA warp issues tcgen05.mma (M=128, N=256, K=16) into one
+// of two 256-column TMEM accumulators; eight epilogue warps read each finished tile with tcgen05.ld
+// and keep, per row, the online max / sum-exp update ("Fused Linear Cross-Entropy", "Forward -- one
+// Triton kernel, online softmax across vocab splits", steps 1-3) and the target logit when the tile
+// holds the target column.  Double-buffered accumulators let the epilogue of tile j overlap the MMAs
+// of tile j+1.
+//
+// lse_merge: per row, log-sum-exp merge of the split partials (the partial-LSE combination of "Cut
+// Cross Entropy visualized", "Forward kernel", done by ownership instead of a spin lock).
+//
+// loss_reduce: one CTA sums the per-row loss terms and the valid count in a fixed order.
+#include <cstdio>
+
+#include "flce_kernels.cuh"
+#include "sm100.cuh"
+
+namespace flce {
+
+namespace {
+
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr uint32_t kABytes = kTileM * kBK * 2;
+constexpr uint32_t kBBytes = kBN * kBK * 2;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 10 * 32;
+constexpr uint32_t kTmemCols = 512;
+
+struct LseSmem {
+  uint8_t stage[kStages][kStageBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  float2 half_ms[kTileM];
+};
+constexpr size_t kLseSmemBytes = sizeof(LseSmem) + 1024;
+
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;
+  const float a = (m == mn) ? s : s * ex2_approx(m - mn);
+  const float b = (m2 == mn) ? s2 : s2 * ex2_approx(m2 - mn);
+  m = mn;
+  s = a + b;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+lse_partial_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
+                   const float* __restrict__ bias, const int64_t* __restrict__ target, int BT, int V,
+                   int64_t ignore_index, int num_kb, int tiles_per_split, int n_tiles, int BTp,
+                   float2* __restrict__ part, float* __restrict__ zy_out, uint32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  LseSmem& sm = *reinterpret_cast<LseSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x;
+  const int split = blockIdx.y;
+  const int t_begin = split * tiles_per_split;
+  const int nt = max(0, min(n_tiles, t_begin + tiles_per_split) - t_begin);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sm.acc_full[a], 1);
+      mbar_init(&sm.acc_empty[a], kEpiWarps);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmap_h);
+    tma_prefetch_desc(&tmap_w);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort = &sm.abort;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0, last_phase = 0;  // per-stage bit masks, for draining after an abort
+      bool ok = true;
+      for (int j = 0; j < nt && ok; ++j) {
+        const int n0 = (t_begin + j) * kBN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
+          tma_load_2d(sm.stage[stage], &tmap_h, &sm.full[stage], kb * kBK, m_tile * kTileM);
+          tma_load_2d(sm.stage[stage] + kABytes, &tmap_w, &sm.full[stage], kb * kBK, n0);
+          filled |= 1u << stage;
+          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s)
+          if (filled & (1u << s)) mbar_wait_drain(&sm.full[s], (last_phase >> s) & 1u);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kBN, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int j = 0; j < nt && ok; ++j) {
+        const int acc = j & 1;
+        if (!mbar_wait(&sm.acc_empty[acc], ((j >> 1) & 1) ^ 1, abort)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kBN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&sm.full[stage], phase, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sm.stage[stage]);
+          const uint32_t b_base = a_base + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            mma_bf16_ss(d_tmem, sdesc_sw128(a_base + 32u * k, 16u, 1024u), sdesc_sw128(b_base + 32u * k, 16u, 1024u),
+                        idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&sm.empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) mma_commit(&sm.acc_full[acc]);
+      }
+      mma_commit(&sm.drain);
+      mbar_wait_drain(&sm.drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------------------- epilogue warps
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int h = warp >> 2; // which 128-column half of the tile
+    const int row_local = q * 32 + lane;
+    const int row = m_tile * kTileM + row_local;
+    int64_t y = -1;
+    if (row < BT) {
+      const int64_t t = target[row];
+      if (t != ignore_index && t >= 0 && t < V) y = t;
+    }
+    float m = -INFINITY, s = 0.f, zy = 0.f;
+    bool found = false;
+    for (int j = 0; j < nt; ++j) {
+      const int acc = j & 1;
+      if (!mbar_wait(&sm.acc_full[acc], (j >> 1) & 1, abort)) break;
+      tc_fence_after();
+      const int n0 = (t_begin + j) * kBN + h * 128;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN + h * 128);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(taddr + 32u * c, r);
+        tmem_wait_ld();
+        const int col0 = n0 + 32 * c;
+        float x[32];
+        float cm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int col = col0 + i;
+          float v = __uint_as_float(r[i]);
+          if (bias != nullptr && col < V) v += __ldg(bias + col);
+          if (col == y) {
+            zy = v;
+            found = true;
+          }
+          x[i] = (col < V) ? v * kLog2e : -INFINITY;
+          cm = fmaxf(cm, x[i]);
+        }
+        const float mn = fmaxf(m, cm);
+        if (mn != -INFINITY) {
+          float acc_s = (m == -INFINITY) ? 0.f : s * ex2_approx(m - mn);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc_s += ex2_approx(x[i] - mn);
+          s = acc_s;
+          m = mn;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+    }
+    if (h == 1) sm.half_ms[row_local] = make_float2(m, s);
+    named_barrier_sync(1, kEpiWarps * 32);
+    if (h == 0) {
+      const float2 o = sm.half_ms[row_local];
+      merge_ms(m, s, o.x, o.y);
+      if (row < BT) part[static_cast<size_t>(split) * BTp + row] = make_float2(m, s);
+    }
+    if (found && row < BT) zy_out[row] = zy;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && sm.abort) atomicOr(status, kStatusTimeout);
+}
+
+__global__ void lse_merge_kernel(const float2* __restrict__ part, int splits, int BTp, const float* __restrict__ zy,
+                                 const int64_t* __restrict__ target, int BT, int V, int64_t ignore_index,
+                                 float z_loss, float4* __restrict__ stats, float* __restrict__ row_loss,
+                                 uint32_t* __restrict__ status) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= BT) return;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, part[static_cast<size_t>(s) * BTp + t].x);
+  float S = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float2 p = part[static_cast<size_t>(s) * BTp + t];
+    if (p.x != -INFINITY) S += p.y * exp2f(p.x - M);
+  }
+  const float lse2 = M + log2f(S);
+  const float lse = lse2 * kLn2;
+  const int64_t y = target[t];
+  const bool valid = (y != ignore_index) && (y >= 0) && (y < V);
+  if (!valid && y != ignore_index) atomicOr(status, kStatusBadTarget);
+  row_loss[t] = valid ? (lse - zy[t]) + z_loss * lse * lse : 0.f;
+  stats[t] = make_float4(lse2, 1.0f + 2.0f * z_loss * lse, valid ? 1.f : 0.f, __int_as_float(valid ? static_cast<int>(y) : -1));
+}
+
+constexpr int kReduceThreads = 1024;
+
+__global__ void __launch_bounds__(kReduceThreads)
+loss_reduce_kernel(const float* __restrict__ row_loss, const float4* __restrict__ stats, int BT, int reduction,
+                   float* __restrict__ scale_ws, int64_t* __restrict__ n_valid_ws, float* __restrict__ loss,
+                   int64_t* __restrict__ n_valid_out) {
+  __shared__ double s_sum[kReduceThreads / 32];
+  __shared__ long long s_cnt[kReduceThreads / 32];
+  double acc = 0.0;
+  long long cnt = 0;
+  for (int t = threadIdx.x; t < BT; t += kReduceThreads) {
+    acc += static_cast<double>(row_loss[t]);
+    cnt += (stats[t].z != 0.f) ? 1 : 0;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    s_sum[threadIdx.x >> 5] = acc;
+    s_cnt[threadIdx.x >> 5] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double total = 0.0;
+    long long n = 0;
+    for (int w = 0; w < kReduceThreads / 32; ++w) {
+      total += s_sum[w];
+      n += s_cnt[w];
+    }
+    const double scale = (reduction == 0) ? 1.0 / static_cast<double>(n > 0 ? n : 1) : 1.0;
+    *loss = static_cast<float>(total * scale);
+    *scale_ws = static_cast<float>(scale);
+    *n_valid_ws = n;
+    if (n_valid_out != nullptr) *n_valid_out = n;
+  }
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int choose_splits(int m_tiles, int n_tiles, int num_sms) {
+  // Pick the split count whose grid fills the SMs best (waves rounded up), preferring fewer splits.
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= kMaxSplits && s <= n_tiles; ++s) {
+    const int tps = (n_tiles + s - 1) / s;
+    const int real = (n_tiles + tps - 1) / tps;
+    const long long ctas = static_cast<long long>(m_tiles) * real;
+    const long long waves = (ctas + num_sms - 1) / num_sms;
+    // work per CTA is tps tiles; the busiest SM does waves * tps tiles; ideal is m_tiles*n_tiles/num_sms
+    const double ideal = static_cast<double>(m_tiles) * n_tiles / num_sms;
+    const double eff = ideal / static_cast<double>(waves * tps);
+    if (eff > best_eff + 1e-3) {
+      best_eff = eff;
+      best = real;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+size_t fused_workspace_bytes(int64_t BT) {
+  const size_t btp = align_up(static_cast<size_t>(BT > 0 ? BT : 0), kTileM);
+  size_t off = 256;
+  off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
+  off += align_up(sizeof(float) * btp, 256);
+  off += align_up(sizeof(float4) * btp, 256);
+  off += align_up(sizeof(float) * btp, 256);
+  return off;
+}
+
+FusedWorkspace carve_workspace(void* base, int64_t BT) {
+  const size_t btp = align_up(static_cast<size_t>(BT > 0 ? BT : 0), kTileM);
+  auto* p = static_cast<unsigned char*>(base);
+  FusedWorkspace w;
+  w.status = reinterpret_cast<uint32_t*>(p);
+  w.scale = reinterpret_cast<float*>(p + 4);
+  w.n_valid = reinterpret_cast<int64_t*>(p + 8);
+  size_t off = 256;
+  w.part = reinterpret_cast<float2*>(p + off);
+  off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
+  w.zy = reinterpret_cast<float*>(p + off);
+  off += align_up(sizeof(float) * btp, 256);
+  w.stats = reinterpret_cast<float4*>(p + off);
+  off += align_up(sizeof(float4) * btp, 256);
+  w.row_loss = reinterpret_cast<float*>(p + off);
+  return w;
+}
+
+cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int num_sms, cudaStream_t stream,
+                              char* err, size_t err_len, cudaEvent_t const* events) {
+  const int BT = static_cast<int>(a.BT);
+  const int V = static_cast<int>(a.V);
+  const int BTp = static_cast<int>(align_up(static_cast<size_t>(BT), kTileM));
+  cudaError_t e;
+  if (BT > 0) {
+    CUtensorMap tm_h, tm_w;
+    if (!make_tmap_bf16(&tm_h, a.hidden, a.BT, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tm_w, a.W, a.V, a.H, kBN, err, err_len)) return cudaErrorInvalidValue;
+    const int m_tiles = BTp / kTileM;
+    const int n_tiles = (V + kBN - 1) / kBN;
+    const int splits = choose_splits(m_tiles, n_tiles, num_sms);
+    const int tps = (n_tiles + splits - 1) / splits;
+    const int num_kb = static_cast<int>((a.H + kBK - 1) / kBK);
+    e = cudaFuncSetAttribute(lse_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kLseSmemBytes));
+    if (e != cudaSuccess) return e;
+    lse_partial_kernel<<<dim3(m_tiles, splits), kThreads, kLseSmemBytes, stream>>>(
+        tm_h, tm_w, a.bias, a.target, BT, V, a.ignore_index, num_kb, tps, n_tiles, BTp, ws.part, ws.zy, ws.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
+    lse_merge_kernel<<<(BT + 255) / 256, 256, 0, stream>>>(ws.part, splits, BTp, ws.zy, a.target, BT, V,
+                                                          a.ignore_index, a.z_loss, ws.stats, ws.row_loss,
+                                                          ws.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) {
+    return e;
+  }
+  loss_reduce_kernel<<<1, kReduceThreads, 0, stream>>>(ws.row_loss, ws.stats, BT, a.reduction, ws.scale, ws.n_valid,
+                                                      a.loss, a.n_valid_out);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

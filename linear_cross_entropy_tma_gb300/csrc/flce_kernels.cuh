@@ -1,0 +1,68 @@
+// flce_kernels.cuh -- workspace layout and launchers of the fused linear cross-entropy kernels.
+//
+// Pass structure of one flce_fwd_bwd call (all on one stream, no host synchronisation):
+//   1. lse_partial   logits tile GEMM (tcgen05, TMEM accumulators, TMA-fed) per (128-token tile,
+//                    vocabulary split); the epilogue keeps an online per-row (max, sum-exp) over the
+//                    split's 256-wide vocabulary tiles and picks up the target logit z_y.
+//   2. lse_merge     per row: log-sum-exp merge of the split partials -> LSE, per-row loss term,
+//                    per-row statistics used by the backward passes.
+//   3. loss_reduce   one CTA: deterministic sum of the per-row terms, the valid count and the scale
+//                    s = 1/max(n_valid, 1) (mean) or 1 (sum).
+//   4. dgrad<tokens> grad_input: per (128-token tile, H chunk) recompute logits tiles over all of V,
+//                    form dlogits in registers, stage it as bf16 in shared memory and feed it to a
+//                    second tcgen05 GEMM that accumulates grad_input in TMEM.
+//   5. dgrad<vocab>  grad_W (+ grad_bias): per (128-row vocabulary tile, H chunk) the same over all
+//                    tokens, accumulating grad_W in TMEM in fp32.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace flce {
+
+constexpr int kMaxSplits = 32;     // vocabulary splits of the LSE pass
+constexpr int kTileM = 128;        // rows of every MMA tile (tokens or vocabulary rows)
+
+struct FusedWorkspace {
+  uint32_t* status;  // header: status word
+  float* scale;      // header: s = 1/max(n_valid, 1) or 1
+  int64_t* n_valid;  // header: valid count
+  float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
+  float* zy;         // [BTp] target logit
+  float4* stats;     // [BTp] (LSE * log2 e, 1 + 2 z_loss LSE, valid ? 1 : 0, target as int bits)
+  float* row_loss;   // [BTp] valid * (LSE - z_y + z_loss LSE^2)
+};
+
+size_t fused_workspace_bytes(int64_t BT);
+FusedWorkspace carve_workspace(void* base, int64_t BT);
+
+struct FusedArgs {
+  const uint16_t* hidden;
+  const uint16_t* W;
+  const float* bias;
+  const int64_t* target;
+  int64_t BT, H, V;
+  int64_t ignore_index;
+  int reduction;
+  float z_loss;
+  float* loss;
+  uint16_t* grad_input;
+  float* grad_W;
+  float* grad_bias;
+  int64_t* n_valid_out;
+};
+
+// Encodes a 2-D bf16 tensor map (rows x cols, row-major) with a box of box_rows x 64 columns and
+// 128-byte swizzle.  Returns false (and fills err) when the driver refuses the descriptor.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    char* err, size_t err_len);
+
+// Enqueues every pass.  Returns cudaSuccess or the first launch error; tensor-map failures are
+// reported as cudaErrorInvalidValue with a message in err.
+// events: NULL, or 5 caller-owned events recorded at the pass boundaries (see flce_fwd_bwd_timed).
+cudaError_t launch_fused(const FusedArgs& a, void* workspace, int num_sms, cudaStream_t stream, char* err,
+                         size_t err_len, cudaEvent_t const* events = nullptr);
+
+}  // namespace flce

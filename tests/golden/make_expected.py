@@ -84,10 +84,9 @@ def make_ce() -> None:
     import math
     ce_sum = math.fsum(parts_ce)
     z_sum = math.fsum(parts_z)
-    r = oracle.ce_reference(d["logits"][rows], d["labels"][rows], z_loss=w.z_loss)
+    # sampled dlogits rows are cheap and are computed by the test itself
     np.savez_compressed(os.path.join(HERE, "expected_ce.npz"), digest=np.array(dig), ce_sum=np.float64(ce_sum),
-                        z_sum=np.float64(z_sum), n_valid=np.int64(n_valid), rows=rows,
-                        dlogits_rows=r["dlogits"].astype(np.float32))
+                        z_sum=np.float64(z_sum), n_valid=np.int64(n_valid), rows=rows)
     print(f"ce: ce_sum={ce_sum:.6f} z_sum={z_sum:.6f} n_valid={n_valid} ({time.time() - t0:.1f} s)")
 
 

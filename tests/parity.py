@@ -1,0 +1,50 @@
+"""Tolerances of the parity tests and helpers to move data between numpy and torch.
+
+Floating-point bars (from the stated targets of this library):
+  * loss, ce_sum, z_sum: relative error <= 2e-4;
+  * every gradient (grad_input, grad_W, grad_bias, dlogits): max-abs error <= 1e-2 * max|ref| and
+    relative Frobenius error <= 5e-3;
+  * n_valid: exact.
+The gradients pass through one bf16 rounding of dlogits (relative 2^-9 per element) before the
+tensor-core GEMMs, which puts the expected Frobenius error near 1e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+LOSS_RTOL = 2e-4
+GRAD_MAXABS = 1e-2
+GRAD_FROB = 5e-3
+
+
+def assert_scalar_close(got: float, ref: float, name: str, rtol: float = LOSS_RTOL, atol: float = 1e-6) -> None:
+    err = abs(float(got) - float(ref))
+    assert err <= max(rtol * abs(float(ref)), atol), f"{name}: got {got!r}, oracle {ref!r}, |err| {err:.3e}"
+
+
+def assert_grad_close(got, ref, name: str) -> None:
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, f"{name}: shape {g.shape} vs {r.shape}"
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    maxref = float(np.max(np.abs(r))) if r.size else 0.0
+    diff = g - r
+    maxerr = float(np.max(np.abs(diff))) if r.size else 0.0
+    if maxref == 0.0:
+        assert maxerr == 0.0, f"{name}: oracle is all zero, kernel max |value| {maxerr:.3e}"
+        return
+    assert maxerr <= GRAD_MAXABS * maxref, f"{name}: max-abs error {maxerr:.3e} > {GRAD_MAXABS} * {maxref:.3e}"
+    frob = float(np.linalg.norm(diff)) / float(np.linalg.norm(r))
+    assert frob <= GRAD_FROB, f"{name}: relative Frobenius error {frob:.3e} > {GRAD_FROB}"
+
+
+def bf16_tensor(bits: np.ndarray, device="cuda"):
+    """uint16 bf16 bit patterns -> torch bfloat16 tensor on the device (bit-exact)."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def bf16_to_numpy_f32(t) -> np.ndarray:
+    import torch
+    u = t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+    return (u.astype(np.uint32) << 16).view(np.float32)

@@ -1,0 +1,101 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/flce.h declares, sizes
+its workspaces, and rejects bad arguments with the documented codes before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_cross_entropy_tma_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+INVALID_ARG, MISALIGNED, WS_SMALL, UNSUPPORTED = 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from linear_cross_entropy_tma_gb300 import build
+        build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "flce.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(\w+)\s*\(", src, flags=re.M)) - {"defined"})
+
+
+def test_header_symbols_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(_lib.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_library_has_no_driver_dependency():
+    # the runtime is linked statically and the driver is reached through the runtime's entry-point
+    # query, so the library loads where no GPU driver exists
+    out = os.popen(f"ldd {_lib.LIB_PATH}").read()
+    assert "libcuda.so" not in out and "libcudart.so" not in out
+
+
+def test_workspace_sizes(lib):
+    assert lib.flce_workspace_size(-1, 8, 8) == 0
+    a = lib.flce_workspace_size(128, 64, 512)
+    b = lib.flce_workspace_size(65535, 1024, 176245)
+    assert 0 < a < b
+    # O(BT): no (BT, V) term
+    assert b < 64 * 1024 * 1024
+    assert lib.flce_workspace_size(65535, 1024, 176245) == lib.flce_workspace_size(65535, 64, 8)
+    assert lib.ce_workspace_size(8192, 128256) == 256 + 16 * 8192
+
+
+def _fwd(lib, hidden=0x1000, W=0x2000, bias=None, target=0x3000, BT=128, H=64, V=512, red=0, loss=0x4000,
+         gi=0x5000, gw=0x6000, gb=None, nv=None, ws=0x7000, wsb=1 << 30):
+    return lib.flce_fwd_bwd(hidden, W, bias, target, BT, H, V, -100, red, 0.0, loss, gi, gw, gb, nv, ws, wsb, None)
+
+
+def test_fwd_bwd_argument_errors(lib):
+    # (all of these are rejected before any CUDA call, so no GPU is needed)
+    assert _fwd(lib, W=None) == INVALID_ARG
+    assert _fwd(lib, loss=None) == INVALID_ARG
+    assert _fwd(lib, ws=None) == INVALID_ARG
+    assert _fwd(lib, BT=-1) == INVALID_ARG
+    assert _fwd(lib, V=0) == INVALID_ARG
+    assert _fwd(lib, red=2) == INVALID_ARG
+    assert _fwd(lib, gb=0x8000) == INVALID_ARG          # grad_bias without bias
+    assert _fwd(lib, gi=0x1000) == INVALID_ARG          # grad_input aliases hidden
+    assert _fwd(lib, H=60) == UNSUPPORTED               # H % 8 != 0
+    assert _fwd(lib, V=1 << 31) == UNSUPPORTED
+    assert _fwd(lib, hidden=0x1008) == MISALIGNED
+    assert _fwd(lib, ws=0x7010) == MISALIGNED
+    assert _fwd(lib, wsb=16) == WS_SMALL
+    assert b"workspace" in lib.flce_last_error()
+
+
+def test_ce_argument_errors(lib):
+    def ce(logits=0x1000, labels=0x2000, B=8, V=16, cs=0x3000, zs=0x3100, nv=0x3200, ws=0x4000, wsb=1 << 20):
+        return lib.ce_with_grad(logits, labels, B, V, -100, 0.0, cs, zs, nv, ws, wsb, None)
+
+    assert ce(logits=None) == INVALID_ARG
+    assert ce(nv=None) == INVALID_ARG
+    assert ce(V=0) == INVALID_ARG
+    assert ce(B=1 << 31) == UNSUPPORTED
+    assert ce(logits=0x1002) == MISALIGNED
+    assert ce(wsb=100) == WS_SMALL
+    assert lib.flce_read_device_status(None, None, None) == INVALID_ARG
+
+
+def test_status_strings(lib):
+    assert lib.flce_status_string(0) == b"FLCE_OK"
+    assert lib.flce_status_string(3) == b"FLCE_ERR_WORKSPACE_TOO_SMALL"
+    assert lib.flce_status_string(99) == b"FLCE_ERR_UNKNOWN"
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        _lib.load()

@@ -1,0 +1,194 @@
+"""Fused linear cross-entropy (flce_fwd_bwd) against the fp64 oracle on the GPU, through the C ABI.
+
+Element-by-element parity at sizes the oracle finishes in seconds (several tiles, ragged tails in
+BT, V and H, bias, z-loss, both reductions, degenerate cases), and at the full benchmark sizes on
+sampled outputs: the loss and n_valid, grad_input rows of sampled tokens and grad_W / grad_bias rows
+of sampled vocabulary entries (stored by tests/golden/make_expected.py, which calls only the oracle).
+"""
+import functools
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from linear_cross_entropy_tma_gb300 import workloads as wl
+from parity import assert_grad_close, assert_scalar_close, bf16_tensor, bf16_to_numpy_f32
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def flce():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for -m gpu tests")
+    import linear_cross_entropy_tma_gb300 as m
+    m.load()
+    return m
+
+
+def _upload(d):
+    import torch
+    hidden = bf16_tensor(d["hidden"])
+    W = bf16_tensor(d["W"])
+    target = torch.from_numpy(d["target"]).cuda()
+    bias = torch.from_numpy(d["bias"]).cuda() if d.get("bias") is not None else None
+    return hidden, W, target, bias
+
+
+def _run(flce, d, **kw):
+    import torch
+    hidden, W, target, bias = _upload(d)
+    out = flce.flce_fwd_bwd(hidden, W, target, bias=bias, ignore_index=d.get("ignore_index", -100),
+                            reduction=d["reduction"], z_loss=d["z_loss"], **kw)
+    torch.cuda.synchronize()
+    out["status"] = flce.read_device_status(out["workspace"])
+    return out
+
+
+def _synthetic(BT, H, V, bias, z_loss, reduction, ignore=(), bad=(), seed=0, h_std=1.0, w_std=0.02):
+    w = wl.FusedWorkload("case", BT=BT, H=H, V=V, hidden_std=h_std, w_std=w_std,
+                         bias_std=0.1 if bias else None, ignore_frac=0.0, z_loss=z_loss, reduction=reduction,
+                         seed=seed)
+    d = wl.make_fused_inputs(w)
+    for r in ignore:
+        d["target"][r] = -100
+    for r in bad:
+        d["target"][r] = V + 5
+    return d
+
+
+def _check_full(out, d):
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], reduction=d["reduction"],
+                                z_loss=d["z_loss"])
+    assert int(out["n_valid"].item()) == ref["n_valid"]
+    assert_scalar_close(out["loss"].item(), ref["loss"], "loss")
+    if out["grad_input"] is not None:
+        assert_grad_close(bf16_to_numpy_f32(out["grad_input"]), ref["grad_input"], "grad_input")
+    if out["grad_W"] is not None:
+        assert_grad_close(out["grad_W"].cpu().numpy(), ref["grad_W"], "grad_W")
+    if out["grad_bias"] is not None:
+        assert_grad_close(out["grad_bias"].cpu().numpy(), ref["grad_bias"], "grad_bias")
+    return ref
+
+
+CASES = {
+    # name: (BT, H, V, bias, z_loss, reduction, ignored rows)
+    "one-tile": (128, 64, 256, False, 0.0, "mean", (5,)),
+    "ragged-BT-V-bias-zloss": (300, 128, 1000, True, 1e-3, "mean", (0, 150, 299)),
+    "two-H-chunks-sum": (257, 320, 777, False, 0.0, "sum", (256,)),
+    "H-not-multiple-of-64": (64, 200, 300, True, 1e-2, "mean", ()),
+    "wide-H-bias": (96, 576, 513, True, 1e-4, "mean", (1, 2)),
+    "V-equals-1": (130, 64, 1, True, 1e-2, "sum", (3,)),
+    "many-vocab-tiles": (40, 64, 5000, False, 0.0, "mean", ()),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_flce_matches_oracle(flce, name):
+    BT, H, V, bias, zl, red, ign = CASES[name]
+    d = _synthetic(BT, H, V, bias, zl, red, ignore=ign, seed=BT * 7 + V)
+    out = _run(flce, d)
+    assert out["status"] == 0
+    _check_full(out, d)
+
+
+def test_flce_tiny_workload(flce):
+    d = wl.make_fused_inputs(wl.TINY)
+    out = _run(flce, d)
+    assert out["status"] == 0
+    ref = _check_full(out, d)
+    assert ref["n_valid"] == 122
+
+
+def test_flce_peaked_logits(flce):
+    # logits std ~8: the online max matters and the softmax is far from uniform
+    d = _synthetic(200, 256, 3000, True, 1e-4, "mean", ignore=(7,), seed=3, w_std=0.5)
+    out = _run(flce, d)
+    _check_full(out, d)
+
+
+def test_flce_all_ignored(flce):
+    d = _synthetic(150, 64, 700, True, 1e-3, "mean", ignore=range(150))
+    out = _run(flce, d)
+    assert int(out["n_valid"].item()) == 0 and out["loss"].item() == 0.0
+    assert np.all(bf16_to_numpy_f32(out["grad_input"]) == 0.0)
+    assert np.all(out["grad_W"].cpu().numpy() == 0.0)
+    assert np.all(out["grad_bias"].cpu().numpy() == 0.0)
+
+
+def test_flce_empty_batch(flce):
+    import torch
+    W = torch.randn(300, 64, device="cuda").to(torch.bfloat16)
+    hidden = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    target = torch.empty((0,), dtype=torch.int64, device="cuda")
+    bias = torch.randn(300, device="cuda")
+    out = flce.flce_fwd_bwd(hidden, W, target, bias=bias)
+    torch.cuda.synchronize()
+    assert out["loss"].item() == 0.0 and out["n_valid"].item() == 0
+    assert torch.count_nonzero(out["grad_W"]).item() == 0 and torch.count_nonzero(out["grad_bias"]).item() == 0
+
+
+def test_flce_bad_targets_flagged_and_ignored(flce):
+    d = _synthetic(140, 64, 400, False, 0.0, "mean", ignore=(2,), bad=(9, 130))
+    out = _run(flce, d)
+    assert out["status"] & flce.STATUS_BAD_TARGET
+    ref = _check_full(out, d)
+    assert ref["n_valid"] == 137
+
+
+def test_flce_output_subsets(flce):
+    d = _synthetic(160, 128, 900, True, 1e-3, "mean", ignore=(4,), seed=11)
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], z_loss=1e-3)
+    only_gi = _run(flce, d, need_grad_W=False)
+    assert only_gi["grad_W"] is None and only_gi["grad_bias"] is None
+    assert_scalar_close(only_gi["loss"].item(), ref["loss"], "loss")
+    assert_grad_close(bf16_to_numpy_f32(only_gi["grad_input"]), ref["grad_input"], "grad_input")
+    only_gw = _run(flce, d, need_grad_input=False)
+    assert only_gw["grad_input"] is None
+    assert_grad_close(only_gw["grad_W"].cpu().numpy(), ref["grad_W"], "grad_W")
+    assert_grad_close(only_gw["grad_bias"].cpu().numpy(), ref["grad_bias"], "grad_bias")
+    # grad_bias alone (grad_W NULL) goes through the C ABI directly
+    import torch
+    from linear_cross_entropy_tma_gb300 import _lib
+    hidden, W, target, bias = _upload(d)
+    loss = torch.empty(1, device="cuda")
+    gb = torch.empty(900, device="cuda")
+    ws = torch.empty(_lib.workspace_size(160, 128, 900), dtype=torch.uint8, device="cuda")
+    _lib.check(_lib.load().flce_fwd_bwd(hidden.data_ptr(), W.data_ptr(), bias.data_ptr(), target.data_ptr(), 160, 128,
+                                        900, -100, 0, 1e-3, loss.data_ptr(), None, None, gb.data_ptr(), None,
+                                        ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert_grad_close(gb.cpu().numpy(), ref["grad_bias"], "grad_bias only")
+
+
+@functools.lru_cache(maxsize=1)
+def _full_inputs(key):
+    return wl.make_fused_inputs(wl.FUSED_WORKLOADS[key])
+
+
+@pytest.mark.parametrize("key", ["qwen3", "gemma2", "long"])
+def test_flce_full_size_sampled(flce, key):
+    import torch
+    w = wl.FUSED_WORKLOADS[key]
+    exp = np.load(os.path.join(GOLDEN, f"expected_{key}.npz"))
+    d = _full_inputs(key)
+    assert wl.digest(d["hidden"], d["W"], d["bias"], d["target"]) == str(exp["digest"]), "input generator drifted"
+    out = _run(flce, d)
+    assert out["status"] == 0
+    assert int(out["n_valid"].item()) == int(exp["n_valid"]) == w.n_valid
+    assert_scalar_close(out["loss"].item(), float(exp["loss"]), "loss")
+    rows = torch.from_numpy(exp["rows"]).cuda()
+    assert_grad_close(bf16_to_numpy_f32(out["grad_input"][rows]), exp["grad_input_rows"], "grad_input rows")
+    vr = torch.from_numpy(exp["vocab_rows"]).cuda()
+    assert_grad_close(out["grad_W"][vr].cpu().numpy(), exp["grad_W_rows"], "grad_W rows")
+    if "grad_bias_rows" in exp.files:
+        assert_grad_close(out["grad_bias"][vr].cpu().numpy(), exp["grad_bias_rows"], "grad_bias rows")
+    # no (BT, V) buffer: the workspace is O(BT)
+    assert out["workspace"].numel() < 64 * 2**20
+    first = out["loss"].item()
+    del out
+    again = _run(flce, d, need_grad_input=False, need_grad_W=False)
+    assert again["loss"].item() == first, "loss is not deterministic"
