@@ -143,6 +143,35 @@ flce_status ce_with_grad(uint16_t* logits, const int64_t* labels, int64_t B, int
                          int64_t* n_valid, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * ce_with_grad without a workspace, for callers that cannot allocate device memory.
+ * (No counterpart on the pages: an addition of this library.)
+ *
+ * Some callers are never allowed to call cudaMalloc themselves: a plugin inside an engine whose
+ * device memory is planned ahead and which receives only its input and output buffers, or a
+ * service that forbids allocation after start-up because an allocation can block or fail at run
+ * time.  This call does the same work as ce_with_grad (same kernel, same results) but takes its
+ * scratch (per-row partial sums, status word, completion counter) from a fixed array inside the
+ * library instead of a workspace.  It allocates nothing.
+ *
+ *   Arguments, layout and results are those of ce_with_grad, without workspace/workspace_bytes.
+ *   B must not exceed FLCE_CE_NOALLOC_MAX_ROWS, else FLCE_ERR_UNSUPPORTED (flce_last_error() says
+ *   why); use ce_with_grad with a workspace for larger batches.
+ *   Memory: every GPU that loads the library holds the array (256 + 16 * FLCE_CE_NOALLOC_MAX_ROWS
+ *   bytes, 4 MiB) until the process exits.
+ *   The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
+ *   that device current) and remembers it; make that first call before any stream capture.
+ *   All calls share the one array, which keeps the previous call's contents; each call clears what
+ *   must start at zero.  Calls whose kernels can overlap on the GPU (e.g. on two streams without
+ *   ordering between them, or from two host threads) race on the array: serialise them.
+ *   The device status word cannot be read back through flce_read_device_status (there is no
+ *   workspace); labels outside [0, V) are still treated as ignored rows.
+ */
+#define FLCE_CE_NOALLOC_MAX_ROWS 262144
+flce_status ce_with_grad_noalloc(uint16_t* logits, const int64_t* labels, int64_t B, int64_t V,
+                                 int64_t ignore_index, float z_loss, float* ce_sum, float* z_sum,
+                                 int64_t* n_valid, void* stream);
+
+/*
  * Copy the device status word of a workspace used by a previous call to *host_status, after
  * synchronising `stream`.  0 means no data error and no timeout.
  */

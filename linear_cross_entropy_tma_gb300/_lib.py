@@ -17,7 +17,7 @@ FLCE_OK = 0
 STATUS_BAD_TARGET = 0x1
 STATUS_TIMEOUT = 0x2
 EXPORTED = ("flce_workspace_size", "flce_fwd_bwd", "flce_fwd_bwd_timed", "ce_workspace_size", "ce_with_grad",
-            "flce_read_device_status", "flce_status_string", "flce_last_error")
+            "flce_read_device_status", "flce_status_string", "flce_last_error", "ce_with_grad_noalloc")
 
 _lib = None
 
@@ -46,6 +46,8 @@ def load() -> ctypes.CDLL:
     lib.ce_workspace_size.argtypes = [c_i64, c_i64]
     lib.ce_with_grad.restype = ctypes.c_int
     lib.ce_with_grad.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, ctypes.c_float, c_p, c_p, c_p, c_p, c_sz, c_p]
+    lib.ce_with_grad_noalloc.restype = ctypes.c_int
+    lib.ce_with_grad_noalloc.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, ctypes.c_float, c_p, c_p, c_p, c_p]
     lib.flce_read_device_status.restype = ctypes.c_int
     lib.flce_read_device_status.argtypes = [c_p, ctypes.POINTER(ctypes.c_uint32), c_p]
     lib.flce_status_string.restype = ctypes.c_char_p

@@ -55,6 +55,8 @@ constexpr int64_t kMax32 = (int64_t(1) << 31) - 1;
 
 namespace flce {
 
+void set_last_error_message(const char* msg) { set_error("%s", msg); }
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
