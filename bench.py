@@ -298,9 +298,9 @@ def cpu_cores():
 
 def cpu_baseline(w: wl.FusedWorkload, target_s: float = 12.0):
     d = wl.make_fused_inputs(w)
-    t64 = time_oracle_tokens(w, d, 64)
-    n = int(max(64, min(w.BT, 64 * target_s / max(t64, 1e-3))))
-    n = min(n, 2048)
+    time_oracle_tokens(w, d, 32)
+    t256 = time_oracle_tokens(w, d, 256)
+    n = int(max(256, min(w.BT - 64, 256 * target_s / max(t256, 1e-3))))
     t = time_oracle_tokens(w, d, n, offset=64)
     return {"value": n / t, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
             "sample": f"fp64 oracle, full loss + grad_input + grad_W work for {n} of the {w.BT} tokens "
@@ -379,8 +379,8 @@ def main():
     # recomputes the logits (2*BT*V*H) and runs its GEMM (2*BT*V*H)
     alg = {"lse_partial": 2 * w.BT * w.V * w.H, "dgrad_grad_input": 4 * w.BT * w.V * w.H,
            "dgrad_grad_W": 4 * w.BT * w.V * w.H}
-    kname = {"lse_partial": "lse_partial_kernel", "dgrad_grad_input": "dgrad_kernel<false>",
-             "dgrad_grad_W": "dgrad_kernel<true>"}
+    kname = {"lse_partial": "lse_pair_kernel", "dgrad_grad_input": "dgrad_pair_kernel<false>",
+             "dgrad_grad_W": "dgrad_pair_kernel<true>"}
     src = kernel_source_digest(["flce_fwd.cu", "flce_bwd.cu", "sm100.cuh"])
     peak_tf = peaks["bf16_tflops_sustained"]
     achieved = alg[dominant] / (passes[dominant] * 1e-3) / 1e12

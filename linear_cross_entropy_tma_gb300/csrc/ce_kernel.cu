@@ -18,6 +18,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kCtasPerSm = 2;
 constexpr int kUnroll = 4;  // 16-byte vectors per thread in flight per step
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -95,7 +96,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return static_cast<uint16_t>(pack_bf16x2(f, 0.0f) & 0xFFFFu);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels, int64_t B, int64_t V,
                int64_t ignore_index, float z_loss, float4* __restrict__ row_out, uint32_t* __restrict__ status,
                uint32_t* __restrict__ done_counter, float* __restrict__ ce_sum, float* __restrict__ z_sum,
@@ -262,7 +263,7 @@ cudaError_t launch_ce_rows(uint16_t* logits, const int64_t* labels, int64_t B, i
     if ((e = cudaMemsetAsync(z_sum, 0, sizeof(float), stream)) != cudaSuccess) return e;
     return cudaMemsetAsync(n_valid, 0, sizeof(int64_t), stream);
   }
-  const int64_t cap = static_cast<int64_t>(num_sms) * 2;
+  const int64_t cap = static_cast<int64_t>(num_sms) * kCtasPerSm;
   const int64_t grid = B < cap ? B : cap;
   ce_rows_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(logits, labels, B, V, ignore_index, z_loss,
                                                                         row_out, status, counter, ce_sum, z_sum,

@@ -1,10 +1,11 @@
 // flce_fwd.cu -- forward passes of fused linear cross-entropy: per-row LSE without logits in HBM.
 //
-// lse_partial: one CTA per (128-token tile, vocabulary split).  A TMA producer warp streams
-// hidden[m-tile, k-block] and W[n-tile, k-block] (128-byte swizzled, 64-wide k-blocks) through a
-// 4-stage mbarrier ring; one thread of the MMA warp issues tcgen05.mma (M=128, N=256, K=16) into one
-// of two 256-column TMEM accumulators; eight epilogue warps read each finished tile with tcgen05.ld
-// and keep, per row, the online max / sum-exp update ("Fused Linear Cross-Entropy", "Forward -- one
+// lse_pair_kernel: one CTA pair (cluster of 2) per (256-token block, vocabulary split).  Each CTA's
+// TMA producer warp streams its 128 rows of hidden[k-block] and 128 of the 256 rows of W[n-tile,
+// k-block] (128-byte swizzled, 64-wide k-blocks) through a 6-stage mbarrier ring; one thread of the
+// even CTA issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) into one of two 256-column TMEM
+// accumulators in each CTA; eight epilogue warps per CTA read each finished tile with tcgen05.ld and
+// keep, per row, the online max / sum-exp update ("Fused Linear Cross-Entropy", "Forward -- one
 // Triton kernel, online softmax across vocab splits", steps 1-3) and the target logit when the tile
 // holds the target column.  Double-buffered accumulators let the epilogue of tile j overlap the MMAs
 // of tile j+1.
@@ -24,28 +25,12 @@ namespace {
 
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
-constexpr uint32_t kABytes = kTileM * kBK * 2;
-constexpr uint32_t kBBytes = kBN * kBK * 2;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 10 * 32;
 constexpr uint32_t kTmemCols = 512;
 
-struct LseSmem {
-  uint8_t stage[kStages][kStageBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort;
-  float2 half_ms[kTileM];
-};
-constexpr size_t kLseSmemBytes = sizeof(LseSmem) + 1024;
 
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
   const float mn = fmaxf(m, m2);
@@ -56,43 +41,68 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2)
   s = a + b;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-lse_partial_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
-                   const float* __restrict__ bias, const int64_t* __restrict__ target, int BT, int V,
-                   int64_t ignore_index, int num_kb, int tiles_per_split, int n_tiles, int BTp,
-                   float2* __restrict__ part, float* __restrict__ zy_out, uint32_t* __restrict__ status) {
+// ---------------------------------------------------------------------------------------------------
+// lse_pair_kernel: the same pass on CTA pairs (cluster of 2, cta_group::2 MMA, M = 256 tokens per
+// pair, N = 256 vocabulary entries per tile).  Each SM streams its own 128 token rows and 128 of the
+// tile's 256 vocabulary rows per k-block, half the shared-memory bytes per FLOP of the one-SM tile.
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairBox = kTileM * kBK * 2;   // 16 KiB
+constexpr uint32_t kPairStage = 2 * kPairBox;
+
+struct LsePairSmem {
+  uint8_t stage[kPairStages][kPairStage];
+  uint64_t full[kPairStages];
+  uint64_t empty[kPairStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  float2 half_ms[kTileM];
+};
+constexpr size_t kLsePairSmemBytes = sizeof(LsePairSmem) + 1024;
+static_assert(kLsePairSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
+                const float* __restrict__ bias, const int64_t* __restrict__ target, int BT, int V,
+                int64_t ignore_index, int num_kb, int tiles_per_split, int n_tiles, int BTp,
+                float2* __restrict__ part, float* __restrict__ zy_out, uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
-  LseSmem& sm = *reinterpret_cast<LseSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  LsePairSmem& sm =
+      *reinterpret_cast<LsePairSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x;
+  const int r0 = (blockIdx.x >> 1) * (2 * kTileM) + static_cast<int>(rank) * kTileM;
   const int split = blockIdx.y;
   const int t_begin = split * tiles_per_split;
   const int nt = max(0, min(n_tiles, t_begin + tiles_per_split) - t_begin);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kPairStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sm.acc_full[a], 1);
-      mbar_init(&sm.acc_empty[a], kEpiWarps);
+      mbar_init(&sm.acc_empty[a], 2 * kEpiWarps);
     }
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbarrier_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(&sm.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(&sm.tmem_base, kTmemCols);
+    tmem_relinquish_pair();
   }
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmap_h);
     tma_prefetch_desc(&tmap_w);
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
@@ -101,40 +111,39 @@ lse_partial_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_cons
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t filled = 0, last_phase = 0;  // per-stage bit masks, for draining after an abort
       bool ok = true;
       for (int j = 0; j < nt && ok; ++j) {
-        const int n0 = (t_begin + j) * kBN;
+        const int n0 = (t_begin + j) * kBN + static_cast<int>(rank) * kTileM;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.full[stage], kStageBytes);
-          tma_load_2d(sm.stage[stage], &tmap_h, &sm.full[stage], kb * kBK, m_tile * kTileM);
-          tma_load_2d(sm.stage[stage] + kABytes, &tmap_w, &sm.full[stage], kb * kBK, n0);
-          filled |= 1u << stage;
-          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
+          const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * kPairStage);
+          tma_load_2d_pair(sm.stage[stage], &tmap_h, fb, kb * kBK, r0);
+          tma_load_2d_pair(sm.stage[stage] + kPairBox, &tmap_w, fb, kb * kBK, n0);
+          if (++stage == kPairStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (!ok) {
-        for (int s = 0; s < kStages; ++s)
-          if (filled & (1u << s)) mbar_wait_drain(&sm.full[s], (last_phase >> s) & 1u);
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 50000ull) {
+        }
       }
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kBN, false, false);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kTileM, kBN, false, false);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int j = 0; j < nt && ok; ++j) {
         const int acc = j & 1;
-        if (!mbar_wait(&sm.acc_empty[acc], ((j >> 1) & 1) ^ 1, abort)) break;
+        if (!mbar_wait_cluster(&sm.acc_empty[acc], ((j >> 1) & 1) ^ 1, abort)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kBN);
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -144,29 +153,29 @@ lse_partial_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_cons
           }
           tc_fence_after();
           const uint32_t a_base = smem_u32(sm.stage[stage]);
-          const uint32_t b_base = a_base + kABytes;
+          const uint32_t b_base = a_base + kPairBox;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            mma_bf16_ss(d_tmem, sdesc_sw128(a_base + 32u * k, 16u, 1024u), sdesc_sw128(b_base + 32u * k, 16u, 1024u),
-                        idesc, (kb | k) != 0 ? 1u : 0u);
-          }
-          mma_commit(&sm.empty[stage]);
-          if (++stage == kStages) {
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_ss_pair(d_tmem, sdesc_sw128(a_base + 32u * k, 16u, 1024u),
+                             sdesc_sw128(b_base + 32u * k, 16u, 1024u), idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair(&sm.empty[stage]);
+          if (++stage == kPairStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) mma_commit(&sm.acc_full[acc]);
+        if (ok) mma_commit_pair(&sm.acc_full[acc]);
       }
-      mma_commit(&sm.drain);
+      mma_commit_pair(&sm.drain);
       mbar_wait_drain(&sm.drain, 0);
     }
   } else {
-    // ---------------------------------------------------------------------------- epilogue warps
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int h = warp >> 2; // which 128-column half of the tile
+    const int q = warp & 3;
+    const int h = warp >> 2;
     const int row_local = q * 32 + lane;
-    const int row = m_tile * kTileM + row_local;
+    const int row = r0 + row_local;
+    const uint32_t acc_empty_c0 = mapa_shared(smem_u32(&sm.acc_empty[0]), 0);
+    const uint32_t acc_empty_c1 = mapa_shared(smem_u32(&sm.acc_empty[1]), 0);
     int64_t y = -1;
     if (row < BT) {
       const int64_t t = target[row];
@@ -211,7 +220,7 @@ lse_partial_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_cons
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+      if (lane == 0) mbar_arrive_cluster(acc ? acc_empty_c1 : acc_empty_c0);
     }
     if (h == 1) sm.half_ms[row_local] = make_float2(m, s);
     named_barrier_sync(1, kEpiWarps * 32);
@@ -224,10 +233,10 @@ lse_partial_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_cons
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
   if (threadIdx.x == 0 && sm.abort) atomicOr(status, kStatusTimeout);
 }
@@ -237,7 +246,11 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, int splits, in
                                  float z_loss, float4* __restrict__ stats, float* __restrict__ row_loss,
                                  uint32_t* __restrict__ status) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= BT) return;
+  if (t >= BT) {
+    // padding rows (up to a multiple of 256 tokens) read by the gradient passes: no contribution
+    if (t < ((BT + 255) & ~255)) stats[t] = make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+    return;
+  }
   float M = -INFINITY;
   for (int s = 0; s < splits; ++s) M = fmaxf(M, part[static_cast<size_t>(s) * BTp + t].x);
   float S = 0.f;
@@ -322,7 +335,7 @@ size_t fused_workspace_bytes(int64_t BT) {
   size_t off = 256;
   off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
   off += align_up(sizeof(float) * btp, 256);
-  off += align_up(sizeof(float4) * btp, 256);
+  off += align_up(sizeof(float4) * align_up(btp, 256), 256);
   off += align_up(sizeof(float) * btp, 256);
   return off;
 }
@@ -340,7 +353,7 @@ FusedWorkspace carve_workspace(void* base, int64_t BT) {
   w.zy = reinterpret_cast<float*>(p + off);
   off += align_up(sizeof(float) * btp, 256);
   w.stats = reinterpret_cast<float4*>(p + off);
-  off += align_up(sizeof(float4) * btp, 256);
+  off += align_up(sizeof(float4) * align_up(btp, 256), 256);
   w.row_loss = reinterpret_cast<float*>(p + off);
   return w;
 }
@@ -354,16 +367,16 @@ cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int 
   if (BT > 0) {
     CUtensorMap tm_h, tm_w;
     if (!make_tmap_bf16(&tm_h, a.hidden, a.BT, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16(&tm_w, a.W, a.V, a.H, kBN, err, err_len)) return cudaErrorInvalidValue;
-    const int m_tiles = BTp / kTileM;
+    if (!make_tmap_bf16(&tm_w, a.W, a.V, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;
+    const int pairs = (BT + 2 * kTileM - 1) / (2 * kTileM);
     const int n_tiles = (V + kBN - 1) / kBN;
-    const int splits = choose_splits(m_tiles, n_tiles, num_sms);
+    const int splits = choose_splits(pairs, n_tiles, num_sms / 2);
     const int tps = (n_tiles + splits - 1) / splits;
     const int num_kb = static_cast<int>((a.H + kBK - 1) / kBK);
-    e = cudaFuncSetAttribute(lse_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kLseSmemBytes));
+    e = cudaFuncSetAttribute(lse_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kLsePairSmemBytes));
     if (e != cudaSuccess) return e;
-    lse_partial_kernel<<<dim3(m_tiles, splits), kThreads, kLseSmemBytes, stream>>>(
+    lse_pair_kernel<<<dim3(2 * pairs, splits), kThreads, kLsePairSmemBytes, stream>>>(
         tm_h, tm_w, a.bias, a.target, BT, V, a.ignore_index, num_kb, tps, n_tiles, BTp, ws.part, ws.zy, ws.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;

@@ -31,7 +31,8 @@ struct FusedWorkspace {
   int64_t* n_valid;  // header: valid count
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
   float* zy;         // [BTp] target logit
-  float4* stats;     // [BTp] (LSE * log2 e, 1 + 2 z_loss LSE, valid ? 1 : 0, target as int bits)
+  float4* stats;     // [BT rounded up to 256] (LSE * log2 e, 1 + 2 z_loss LSE, valid ? 1 : 0, target as
+                     // int bits); rows past BT hold (0, 0, 0, -1)
   float* row_loss;   // [BTp] valid * (LSE - z_y + z_loss LSE^2)
 };
 
@@ -53,6 +54,25 @@ struct FusedArgs {
   float* grad_bias;
   int64_t* n_valid_out;
 };
+
+// Arguments of the gradient passes on CTA pairs (flce_bwd2.cu).
+struct DgPairArgs {
+  const float* bias;
+  const float4* stats;
+  const float* scale;
+  int BT, V, H;
+  uint16_t* grad_input;
+  float* grad_W;
+  float* grad_bias;
+  uint32_t* status;
+};
+
+// kVocabRows = false: grad_input pass (rows = tokens, reduction over the vocabulary);
+// true: grad_W / grad_bias pass (rows = vocabulary entries, reduction over tokens).
+// rows / cols: tensor maps with 128-row x 64-column boxes of the row and column matrices.
+template <bool kVocabRows>
+cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, const DgPairArgs& a,
+                              cudaStream_t stream);
 
 // Encodes a 2-D bf16 tensor map (rows x cols, row-major) with a box of box_rows x 64 columns and
 // 128-byte swizzle.  Returns false (and fills err) when the driver refuses the descriptor.

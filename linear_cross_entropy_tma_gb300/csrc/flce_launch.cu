@@ -1,0 +1,58 @@
+// flce_launch.cu -- enqueues every pass of one flce_fwd_bwd call on the caller's stream:
+//   header clear -> LSE tiles (flce_fwd.cu) -> split merge -> loss reduction
+//   -> grad_input pass -> grad_W / grad_bias pass (flce_bwd.cu)
+// with optional caller events at the pass boundaries.  No host synchronisation, no allocation.
+#include "flce_kernels.cuh"
+
+namespace flce {
+
+cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int num_sms, cudaStream_t stream,
+                              char* err, size_t err_len, cudaEvent_t const* events);
+
+cudaError_t launch_fused(const FusedArgs& a, void* workspace, int num_sms, cudaStream_t stream, char* err,
+                         size_t err_len, cudaEvent_t const* events) {
+  const FusedWorkspace ws = carve_workspace(workspace, a.BT);
+  auto mark = [&](int i) { return events != nullptr ? cudaEventRecord(events[i], stream) : cudaSuccess; };
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, stream);
+  if (e != cudaSuccess) return e;
+  if ((e = mark(0)) != cudaSuccess) return e;
+  if ((e = launch_lse_passes(a, ws, num_sms, stream, err, err_len, events)) != cudaSuccess) return e;
+  if ((e = mark(2)) != cudaSuccess) return e;
+
+  const bool want_dw = (a.grad_W != nullptr) || (a.grad_bias != nullptr);
+  if (a.BT == 0) {
+    // no tokens: every gradient is zero
+    if (a.grad_W != nullptr && (e = cudaMemsetAsync(a.grad_W, 0, sizeof(float) * a.V * a.H, stream)) != cudaSuccess)
+      return e;
+    if (a.grad_bias != nullptr && (e = cudaMemsetAsync(a.grad_bias, 0, sizeof(float) * a.V, stream)) != cudaSuccess)
+      return e;
+    if ((e = mark(3)) != cudaSuccess) return e;
+    return mark(4);
+  }
+  DgPairArgs pa{};
+  pa.bias = a.bias;
+  pa.stats = ws.stats;
+  pa.scale = ws.scale;
+  pa.BT = static_cast<int>(a.BT);
+  pa.V = static_cast<int>(a.V);
+  pa.H = static_cast<int>(a.H);
+  pa.grad_input = a.grad_input;
+  pa.grad_W = a.grad_W;
+  pa.grad_bias = a.grad_bias;
+  pa.status = ws.status;
+  CUtensorMap tm_h128, tm_w128;
+  if (a.grad_input != nullptr || want_dw) {
+    if (!make_tmap_bf16(&tm_h128, a.hidden, a.BT, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tm_w128, a.W, a.V, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;
+  }
+  if (a.grad_input != nullptr) {
+    if ((e = launch_dgrad_pair<false>(tm_h128, tm_w128, pa, stream)) != cudaSuccess) return e;
+  }
+  if ((e = mark(3)) != cudaSuccess) return e;
+  if (want_dw) {
+    if ((e = launch_dgrad_pair<true>(tm_w128, tm_h128, pa, stream)) != cudaSuccess) return e;
+  }
+  return mark(4);
+}
+
+}  // namespace flce
