@@ -3,10 +3,13 @@
 // fp32 online max/sum across the row, warp reductions to the row LSE, a second pass that overwrites
 // the logits with dlogits; z-loss scales the softmax term before the target column is adjusted).
 //
-// GB300 shape of it: a persistent grid of two 512-thread CTAs per SM walks the rows.  Pass 1 streams
-// the row with 16-byte loads tagged to stay in L2, pass 2 re-reads it (an L2 hit: at most
-// 2 x 152 rows x 250 KB = 76 MB are in flight, well under the 126 MB L2) and writes dlogits with
-// 16-byte stores tagged evict-first.  HBM therefore sees one read and one write of the logits.
+// GB300 shape of it: a persistent grid of two 512-thread CTAs per SM walks the rows.  The first 96 KiB
+// of each row (its "head") is fetched into shared memory by one bulk copy, issued as soon as the
+// previous row no longer needs the buffer; pass 1 streams the rest of the row with 16-byte loads
+// tagged to stay in L2 while the head lands, then reads the head from shared memory; pass 2 writes
+// the head's dlogits from shared memory and re-reads the rest (an L2 hit: about 2 x 152 x 154 KB
+// = 47 MB of rows are in flight), storing with 16-byte stores tagged evict-first.  HBM therefore
+// sees one read and one write of the logits.
 // Per-row (ce, LSE^2, valid) land in the workspace; the last CTA to finish sums them in a fixed
 // order (float64), so the three outputs are deterministic.
 #include "ce_kernel.cuh"
@@ -19,6 +22,10 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCtasPerSm = 2;
+// The first kCacheVec 16-byte vectors of each row are kept in shared memory between the two passes
+// (80 KiB per CTA), so only the rest of the row is read a second time.
+constexpr int kCacheVec = 5120;
+constexpr size_t kCacheBytes = static_cast<size_t>(kCacheVec) * 16u;
 constexpr int kUnroll = 4;  // 16-byte vectors per thread in flight per step
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -58,16 +65,16 @@ __device__ __forceinline__ void accumulate8(const uint4 v, float& m, float& s) {
   float x[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    x[2 * i] = bf16_lo(w[i]) * kLog2e;
-    x[2 * i + 1] = bf16_hi(w[i]) * kLog2e;
+    x[2 * i] = bf16_lo(w[i]);
+    x[2 * i + 1] = bf16_hi(w[i]);
   }
   float cm = x[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) cm = fmaxf(cm, x[i]);
-  const float mn = fmaxf(m, cm);
+  const float mn = fmaxf(m, cm * kLog2e);
   float acc = s * ex2_approx(m - mn);  // m = -inf on the first call gives 0 * 0
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc += ex2_approx(x[i] - mn);
+  for (int i = 0; i < 8; ++i) acc += ex2_approx(fmaf(x[i], kLog2e, -mn));
   m = mn;
   s = acc;
 }
@@ -75,16 +82,20 @@ __device__ __forceinline__ void accumulate8(const uint4 v, float& m, float& s) {
 // dlogits of 8 consecutive columns starting at column c0 (softmax * zf - onehot).
 __device__ __forceinline__ uint4 grad8(const uint4 v, int64_t c0, int64_t y, float lse2, float zf) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[4];
+  float g[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float a = ex2_approx(fmaf(bf16_lo(w[i]), kLog2e, -lse2)) * zf;
-    float b = ex2_approx(fmaf(bf16_hi(w[i]), kLog2e, -lse2)) * zf;
-    if (c0 + 2 * i == y) a -= 1.0f;
-    if (c0 + 2 * i + 1 == y) b -= 1.0f;
-    o[i] = pack_bf16x2(a, b);
+    g[2 * i] = ex2_approx(fmaf(bf16_lo(w[i]), kLog2e, -lse2)) * zf;
+    g[2 * i + 1] = ex2_approx(fmaf(bf16_hi(w[i]), kLog2e, -lse2)) * zf;
   }
-  return make_uint4(o[0], o[1], o[2], o[3]);
+  const uint64_t t = static_cast<uint64_t>(y - c0);  // target column relative to c0
+  if (t < 8u) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (static_cast<uint64_t>(i) == t) g[i] -= 1.0f;
+  }
+  return make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]),
+                    pack_bf16x2(g[6], g[7]));
 }
 
 __device__ __forceinline__ float grad1(uint16_t raw, int64_t c, int64_t y, float lse2, float zf) {
@@ -101,6 +112,8 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
                int64_t ignore_index, float z_loss, float4* __restrict__ row_out, uint32_t* __restrict__ status,
                uint32_t* __restrict__ done_counter, float* __restrict__ ce_sum, float* __restrict__ z_sum,
                int64_t* __restrict__ n_valid) {
+  extern __shared__ uint4 s_cache[];  // kCacheVec vectors of the current row
+  __shared__ uint64_t s_head_bar;
   __shared__ float s_m[kWarps], s_s[kWarps];
   __shared__ float s_lse2;
   __shared__ float s_zy;
@@ -112,6 +125,34 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
   const int warp = tid >> 5;
   const uint64_t keep = policy_evict_last();
   const uint64_t drop = policy_evict_first();
+
+  // Head of row r: the first min(kCacheVec, nvec) 16-byte vectors of its aligned part.
+  auto head_bytes = [&](int64_t r, const uint4*& src) -> uint32_t {
+    const int64_t y = labels[r];
+    if (!((y != ignore_index) && (y >= 0) && (y < V))) return 0u;
+    const uint16_t* rw = logits + r * V;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(rw);
+    const int64_t hd_raw = static_cast<int64_t>(((16u - (a & 15u)) & 15u) >> 1);
+    const int64_t hd = hd_raw < V ? hd_raw : V;
+    const int64_t nv = (V - hd) >> 3;
+    src = reinterpret_cast<const uint4*>(rw + hd);
+    return static_cast<uint32_t>((nv < kCacheVec ? nv : kCacheVec) * 16);
+  };
+  if (tid == 0) {
+    mbar_init(&s_head_bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  uint32_t head_phase = 0;
+  volatile int no_abort = 0;
+  if (tid == 0 && blockIdx.x < B) {
+    const uint4* src = nullptr;
+    const uint32_t bytes = head_bytes(blockIdx.x, src);
+    if (bytes) {
+      mbar_arrive_expect_tx(&s_head_bar, bytes);
+      bulk_load_1d_hint(s_cache, src, bytes, &s_head_bar, keep);
+    }
+  }
 
   for (int64_t r = blockIdx.x; r < B; r += gridDim.x) {
     const int64_t y = labels[r];
@@ -129,6 +170,16 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
       if (tid == 0) {
         if (y != ignore_index) atomicOr(status, kStatusBadTarget);
         row_out[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        // no head was fetched for this row; fetch the next row's head now
+        if (r + gridDim.x < B) {
+          const uint4* src = nullptr;
+          const uint32_t bytes = head_bytes(r + gridDim.x, src);
+          if (bytes) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&s_head_bar, bytes);
+            bulk_load_1d_hint(s_cache, src, bytes, &s_head_bar, keep);
+          }
+        }
       }
       for (int64_t i = tid; i < nvec; i += kThreads) st16_hint(vrow + i, make_uint4(0, 0, 0, 0), drop);
       for (int64_t c = tid; c < head; c += kThreads) row[c] = 0;
@@ -148,7 +199,9 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
       const float x = __uint_as_float(static_cast<uint32_t>(row[c]) << 16) * kLog2e;
       merge_ms(m, s, x, 1.0f);
     }
-    int64_t i = tid;
+    const int64_t ncache = nvec < kCacheVec ? nvec : kCacheVec;
+    // the tail (vectors ncache..nvec-1) from global memory while the head's bulk copy lands
+    int64_t i = ncache + tid;
     for (; i + (kUnroll - 1) * kThreads < nvec; i += kUnroll * kThreads) {
       uint4 v[kUnroll];
 #pragma unroll
@@ -157,6 +210,12 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
       for (int u = 0; u < kUnroll; ++u) accumulate8(v[u], m, s);
     }
     for (; i < nvec; i += kThreads) accumulate8(ld16_hint(vrow + i, keep), m, s);
+    // the head from shared memory
+    if (ncache > 0) {
+      if (!mbar_wait(&s_head_bar, head_phase, &no_abort) && (tid & 31) == 0) atomicOr(status, kStatusTimeout);
+      head_phase ^= 1u;
+      for (int64_t k = tid; k < ncache; k += kThreads) accumulate8(s_cache[k], m, s);
+    }
 
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -192,7 +251,20 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
     // ---- pass 2: overwrite with dlogits
     for (int64_t c = tid; c < head; c += kThreads) row[c] = f32_to_bf16_bits(grad1(row[c], c, y, lse2, zf));
     for (int64_t c = tail0 + tid; c < V; c += kThreads) row[c] = f32_to_bf16_bits(grad1(row[c], c, y, lse2, zf));
-    i = tid;
+    for (int64_t k = tid; k < ncache; k += kThreads)
+      st16_hint(vrow + k, grad8(s_cache[k], head + k * 8, y, lse2, zf), drop);
+    // every thread is done reading the cache: start copying the head of this CTA's next row
+    __syncthreads();
+    if (tid == 0 && r + gridDim.x < B) {
+      const uint4* src = nullptr;
+      const uint32_t bytes = head_bytes(r + gridDim.x, src);
+      if (bytes) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&s_head_bar, bytes);
+        bulk_load_1d_hint(s_cache, src, bytes, &s_head_bar, keep);
+      }
+    }
+    i = ncache + tid;
     for (; i + (kUnroll - 1) * kThreads < nvec; i += kUnroll * kThreads) {
       uint4 v[kUnroll];
 #pragma unroll
@@ -263,11 +335,13 @@ cudaError_t launch_ce_rows(uint16_t* logits, const int64_t* labels, int64_t B, i
     if ((e = cudaMemsetAsync(z_sum, 0, sizeof(float), stream)) != cudaSuccess) return e;
     return cudaMemsetAsync(n_valid, 0, sizeof(int64_t), stream);
   }
+  e = cudaFuncSetAttribute(ce_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kCacheBytes));
+  if (e != cudaSuccess) return e;
   const int64_t cap = static_cast<int64_t>(num_sms) * kCtasPerSm;
   const int64_t grid = B < cap ? B : cap;
-  ce_rows_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(logits, labels, B, V, ignore_index, z_loss,
-                                                                        row_out, status, counter, ce_sum, z_sum,
-                                                                        n_valid);
+  ce_rows_kernel<<<static_cast<unsigned>(grid), kThreads, kCacheBytes, stream>>>(
+      logits, labels, B, V, ignore_index, z_loss, row_out, status, counter, ce_sum, z_sum, n_valid);
   return cudaGetLastError();
 }
 
