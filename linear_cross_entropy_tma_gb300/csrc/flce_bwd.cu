@@ -318,8 +318,8 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       if (row < p.BT) {
         const float4 st = p.stats[row];
         row_lse2 = st.x;
-        row_zf = st.y;
-        row_coef = st.z * scale;
+        row_zf = st.y;              // valid * (1 + 2 z_loss LSE)
+        row_coef = st.z * scale;    // s * valid
         row_y = __float_as_int(st.w);
       }
     } else {

@@ -181,6 +181,7 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
       const int64_t t = target[row];
       if (t != ignore_index && t >= 0 && t < V) y = t;
     }
+    const bool has_bias = (bias != nullptr);
     float m = -INFINITY, s = 0.f, zy = 0.f;
     bool found = false;
     for (int j = 0; j < nt; ++j) {
@@ -195,25 +196,31 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
         tmem_ld_32cols(taddr + 32u * c, r);
         tmem_wait_ld();
         const int col0 = n0 + 32 * c;
+        // One range test per 32-column chunk: the vocabulary tail and the target column.
+        const bool full = col0 + 32 <= V;
+        const bool has_y = static_cast<uint64_t>(y - col0) < 32u;
         float x[32];
         float cm = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int col = col0 + i;
           float v = __uint_as_float(r[i]);
-          if (bias != nullptr && col < V) v += __ldg(bias + col);
-          if (col == y) {
-            zy = v;
-            found = true;
-          }
-          x[i] = (col < V) ? v * kLog2e : -INFINITY;
-          cm = fmaxf(cm, x[i]);
+          if (has_bias && (full || col0 + i < V)) v += __ldg(bias + col0 + i);
+          if (!full && col0 + i >= V) v = -INFINITY;
+          x[i] = v;
+          cm = fmaxf(cm, v);
         }
-        const float mn = fmaxf(m, cm);
+        if (has_y) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col0 + i == static_cast<int>(y)) zy = x[i];
+          found = true;
+        }
+        // log2 e > 0, so the max of the scaled values is the scaled max
+        const float mn = fmaxf(m, cm * kLog2e);
         if (mn != -INFINITY) {
           float acc_s = (m == -INFINITY) ? 0.f : s * ex2_approx(m - mn);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc_s += ex2_approx(x[i] - mn);
+          for (int i = 0; i < 32; ++i) acc_s += ex2_approx(fmaf(x[i], kLog2e, -mn));
           s = acc_s;
           m = mn;
         }
@@ -264,7 +271,8 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, int splits, in
   const bool valid = (y != ignore_index) && (y >= 0) && (y < V);
   if (!valid && y != ignore_index) atomicOr(status, kStatusBadTarget);
   row_loss[t] = valid ? (lse - zy[t]) + z_loss * lse * lse : 0.f;
-  stats[t] = make_float4(lse2, 1.0f + 2.0f * z_loss * lse, valid ? 1.f : 0.f, __int_as_float(valid ? static_cast<int>(y) : -1));
+  stats[t] = make_float4(lse2, valid ? 1.0f + 2.0f * z_loss * lse : 0.f, valid ? 1.f : 0.f,
+                         __int_as_float(valid ? static_cast<int>(y) : -1));
 }
 
 constexpr int kReduceThreads = 1024;

@@ -31,7 +31,7 @@ struct FusedWorkspace {
   int64_t* n_valid;  // header: valid count
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
   float* zy;         // [BTp] target logit
-  float4* stats;     // [BT rounded up to 256] (LSE * log2 e, 1 + 2 z_loss LSE, valid ? 1 : 0, target as
+  float4* stats;     // [BT rounded up to 256] (LSE * log2 e, valid ? 1 + 2 z_loss LSE : 0, valid ? 1 : 0, target as
                      // int bits); rows past BT hold (0, 0, 0, -1)
   float* row_loss;   // [BTp] valid * (LSE - z_y + z_loss LSE^2)
 };
