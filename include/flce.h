@@ -67,8 +67,9 @@ typedef enum flce_status {
 #define FLCE_STATUS_TIMEOUT 0x2u
 
 /*
- * Bytes of workspace flce_fwd_bwd needs for these sizes (O(BT) floats: per-row LSE statistics,
- * per-row loss terms, the status word and the valid count).  Returns 0 for negative sizes.
+ * Bytes of workspace flce_fwd_bwd needs for these sizes (O(BT + V) floats: per-row LSE statistics,
+ * per-row loss terms, the per-column bias in log2 units, the status word and the valid count).
+ * Returns 0 for negative sizes.
  */
 size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V);
 

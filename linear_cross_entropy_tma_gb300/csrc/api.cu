@@ -95,7 +95,7 @@ extern "C" {
 
 size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V) {
   if (BT < 0 || H < 0 || V < 0) return 0;
-  return flce::fused_workspace_bytes(BT);
+  return flce::fused_workspace_bytes(BT, V);
 }
 
 static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const float* bias, const int64_t* target,

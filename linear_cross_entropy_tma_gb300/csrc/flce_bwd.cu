@@ -15,15 +15,24 @@
 //     column block j is computed once, by pair (j mod P):
 //       GEMM1   S[256, 256] = rows[256, H] . cols[256, H]^T          (TMEM, 256 columns)
 //       epi     dS = f(S, statistics) in registers -> bf16 in shared memory, in the 128-byte-swizzled
-//               K-major layout of the next MMA's A operand; then copied with cp.async.bulk into the
-//               same buffer of the other P-1 pairs' CTAs (distributed shared memory, never HBM)
+//               K-major layout of the next MMA's A operand; each 128-column half is then copied with
+//               cp.async.bulk into the same buffer of the other P-1 pairs' CTAs (distributed shared
+//               memory, never HBM)
 //     and every pair accumulates its own H chunk:
 //       GEMM2   O[256, 256] += dS[256, 256] . cols[256, chunk]      (TMEM, 256 columns, fp32)
 //     So the logits of each (row block, column block) are computed ceil(H / (256 P)) times instead of
 //     ceil(H / 256) times.
-//   * dS buffers form a ring of one or two per CTA: every pair's GEMM2 of block j commits, with
-//     multicast to all CTAs of the cluster, on that buffer's "ds_free"; the owner of the next block
-//     that uses the buffer writes and sends only after all P commits.
+//   * Issue order of a pair's tensor-core work, in steps s = -2P .. n_blocks-1:
+//       step s:  GEMM2 of block s (two 128-column halves), then 1/P of the k-blocks of GEMM1 of the
+//                pair's own block in [s+P+1, s+2P]
+//     so every step carries the same amount of work, and the logits of block j are complete P steps
+//     before any pair needs dS of block j: the owner's epilogue computes dS early, stores and sends
+//     it as soon as block j-1 has left the dS slots, and the copies overlap the GEMM1 share of step
+//     j-1.
+//   * The dS buffer holds one block as two half slots.  Every pair's GEMM2 of half h of block j
+//     commits on "ds_free[h]" of the pair that writes block j+1 (its owner), and only there, so each
+//     ds_free barrier completes exactly one phase per block its CTA writes: the owner's parity waits
+//     can never be two phases behind or ahead.
 //   * grad_bias (vocabulary rows) is each CTA's fp32 row sum of dS over the blocks it owns, gathered
 //     across the pairs in distributed shared memory and added in pair order (deterministic).
 // All waits are bounded; a wait that gives up flags the status word and the kernel winds down.
@@ -37,30 +46,25 @@ namespace {
 constexpr int kPN = 256;                      // logits tile columns = K of GEMM2 per block
 constexpr int kBK = 64;
 constexpr int kHc = 256;                      // H columns per pair (GEMM2 N)
-// Pairs per cluster.  Sharing logits tiles across P > 1 pairs is implemented and correct, but on GB300
-// it measured slower than recomputing them (P = 2: 68 ms vs 62 ms clock-adjusted per gradient pass at
-// the long workload; P = 4: 106 ms): a pair's in-order MMA stream can hold the GEMM2 another pair is
-// waiting for behind an 8192-cycle GEMM1, and the distributed-shared-memory copies run near 25 B/clk
-// per SM.  One pair per cluster is used.
-constexpr int kMaxPairs = 1;
+constexpr int kMaxPairs = 4;                  // pairs per cluster that share each logits tile
 constexpr uint32_t kBox = kTileM * kBK * 2;   // 16 KiB: a 128-row x 64-column bf16 box
 constexpr uint32_t kStage = 2 * kBox;
-constexpr uint32_t kDsBytes = kTileM * kPN * 2;
+constexpr uint32_t kHalfBytes = 2 * kBox;     // one 128-column half of a dS block (per CTA)
+constexpr uint32_t kDsBytes = 2 * kHalfBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kRecvWarp = 10;
+constexpr int kThreads = 11 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
 
 // Shared memory per CTA: an operand ring (5 stages of 32 KiB for the grad_input pass, 4 for the grad_W
-// pass, which also stages each owned block's 256 per-token statistics in a two-slot ring and gathers
-// grad_bias partials) and the dS buffer ring (kDsBuf buffers of 64 KiB; two allow block j+1 to be
-// produced and sent while the pairs' GEMM2 still read block j, measured no faster at P = 1).
+// pass, which also stages each owned block's 256 per-token statistics in a two-slot ring) and the dS
+// block (two 32 KiB half slots).
 template <bool kVocabRows>
 struct PairCfg {
-  static constexpr int kDsBuf = 1;                         // dS buffers (a ring) per CTA
   static constexpr int kStages = kVocabRows ? 4 : 5;
   static constexpr int kStatSlots = kVocabRows ? 2 : 1;
   static constexpr int kStatCols = kVocabRows ? kPN : 4;
@@ -70,7 +74,7 @@ struct PairCfg {
 template <bool kVocabRows>
 struct PairSmem {
   uint8_t stage[PairCfg<kVocabRows>::kStages][kStage];
-  uint8_t ds[PairCfg<kVocabRows>::kDsBuf][kDsBytes];
+  uint8_t ds[kDsBytes];
   float4 colstats[PairCfg<kVocabRows>::kStatSlots][PairCfg<kVocabRows>::kStatCols];
   float gb_gather[PairCfg<kVocabRows>::kGather][kTileM];
   uint64_t full[PairCfg<kVocabRows>::kStages];
@@ -79,9 +83,9 @@ struct PairSmem {
   uint64_t st_empty[2];
   uint64_t s_full;
   uint64_t s_empty;
-  uint64_t ds_full[PairCfg<kVocabRows>::kDsBuf];
-  uint64_t ds_free[PairCfg<kVocabRows>::kDsBuf];
-  uint64_t rx_full[PairCfg<kVocabRows>::kDsBuf];
+  uint64_t ds_full[2];
+  uint64_t ds_free[2];
+  uint64_t rx_full[2];
   uint64_t o_full;
   uint64_t drain;
   uint32_t tmem_base;
@@ -96,7 +100,9 @@ static_assert(pair_smem_bytes<true>() <= 232448, "shared memory budget of one CT
 struct PairParams {
   const float* bias;
   const float4* stats;
+  const float* colb2;
   const float* scale;
+  const uint32_t* zf_neg;
   int BT, V, H;
   int n_rows, n_cols, num_kb;
   int P;                    // pairs per cluster
@@ -105,12 +111,104 @@ struct PairParams {
   float* grad_bias;
 };
 
+// The block whose GEMM1 pair `pr` works on in step s (the one it owns in [s+P+1, s+2P]) and which
+// share (0 .. P-1) of that block's k-blocks belongs to this step.  The logits of block j are then
+// complete P steps before GEMM2 of block j, so the owner has time to turn them into dS and send
+// them; and the owner's previous block j-P left the dS slots at step j-P-1, before the first share of
+// its next GEMM1 (step j-P+1) needs the logits buffer back, so that GEMM1 never waits on a store.
+struct G1Share {
+  int block;
+  int prog;
+};
+__device__ __forceinline__ G1Share g1_share(int s, int pr, int P) {
+  const int lead = P + 1;
+  int d = (pr - (s + lead)) % P;
+  if (d < 0) d += P;
+  return G1Share{s + lead + d, P - 1 - d};
+}
+__device__ __forceinline__ int share_begin(int prog, int num_kb, int P) { return (prog * num_kb) / P; }
+
+// Row constants of the dS arithmetic of one epilogue thread.
+struct DsRow {
+  float c;      // grad_input pass: log2(s f) - LSE2 (-inf for ignored rows); grad_W pass: b log2 e + log2 s
+  float f;      // grad_input pass, general form: valid * f
+  float lse2;   // grad_input pass, general form: LSE log2 e
+  float coef;   // grad_input pass, general form: s * valid
+  float bias2;  // grad_W pass, general form: b log2 e
+  float scale;  // s
+  int y;        // grad_input pass: target column (-1 if none); grad_W pass: this row's vocabulary index
+};
+
+// dS of 64 consecutive logits of one row, in place (fp32 bits in, fp32 bits out).
+//   grad_input pass (rows = tokens): columns col0.. are vocabulary entries; colb2 holds the bias in
+//     log2 units (-inf past V); `plain` means no bias and no column past V in this chunk.
+//   grad_W pass (rows = vocabulary): columns are tokens; tstats holds their statistics.
+template <bool kVocabRows>
+__device__ __forceinline__ void ds_chunk64(uint32_t (&r)[64], int col0, const DsRow& rc, bool general, bool plain,
+                                           const float* __restrict__ colb2, const float4* tstats, float& gbias) {
+  if (!kVocabRows) {
+    if (general) {
+#pragma unroll
+      for (int i4 = 0; i4 < 16; ++i4) {
+        const float4 b = __ldg(reinterpret_cast<const float4*>(colb2 + col0) + i4);
+        const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = 4 * i4 + k;
+          const float e = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, bb[k] - rc.lse2)) * rc.f;
+          r[i] = __float_as_uint(rc.coef * (col0 + i == rc.y ? e - 1.0f : e));
+        }
+      }
+      return;
+    }
+    if (plain) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.c)));
+    } else {
+#pragma unroll
+      for (int i4 = 0; i4 < 16; ++i4) {
+        const float4 b = __ldg(reinterpret_cast<const float4*>(colb2 + col0) + i4);
+        r[4 * i4 + 0] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(r[4 * i4 + 0]), kLog2e, rc.c + b.x)));
+        r[4 * i4 + 1] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(r[4 * i4 + 1]), kLog2e, rc.c + b.y)));
+        r[4 * i4 + 2] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(r[4 * i4 + 2]), kLog2e, rc.c + b.z)));
+        r[4 * i4 + 3] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(r[4 * i4 + 3]), kLog2e, rc.c + b.w)));
+      }
+    }
+    if (static_cast<unsigned>(rc.y - col0) < 64u) {
+      // the target column lies in this chunk (rare): subtract the onehot weight there
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        if (col0 + i == rc.y) r[i] = __float_as_uint(__uint_as_float(r[i]) - rc.scale);
+    }
+  } else {
+    if (general) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float4 st = tstats[i];
+        const int yt = __float_as_int(st.w);
+        const float e = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.bias2 - st.z)) * st.y;
+        const float g = (yt >= 0 ? rc.scale : 0.f) * (yt == rc.y ? e - 1.0f : e);
+        gbias += g;
+        r[i] = __float_as_uint(g);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float4 st = tstats[i];
+        float g = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.c + st.x));
+        if (__float_as_int(st.w) == rc.y) g -= rc.scale;
+        gbias += g;
+        r[i] = __float_as_uint(g);
+      }
+    }
+  }
+}
+
 template <bool kVocabRows>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
                   const PairParams p, uint32_t* __restrict__ status) {
   constexpr int kStages = PairCfg<kVocabRows>::kStages;
-  constexpr int kDsBuf = PairCfg<kVocabRows>::kDsBuf;
   extern __shared__ uint8_t smem_raw[];
   PairSmem<kVocabRows>& sm =
       *reinterpret_cast<PairSmem<kVocabRows>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -121,7 +219,6 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
   const bool leader = (q == 0);
   const uint32_t lead_rank = rank & ~1u;
   const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pr));
-  const uint16_t all_mask = static_cast<uint16_t>((1u << (2 * P)) - 1u);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int r0 = (blockIdx.x / (2 * P)) * (2 * kTileM) + static_cast<int>(q) * kTileM;
@@ -130,7 +227,7 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
   const uint32_t n2 = hc > 128 ? 256u : 128u;   // GEMM2 N; columns past H are zero-filled by TMA
   const int nbox2 = static_cast<int>(n2) / 128; // 64-column boxes per CTA per GEMM2 stage
   const int nt = (p.n_cols + kPN - 1) / kPN;
-  auto owned = [&](int j) { return (j % P) == pr; };
+  const int nkb = p.num_kb;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -140,14 +237,12 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.st_full[b], 1);
       mbar_init(&sm.st_empty[b], kEpiWarps);
-    }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_empty, 2 * kEpiWarps);
-    for (int b = 0; b < kDsBuf; ++b) {
       mbar_init(&sm.ds_full[b], 2);
       mbar_init(&sm.ds_free[b], static_cast<uint32_t>(P));
       mbar_init(&sm.rx_full[b], 1);
     }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_empty, 2 * kEpiWarps);
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
@@ -168,6 +263,7 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
   volatile int* abort = &sm.abort;
 
   if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -176,29 +272,6 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
-        }
-      };
-      auto load_gemm1 = [&](int j, int u) {
-        if (kVocabRows) {
-          // this block's per-token statistics (stats is padded to a multiple of 256 tokens)
-          const int sb = u & 1;
-          if (!mbar_wait(&sm.st_empty[sb], ((u >> 1) & 1) ^ 1, abort)) {
-            ok = false;
-            return;
-          }
-          mbar_arrive_expect_tx(&sm.st_full[sb], kPN * sizeof(float4));
-          bulk_load_1d(sm.colstats[sb], p.stats + static_cast<size_t>(j) * kPN, kPN * sizeof(float4), &sm.st_full[sb]);
-        }
-        for (int kb = 0; kb < p.num_kb && ok; ++kb) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
-            ok = false;
-            return;
-          }
-          const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), lead_rank);
-          if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * kStage);
-          tma_load_2d_pair(sm.stage[stage], &tm_rows, fb, kb * kBK, r0);
-          tma_load_2d_pair(sm.stage[stage] + kBox, &tm_cols, fb, kb * kBK, j * kPN + static_cast<int>(q) * kTileM);
-          next();
         }
       };
       auto load_gemm2 = [&](int j) {
@@ -215,12 +288,36 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           next();
         }
       };
-      int u = 0;
-      for (int j = 0; j < nt && ok; ++j) {
-        if (owned(j)) load_gemm1(j, u++);
-        if (j >= 1) load_gemm2(j - 1);
+      int u = 0;   // owned blocks whose GEMM1 has been fully loaded
+      for (int s = -2 * P; s < nt && ok; ++s) {
+        if (s >= 0) load_gemm2(s);
+        const G1Share g = g1_share(s, pr, P);
+        if (!ok || g.block < 0 || g.block >= nt) continue;
+        if (kVocabRows && g.prog == 0) {
+          // this block's per-token statistics (stats is padded to a multiple of 256 tokens)
+          const int sb = u & 1;
+          if (!mbar_wait(&sm.st_empty[sb], ((u >> 1) & 1) ^ 1, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.st_full[sb], kPN * sizeof(float4));
+          bulk_load_1d(sm.colstats[sb], p.stats + static_cast<size_t>(g.block) * kPN, kPN * sizeof(float4),
+                       &sm.st_full[sb]);
+        }
+        const int kb1 = share_begin(g.prog + 1, nkb, P);
+        for (int kb = share_begin(g.prog, nkb, P); kb < kb1; ++kb) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), lead_rank);
+          if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * kStage);
+          tma_load_2d_pair(sm.stage[stage], &tm_rows, fb, kb * kBK, r0);
+          tma_load_2d_pair(sm.stage[stage] + kBox, &tm_cols, fb, kb * kBK, g.block * kPN + static_cast<int>(q) * kTileM);
+          next();
+        }
+        if (g.prog == P - 1) ++u;
       }
-      if (ok) load_gemm2(nt - 1);
       if (!ok) {
         // let copies already issued land before the CTA can finish
         const uint64_t t0 = globaltimer_ns();
@@ -229,6 +326,7 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       }
     }
   } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------------- MMA issuer (even CTA)
     if (lane == 0 && leader) {
       constexpr uint32_t idesc1 = idesc_bf16_f32(2 * kTileM, kPN, false, false);
       const uint32_t idesc2 = idesc_bf16_f32(2 * kTileM, n2, false, true);
@@ -241,66 +339,90 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           phase ^= 1u;
         }
       };
-      auto gemm2 = [&](int i) {
-        const int db = i % kDsBuf;
-        if (!mbar_wait_cluster(&sm.ds_full[db], (i / kDsBuf) & 1, abort)) {
-          ok = false;
-          return;
-        }
-        tc_fence_after();
-        const uint32_t a_base = smem_u32(sm.ds[db]);
+      auto gemm2 = [&](int j) {
+        // the pair that writes block j+1 reuses both dS halves once every pair is done with block j
+        const uint16_t next_owner = static_cast<uint16_t>(3u << (2 * ((j + 1) % P)));
         for (int half = 0; half < 2; ++half) {
+          if (!mbar_wait_cluster(&sm.ds_full[half], static_cast<uint32_t>(j) & 1u, abort)) {
+            ok = false;
+            return;
+          }
           if (!mbar_wait(&sm.full[stage], phase, abort)) {
             ok = false;
             return;
           }
           tc_fence_after();
+          const uint32_t a_base = smem_u32(sm.ds) + static_cast<uint32_t>(half) * kHalfBytes;
           const uint32_t b_base = smem_u32(sm.stage[stage]);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = sdesc_sw128(a_base + (2 * half + (k >> 2)) * kBox + 32u * (k & 3), 16u, 1024u);
+            const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * kBox + 32u * (k & 3), 16u, 1024u);
             const uint64_t bd = sdesc_sw128(b_base + 2048u * k, kBox, 1024u);
-            mma_bf16_ss_pair(tmem + kTmemO, ad, bd, idesc2, (i | half | k) != 0 ? 1u : 0u);
+            mma_bf16_ss_pair(tmem + kTmemO, ad, bd, idesc2, (j | half | k) != 0 ? 1u : 0u);
           }
           mma_commit_mc(&sm.empty[stage], pair_mask);
           advance();
+          if (j + 1 < nt) mma_commit_mc(&sm.ds_free[half], next_owner);
         }
-        // this pair is done reading dS of block i: tell every CTA of the cluster
-        mma_commit_mc(&sm.ds_free[db], all_mask);
       };
-      int u = 0;
-      for (int j = 0; j < nt && ok; ++j) {
-        if (owned(j)) {
+      int u = 0;   // owned blocks whose GEMM1 has been issued in full
+      for (int s = -2 * P; s < nt && ok; ++s) {
+        if (s >= 0) gemm2(s);
+        const G1Share g = g1_share(s, pr, P);
+        if (!ok || g.block < 0 || g.block >= nt) continue;
+        if (g.prog == 0) {
+          // the epilogue must have read the previous logits tile out of TMEM
           if (!mbar_wait_cluster(&sm.s_empty, (u & 1) ^ 1, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!mbar_wait(&sm.full[stage], phase, abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_base = smem_u32(sm.stage[stage]);
-            const uint32_t b_base = a_base + kBox;
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              mma_bf16_ss_pair(tmem + kTmemS, sdesc_sw128(a_base + 32u * k, 16u, 1024u),
-                               sdesc_sw128(b_base + 32u * k, 16u, 1024u), idesc1, (kb | k) != 0 ? 1u : 0u);
-            mma_commit_mc(&sm.empty[stage], pair_mask);
-            advance();
+        }
+        const int kb0 = share_begin(g.prog, nkb, P);
+        const int kb1 = share_begin(g.prog + 1, nkb, P);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&sm.full[stage], phase, abort)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sm.stage[stage]);
+          const uint32_t b_base = a_base + kBox;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_ss_pair(tmem + kTmemS, sdesc_sw128(a_base + 32u * k, 16u, 1024u),
+                             sdesc_sw128(b_base + 32u * k, 16u, 1024u), idesc1, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_mc(&sm.empty[stage], pair_mask);
+          advance();
+        }
+        if (ok && g.prog == P - 1) {
           mma_commit_mc(&sm.s_full, pair_mask);
           ++u;
         }
-        if (j >= 1) gemm2(j - 1);
       }
-      if (ok) gemm2(nt - 1);
       if (ok) mma_commit_mc(&sm.o_full, pair_mask);
       mma_commit_mc(&sm.drain, pair_mask);
       mbar_wait_drain(&sm.drain, 0);
+    }
+  } else if (warp == kRecvWarp) {
+    // ---------------------------------------- dS halves of blocks computed by the other pairs
+    if (lane == 0 && P > 1) {
+      const uint32_t ds_full_c0 = mapa_shared(smem_u32(&sm.ds_full[0]), lead_rank);
+      const uint32_t ds_full_c1 = mapa_shared(smem_u32(&sm.ds_full[1]), lead_rank);
+      int v = 0;   // blocks received so far
+      bool ok = true;
+      for (int j = 0; j < nt && ok; ++j) {
+        if (j % P == pr) continue;
+        for (int half = 0; half < 2; ++half) {
+          mbar_arrive_expect_tx(&sm.rx_full[half], kHalfBytes);
+          if (!mbar_wait(&sm.rx_full[half], static_cast<uint32_t>(v) & 1u, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(half ? ds_full_c1 : ds_full_c0);
+        }
+        ++v;
+      }
     }
   } else {
     // ---------------------------------------------------------------------------- epilogue warps
@@ -310,56 +432,39 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
     const int row = r0 + rl;
     const float scale = *p.scale;
     const uint32_t s_empty_c = mapa_shared(smem_u32(&sm.s_empty), lead_rank);
-    uint32_t ds_full_c[kDsBuf];
-    for (int b = 0; b < kDsBuf; ++b) ds_full_c[b] = mapa_shared(smem_u32(&sm.ds_full[b]), lead_rank);
-    float row_lse2 = 0.f, row_zf = 0.f, row_coef = 0.f, row_bias2 = 0.f;
-    int row_y = -1;
+    const uint32_t ds_full_c = mapa_shared(smem_u32(&sm.ds_full[hh]), lead_rank);
+    // dS[m, n] = s [m valid] f_m 2^(S log2 e + b_n log2 e - LSE2_m) - s [n = y_m], with f = 1 + 2 z_loss LSE,
+    // evaluated as 2^(S log2 e + c) with c = log2(s f) - LSE2 + b log2 e gathered per row or column.
+    // When some valid row has f <= 0 (LSE <= -1/(2 z_loss)) the log form does not apply and every tile
+    // takes the general form, with f and the onehot weight as separate factors.
+    const bool general = (*p.zf_neg != 0u);
+    const float log2s = log2f(scale);
+    DsRow rc{-INFINITY, 0.f, 0.f, 0.f, 0.f, scale, -1};
     if (!kVocabRows) {
       if (row < p.BT) {
         const float4 st = p.stats[row];
-        row_lse2 = st.x;
-        row_zf = st.y;              // valid * (1 + 2 z_loss LSE)
-        row_coef = st.z * scale;    // s * valid
-        row_y = __float_as_int(st.w);
+        rc.c = st.x + log2s;
+        rc.f = st.y;
+        rc.lse2 = st.z;
+        rc.y = __float_as_int(st.w);
+        rc.coef = rc.y >= 0 ? scale : 0.f;
       }
     } else {
-      if (p.bias != nullptr && row < p.V) row_bias2 = __ldg(p.bias + row) * kLog2e;
+      if (p.bias != nullptr && row < p.V) rc.bias2 = __ldg(p.bias + row) * kLog2e;
+      rc.c = rc.bias2 + log2s;
+      rc.y = row;
     }
     float gbias = 0.f;
     bool ok = true;
-    const uint32_t ds_row_off = static_cast<uint32_t>(2 * hh) * kBox + static_cast<uint32_t>(rl) * 128u;
+    uint8_t* const ds_row = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(rl) * 128u;
     int u = 0;
-    int v[kDsBuf] = {};    // blocks received so far into each dS buffer
-    for (int j = 0; j < nt && ok; ++j) {
-      const int db = j % kDsBuf;
-      if (!owned(j)) {
-        // block computed by another pair: its dS arrives by bulk copy into this CTA's buffer
-        if (warp == 0 && lane == 0) {
-          mbar_arrive_expect_tx(&sm.rx_full[db], kDsBytes);
-          if (!mbar_wait(&sm.rx_full[db], v[db] & 1, abort)) {
-            ok = false;
-          } else {
-            mbar_arrive_cluster(ds_full_c[db]);
-          }
-        }
-        ++v[db];
-        continue;
-      }
+    for (int j = pr; j < nt && ok; j += P, ++u) {
       if (!mbar_wait(&sm.s_full, u & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t r[128];
-      {
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(qq * 32) << 16) + kTmemS + static_cast<uint32_t>(hh * 128);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_32cols(taddr + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
-        tmem_wait_ld();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(s_empty_c);
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(qq * 32) << 16) + kTmemS + static_cast<uint32_t>(hh * 128);
       const int sb = u & 1;
       if (kVocabRows && !mbar_wait(&sm.st_full[sb], (u >> 1) & 1, abort)) {
         ok = false;
@@ -367,58 +472,61 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       }
       const float4* tstats = sm.colstats[kVocabRows ? sb : 0] + (kVocabRows ? hh * 128 : 0);
       const int col0 = j * kPN + hh * 128;
-      // every pair must be done with this buffer's previous block before this CTA overwrites it
-      if (!mbar_wait_cluster(&sm.ds_free[db], ((j / kDsBuf) & 1) ^ 1, abort)) {
+      // dS of this row's 128 columns in two chunks of 64, packed to bf16 pairs
+      uint32_t pk0[32], pk1[32];
+      {
+        uint32_t r[64];
+        tmem_ld_32cols(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld_32cols(taddr + 32u, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_wait_ld();
+        ds_chunk64<kVocabRows>(r, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gbias);
+#pragma unroll
+        for (int i2 = 0; i2 < 32; ++i2) pk0[i2] = pack_bf16x2(__uint_as_float(r[2 * i2]), __uint_as_float(r[2 * i2 + 1]));
+      }
+      {
+        uint32_t r[64];
+        tmem_ld_32cols(taddr + 64u, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld_32cols(taddr + 96u, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_wait_ld();
+        // the logits tile is no longer needed: the next GEMM1 may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(s_empty_c);
+        ds_chunk64<kVocabRows>(r, col0 + 64, rc, general, p.bias == nullptr && col0 + 128 <= p.V, p.colb2,
+                               tstats + 64, gbias);
+#pragma unroll
+        for (int i2 = 0; i2 < 32; ++i2) pk1[i2] = pack_bf16x2(__uint_as_float(r[2 * i2]), __uint_as_float(r[2 * i2 + 1]));
+      }
+      // every pair must be done with block j-1 in this half slot before it is overwritten here and
+      // in the other pairs' CTAs (phase = blocks this pair wrote after block 0)
+      if (j >= 1 && !mbar_wait_cluster(&sm.ds_free[hh], static_cast<uint32_t>(u - (pr == 0 ? 1 : 0)) & 1u, abort)) {
         ok = false;
         break;
       }
-      uint8_t* const ds_row = sm.ds[db] + ds_row_off;
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        uint32_t packed[4];
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (rl & 7)) << 4)) =
+            make_uint4(pk0[4 * ch + 0], pk0[4 * ch + 1], pk0[4 * ch + 2], pk0[4 * ch + 3]);
 #pragma unroll
-        for (int i2 = 0; i2 < 4; ++i2) {
-          float d[2];
-#pragma unroll
-          for (int w2 = 0; w2 < 2; ++w2) {
-            const int i = 8 * ch + 2 * i2 + w2;
-            const int col = col0 + i;
-            const float sv = __uint_as_float(r[i]);
-            float g;
-            if (!kVocabRows) {
-              const float b2 = (p.bias != nullptr && col < p.V) ? __ldg(p.bias + col) * kLog2e : 0.f;
-              const float e = ex2_approx(fmaf(sv, kLog2e, b2 - row_lse2)) * row_zf;
-              g = row_coef * (col == row_y ? e - 1.0f : e);
-            } else {
-              const float4 st = tstats[i];
-              const float e = ex2_approx(fmaf(sv, kLog2e, row_bias2 - st.x)) * st.y;
-              g = (st.z * scale) * (__float_as_int(st.w) == row ? e - 1.0f : e);
-              gbias += g;
-            }
-            d[w2] = g;
-          }
-          packed[i2] = pack_bf16x2(d[0], d[1]);
-        }
-        uint8_t* dst = ds_row + static_cast<uint32_t>(ch >> 3) * kBox;
-        const int c = ch & 7;
-        *reinterpret_cast<uint4*>(dst + ((c ^ (rl & 7)) << 4)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      }
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(ds_row + kBox + ((ch ^ (rl & 7)) << 4)) =
+            make_uint4(pk1[4 * ch + 0], pk1[4 * ch + 1], pk1[4 * ch + 2], pk1[4 * ch + 3]);
       if (kVocabRows) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.st_empty[sb]);
       }
       fence_proxy_async_smem();
-      named_barrier_sync(1, kEpiWarps * 32);
-      if (warp == 0 && lane == 0) {
+      named_barrier_sync(1 + hh, 4 * 32);
+      if (qq == 0 && lane == 0) {
+        uint8_t* const half_base = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes;
         for (int pp = 0; pp < P; ++pp) {
           if (pp == pr) continue;
           const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
-          bulk_copy_to_peer(mapa_shared(smem_u32(sm.ds[db]), dst_rank), sm.ds[db], kDsBytes,
-                            mapa_shared(smem_u32(&sm.rx_full[db]), dst_rank));
+          bulk_copy_to_peer(mapa_shared(smem_u32(half_base), dst_rank), half_base, kHalfBytes,
+                            mapa_shared(smem_u32(&sm.rx_full[hh]), dst_rank));
         }
-        mbar_arrive_cluster(ds_full_c[db]);
+        mbar_arrive_cluster(ds_full_c);
       }
-      ++u;
     }
 
     if (ok && mbar_wait(&sm.o_full, 0, abort)) {
@@ -460,7 +568,7 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
     if (kVocabRows) {
       // this CTA's share of grad_bias (its owned blocks) -> pair 0's CTA with the same rows
       if (hh == 1) sm.half_bias[rl] = gbias;
-      named_barrier_sync(1, kEpiWarps * 32);
+      named_barrier_sync(3, kEpiWarps * 32);
       if (hh == 0) st_shared_cluster_f32(mapa_shared(smem_u32(&sm.gb_gather[pr][rl]), q), gbias + sm.half_bias[rl]);
     }
   }
@@ -483,10 +591,10 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
   if (threadIdx.x == 0 && sm.abort) atomicOr(status, kStatusTimeout);
 }
 
-// Pairs per cluster: the largest of 4, 3, 2, 1 that divides the number of 256-wide H chunks.
+// Pairs per cluster: 2 when the number of 256-wide H chunks is even, else 3 when it divides, else 1.
 int pairs_per_cluster(int h_chunks) {
-  for (int P = kMaxPairs; P > 1; --P)
-    if (h_chunks % P == 0) return P;
+  if (h_chunks % 2 == 0) return 2;
+  if (h_chunks % 3 == 0) return 3;
   return 1;
 }
 
@@ -498,7 +606,9 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   PairParams p{};
   p.bias = a.bias;
   p.stats = a.stats;
+  p.colb2 = a.colb2;
   p.scale = a.scale;
+  p.zf_neg = a.zf_neg;
   p.BT = a.BT;
   p.V = a.V;
   p.H = a.H;

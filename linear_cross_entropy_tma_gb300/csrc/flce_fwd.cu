@@ -248,14 +248,19 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
   if (threadIdx.x == 0 && sm.abort) atomicOr(status, kStatusTimeout);
 }
 
+// Per row: merge of the split partials into LSE, the row's loss term and the statistics the gradient
+// passes read; per vocabulary column: the bias in log2 units, -inf past V.
 __global__ void lse_merge_kernel(const float2* __restrict__ part, int splits, int BTp, const float* __restrict__ zy,
                                  const int64_t* __restrict__ target, int BT, int V, int64_t ignore_index,
-                                 float z_loss, float4* __restrict__ stats, float* __restrict__ row_loss,
-                                 uint32_t* __restrict__ status) {
+                                 float z_loss, const float* __restrict__ bias, float4* __restrict__ stats,
+                                 float* __restrict__ row_loss, float* __restrict__ colb2,
+                                 uint32_t* __restrict__ zf_neg, uint32_t* __restrict__ status) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  // per-column bias in log2 units for the gradient passes; -inf masks the columns past V
+  if (t < ((V + 255) & ~255)) colb2[t] = t < V ? (bias != nullptr ? bias[t] * kLog2e : 0.f) : -INFINITY;
   if (t >= BT) {
     // padding rows (up to a multiple of 256 tokens) read by the gradient passes: no contribution
-    if (t < ((BT + 255) & ~255)) stats[t] = make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+    if (t < ((BT + 255) & ~255)) stats[t] = make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
     return;
   }
   float M = -INFINITY;
@@ -271,7 +276,9 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, int splits, in
   const bool valid = (y != ignore_index) && (y >= 0) && (y < V);
   if (!valid && y != ignore_index) atomicOr(status, kStatusBadTarget);
   row_loss[t] = valid ? (lse - zy[t]) + z_loss * lse * lse : 0.f;
-  stats[t] = make_float4(lse2, valid ? 1.0f + 2.0f * z_loss * lse : 0.f, valid ? 1.f : 0.f,
+  const float f = 1.0f + 2.0f * z_loss * lse;
+  if (valid && !(f > 0.f)) atomicOr(zf_neg, 1u);
+  stats[t] = make_float4(valid && f > 0.f ? log2f(f) - lse2 : -INFINITY, valid ? f : 0.f, lse2,
                          __int_as_float(valid ? static_cast<int>(y) : -1));
 }
 
@@ -287,7 +294,7 @@ loss_reduce_kernel(const float* __restrict__ row_loss, const float4* __restrict_
   long long cnt = 0;
   for (int t = threadIdx.x; t < BT; t += kReduceThreads) {
     acc += static_cast<double>(row_loss[t]);
-    cnt += (stats[t].z != 0.f) ? 1 : 0;
+    cnt += (__float_as_int(stats[t].w) >= 0) ? 1 : 0;
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -338,23 +345,27 @@ int choose_splits(int m_tiles, int n_tiles, int num_sms) {
 
 }  // namespace
 
-size_t fused_workspace_bytes(int64_t BT) {
+size_t fused_workspace_bytes(int64_t BT, int64_t V) {
   const size_t btp = align_up(static_cast<size_t>(BT > 0 ? BT : 0), kTileM);
+  const size_t vp = align_up(static_cast<size_t>(V > 0 ? V : 0), 256);
   size_t off = 256;
   off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
   off += align_up(sizeof(float) * btp, 256);
   off += align_up(sizeof(float4) * align_up(btp, 256), 256);
   off += align_up(sizeof(float) * btp, 256);
+  off += align_up(sizeof(float) * vp, 256);
   return off;
 }
 
-FusedWorkspace carve_workspace(void* base, int64_t BT) {
+FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
+  (void)V;
   const size_t btp = align_up(static_cast<size_t>(BT > 0 ? BT : 0), kTileM);
   auto* p = static_cast<unsigned char*>(base);
   FusedWorkspace w;
   w.status = reinterpret_cast<uint32_t*>(p);
   w.scale = reinterpret_cast<float*>(p + 4);
   w.n_valid = reinterpret_cast<int64_t*>(p + 8);
+  w.zf_neg = reinterpret_cast<uint32_t*>(p + 16);
   size_t off = 256;
   w.part = reinterpret_cast<float2*>(p + off);
   off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
@@ -363,6 +374,8 @@ FusedWorkspace carve_workspace(void* base, int64_t BT) {
   w.stats = reinterpret_cast<float4*>(p + off);
   off += align_up(sizeof(float4) * align_up(btp, 256), 256);
   w.row_loss = reinterpret_cast<float*>(p + off);
+  off += align_up(sizeof(float) * btp, 256);
+  w.colb2 = reinterpret_cast<float*>(p + off);
   return w;
 }
 
@@ -388,9 +401,10 @@ cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int 
         tm_h, tm_w, a.bias, a.target, BT, V, a.ignore_index, num_kb, tps, n_tiles, BTp, ws.part, ws.zy, ws.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
-    lse_merge_kernel<<<(BT + 255) / 256, 256, 0, stream>>>(ws.part, splits, BTp, ws.zy, a.target, BT, V,
-                                                          a.ignore_index, a.z_loss, ws.stats, ws.row_loss,
-                                                          ws.status);
+    const int merge_threads = max((BT + 255) & ~255, (V + 255) & ~255);
+    lse_merge_kernel<<<merge_threads / 256, 256, 0, stream>>>(ws.part, splits, BTp, ws.zy, a.target, BT, V,
+                                                            a.ignore_index, a.z_loss, a.bias, ws.stats,
+                                                            ws.row_loss, ws.colb2, ws.zf_neg, ws.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) {
     return e;

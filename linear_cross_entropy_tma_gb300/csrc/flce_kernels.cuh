@@ -29,15 +29,18 @@ struct FusedWorkspace {
   uint32_t* status;  // header: status word
   float* scale;      // header: s = 1/max(n_valid, 1) or 1
   int64_t* n_valid;  // header: valid count
+  uint32_t* zf_neg;  // header: non-zero when a valid row has 1 + 2 z_loss LSE <= 0
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
   float* zy;         // [BTp] target logit
-  float4* stats;     // [BT rounded up to 256] (LSE * log2 e, valid ? 1 + 2 z_loss LSE : 0, valid ? 1 : 0, target as
-                     // int bits); rows past BT hold (0, 0, 0, -1)
+  float4* stats;     // [BT rounded up to 256] per row t, with LSE2 = LSE log2 e and f = 1 + 2 z_loss LSE:
+                     //   x = log2(f) - LSE2 (-inf for ignored rows and when f <= 0), y = valid ? f : 0,
+                     //   z = LSE2, w = target as int bits (-1 for ignored rows); rows past BT: (-inf, 0, 0, -1)
   float* row_loss;   // [BTp] valid * (LSE - z_y + z_loss LSE^2)
+  float* colb2;      // [V rounded up to 256] bias * log2 e (0 without bias); -inf past V
 };
 
-size_t fused_workspace_bytes(int64_t BT);
-FusedWorkspace carve_workspace(void* base, int64_t BT);
+size_t fused_workspace_bytes(int64_t BT, int64_t V);
+FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V);
 
 struct FusedArgs {
   const uint16_t* hidden;
@@ -55,11 +58,13 @@ struct FusedArgs {
   int64_t* n_valid_out;
 };
 
-// Arguments of the gradient passes on CTA pairs (flce_bwd2.cu).
+// Arguments of the gradient passes on CTA pairs (flce_bwd.cu).
 struct DgPairArgs {
   const float* bias;
   const float4* stats;
+  const float* colb2;
   const float* scale;
+  const uint32_t* zf_neg;
   int BT, V, H;
   uint16_t* grad_input;
   float* grad_W;

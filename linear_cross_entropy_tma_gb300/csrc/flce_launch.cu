@@ -11,7 +11,7 @@ cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int 
 
 cudaError_t launch_fused(const FusedArgs& a, void* workspace, int num_sms, cudaStream_t stream, char* err,
                          size_t err_len, cudaEvent_t const* events) {
-  const FusedWorkspace ws = carve_workspace(workspace, a.BT);
+  const FusedWorkspace ws = carve_workspace(workspace, a.BT, a.V);
   auto mark = [&](int i) { return events != nullptr ? cudaEventRecord(events[i], stream) : cudaSuccess; };
   cudaError_t e = cudaMemsetAsync(workspace, 0, 256, stream);
   if (e != cudaSuccess) return e;
@@ -32,7 +32,9 @@ cudaError_t launch_fused(const FusedArgs& a, void* workspace, int num_sms, cudaS
   DgPairArgs pa{};
   pa.bias = a.bias;
   pa.stats = ws.stats;
+  pa.colb2 = ws.colb2;
   pa.scale = ws.scale;
+  pa.zf_neg = ws.zf_neg;
   pa.BT = static_cast<int>(a.BT);
   pa.V = static_cast<int>(a.V);
   pa.H = static_cast<int>(a.H);

@@ -46,9 +46,10 @@ def test_workspace_sizes(lib):
     a = lib.flce_workspace_size(128, 64, 512)
     b = lib.flce_workspace_size(65535, 1024, 176245)
     assert 0 < a < b
-    # O(BT): no (BT, V) term
+    # O(BT + V): no (BT, V) term; independent of H
     assert b < 64 * 1024 * 1024
-    assert lib.flce_workspace_size(65535, 1024, 176245) == lib.flce_workspace_size(65535, 64, 8)
+    assert lib.flce_workspace_size(65535, 1024, 176245) == lib.flce_workspace_size(65535, 64, 176245)
+    assert lib.flce_workspace_size(65535, 64, 176245) - lib.flce_workspace_size(65535, 64, 8) == 4 * (176384 - 256)
     assert lib.ce_workspace_size(8192, 128256) == 256 + 16 * 8192
 
 
