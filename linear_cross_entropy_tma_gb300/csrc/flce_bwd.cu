@@ -15,9 +15,10 @@
 //     column block j is computed once, by pair (j mod P):
 //       GEMM1   S[256, 256] = rows[256, H] . cols[256, H]^T          (TMEM, 256 columns)
 //       epi     dS = f(S, statistics) in registers -> bf16 in shared memory, in the 128-byte-swizzled
-//               K-major layout of the next MMA's A operand; each 128-column half is then copied with
-//               cp.async.bulk into the same buffer of the other P-1 pairs' CTAs (distributed shared
-//               memory, never HBM)
+//               K-major layout of the next MMA's A operand; each epilogue warp copies its 32 rows
+//               with cp.async.bulk into the same buffer of the other P-1 pairs' CTAs (distributed
+//               shared memory, never HBM).  (Stores by the threads themselves, st.shared::cluster,
+//               measured about four times slower.)
 //     and every pair accumulates its own H chunk:
 //       GEMM2   O[256, 256] += dS[256, 256] . cols[256, chunk]      (TMEM, 256 columns, fp32)
 //     So the logits of each (row block, column block) are computed ceil(H / (256 P)) times instead of
@@ -415,7 +416,7 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
         if (j % P == pr) continue;
         for (int half = 0; half < 2; ++half) {
           mbar_arrive_expect_tx(&sm.rx_full[half], kHalfBytes);
-          if (!mbar_wait(&sm.rx_full[half], static_cast<uint32_t>(v) & 1u, abort)) {
+          if (!mbar_wait_cluster(&sm.rx_full[half], static_cast<uint32_t>(v) & 1u, abort)) {
             ok = false;
             break;
           }
@@ -475,27 +476,23 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       // dS of this row's 128 columns in two chunks of 64, packed to bf16 pairs
       uint32_t pk0[32], pk1[32];
       {
-        uint32_t r[64];
-        tmem_ld_32cols(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld_32cols(taddr + 32u, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-        tmem_wait_ld();
-        ds_chunk64<kVocabRows>(r, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gbias);
-#pragma unroll
-        for (int i2 = 0; i2 < 32; ++i2) pk0[i2] = pack_bf16x2(__uint_as_float(r[2 * i2]), __uint_as_float(r[2 * i2 + 1]));
-      }
-      {
-        uint32_t r[64];
-        tmem_ld_32cols(taddr + 64u, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld_32cols(taddr + 96u, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        uint32_t ra[64], rb[64];
+        tmem_ld_32cols(taddr, *reinterpret_cast<uint32_t(*)[32]>(&ra[0]));
+        tmem_ld_32cols(taddr + 32u, *reinterpret_cast<uint32_t(*)[32]>(&ra[32]));
+        tmem_ld_32cols(taddr + 64u, *reinterpret_cast<uint32_t(*)[32]>(&rb[0]));
+        tmem_ld_32cols(taddr + 96u, *reinterpret_cast<uint32_t(*)[32]>(&rb[32]));
         tmem_wait_ld();
         // the logits tile is no longer needed: the next GEMM1 may overwrite it
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(s_empty_c);
-        ds_chunk64<kVocabRows>(r, col0 + 64, rc, general, p.bias == nullptr && col0 + 128 <= p.V, p.colb2,
+        ds_chunk64<kVocabRows>(ra, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gbias);
+#pragma unroll
+        for (int i2 = 0; i2 < 32; ++i2) pk0[i2] = pack_bf16x2(__uint_as_float(ra[2 * i2]), __uint_as_float(ra[2 * i2 + 1]));
+        ds_chunk64<kVocabRows>(rb, col0 + 64, rc, general, p.bias == nullptr && col0 + 128 <= p.V, p.colb2,
                                tstats + 64, gbias);
 #pragma unroll
-        for (int i2 = 0; i2 < 32; ++i2) pk1[i2] = pack_bf16x2(__uint_as_float(r[2 * i2]), __uint_as_float(r[2 * i2 + 1]));
+        for (int i2 = 0; i2 < 32; ++i2) pk1[i2] = pack_bf16x2(__uint_as_float(rb[2 * i2]), __uint_as_float(rb[2 * i2 + 1]));
       }
       // every pair must be done with block j-1 in this half slot before it is overwritten here and
       // in the other pairs' CTAs (phase = blocks this pair wrote after block 0)
@@ -516,17 +513,20 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
         if (lane == 0) mbar_arrive(&sm.st_empty[sb]);
       }
       fence_proxy_async_smem();
-      named_barrier_sync(1 + hh, 4 * 32);
-      if (qq == 0 && lane == 0) {
-        uint8_t* const half_base = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes;
+      __syncwarp();
+      if (lane == 0) {
+        // this warp's 32 rows of both 64-column boxes to the other pairs' CTAs with the same rows
+        uint8_t* const src = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
         for (int pp = 0; pp < P; ++pp) {
           if (pp == pr) continue;
           const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
-          bulk_copy_to_peer(mapa_shared(smem_u32(half_base), dst_rank), half_base, kHalfBytes,
-                            mapa_shared(smem_u32(&sm.rx_full[hh]), dst_rank));
+          const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[hh]), dst_rank);
+          bulk_copy_to_peer(mapa_shared(smem_u32(src), dst_rank), src, 4096u, bar);
+          bulk_copy_to_peer(mapa_shared(smem_u32(src + kBox), dst_rank), src + kBox, 4096u, bar);
         }
-        mbar_arrive_cluster(ds_full_c);
       }
+      named_barrier_sync(1 + hh, 4 * 32);
+      if (qq == 0 && lane == 0) mbar_arrive_cluster(ds_full_c);
     }
 
     if (ok && mbar_wait(&sm.o_full, 0, abort)) {

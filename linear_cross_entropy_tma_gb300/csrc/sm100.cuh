@@ -312,6 +312,18 @@ __device__ __forceinline__ void st_shared_cluster_f32(uint32_t cluster_addr, flo
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Makes this thread's generic-proxy writes to shared memory anywhere in the cluster visible to later
+// async-proxy reads (tensor-core operands), once the reader has synchronised with this thread.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor of tcgen05.mma for a 128-byte-swizzled operand tile.
 //   bits  0-13  start address >> 4
