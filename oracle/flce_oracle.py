@@ -29,6 +29,10 @@ Readings where the pages are silent (each also listed in the design notes):
   * with z-loss in the fused loss, l_t = LSE_t - z_y + z_loss * LSE_t^2, so the gradient row is
     p * (1 + 2 z_loss LSE_t) - onehot(y_t);
   * n_valid = 0 gives loss 0 and all-zero gradients (the clamp of p3 "Usage");
+  * reduction "none" returns the per-token losses; its gradients are those of sum_t g_t l_t for an
+    upstream gradient g (PyTorch's convention for an unreduced loss), and every gradient is
+    multiplied by the scalar upstream gradient of the reduced loss (the d_out / grad_scale factor of
+    p2 "Breakdown: Backward Pass", step 4);
   * a target outside [0, V) that is not ignore_index is treated as ignored;
   * z_sum of the standalone CE is the unscaled sum of LSE^2 over valid rows.
 
@@ -78,17 +82,24 @@ def _valid_mask(target: np.ndarray, V: int, ignore_index: int) -> np.ndarray:
 def _scale(n_valid: int, reduction: str) -> float:
     if reduction == "mean":
         return 1.0 / max(n_valid, 1)
-    if reduction == "sum":
+    if reduction in ("sum", "none"):
         return 1.0
-    raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
+    raise ValueError(f"reduction must be 'mean', 'sum' or 'none', got {reduction!r}")
 
 
 def flce_reference(hidden, W, target, bias=None, ignore_index: int = -100, reduction: str = "mean",
-                   z_loss: float = 0.0, want_grads: bool = True, row_block: int = 512) -> dict:
+                   z_loss: float = 0.0, want_grads: bool = True, row_block: int = 512, grad_scale: float = 1.0,
+                   grad_loss_per_token=None) -> dict:
     """Loss and gradients of fused linear cross-entropy, straight from the definitions.
 
-    Returns a dict with ``loss`` (float), ``n_valid`` (int), ``lse`` [BT], and when ``want_grads``
-    ``grad_input`` [BT, H], ``grad_W`` [V, H], ``grad_bias`` [V] (None without a bias), all float64.
+    Returns a dict with ``loss`` (float), ``n_valid`` (int), ``lse`` [BT], ``loss_per_token`` [BT]
+    (l_t on valid rows, 0 elsewhere), and when ``want_grads`` ``grad_input`` [BT, H], ``grad_W`` [V, H],
+    ``grad_bias`` [V] (None without a bias), all float64.
+
+    reduction "mean" / "sum": ``loss`` is the reduced loss.  reduction "none": ``loss`` is the plain
+    sum of ``loss_per_token`` and the gradients are those of sum_t g_t l_t, with g_t the upstream
+    gradient of token t's loss (``grad_loss_per_token``; all ones when None).  Every gradient is
+    multiplied by ``grad_scale`` (the upstream gradient of the reduced loss).
     """
     h = widen(hidden)
     w = widen(W)
@@ -102,6 +113,7 @@ def flce_reference(hidden, W, target, bias=None, ignore_index: int = -100, reduc
 
     loss_terms = []
     lse_all = np.empty(BT)
+    u = np.ones(BT) if grad_loss_per_token is None else np.asarray(grad_loss_per_token, dtype=np.float64)
     if want_grads:
         grad_input = np.zeros((BT, H))
         grad_W = np.zeros((V, H))
@@ -126,12 +138,14 @@ def flce_reference(hidden, W, target, bias=None, ignore_index: int = -100, reduc
             d = p * (1.0 + 2.0 * z_loss * L)[:, None]
             d[rows, y] -= 1.0
             d *= (s * v)[:, None]
+            d *= (grad_scale * u[r0:r1])[:, None]
             grad_input[r0:r1] = d @ w
             grad_W += d.T @ h[r0:r1]
             if grad_b is not None:
                 grad_b += d.sum(axis=0)
-    loss = s * math.fsum(np.concatenate(loss_terms).tolist()) if loss_terms else 0.0
-    out = dict(loss=loss, n_valid=n_valid, lse=lse_all)
+    per_token = np.concatenate(loss_terms) if loss_terms else np.zeros(0)
+    loss = s * math.fsum(per_token.tolist()) if loss_terms else 0.0
+    out = dict(loss=loss, n_valid=n_valid, lse=lse_all, loss_per_token=per_token)
     if want_grads:
         out.update(grad_input=grad_input, grad_W=grad_W, grad_bias=grad_b)
     return out

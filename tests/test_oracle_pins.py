@@ -5,7 +5,8 @@
     (the boxed identity dl/dz = softmax - onehot of "Fused Linear Cross-Entropy", "The identity ...");
   * an independent library: torch.nn.functional.cross_entropy in float64 on the CPU, with autograd;
   * closed forms: W = 0, V = 1, and the hand-evaluated values in tests/golden/ce_closed_forms.txt;
-  * invariants: LSE shift, dlogits row sums, ignored rows, n_valid = 0, vocabulary permutation.
+  * invariants: LSE shift, dlogits row sums, ignored rows, n_valid = 0, vocabulary permutation;
+  * the unreduced loss with an upstream gradient against finite differences and torch autograd.
 
 The same checks run against deliberately broken copies of the oracle (test_planted_mistakes) to show
 that a dropped term, a wrong sign, a wrong index or a wrong scale fails at least one of them.
@@ -230,8 +231,57 @@ def pin_sampled_matches_full(orc):
     assert _rel(smp["grad_bias_rows"], full["grad_bias"][vrows]) < 1e-12
 
 
+def pin_unreduced_and_upstream(orc):
+    # reduction "none" with an upstream gradient g (negative and zero entries included) and a scalar
+    # grad_scale: the gradients are those of grad_scale * sum_t g_t l_t
+    hidden, W, b, t = _tiny_case(seed=19)
+    g = np.array([0.7, -1.3, 2.0, 0.0, 0.25, -0.5])
+    zl, gs = 1e-2, -0.75
+    got = orc.flce_reference(hidden, W, t, bias=b, reduction="none", z_loss=zl, grad_scale=gs,
+                             grad_loss_per_token=g, row_block=4)
+    h_step = 1e-6
+
+    def fun(hh, ww, bb):
+        r = orc.flce_reference(hh, ww, t, bias=bb, reduction="none", z_loss=zl, want_grads=False, row_block=4)
+        return gs * float(np.dot(g, r["loss_per_token"]))
+
+    for name, arr, grad in (("hidden", hidden, got["grad_input"]), ("W", W, got["grad_W"]),
+                            ("bias", b, got["grad_bias"])):
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            plus = arr.copy()
+            minus = arr.copy()
+            plus[idx] += h_step
+            minus[idx] -= h_step
+            args_p = {"hidden": (plus, W, b), "W": (hidden, plus, b), "bias": (hidden, W, plus)}[name]
+            args_m = {"hidden": (minus, W, b), "W": (hidden, minus, b), "bias": (hidden, W, minus)}[name]
+            fd[idx] = (fun(*args_p) - fun(*args_m)) / (2 * h_step)
+        assert _rel(grad, fd) < 1e-6, name
+    # an independent library: per-token cross entropy + z-loss in torch, backward with g * grad_scale
+    th = torch.tensor(hidden, requires_grad=True)
+    tw = torch.tensor(W, requires_grad=True)
+    tb = torch.tensor(b, requires_grad=True)
+    tt = torch.tensor(t)
+    z = th @ tw.T + tb
+    valid = (tt != -100).double()
+    per = torch.nn.functional.cross_entropy(z, tt, ignore_index=-100, reduction="none") + \
+        zl * torch.logsumexp(z, dim=1) ** 2 * valid
+    per.backward(torch.tensor(g * gs))
+    assert _rel(got["loss_per_token"], per.detach().numpy()) < 1e-13
+    assert _rel(got["grad_input"], th.grad.numpy()) < 1e-10
+    assert _rel(got["grad_W"], tw.grad.numpy()) < 1e-10
+    assert _rel(got["grad_bias"], tb.grad.numpy()) < 1e-10
+    # consistency of the reductions: sum of per-token losses, and mean = none with g = 1/n_valid
+    m = orc.flce_reference(hidden, W, t, bias=b, reduction="mean", z_loss=zl, row_block=4)
+    n = orc.flce_reference(hidden, W, t, bias=b, reduction="none", z_loss=zl, row_block=4,
+                           grad_loss_per_token=np.full(len(t), 1.0 / m["n_valid"]))
+    assert abs(n["loss"] - m["loss"] * m["n_valid"]) < 1e-12 * abs(n["loss"])
+    for k in ("grad_input", "grad_W", "grad_bias"):
+        assert _rel(n[k], m[k]) < 1e-12, k
+
+
 PINS = [pin_loops_vs_vectorised, pin_finite_differences, pin_torch_fp64, pin_closed_forms,
-        pin_invariants, pin_ce, pin_sampled_matches_full]
+        pin_invariants, pin_ce, pin_sampled_matches_full, pin_unreduced_and_upstream]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -252,6 +302,8 @@ MUTATIONS = {
     "bias sign flipped": ("        z = h[r0:r1] @ w.T\n        if b is not None:\n            z += b[None, :]\n        m = z.max", "        z = h[r0:r1] @ w.T\n        if b is not None:\n            z -= b[None, :]\n        m = z.max"),
     "ignored CE rows not zeroed": ("dl[r0:r1] = d * v[:, None]", "dl[r0:r1] = d"),
     "CE target column not adjusted": ("        d[rows, y[r0:r1]] -= 1.0\n        dl[r0:r1]", "        dl[r0:r1]"),
+    "upstream gradient ignored": ("d *= (grad_scale * u[r0:r1])[:, None]", "d *= grad_scale"),
+    "grad_scale applied twice": ("d *= (grad_scale * u[r0:r1])[:, None]", "d *= (grad_scale * grad_scale * u[r0:r1])[:, None]"),
     "grad_input uses transposed product": ("grad_input[r0:r1] = d @ w", "grad_input[r0:r1] = (w.T @ d.T).T * 0 + d @ w[::-1]"),
 }
 
