@@ -61,6 +61,7 @@ typedef enum flce_status {
 /* reduction argument of flce_fwd_bwd */
 #define FLCE_REDUCTION_MEAN 0
 #define FLCE_REDUCTION_SUM 1
+#define FLCE_REDUCTION_NONE 2  /* per-token losses; flce_fwd_bwd_ex only */
 
 /* bits of the device status word (first 4 bytes of either workspace) */
 #define FLCE_STATUS_BAD_TARGET 0x1u
@@ -121,6 +122,42 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
                                uint16_t* grad_input, float* grad_W, float* grad_bias,
                                int64_t* n_valid, void* workspace, size_t workspace_bytes,
                                void* stream, void* const* events, int n_events);
+
+/*
+ * Options of flce_fwd_bwd_ex (all zero / NULL except grad_scale = 1 reproduces flce_fwd_bwd).
+ *
+ * The loss gradient is scaled by the upstream gradient as in "Cut Cross Entropy visualized",
+ * "Breakdown: Backward Pass", step 4 (the d_out * grad_scale factor); for an unreduced loss the upstream
+ * gradient has one entry per token (PyTorch's convention for reduction='none').
+ *
+ *   grad_scale           multiplies every gradient (the upstream gradient of the reduced loss).
+ *                        Any finite value; 0 gives zero gradients.  Does not change the loss.
+ *   grad_loss_per_token  [BT] fp32, device, or NULL (all ones): with FLCE_REDUCTION_NONE, the upstream
+ *                        gradient g_t of token t's loss; the gradients are those of
+ *                        grad_scale * sum_t g_t l_t.  Must be NULL for MEAN and SUM.
+ *   loss_per_token       [BT] fp32, device, or NULL: receives l_t = LSE_t - z_y + z_loss LSE_t^2 on
+ *                        valid rows and 0 on ignored rows (any reduction).
+ *   accumulate           non-zero: grad_input, grad_W and grad_bias receive += instead of = (their
+ *                        previous contents are added to; grad_input is re-rounded to bf16).
+ */
+typedef struct flce_fwd_bwd_options {
+  float grad_scale;
+  const float* grad_loss_per_token;
+  float* loss_per_token;
+  int accumulate;
+} flce_fwd_bwd_options;
+
+/*
+ * flce_fwd_bwd with options (NULL options = the defaults above).  reduction may also be
+ * FLCE_REDUCTION_NONE; then `loss` may be NULL and, when given, receives the plain sum of the
+ * per-token losses.  Pointer alignment: loss_per_token and grad_loss_per_token 4 bytes.
+ */
+flce_status flce_fwd_bwd_ex(const uint16_t* hidden, const uint16_t* W, const float* bias,
+                            const int64_t* target, int64_t BT, int64_t H, int64_t V,
+                            int64_t ignore_index, int reduction, float z_loss, float* loss,
+                            uint16_t* grad_input, float* grad_W, float* grad_bias, int64_t* n_valid,
+                            void* workspace, size_t workspace_bytes,
+                            const flce_fwd_bwd_options* options, void* stream);
 
 /* Bytes of workspace ce_with_grad needs for B rows (per-row partial sums and the status word). */
 size_t ce_workspace_size(int64_t B, int64_t V);

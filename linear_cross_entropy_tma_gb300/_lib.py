@@ -16,14 +16,22 @@ LIB_PATH = os.path.join(PKG, "libflce.so")
 FLCE_OK = 0
 STATUS_BAD_TARGET = 0x1
 STATUS_TIMEOUT = 0x2
-EXPORTED = ("flce_workspace_size", "flce_fwd_bwd", "flce_fwd_bwd_timed", "ce_workspace_size", "ce_with_grad",
-            "flce_read_device_status", "flce_status_string", "flce_last_error", "ce_with_grad_noalloc")
+EXPORTED = ("flce_workspace_size", "flce_fwd_bwd", "flce_fwd_bwd_timed", "flce_fwd_bwd_ex", "ce_workspace_size",
+            "ce_with_grad", "flce_read_device_status", "flce_status_string", "flce_last_error",
+            "ce_with_grad_noalloc")
+REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 _lib = None
 
 c_p = ctypes.c_void_p
 c_i64 = ctypes.c_int64
 c_sz = ctypes.c_size_t
+
+
+class FwdBwdOptions(ctypes.Structure):
+    """flce_fwd_bwd_options of include/flce.h."""
+    _fields_ = [("grad_scale", ctypes.c_float), ("grad_loss_per_token", c_p), ("loss_per_token", c_p),
+                ("accumulate", ctypes.c_int)]
 
 
 def load() -> ctypes.CDLL:
@@ -42,6 +50,8 @@ def load() -> ctypes.CDLL:
                                  c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]
     lib.flce_fwd_bwd_timed.restype = ctypes.c_int
     lib.flce_fwd_bwd_timed.argtypes = lib.flce_fwd_bwd.argtypes + [ctypes.POINTER(c_p), ctypes.c_int]
+    lib.flce_fwd_bwd_ex.restype = ctypes.c_int
+    lib.flce_fwd_bwd_ex.argtypes = lib.flce_fwd_bwd.argtypes[:-1] + [ctypes.POINTER(FwdBwdOptions), c_p]
     lib.ce_workspace_size.restype = c_sz
     lib.ce_workspace_size.argtypes = [c_i64, c_i64]
     lib.ce_with_grad.restype = ctypes.c_int
@@ -90,15 +100,22 @@ def _bf16_ptr_ok(t, name):
 
 def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reduction: str = "mean",
                  z_loss: float = 0.0, need_grad_input: bool = True, need_grad_W: bool = True, workspace=None,
-                 out=None, stream=None, pass_events=None) -> dict:
+                 out=None, stream=None, pass_events=None, grad_scale: float = 1.0, grad_loss_per_token=None,
+                 accumulate: bool = False, want_loss_per_token: bool = False) -> dict:
     """Fused linear cross-entropy forward + backward on the current CUDA device.
 
     hidden [BT, H] bf16, W [V, H] bf16, target [BT] int64, bias [V] fp32 or None.  Returns a dict with
-    ``loss`` (fp32 [1]), ``n_valid`` (int64 [1]), ``grad_input`` (bf16 [BT, H] or None), ``grad_W``
-    (fp32 [V, H] or None), ``grad_bias`` (fp32 [V] or None).  ``out`` may supply preallocated outputs
-    with the same keys; ``workspace`` a uint8 CUDA tensor of at least ``workspace_size`` bytes.
-    ``pass_events``: five recorded ``torch.cuda.Event(enable_timing=True)`` objects; the library
-    re-records them at the pass boundaries (flce_fwd_bwd_timed) for per-kernel timing.
+    ``loss`` (fp32 [1]; for reduction "none" the plain sum of the per-token losses), ``n_valid``
+    (int64 [1]), ``grad_input`` (bf16 [BT, H] or None), ``grad_W`` (fp32 [V, H] or None),
+    ``grad_bias`` (fp32 [V] or None) and ``loss_per_token`` (fp32 [BT], for reduction "none" or when
+    ``want_loss_per_token``; else None).  ``out`` may supply preallocated outputs with the same keys;
+    ``workspace`` a uint8 CUDA tensor of at least ``workspace_size`` bytes.
+
+    ``grad_scale`` multiplies every gradient; ``grad_loss_per_token`` (fp32 [BT], reduction "none"
+    only) is the upstream gradient of each token's loss; ``accumulate`` adds the gradients to the
+    tensors given in ``out`` instead of overwriting them (flce_fwd_bwd_ex).  ``pass_events``: five
+    recorded ``torch.cuda.Event(enable_timing=True)`` objects; the library re-records them at the pass
+    boundaries (flce_fwd_bwd_timed) for per-kernel timing; only with the default options.
     """
     import torch
     _bf16_ptr_ok(hidden, "hidden")
@@ -109,13 +126,22 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
         raise ValueError("shapes must be hidden [BT, H], W [V, H], target [BT] int64 on the GPU")
     if bias is not None and (bias.dtype != torch.float32 or bias.shape != (V,) or not bias.is_cuda):
         raise ValueError("bias must be a CUDA float32 tensor of shape [V]")
-    red = {"mean": 0, "sum": 1}[reduction]
+    if grad_loss_per_token is not None and (grad_loss_per_token.dtype != torch.float32 or
+                                            grad_loss_per_token.shape != (BT,) or not grad_loss_per_token.is_cuda
+                                            or not grad_loss_per_token.is_contiguous()):
+        raise ValueError("grad_loss_per_token must be a contiguous CUDA float32 tensor of shape [BT]")
+    red = REDUCTIONS[reduction]
     dev = hidden.device
     o = dict(out or {})
     if "loss" not in o:
         o["loss"] = torch.empty(1, dtype=torch.float32, device=dev)
     if "n_valid" not in o:
         o["n_valid"] = torch.empty(1, dtype=torch.int64, device=dev)
+    if (reduction == "none" or want_loss_per_token) and o.get("loss_per_token") is None:
+        o["loss_per_token"] = torch.empty(BT, dtype=torch.float32, device=dev)
+    if accumulate and ((need_grad_input and o.get("grad_input") is None) or (need_grad_W and o.get("grad_W") is None)
+                       or (need_grad_W and bias is not None and o.get("grad_bias") is None)):
+        raise ValueError("accumulate needs the gradient tensors to add to in `out`")
     if need_grad_input and o.get("grad_input") is None:
         o["grad_input"] = torch.empty((BT, H), dtype=torch.bfloat16, device=dev)
     if need_grad_W and o.get("grad_W") is None:
@@ -125,20 +151,27 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     gi = o.get("grad_input") if need_grad_input else None
     gw = o.get("grad_W") if need_grad_W else None
     gb = o.get("grad_bias") if (need_grad_W and bias is not None) else None
+    lt = o.get("loss_per_token")
     need = workspace_size(BT, H, V)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     args = (_ptr(hidden), _ptr(W), _ptr(bias), _ptr(target), BT, H, V, ignore_index, red, float(z_loss),
-            _ptr(o["loss"]), _ptr(gi), _ptr(gw), _ptr(gb), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel(),
-            _stream_ptr(stream))
-    if pass_events is None:
-        check(load().flce_fwd_bwd(*args))
-    else:
+            _ptr(o["loss"]), _ptr(gi), _ptr(gw), _ptr(gb), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel())
+    plain = red != 2 and grad_scale == 1.0 and grad_loss_per_token is None and not accumulate and lt is None
+    if pass_events is not None:
+        if not plain:
+            raise ValueError("pass_events only with the default options")
         if len(pass_events) != 5:
             raise ValueError("pass_events needs exactly 5 events")
         handles = (c_p * 5)(*[ev.cuda_event for ev in pass_events])
-        check(load().flce_fwd_bwd_timed(*args, handles, 5))
-    return dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, workspace=workspace)
+        check(load().flce_fwd_bwd_timed(*args, _stream_ptr(stream), handles, 5))
+    elif plain:
+        check(load().flce_fwd_bwd(*args, _stream_ptr(stream)))
+    else:
+        opts = FwdBwdOptions(float(grad_scale), _ptr(grad_loss_per_token), _ptr(lt), 1 if accumulate else 0)
+        check(load().flce_fwd_bwd_ex(*args, ctypes.byref(opts), _stream_ptr(stream)))
+    return dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, loss_per_token=lt,
+                workspace=workspace)
 
 
 def ce_with_grad(logits, labels, ignore_index: int = -100, z_loss: float = 0.0, workspace=None, out=None,

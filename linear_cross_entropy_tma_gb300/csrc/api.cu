@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libflce.so: argument validation, device checks, tensor-map encoding and
 // dispatch to the kernels.  No memory is allocated here; every buffer comes from the caller.
 #include <cstdarg>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 
@@ -101,9 +102,10 @@ size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V) {
 static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const float* bias, const int64_t* target,
                                 int64_t BT, int64_t H, int64_t V, int64_t ignore_index, int reduction, float z_loss,
                                 float* loss, uint16_t* grad_input, float* grad_W, float* grad_bias, int64_t* n_valid,
-                                void* workspace, size_t workspace_bytes, void* stream, void* const* events,
-                                int n_events) {
+                                void* workspace, size_t workspace_bytes, const flce_fwd_bwd_options* options,
+                                void* stream, void* const* events, int n_events) {
   g_last_error[0] = '\0';
+  const flce_fwd_bwd_options opt = options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0};
   if (n_events != 0 && (n_events != 5 || events == nullptr)) {
     set_error("n_events must be 0 or 5 (with a non-NULL event array)");
     return FLCE_ERR_INVALID_ARG;
@@ -113,12 +115,21 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
               (long long)V);
     return FLCE_ERR_INVALID_ARG;
   }
-  if (W == nullptr || loss == nullptr || workspace == nullptr || (BT > 0 && (hidden == nullptr || target == nullptr))) {
-    set_error("hidden, W, target, loss and workspace must not be NULL");
+  if (reduction != FLCE_REDUCTION_MEAN && reduction != FLCE_REDUCTION_SUM && reduction != FLCE_REDUCTION_NONE) {
+    set_error("reduction must be 0 (mean), 1 (sum) or 2 (none), got %d", reduction);
     return FLCE_ERR_INVALID_ARG;
   }
-  if (reduction != FLCE_REDUCTION_MEAN && reduction != FLCE_REDUCTION_SUM) {
-    set_error("reduction must be 0 (mean) or 1 (sum), got %d", reduction);
+  if (W == nullptr || workspace == nullptr || (BT > 0 && (hidden == nullptr || target == nullptr)) ||
+      (loss == nullptr && reduction != FLCE_REDUCTION_NONE)) {
+    set_error("hidden, W, target, loss and workspace must not be NULL (loss may be NULL only for reduction none)");
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (opt.grad_loss_per_token != nullptr && reduction != FLCE_REDUCTION_NONE) {
+    set_error("grad_loss_per_token is only defined for reduction none");
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(opt.grad_scale)) {
+    set_error("grad_scale must be finite");
     return FLCE_ERR_INVALID_ARG;
   }
   if (bias == nullptr && grad_bias != nullptr) {
@@ -137,7 +148,8 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   }
   if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(grad_input, 16) || !aligned(grad_W, 16) ||
       !aligned(workspace, 256) || !aligned(bias, 4) || !aligned(grad_bias, 4) || !aligned(loss, 4) ||
-      !aligned(target, 8) || !aligned(n_valid, 8)) {
+      !aligned(target, 8) || !aligned(n_valid, 8) || !aligned(opt.loss_per_token, 4) ||
+      !aligned(opt.grad_loss_per_token, 4)) {
     set_error("misaligned pointer (hidden, W, grad_input, grad_W need 16 bytes; workspace 256)");
     return FLCE_ERR_MISALIGNED;
   }
@@ -166,6 +178,10 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   a.grad_W = grad_W;
   a.grad_bias = grad_bias;
   a.n_valid_out = n_valid;
+  a.grad_scale = opt.grad_scale;
+  a.grad_tok = opt.grad_loss_per_token;
+  a.loss_tok = opt.loss_per_token;
+  a.accumulate = opt.accumulate != 0;
   char err[256] = "";
   const cudaError_t e = flce::launch_fused(a, workspace, num_sms, static_cast<cudaStream_t>(stream), err, sizeof(err),
                                            n_events ? reinterpret_cast<cudaEvent_t const*>(events) : nullptr);
@@ -177,8 +193,18 @@ flce_status flce_fwd_bwd(const uint16_t* hidden, const uint16_t* W, const float*
                          int64_t BT, int64_t H, int64_t V, int64_t ignore_index, int reduction, float z_loss,
                          float* loss, uint16_t* grad_input, float* grad_W, float* grad_bias, int64_t* n_valid,
                          void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_bwd_impl(hidden, W, bias, target, BT, H, V, ignore_index, reduction == FLCE_REDUCTION_NONE ? -1 : reduction,
+                      z_loss, loss, grad_input, grad_W, grad_bias, n_valid, workspace, workspace_bytes, nullptr,
+                      stream, nullptr, 0);
+}
+
+flce_status flce_fwd_bwd_ex(const uint16_t* hidden, const uint16_t* W, const float* bias, const int64_t* target,
+                            int64_t BT, int64_t H, int64_t V, int64_t ignore_index, int reduction, float z_loss,
+                            float* loss, uint16_t* grad_input, float* grad_W, float* grad_bias, int64_t* n_valid,
+                            void* workspace, size_t workspace_bytes, const flce_fwd_bwd_options* options,
+                            void* stream) {
   return fwd_bwd_impl(hidden, W, bias, target, BT, H, V, ignore_index, reduction, z_loss, loss, grad_input, grad_W,
-                      grad_bias, n_valid, workspace, workspace_bytes, stream, nullptr, 0);
+                      grad_bias, n_valid, workspace, workspace_bytes, options, stream, nullptr, 0);
 }
 
 flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const float* bias, const int64_t* target,
@@ -186,8 +212,9 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
                                float* loss, uint16_t* grad_input, float* grad_W, float* grad_bias, int64_t* n_valid,
                                void* workspace, size_t workspace_bytes, void* stream, void* const* events,
                                int n_events) {
-  return fwd_bwd_impl(hidden, W, bias, target, BT, H, V, ignore_index, reduction, z_loss, loss, grad_input, grad_W,
-                      grad_bias, n_valid, workspace, workspace_bytes, stream, events, n_events);
+  return fwd_bwd_impl(hidden, W, bias, target, BT, H, V, ignore_index, reduction == FLCE_REDUCTION_NONE ? -1 : reduction,
+                      z_loss, loss, grad_input, grad_W, grad_bias, n_valid, workspace, workspace_bytes, nullptr,
+                      stream, events, n_events);
 }
 
 size_t ce_workspace_size(int64_t B, int64_t V) {

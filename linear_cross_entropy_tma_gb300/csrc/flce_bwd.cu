@@ -104,6 +104,8 @@ struct PairParams {
   const float* colb2;
   const float* scale;
   const uint32_t* zf_neg;
+  float z_loss;
+  int accumulate;
   int BT, V, H;
   int n_rows, n_cols, num_kb;
   int P;                    // pairs per cluster
@@ -129,14 +131,16 @@ __device__ __forceinline__ G1Share g1_share(int s, int pr, int P) {
 }
 __device__ __forceinline__ int share_begin(int prog, int num_kb, int P) { return (prog * num_kb) / P; }
 
-// Row constants of the dS arithmetic of one epilogue thread.
+// Row constants of the dS arithmetic of one epilogue thread (G: the gradient scale, u: a token's
+// upstream gradient, f = 1 + 2 z_loss LSE).
 struct DsRow {
-  float c;      // grad_input pass: log2(s f) - LSE2 (-inf for ignored rows); grad_W pass: b log2 e + log2 s
-  float f;      // grad_input pass, general form: valid * f
+  float c;      // grad_input pass: log2(G u f) - LSE2 (-inf for ignored rows); grad_W pass: b log2 e + log2 G
+  float f;      // grad_input pass, general form: f
   float lse2;   // grad_input pass, general form: LSE log2 e
-  float coef;   // grad_input pass, general form: s * valid
+  float coef;   // grad_input pass: G u [valid], the weight of the onehot term
   float bias2;  // grad_W pass, general form: b log2 e
-  float scale;  // s
+  float scale;  // G
+  float zl2;    // 2 z_loss ln 2 (f = 1 + zl2 LSE2)
   int y;        // grad_input pass: target column (-1 if none); grad_W pass: this row's vocabulary index
 };
 
@@ -179,7 +183,7 @@ __device__ __forceinline__ void ds_chunk64(uint32_t (&r)[64], int col0, const Ds
       // the target column lies in this chunk (rare): subtract the onehot weight there
 #pragma unroll
       for (int i = 0; i < 64; ++i)
-        if (col0 + i == rc.y) r[i] = __float_as_uint(__uint_as_float(r[i]) - rc.scale);
+        if (col0 + i == rc.y) r[i] = __float_as_uint(__uint_as_float(r[i]) - rc.coef);
     }
   } else {
     if (general) {
@@ -187,8 +191,8 @@ __device__ __forceinline__ void ds_chunk64(uint32_t (&r)[64], int col0, const Ds
       for (int i = 0; i < 64; ++i) {
         const float4 st = tstats[i];
         const int yt = __float_as_int(st.w);
-        const float e = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.bias2 - st.z)) * st.y;
-        const float g = (yt >= 0 ? rc.scale : 0.f) * (yt == rc.y ? e - 1.0f : e);
+        const float e = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.bias2 - st.z)) * fmaf(rc.zl2, st.z, 1.0f);
+        const float g = (rc.scale * st.y) * (yt == rc.y ? e - 1.0f : e);
         gbias += g;
         r[i] = __float_as_uint(g);
       }
@@ -197,7 +201,7 @@ __device__ __forceinline__ void ds_chunk64(uint32_t (&r)[64], int col0, const Ds
       for (int i = 0; i < 64; ++i) {
         const float4 st = tstats[i];
         float g = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.c + st.x));
-        if (__float_as_int(st.w) == rc.y) g -= rc.scale;
+        if (__float_as_int(st.w) == rc.y) g -= rc.scale * st.y;
         gbias += g;
         r[i] = __float_as_uint(g);
       }
@@ -440,15 +444,15 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
     // takes the general form, with f and the onehot weight as separate factors.
     const bool general = (*p.zf_neg != 0u);
     const float log2s = log2f(scale);
-    DsRow rc{-INFINITY, 0.f, 0.f, 0.f, 0.f, scale, -1};
+    DsRow rc{-INFINITY, 0.f, 0.f, 0.f, 0.f, scale, 2.0f * p.z_loss * kLn2, -1};
     if (!kVocabRows) {
       if (row < p.BT) {
         const float4 st = p.stats[row];
         rc.c = st.x + log2s;
-        rc.f = st.y;
         rc.lse2 = st.z;
+        rc.f = fmaf(rc.zl2, st.z, 1.0f);
         rc.y = __float_as_int(st.w);
-        rc.coef = rc.y >= 0 ? scale : 0.f;
+        rc.coef = scale * st.y;
       }
     } else {
       if (p.bias != nullptr && row < p.V) rc.bias2 = __ldg(p.bias + row) * kLog2e;
@@ -543,11 +547,20 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
               if (cb + 8 * g8 + 8 <= hc) {
-                *reinterpret_cast<uint4*>(out + 8 * g8) =
-                    make_uint4(pack_bf16x2(__uint_as_float(vv[8 * g8 + 0]), __uint_as_float(vv[8 * g8 + 1])),
-                               pack_bf16x2(__uint_as_float(vv[8 * g8 + 2]), __uint_as_float(vv[8 * g8 + 3])),
-                               pack_bf16x2(__uint_as_float(vv[8 * g8 + 4]), __uint_as_float(vv[8 * g8 + 5])),
-                               pack_bf16x2(__uint_as_float(vv[8 * g8 + 6]), __uint_as_float(vv[8 * g8 + 7])));
+                float o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(vv[8 * g8 + e]);
+                if (p.accumulate) {
+                  const uint4 old = *reinterpret_cast<const uint4*>(out + 8 * g8);
+                  const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    o[2 * e] += bf16_lo(ow[e]);
+                    o[2 * e + 1] += bf16_hi(ow[e]);
+                  }
+                }
+                *reinterpret_cast<uint4*>(out + 8 * g8) = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                                                                     pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
               }
             }
           }
@@ -556,10 +569,18 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
             float* out = p.grad_W + static_cast<size_t>(row) * p.H + h0 + cb;
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
-              if (cb + 4 * g4 + 4 <= hc)
-                *reinterpret_cast<float4*>(out + 4 * g4) =
-                    make_float4(__uint_as_float(vv[4 * g4 + 0]), __uint_as_float(vv[4 * g4 + 1]),
-                                __uint_as_float(vv[4 * g4 + 2]), __uint_as_float(vv[4 * g4 + 3]));
+              if (cb + 4 * g4 + 4 <= hc) {
+                float4 o = make_float4(__uint_as_float(vv[4 * g4 + 0]), __uint_as_float(vv[4 * g4 + 1]),
+                                       __uint_as_float(vv[4 * g4 + 2]), __uint_as_float(vv[4 * g4 + 3]));
+                if (p.accumulate) {
+                  const float4 old = *reinterpret_cast<const float4*>(out + 4 * g4);
+                  o.x += old.x;
+                  o.y += old.y;
+                  o.z += old.z;
+                  o.w += old.w;
+                }
+                *reinterpret_cast<float4*>(out + 4 * g4) = o;
+              }
             }
           }
         }
@@ -581,7 +602,7 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
     if (row < p.V) {
       float acc = 0.f;
       for (int pp = 0; pp < P; ++pp) acc += sm.gb_gather[pp][rl];
-      p.grad_bias[row] = acc;
+      p.grad_bias[row] = p.accumulate ? p.grad_bias[row] + acc : acc;
     }
   }
   if (warp == kMmaWarp) {
@@ -609,6 +630,8 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   p.colb2 = a.colb2;
   p.scale = a.scale;
   p.zf_neg = a.zf_neg;
+  p.z_loss = a.z_loss;
+  p.accumulate = a.accumulate ? 1 : 0;
   p.BT = a.BT;
   p.V = a.V;
   p.H = a.H;

@@ -252,8 +252,9 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
 // passes read; per vocabulary column: the bias in log2 units, -inf past V.
 __global__ void lse_merge_kernel(const float2* __restrict__ part, int splits, int BTp, const float* __restrict__ zy,
                                  const int64_t* __restrict__ target, int BT, int V, int64_t ignore_index,
-                                 float z_loss, const float* __restrict__ bias, float4* __restrict__ stats,
-                                 float* __restrict__ row_loss, float* __restrict__ colb2,
+                                 float z_loss, const float* __restrict__ bias, const float* __restrict__ grad_tok,
+                                 float4* __restrict__ stats, float* __restrict__ row_loss,
+                                 float* __restrict__ loss_tok, float* __restrict__ colb2,
                                  uint32_t* __restrict__ zf_neg, uint32_t* __restrict__ status) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   // per-column bias in log2 units for the gradient passes; -inf masks the columns past V
@@ -275,10 +276,16 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, int splits, in
   const int64_t y = target[t];
   const bool valid = (y != ignore_index) && (y >= 0) && (y < V);
   if (!valid && y != ignore_index) atomicOr(status, kStatusBadTarget);
-  row_loss[t] = valid ? (lse - zy[t]) + z_loss * lse * lse : 0.f;
+  const float lt = valid ? (lse - zy[t]) + z_loss * lse * lse : 0.f;
+  row_loss[t] = lt;
+  if (loss_tok != nullptr) loss_tok[t] = lt;
+  // dS of this row = G u f 2^(S log2 e - LSE2) - G u [n = y] with G the scalar gradient scale and u the
+  // row's upstream gradient; the log form 2^(S log2 e + log2(u f) - LSE2) needs u f > 0
+  const float u = grad_tok != nullptr ? grad_tok[t] : 1.0f;
   const float f = 1.0f + 2.0f * z_loss * lse;
-  if (valid && !(f > 0.f)) atomicOr(zf_neg, 1u);
-  stats[t] = make_float4(valid && f > 0.f ? log2f(f) - lse2 : -INFINITY, valid ? f : 0.f, lse2,
+  const float uf = u * f;
+  if (valid && u != 0.f && !(uf > 0.f)) atomicOr(zf_neg, 1u);
+  stats[t] = make_float4(valid && uf > 0.f ? log2f(uf) - lse2 : -INFINITY, valid ? u : 0.f, lse2,
                          __int_as_float(valid ? static_cast<int>(y) : -1));
 }
 
@@ -286,8 +293,8 @@ constexpr int kReduceThreads = 1024;
 
 __global__ void __launch_bounds__(kReduceThreads)
 loss_reduce_kernel(const float* __restrict__ row_loss, const float4* __restrict__ stats, int BT, int reduction,
-                   float* __restrict__ scale_ws, int64_t* __restrict__ n_valid_ws, float* __restrict__ loss,
-                   int64_t* __restrict__ n_valid_out) {
+                   float grad_scale, float* __restrict__ scale_ws, int64_t* __restrict__ n_valid_ws,
+                   uint32_t* __restrict__ zf_neg, float* __restrict__ loss, int64_t* __restrict__ n_valid_out) {
   __shared__ double s_sum[kReduceThreads / 32];
   __shared__ long long s_cnt[kReduceThreads / 32];
   double acc = 0.0;
@@ -314,8 +321,11 @@ loss_reduce_kernel(const float* __restrict__ row_loss, const float4* __restrict_
       n += s_cnt[w];
     }
     const double scale = (reduction == 0) ? 1.0 / static_cast<double>(n > 0 ? n : 1) : 1.0;
-    *loss = static_cast<float>(total * scale);
-    *scale_ws = static_cast<float>(scale);
+    if (loss != nullptr) *loss = static_cast<float>(total * scale);
+    // the gradient scale; the log form of dS needs it positive
+    const float G = static_cast<float>(scale * static_cast<double>(grad_scale));
+    *scale_ws = G;
+    if (!(G > 0.f)) *zf_neg |= 1u;
     *n_valid_ws = n;
     if (n_valid_out != nullptr) *n_valid_out = n;
   }
@@ -403,14 +413,14 @@ cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int 
     if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
     const int merge_threads = max((BT + 255) & ~255, (V + 255) & ~255);
     lse_merge_kernel<<<merge_threads / 256, 256, 0, stream>>>(ws.part, splits, BTp, ws.zy, a.target, BT, V,
-                                                            a.ignore_index, a.z_loss, a.bias, ws.stats,
-                                                            ws.row_loss, ws.colb2, ws.zf_neg, ws.status);
+                                                            a.ignore_index, a.z_loss, a.bias, a.grad_tok, ws.stats,
+                                                            ws.row_loss, a.loss_tok, ws.colb2, ws.zf_neg, ws.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) {
     return e;
   }
-  loss_reduce_kernel<<<1, kReduceThreads, 0, stream>>>(ws.row_loss, ws.stats, BT, a.reduction, ws.scale, ws.n_valid,
-                                                      a.loss, a.n_valid_out);
+  loss_reduce_kernel<<<1, kReduceThreads, 0, stream>>>(ws.row_loss, ws.stats, BT, a.reduction, a.grad_scale, ws.scale,
+                                                      ws.n_valid, ws.zf_neg, a.loss, a.n_valid_out);
   return cudaGetLastError();
 }
 

@@ -27,13 +27,15 @@ constexpr int kTileM = 128;        // rows of every MMA tile (tokens or vocabula
 
 struct FusedWorkspace {
   uint32_t* status;  // header: status word
-  float* scale;      // header: s = 1/max(n_valid, 1) or 1
+  float* scale;      // header: gradient scale G = grad_scale / max(n_valid, 1) (mean) or grad_scale
   int64_t* n_valid;  // header: valid count
-  uint32_t* zf_neg;  // header: non-zero when a valid row has 1 + 2 z_loss LSE <= 0
+  uint32_t* zf_neg;  // header: non-zero when the log form of dS does not apply (some valid row has
+                     // f u <= 0 with u its upstream gradient, or the gradient scale is <= 0)
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
   float* zy;         // [BTp] target logit
-  float4* stats;     // [BT rounded up to 256] per row t, with LSE2 = LSE log2 e and f = 1 + 2 z_loss LSE:
-                     //   x = log2(f) - LSE2 (-inf for ignored rows and when f <= 0), y = valid ? f : 0,
+  float4* stats;     // [BT rounded up to 256] per row t, with LSE2 = LSE log2 e, f = 1 + 2 z_loss LSE and u
+                     // the row's upstream gradient (1 unless reduction none):
+                     //   x = log2(f u) - LSE2 (-inf for ignored rows and when f u <= 0), y = valid ? u : 0,
                      //   z = LSE2, w = target as int bits (-1 for ignored rows); rows past BT: (-inf, 0, 0, -1)
   float* row_loss;   // [BTp] valid * (LSE - z_y + z_loss LSE^2)
   float* colb2;      // [V rounded up to 256] bias * log2 e (0 without bias); -inf past V
@@ -49,13 +51,17 @@ struct FusedArgs {
   const int64_t* target;
   int64_t BT, H, V;
   int64_t ignore_index;
-  int reduction;
+  int reduction;              // 0 mean, 1 sum, 2 none
   float z_loss;
-  float* loss;
+  float* loss;                // may be NULL for reduction none
   uint16_t* grad_input;
   float* grad_W;
   float* grad_bias;
   int64_t* n_valid_out;
+  float grad_scale;           // upstream gradient of the reduced loss
+  const float* grad_tok;      // reduction none: upstream gradient per token, or NULL (ones)
+  float* loss_tok;            // per-token losses out, or NULL
+  bool accumulate;            // gradients += instead of =
 };
 
 // Arguments of the gradient passes on CTA pairs (flce_bwd.cu).
@@ -65,6 +71,8 @@ struct DgPairArgs {
   const float* colb2;
   const float* scale;
   const uint32_t* zf_neg;
+  float z_loss;
+  bool accumulate;
   int BT, V, H;
   uint16_t* grad_input;
   float* grad_W;

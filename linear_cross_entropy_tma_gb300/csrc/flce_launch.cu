@@ -21,10 +21,12 @@ cudaError_t launch_fused(const FusedArgs& a, void* workspace, int num_sms, cudaS
 
   const bool want_dw = (a.grad_W != nullptr) || (a.grad_bias != nullptr);
   if (a.BT == 0) {
-    // no tokens: every gradient is zero
-    if (a.grad_W != nullptr && (e = cudaMemsetAsync(a.grad_W, 0, sizeof(float) * a.V * a.H, stream)) != cudaSuccess)
+    // no tokens: every gradient is zero (unchanged when accumulating)
+    if (!a.accumulate && a.grad_W != nullptr &&
+        (e = cudaMemsetAsync(a.grad_W, 0, sizeof(float) * a.V * a.H, stream)) != cudaSuccess)
       return e;
-    if (a.grad_bias != nullptr && (e = cudaMemsetAsync(a.grad_bias, 0, sizeof(float) * a.V, stream)) != cudaSuccess)
+    if (!a.accumulate && a.grad_bias != nullptr &&
+        (e = cudaMemsetAsync(a.grad_bias, 0, sizeof(float) * a.V, stream)) != cudaSuccess)
       return e;
     if ((e = mark(3)) != cudaSuccess) return e;
     return mark(4);
@@ -35,6 +37,8 @@ cudaError_t launch_fused(const FusedArgs& a, void* workspace, int num_sms, cudaS
   pa.colb2 = ws.colb2;
   pa.scale = ws.scale;
   pa.zf_neg = ws.zf_neg;
+  pa.z_loss = a.z_loss;
+  pa.accumulate = a.accumulate;
   pa.BT = static_cast<int>(a.BT);
   pa.V = static_cast<int>(a.V);
   pa.H = static_cast<int>(a.H);
