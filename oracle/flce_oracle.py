@@ -29,6 +29,8 @@ Readings where the pages are silent (each also listed in the design notes):
   * with z-loss in the fused loss, l_t = LSE_t - z_y + z_loss * LSE_t^2, so the gradient row is
     p * (1 + 2 z_loss LSE_t) - onehot(y_t);
   * n_valid = 0 gives loss 0 and all-zero gradients (the clamp of p3 "Usage");
+  * the per-row entropy that verl's forward kernel returns (p1 "Strategy 2", entropy_b) is read as the
+    Shannon entropy of softmax(z_t), computed for every row whatever its target;
   * reduction "none" returns the per-token losses; its gradients are those of sum_t g_t l_t for an
     upstream gradient g (PyTorch's convention for an unreduced loss), and every gradient is
     multiplied by the scalar upstream gradient of the reduced loss (the d_out / grad_scale factor of
@@ -93,7 +95,8 @@ def flce_reference(hidden, W, target, bias=None, ignore_index: int = -100, reduc
     """Loss and gradients of fused linear cross-entropy, straight from the definitions.
 
     Returns a dict with ``loss`` (float), ``n_valid`` (int), ``lse`` [BT], ``loss_per_token`` [BT]
-    (l_t on valid rows, 0 elsewhere), and when ``want_grads`` ``grad_input`` [BT, H], ``grad_W`` [V, H],
+    (l_t on valid rows, 0 elsewhere), ``entropy`` [BT] (the entropy of softmax(z_t) for every row,
+    -sum_n p log p = LSE_t - sum_n p_n z_n), and when ``want_grads`` ``grad_input`` [BT, H], ``grad_W`` [V, H],
     ``grad_bias`` [V] (None without a bias), all float64.
 
     reduction "mean" / "sum": ``loss`` is the reduced loss.  reduction "none": ``loss`` is the plain
@@ -113,6 +116,7 @@ def flce_reference(hidden, W, target, bias=None, ignore_index: int = -100, reduc
 
     loss_terms = []
     lse_all = np.empty(BT)
+    ent_all = np.empty(BT)
     u = np.ones(BT) if grad_loss_per_token is None else np.asarray(grad_loss_per_token, dtype=np.float64)
     if want_grads:
         grad_input = np.zeros((BT, H))
@@ -129,6 +133,7 @@ def flce_reference(hidden, W, target, bias=None, ignore_index: int = -100, reduc
         denom = e.sum(axis=1)
         L = m + np.log(denom)
         lse_all[r0:r1] = L
+        ent_all[r0:r1] = L - (e * z).sum(axis=1) / denom
         v = valid[r0:r1]
         y = np.where(v, t[r0:r1], 0)
         z_y = z[rows, y]
@@ -145,7 +150,7 @@ def flce_reference(hidden, W, target, bias=None, ignore_index: int = -100, reduc
                 grad_b += d.sum(axis=0)
     per_token = np.concatenate(loss_terms) if loss_terms else np.zeros(0)
     loss = s * math.fsum(per_token.tolist()) if loss_terms else 0.0
-    out = dict(loss=loss, n_valid=n_valid, lse=lse_all, loss_per_token=per_token)
+    out = dict(loss=loss, n_valid=n_valid, lse=lse_all, loss_per_token=per_token, entropy=ent_all)
     if want_grads:
         out.update(grad_input=grad_input, grad_W=grad_W, grad_bias=grad_b)
     return out

@@ -6,7 +6,8 @@
   * an independent library: torch.nn.functional.cross_entropy in float64 on the CPU, with autograd;
   * closed forms: W = 0, V = 1, and the hand-evaluated values in tests/golden/ce_closed_forms.txt;
   * invariants: LSE shift, dlogits row sums, ignored rows, n_valid = 0, vocabulary permutation;
-  * the unreduced loss with an upstream gradient against finite differences and torch autograd.
+  * the unreduced loss with an upstream gradient against finite differences and torch autograd;
+  * the per-row entropy against torch, plain loops, closed forms and its bounds.
 
 The same checks run against deliberately broken copies of the oracle (test_planted_mistakes) to show
 that a dropped term, a wrong sign, a wrong index or a wrong scale fails at least one of them.
@@ -280,8 +281,33 @@ def pin_unreduced_and_upstream(orc):
         assert _rel(n[k], m[k]) < 1e-12, k
 
 
+def pin_entropy(orc):
+    # torch: -(softmax * log_softmax).sum over the vocabulary, for every row (ignored ones included)
+    hidden, W, b, t = _tiny_case(seed=23, BT=21, H=9, V=40, ignore_rows=(0, 4))
+    got = orc.flce_reference(hidden, W, t, bias=b, row_block=5, want_grads=False)
+    z = torch.tensor(hidden) @ torch.tensor(W).T + torch.tensor(b)
+    ref = -(torch.softmax(z, dim=1) * torch.log_softmax(z, dim=1)).sum(dim=1).numpy()
+    assert _rel(got["entropy"], ref) < 1e-13
+    # brute force per row from the definition, in plain loops
+    for r in (0, 7, 20):
+        zr = hidden[r] @ W.T + b
+        pr = [math.exp(v - max(zr)) for v in zr]
+        tot = math.fsum(pr)
+        h = -math.fsum((q / tot) * math.log(q / tot) for q in pr)
+        assert abs(got["entropy"][r] - h) < 1e-12
+    # closed forms and bounds: W = 0 gives the uniform distribution (log V); V = 1 gives 0; a constant
+    # added to every logit changes nothing; 0 <= H <= log V
+    g0 = orc.flce_reference(hidden, np.zeros_like(W), t, want_grads=False, row_block=5)
+    assert np.max(np.abs(g0["entropy"] - math.log(W.shape[0]))) < 1e-13
+    g1 = orc.flce_reference(hidden, W[:1], np.zeros_like(t), want_grads=False, row_block=5)
+    assert np.max(np.abs(g1["entropy"])) < 1e-15
+    g2 = orc.flce_reference(hidden, W, t, bias=b + 7.5, row_block=5, want_grads=False)
+    assert _rel(g2["entropy"], got["entropy"]) < 1e-12
+    assert np.all(got["entropy"] >= 0) and np.all(got["entropy"] <= math.log(W.shape[0]) + 1e-12)
+
+
 PINS = [pin_loops_vs_vectorised, pin_finite_differences, pin_torch_fp64, pin_closed_forms,
-        pin_invariants, pin_ce, pin_sampled_matches_full, pin_unreduced_and_upstream]
+        pin_invariants, pin_ce, pin_sampled_matches_full, pin_unreduced_and_upstream, pin_entropy]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -304,6 +330,8 @@ MUTATIONS = {
     "CE target column not adjusted": ("        d[rows, y[r0:r1]] -= 1.0\n        dl[r0:r1]", "        dl[r0:r1]"),
     "upstream gradient ignored": ("d *= (grad_scale * u[r0:r1])[:, None]", "d *= grad_scale"),
     "grad_scale applied twice": ("d *= (grad_scale * u[r0:r1])[:, None]", "d *= (grad_scale * grad_scale * u[r0:r1])[:, None]"),
+    "entropy sign flipped": ("ent_all[r0:r1] = L - (e * z).sum(axis=1) / denom", "ent_all[r0:r1] = (e * z).sum(axis=1) / denom - L"),
+    "entropy unnormalised": ("ent_all[r0:r1] = L - (e * z).sum(axis=1) / denom", "ent_all[r0:r1] = L - (e * z).sum(axis=1)"),
     "grad_input uses transposed product": ("grad_input[r0:r1] = d @ w", "grad_input[r0:r1] = (w.T @ d.T).T * 0 + d @ w[::-1]"),
 }
 
