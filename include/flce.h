@@ -139,18 +139,23 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        valid rows and 0 on ignored rows (any reduction).
  *   accumulate           non-zero: grad_input, grad_W and grad_bias receive += instead of = (their
  *                        previous contents are added to; grad_input is re-rounded to bf16).
+ *   entropy              [BT] fp32, device, or NULL: the entropy of softmax(z_t) for every row,
+ *                        -sum_n p_n log p_n = LSE_t - sum_n p_n z_n (verl's per-row entropy output,
+ *                        "Fused Linear Cross-Entropy", "Strategy 2"), ignored rows included.  Costs
+ *                        one more multiply-add per logit in the LSE pass.
  */
 typedef struct flce_fwd_bwd_options {
   float grad_scale;
   const float* grad_loss_per_token;
   float* loss_per_token;
   int accumulate;
+  float* entropy;
 } flce_fwd_bwd_options;
 
 /*
  * flce_fwd_bwd with options (NULL options = the defaults above).  reduction may also be
  * FLCE_REDUCTION_NONE; then `loss` may be NULL and, when given, receives the plain sum of the
- * per-token losses.  Pointer alignment: loss_per_token and grad_loss_per_token 4 bytes.
+ * per-token losses.  Pointer alignment: loss_per_token, grad_loss_per_token and entropy 4 bytes.
  */
 flce_status flce_fwd_bwd_ex(const uint16_t* hidden, const uint16_t* W, const float* bias,
                             const int64_t* target, int64_t BT, int64_t H, int64_t V,

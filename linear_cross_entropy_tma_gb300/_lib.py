@@ -31,7 +31,7 @@ c_sz = ctypes.c_size_t
 class FwdBwdOptions(ctypes.Structure):
     """flce_fwd_bwd_options of include/flce.h."""
     _fields_ = [("grad_scale", ctypes.c_float), ("grad_loss_per_token", c_p), ("loss_per_token", c_p),
-                ("accumulate", ctypes.c_int)]
+                ("accumulate", ctypes.c_int), ("entropy", c_p)]
 
 
 def load() -> ctypes.CDLL:
@@ -101,14 +101,15 @@ def _bf16_ptr_ok(t, name):
 def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reduction: str = "mean",
                  z_loss: float = 0.0, need_grad_input: bool = True, need_grad_W: bool = True, workspace=None,
                  out=None, stream=None, pass_events=None, grad_scale: float = 1.0, grad_loss_per_token=None,
-                 accumulate: bool = False, want_loss_per_token: bool = False) -> dict:
+                 accumulate: bool = False, want_loss_per_token: bool = False, want_entropy: bool = False) -> dict:
     """Fused linear cross-entropy forward + backward on the current CUDA device.
 
     hidden [BT, H] bf16, W [V, H] bf16, target [BT] int64, bias [V] fp32 or None.  Returns a dict with
     ``loss`` (fp32 [1]; for reduction "none" the plain sum of the per-token losses), ``n_valid``
     (int64 [1]), ``grad_input`` (bf16 [BT, H] or None), ``grad_W`` (fp32 [V, H] or None),
-    ``grad_bias`` (fp32 [V] or None) and ``loss_per_token`` (fp32 [BT], for reduction "none" or when
-    ``want_loss_per_token``; else None).  ``out`` may supply preallocated outputs with the same keys;
+    ``grad_bias`` (fp32 [V] or None), ``loss_per_token`` (fp32 [BT], for reduction "none" or when
+    ``want_loss_per_token``; else None) and ``entropy`` (fp32 [BT], the entropy of each row's softmax,
+    when ``want_entropy``; else None).  ``out`` may supply preallocated outputs with the same keys;
     ``workspace`` a uint8 CUDA tensor of at least ``workspace_size`` bytes.
 
     ``grad_scale`` multiplies every gradient; ``grad_loss_per_token`` (fp32 [BT], reduction "none"
@@ -139,6 +140,8 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
         o["n_valid"] = torch.empty(1, dtype=torch.int64, device=dev)
     if (reduction == "none" or want_loss_per_token) and o.get("loss_per_token") is None:
         o["loss_per_token"] = torch.empty(BT, dtype=torch.float32, device=dev)
+    if want_entropy and o.get("entropy") is None:
+        o["entropy"] = torch.empty(BT, dtype=torch.float32, device=dev)
     if accumulate and ((need_grad_input and o.get("grad_input") is None) or (need_grad_W and o.get("grad_W") is None)
                        or (need_grad_W and bias is not None and o.get("grad_bias") is None)):
         raise ValueError("accumulate needs the gradient tensors to add to in `out`")
@@ -152,12 +155,14 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     gw = o.get("grad_W") if need_grad_W else None
     gb = o.get("grad_bias") if (need_grad_W and bias is not None) else None
     lt = o.get("loss_per_token")
+    ent = o.get("entropy") if want_entropy else None
     need = workspace_size(BT, H, V)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     args = (_ptr(hidden), _ptr(W), _ptr(bias), _ptr(target), BT, H, V, ignore_index, red, float(z_loss),
             _ptr(o["loss"]), _ptr(gi), _ptr(gw), _ptr(gb), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel())
-    plain = red != 2 and grad_scale == 1.0 and grad_loss_per_token is None and not accumulate and lt is None
+    plain = (red != 2 and grad_scale == 1.0 and grad_loss_per_token is None and not accumulate and lt is None
+             and ent is None)
     if pass_events is not None:
         if not plain:
             raise ValueError("pass_events only with the default options")
@@ -168,10 +173,10 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     elif plain:
         check(load().flce_fwd_bwd(*args, _stream_ptr(stream)))
     else:
-        opts = FwdBwdOptions(float(grad_scale), _ptr(grad_loss_per_token), _ptr(lt), 1 if accumulate else 0)
+        opts = FwdBwdOptions(float(grad_scale), _ptr(grad_loss_per_token), _ptr(lt), 1 if accumulate else 0, _ptr(ent))
         check(load().flce_fwd_bwd_ex(*args, ctypes.byref(opts), _stream_ptr(stream)))
     return dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, loss_per_token=lt,
-                workspace=workspace)
+                entropy=ent, workspace=workspace)
 
 
 def ce_with_grad(logits, labels, ignore_index: int = -100, z_loss: float = 0.0, workspace=None, out=None,

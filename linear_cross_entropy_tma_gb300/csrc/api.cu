@@ -105,7 +105,8 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
                                 void* workspace, size_t workspace_bytes, const flce_fwd_bwd_options* options,
                                 void* stream, void* const* events, int n_events) {
   g_last_error[0] = '\0';
-  const flce_fwd_bwd_options opt = options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0};
+  const flce_fwd_bwd_options opt =
+      options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0, nullptr};
   if (n_events != 0 && (n_events != 5 || events == nullptr)) {
     set_error("n_events must be 0 or 5 (with a non-NULL event array)");
     return FLCE_ERR_INVALID_ARG;
@@ -149,7 +150,7 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(grad_input, 16) || !aligned(grad_W, 16) ||
       !aligned(workspace, 256) || !aligned(bias, 4) || !aligned(grad_bias, 4) || !aligned(loss, 4) ||
       !aligned(target, 8) || !aligned(n_valid, 8) || !aligned(opt.loss_per_token, 4) ||
-      !aligned(opt.grad_loss_per_token, 4)) {
+      !aligned(opt.grad_loss_per_token, 4) || !aligned(opt.entropy, 4)) {
     set_error("misaligned pointer (hidden, W, grad_input, grad_W need 16 bytes; workspace 256)");
     return FLCE_ERR_MISALIGNED;
   }
@@ -182,6 +183,7 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   a.grad_tok = opt.grad_loss_per_token;
   a.loss_tok = opt.loss_per_token;
   a.accumulate = opt.accumulate != 0;
+  a.entropy = opt.entropy;
   char err[256] = "";
   const cudaError_t e = flce::launch_fused(a, workspace, num_sms, static_cast<cudaStream_t>(stream), err, sizeof(err),
                                            n_events ? reinterpret_cast<cudaEvent_t const*>(events) : nullptr);

@@ -32,13 +32,16 @@ constexpr int kThreads = 10 * 32;
 constexpr uint32_t kTmemCols = 512;
 
 
-__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
+// Merge of two online (max, sum, weighted sum) states: m in log2 units, s = sum 2^(x - m),
+// t = sum 2^(x - m) z (z the logit; used for the entropy).
+__device__ __forceinline__ void merge_mst(float& m, float& s, float& t, float m2, float s2, float t2) {
   const float mn = fmaxf(m, m2);
   if (mn == -INFINITY) return;
-  const float a = (m == mn) ? s : s * ex2_approx(m - mn);
-  const float b = (m2 == mn) ? s2 : s2 * ex2_approx(m2 - mn);
+  const float a = (m == mn) ? 1.f : ex2_approx(m - mn);
+  const float b = (m2 == mn) ? 1.f : ex2_approx(m2 - mn);
   m = mn;
-  s = a + b;
+  s = s * a + s2 * b;
+  t = t * a + t2 * b;
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -59,15 +62,19 @@ struct LsePairSmem {
   uint32_t tmem_base;
   int abort;
   float2 half_ms[kTileM];
+  float half_t[kTileM];
 };
 constexpr size_t kLsePairSmemBytes = sizeof(LsePairSmem) + 1024;
 static_assert(kLsePairSmemBytes <= 232448, "shared memory budget of one CTA exceeded");
 
+// kEntropy: also accumulate t = sum 2^(x - m) z per row and split (part_t) for the row entropy.
+template <bool kEntropy>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                 const float* __restrict__ bias, const int64_t* __restrict__ target, int BT, int V,
                 int64_t ignore_index, int num_kb, int tiles_per_split, int n_tiles, int BTp,
-                float2* __restrict__ part, float* __restrict__ zy_out, uint32_t* __restrict__ status) {
+                float2* __restrict__ part, float* __restrict__ part_t, float* __restrict__ zy_out,
+                uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   LsePairSmem& sm =
       *reinterpret_cast<LsePairSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,7 +189,7 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
       if (t != ignore_index && t >= 0 && t < V) y = t;
     }
     const bool has_bias = (bias != nullptr);
-    float m = -INFINITY, s = 0.f, zy = 0.f;
+    float m = -INFINITY, s = 0.f, t = 0.f, zy = 0.f;
     bool found = false;
     for (int j = 0; j < nt; ++j) {
       const int acc = j & 1;
@@ -218,10 +225,17 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
         // log2 e > 0, so the max of the scaled values is the scaled max
         const float mn = fmaxf(m, cm * kLog2e);
         if (mn != -INFINITY) {
-          float acc_s = (m == -INFINITY) ? 0.f : s * ex2_approx(m - mn);
+          const float resc = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+          float acc_s = s * resc;
+          float acc_t = t * resc;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc_s += ex2_approx(fmaf(x[i], kLog2e, -mn));
+          for (int i = 0; i < 32; ++i) {
+            const float e = ex2_approx(fmaf(x[i], kLog2e, -mn));
+            acc_s += e;
+            if (kEntropy) acc_t = fmaf(e, (full || col0 + i < V) ? x[i] : 0.f, acc_t);
+          }
           s = acc_s;
+          t = acc_t;
           m = mn;
         }
       }
@@ -229,12 +243,18 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? acc_empty_c1 : acc_empty_c0);
     }
-    if (h == 1) sm.half_ms[row_local] = make_float2(m, s);
+    if (h == 1) {
+      sm.half_ms[row_local] = make_float2(m, s);
+      if (kEntropy) sm.half_t[row_local] = t;
+    }
     named_barrier_sync(1, kEpiWarps * 32);
     if (h == 0) {
       const float2 o = sm.half_ms[row_local];
-      merge_ms(m, s, o.x, o.y);
-      if (row < BT) part[static_cast<size_t>(split) * BTp + row] = make_float2(m, s);
+      merge_mst(m, s, t, o.x, o.y, kEntropy ? sm.half_t[row_local] : 0.f);
+      if (row < BT) {
+        part[static_cast<size_t>(split) * BTp + row] = make_float2(m, s);
+        if (kEntropy) part_t[static_cast<size_t>(split) * BTp + row] = t;
+      }
     }
     if (found && row < BT) zy_out[row] = zy;
   }
@@ -250,7 +270,8 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
 
 // Per row: merge of the split partials into LSE, the row's loss term and the statistics the gradient
 // passes read; per vocabulary column: the bias in log2 units, -inf past V.
-__global__ void lse_merge_kernel(const float2* __restrict__ part, int splits, int BTp, const float* __restrict__ zy,
+__global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ part_t, int splits, int BTp,
+                                 float* __restrict__ entropy, const float* __restrict__ zy,
                                  const int64_t* __restrict__ target, int BT, int V, int64_t ignore_index,
                                  float z_loss, const float* __restrict__ bias, const float* __restrict__ grad_tok,
                                  float4* __restrict__ stats, float* __restrict__ row_loss,
@@ -266,13 +287,19 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, int splits, in
   }
   float M = -INFINITY;
   for (int s = 0; s < splits; ++s) M = fmaxf(M, part[static_cast<size_t>(s) * BTp + t].x);
-  float S = 0.f;
+  float S = 0.f, T = 0.f;
   for (int s = 0; s < splits; ++s) {
     const float2 p = part[static_cast<size_t>(s) * BTp + t];
-    if (p.x != -INFINITY) S += p.y * exp2f(p.x - M);
+    if (p.x != -INFINITY) {
+      const float w = exp2f(p.x - M);
+      S += p.y * w;
+      if (entropy != nullptr) T += part_t[static_cast<size_t>(s) * BTp + t] * w;
+    }
   }
   const float lse2 = M + log2f(S);
   const float lse = lse2 * kLn2;
+  // entropy of softmax(z_t) = LSE - sum_n p_n z_n, for every row
+  if (entropy != nullptr) entropy[t] = lse - T / S;
   const int64_t y = target[t];
   const bool valid = (y != ignore_index) && (y >= 0) && (y < V);
   if (!valid && y != ignore_index) atomicOr(status, kStatusBadTarget);
@@ -360,6 +387,7 @@ size_t fused_workspace_bytes(int64_t BT, int64_t V) {
   const size_t vp = align_up(static_cast<size_t>(V > 0 ? V : 0), 256);
   size_t off = 256;
   off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
+  off += align_up(sizeof(float) * kMaxSplits * btp, 256);
   off += align_up(sizeof(float) * btp, 256);
   off += align_up(sizeof(float4) * align_up(btp, 256), 256);
   off += align_up(sizeof(float) * btp, 256);
@@ -379,6 +407,8 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   size_t off = 256;
   w.part = reinterpret_cast<float2*>(p + off);
   off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
+  w.part_t = reinterpret_cast<float*>(p + off);
+  off += align_up(sizeof(float) * kMaxSplits * btp, 256);
   w.zy = reinterpret_cast<float*>(p + off);
   off += align_up(sizeof(float) * btp, 256);
   w.stats = reinterpret_cast<float4*>(p + off);
@@ -404,15 +434,18 @@ cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int 
     const int splits = choose_splits(pairs, n_tiles, num_sms / 2);
     const int tps = (n_tiles + splits - 1) / splits;
     const int num_kb = static_cast<int>((a.H + kBK - 1) / kBK);
-    e = cudaFuncSetAttribute(lse_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kLsePairSmemBytes));
+    const bool want_entropy = (a.entropy != nullptr);
+    auto kern = want_entropy ? lse_pair_kernel<true> : lse_pair_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kLsePairSmemBytes));
     if (e != cudaSuccess) return e;
-    lse_pair_kernel<<<dim3(2 * pairs, splits), kThreads, kLsePairSmemBytes, stream>>>(
-        tm_h, tm_w, a.bias, a.target, BT, V, a.ignore_index, num_kb, tps, n_tiles, BTp, ws.part, ws.zy, ws.status);
+    kern<<<dim3(2 * pairs, splits), kThreads, kLsePairSmemBytes, stream>>>(
+        tm_h, tm_w, a.bias, a.target, BT, V, a.ignore_index, num_kb, tps, n_tiles, BTp, ws.part, ws.part_t, ws.zy,
+        ws.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
     const int merge_threads = max((BT + 255) & ~255, (V + 255) & ~255);
-    lse_merge_kernel<<<merge_threads / 256, 256, 0, stream>>>(ws.part, splits, BTp, ws.zy, a.target, BT, V,
+    lse_merge_kernel<<<merge_threads / 256, 256, 0, stream>>>(ws.part, ws.part_t, splits, BTp, a.entropy, ws.zy,
+                                                            a.target, BT, V,
                                                             a.ignore_index, a.z_loss, a.bias, a.grad_tok, ws.stats,
                                                             ws.row_loss, a.loss_tok, ws.colb2, ws.zf_neg, ws.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

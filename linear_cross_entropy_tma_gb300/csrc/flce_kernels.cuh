@@ -32,6 +32,7 @@ struct FusedWorkspace {
   uint32_t* zf_neg;  // header: non-zero when the log form of dS does not apply (some valid row has
                      // f u <= 0 with u its upstream gradient, or the gradient scale is <= 0)
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
+  float* part_t;     // [kMaxSplits][BTp] sum of 2^(x - max) z (only when the entropy is requested)
   float* zy;         // [BTp] target logit
   float4* stats;     // [BT rounded up to 256] per row t, with LSE2 = LSE log2 e, f = 1 + 2 z_loss LSE and u
                      // the row's upstream gradient (1 unless reduction none):
@@ -61,6 +62,7 @@ struct FusedArgs {
   float grad_scale;           // upstream gradient of the reduced loss
   const float* grad_tok;      // reduction none: upstream gradient per token, or NULL (ones)
   float* loss_tok;            // per-token losses out, or NULL
+  float* entropy;             // per-row entropy of softmax(z) out, or NULL
   bool accumulate;            // gradients += instead of =
 };
 

@@ -1,7 +1,7 @@
 """flce_fwd_bwd_ex options against the fp64 oracle on the GPU, through the C ABI: reduction "none" with
 per-token upstream gradients (positive, negative and zero), a scalar gradient scale (including a
 negative one, which takes the general form of the dS arithmetic), per-token losses, and accumulation
-into existing gradient buffers.  Sizes span several tiles, ragged tails, and both the one-pair (H <=
+into existing gradient buffers, and the per-row entropy output.  Sizes span several tiles, ragged tails, and both the one-pair (H <=
 256) and the cluster (H = 512, two pairs sharing each logits tile) variants of the gradient passes.
 """
 import numpy as np
@@ -137,3 +137,38 @@ def test_unreduced_empty_batch_leaves_accumulators(flce):
     assert int(res["n_valid"].item()) == 0
     assert torch.all(gw0 == 0.5) and torch.all(gb0 == -0.25)
     assert res["loss"].item() == 0.0
+
+
+@pytest.mark.parametrize("shape", sorted(SHAPES))
+def test_entropy(flce, shape):
+    # per-row entropy of softmax(z); tolerance: H = LSE - sum p z is a difference of two fp32 quantities of
+    # size about LSE, so each row is held to the loss bar relative to max(1, LSE)
+    import torch
+    BT, H, V, bias, zl, ign = SHAPES[shape]
+    d = _inputs(BT, H, V, bias, zl, seed=7 * BT + H, ignore=ign)
+    hidden, W, target, b = _upload(d)
+    out = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction="mean", z_loss=zl, want_entropy=True)
+    torch.cuda.synchronize()
+    assert flce.read_device_status(out["workspace"]) == 0
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], reduction="mean", z_loss=zl)
+    got = out["entropy"].cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref["entropy"])
+    assert np.all(err <= 2e-4 * np.maximum(1.0, ref["lse"])), float(np.max(err))
+    # the other outputs are unchanged by the extra accumulation
+    assert_scalar_close(out["loss"].item(), ref["loss"], "loss")
+    _compare(out, ref)
+
+
+def test_entropy_peaked(flce):
+    # logits with a standard deviation near 5 (hidden scaled): low-entropy rows
+    import torch
+    w = wl.FusedWorkload("peaked", BT=130, H=64, V=700, hidden_std=31.0, w_std=0.02, bias_std=None,
+                         ignore_frac=0.0, z_loss=0.0, reduction="sum", seed=21)
+    d = wl.make_fused_inputs(w)
+    hidden, W, target, b = _upload(d)
+    out = flce.flce_fwd_bwd(hidden, W, target, reduction="sum", want_entropy=True, need_grad_W=False)
+    torch.cuda.synchronize()
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], reduction="sum", want_grads=False)
+    got = out["entropy"].cpu().numpy().astype(np.float64)
+    assert float(np.min(ref["entropy"])) < 1.0
+    assert np.all(np.abs(got - ref["entropy"]) <= 2e-4 * np.maximum(1.0, np.abs(ref["lse"])))
