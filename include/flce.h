@@ -185,6 +185,28 @@ flce_status ce_with_grad(uint16_t* logits, const int64_t* labels, int64_t B, int
                          int64_t ignore_index, float z_loss, float* ce_sum, float* z_sum,
                          int64_t* n_valid, void* workspace, size_t workspace_bytes, void* stream);
 
+/* element types of the standalone CE's logits */
+#define FLCE_DTYPE_BF16 0
+#define FLCE_DTYPE_F16 1
+#define FLCE_DTYPE_F32 2
+
+/*
+ * ce_with_grad for bf16, fp16 or fp32 logits ("Greyhound -- Cross-Entropy", "Shape and dtype
+ * constraints"), with the gradient in place, into a separate buffer (the non-mutating form of the
+ * functional wrapper in "Usage"), or not at all.
+ *
+ *   logits      [B, V] of `dtype`, device, 16-byte aligned.  Read only, unless dlogits == logits.
+ *   dlogits     [B, V] of `dtype`, device, 16-byte aligned: == logits (in place, exactly ce_with_grad for
+ *               bf16), a separate buffer that must not overlap the logits (the logits are left
+ *               unchanged), or NULL (ce_sum, z_sum and n_valid only; no gradient is written).
+ *   dtype       FLCE_DTYPE_BF16, FLCE_DTYPE_F16 or FLCE_DTYPE_F32.
+ * The other arguments, the results and the errors are those of ce_with_grad; the arithmetic is fp32
+ * for every dtype and dlogits is rounded to nearest-even in the logits' type.
+ */
+flce_status ce_with_grad_ex(const void* logits, void* dlogits, int dtype, const int64_t* labels, int64_t B,
+                            int64_t V, int64_t ignore_index, float z_loss, float* ce_sum, float* z_sum,
+                            int64_t* n_valid, void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * ce_with_grad without a workspace, for callers that cannot allocate device memory.
  * (No counterpart on the pages: an addition of this library.)

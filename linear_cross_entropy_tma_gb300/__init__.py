@@ -9,6 +9,7 @@ from ._lib import (  # noqa: F401
     STATUS_TIMEOUT,
     ce_with_grad,
     ce_workspace_size,
+    cross_entropy,
     flce_fwd_bwd,
     load,
     read_device_status,

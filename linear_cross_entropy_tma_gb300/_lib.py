@@ -17,7 +17,7 @@ FLCE_OK = 0
 STATUS_BAD_TARGET = 0x1
 STATUS_TIMEOUT = 0x2
 EXPORTED = ("flce_workspace_size", "flce_fwd_bwd", "flce_fwd_bwd_timed", "flce_fwd_bwd_ex", "ce_workspace_size",
-            "ce_with_grad", "flce_read_device_status", "flce_status_string", "flce_last_error",
+            "ce_with_grad", "ce_with_grad_ex", "flce_read_device_status", "flce_status_string", "flce_last_error",
             "ce_with_grad_noalloc")
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
@@ -56,6 +56,9 @@ def load() -> ctypes.CDLL:
     lib.ce_workspace_size.argtypes = [c_i64, c_i64]
     lib.ce_with_grad.restype = ctypes.c_int
     lib.ce_with_grad.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, ctypes.c_float, c_p, c_p, c_p, c_p, c_sz, c_p]
+    lib.ce_with_grad_ex.restype = ctypes.c_int
+    lib.ce_with_grad_ex.argtypes = [c_p, c_p, ctypes.c_int, c_p, c_i64, c_i64, c_i64, ctypes.c_float, c_p, c_p, c_p,
+                                    c_p, c_sz, c_p]
     lib.ce_with_grad_noalloc.restype = ctypes.c_int
     lib.ce_with_grad_noalloc.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, ctypes.c_float, c_p, c_p, c_p, c_p]
     lib.flce_read_device_status.restype = ctypes.c_int
@@ -179,14 +182,17 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
                 entropy=ent, workspace=workspace)
 
 
-def ce_with_grad(logits, labels, ignore_index: int = -100, z_loss: float = 0.0, workspace=None, out=None,
-                 stream=None) -> dict:
-    """Row-wise CE over bf16 logits [B, V]; overwrites ``logits`` with dlogits in place.
-
-    Returns ``ce_sum`` (fp32 [1]), ``z_sum`` (fp32 [1]) and ``n_valid`` (int64 [1]).
-    """
+def _ce_dtype(t) -> int:
     import torch
-    _bf16_ptr_ok(logits, "logits")
+    codes = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+    if t.dtype not in codes or not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+        raise ValueError("logits must be a contiguous 2-D CUDA bfloat16, float16 or float32 tensor")
+    return codes[t.dtype]
+
+
+def _ce_call(logits, dlogits, labels, ignore_index, z_loss, workspace, out, stream) -> dict:
+    import torch
+    dtype = _ce_dtype(logits)
     B, V = logits.shape
     if labels.shape != (B,) or labels.dtype != torch.int64 or not labels.is_cuda:
         raise ValueError("labels must be a CUDA int64 tensor of shape [B]")
@@ -197,10 +203,43 @@ def ce_with_grad(logits, labels, ignore_index: int = -100, z_loss: float = 0.0, 
             o[k] = torch.empty(1, dtype=dt, device=dev)
     if workspace is None:
         workspace = torch.empty(ce_workspace_size(B, V), dtype=torch.uint8, device=dev)
-    check(load().ce_with_grad(_ptr(logits), _ptr(labels), B, V, ignore_index, float(z_loss), _ptr(o["ce_sum"]),
-                              _ptr(o["z_sum"]), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel(),
-                              _stream_ptr(stream)))
+    if dtype == 0 and dlogits is not None and dlogits.data_ptr() == logits.data_ptr():
+        check(load().ce_with_grad(_ptr(logits), _ptr(labels), B, V, ignore_index, float(z_loss), _ptr(o["ce_sum"]),
+                                  _ptr(o["z_sum"]), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel(),
+                                  _stream_ptr(stream)))
+    else:
+        check(load().ce_with_grad_ex(_ptr(logits), _ptr(dlogits), dtype, _ptr(labels), B, V, ignore_index,
+                                     float(z_loss), _ptr(o["ce_sum"]), _ptr(o["z_sum"]), _ptr(o["n_valid"]),
+                                     _ptr(workspace), workspace.numel(), _stream_ptr(stream)))
     return dict(ce_sum=o["ce_sum"], z_sum=o["z_sum"], n_valid=o["n_valid"], workspace=workspace)
+
+
+def ce_with_grad(logits, labels, ignore_index: int = -100, z_loss: float = 0.0, workspace=None, out=None,
+                 stream=None) -> dict:
+    """Row-wise CE over logits [B, V] (bf16, fp16 or fp32); overwrites ``logits`` with dlogits in place.
+
+    Returns ``ce_sum`` (fp32 [1]), ``z_sum`` (fp32 [1]) and ``n_valid`` (int64 [1]).
+    """
+    return _ce_call(logits, logits, labels, ignore_index, z_loss, workspace, out, stream)
+
+
+def cross_entropy(logits, labels, ignore_index: int = -100, z_loss: float = 0.0, want_grad: bool = True,
+                  workspace=None, out=None, stream=None) -> dict:
+    """Non-mutating form of ce_with_grad: the logits are left unchanged and dlogits (same dtype and shape)
+    is returned as a new tensor (or written into ``out["dlogits"]``), or not computed at all when
+    ``want_grad`` is False.  Returns ``ce_sum``, ``z_sum``, ``n_valid`` and ``dlogits`` (or None)."""
+    import torch
+    o = dict(out or {})
+    dl = None
+    if want_grad:
+        dl = o.get("dlogits")
+        if dl is None:
+            dl = torch.empty_like(logits)
+        elif dl.dtype != logits.dtype or dl.shape != logits.shape or not dl.is_contiguous():
+            raise ValueError("out['dlogits'] must match the logits' dtype and shape")
+    r = _ce_call(logits, dl, labels, ignore_index, z_loss, workspace, o, stream)
+    r["dlogits"] = dl
+    return r
 
 
 def read_device_status(workspace, stream=None) -> int:

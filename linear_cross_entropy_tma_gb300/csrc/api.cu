@@ -224,12 +224,16 @@ size_t ce_workspace_size(int64_t B, int64_t V) {
   return flce::ce_workspace_bytes(B);
 }
 
-flce_status ce_with_grad(uint16_t* logits, const int64_t* labels, int64_t B, int64_t V, int64_t ignore_index,
-                         float z_loss, float* ce_sum, float* z_sum, int64_t* n_valid, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+static flce_status ce_impl(const void* logits, void* dlogits, int dtype, const int64_t* labels, int64_t B, int64_t V,
+                           int64_t ignore_index, float z_loss, float* ce_sum, float* z_sum, int64_t* n_valid,
+                           void* workspace, size_t workspace_bytes, void* stream, const char* name) {
   g_last_error[0] = '\0';
   if (B < 0 || V <= 0) {
     set_error("sizes must satisfy B >= 0, V > 0 (got %lld, %lld)", (long long)B, (long long)V);
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_F16 && dtype != FLCE_DTYPE_F32) {
+    set_error("dtype must be FLCE_DTYPE_BF16, FLCE_DTYPE_F16 or FLCE_DTYPE_F32, got %d", dtype);
     return FLCE_ERR_INVALID_ARG;
   }
   if (ce_sum == nullptr || z_sum == nullptr || n_valid == nullptr || workspace == nullptr ||
@@ -241,9 +245,18 @@ flce_status ce_with_grad(uint16_t* logits, const int64_t* labels, int64_t B, int
     set_error("unsupported sizes: B and V must be below 2^31");
     return FLCE_ERR_UNSUPPORTED;
   }
-  if (!aligned(logits, 16) || !aligned(workspace, 256) || !aligned(labels, 8) || !aligned(ce_sum, 4) ||
-      !aligned(z_sum, 4) || !aligned(n_valid, 8)) {
-    set_error("misaligned pointer (logits need 16 bytes, workspace 256)");
+  const size_t elem = dtype == FLCE_DTYPE_F32 ? 4u : 2u;
+  if (dlogits != nullptr && dlogits != logits) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(logits), b = reinterpret_cast<uintptr_t>(dlogits);
+    const uintptr_t n = static_cast<uintptr_t>(B) * static_cast<uintptr_t>(V) * elem;
+    if (a < b + n && b < a + n) {
+      set_error("a separate dlogits buffer must not overlap the logits");
+      return FLCE_ERR_INVALID_ARG;
+    }
+  }
+  if (!aligned(logits, 16) || !aligned(dlogits, 16) || !aligned(workspace, 256) || !aligned(labels, 8) ||
+      !aligned(ce_sum, 4) || !aligned(z_sum, 4) || !aligned(n_valid, 8)) {
+    set_error("misaligned pointer (logits and dlogits need 16 bytes, workspace 256)");
     return FLCE_ERR_MISALIGNED;
   }
   const size_t need = ce_workspace_size(B, V);
@@ -254,9 +267,23 @@ flce_status ce_with_grad(uint16_t* logits, const int64_t* labels, int64_t B, int
   int num_sms = 0;
   const flce_status ds = check_device(&num_sms);
   if (ds != FLCE_OK) return ds;
-  return from_cuda(flce::launch_ce_rows(logits, labels, B, V, ignore_index, z_loss, ce_sum, z_sum, n_valid, workspace,
-                                        num_sms, static_cast<cudaStream_t>(stream)),
-                   "ce_with_grad launch");
+  return from_cuda(flce::launch_ce_rows(logits, dlogits, dtype, labels, B, V, ignore_index, z_loss, ce_sum, z_sum,
+                                        n_valid, workspace, num_sms, static_cast<cudaStream_t>(stream)),
+                   name);
+}
+
+flce_status ce_with_grad(uint16_t* logits, const int64_t* labels, int64_t B, int64_t V, int64_t ignore_index,
+                         float z_loss, float* ce_sum, float* z_sum, int64_t* n_valid, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return ce_impl(logits, logits, FLCE_DTYPE_BF16, labels, B, V, ignore_index, z_loss, ce_sum, z_sum, n_valid,
+                 workspace, workspace_bytes, stream, "ce_with_grad launch");
+}
+
+flce_status ce_with_grad_ex(const void* logits, void* dlogits, int dtype, const int64_t* labels, int64_t B, int64_t V,
+                            int64_t ignore_index, float z_loss, float* ce_sum, float* z_sum, int64_t* n_valid,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return ce_impl(logits, dlogits, dtype, labels, B, V, ignore_index, z_loss, ce_sum, z_sum, n_valid, workspace,
+                 workspace_bytes, stream, "ce_with_grad_ex launch");
 }
 
 flce_status flce_read_device_status(const void* workspace, uint32_t* host_status, void* stream) {

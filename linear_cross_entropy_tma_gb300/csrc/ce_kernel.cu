@@ -1,17 +1,20 @@
-// ce_kernel.cu -- standalone row-wise cross-entropy over materialised bf16 logits, with the logits
-// gradient written back in place ("Greyhound -- Cross-Entropy", "Kernel design": one block per row,
-// fp32 online max/sum across the row, warp reductions to the row LSE, a second pass that overwrites
-// the logits with dlogits; z-loss scales the softmax term before the target column is adjusted).
+// ce_kernel.cu -- standalone row-wise cross-entropy over materialised logits (bf16, fp16 or fp32), with
+// the logits gradient written in place or to a separate buffer ("Greyhound -- Cross-Entropy", "Kernel
+// design": one block per row, fp32 online max/sum across the row, warp reductions to the row LSE, a
+// second pass that overwrites the logits with dlogits; z-loss scales the softmax term before the
+// target column is adjusted; "Shape and dtype constraints": bf16, fp16 or fp32 logits).
 //
-// GB300 shape of it: a persistent grid of two 512-thread CTAs per SM walks the rows.  The first 96 KiB
+// GB300 shape of it: a persistent grid of two 512-thread CTAs per SM walks the rows.  The first 80 KiB
 // of each row (its "head") is fetched into shared memory by one bulk copy, issued as soon as the
 // previous row no longer needs the buffer; pass 1 streams the rest of the row with 16-byte loads
 // tagged to stay in L2 while the head lands, then reads the head from shared memory; pass 2 writes
-// the head's dlogits from shared memory and re-reads the rest (an L2 hit: about 2 x 152 x 154 KB
-// = 47 MB of rows are in flight), storing with 16-byte stores tagged evict-first.  HBM therefore
-// sees one read and one write of the logits.
+// the head's dlogits from shared memory and re-reads the rest (an L2 hit: about 2 x 152 x 170 KB
+// = 52 MB of rows are in flight at bf16), storing with 16-byte stores tagged evict-first.  HBM
+// therefore sees one read and one write of the logits.  Without a gradient buffer pass 2 is skipped.
 // Per-row (ce, LSE^2, valid) land in the workspace; the last CTA to finish sums them in a fixed
 // order (float64), so the three outputs are deterministic.
+#include <cuda_fp16.h>
+
 #include "ce_kernel.cuh"
 #include "sm100.cuh"
 
@@ -60,58 +63,114 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2)
   s = a + b;
 }
 
-__device__ __forceinline__ void accumulate8(const uint4 v, float& m, float& s) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float x[8];
+// Element types of the logits: raw storage, elements per 16-byte vector, and conversions.
+struct Bf16Elem {
+  using raw = uint16_t;
+  static constexpr int kPer = 8;
+  __device__ static float load1(raw r) { return __uint_as_float(static_cast<uint32_t>(r) << 16); }
+  __device__ static raw store1(float f) { return static_cast<uint16_t>(pack_bf16x2(f, 0.0f) & 0xFFFFu); }
+  __device__ static void unpack(const uint4 v, float (&x)[kPer]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = bf16_lo(w[i]);
-    x[2 * i + 1] = bf16_hi(w[i]);
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16_lo(w[i]);
+      x[2 * i + 1] = bf16_hi(w[i]);
+    }
   }
+  __device__ static uint4 pack(const float (&g)[kPer]) {
+    return make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]),
+                      pack_bf16x2(g[6], g[7]));
+  }
+};
+
+struct F16Elem {
+  using raw = uint16_t;
+  static constexpr int kPer = 8;
+  __device__ static float load1(raw r) { return __half2float(__ushort_as_half(r)); }
+  __device__ static raw store1(float f) { return __half_as_ushort(__float2half_rn(f)); }
+  __device__ static void unpack(const uint4 v, float (&x)[kPer]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  }
+  __device__ static uint4 pack(const float (&g)[kPer]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(g[2 * i], g[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+struct F32Elem {
+  using raw = float;
+  static constexpr int kPer = 4;
+  __device__ static float load1(raw r) { return r; }
+  __device__ static raw store1(float f) { return f; }
+  __device__ static void unpack(const uint4 v, float (&x)[kPer]) {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+  }
+  __device__ static uint4 pack(const float (&g)[kPer]) {
+    return make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]), __float_as_uint(g[2]), __float_as_uint(g[3]));
+  }
+};
+
+template <class E>
+__device__ __forceinline__ void accumulate_vec(const uint4 v, float& m, float& s) {
+  float x[E::kPer];
+  E::unpack(v, x);
   float cm = x[0];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) cm = fmaxf(cm, x[i]);
+  for (int i = 1; i < E::kPer; ++i) cm = fmaxf(cm, x[i]);
   const float mn = fmaxf(m, cm * kLog2e);
   float acc = s * ex2_approx(m - mn);  // m = -inf on the first call gives 0 * 0
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc += ex2_approx(fmaf(x[i], kLog2e, -mn));
+  for (int i = 0; i < E::kPer; ++i) acc += ex2_approx(fmaf(x[i], kLog2e, -mn));
   m = mn;
   s = acc;
 }
 
-// dlogits of 8 consecutive columns starting at column c0 (softmax * zf - onehot).
-__device__ __forceinline__ uint4 grad8(const uint4 v, int64_t c0, int64_t y, float lse2, float zf) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float g[8];
+// dlogits of one 16-byte vector of consecutive columns starting at column c0 (softmax * zf - onehot).
+template <class E>
+__device__ __forceinline__ uint4 grad_vec(const uint4 v, int64_t c0, int64_t y, float lse2, float zf) {
+  float g[E::kPer];
+  E::unpack(v, g);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    g[2 * i] = ex2_approx(fmaf(bf16_lo(w[i]), kLog2e, -lse2)) * zf;
-    g[2 * i + 1] = ex2_approx(fmaf(bf16_hi(w[i]), kLog2e, -lse2)) * zf;
-  }
+  for (int i = 0; i < E::kPer; ++i) g[i] = ex2_approx(fmaf(g[i], kLog2e, -lse2)) * zf;
   const uint64_t t = static_cast<uint64_t>(y - c0);  // target column relative to c0
-  if (t < 8u) {
+  if (t < static_cast<uint64_t>(E::kPer)) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < E::kPer; ++i)
       if (static_cast<uint64_t>(i) == t) g[i] -= 1.0f;
   }
-  return make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]),
-                    pack_bf16x2(g[6], g[7]));
+  return E::pack(g);
 }
 
-__device__ __forceinline__ float grad1(uint16_t raw, int64_t c, int64_t y, float lse2, float zf) {
-  float g = ex2_approx(fmaf(__uint_as_float(static_cast<uint32_t>(raw) << 16), kLog2e, -lse2)) * zf;
+template <class E>
+__device__ __forceinline__ float grad1(typename E::raw raw, int64_t c, int64_t y, float lse2, float zf) {
+  const float g = ex2_approx(fmaf(E::load1(raw), kLog2e, -lse2)) * zf;
   return (c == y) ? g - 1.0f : g;
 }
 
-__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
-  return static_cast<uint16_t>(pack_bf16x2(f, 0.0f) & 0xFFFFu);
-}
-
+// in: logits [B, V]; out: dlogits [B, V] (== in for the in-place call, NULL for no gradient).
+template <class E>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels, int64_t B, int64_t V,
-               int64_t ignore_index, float z_loss, float4* __restrict__ row_out, uint32_t* __restrict__ status,
-               uint32_t* __restrict__ done_counter, float* __restrict__ ce_sum, float* __restrict__ z_sum,
-               int64_t* __restrict__ n_valid) {
+ce_rows_kernel(const typename E::raw* in, typename E::raw* out, const int64_t* __restrict__ labels, int64_t B,
+               int64_t V, int64_t ignore_index, float z_loss, float4* __restrict__ row_out,
+               uint32_t* __restrict__ status, uint32_t* __restrict__ done_counter, float* __restrict__ ce_sum,
+               float* __restrict__ z_sum, int64_t* __restrict__ n_valid) {
+  using raw = typename E::raw;
+  constexpr int kPer = E::kPer;
+  constexpr int kShift = sizeof(raw) == 2 ? 1 : 2;
   extern __shared__ uint4 s_cache[];  // kCacheVec vectors of the current row
   __shared__ uint64_t s_head_bar;
   __shared__ float s_m[kWarps], s_s[kWarps];
@@ -123,6 +182,7 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  const bool want_grad = (out != nullptr);
   const uint64_t keep = policy_evict_last();
   const uint64_t drop = policy_evict_first();
 
@@ -130,13 +190,22 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
   auto head_bytes = [&](int64_t r, const uint4*& src) -> uint32_t {
     const int64_t y = labels[r];
     if (!((y != ignore_index) && (y >= 0) && (y < V))) return 0u;
-    const uint16_t* rw = logits + r * V;
+    const raw* rw = in + r * V;
     const uintptr_t a = reinterpret_cast<uintptr_t>(rw);
-    const int64_t hd_raw = static_cast<int64_t>(((16u - (a & 15u)) & 15u) >> 1);
+    const int64_t hd_raw = static_cast<int64_t>(((16u - (a & 15u)) & 15u) >> kShift);
     const int64_t hd = hd_raw < V ? hd_raw : V;
-    const int64_t nv = (V - hd) >> 3;
+    const int64_t nv = (V - hd) / kPer;
     src = reinterpret_cast<const uint4*>(rw + hd);
     return static_cast<uint32_t>((nv < kCacheVec ? nv : kCacheVec) * 16);
+  };
+  auto prefetch_head = [&](int64_t r) {
+    const uint4* src = nullptr;
+    const uint32_t bytes = head_bytes(r, src);
+    if (bytes) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&s_head_bar, bytes);
+      bulk_load_1d_hint(s_cache, src, bytes, &s_head_bar, keep);
+    }
   };
   if (tid == 0) {
     mbar_init(&s_head_bar, 1);
@@ -145,60 +214,44 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
   __syncthreads();
   uint32_t head_phase = 0;
   volatile int no_abort = 0;
-  if (tid == 0 && blockIdx.x < B) {
-    const uint4* src = nullptr;
-    const uint32_t bytes = head_bytes(blockIdx.x, src);
-    if (bytes) {
-      mbar_arrive_expect_tx(&s_head_bar, bytes);
-      bulk_load_1d_hint(s_cache, src, bytes, &s_head_bar, keep);
-    }
-  }
+  if (tid == 0 && blockIdx.x < B) prefetch_head(blockIdx.x);
 
   for (int64_t r = blockIdx.x; r < B; r += gridDim.x) {
     const int64_t y = labels[r];
     const bool valid = (y != ignore_index) && (y >= 0) && (y < V);
-    uint16_t* row = logits + r * V;
-    // 16-byte aligned middle part of the row; scalar head and tail around it
+    const raw* row = in + r * V;
+    raw* orow = want_grad ? out + r * V : nullptr;
+    // 16-byte aligned middle part of the row; scalar head and tail around it (in and out rows have
+    // the same alignment: both buffers start on a 16-byte boundary)
     const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
-    const int64_t head_raw = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) >> 1);
+    const int64_t head_raw = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) >> kShift);
     const int64_t head = head_raw < V ? head_raw : V;
-    const int64_t nvec = (V - head) >> 3;
-    const int64_t tail0 = head + nvec * 8;
-    uint4* vrow = reinterpret_cast<uint4*>(row + head);
+    const int64_t nvec = (V - head) / kPer;
+    const int64_t tail0 = head + nvec * kPer;
+    const uint4* vrow = reinterpret_cast<const uint4*>(row + head);
+    uint4* ovrow = want_grad ? reinterpret_cast<uint4*>(orow + head) : nullptr;
 
     if (!valid) {
       if (tid == 0) {
         if (y != ignore_index) atomicOr(status, kStatusBadTarget);
         row_out[r] = make_float4(0.f, 0.f, 0.f, 0.f);
         // no head was fetched for this row; fetch the next row's head now
-        if (r + gridDim.x < B) {
-          const uint4* src = nullptr;
-          const uint32_t bytes = head_bytes(r + gridDim.x, src);
-          if (bytes) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&s_head_bar, bytes);
-            bulk_load_1d_hint(s_cache, src, bytes, &s_head_bar, keep);
-          }
-        }
+        if (r + gridDim.x < B) prefetch_head(r + gridDim.x);
       }
-      for (int64_t i = tid; i < nvec; i += kThreads) st16_hint(vrow + i, make_uint4(0, 0, 0, 0), drop);
-      for (int64_t c = tid; c < head; c += kThreads) row[c] = 0;
-      for (int64_t c = tail0 + tid; c < V; c += kThreads) row[c] = 0;
+      if (want_grad) {
+        for (int64_t i = tid; i < nvec; i += kThreads) st16_hint(ovrow + i, make_uint4(0, 0, 0, 0), drop);
+        for (int64_t c = tid; c < head; c += kThreads) orow[c] = E::store1(0.f);
+        for (int64_t c = tail0 + tid; c < V; c += kThreads) orow[c] = E::store1(0.f);
+      }
       continue;
     }
 
-    if (tid == 0) s_zy = __uint_as_float(static_cast<uint32_t>(row[y]) << 16);
+    if (tid == 0) s_zy = E::load1(row[y]);
 
     // ---- pass 1: online (max, sum) in the log2 domain
     float m = -INFINITY, s = 0.f;
-    for (int64_t c = tid; c < head; c += kThreads) {
-      const float x = __uint_as_float(static_cast<uint32_t>(row[c]) << 16) * kLog2e;
-      merge_ms(m, s, x, 1.0f);
-    }
-    for (int64_t c = tail0 + tid; c < V; c += kThreads) {
-      const float x = __uint_as_float(static_cast<uint32_t>(row[c]) << 16) * kLog2e;
-      merge_ms(m, s, x, 1.0f);
-    }
+    for (int64_t c = tid; c < head; c += kThreads) merge_ms(m, s, E::load1(row[c]) * kLog2e, 1.0f);
+    for (int64_t c = tail0 + tid; c < V; c += kThreads) merge_ms(m, s, E::load1(row[c]) * kLog2e, 1.0f);
     const int64_t ncache = nvec < kCacheVec ? nvec : kCacheVec;
     // the tail (vectors ncache..nvec-1) from global memory while the head's bulk copy lands
     int64_t i = ncache + tid;
@@ -207,14 +260,14 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) v[u] = ld16_hint(vrow + i + u * kThreads, keep);
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) accumulate8(v[u], m, s);
+      for (int u = 0; u < kUnroll; ++u) accumulate_vec<E>(v[u], m, s);
     }
-    for (; i < nvec; i += kThreads) accumulate8(ld16_hint(vrow + i, keep), m, s);
+    for (; i < nvec; i += kThreads) accumulate_vec<E>(ld16_hint(vrow + i, keep), m, s);
     // the head from shared memory
     if (ncache > 0) {
       if (!mbar_wait(&s_head_bar, head_phase, &no_abort) && (tid & 31) == 0) atomicOr(status, kStatusTimeout);
       head_phase ^= 1u;
-      for (int64_t k = tid; k < ncache; k += kThreads) accumulate8(s_cache[k], m, s);
+      for (int64_t k = tid; k < ncache; k += kThreads) accumulate_vec<E>(s_cache[k], m, s);
     }
 
 #pragma unroll
@@ -242,28 +295,23 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
         s_lse2 = lse2;
         const float lse = lse2 * kLn2;
         row_out[r] = make_float4(lse - s_zy, lse * lse, 1.f, 0.f);
+        // without a gradient the cache is free as soon as every thread has read it (the barrier above)
+        if (!want_grad && r + gridDim.x < B) prefetch_head(r + gridDim.x);
       }
     }
     __syncthreads();
+    if (!want_grad) continue;
     const float lse2 = s_lse2;
     const float zf = 1.0f + 2.0f * z_loss * (lse2 * kLn2);
 
-    // ---- pass 2: overwrite with dlogits
-    for (int64_t c = tid; c < head; c += kThreads) row[c] = f32_to_bf16_bits(grad1(row[c], c, y, lse2, zf));
-    for (int64_t c = tail0 + tid; c < V; c += kThreads) row[c] = f32_to_bf16_bits(grad1(row[c], c, y, lse2, zf));
+    // ---- pass 2: dlogits
+    for (int64_t c = tid; c < head; c += kThreads) orow[c] = E::store1(grad1<E>(row[c], c, y, lse2, zf));
+    for (int64_t c = tail0 + tid; c < V; c += kThreads) orow[c] = E::store1(grad1<E>(row[c], c, y, lse2, zf));
     for (int64_t k = tid; k < ncache; k += kThreads)
-      st16_hint(vrow + k, grad8(s_cache[k], head + k * 8, y, lse2, zf), drop);
+      st16_hint(ovrow + k, grad_vec<E>(s_cache[k], head + k * kPer, y, lse2, zf), drop);
     // every thread is done reading the cache: start copying the head of this CTA's next row
     __syncthreads();
-    if (tid == 0 && r + gridDim.x < B) {
-      const uint4* src = nullptr;
-      const uint32_t bytes = head_bytes(r + gridDim.x, src);
-      if (bytes) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&s_head_bar, bytes);
-        bulk_load_1d_hint(s_cache, src, bytes, &s_head_bar, keep);
-      }
-    }
+    if (tid == 0 && r + gridDim.x < B) prefetch_head(r + gridDim.x);
     i = ncache + tid;
     for (; i + (kUnroll - 1) * kThreads < nvec; i += kUnroll * kThreads) {
       uint4 v[kUnroll];
@@ -271,9 +319,10 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
       for (int u = 0; u < kUnroll; ++u) v[u] = ld16_hint(vrow + i + u * kThreads, drop);
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u)
-        st16_hint(vrow + i + u * kThreads, grad8(v[u], head + (i + u * kThreads) * 8, y, lse2, zf), drop);
+        st16_hint(ovrow + i + u * kThreads, grad_vec<E>(v[u], head + (i + u * kThreads) * kPer, y, lse2, zf), drop);
     }
-    for (; i < nvec; i += kThreads) st16_hint(vrow + i, grad8(ld16_hint(vrow + i, drop), head + i * 8, y, lse2, zf), drop);
+    for (; i < nvec; i += kThreads)
+      st16_hint(ovrow + i, grad_vec<E>(ld16_hint(vrow + i, drop), head + i * kPer, y, lse2, zf), drop);
     __syncthreads();  // s_m / s_s / s_lse2 / s_zy are reused by the next row
   }
 
@@ -319,11 +368,28 @@ ce_rows_kernel(uint16_t* __restrict__ logits, const int64_t* __restrict__ labels
   }
 }
 
+
+template <class E>
+cudaError_t launch_ce_rows_t(const void* logits, void* dlogits, const int64_t* labels, int64_t B, int64_t V,
+                             int64_t ignore_index, float z_loss, float4* row_out, uint32_t* status, uint32_t* counter,
+                             float* ce_sum, float* z_sum, int64_t* n_valid, int num_sms, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(ce_rows_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kCacheBytes));
+  if (e != cudaSuccess) return e;
+  const int64_t cap = static_cast<int64_t>(num_sms) * kCtasPerSm;
+  const int64_t grid = B < cap ? B : cap;
+  using raw = typename E::raw;
+  ce_rows_kernel<E><<<static_cast<unsigned>(grid), kThreads, kCacheBytes, stream>>>(
+      static_cast<const raw*>(logits), static_cast<raw*>(dlogits), labels, B, V, ignore_index, z_loss, row_out, status,
+      counter, ce_sum, z_sum, n_valid);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_ce_rows(uint16_t* logits, const int64_t* labels, int64_t B, int64_t V, int64_t ignore_index,
-                           float z_loss, float* ce_sum, float* z_sum, int64_t* n_valid, void* workspace,
-                           int num_sms, cudaStream_t stream) {
+cudaError_t launch_ce_rows(const void* logits, void* dlogits, int dtype, const int64_t* labels, int64_t B, int64_t V,
+                           int64_t ignore_index, float z_loss, float* ce_sum, float* z_sum, int64_t* n_valid,
+                           void* workspace, int num_sms, cudaStream_t stream) {
   auto* ws = static_cast<unsigned char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   uint32_t* counter = reinterpret_cast<uint32_t*>(ws + 4);
@@ -335,14 +401,19 @@ cudaError_t launch_ce_rows(uint16_t* logits, const int64_t* labels, int64_t B, i
     if ((e = cudaMemsetAsync(z_sum, 0, sizeof(float), stream)) != cudaSuccess) return e;
     return cudaMemsetAsync(n_valid, 0, sizeof(int64_t), stream);
   }
-  e = cudaFuncSetAttribute(ce_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kCacheBytes));
-  if (e != cudaSuccess) return e;
-  const int64_t cap = static_cast<int64_t>(num_sms) * kCtasPerSm;
-  const int64_t grid = B < cap ? B : cap;
-  ce_rows_kernel<<<static_cast<unsigned>(grid), kThreads, kCacheBytes, stream>>>(
-      logits, labels, B, V, ignore_index, z_loss, row_out, status, counter, ce_sum, z_sum, n_valid);
-  return cudaGetLastError();
+  switch (dtype) {
+    case kCeBf16:
+      return launch_ce_rows_t<Bf16Elem>(logits, dlogits, labels, B, V, ignore_index, z_loss, row_out, status, counter,
+                                        ce_sum, z_sum, n_valid, num_sms, stream);
+    case kCeF16:
+      return launch_ce_rows_t<F16Elem>(logits, dlogits, labels, B, V, ignore_index, z_loss, row_out, status, counter,
+                                       ce_sum, z_sum, n_valid, num_sms, stream);
+    case kCeF32:
+      return launch_ce_rows_t<F32Elem>(logits, dlogits, labels, B, V, ignore_index, z_loss, row_out, status, counter,
+                                       ce_sum, z_sum, n_valid, num_sms, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace flce

@@ -90,8 +90,8 @@ flce_status ce_with_grad_noalloc(uint16_t* logits, const int64_t* labels, int64_
     flce::set_last_error_message(msg);
     return FLCE_ERR_CUDA;
   }
-  e = flce::launch_ce_rows(logits, labels, B, V, ignore_index, z_loss, ce_sum, z_sum, n_valid, scratch, num_sms,
-                           static_cast<cudaStream_t>(stream));
+  e = flce::launch_ce_rows(logits, logits, flce::kCeBf16, labels, B, V, ignore_index, z_loss, ce_sum, z_sum, n_valid,
+                           scratch, num_sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     snprintf(msg, sizeof(msg), "ce_with_grad_noalloc launch: %s", cudaGetErrorString(e));
     flce::set_last_error_message(msg);

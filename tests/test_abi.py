@@ -113,6 +113,24 @@ def test_ce_argument_errors(lib):
     assert lib.flce_read_device_status(None, None, None) == INVALID_ARG
 
 
+def test_ce_ex_argument_errors(lib):
+    def ce(logits=0x10000, dl=0x10000, dtype=1, B=8, V=16, ws=0x40000):
+        return lib.ce_with_grad_ex(logits, dl, dtype, 0x2000, B, V, -100, 0.0, 0x3000, 0x3100, 0x3200, ws, 1 << 20,
+                                   None)
+
+    assert ce(dtype=3) == INVALID_ARG
+    assert ce(dtype=-1) == INVALID_ARG
+    assert ce(dl=0x10010) == INVALID_ARG          # separate buffer overlapping the logits (8 x 16 x 2 bytes)
+    assert ce(dl=0x10000 + 8 * 16 * 2 + 8) == MISALIGNED
+    assert ce(logits=0x10008, dl=None) == MISALIGNED
+    # in place, out of place right after the logits, and no gradient reach the device check
+    assert ce() == NO_DEVICE
+    assert ce(dl=0x10000 + 8 * 16 * 2) == NO_DEVICE
+    assert ce(dl=None, dtype=2) == NO_DEVICE
+    assert ce(dl=0x10000 + 8 * 16 * 4, dtype=2) == NO_DEVICE
+    assert ce(dl=0x10000 + 8 * 16 * 2, dtype=2) == INVALID_ARG   # overlaps at 4 bytes per element
+
+
 def test_status_strings(lib):
     assert lib.flce_status_string(0) == b"FLCE_OK"
     assert lib.flce_status_string(3) == b"FLCE_ERR_WORKSPACE_TOO_SMALL"

@@ -107,3 +107,53 @@ def test_ce_full_size(flce):
     del logits
     out2, logits2, _ = _run(flce, d["logits"], d["labels"], w.z_loss)
     assert (out2["ce_sum"].item(), out2["z_sum"].item()) == first, "reduction is not deterministic"
+
+
+@pytest.mark.parametrize("dtype", ["float16", "float32", "bfloat16"])
+@pytest.mark.parametrize("mode", ["inplace", "separate", "nograd"])
+@pytest.mark.parametrize("B,V,z_loss,ignore", [(300, 4101, 1e-4, (7, 299)), (37, 1003, 0.0, (0,)), (4, 130001, 1e-3, (1,))])
+def test_ce_dtypes_and_modes(flce, dtype, mode, B, V, z_loss, ignore):
+    import torch
+    tdt = getattr(torch, dtype)
+    rng = np.random.default_rng(B * 7 + V)
+    x32 = (rng.standard_normal((B, V)) * 2.0).astype(np.float32)
+    lab = rng.integers(0, V, B).astype(np.int64)
+    for r in ignore:
+        lab[r] = -100
+    logits = torch.from_numpy(x32).to(tdt).cuda()
+    xin = logits.float().cpu().numpy().astype(np.float64)    # the exact values the kernel reads
+    orig = logits.clone()
+    labels = torch.from_numpy(lab).cuda()
+    if mode == "inplace":
+        r = flce.ce_with_grad(logits, labels, z_loss=z_loss)
+        dl = logits
+    else:
+        r = flce.cross_entropy(logits, labels, z_loss=z_loss, want_grad=(mode == "separate"))
+        dl = r["dlogits"]
+    torch.cuda.synchronize()
+    assert flce.read_device_status(r["workspace"]) == 0
+    ref = oracle.ce_reference(xin, lab, z_loss=z_loss)
+    assert int(r["n_valid"].item()) == ref["n_valid"]
+    assert_scalar_close(r["ce_sum"].item(), ref["ce_sum"], "ce_sum")
+    assert_scalar_close(r["z_sum"].item(), ref["z_sum"], "z_sum")
+    if mode != "inplace":
+        assert torch.equal(logits, orig), "the logits must be left unchanged"
+    if mode == "nograd":
+        assert dl is None
+        return
+    assert dl.dtype == tdt
+    assert_grad_close(dl.float().cpu().numpy(), ref["dlogits"], "dlogits")
+
+
+def test_ce_separate_equals_inplace_bitwise(flce):
+    # the non-mutating form runs the same arithmetic: its dlogits must equal the in-place result bit for bit
+    import torch
+    x, lab = _case(96, 5003, ignore=(3,), seed=11)
+    a = bf16_tensor(x)
+    labels = torch.from_numpy(lab).cuda()
+    r = flce.cross_entropy(a, labels, z_loss=1e-4)
+    b = bf16_tensor(x)
+    flce.ce_with_grad(b, labels, z_loss=1e-4)
+    torch.cuda.synchronize()
+    assert torch.equal(r["dlogits"].view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), bf16_tensor(x).view(torch.int16))
