@@ -49,7 +49,7 @@ import math
 import numpy as np
 
 __all__ = [
-    "widen", "logits", "lse", "flce_reference", "flce_lse", "flce_sampled", "flce_reference_loops",
+    "widen", "logits", "lse", "flce_reference", "flce_dlogits", "flce_lse", "flce_sampled", "flce_reference_loops",
     "ce_reference", "ce_reference_loops",
 ]
 
@@ -154,6 +154,25 @@ def flce_reference(hidden, W, target, bias=None, ignore_index: int = -100, reduc
     if want_grads:
         out.update(grad_input=grad_input, grad_W=grad_W, grad_bias=grad_b)
     return out
+
+
+def flce_dlogits(hidden, W, target, bias=None, ignore_index: int = -100, reduction: str = "mean",
+                 z_loss: float = 0.0) -> np.ndarray:
+    """The full [BT, V] dlogits matrix of the fused loss (small cases only): s [y_t valid]
+    (softmax(z_t) (1 + 2 z_loss LSE_t) - onehot(y_t)), p1 "From dlogits to grad_input and grad_W"."""
+    z = logits(hidden, W, bias)
+    t = np.asarray(target, dtype=np.int64)
+    V = z.shape[1]
+    valid = _valid_mask(t, V, ignore_index)
+    s = _scale(int(valid.sum()), reduction)
+    m = z.max(axis=1)
+    e = np.exp(z - m[:, None])
+    tot = e.sum(axis=1)
+    lse_rows = m + np.log(tot)
+    d = e / tot[:, None] * (1.0 + 2.0 * z_loss * lse_rows)[:, None]
+    rows = np.nonzero(valid)[0]
+    d[rows, t[rows]] -= 1.0
+    return d * (s * valid)[:, None]
 
 
 def flce_lse(hidden, W, bias=None, row_block: int = 512) -> np.ndarray:

@@ -306,8 +306,27 @@ def pin_entropy(orc):
     assert np.all(got["entropy"] >= 0) and np.all(got["entropy"] <= math.log(W.shape[0]) + 1e-12)
 
 
+def pin_dlogits_matrix(orc):
+    # the dlogits matrix against torch autograd of the logits, and against the oracle's own GEMMs
+    hidden, W, b, t = _tiny_case(seed=29, BT=15, H=7, V=19, ignore_rows=(2, 11))
+    for reduction, zl in (("mean", 1e-2), ("sum", 0.0)):
+        d = orc.flce_dlogits(hidden, W, t, bias=b, reduction=reduction, z_loss=zl)
+        z = torch.tensor(hidden @ W.T + b, requires_grad=True)
+        tt = torch.tensor(t)
+        valid = (tt != -100).double()
+        scale = 1.0 / valid.sum() if reduction == "mean" else 1.0
+        loss = torch.nn.functional.cross_entropy(z, tt, ignore_index=-100, reduction=reduction) + \
+            zl * scale * (torch.logsumexp(z, dim=1) ** 2 * valid).sum()
+        loss.backward()
+        assert _rel(d, z.grad.numpy()) < 1e-12
+        g = orc.flce_reference(hidden, W, t, bias=b, reduction=reduction, z_loss=zl, row_block=4)
+        assert _rel(d @ W, g["grad_input"]) < 1e-12
+        assert _rel(d.T @ hidden, g["grad_W"]) < 1e-12
+
+
 PINS = [pin_loops_vs_vectorised, pin_finite_differences, pin_torch_fp64, pin_closed_forms,
-        pin_invariants, pin_ce, pin_sampled_matches_full, pin_unreduced_and_upstream, pin_entropy]
+        pin_invariants, pin_ce, pin_sampled_matches_full, pin_unreduced_and_upstream, pin_entropy,
+        pin_dlogits_matrix]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -332,6 +351,7 @@ MUTATIONS = {
     "grad_scale applied twice": ("d *= (grad_scale * u[r0:r1])[:, None]", "d *= (grad_scale * grad_scale * u[r0:r1])[:, None]"),
     "entropy sign flipped": ("ent_all[r0:r1] = L - (e * z).sum(axis=1) / denom", "ent_all[r0:r1] = (e * z).sum(axis=1) / denom - L"),
     "entropy unnormalised": ("ent_all[r0:r1] = L - (e * z).sum(axis=1) / denom", "ent_all[r0:r1] = L - (e * z).sum(axis=1)"),
+    "dlogits matrix target column not adjusted": ("    d[rows, t[rows]] -= 1.0\n    return d * (s * valid)", "    return d * (s * valid)"),
     "grad_input uses transposed product": ("grad_input[r0:r1] = d @ w", "grad_input[r0:r1] = (w.T @ d.T).T * 0 + d @ w[::-1]"),
 }
 
