@@ -151,7 +151,8 @@ def to_device_bf16(bits, device):
 
 
 # ----------------------------------------------------------------------------------- our arm
-def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local: int, peaks: dict):
+def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local: int, peaks: dict,
+                filter_eps: float = 0.0):
     import torch
     import linear_cross_entropy_tma_gb300 as flce
 
@@ -242,8 +243,27 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
     barrier(world)
     e2e_ms = max_over_ranks(a.elapsed_time(b), world) / e2e_steps
     del h_hidden, h_W, r_gi, r_gw
+
+    # the gradient-filtering variant (not the headline: it skips GEMM2 work the exact path does)
+    filt = None
+    if filter_eps > 0:
+        for _ in range(warmup):
+            flce.flce_fwd_bwd(hidden, W, target, filter_eps=filter_eps, **kw)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(steps):
+            flce.flce_fwd_bwd(hidden, W, target, filter_eps=filter_eps, **kw)
+        b.record()
+        torch.cuda.synchronize()
+        f_ms = a.elapsed_time(b) / steps
+        skips = flce.read_filter_skips(ws)
+        hb = -(-w.H // 256)
+        halves = 2 * (-(-w.BT // 256) * hb * -(-w.V // 256) + -(-w.V // 256) * hb * -(-w.BT // 256))
+        filt = {"filter_eps": filter_eps, "ms_per_step": f_ms, "tokens_per_s": world * w.BT / (f_ms * 1e-3),
+                "skipped_dS_blocks": skips, "skipped_fraction": skips / halves,
+                "note": "CCE-style gradient filtering; error bound in include/flce.h; not the headline"}
     return dict(elapsed_ms=elapsed_ms, passes=passes, clocks=clocks, peak_mem=peak_mem, loss=loss, e2e_ms=e2e_ms,
-                h2d=h2d, d2h=d2h, workspace_bytes=ws.numel())
+                h2d=h2d, d2h=d2h, workspace_bytes=ws.numel(), filter=filt)
 
 
 def bench_ce(steps: int, warmup: int, local: int, peaks: dict):
@@ -351,6 +371,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(wl.FUSED_WORKLOADS), default="long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ce", action="store_true")
+    ap.add_argument("--filter-eps", type=float, default=2.0 ** -12,
+                    help="also time the gradient-filtering variant at this threshold (0: skip)")
     args = ap.parse_args()
     w = wl.FUSED_WORKLOADS[args.workload]
     if args.warmup < 3:
@@ -370,7 +392,7 @@ def main():
     flce.load()
     peaks = load_peaks()
 
-    r = bench_fused(w, args.steps, args.warmup, world, local, peaks)
+    r = bench_fused(w, args.steps, args.warmup, world, local, peaks, filter_eps=args.filter_eps)
     ms = r["elapsed_ms"] / args.steps
     value = world * w.BT / (ms * 1e-3)
     passes = r["passes"]
@@ -407,6 +429,7 @@ def main():
         "memory": {"peak_allocated_bytes": r["peak_mem"], "workspace_bytes": r["workspace_bytes"],
                    "avoided_fp32_logits_bytes": 4 * w.BT * w.V},
         "loss": r["loss"],
+        "filter_variant": r["filter"],
     }
     if not args.no_ce and world == 1:
         line["ce_standalone"] = bench_ce(args.steps, args.warmup, local, peaks)

@@ -143,6 +143,17 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        -sum_n p_n log p_n = LSE_t - sum_n p_n z_n (verl's per-row entropy output,
  *                        "Fused Linear Cross-Entropy", "Strategy 2"), ignored rows included.  Costs
  *                        one more multiply-add per logit in the LSE pass.
+ *   filter_eps           0 (exact) or a positive threshold: the gradient-filtering variant of "Cut Cross
+ *                        Entropy visualized", "Gradient filtering", applied as there to the unscaled
+ *                        gradient p f - onehot (before the upstream gradient and the mean scale).  A
+ *                        256-row x 128-column block of dS (two CTAs' 128 rows; tokens x vocabulary in
+ *                        the grad_input pass, vocabulary x tokens in the grad_W pass) whose unscaled
+ *                        entries are all at most filter_eps in magnitude adds nothing to grad_input /
+ *                        grad_W (its tensor-core GEMM is skipped).  grad_bias and the loss stay exact.
+ *                        Error bound: each element of grad_input (grad_W) differs from the exact
+ *                        gradient by at most the sum of |dS| |W| (|dS| |hidden|) over the entries whose
+ *                        unscaled magnitude is at most filter_eps, plus the usual rounding.
+ *                        The number of skipped blocks is the 32-bit word at byte 20 of the workspace.
  */
 typedef struct flce_fwd_bwd_options {
   float grad_scale;
@@ -150,6 +161,7 @@ typedef struct flce_fwd_bwd_options {
   float* loss_per_token;
   int accumulate;
   float* entropy;
+  float filter_eps;
 } flce_fwd_bwd_options;
 
 /*

@@ -13,5 +13,6 @@ from ._lib import (  # noqa: F401
     flce_fwd_bwd,
     load,
     read_device_status,
+    read_filter_skips,
     workspace_size,
 )

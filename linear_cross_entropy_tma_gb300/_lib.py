@@ -31,7 +31,7 @@ c_sz = ctypes.c_size_t
 class FwdBwdOptions(ctypes.Structure):
     """flce_fwd_bwd_options of include/flce.h."""
     _fields_ = [("grad_scale", ctypes.c_float), ("grad_loss_per_token", c_p), ("loss_per_token", c_p),
-                ("accumulate", ctypes.c_int), ("entropy", c_p)]
+                ("accumulate", ctypes.c_int), ("entropy", c_p), ("filter_eps", ctypes.c_float)]
 
 
 def load() -> ctypes.CDLL:
@@ -104,7 +104,8 @@ def _bf16_ptr_ok(t, name):
 def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reduction: str = "mean",
                  z_loss: float = 0.0, need_grad_input: bool = True, need_grad_W: bool = True, workspace=None,
                  out=None, stream=None, pass_events=None, grad_scale: float = 1.0, grad_loss_per_token=None,
-                 accumulate: bool = False, want_loss_per_token: bool = False, want_entropy: bool = False) -> dict:
+                 accumulate: bool = False, want_loss_per_token: bool = False, want_entropy: bool = False,
+                 filter_eps: float = 0.0) -> dict:
     """Fused linear cross-entropy forward + backward on the current CUDA device.
 
     hidden [BT, H] bf16, W [V, H] bf16, target [BT] int64, bias [V] fp32 or None.  Returns a dict with
@@ -117,7 +118,9 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
 
     ``grad_scale`` multiplies every gradient; ``grad_loss_per_token`` (fp32 [BT], reduction "none"
     only) is the upstream gradient of each token's loss; ``accumulate`` adds the gradients to the
-    tensors given in ``out`` instead of overwriting them (flce_fwd_bwd_ex).  ``pass_events``: five
+    tensors given in ``out`` instead of overwriting them; ``filter_eps`` > 0 turns on gradient filtering
+    (GEMM2 of dS blocks whose entries are all below it is skipped; see include/flce.h for the error
+    bound) (flce_fwd_bwd_ex).  ``pass_events``: five
     recorded ``torch.cuda.Event(enable_timing=True)`` objects; the library re-records them at the pass
     boundaries (flce_fwd_bwd_timed) for per-kernel timing; only with the default options.
     """
@@ -165,7 +168,7 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     args = (_ptr(hidden), _ptr(W), _ptr(bias), _ptr(target), BT, H, V, ignore_index, red, float(z_loss),
             _ptr(o["loss"]), _ptr(gi), _ptr(gw), _ptr(gb), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel())
     plain = (red != 2 and grad_scale == 1.0 and grad_loss_per_token is None and not accumulate and lt is None
-             and ent is None)
+             and ent is None and filter_eps == 0.0)
     if pass_events is not None:
         if not plain:
             raise ValueError("pass_events only with the default options")
@@ -176,7 +179,8 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     elif plain:
         check(load().flce_fwd_bwd(*args, _stream_ptr(stream)))
     else:
-        opts = FwdBwdOptions(float(grad_scale), _ptr(grad_loss_per_token), _ptr(lt), 1 if accumulate else 0, _ptr(ent))
+        opts = FwdBwdOptions(float(grad_scale), _ptr(grad_loss_per_token), _ptr(lt), 1 if accumulate else 0, _ptr(ent),
+                             float(filter_eps))
         check(load().flce_fwd_bwd_ex(*args, ctypes.byref(opts), _stream_ptr(stream)))
     return dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, loss_per_token=lt,
                 entropy=ent, workspace=workspace)
@@ -240,6 +244,14 @@ def cross_entropy(logits, labels, ignore_index: int = -100, z_loss: float = 0.0,
     r = _ce_call(logits, dl, labels, ignore_index, z_loss, workspace, o, stream)
     r["dlogits"] = dl
     return r
+
+
+def read_filter_skips(workspace) -> int:
+    """dS blocks whose GEMM2 the gradient filter skipped in the last flce_fwd_bwd on this workspace
+    (the 32-bit word at byte 20; synchronises the device)."""
+    import torch
+    torch.cuda.synchronize(workspace.device)
+    return int(workspace[20:24].cpu().view(torch.int32).item())
 
 
 def read_device_status(workspace, stream=None) -> int:

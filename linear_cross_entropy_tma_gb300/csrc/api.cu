@@ -106,7 +106,7 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
                                 void* stream, void* const* events, int n_events) {
   g_last_error[0] = '\0';
   const flce_fwd_bwd_options opt =
-      options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0, nullptr};
+      options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0, nullptr, 0.0f};
   if (n_events != 0 && (n_events != 5 || events == nullptr)) {
     set_error("n_events must be 0 or 5 (with a non-NULL event array)");
     return FLCE_ERR_INVALID_ARG;
@@ -131,6 +131,10 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   }
   if (!std::isfinite(opt.grad_scale)) {
     set_error("grad_scale must be finite");
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (!(opt.filter_eps >= 0.0f) || !std::isfinite(opt.filter_eps)) {
+    set_error("filter_eps must be finite and >= 0");
     return FLCE_ERR_INVALID_ARG;
   }
   if (bias == nullptr && grad_bias != nullptr) {
@@ -184,6 +188,7 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   a.loss_tok = opt.loss_per_token;
   a.accumulate = opt.accumulate != 0;
   a.entropy = opt.entropy;
+  a.filter_eps = opt.filter_eps;
   char err[256] = "";
   const cudaError_t e = flce::launch_fused(a, workspace, num_sms, static_cast<cudaStream_t>(stream), err, sizeof(err),
                                            n_events ? reinterpret_cast<cudaEvent_t const*>(events) : nullptr);

@@ -88,7 +88,11 @@ struct PairSmem {
   uint64_t ds_free[2];
   uint64_t rx_full[2];
   uint64_t o_full;
+  uint64_t o_zero;
   uint64_t drain;
+  uint32_t skip_mail[2];      // filter: skip flag of the half received into this CTA's slot
+  uint32_t skip_pair[2][2];   // filter, pair leader: [half][CTA of the pair] skip flags of the current block
+  float wmax[2][4];           // filter: per warp, 1 when every dS entry of its rows in the half is small
   uint32_t tmem_base;
   int abort;
   float half_bias[kTileM];
@@ -106,6 +110,8 @@ struct PairParams {
   const uint32_t* zf_neg;
   float z_loss;
   int accumulate;
+  float filter_eps;         // > 0: skip GEMM2 of dS halves whose entries are all below it
+  uint32_t* skip_count;     // halves skipped (filter statistics)
   int BT, V, H;
   int n_rows, n_cols, num_kb;
   int P;                    // pairs per cluster
@@ -148,9 +154,12 @@ struct DsRow {
 //   grad_input pass (rows = tokens): columns col0.. are vocabulary entries; colb2 holds the bias in
 //     log2 units (-inf past V); `plain` means no bias and no column past V in this chunk.
 //   grad_W pass (rows = vocabulary): columns are tokens; tstats holds their statistics.
+//   fge > 0 (gradient filter, grad_W pass): fover is set when some |dS| exceeds fge |w| (w the column's
+//   gradient weight), checked where each column's statistics are loaded anyway.
 template <bool kVocabRows>
 __device__ __forceinline__ void ds_chunk64(uint32_t (&r)[64], int col0, const DsRow& rc, bool general, bool plain,
-                                           const float* __restrict__ colb2, const float4* tstats, float& gbias) {
+                                           const float* __restrict__ colb2, const float4* tstats, float& gbias,
+                                           float fge = 0.f, int* fover = nullptr) {
   if (!kVocabRows) {
     if (general) {
 #pragma unroll
@@ -194,6 +203,7 @@ __device__ __forceinline__ void ds_chunk64(uint32_t (&r)[64], int col0, const Ds
         const float e = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.bias2 - st.z)) * fmaf(rc.zl2, st.z, 1.0f);
         const float g = (rc.scale * st.y) * (yt == rc.y ? e - 1.0f : e);
         gbias += g;
+        if (fover != nullptr) *fover |= fabsf(g) > fge * fabsf(st.y) ? 1 : 0;
         r[i] = __float_as_uint(g);
       }
     } else {
@@ -203,13 +213,25 @@ __device__ __forceinline__ void ds_chunk64(uint32_t (&r)[64], int col0, const Ds
         float g = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.c + st.x));
         if (__float_as_int(st.w) == rc.y) g -= rc.scale * st.y;
         gbias += g;
+        if (fover != nullptr) *fover |= fabsf(g) > fge * fabsf(st.y) ? 1 : 0;
         r[i] = __float_as_uint(g);
       }
     }
   }
 }
 
-template <bool kVocabRows>
+// Gradient filter, grad_input pass: true when every one of this row's 64 dS values (fp32 bits) is small
+// relative to the row's gradient weight, |dS| <= eps |G u [valid]| (zero-weight rows are all zero).
+__device__ __forceinline__ bool filter_small_row(const uint32_t (&r)[64], const DsRow& rc, float eps) {
+  float worst = 0.f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) worst = fmaxf(worst, fabsf(__uint_as_float(r[i])));
+  return worst <= eps * fabsf(rc.coef);
+}
+
+// kFilter: the gradient-filtering variant (a separate instantiation, so the exact path carries none of
+// its checks).
+template <bool kVocabRows, bool kFilter>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
                   const PairParams p, uint32_t* __restrict__ status) {
@@ -233,6 +255,7 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
   const int nbox2 = static_cast<int>(n2) / 128; // 64-column boxes per CTA per GEMM2 stage
   const int nt = (p.n_cols + kPN - 1) / kPN;
   const int nkb = p.num_kb;
+  constexpr bool filt = kFilter;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -244,11 +267,13 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       mbar_init(&sm.st_empty[b], kEpiWarps);
       mbar_init(&sm.ds_full[b], 2);
       mbar_init(&sm.ds_free[b], static_cast<uint32_t>(P));
-      mbar_init(&sm.rx_full[b], 1);
+      // with the filter, the owner also arrives (after writing the half's skip flag)
+      mbar_init(&sm.rx_full[b], filt ? 2 : 1);
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_empty, 2 * kEpiWarps);
     mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.o_zero, 2 * kEpiWarps);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbarrier_init();
@@ -347,6 +372,13 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       auto gemm2 = [&](int j) {
         // the pair that writes block j+1 reuses both dS halves once every pair is done with block j
         const uint16_t next_owner = static_cast<uint16_t>(3u << (2 * ((j + 1) % P)));
+        if (filt && j == 0) {
+          // with the filter O starts from the epilogue's zeros and every GEMM2 accumulates
+          if (!mbar_wait_cluster(&sm.o_zero, 0, abort)) {
+            ok = false;
+            return;
+          }
+        }
         for (int half = 0; half < 2; ++half) {
           if (!mbar_wait_cluster(&sm.ds_full[half], static_cast<uint32_t>(j) & 1u, abort)) {
             ok = false;
@@ -357,13 +389,19 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
             return;
           }
           tc_fence_after();
+          const volatile uint32_t* sp = sm.skip_pair[half];
+          const bool skip = filt && sp[0] != 0u && sp[1] != 0u;
           const uint32_t a_base = smem_u32(sm.ds) + static_cast<uint32_t>(half) * kHalfBytes;
           const uint32_t b_base = smem_u32(sm.stage[stage]);
+          if (!skip) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * kBox + 32u * (k & 3), 16u, 1024u);
-            const uint64_t bd = sdesc_sw128(b_base + 2048u * k, kBox, 1024u);
-            mma_bf16_ss_pair(tmem + kTmemO, ad, bd, idesc2, (j | half | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * kBox + 32u * (k & 3), 16u, 1024u);
+              const uint64_t bd = sdesc_sw128(b_base + 2048u * k, kBox, 1024u);
+              mma_bf16_ss_pair(tmem + kTmemO, ad, bd, idesc2, (filt || (j | half | k) != 0) ? 1u : 0u);
+            }
+          } else if (p.skip_count != nullptr) {
+            atomicAdd(p.skip_count, 1u);
           }
           mma_commit_mc(&sm.empty[stage], pair_mask);
           advance();
@@ -424,6 +462,11 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
             ok = false;
             break;
           }
+          if (filt) {
+            // the owner's skip flag for this half, on to the pair leader's table
+            const uint32_t f = *reinterpret_cast<volatile uint32_t*>(&sm.skip_mail[half]);
+            st_shared_cluster_u32(mapa_shared(smem_u32(&sm.skip_pair[half][q]), lead_rank), f);
+          }
           mbar_arrive_cluster(half ? ds_full_c1 : ds_full_c0);
         }
         ++v;
@@ -462,6 +505,16 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
     float gbias = 0.f;
     bool ok = true;
     uint8_t* const ds_row = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(rl) * 128u;
+    if (filt) {
+      // O starts at zero (GEMM2 then always accumulates, whichever halves are skipped): this warp's 32
+      // lanes of its 128 of the 256 accumulator columns
+      for (int c = 0; c < 4; ++c)
+        tmem_st_32cols_zero(tmem + (static_cast<uint32_t>(qq * 32) << 16) + kTmemO + static_cast<uint32_t>(hh * 128 + 32 * c));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.o_zero), lead_rank));
+    }
     int u = 0;
     for (int j = pr; j < nt && ok; j += P, ++u) {
       if (!mbar_wait(&sm.s_full, u & 1, abort)) {
@@ -490,13 +543,28 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(s_empty_c);
-        ds_chunk64<kVocabRows>(ra, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gbias);
+        // with the filter: is every entry of this row's half small, |dS| <= eps |w| with w the entry's
+        // gradient weight (the row's for grad_input, the token column's for grad_W), i.e. the unscaled
+        // p f - onehot below eps?  (fp32, before rounding; zero-weight entries are zero and count as small)
+        bool small = true;
+        int over = 0;
+        const float fge = (kVocabRows && filt) ? p.filter_eps * fabsf(scale) : 0.f;
+        int* const fov = (kVocabRows && filt) ? &over : nullptr;
+        ds_chunk64<kVocabRows>(ra, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gbias,
+                               fge, fov);
+        if (!kVocabRows && filt) small = filter_small_row(ra, rc, p.filter_eps);
 #pragma unroll
         for (int i2 = 0; i2 < 32; ++i2) pk0[i2] = pack_bf16x2(__uint_as_float(ra[2 * i2]), __uint_as_float(ra[2 * i2 + 1]));
         ds_chunk64<kVocabRows>(rb, col0 + 64, rc, general, p.bias == nullptr && col0 + 128 <= p.V, p.colb2,
-                               tstats + 64, gbias);
+                               tstats + 64, gbias, fge, fov);
+        if (!kVocabRows && filt) small = filter_small_row(rb, rc, p.filter_eps) && small;
+        if (kVocabRows && filt) small = (over == 0);
 #pragma unroll
         for (int i2 = 0; i2 < 32; ++i2) pk1[i2] = pack_bf16x2(__uint_as_float(rb[2 * i2]), __uint_as_float(rb[2 * i2 + 1]));
+        if (filt) {
+          const bool all_small = __all_sync(0xffffffffu, small);
+          if (lane == 0) sm.wmax[hh][qq] = all_small ? 1.f : 0.f;
+        }
       }
       // every pair must be done with block j-1 in this half slot before it is overwritten here and
       // in the other pairs' CTAs (phase = blocks this pair wrote after block 0)
@@ -530,7 +598,22 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
         }
       }
       named_barrier_sync(1 + hh, 4 * 32);
-      if (qq == 0 && lane == 0) mbar_arrive_cluster(ds_full_c);
+      if (qq == 0 && lane == 0) {
+        if (filt) {
+          // the half is skipped by every pair when both CTAs of the owner pair find all of their dS below
+          // the threshold; this CTA's flag goes to its pair leader and to the other pairs' CTAs
+          const uint32_t f = (sm.wmax[hh][0] != 0.f && sm.wmax[hh][1] != 0.f && sm.wmax[hh][2] != 0.f &&
+                              sm.wmax[hh][3] != 0.f) ? 1u : 0u;
+          st_shared_cluster_u32(mapa_shared(smem_u32(&sm.skip_pair[hh][q]), lead_rank), f);
+          for (int pp = 0; pp < P; ++pp) {
+            if (pp == pr) continue;
+            const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
+            st_shared_cluster_u32(mapa_shared(smem_u32(&sm.skip_mail[hh]), dst_rank), f);
+            mbar_arrive_cluster(mapa_shared(smem_u32(&sm.rx_full[hh]), dst_rank));
+          }
+        }
+        mbar_arrive_cluster(ds_full_c);
+      }
     }
 
     if (ok && mbar_wait(&sm.o_full, 0, abort)) {
@@ -632,6 +715,8 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   p.zf_neg = a.zf_neg;
   p.z_loss = a.z_loss;
   p.accumulate = a.accumulate ? 1 : 0;
+  p.filter_eps = a.filter_eps;
+  p.skip_count = a.skip_count;
   p.BT = a.BT;
   p.V = a.V;
   p.H = a.H;
@@ -645,8 +730,8 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   const int h_chunks = (kVocabRows && p.grad_W == nullptr) ? 1 : (p.H + kHc - 1) / kHc;
   p.P = pairs_per_cluster(h_chunks);
   constexpr size_t smem = pair_smem_bytes<kVocabRows>();
-  cudaError_t e = cudaFuncSetAttribute(dgrad_pair_kernel<kVocabRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kern = p.filter_eps > 0.f ? dgrad_pair_kernel<kVocabRows, true> : dgrad_pair_kernel<kVocabRows, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int row_pairs = (p.n_rows + 2 * kTileM - 1) / (2 * kTileM);
   cudaLaunchConfig_t cfg = {};
@@ -661,7 +746,7 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, dgrad_pair_kernel<kVocabRows>, rows, cols, p, a.status);
+  e = cudaLaunchKernelEx(&cfg, kern, rows, cols, p, a.status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -404,6 +404,7 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   w.scale = reinterpret_cast<float*>(p + 4);
   w.n_valid = reinterpret_cast<int64_t*>(p + 8);
   w.zf_neg = reinterpret_cast<uint32_t*>(p + 16);
+  w.skipped = reinterpret_cast<uint32_t*>(p + 20);
   size_t off = 256;
   w.part = reinterpret_cast<float2*>(p + off);
   off += align_up(sizeof(float2) * kMaxSplits * btp, 256);

@@ -29,6 +29,7 @@ struct FusedWorkspace {
   uint32_t* status;  // header: status word
   float* scale;      // header: gradient scale G = grad_scale / max(n_valid, 1) (mean) or grad_scale
   int64_t* n_valid;  // header: valid count
+  uint32_t* skipped; // header: dS halves whose GEMM2 the gradient filter skipped (both passes)
   uint32_t* zf_neg;  // header: non-zero when the log form of dS does not apply (some valid row has
                      // f u <= 0 with u its upstream gradient, or the gradient scale is <= 0)
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
@@ -63,6 +64,7 @@ struct FusedArgs {
   const float* grad_tok;      // reduction none: upstream gradient per token, or NULL (ones)
   float* loss_tok;            // per-token losses out, or NULL
   float* entropy;             // per-row entropy of softmax(z) out, or NULL
+  float filter_eps;           // > 0: gradient filtering threshold
   bool accumulate;            // gradients += instead of =
 };
 
@@ -75,6 +77,8 @@ struct DgPairArgs {
   const uint32_t* zf_neg;
   float z_loss;
   bool accumulate;
+  float filter_eps;
+  uint32_t* skip_count;
   int BT, V, H;
   uint16_t* grad_input;
   float* grad_W;

@@ -39,6 +39,8 @@ cudaError_t launch_fused(const FusedArgs& a, void* workspace, int num_sms, cudaS
   pa.zf_neg = ws.zf_neg;
   pa.z_loss = a.z_loss;
   pa.accumulate = a.accumulate;
+  pa.filter_eps = a.filter_eps;
+  pa.skip_count = ws.skipped;
   pa.BT = static_cast<int>(a.BT);
   pa.V = static_cast<int>(a.V);
   pa.H = static_cast<int>(a.H);

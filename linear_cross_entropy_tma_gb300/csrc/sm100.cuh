@@ -203,6 +203,12 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
+// Writes zero into 32 consecutive TMEM columns of this warp's 32 lanes (tcgen05.st, 32x32b shape).
+__device__ __forceinline__ void tmem_st_32cols_zero(uint32_t taddr) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1};" ::"r"(taddr), "r"(0u) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ------------------------------------------------------------------------- CTA pairs (cta_group::2)
 // Two CTAs of a cluster whose ranks differ in bit 0 form a pair: one tcgen05.mma issued by the
 // even CTA reads A rows 0-127 from the even CTA's shared memory and rows 128-255 from the odd CTA's,
@@ -310,6 +316,10 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
 
 __device__ __forceinline__ void st_shared_cluster_f32(uint32_t cluster_addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, uint4 v) {

@@ -76,8 +76,8 @@ def test_fwd_bwd_argument_errors(lib):
     assert b"workspace" in lib.flce_last_error()
 
 
-def _fwd_ex(lib, red=2, loss=None, grad_scale=1.0, gtok=None, ltok=None, acc=0, gi=0x5000, ent=None):
-    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent)
+def _fwd_ex(lib, red=2, loss=None, grad_scale=1.0, gtok=None, ltok=None, acc=0, gi=0x5000, ent=None, eps=0.0):
+    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent, eps)
     return lib.flce_fwd_bwd_ex(0x1000, 0x2000, None, 0x3000, 128, 64, 512, -100, red, 0.0, loss, gi, 0x6000, None,
                                None, 0x7000, 1 << 30, ctypes.byref(opts), None)
 
@@ -88,6 +88,8 @@ def test_fwd_bwd_ex_argument_errors(lib):
     assert _fwd_ex(lib, red=0, loss=0x4000, gtok=0x9000) == INVALID_ARG  # per-token upstream grads: none only
     assert _fwd_ex(lib, grad_scale=float("nan")) == INVALID_ARG
     assert _fwd_ex(lib, grad_scale=float("inf")) == INVALID_ARG
+    assert _fwd_ex(lib, eps=-1e-3) == INVALID_ARG
+    assert _fwd_ex(lib, eps=float("nan")) == INVALID_ARG
     assert _fwd_ex(lib, ltok=0x9002) == MISALIGNED
     assert _fwd_ex(lib, gtok=0x9001) == MISALIGNED
     assert _fwd_ex(lib, ent=0x9003) == MISALIGNED
@@ -96,6 +98,7 @@ def test_fwd_bwd_ex_argument_errors(lib):
     assert _fwd_ex(lib, gtok=0x9000, ltok=0xA000, acc=1, grad_scale=-2.0) == NO_DEVICE
     assert _fwd_ex(lib, red=1, loss=0x4000, acc=1) == NO_DEVICE
     assert _fwd_ex(lib, red=0, loss=0x4000, ent=0xB000) == NO_DEVICE
+    assert _fwd_ex(lib, red=0, loss=0x4000, eps=2.0 ** -12) == NO_DEVICE
     # the plain entry points do not take reduction none
     assert _fwd(lib, red=2) == INVALID_ARG
 
