@@ -48,6 +48,9 @@ constexpr int kPN = 256;                      // logits tile columns = K of GEMM
 constexpr int kBK = 64;
 constexpr int kHc = 256;                      // H columns per pair (GEMM2 N)
 constexpr int kMaxPairs = 4;                  // pairs per cluster that share each logits tile
+// Order of a step's tensor work: 0 = GEMM2 half 0, half 1, then the GEMM1 share; 1 = the GEMM1 share
+// first; 2 = GEMM2 half 0, half of the share, GEMM2 half 1, the rest of the share.
+constexpr int kStepOrder = 0;
 constexpr uint32_t kBox = kTileM * kBK * 2;   // 16 KiB: a 128-row x 64-column bf16 box
 constexpr uint32_t kStage = 2 * kBox;
 constexpr uint32_t kHalfBytes = 2 * kBox;     // one 128-column half of a dS block (per CTA)
@@ -304,26 +307,24 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           phase ^= 1u;
         }
       };
-      auto load_gemm2 = [&](int j) {
-        for (int half = 0; half < 2 && ok; ++half) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
-            ok = false;
-            return;
-          }
-          const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), lead_rank);
-          if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2u * nbox2 * kBox);
-          for (int b = 0; b < nbox2; ++b)
-            tma_load_2d_pair(sm.stage[stage] + b * kBox, &tm_cols, fb,
-                             h0 + static_cast<int>(q * (n2 / 2)) + 64 * b, j * kPN + half * kTileM);
-          next();
+      auto load_gemm2 = [&](int j, int half) {
+        if (!ok || j < 0) return;
+        if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
+          ok = false;
+          return;
         }
+        const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), lead_rank);
+        if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2u * nbox2 * kBox);
+        for (int b = 0; b < nbox2; ++b)
+          tma_load_2d_pair(sm.stage[stage] + b * kBox, &tm_cols, fb,
+                           h0 + static_cast<int>(q * (n2 / 2)) + 64 * b, j * kPN + half * kTileM);
+        next();
       };
       int u = 0;   // owned blocks whose GEMM1 has been fully loaded
       for (int s = -2 * P; s < nt && ok; ++s) {
-        if (s >= 0) load_gemm2(s);
         const G1Share g = g1_share(s, pr, P);
-        if (!ok || g.block < 0 || g.block >= nt) continue;
-        if (kVocabRows && g.prog == 0) {
+        const bool has_g1 = g.block >= 0 && g.block < nt;
+        if (kVocabRows && has_g1 && g.prog == 0) {
           // this block's per-token statistics (stats is padded to a multiple of 256 tokens)
           const int sb = u & 1;
           if (!mbar_wait(&sm.st_empty[sb], ((u >> 1) & 1) ^ 1, abort)) {
@@ -334,19 +335,30 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           bulk_load_1d(sm.colstats[sb], p.stats + static_cast<size_t>(g.block) * kPN, kPN * sizeof(float4),
                        &sm.st_full[sb]);
         }
-        const int kb1 = share_begin(g.prog + 1, nkb, P);
-        for (int kb = share_begin(g.prog, nkb, P); kb < kb1; ++kb) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
-            ok = false;
-            break;
+        const int kb0 = has_g1 ? share_begin(g.prog, nkb, P) : 0;
+        const int kb1 = has_g1 ? share_begin(g.prog + 1, nkb, P) : 0;
+        const int kbm = kStepOrder == 2 ? (kb0 + kb1) / 2 : kb1;
+        auto load_gemm1 = [&](int kb_begin, int kb_end) {
+          for (int kb = kb_begin; kb < kb_end && ok; ++kb) {
+            if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
+              ok = false;
+              return;
+            }
+            const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), lead_rank);
+            if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * kStage);
+            tma_load_2d_pair(sm.stage[stage], &tm_rows, fb, kb * kBK, r0);
+            tma_load_2d_pair(sm.stage[stage] + kBox, &tm_cols, fb, kb * kBK,
+                             g.block * kPN + static_cast<int>(q) * kTileM);
+            next();
           }
-          const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), lead_rank);
-          if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * kStage);
-          tma_load_2d_pair(sm.stage[stage], &tm_rows, fb, kb * kBK, r0);
-          tma_load_2d_pair(sm.stage[stage] + kBox, &tm_cols, fb, kb * kBK, g.block * kPN + static_cast<int>(q) * kTileM);
-          next();
-        }
-        if (g.prog == P - 1) ++u;
+        };
+        if (kStepOrder == 1) load_gemm1(kb0, kb1);
+        load_gemm2(s, 0);
+        if (kStepOrder == 2) load_gemm1(kb0, kbm);
+        load_gemm2(s, 1);
+        if (kStepOrder == 0) load_gemm1(kb0, kb1);
+        if (kStepOrder == 2) load_gemm1(kbm, kb1);
+        if (has_g1 && g.prog == P - 1) ++u;
       }
       if (!ok) {
         // let copies already issued land before the CTA can finish
@@ -369,17 +381,18 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           phase ^= 1u;
         }
       };
-      auto gemm2 = [&](int j) {
+      auto gemm2 = [&](int j, int half) {
+        if (!ok || j < 0) return;
         // the pair that writes block j+1 reuses both dS halves once every pair is done with block j
         const uint16_t next_owner = static_cast<uint16_t>(3u << (2 * ((j + 1) % P)));
-        if (filt && j == 0) {
+        if (filt && j == 0 && half == 0) {
           // with the filter O starts from the epilogue's zeros and every GEMM2 accumulates
           if (!mbar_wait_cluster(&sm.o_zero, 0, abort)) {
             ok = false;
             return;
           }
         }
-        for (int half = 0; half < 2; ++half) {
+        {
           if (!mbar_wait_cluster(&sm.ds_full[half], static_cast<uint32_t>(j) & 1u, abort)) {
             ok = false;
             return;
@@ -410,35 +423,46 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       };
       int u = 0;   // owned blocks whose GEMM1 has been issued in full
       for (int s = -2 * P; s < nt && ok; ++s) {
-        if (s >= 0) gemm2(s);
         const G1Share g = g1_share(s, pr, P);
-        if (!ok || g.block < 0 || g.block >= nt) continue;
-        if (g.prog == 0) {
-          // the epilogue must have read the previous logits tile out of TMEM
-          if (!mbar_wait_cluster(&sm.s_empty, (u & 1) ^ 1, abort)) {
-            ok = false;
-            break;
+        const bool has_g1 = g.block >= 0 && g.block < nt;
+        const int kb0 = has_g1 ? share_begin(g.prog, nkb, P) : 0;
+        const int kb1 = has_g1 ? share_begin(g.prog + 1, nkb, P) : 0;
+        const int kbm = kStepOrder == 2 ? (kb0 + kb1) / 2 : kb1;
+        bool first = true;
+        auto gemm1 = [&](int kb_begin, int kb_end) {
+          if (!ok || !has_g1) return;
+          if (first && g.prog == 0) {
+            // the epilogue must have read the previous logits tile out of TMEM
+            if (!mbar_wait_cluster(&sm.s_empty, (u & 1) ^ 1, abort)) {
+              ok = false;
+              return;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
-        }
-        const int kb0 = share_begin(g.prog, nkb, P);
-        const int kb1 = share_begin(g.prog + 1, nkb, P);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&sm.full[stage], phase, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(sm.stage[stage]);
-          const uint32_t b_base = a_base + kBox;
+          first = false;
+          for (int kb = kb_begin; kb < kb_end; ++kb) {
+            if (!mbar_wait(&sm.full[stage], phase, abort)) {
+              ok = false;
+              return;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sm.stage[stage]);
+            const uint32_t b_base = a_base + kBox;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_ss_pair(tmem + kTmemS, sdesc_sw128(a_base + 32u * k, 16u, 1024u),
-                             sdesc_sw128(b_base + 32u * k, 16u, 1024u), idesc1, (kb | k) != 0 ? 1u : 0u);
-          mma_commit_mc(&sm.empty[stage], pair_mask);
-          advance();
-        }
-        if (ok && g.prog == P - 1) {
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_ss_pair(tmem + kTmemS, sdesc_sw128(a_base + 32u * k, 16u, 1024u),
+                               sdesc_sw128(b_base + 32u * k, 16u, 1024u), idesc1, (kb | k) != 0 ? 1u : 0u);
+            mma_commit_mc(&sm.empty[stage], pair_mask);
+            advance();
+          }
+        };
+        if (kStepOrder == 1) gemm1(kb0, kb1);
+        gemm2(s, 0);
+        if (kStepOrder == 2) gemm1(kb0, kbm);
+        gemm2(s, 1);
+        if (kStepOrder == 0) gemm1(kb0, kb1);
+        if (kStepOrder == 2) gemm1(kbm, kb1);
+        if (ok && has_g1 && g.prog == P - 1) {
           mma_commit_mc(&sm.s_full, pair_mask);
           ++u;
         }
