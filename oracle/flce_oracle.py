@@ -37,6 +37,11 @@ Readings where the pages are silent (each also listed in the design notes):
     p2 "Breakdown: Backward Pass", step 4);
   * a target outside [0, V) that is not ignore_index is treated as ignored;
   * z_sum of the standalone CE is the unscaled sum of LSE^2 over valid rows.
+  * logit_avg (p2 "Forward pass", the by-product of the LSE kernel that keys the vocabulary sort) is the
+    mean of z[t, n] over all BT rows of the batch, ignored rows included (the forward kernel sees every
+    row); an empty batch gives 0 (+ b);
+  * the vocabulary order of p2 "Vocabulary Sorting" is by average logit, largest first, equal keys in
+    increasing vocabulary index (a stable sort).
 
 Rows are processed in blocks only to bound memory: the loss is a sum over tokens and both gradients
 are sums of per-token terms, and p1 ("The identity ...", consequence 2) states that this sum commutes
@@ -50,7 +55,7 @@ import numpy as np
 
 __all__ = [
     "widen", "logits", "lse", "flce_reference", "flce_dlogits", "flce_lse", "flce_sampled", "flce_reference_loops",
-    "ce_reference", "ce_reference_loops",
+    "ce_reference", "ce_reference_loops", "logit_avg", "vocab_order",
 ]
 
 
@@ -328,3 +333,30 @@ def ce_reference_loops(logits_, labels, ignore_index: int = -100, z_loss: float 
         for j in range(V):
             D[i, j] = math.exp(row[j] - L) * (1.0 + 2.0 * z_loss * L) - (1.0 if j == y else 0.0)
     return dict(ce_sum=math.fsum(ce_sum), z_sum=math.fsum(z_sum), n_valid=n_valid, dlogits=D)
+
+
+def logit_avg(hidden, W, bias=None, row_block: int = 512) -> np.ndarray:
+    """Average logit of every vocabulary entry over the batch, (1/BT) sum_t z[t, n] with z = hidden . W^T
+    (+ b) (p2 "Forward pass": logit_avg, the mean logit per vocabulary entry, saved for the backward
+    pass).  float64; the rows are summed block by block to bound memory."""
+    h = widen(hidden)
+    w = widen(W)
+    b = None if bias is None else widen(bias)
+    BT = h.shape[0]
+    col_sum = np.zeros(w.shape[0])
+    for r0 in range(0, BT, row_block):
+        z = h[r0:r0 + row_block] @ w.T
+        if b is not None:
+            z += b[None, :]
+        col_sum += z.sum(axis=0)
+    if BT == 0:
+        return col_sum + (b if b is not None else 0.0)
+    return col_sum / BT
+
+
+def vocab_order(avg) -> np.ndarray:
+    """The vocabulary sorted by average logit, largest first (p2 "Vocabulary Sorting"): entry k of the
+    result is the vocabulary index placed at sorted position k.  Equal keys keep increasing index
+    order."""
+    a = np.asarray(avg, dtype=np.float64)
+    return np.argsort(-a, kind="stable").astype(np.int64)

@@ -7,7 +7,9 @@
   * closed forms: W = 0, V = 1, and the hand-evaluated values in tests/golden/ce_closed_forms.txt;
   * invariants: LSE shift, dlogits row sums, ignored rows, n_valid = 0, vocabulary permutation;
   * the unreduced loss with an upstream gradient against finite differences and torch autograd;
-  * the per-row entropy against torch, plain loops, closed forms and its bounds.
+  * the per-row entropy against torch, plain loops, closed forms and its bounds;
+  * the average logit per vocabulary entry against loops, closed forms and the linearity identity, and
+    the vocabulary order against a hand-evaluated case and brute force.
 
 The same checks run against deliberately broken copies of the oracle (test_planted_mistakes) to show
 that a dropped term, a wrong sign, a wrong index or a wrong scale fails at least one of them.
@@ -324,9 +326,34 @@ def pin_dlogits_matrix(orc):
         assert _rel(d.T @ hidden, g["grad_W"]) < 1e-12
 
 
+def pin_logit_avg_and_order(orc):
+    # logit_avg: plain loops with exactly rounded sums; closed forms (W = 0 gives the bias, equal rows
+    # give one matrix-vector product); the linearity identity mean_t z[t, n] = W[n] . mean_t hidden[t]
+    # + b[n] (a different route to the same number); an empty batch
+    hidden, W, b, _ = _tiny_case(seed=31, BT=9, H=4, V=6)
+    got = orc.logit_avg(hidden, W, bias=b, row_block=4)
+    for n in range(W.shape[0]):
+        zs = [math.fsum(hidden[t, k] * W[n, k] for k in range(W.shape[1])) + b[n] for t in range(hidden.shape[0])]
+        assert abs(got[n] - math.fsum(zs) / len(zs)) < 1e-13 * max(1.0, abs(got[n]))
+    assert _rel(orc.logit_avg(hidden, np.zeros_like(W), bias=b), b) < 1e-15
+    same = np.repeat(hidden[:1], 5, axis=0)
+    assert _rel(orc.logit_avg(same, W, bias=b), W @ hidden[0] + b) < 1e-13
+    assert _rel(orc.logit_avg(hidden, W, bias=b), W @ hidden.mean(axis=0) + b) < 1e-13
+    assert _rel(orc.logit_avg(hidden, W), W @ hidden.mean(axis=0)) < 1e-13
+    assert np.array_equal(orc.logit_avg(hidden[:0], W, bias=b), b)
+    # the order: a hand-evaluated case with ties (largest first, ties by index), then brute force
+    assert orc.vocab_order(np.array([0.0, 5.0, -1.0, 5.0, 2.0])).tolist() == [1, 3, 4, 0, 2]
+    rng = np.random.default_rng(32)
+    keys = rng.integers(-3, 4, 40).astype(np.float64) / 2.0
+    order = orc.vocab_order(keys)
+    assert order.tolist() == sorted(range(40), key=lambda n: (-keys[n], n))
+    assert sorted(order.tolist()) == list(range(40))
+    assert np.all(np.diff(keys[order]) <= 0)
+
+
 PINS = [pin_loops_vs_vectorised, pin_finite_differences, pin_torch_fp64, pin_closed_forms,
         pin_invariants, pin_ce, pin_sampled_matches_full, pin_unreduced_and_upstream, pin_entropy,
-        pin_dlogits_matrix]
+        pin_dlogits_matrix, pin_logit_avg_and_order]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -352,6 +379,11 @@ MUTATIONS = {
     "entropy sign flipped": ("ent_all[r0:r1] = L - (e * z).sum(axis=1) / denom", "ent_all[r0:r1] = (e * z).sum(axis=1) / denom - L"),
     "entropy unnormalised": ("ent_all[r0:r1] = L - (e * z).sum(axis=1) / denom", "ent_all[r0:r1] = L - (e * z).sum(axis=1)"),
     "dlogits matrix target column not adjusted": ("    d[rows, t[rows]] -= 1.0\n    return d * (s * valid)", "    return d * (s * valid)"),
+    "logit_avg bias dropped": ("            z += b[None, :]\n        col_sum", "            pass\n        col_sum"),
+    "logit_avg divided by V": ("return col_sum / BT", "return col_sum / w.shape[0]"),
+    "vocabulary order ascending": ('np.argsort(-a, kind="stable")', 'np.argsort(a, kind="stable")'),
+    "vocabulary ties in reverse index order": ('np.argsort(-a, kind="stable")',
+                                               '(len(a) - 1 - np.argsort(-a[::-1], kind="stable"))'),
     "grad_input uses transposed product": ("grad_input[r0:r1] = d @ w", "grad_input[r0:r1] = (w.T @ d.T).T * 0 + d @ w[::-1]"),
 }
 
