@@ -66,10 +66,12 @@ typedef enum flce_status {
 /* bits of the device status word (first 4 bytes of either workspace) */
 #define FLCE_STATUS_BAD_TARGET 0x1u
 #define FLCE_STATUS_TIMEOUT 0x2u
+#define FLCE_STATUS_INTERNAL 0x4u   /* a self-check of the vocabulary sort failed (a defect; results invalid) */
 
 /*
  * Bytes of workspace flce_fwd_bwd needs for these sizes (O(BT + V) floats: per-row LSE statistics,
- * per-row loss terms, the per-column bias in log2 units, the status word and the valid count).
+ * per-row loss terms, the per-column bias in log2 units, the status word and the valid count; plus a
+ * fixed 16 MiB of per-SM staging blocks through which the gradient passes hand dS tiles between SMs).
  * Returns 0 for negative sizes.
  */
 size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V);
@@ -154,6 +156,17 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        gradient by at most the sum of |dS| |W| (|dS| |hidden|) over the entries whose
  *                        unscaled magnitude is at most filter_eps, plus the usual rounding.
  *                        The number of skipped blocks is the 32-bit word at byte 20 of the workspace.
+ *   sort_vocab           non-zero: the vocabulary sort of "Cut Cross Entropy visualized", "Vocabulary
+ *                        Sorting", which makes filtering skip more blocks.  logit_avg[n], the mean of
+ *                        z[t, n] over all BT rows (ignored rows included; "Forward pass"), is computed
+ *                        as W[n] . mean_t hidden[t] + b[n]; every pass then runs on the vocabulary in
+ *                        decreasing logit_avg order (equal keys by index).  Results are those of the
+ *                        unsorted call up to rounding order; the filter's error bound is unchanged.
+ *                        Needs flce_workspace_size_ex(BT, H, V, options) bytes of workspace (adds a
+ *                        sorted copy of W: V x H bf16).
+ *   logit_avg            [V] fp32, device, or NULL: receives logit_avg (requires sort_vocab).
+ *   vocab_order          [V] int32, device, or NULL: receives the sorted order, entry k = the vocabulary
+ *                        index at sorted position k (requires sort_vocab).
  */
 typedef struct flce_fwd_bwd_options {
   float grad_scale;
@@ -162,12 +175,19 @@ typedef struct flce_fwd_bwd_options {
   int accumulate;
   float* entropy;
   float filter_eps;
+  int sort_vocab;
+  float* logit_avg;
+  int32_t* vocab_order;
 } flce_fwd_bwd_options;
+
+/* Bytes of workspace flce_fwd_bwd_ex needs with these options (NULL: flce_workspace_size). */
+size_t flce_workspace_size_ex(int64_t BT, int64_t H, int64_t V, const flce_fwd_bwd_options* options);
 
 /*
  * flce_fwd_bwd with options (NULL options = the defaults above).  reduction may also be
  * FLCE_REDUCTION_NONE; then `loss` may be NULL and, when given, receives the plain sum of the
- * per-token losses.  Pointer alignment: loss_per_token, grad_loss_per_token and entropy 4 bytes.
+ * per-token losses.  Pointer alignment: loss_per_token, grad_loss_per_token, entropy, logit_avg and
+ * vocab_order 4 bytes.
  */
 flce_status flce_fwd_bwd_ex(const uint16_t* hidden, const uint16_t* W, const float* bias,
                             const int64_t* target, int64_t BT, int64_t H, int64_t V,

@@ -16,7 +16,8 @@ LIB_PATH = os.path.join(PKG, "libflce.so")
 FLCE_OK = 0
 STATUS_BAD_TARGET = 0x1
 STATUS_TIMEOUT = 0x2
-EXPORTED = ("flce_workspace_size", "flce_fwd_bwd", "flce_fwd_bwd_timed", "flce_fwd_bwd_ex", "ce_workspace_size",
+STATUS_INTERNAL = 0x4
+EXPORTED = ("flce_workspace_size", "flce_workspace_size_ex", "flce_fwd_bwd", "flce_fwd_bwd_timed", "flce_fwd_bwd_ex", "ce_workspace_size",
             "ce_with_grad", "ce_with_grad_ex", "flce_read_device_status", "flce_status_string", "flce_last_error",
             "ce_with_grad_noalloc")
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
@@ -31,7 +32,8 @@ c_sz = ctypes.c_size_t
 class FwdBwdOptions(ctypes.Structure):
     """flce_fwd_bwd_options of include/flce.h."""
     _fields_ = [("grad_scale", ctypes.c_float), ("grad_loss_per_token", c_p), ("loss_per_token", c_p),
-                ("accumulate", ctypes.c_int), ("entropy", c_p), ("filter_eps", ctypes.c_float)]
+                ("accumulate", ctypes.c_int), ("entropy", c_p), ("filter_eps", ctypes.c_float),
+                ("sort_vocab", ctypes.c_int), ("logit_avg", c_p), ("vocab_order", c_p)]
 
 
 def load() -> ctypes.CDLL:
@@ -45,6 +47,8 @@ def load() -> ctypes.CDLL:
     lib = ctypes.CDLL(LIB_PATH)
     lib.flce_workspace_size.restype = c_sz
     lib.flce_workspace_size.argtypes = [c_i64, c_i64, c_i64]
+    lib.flce_workspace_size_ex.restype = c_sz
+    lib.flce_workspace_size_ex.argtypes = [c_i64, c_i64, c_i64, ctypes.POINTER(FwdBwdOptions)]
     lib.flce_fwd_bwd.restype = ctypes.c_int
     lib.flce_fwd_bwd.argtypes = [c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i64, ctypes.c_int, ctypes.c_float,
                                  c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]
@@ -87,8 +91,12 @@ def _stream_ptr(stream) -> int | None:
     return s.cuda_stream
 
 
-def workspace_size(BT: int, H: int, V: int) -> int:
-    return int(load().flce_workspace_size(BT, H, V))
+def workspace_size(BT: int, H: int, V: int, sort_vocab: bool = False) -> int:
+    """Workspace bytes of flce_fwd_bwd; with ``sort_vocab`` those of the vocabulary-sorting call."""
+    if not sort_vocab:
+        return int(load().flce_workspace_size(BT, H, V))
+    opts = FwdBwdOptions(1.0, None, None, 0, None, 0.0, 1, None, None)
+    return int(load().flce_workspace_size_ex(BT, H, V, ctypes.byref(opts)))
 
 
 def ce_workspace_size(B: int, V: int) -> int:
@@ -105,7 +113,7 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
                  z_loss: float = 0.0, need_grad_input: bool = True, need_grad_W: bool = True, workspace=None,
                  out=None, stream=None, pass_events=None, grad_scale: float = 1.0, grad_loss_per_token=None,
                  accumulate: bool = False, want_loss_per_token: bool = False, want_entropy: bool = False,
-                 filter_eps: float = 0.0) -> dict:
+                 filter_eps: float = 0.0, sort_vocab: bool = False) -> dict:
     """Fused linear cross-entropy forward + backward on the current CUDA device.
 
     hidden [BT, H] bf16, W [V, H] bf16, target [BT] int64, bias [V] fp32 or None.  Returns a dict with
@@ -120,7 +128,8 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     only) is the upstream gradient of each token's loss; ``accumulate`` adds the gradients to the
     tensors given in ``out`` instead of overwriting them; ``filter_eps`` > 0 turns on gradient filtering
     (GEMM2 of dS blocks whose entries are all below it is skipped; see include/flce.h for the error
-    bound) (flce_fwd_bwd_ex).  ``pass_events``: five
+    bound); ``sort_vocab`` runs every pass on the vocabulary sorted by average logit (adds ``logit_avg``,
+    fp32 [V], and ``vocab_order``, int32 [V], to the result) (flce_fwd_bwd_ex).  ``pass_events``: five
     recorded ``torch.cuda.Event(enable_timing=True)`` objects; the library re-records them at the pass
     boundaries (flce_fwd_bwd_timed) for per-kernel timing; only with the default options.
     """
@@ -162,13 +171,20 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     gb = o.get("grad_bias") if (need_grad_W and bias is not None) else None
     lt = o.get("loss_per_token")
     ent = o.get("entropy") if want_entropy else None
-    need = workspace_size(BT, H, V)
+    if sort_vocab:
+        if o.get("logit_avg") is None:
+            o["logit_avg"] = torch.empty(V, dtype=torch.float32, device=dev)
+        if o.get("vocab_order") is None:
+            o["vocab_order"] = torch.empty(V, dtype=torch.int32, device=dev)
+    la = o.get("logit_avg") if sort_vocab else None
+    vo = o.get("vocab_order") if sort_vocab else None
+    need = workspace_size(BT, H, V, sort_vocab=sort_vocab)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     args = (_ptr(hidden), _ptr(W), _ptr(bias), _ptr(target), BT, H, V, ignore_index, red, float(z_loss),
             _ptr(o["loss"]), _ptr(gi), _ptr(gw), _ptr(gb), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel())
     plain = (red != 2 and grad_scale == 1.0 and grad_loss_per_token is None and not accumulate and lt is None
-             and ent is None and filter_eps == 0.0)
+             and ent is None and filter_eps == 0.0 and not sort_vocab)
     if pass_events is not None:
         if not plain:
             raise ValueError("pass_events only with the default options")
@@ -180,10 +196,14 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
         check(load().flce_fwd_bwd(*args, _stream_ptr(stream)))
     else:
         opts = FwdBwdOptions(float(grad_scale), _ptr(grad_loss_per_token), _ptr(lt), 1 if accumulate else 0, _ptr(ent),
-                             float(filter_eps))
+                             float(filter_eps), 1 if sort_vocab else 0, _ptr(la), _ptr(vo))
         check(load().flce_fwd_bwd_ex(*args, ctypes.byref(opts), _stream_ptr(stream)))
-    return dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, loss_per_token=lt,
-                entropy=ent, workspace=workspace)
+    res = dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, loss_per_token=lt,
+               entropy=ent, workspace=workspace)
+    if sort_vocab:
+        res["logit_avg"] = la
+        res["vocab_order"] = vo
+    return res
 
 
 def _ce_dtype(t) -> int:

@@ -99,6 +99,13 @@ size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V) {
   return flce::fused_workspace_bytes(BT, V);
 }
 
+size_t flce_workspace_size_ex(int64_t BT, int64_t H, int64_t V, const flce_fwd_bwd_options* options) {
+  if (BT < 0 || H < 0 || V < 0) return 0;
+  size_t n = flce::fused_workspace_bytes(BT, V);
+  if (options != nullptr && options->sort_vocab != 0) n += flce::vocab_sort_workspace_bytes(BT, H, V);
+  return n;
+}
+
 static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const float* bias, const int64_t* target,
                                 int64_t BT, int64_t H, int64_t V, int64_t ignore_index, int reduction, float z_loss,
                                 float* loss, uint16_t* grad_input, float* grad_W, float* grad_bias, int64_t* n_valid,
@@ -106,7 +113,7 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
                                 void* stream, void* const* events, int n_events) {
   g_last_error[0] = '\0';
   const flce_fwd_bwd_options opt =
-      options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0, nullptr, 0.0f};
+      options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0, nullptr, 0.0f, 0, nullptr, nullptr};
   if (n_events != 0 && (n_events != 5 || events == nullptr)) {
     set_error("n_events must be 0 or 5 (with a non-NULL event array)");
     return FLCE_ERR_INVALID_ARG;
@@ -137,6 +144,10 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
     set_error("filter_eps must be finite and >= 0");
     return FLCE_ERR_INVALID_ARG;
   }
+  if (opt.sort_vocab == 0 && (opt.logit_avg != nullptr || opt.vocab_order != nullptr)) {
+    set_error("logit_avg and vocab_order are outputs of the vocabulary sort (set sort_vocab)");
+    return FLCE_ERR_INVALID_ARG;
+  }
   if (bias == nullptr && grad_bias != nullptr) {
     set_error("grad_bias requires a bias");
     return FLCE_ERR_INVALID_ARG;
@@ -154,11 +165,12 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(grad_input, 16) || !aligned(grad_W, 16) ||
       !aligned(workspace, 256) || !aligned(bias, 4) || !aligned(grad_bias, 4) || !aligned(loss, 4) ||
       !aligned(target, 8) || !aligned(n_valid, 8) || !aligned(opt.loss_per_token, 4) ||
-      !aligned(opt.grad_loss_per_token, 4) || !aligned(opt.entropy, 4)) {
+      !aligned(opt.grad_loss_per_token, 4) || !aligned(opt.entropy, 4) || !aligned(opt.logit_avg, 4) ||
+      !aligned(opt.vocab_order, 4)) {
     set_error("misaligned pointer (hidden, W, grad_input, grad_W need 16 bytes; workspace 256)");
     return FLCE_ERR_MISALIGNED;
   }
-  const size_t need = flce_workspace_size(BT, H, V);
+  const size_t need = flce_workspace_size_ex(BT, H, V, &opt);
   if (workspace_bytes < need) {
     set_error("workspace has %zu bytes, needs %zu", workspace_bytes, need);
     return FLCE_ERR_WORKSPACE_TOO_SMALL;
@@ -189,6 +201,9 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   a.accumulate = opt.accumulate != 0;
   a.entropy = opt.entropy;
   a.filter_eps = opt.filter_eps;
+  a.sort_vocab = opt.sort_vocab != 0;
+  a.logit_avg_out = opt.logit_avg;
+  a.vocab_order_out = opt.vocab_order;
   char err[256] = "";
   const cudaError_t e = flce::launch_fused(a, workspace, num_sms, static_cast<cudaStream_t>(stream), err, sizeof(err),
                                            n_events ? reinterpret_cast<cudaEvent_t const*>(events) : nullptr);

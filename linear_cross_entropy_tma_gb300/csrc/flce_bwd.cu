@@ -15,10 +15,11 @@
 //     column block j is computed once, by pair (j mod P):
 //       GEMM1   S[256, 256] = rows[256, H] . cols[256, H]^T          (TMEM, 256 columns)
 //       epi     dS = f(S, statistics) in registers -> bf16 in shared memory, in the 128-byte-swizzled
-//               K-major layout of the next MMA's A operand; each epilogue warp copies its 32 rows
-//               with cp.async.bulk into the same buffer of the other P-1 pairs' CTAs (distributed
-//               shared memory, never HBM).  (Stores by the threads themselves, st.shared::cluster,
-//               measured about four times slower.)
+//               K-major layout of the next MMA's A operand; each epilogue warp hands its 32 rows to
+//               the same buffer of the other P-1 pairs' CTAs, either by cp.async.bulk copies between
+//               shared memories or through a 64 KiB per-SM staging block in L2 (a bulk store, then
+//               one multicast bulk load); never through HBM.  (Stores by the threads themselves,
+//               st.shared::cluster, measured about four times slower.)
 //     and every pair accumulates its own H chunk:
 //       GEMM2   O[256, 256] += dS[256, 256] . cols[256, chunk]      (TMEM, 256 columns, fp32)
 //     So the logits of each (row block, column block) are computed ceil(H / (256 P)) times instead of
@@ -51,6 +52,15 @@ constexpr int kMaxPairs = 4;                  // pairs per cluster that share ea
 // Order of a step's tensor work: 0 = GEMM2 half 0, half 1, then the GEMM1 share; 1 = the GEMM1 share
 // first; 2 = GEMM2 half 0, half of the share, GEMM2 half 1, the rest of the share.
 constexpr int kStepOrder = 0;
+// Hand-over of dS to the other pairs, per 128-column half (bit h of the mask of the grad_input pass,
+// resp. the grad_W pass): set = bulk store of the owner's rows to a per-SM staging block in L2, then one
+// multicast bulk load into the other pairs' CTAs; clear = shared-memory to shared-memory bulk copies
+// (also the fallback of a CTA whose SM id is past the staging table).
+// Measured on the 65535 x 1024 x 176245 workload: L2 for half 0 costs the grad_input pass ~3.5 ms (its
+// hand-over window is shorter than the store + load latency), half 1 is neutral there and saves ~0.6 ms
+// in the grad_W pass (fewer bulk copies competing with the operand loads).
+constexpr int kDsL2HalvesInput = 0;
+constexpr int kDsL2HalvesVocab = 2;
 constexpr uint32_t kBox = kTileM * kBK * 2;   // 16 KiB: a 128-row x 64-column bf16 box
 constexpr uint32_t kStage = 2 * kBox;
 constexpr uint32_t kHalfBytes = 2 * kBox;     // one 128-column half of a dS block (per CTA)
@@ -104,6 +114,7 @@ template <bool kVocabRows>
 constexpr size_t pair_smem_bytes() { return sizeof(PairSmem<kVocabRows>) + 1024; }
 static_assert(pair_smem_bytes<false>() <= 232448, "shared memory budget of one CTA exceeded");
 static_assert(pair_smem_bytes<true>() <= 232448, "shared memory budget of one CTA exceeded");
+static_assert(kDsBytes == kDsL2SlotBytes, "an L2 staging block holds one CTA's dS block");
 
 struct PairParams {
   const float* bias;
@@ -115,6 +126,8 @@ struct PairParams {
   int accumulate;
   float filter_eps;         // > 0: skip GEMM2 of dS halves whose entries are all below it
   uint32_t* skip_count;     // halves skipped (filter statistics)
+  uint8_t* ds_l2;           // per-SM dS staging blocks (kDsL2Slots x kDsL2SlotBytes), or null
+  const int32_t* row_perm;  // grad_W pass: output row of each vocabulary row (vocabulary sort), or null
   int BT, V, H;
   int n_rows, n_cols, num_kb;
   int P;                    // pairs per cluster
@@ -528,6 +541,14 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
     }
     float gbias = 0.f;
     bool ok = true;
+    // this CTA's L2 staging block for the dS it hands to the other pairs (null: shared-memory copies)
+    uint8_t* l2_stage = nullptr;
+    if (((kVocabRows ? kDsL2HalvesVocab : kDsL2HalvesInput) >> hh) & 1) {
+      if (P > 1 && p.ds_l2 != nullptr) {
+        const uint32_t sid = sm_id();
+        if (sid < static_cast<uint32_t>(kDsL2Slots)) l2_stage = p.ds_l2 + static_cast<size_t>(sid) * kDsL2SlotBytes;
+      }
+    }
     uint8_t* const ds_row = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(rl) * 128u;
     if (filt) {
       // O starts at zero (GEMM2 then always accumulates, whichever halves are skipped): this warp's 32
@@ -610,7 +631,7 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && l2_stage == nullptr) {
         // this warp's 32 rows of both 64-column boxes to the other pairs' CTAs with the same rows
         uint8_t* const src = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
         for (int pp = 0; pp < P; ++pp) {
@@ -637,6 +658,24 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           }
         }
         mbar_arrive_cluster(ds_full_c);
+      }
+      if (l2_stage != nullptr && lane == 0) {
+        // this warp's 32 rows of both 64-column boxes through L2: store, wait until the writes are done,
+        // then one multicast load into the other pairs' CTAs with the same rows (completing on their
+        // rx_full[hh]).  The staging block is rewritten only for this CTA's next block, after every pair
+        // has finished GEMM2 with this one (ds_free), so after these loads have landed.
+        const uint32_t off = static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
+        uint8_t* const src = sm.ds + off;
+        bulk_store_1d(l2_stage + off, src, 4096u);
+        bulk_store_1d(l2_stage + off + kBox, src + kBox, 4096u);
+        bulk_commit_group();
+        bulk_wait_group_all();
+        fence_proxy_async_global();
+        uint16_t mask = 0;
+        for (int pp = 0; pp < P; ++pp)
+          if (pp != pr) mask |= static_cast<uint16_t>(1u << (2 * pp + static_cast<int>(q)));
+        bulk_load_1d_multicast(src, l2_stage + off, 4096u, &sm.rx_full[hh], mask);
+        bulk_load_1d_multicast(src + kBox, l2_stage + off + kBox, 4096u, &sm.rx_full[hh], mask);
       }
     }
 
@@ -673,7 +712,8 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           }
         } else {
           if (row < p.V && p.grad_W != nullptr) {
-            float* out = p.grad_W + static_cast<size_t>(row) * p.H + h0 + cb;
+            const int orow = p.row_perm != nullptr ? p.row_perm[row] : row;
+            float* out = p.grad_W + static_cast<size_t>(orow) * p.H + h0 + cb;
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
               if (cb + 4 * g4 + 4 <= hc) {
@@ -709,7 +749,8 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
     if (row < p.V) {
       float acc = 0.f;
       for (int pp = 0; pp < P; ++pp) acc += sm.gb_gather[pp][rl];
-      p.grad_bias[row] = p.accumulate ? p.grad_bias[row] + acc : acc;
+      const int orow = p.row_perm != nullptr ? p.row_perm[row] : row;
+      p.grad_bias[orow] = p.accumulate ? p.grad_bias[orow] + acc : acc;
     }
   }
   if (warp == kMmaWarp) {
@@ -741,6 +782,8 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   p.accumulate = a.accumulate ? 1 : 0;
   p.filter_eps = a.filter_eps;
   p.skip_count = a.skip_count;
+  p.ds_l2 = a.ds_l2;
+  p.row_perm = a.row_perm;
   p.BT = a.BT;
   p.V = a.V;
   p.H = a.H;

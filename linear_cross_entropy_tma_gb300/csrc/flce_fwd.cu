@@ -392,11 +392,12 @@ size_t fused_workspace_bytes(int64_t BT, int64_t V) {
   off += align_up(sizeof(float4) * align_up(btp, 256), 256);
   off += align_up(sizeof(float) * btp, 256);
   off += align_up(sizeof(float) * vp, 256);
+  off += kDsL2Slots * kDsL2SlotBytes;
   return off;
 }
 
 FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
-  (void)V;
+  const size_t vp = align_up(static_cast<size_t>(V > 0 ? V : 0), 256);
   const size_t btp = align_up(static_cast<size_t>(BT > 0 ? BT : 0), kTileM);
   auto* p = static_cast<unsigned char*>(base);
   FusedWorkspace w;
@@ -417,6 +418,8 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   w.row_loss = reinterpret_cast<float*>(p + off);
   off += align_up(sizeof(float) * btp, 256);
   w.colb2 = reinterpret_cast<float*>(p + off);
+  off += align_up(sizeof(float) * vp, 256);
+  w.ds_l2 = p + off;
   return w;
 }
 

@@ -25,6 +25,11 @@ namespace flce {
 constexpr int kMaxSplits = 32;     // vocabulary splits of the LSE pass
 constexpr int kTileM = 128;        // rows of every MMA tile (tokens or vocabulary rows)
 
+// dS hand-over through L2 in the gradient passes: one 64 KiB staging block per SM id (a CTA of those
+// passes occupies its SM alone); CTAs on SM ids past the table use shared-memory copies instead.
+constexpr int kDsL2Slots = 256;
+constexpr size_t kDsL2SlotBytes = 65536;
+
 struct FusedWorkspace {
   uint32_t* status;  // header: status word
   float* scale;      // header: gradient scale G = grad_scale / max(n_valid, 1) (mean) or grad_scale
@@ -41,10 +46,27 @@ struct FusedWorkspace {
                      //   z = LSE2, w = target as int bits (-1 for ignored rows); rows past BT: (-inf, 0, 0, -1)
   float* row_loss;   // [BTp] valid * (LSE - z_y + z_loss LSE^2)
   float* colb2;      // [V rounded up to 256] bias * log2 e (0 without bias); -inf past V
+  uint8_t* ds_l2;    // [kDsL2Slots][kDsL2SlotBytes] per-SM staging of dS blocks handed to the other pairs
 };
 
 size_t fused_workspace_bytes(int64_t BT, int64_t V);
 FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V);
+
+// Scratch of the vocabulary sort (vocab_sort.cu), placed after the fused workspace when requested.
+struct VocabSortWorkspace {
+  float* col_part;      // [64][H] partial column sums of hidden
+  float* hbar;          // [H] mean of the hidden rows
+  float* logit_avg;     // [V] average logit per vocabulary entry
+  uint32_t* keys[2];    // [V] radix keys (double buffer)
+  int32_t* vals[2];     // [V] vocabulary indices (double buffer); vals[0] ends as the sorted order
+  uint32_t* hist;       // [ceil(V / 8192)][256] per-block digit counts / offsets
+  int32_t* inv;         // [V] sorted position of each vocabulary entry
+  float* bias;          // [V] bias in sorted order
+  int64_t* target;      // [BT] targets as sorted positions (-1: ignored or out of range)
+  uint16_t* W;          // [V][H] W in sorted row order
+};
+size_t vocab_sort_workspace_bytes(int64_t BT, int64_t H, int64_t V);
+VocabSortWorkspace carve_vocab_sort(void* base, int64_t BT, int64_t H, int64_t V);
 
 struct FusedArgs {
   const uint16_t* hidden;
@@ -66,7 +88,15 @@ struct FusedArgs {
   float* entropy;             // per-row entropy of softmax(z) out, or NULL
   float filter_eps;           // > 0: gradient filtering threshold
   bool accumulate;            // gradients += instead of =
+  bool sort_vocab;            // run the passes on the vocabulary sorted by average logit
+  float* logit_avg_out;       // [V] average logit per vocabulary entry out, or NULL (needs sort_vocab)
+  int32_t* vocab_order_out;   // [V] sorted order out, or NULL (needs sort_vocab)
 };
+
+// The vocabulary sort: logit_avg, the sorted order (in w.vals[0]), the sorted copies of W, the bias and
+// the targets.  Bad targets set the status bit here.
+cudaError_t launch_vocab_sort(const FusedArgs& a, const VocabSortWorkspace& w, uint32_t* status, int num_sms,
+                              cudaStream_t stream);
 
 // Arguments of the gradient passes on CTA pairs (flce_bwd.cu).
 struct DgPairArgs {
@@ -79,6 +109,8 @@ struct DgPairArgs {
   bool accumulate;
   float filter_eps;
   uint32_t* skip_count;
+  uint8_t* ds_l2;
+  const int32_t* row_perm;   // grad_W pass: output row of each (sorted) vocabulary row, or NULL
   int BT, V, H;
   uint16_t* grad_input;
   float* grad_W;

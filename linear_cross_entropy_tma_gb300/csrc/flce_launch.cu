@@ -1,6 +1,6 @@
 // flce_launch.cu -- enqueues every pass of one flce_fwd_bwd call on the caller's stream:
-//   header clear -> LSE tiles (flce_fwd.cu) -> split merge -> loss reduction
-//   -> grad_input pass -> grad_W / grad_bias pass (flce_bwd.cu)
+//   header clear -> [vocabulary sort (vocab_sort.cu)] -> LSE tiles (flce_fwd.cu) -> split merge
+//   -> loss reduction -> grad_input pass -> grad_W / grad_bias pass (flce_bwd.cu)
 // with optional caller events at the pass boundaries.  No host synchronisation, no allocation.
 #include "flce_kernels.cuh"
 
@@ -9,13 +9,34 @@ namespace flce {
 cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int num_sms, cudaStream_t stream,
                               char* err, size_t err_len, cudaEvent_t const* events);
 
-cudaError_t launch_fused(const FusedArgs& a, void* workspace, int num_sms, cudaStream_t stream, char* err,
+cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cudaStream_t stream, char* err,
                          size_t err_len, cudaEvent_t const* events) {
-  const FusedWorkspace ws = carve_workspace(workspace, a.BT, a.V);
+  const FusedWorkspace ws = carve_workspace(workspace, args.BT, args.V);
   auto mark = [&](int i) { return events != nullptr ? cudaEventRecord(events[i], stream) : cudaSuccess; };
   cudaError_t e = cudaMemsetAsync(workspace, 0, 256, stream);
   if (e != cudaSuccess) return e;
   if ((e = mark(0)) != cudaSuccess) return e;
+  FusedArgs a = args;
+  const int32_t* row_perm = nullptr;
+  if (args.sort_vocab) {
+    // every pass below runs on the sorted vocabulary (sorted W, bias and targets, ignore index -1); the
+    // grad_W pass maps its rows back to the caller's order
+    const VocabSortWorkspace vs = carve_vocab_sort(
+        static_cast<unsigned char*>(workspace) + fused_workspace_bytes(args.BT, args.V), args.BT, args.H, args.V);
+    if ((e = launch_vocab_sort(args, vs, ws.status, num_sms, stream)) != cudaSuccess) return e;
+    const size_t vb = sizeof(float) * static_cast<size_t>(args.V);
+    if (args.logit_avg_out != nullptr &&
+        (e = cudaMemcpyAsync(args.logit_avg_out, vs.logit_avg, vb, cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
+      return e;
+    if (args.vocab_order_out != nullptr &&
+        (e = cudaMemcpyAsync(args.vocab_order_out, vs.vals[0], vb, cudaMemcpyDeviceToDevice, stream)) != cudaSuccess)
+      return e;
+    a.W = vs.W;
+    a.bias = args.bias != nullptr ? vs.bias : nullptr;
+    a.target = vs.target;
+    a.ignore_index = -1;
+    row_perm = vs.vals[0];
+  }
   if ((e = launch_lse_passes(a, ws, num_sms, stream, err, err_len, events)) != cudaSuccess) return e;
   if ((e = mark(2)) != cudaSuccess) return e;
 
@@ -41,6 +62,8 @@ cudaError_t launch_fused(const FusedArgs& a, void* workspace, int num_sms, cudaS
   pa.accumulate = a.accumulate;
   pa.filter_eps = a.filter_eps;
   pa.skip_count = ws.skipped;
+  pa.ds_l2 = ws.ds_l2;
+  pa.row_perm = row_perm;
   pa.BT = static_cast<int>(a.BT);
   pa.V = static_cast<int>(a.V);
   pa.H = static_cast<int>(a.H);

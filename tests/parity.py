@@ -38,6 +38,17 @@ def assert_grad_close(got, ref, name: str) -> None:
     assert frob <= GRAD_FROB, f"{name}: relative Frobenius error {frob:.3e} > {GRAD_FROB}"
 
 
+def assert_within_bound(got, ref, bound, name: str) -> None:
+    """The gradient bars applied to the error left after subtracting a per-element allowance (the
+    gradient filter's bound): max(|got - ref| - bound, 0)."""
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    excess = np.maximum(np.abs(g - r) - bound, 0.0)
+    maxref = float(np.max(np.abs(r)))
+    assert float(np.max(excess)) <= GRAD_MAXABS * maxref, f"{name}: error beyond the filter bound"
+    assert float(np.linalg.norm(excess)) <= GRAD_FROB * float(np.linalg.norm(r)), f"{name}: Frobenius"
+
+
 def bf16_tensor(bits: np.ndarray, device="cuda"):
     """uint16 bf16 bit patterns -> torch bfloat16 tensor on the device (bit-exact)."""
     import torch

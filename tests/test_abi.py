@@ -51,6 +51,14 @@ def test_workspace_sizes(lib):
     assert lib.flce_workspace_size(65535, 1024, 176245) == lib.flce_workspace_size(65535, 64, 176245)
     assert lib.flce_workspace_size(65535, 64, 176245) - lib.flce_workspace_size(65535, 64, 8) == 4 * (176384 - 256)
     assert lib.ce_workspace_size(8192, 128256) == 256 + 16 * 8192
+    # the vocabulary sort adds a sorted copy of W (V x H bf16) and O(V + BT + H) scratch
+    plain = _lib.FwdBwdOptions(1.0, None, None, 0, None, 0.0, 0, None, None)
+    sort = _lib.FwdBwdOptions(1.0, None, None, 0, None, 0.0, 1, None, None)
+    assert lib.flce_workspace_size_ex(128, 64, 512, None) == a
+    assert lib.flce_workspace_size_ex(128, 64, 512, ctypes.byref(plain)) == a
+    extra = lib.flce_workspace_size_ex(65535, 1024, 176245, ctypes.byref(sort)) - b
+    assert 176245 * 1024 * 2 <= extra < 176245 * 1024 * 2 + 16 * 1024 * 1024
+    assert lib.flce_workspace_size_ex(-1, 64, 512, ctypes.byref(sort)) == 0
 
 
 def _fwd(lib, hidden=0x1000, W=0x2000, bias=None, target=0x3000, BT=128, H=64, V=512, red=0, loss=0x4000,
@@ -76,10 +84,11 @@ def test_fwd_bwd_argument_errors(lib):
     assert b"workspace" in lib.flce_last_error()
 
 
-def _fwd_ex(lib, red=2, loss=None, grad_scale=1.0, gtok=None, ltok=None, acc=0, gi=0x5000, ent=None, eps=0.0):
-    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent, eps)
+def _fwd_ex(lib, red=2, loss=None, grad_scale=1.0, gtok=None, ltok=None, acc=0, gi=0x5000, ent=None, eps=0.0,
+            sort=0, la=None, vo=None, wsb=1 << 30):
+    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent, eps, sort, la, vo)
     return lib.flce_fwd_bwd_ex(0x1000, 0x2000, None, 0x3000, 128, 64, 512, -100, red, 0.0, loss, gi, 0x6000, None,
-                               None, 0x7000, 1 << 30, ctypes.byref(opts), None)
+                               None, 0x7000, wsb, ctypes.byref(opts), None)
 
 
 def test_fwd_bwd_ex_argument_errors(lib):
@@ -93,6 +102,13 @@ def test_fwd_bwd_ex_argument_errors(lib):
     assert _fwd_ex(lib, ltok=0x9002) == MISALIGNED
     assert _fwd_ex(lib, gtok=0x9001) == MISALIGNED
     assert _fwd_ex(lib, ent=0x9003) == MISALIGNED
+    # the vocabulary sort: its outputs need sort_vocab, 4-byte alignment and the larger workspace
+    assert _fwd_ex(lib, la=0xC000) == INVALID_ARG
+    assert _fwd_ex(lib, vo=0xD000) == INVALID_ARG
+    assert _fwd_ex(lib, sort=1, la=0xC002) == MISALIGNED
+    assert _fwd_ex(lib, sort=1, vo=0xD001) == MISALIGNED
+    assert _fwd_ex(lib, sort=1, wsb=lib.flce_workspace_size(128, 64, 512)) == WS_SMALL
+    assert _fwd_ex(lib, sort=1, la=0xC000, vo=0xD000, eps=1e-3) == NO_DEVICE
     # valid argument sets get as far as the device check (no GPU here)
     assert _fwd_ex(lib) == NO_DEVICE
     assert _fwd_ex(lib, gtok=0x9000, ltok=0xA000, acc=1, grad_scale=-2.0) == NO_DEVICE
