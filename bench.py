@@ -262,6 +262,23 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
         filt = {"filter_eps": filter_eps, "ms_per_step": f_ms, "tokens_per_s": world * w.BT / (f_ms * 1e-3),
                 "skipped_dS_blocks": skips, "skipped_fraction": skips / halves,
                 "note": "CCE-style gradient filtering; error bound in include/flce.h; not the headline"}
+        # the same with the vocabulary sorted by average logit first (its own workspace: + a sorted W)
+        ws_sort = torch.empty(flce.workspace_size(w.BT, w.H, w.V, sort_vocab=True), dtype=torch.uint8, device=dev)
+        kw_sort = dict(kw, workspace=ws_sort)
+        for _ in range(warmup):
+            flce.flce_fwd_bwd(hidden, W, target, filter_eps=filter_eps, sort_vocab=True, **kw_sort)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(steps):
+            flce.flce_fwd_bwd(hidden, W, target, filter_eps=filter_eps, sort_vocab=True, **kw_sort)
+        b.record()
+        torch.cuda.synchronize()
+        s_ms = a.elapsed_time(b) / steps
+        s_skips = flce.read_filter_skips(ws_sort)
+        filt["with_vocab_sort"] = {"ms_per_step": s_ms, "tokens_per_s": world * w.BT / (s_ms * 1e-3),
+                                   "skipped_dS_blocks": s_skips, "skipped_fraction": s_skips / halves,
+                                   "workspace_bytes": ws_sort.numel()}
+        del ws_sort
     return dict(elapsed_ms=elapsed_ms, passes=passes, clocks=clocks, peak_mem=peak_mem, loss=loss, e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, workspace_bytes=ws.numel(), filter=filt)
 

@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kColSplits = 64;        // row splits of the hidden column sum
 constexpr int kSortThreads = 1024;
-constexpr int kSortChunk = 8 * kSortThreads;   // keys per block of the radix passes
+constexpr int kSortChunk = 2 * kSortThreads;   // keys per block of the radix passes
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -45,13 +45,21 @@ __global__ void __launch_bounds__(256) hidden_colsum_kernel(const uint16_t* __re
   const int r_end = min(BT, r_begin + rows_per);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (c0 < H) {
-    for (int r = r_begin + warp; r < r_end; r += 8) {
-      const uint4 v = *reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(r) * H + c0);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    // four rows per warp in flight, accumulated in row order
+    for (int r = r_begin + warp; r < r_end; r += 32) {
+      uint4 v[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc[2 * e] += bf16_to_f32(static_cast<uint16_t>(w[e] & 0xFFFFu));
-        acc[2 * e + 1] += bf16_to_f32(static_cast<uint16_t>(w[e] >> 16));
+      for (int u = 0; u < 4; ++u)
+        v[u] = r + 8 * u < r_end ? *reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(r + 8 * u) * H + c0)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * e] += bf16_to_f32(static_cast<uint16_t>(w[e] & 0xFFFFu));
+          acc[2 * e + 1] += bf16_to_f32(static_cast<uint16_t>(w[e] >> 16));
+        }
       }
     }
   }
@@ -88,16 +96,24 @@ __global__ void __launch_bounds__(256) logit_avg_kernel(const uint16_t* __restri
   for (int n = blockIdx.x * warps + warp; n < V; n += gridDim.x * warps) {
     const uint16_t* row = W + static_cast<size_t>(n) * H;
     float s = 0.f;
-    for (int c = lane * 8; c < H; c += 256) {
-      const uint4 v = *reinterpret_cast<const uint4*>(row + c);
-      const float4 h0 = __ldg(reinterpret_cast<const float4*>(hbar + c));
-      const float4 h1 = __ldg(reinterpret_cast<const float4*>(hbar + c + 4));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      const float hb[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    // four 16-byte pieces of the row per lane in flight
+    for (int c = lane * 8; c < H; c += 1024) {
+      uint4 v[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        s = fmaf(bf16_to_f32(static_cast<uint16_t>(w[e] & 0xFFFFu)), hb[2 * e], s);
-        s = fmaf(bf16_to_f32(static_cast<uint16_t>(w[e] >> 16)), hb[2 * e + 1], s);
+      for (int u = 0; u < 4; ++u)
+        v[u] = c + 256 * u < H ? *reinterpret_cast<const uint4*>(row + c + 256 * u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c + 256 * u >= H) break;
+        const float4 h0 = __ldg(reinterpret_cast<const float4*>(hbar + c + 256 * u));
+        const float4 h1 = __ldg(reinterpret_cast<const float4*>(hbar + c + 256 * u + 4));
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const float hb[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s = fmaf(bf16_to_f32(static_cast<uint16_t>(w[e] & 0xFFFFu)), hb[2 * e], s);
+          s = fmaf(bf16_to_f32(static_cast<uint16_t>(w[e] >> 16)), hb[2 * e + 1], s);
+        }
       }
     }
 #pragma unroll
@@ -215,7 +231,16 @@ __global__ void __launch_bounds__(256) vocab_gather_kernel(const uint16_t* __res
     }
     const uint4* from = reinterpret_cast<const uint4*>(W + static_cast<size_t>(src) * H);
     uint4* to = reinterpret_cast<uint4*>(W_s + static_cast<size_t>(i) * H);
-    for (int c = lane; c < H / 8; c += 32) to[c] = from[c];
+    const int n16 = H / 8;
+    for (int c = lane; c < n16; c += 128) {
+      uint4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < n16) t[u] = from[c + 32 * u];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c + 32 * u < n16) to[c + 32 * u] = t[u];
+    }
     if (lane == 0) {
       if (bias != nullptr) bias_s[i] = bias[src];
       inv[src] = i;
