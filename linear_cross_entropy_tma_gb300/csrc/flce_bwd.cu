@@ -49,6 +49,11 @@ constexpr int kPN = 256;                      // logits tile columns = K of GEMM
 constexpr int kBK = 64;
 constexpr int kHc = 256;                      // H columns per pair (GEMM2 N)
 constexpr int kMaxPairs = 4;                  // pairs per cluster that share each logits tile
+// Gradient filter: ring of per-block skip verdicts.  The owner of block b publishes them once the logits
+// of b are complete, which (in the issue order below) is after every pair finished GEMM2 of block
+// b - P - 2, so a ring of more than P + 2 blocks is never overwritten before every CTA has read it.
+constexpr int kFlagRing = 8;
+static_assert(kFlagRing >= kMaxPairs + 2, "the skip-verdict ring must outlast P + 2 blocks");
 // Order of a step's tensor work: 0 = GEMM2 half 0, half 1, then the GEMM1 share; 1 = the GEMM1 share
 // first; 2 = GEMM2 half 0, half of the share, GEMM2 half 1, the rest of the share.
 constexpr int kStepOrder = 0;
@@ -103,9 +108,8 @@ struct PairSmem {
   uint64_t o_full;
   uint64_t o_zero;
   uint64_t drain;
-  uint32_t skip_mail[2];      // filter: skip flag of the half received into this CTA's slot
-  uint32_t skip_pair[2][2];   // filter, pair leader: [half][CTA of the pair] skip flags of the current block
-  float wmax[2][4];           // filter: per warp, 1 when every dS entry of its rows in the half is small
+  uint64_t flag_full[kFlagRing][2];   // filter: the 8 owner warps' verdicts of [block mod ring][half] are in
+  uint32_t skipf[kFlagRing][2][8];    // filter: [block mod ring][half][4 x owner CTA + warp] 1 = all small
   uint32_t tmem_base;
   int abort;
   float half_bias[kTileM];
@@ -115,6 +119,20 @@ constexpr size_t pair_smem_bytes() { return sizeof(PairSmem<kVocabRows>) + 1024;
 static_assert(pair_smem_bytes<false>() <= 232448, "shared memory budget of one CTA exceeded");
 static_assert(pair_smem_bytes<true>() <= 232448, "shared memory budget of one CTA exceeded");
 static_assert(kDsBytes == kDsL2SlotBytes, "an L2 staging block holds one CTA's dS block");
+
+// Gradient filter: the verdict on half `half` of block j, once the 8 epilogue warps of its owner pair that
+// hold the half (4 per CTA) have published theirs: 1 = every pair skips it (no operand stage, no MMA, no
+// dS hand-over), 0 = keep, -1 = the bounded wait gave up.
+template <bool kVocabRows>
+__device__ __forceinline__ int filter_verdict(PairSmem<kVocabRows>& sm, int j, int half, volatile int* abort) {
+  const int r = j % kFlagRing;
+  if (!mbar_wait_cluster(&sm.flag_full[r][half], static_cast<uint32_t>(j / kFlagRing) & 1u, abort)) return -1;
+  const volatile uint32_t* f = sm.skipf[r][half];
+  uint32_t all = 1u;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) all &= f[w];
+  return all != 0u ? 1 : 0;
+}
 
 struct PairParams {
   const float* bias;
@@ -283,8 +301,11 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       mbar_init(&sm.st_empty[b], kEpiWarps);
       mbar_init(&sm.ds_full[b], 2);
       mbar_init(&sm.ds_free[b], static_cast<uint32_t>(P));
-      // with the filter, the owner also arrives (after writing the half's skip flag)
-      mbar_init(&sm.rx_full[b], filt ? 2 : 1);
+      mbar_init(&sm.rx_full[b], 1);
+    }
+    if (filt) {
+      for (int r = 0; r < kFlagRing; ++r)
+        for (int b = 0; b < 2; ++b) mbar_init(&sm.flag_full[r][b], 8);
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_empty, 2 * kEpiWarps);
@@ -322,6 +343,14 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       };
       auto load_gemm2 = [&](int j, int half) {
         if (!ok || j < 0) return;
+        if (filt) {
+          const int verdict = filter_verdict(sm, j, half, abort);
+          if (verdict < 0) {
+            ok = false;
+            return;
+          }
+          if (verdict == 1) return;   // skipped by every pair: no operand stage
+        }
         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
           ok = false;
           return;
@@ -406,31 +435,39 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           }
         }
         {
+          // (also for a skipped half: its slot may be rewritten only after anything sent into it landed)
           if (!mbar_wait_cluster(&sm.ds_full[half], static_cast<uint32_t>(j) & 1u, abort)) {
             ok = false;
             return;
           }
-          if (!mbar_wait(&sm.full[stage], phase, abort)) {
-            ok = false;
-            return;
+          bool skip = false;
+          if (filt) {
+            const int verdict = filter_verdict(sm, j, half, abort);
+            if (verdict < 0) {
+              ok = false;
+              return;
+            }
+            skip = verdict == 1;
           }
-          tc_fence_after();
-          const volatile uint32_t* sp = sm.skip_pair[half];
-          const bool skip = filt && sp[0] != 0u && sp[1] != 0u;
-          const uint32_t a_base = smem_u32(sm.ds) + static_cast<uint32_t>(half) * kHalfBytes;
-          const uint32_t b_base = smem_u32(sm.stage[stage]);
           if (!skip) {
+            if (!mbar_wait(&sm.full[stage], phase, abort)) {
+              ok = false;
+              return;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sm.ds) + static_cast<uint32_t>(half) * kHalfBytes;
+            const uint32_t b_base = smem_u32(sm.stage[stage]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint64_t ad = sdesc_sw128(a_base + (k >> 2) * kBox + 32u * (k & 3), 16u, 1024u);
               const uint64_t bd = sdesc_sw128(b_base + 2048u * k, kBox, 1024u);
               mma_bf16_ss_pair(tmem + kTmemO, ad, bd, idesc2, (filt || (j | half | k) != 0) ? 1u : 0u);
             }
+            mma_commit_mc(&sm.empty[stage], pair_mask);
+            advance();
           } else if (p.skip_count != nullptr) {
             atomicAdd(p.skip_count, 1u);
           }
-          mma_commit_mc(&sm.empty[stage], pair_mask);
-          advance();
           if (j + 1 < nt) mma_commit_mc(&sm.ds_free[half], next_owner);
         }
       };
@@ -498,11 +535,6 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           if (!mbar_wait_cluster(&sm.rx_full[half], static_cast<uint32_t>(v) & 1u, abort)) {
             ok = false;
             break;
-          }
-          if (filt) {
-            // the owner's skip flag for this half, on to the pair leader's table
-            const uint32_t f = *reinterpret_cast<volatile uint32_t*>(&sm.skip_mail[half]);
-            st_shared_cluster_u32(mapa_shared(smem_u32(&sm.skip_pair[half][q]), lead_rank), f);
           }
           mbar_arrive_cluster(half ? ds_full_c1 : ds_full_c0);
         }
@@ -607,8 +639,18 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
 #pragma unroll
         for (int i2 = 0; i2 < 32; ++i2) pk1[i2] = pack_bf16x2(__uint_as_float(rb[2 * i2]), __uint_as_float(rb[2 * i2 + 1]));
         if (filt) {
+          // this warp's verdict on its 32 rows of half hh of block j, published at once to every CTA of the
+          // cluster: their producers and MMA threads skip the half when all 8 owner warps say "small"
           const bool all_small = __all_sync(0xffffffffu, small);
-          if (lane == 0) sm.wmax[hh][qq] = all_small ? 1.f : 0.f;
+          if (lane == 0) {
+            const int r = j % kFlagRing;
+            const int slot = 4 * static_cast<int>(q) + qq;
+            for (int c = 0; c < 2 * P; ++c) {
+              st_shared_cluster_u32(mapa_shared(smem_u32(&sm.skipf[r][hh][slot]), static_cast<uint32_t>(c)),
+                                    all_small ? 1u : 0u);
+              mbar_arrive_cluster(mapa_shared(smem_u32(&sm.flag_full[r][hh]), static_cast<uint32_t>(c)));
+            }
+          }
         }
       }
       // every pair must be done with block j-1 in this half slot before it is overwritten here and
@@ -631,6 +673,11 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
       }
       fence_proxy_async_smem();
       __syncwarp();
+      // with the filter, a half every pair skips is not sent: the other pairs' receivers get its byte count
+      // as a bare transaction completion (after the slot wait above, so blocks still complete in order).
+      // A verdict wait that gave up sends the data (the kernel is winding down by then).
+      bool send = true;
+      if (filt && lane == 0) send = filter_verdict(sm, j, hh, abort) != 1;
       if (lane == 0 && l2_stage == nullptr) {
         // this warp's 32 rows of both 64-column boxes to the other pairs' CTAs with the same rows
         uint8_t* const src = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
@@ -638,28 +685,23 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
           if (pp == pr) continue;
           const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
           const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[hh]), dst_rank);
-          bulk_copy_to_peer(mapa_shared(smem_u32(src), dst_rank), src, 4096u, bar);
-          bulk_copy_to_peer(mapa_shared(smem_u32(src + kBox), dst_rank), src + kBox, 4096u, bar);
+          if (send) {
+            bulk_copy_to_peer(mapa_shared(smem_u32(src), dst_rank), src, 4096u, bar);
+            bulk_copy_to_peer(mapa_shared(smem_u32(src + kBox), dst_rank), src + kBox, 4096u, bar);
+          } else {
+            mbar_complete_tx_cluster(bar, 2u * 4096u);
+          }
         }
       }
       named_barrier_sync(1 + hh, 4 * 32);
-      if (qq == 0 && lane == 0) {
-        if (filt) {
-          // the half is skipped by every pair when both CTAs of the owner pair find all of their dS below
-          // the threshold; this CTA's flag goes to its pair leader and to the other pairs' CTAs
-          const uint32_t f = (sm.wmax[hh][0] != 0.f && sm.wmax[hh][1] != 0.f && sm.wmax[hh][2] != 0.f &&
-                              sm.wmax[hh][3] != 0.f) ? 1u : 0u;
-          st_shared_cluster_u32(mapa_shared(smem_u32(&sm.skip_pair[hh][q]), lead_rank), f);
-          for (int pp = 0; pp < P; ++pp) {
-            if (pp == pr) continue;
-            const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
-            st_shared_cluster_u32(mapa_shared(smem_u32(&sm.skip_mail[hh]), dst_rank), f);
-            mbar_arrive_cluster(mapa_shared(smem_u32(&sm.rx_full[hh]), dst_rank));
-          }
+      if (qq == 0 && lane == 0) mbar_arrive_cluster(ds_full_c);
+      if (l2_stage != nullptr && lane == 0 && !send) {
+        for (int pp = 0; pp < P; ++pp) {
+          if (pp == pr) continue;
+          mbar_complete_tx_cluster(mapa_shared(smem_u32(&sm.rx_full[hh]), static_cast<uint32_t>(2 * pp) + q), 2u * 4096u);
         }
-        mbar_arrive_cluster(ds_full_c);
       }
-      if (l2_stage != nullptr && lane == 0) {
+      if (l2_stage != nullptr && lane == 0 && send) {
         // this warp's 32 rows of both 64-column boxes through L2: store, wait until the writes are done,
         // then one multicast load into the other pairs' CTAs with the same rows (completing on their
         // rx_full[hh]).  The staging block is rewritten only for this CTA's next block, after every pair
