@@ -115,7 +115,9 @@ flce_status flce_fwd_bwd(const uint16_t* hidden, const uint16_t* W, const float*
  *   events[0] before the LSE pass        events[1] after the LSE tile kernel
  *   events[2] after the merge + loss reduction
  *   events[3] after the grad_input pass  events[4] after the grad_W pass
- * (a skipped pass records its two events back to back).  n_events must be 0 or 5; events may be
+ * (a skipped pass records its two events back to back; when both gradient passes run as one launch,
+ * which they do whenever both are requested and have the same cluster shape, events[3] is recorded
+ * together with events[4], after that launch).  n_events must be 0 or 5; events may be
  * NULL when n_events is 0.  The events are owned by the caller (cudaEvent_t handles).
  */
 flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const float* bias,

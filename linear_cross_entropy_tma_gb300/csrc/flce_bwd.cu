@@ -265,10 +265,12 @@ __device__ __forceinline__ bool filter_small_row(const uint32_t (&r)[64], const 
 
 // kFilter: the gradient-filtering variant (a separate instantiation, so the exact path carries none of
 // its checks).
+// One cluster's work: rows [256 row_pair, +256) (128 per CTA of each pair) and the H chunks of
+// group hgroup (P consecutive 256-wide chunks, one per pair).
 template <bool kVocabRows, bool kFilter>
-__global__ void __launch_bounds__(kThreads, 1)
-dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
-                  const PairParams p, uint32_t* __restrict__ status) {
+__device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols,
+                                                const PairParams& p, uint32_t* __restrict__ status, int row_pair,
+                                                int hgroup) {
   constexpr int kStages = PairCfg<kVocabRows>::kStages;
   extern __shared__ uint8_t smem_raw[];
   PairSmem<kVocabRows>& sm =
@@ -282,8 +284,8 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
   const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pr));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int r0 = (blockIdx.x / (2 * P)) * (2 * kTileM) + static_cast<int>(q) * kTileM;
-  const int h0 = (blockIdx.y * P + pr) * kHc;
+  const int r0 = row_pair * (2 * kTileM) + static_cast<int>(q) * kTileM;
+  const int h0 = (hgroup * P + pr) * kHc;
   const int hc = min(kHc, p.H - h0);
   const uint32_t n2 = hc > 128 ? 256u : 128u;   // GEMM2 N; columns past H are zero-filled by TMA
   const int nbox2 = static_cast<int>(n2) / 128; // 64-column boxes per CTA per GEMM2 stage
@@ -785,7 +787,7 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
 
   tc_fence_before();
   cluster_sync();
-  if (kVocabRows && pr == 0 && warp < 4 && blockIdx.y == 0 && p.grad_bias != nullptr && !sm.abort) {
+  if (kVocabRows && pr == 0 && warp < 4 && hgroup == 0 && p.grad_bias != nullptr && !sm.abort) {
     const int rl = warp * 32 + lane;
     const int row = r0 + rl;
     if (row < p.V) {
@@ -802,6 +804,32 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
   if (threadIdx.x == 0 && sm.abort) atomicOr(status, kStatusTimeout);
 }
 
+// One gradient pass: cluster (blockIdx.x / 2P, blockIdx.y).
+template <bool kVocabRows, bool kFilter>
+__global__ void __launch_bounds__(kThreads, 1)
+dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
+                  const PairParams p, uint32_t* __restrict__ status) {
+  dgrad_pair_body<kVocabRows, kFilter>(tm_rows, tm_cols, p, status, static_cast<int>(blockIdx.x) / (2 * p.P),
+                                       static_cast<int>(blockIdx.y));
+}
+
+// Both gradient passes in one grid, so that the grad_W pass's clusters take the SMs the grad_input pass's
+// last wave leaves idle: clusters 0 .. n_in-1 (in the grad_input pass's own order, row pairs fastest) run
+// the grad_input pass, the rest the grad_W pass.  Both passes have the same number of pairs per cluster.
+template <bool kFilter>
+__global__ void __launch_bounds__(kThreads, 1)
+dgrad_both_kernel(const __grid_constant__ CUtensorMap tm_hidden, const __grid_constant__ CUtensorMap tm_w,
+                  const PairParams p_in, const PairParams p_w, uint32_t* __restrict__ status, int n_in,
+                  int in_row_pairs, int w_row_pairs) {
+  const int c = static_cast<int>(blockIdx.x) / (2 * p_in.P);
+  if (c < n_in) {
+    dgrad_pair_body<false, kFilter>(tm_hidden, tm_w, p_in, status, c % in_row_pairs, c / in_row_pairs);
+  } else {
+    const int cw = c - n_in;
+    dgrad_pair_body<true, kFilter>(tm_w, tm_hidden, p_w, status, cw % w_row_pairs, cw / w_row_pairs);
+  }
+}
+
 // Pairs per cluster: 2 when the number of 256-wide H chunks is even, else 3 when it divides, else 1.
 int pairs_per_cluster(int h_chunks) {
   if (h_chunks % 2 == 0) return 2;
@@ -809,11 +837,9 @@ int pairs_per_cluster(int h_chunks) {
   return 1;
 }
 
-}  // namespace
-
+// Kernel parameters of one pass; h_chunks receives the number of 256-wide H chunks it covers.
 template <bool kVocabRows>
-cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, const DgPairArgs& a,
-                              cudaStream_t stream) {
+PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
   PairParams p{};
   p.bias = a.bias;
   p.stats = a.stats;
@@ -836,26 +862,68 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   p.grad_W = a.grad_W;
   p.grad_bias = a.grad_bias;
   // with only grad_bias requested one H chunk suffices (the GEMM2 result is not stored)
-  const int h_chunks = (kVocabRows && p.grad_W == nullptr) ? 1 : (p.H + kHc - 1) / kHc;
-  p.P = pairs_per_cluster(h_chunks);
-  constexpr size_t smem = pair_smem_bytes<kVocabRows>();
-  auto kern = p.filter_eps > 0.f ? dgrad_pair_kernel<kVocabRows, true> : dgrad_pair_kernel<kVocabRows, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  const int row_pairs = (p.n_rows + 2 * kTileM - 1) / (2 * kTileM);
+  *h_chunks = (kVocabRows && p.grad_W == nullptr) ? 1 : (p.H + kHc - 1) / kHc;
+  p.P = pairs_per_cluster(*h_chunks);
+  return p;
+}
+
+int row_pairs_of(const PairParams& p) { return (p.n_rows + 2 * kTileM - 1) / (2 * kTileM); }
+
+cudaLaunchConfig_t cluster_config(dim3 grid, size_t smem, int P, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * p.P * row_pairs, h_chunks / p.P, 1);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2 * p.P;
+  attr[0].val.clusterDim.x = 2 * P;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cfg;
+}
+
+}  // namespace
+
+template <bool kVocabRows>
+cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, const DgPairArgs& a,
+                              cudaStream_t stream) {
+  int h_chunks = 0;
+  const PairParams p = make_pair_params<kVocabRows>(a, &h_chunks);
+  constexpr size_t smem = pair_smem_bytes<kVocabRows>();
+  auto kern = p.filter_eps > 0.f ? dgrad_pair_kernel<kVocabRows, true> : dgrad_pair_kernel<kVocabRows, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * row_pairs_of(p), h_chunks / p.P, 1), smem, p.P, stream, attr);
   e = cudaLaunchKernelEx(&cfg, kern, rows, cols, p, a.status);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dgrad_both(const CUtensorMap& hidden_map, const CUtensorMap& w_map, const DgPairArgs& a,
+                              cudaStream_t stream) {
+  int hc_in = 0, hc_w = 0;
+  const PairParams p_in = make_pair_params<false>(a, &hc_in);
+  const PairParams p_w = make_pair_params<true>(a, &hc_w);
+  if (p_in.P != p_w.P) {
+    // different cluster shapes: two launches
+    cudaError_t e = launch_dgrad_pair<false>(hidden_map, w_map, a, stream);
+    if (e != cudaSuccess) return e;
+    return launch_dgrad_pair<true>(w_map, hidden_map, a, stream);
+  }
+  constexpr size_t smem = pair_smem_bytes<false>() > pair_smem_bytes<true>() ? pair_smem_bytes<false>()
+                                                                               : pair_smem_bytes<true>();
+  auto kern = a.filter_eps > 0.f ? dgrad_both_kernel<true> : dgrad_both_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int in_rp = row_pairs_of(p_in), w_rp = row_pairs_of(p_w);
+  const int n_in = in_rp * (hc_in / p_in.P);
+  const int n_w = w_rp * (hc_w / p_w.P);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p_in.P * (n_in + n_w), 1, 1), smem, p_in.P, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, kern, hidden_map, w_map, p_in, p_w, a.status, n_in, in_rp, w_rp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

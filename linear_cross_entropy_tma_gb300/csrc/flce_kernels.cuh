@@ -125,6 +125,12 @@ template <bool kVocabRows>
 cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, const DgPairArgs& a,
                               cudaStream_t stream);
 
+// Both gradient passes, as one launch when they have the same cluster shape (the grad_W pass's clusters
+// then fill the SMs the grad_input pass's last wave leaves idle), else as two.  hidden_map / w_map: the
+// 128-row x 64-column box maps of hidden and W.
+cudaError_t launch_dgrad_both(const CUtensorMap& hidden_map, const CUtensorMap& w_map, const DgPairArgs& a,
+                              cudaStream_t stream);
+
 // Encodes a 2-D bf16 tensor map (rows x cols, row-major) with a box of box_rows x 64 columns and
 // 128-byte swizzle.  Returns false (and fills err) when the driver refuses the descriptor.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,

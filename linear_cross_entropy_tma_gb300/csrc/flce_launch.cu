@@ -76,6 +76,12 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     if (!make_tmap_bf16(&tm_h128, a.hidden, a.BT, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;
     if (!make_tmap_bf16(&tm_w128, a.W, a.V, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;
   }
+  if (a.grad_input != nullptr && want_dw) {
+    // both passes in one launch; caller events 3 and 4 are both recorded after it
+    if ((e = launch_dgrad_both(tm_h128, tm_w128, pa, stream)) != cudaSuccess) return e;
+    if ((e = mark(3)) != cudaSuccess) return e;
+    return mark(4);
+  }
   if (a.grad_input != nullptr) {
     if ((e = launch_dgrad_pair<false>(tm_h128, tm_w128, pa, stream)) != cudaSuccess) return e;
   }
