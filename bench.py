@@ -279,7 +279,7 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
         if end_ev is not None:
             end_ev.record(s_out)
 
-    e2e_steps = max(3, min(steps, 5))
+    e2e_steps = max(3, min(steps, 10))
     e2e_serial(1)
     e2e_pipelined(2)
     torch.cuda.synchronize()

@@ -164,6 +164,28 @@ def test_flce_output_subsets(flce):
     assert_grad_close(gb.cpu().numpy(), ref["grad_bias"], "grad_bias only")
 
 
+def test_flce_grad_input_and_bias_without_grad_W(flce):
+    # grad_W NULL with a bias: the grad_W pass covers one H chunk (one pair per cluster) while the
+    # grad_input pass at H = 512 has two, so the two passes run as separate launches
+    import torch
+    from linear_cross_entropy_tma_gb300 import _lib
+    d = _synthetic(300, 512, 1500, True, 1e-4, "mean", ignore=(5, 299), seed=13)
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], z_loss=1e-4)
+    hidden, W, target, bias = _upload(d)
+    loss = torch.empty(1, device="cuda")
+    gi = torch.empty((300, 512), dtype=torch.bfloat16, device="cuda")
+    gb = torch.empty(1500, device="cuda")
+    ws = torch.empty(_lib.workspace_size(300, 512, 1500), dtype=torch.uint8, device="cuda")
+    _lib.check(_lib.load().flce_fwd_bwd(hidden.data_ptr(), W.data_ptr(), bias.data_ptr(), target.data_ptr(), 300, 512,
+                                        1500, -100, 0, 1e-4, loss.data_ptr(), gi.data_ptr(), None, gb.data_ptr(), None,
+                                        ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert flce.read_device_status(ws) == 0
+    assert_scalar_close(loss.item(), ref["loss"], "loss")
+    assert_grad_close(bf16_to_numpy_f32(gi), ref["grad_input"], "grad_input")
+    assert_grad_close(gb.cpu().numpy(), ref["grad_bias"], "grad_bias")
+
+
 @functools.lru_cache(maxsize=1)
 def _full_inputs(key):
     return wl.make_fused_inputs(wl.FUSED_WORKLOADS[key])
