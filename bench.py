@@ -35,6 +35,9 @@ from linear_cross_entropy_tma_gb300 import workloads as wl  # noqa: E402
 # Cross-Entropy", "Putting numbers on it") -> 65535 / 0.356 s tokens/s.  Another machine: context only.
 PAGES_TOKENS_PER_S = {"long": 65535 / 0.356}
 KERNELS_PER_STEP = 5  # lse_partial, lse_merge, loss_reduce, dgrad(grad_input), dgrad(grad_W); the two dgrad passes are one launch when both run
+# online flow: bias table, count, grad_input pass with the LSE, loss reduction, four gated classic kernels
+# (launched, exit at once unless the online pass asked for them), grad_W pass
+KERNELS_PER_STEP_ONLINE = 9
 
 
 def load_peaks():
@@ -471,20 +474,28 @@ def main():
     ms = r["elapsed_ms"] / args.steps
     value = world * w.BT / (ms * 1e-3)
     passes = r["passes"]
-    # the library runs both gradient passes as one launch when both are requested (the grad_W event is
-    # then recorded right after the grad_input one): report that launch as one kernel
-    merged = passes["dgrad_grad_W"] < 0.01 * passes["dgrad_grad_input"]
+    # which flow ran: the online one (no LSE tile pass: its first interval holds two small kernels) or the
+    # classic one; in the classic flow both gradient passes are one launch when both run (the grad_W event
+    # is then recorded right after the grad_input one): report that launch as one kernel
+    online = passes["lse_partial"] < 0.01 * sum(passes.values())
+    merged = not online and passes["dgrad_grad_W"] < 0.01 * passes["dgrad_grad_input"]
+    if online:
+        passes = {"online_prep": passes["lse_partial"], "dgrad_grad_input_online": passes["lse_merge+loss_reduce"],
+                  "loss_reduce+gated_classic": passes["dgrad_grad_input"], "dgrad_grad_W": passes["dgrad_grad_W"]}
     if merged:
         passes = {"lse_partial": passes["lse_partial"], "lse_merge+loss_reduce": passes["lse_merge+loss_reduce"],
                   "dgrad_both_passes": passes["dgrad_grad_input"] + passes["dgrad_grad_W"]}
-    tensor_kernels = [k for k in ("lse_partial", "dgrad_grad_input", "dgrad_grad_W", "dgrad_both_passes") if k in passes]
+    tensor_kernels = [k for k in ("lse_partial", "dgrad_grad_input", "dgrad_grad_W", "dgrad_both_passes",
+                                  "dgrad_grad_input_online") if k in passes]
     dominant = max(tensor_kernels, key=lambda k: passes[k])
     # algorithmic work per launch of each tensor-core kernel: logits 2*BT*V*H; each gradient pass
     # recomputes the logits (2*BT*V*H) and runs its GEMM (2*BT*V*H)
     alg = {"lse_partial": 2 * w.BT * w.V * w.H, "dgrad_grad_input": 4 * w.BT * w.V * w.H,
-           "dgrad_grad_W": 4 * w.BT * w.V * w.H, "dgrad_both_passes": 8 * w.BT * w.V * w.H}
+           "dgrad_grad_W": 4 * w.BT * w.V * w.H, "dgrad_both_passes": 8 * w.BT * w.V * w.H,
+           "dgrad_grad_input_online": 4 * w.BT * w.V * w.H}
     kname = {"lse_partial": "lse_pair_kernel", "dgrad_grad_input": "dgrad_pair_kernel<false>",
-             "dgrad_grad_W": "dgrad_pair_kernel<true>", "dgrad_both_passes": "dgrad_both_kernel"}
+             "dgrad_grad_W": "dgrad_pair_kernel<true>", "dgrad_both_passes": "dgrad_both_kernel",
+             "dgrad_grad_input_online": "dgrad_online_kernel"}
     src = kernel_source_digest(["flce_fwd.cu", "flce_bwd.cu", "sm100.cuh"])
     peak_tf = peaks["bf16_tflops_sustained"]
     achieved = alg[dominant] / (passes[dominant] * 1e-3) / 1e12
@@ -504,7 +515,8 @@ def main():
                           "frac_of_sustained": step_tflops / peak_tf, "frac_of_burst": step_tflops / peaks["bf16_tflops"],
                           "convention": "8*BT*V*H per fused forward+backward"},
         "pass_ms": passes,
-        "gpu_launches": (KERNELS_PER_STEP - 1 if merged else KERNELS_PER_STEP) * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP_ONLINE if online else KERNELS_PER_STEP - 1 if merged else KERNELS_PER_STEP)
+                        * args.steps,
         "clocks": r["clocks"],
         "e2e": {"value": world * w.BT / (r["e2e_ms"] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],

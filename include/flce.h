@@ -169,6 +169,13 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *   logit_avg            [V] fp32, device, or NULL: receives logit_avg (requires sort_vocab).
  *   vocab_order          [V] int32, device, or NULL: receives the sorted order, entry k = the vocabulary
  *                        index at sorted position k (requires sort_vocab).
+ *   separate_lse_pass    non-zero: compute every row's LSE in a pass of its own before the gradient passes
+ *                        (the two-pass scheme of "Cut Cross Entropy visualized", "Backward pass").  By
+ *                        default, when grad_input is requested without accumulate, filter_eps or entropy,
+ *                        the grad_input pass finds the LSE itself (online softmax against a per-row
+ *                        reference, "Fused Linear Cross-Entropy", "Strategy 2"), one GEMM over the logits
+ *                        fewer; rows whose sums leave that pass's safe range make the call redo the work
+ *                        with the separate pass, on the device.  Both give the same results up to rounding.
  */
 typedef struct flce_fwd_bwd_options {
   float grad_scale;
@@ -180,6 +187,7 @@ typedef struct flce_fwd_bwd_options {
   int sort_vocab;
   float* logit_avg;
   int32_t* vocab_order;
+  int separate_lse_pass;
 } flce_fwd_bwd_options;
 
 /* Bytes of workspace flce_fwd_bwd_ex needs with these options (NULL: flce_workspace_size). */

@@ -33,7 +33,8 @@ class FwdBwdOptions(ctypes.Structure):
     """flce_fwd_bwd_options of include/flce.h."""
     _fields_ = [("grad_scale", ctypes.c_float), ("grad_loss_per_token", c_p), ("loss_per_token", c_p),
                 ("accumulate", ctypes.c_int), ("entropy", c_p), ("filter_eps", ctypes.c_float),
-                ("sort_vocab", ctypes.c_int), ("logit_avg", c_p), ("vocab_order", c_p)]
+                ("sort_vocab", ctypes.c_int), ("logit_avg", c_p), ("vocab_order", c_p),
+                ("separate_lse_pass", ctypes.c_int)]
 
 
 def load() -> ctypes.CDLL:
@@ -95,7 +96,7 @@ def workspace_size(BT: int, H: int, V: int, sort_vocab: bool = False) -> int:
     """Workspace bytes of flce_fwd_bwd; with ``sort_vocab`` those of the vocabulary-sorting call."""
     if not sort_vocab:
         return int(load().flce_workspace_size(BT, H, V))
-    opts = FwdBwdOptions(1.0, None, None, 0, None, 0.0, 1, None, None)
+    opts = FwdBwdOptions(1.0, None, None, 0, None, 0.0, 1, None, None, 0)
     return int(load().flce_workspace_size_ex(BT, H, V, ctypes.byref(opts)))
 
 
@@ -113,7 +114,7 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
                  z_loss: float = 0.0, need_grad_input: bool = True, need_grad_W: bool = True, workspace=None,
                  out=None, stream=None, pass_events=None, grad_scale: float = 1.0, grad_loss_per_token=None,
                  accumulate: bool = False, want_loss_per_token: bool = False, want_entropy: bool = False,
-                 filter_eps: float = 0.0, sort_vocab: bool = False) -> dict:
+                 filter_eps: float = 0.0, sort_vocab: bool = False, separate_lse_pass: bool = False) -> dict:
     """Fused linear cross-entropy forward + backward on the current CUDA device.
 
     hidden [BT, H] bf16, W [V, H] bf16, target [BT] int64, bias [V] fp32 or None.  Returns a dict with
@@ -129,7 +130,8 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     tensors given in ``out`` instead of overwriting them; ``filter_eps`` > 0 turns on gradient filtering
     (GEMM2 of dS blocks whose entries are all below it is skipped; see include/flce.h for the error
     bound); ``sort_vocab`` runs every pass on the vocabulary sorted by average logit (adds ``logit_avg``,
-    fp32 [V], and ``vocab_order``, int32 [V], to the result) (flce_fwd_bwd_ex).  ``pass_events``: five
+    fp32 [V], and ``vocab_order``, int32 [V], to the result); ``separate_lse_pass`` computes the LSE in a
+    pass of its own first instead of inside the grad_input pass (flce_fwd_bwd_ex).  ``pass_events``: five
     recorded ``torch.cuda.Event(enable_timing=True)`` objects; the library re-records them at the pass
     boundaries (flce_fwd_bwd_timed) for per-kernel timing; only with the default options.
     """
@@ -184,7 +186,7 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     args = (_ptr(hidden), _ptr(W), _ptr(bias), _ptr(target), BT, H, V, ignore_index, red, float(z_loss),
             _ptr(o["loss"]), _ptr(gi), _ptr(gw), _ptr(gb), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel())
     plain = (red != 2 and grad_scale == 1.0 and grad_loss_per_token is None and not accumulate and lt is None
-             and ent is None and filter_eps == 0.0 and not sort_vocab)
+             and ent is None and filter_eps == 0.0 and not sort_vocab and not separate_lse_pass)
     if pass_events is not None:
         if not plain:
             raise ValueError("pass_events only with the default options")
@@ -196,7 +198,8 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
         check(load().flce_fwd_bwd(*args, _stream_ptr(stream)))
     else:
         opts = FwdBwdOptions(float(grad_scale), _ptr(grad_loss_per_token), _ptr(lt), 1 if accumulate else 0, _ptr(ent),
-                             float(filter_eps), 1 if sort_vocab else 0, _ptr(la), _ptr(vo))
+                             float(filter_eps), 1 if sort_vocab else 0, _ptr(la), _ptr(vo),
+                             1 if separate_lse_pass else 0)
         check(load().flce_fwd_bwd_ex(*args, ctypes.byref(opts), _stream_ptr(stream)))
     res = dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, loss_per_token=lt,
                entropy=ent, workspace=workspace)

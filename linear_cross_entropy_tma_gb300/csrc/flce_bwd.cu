@@ -108,6 +108,8 @@ struct PairSmem {
   uint64_t o_full;
   uint64_t o_zero;
   uint64_t drain;
+  uint64_t mref_ready;        // online grad_input pass: the per-row reference is in
+  uint64_t part_ready;        // online grad_input pass: every pair's per-row partial sums are in
   uint64_t flag_full[kFlagRing][2];   // filter: the 8 owner warps' verdicts of [block mod ring][half] are in
   uint32_t skipf[kFlagRing][2][8];    // filter: [block mod ring][half][4 x owner CTA + warp] 1 = all small
   uint32_t tmem_base;
@@ -152,6 +154,19 @@ struct PairParams {
   uint16_t* grad_input;
   float* grad_W;
   float* grad_bias;
+  const uint32_t* gate;     // non-null: the launch does nothing unless *gate != 0
+  // grad_input pass without a prior LSE pass (online softmax against a fixed per-row reference)
+  const int64_t* target;
+  int64_t ignore_index;
+  const float* grad_tok;    // per-token upstream gradient, or null (ones)
+  const uint16_t* Wmat;     // W, for the target-row term
+  float* mref_g;            // [BT rounded up to 256] per-row reference, log2 units
+  float2* part_g;           // [BT rounded up to 256][kMaxPairs][2]: (sum of 2^(x - ref), z_y or -inf)
+  float4* stats_out;        // per-token statistics for the grad_W pass
+  float* row_loss;
+  float* loss_tok;
+  uint32_t* zf_neg_out;
+  uint32_t* fallback;       // set when a row's sum left the safe range: the classic passes redo the work
 };
 
 // The block whose GEMM1 pair `pr` works on in step s (the one it owns in [s+P+1, s+2P]) and which
@@ -263,15 +278,59 @@ __device__ __forceinline__ bool filter_small_row(const uint32_t (&r)[64], const 
   return worst <= eps * fabsf(rc.coef);
 }
 
+// Online grad_input pass: 64 consecutive logits of one row (fp32 bits in) -> 2^(S log2 e + b log2 e - ref)
+// (fp32 bits out), with c = -ref, and their sum added to lsum; the target column's logit (+ bias) goes to
+// zy and its entry to 0 (its gradient term is added exactly at the end; it stays in the sum).
+__device__ __forceinline__ void online_chunk64(uint32_t (&r)[64], int col0, float c, bool plain,
+                                               const float* __restrict__ colb2, const float* __restrict__ bias, int y,
+                                               float& lsum, float& zy) {
+  const bool has_y = static_cast<unsigned>(y - col0) < 64u;
+  if (has_y) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (col0 + i == y) zy = __uint_as_float(r[i]) + (bias != nullptr ? __ldg(bias + y) : 0.f);
+  }
+  float sum = 0.f;
+  if (plain) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float v = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, c));
+      r[i] = __float_as_uint(v);
+      sum += v;
+    }
+  } else {
+#pragma unroll
+    for (int i4 = 0; i4 < 16; ++i4) {
+      const float4 b = __ldg(reinterpret_cast<const float4*>(colb2 + col0) + i4);
+      const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float v = ex2_approx(fmaf(__uint_as_float(r[4 * i4 + k]), kLog2e, c + bb[k]));
+        r[4 * i4 + k] = __float_as_uint(v);
+        sum += v;
+      }
+    }
+  }
+  if (has_y) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (col0 + i == y) r[i] = 0u;
+  }
+  lsum += sum;
+}
+
 // kFilter: the gradient-filtering variant (a separate instantiation, so the exact path carries none of
 // its checks).
 // One cluster's work: rows [256 row_pair, +256) (128 per CTA of each pair) and the H chunks of
 // group hgroup (P consecutive 256-wide chunks, one per pair).
-template <bool kVocabRows, bool kFilter>
+template <bool kVocabRows, bool kFilter, bool kOnline = false>
 __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols,
                                                 const PairParams& p, uint32_t* __restrict__ status, int row_pair,
                                                 int hgroup) {
+  static_assert(!kOnline || (!kVocabRows && !kFilter), "the online form is a grad_input pass without the filter");
   constexpr int kStages = PairCfg<kVocabRows>::kStages;
+  // the classic passes behind an online grad_input pass run only when it asked for them
+  if (p.gate != nullptr && *reinterpret_cast<const volatile uint32_t*>(p.gate) == 0u) return;
   extern __shared__ uint8_t smem_raw[];
   PairSmem<kVocabRows>& sm =
       *reinterpret_cast<PairSmem<kVocabRows>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -314,6 +373,10 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.o_zero, 2 * kEpiWarps);
     mbar_init(&sm.drain, 1);
+    if (kOnline) {
+      mbar_init(&sm.mref_ready, 4);       // the 4 warps of pair 0's CTA with these rows that hold half 0
+      mbar_init(&sm.part_ready, 8 * P);   // the 8 epilogue warps of every pair's CTA with these rows
+    }
     sm.abort = 0;
     fence_mbarrier_init();
   }
@@ -556,10 +619,20 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     // evaluated as 2^(S log2 e + c) with c = log2(s f) - LSE2 + b log2 e gathered per row or column.
     // When some valid row has f <= 0 (LSE <= -1/(2 z_loss)) the log form does not apply and every tile
     // takes the general form, with f and the onehot weight as separate factors.
-    const bool general = (*p.zf_neg != 0u);
+    const bool general = !kOnline && (*p.zf_neg != 0u);
     const float log2s = log2f(scale);
     DsRow rc{-INFINITY, 0.f, 0.f, 0.f, 0.f, scale, 2.0f * p.z_loss * kLn2, -1};
-    if (!kVocabRows) {
+    // online form: no statistics yet; this row's target and upstream gradient, its reference (from the first
+    // block, once pair 0 has published it), and the running sum / target logit of the columns it owns
+    float on_ref = 0.f, on_lsum = 0.f, on_zy = -INFINITY, on_u = 0.f;
+    bool on_have_ref = false;
+    if (kOnline) {
+      if (row < p.BT) {
+        const int64_t y = p.target[row];
+        rc.y = (y != p.ignore_index && y >= 0 && y < p.V) ? static_cast<int>(y) : -1;
+        on_u = p.grad_tok != nullptr ? p.grad_tok[row] : 1.0f;
+      }
+    } else if (!kVocabRows) {
       if (row < p.BT) {
         const float4 st = p.stats[row];
         rc.c = st.x + log2s;
@@ -622,6 +695,29 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(s_empty_c);
+        if (kOnline && !on_have_ref) {
+          if (pr == 0 && j == 0 && hh == 0) {
+            // the row's reference: its largest logit (+ bias) among the first 128 columns of block 0, in log2
+            // units (the same number in every pair, so their accumulators share one scale)
+            float m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              m = fmaxf(m, fmaf(__uint_as_float(ra[i]), kLog2e, __ldg(p.colb2 + col0 + i)));
+              m = fmaxf(m, fmaf(__uint_as_float(rb[i]), kLog2e, __ldg(p.colb2 + col0 + 64 + i)));
+            }
+            p.mref_g[row] = m;
+            __syncwarp();
+            if (lane == 0)
+              for (int pp = 0; pp < P; ++pp)
+                mbar_arrive_cluster(mapa_shared(smem_u32(&sm.mref_ready), static_cast<uint32_t>(2 * pp) + q));
+          }
+          if (!mbar_wait_cluster(&sm.mref_ready, 0, abort)) {
+            ok = false;
+            break;
+          }
+          on_ref = __ldcg(p.mref_g + row);
+          on_have_ref = true;
+        }
         // with the filter: is every entry of this row's half small, |dS| <= eps |w| with w the entry's
         // gradient weight (the row's for grad_input, the token column's for grad_W), i.e. the unscaled
         // p f - onehot below eps?  (fp32, before rounding; zero-weight entries are zero and count as small)
@@ -629,13 +725,20 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         int over = 0;
         const float fge = (kVocabRows && filt) ? p.filter_eps * fabsf(scale) : 0.f;
         int* const fov = (kVocabRows && filt) ? &over : nullptr;
-        ds_chunk64<kVocabRows>(ra, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gbias,
-                               fge, fov);
+        if (kOnline)
+          online_chunk64(ra, col0, -on_ref, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, p.bias, rc.y, on_lsum, on_zy);
+        else
+          ds_chunk64<kVocabRows>(ra, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gbias,
+                                 fge, fov);
         if (!kVocabRows && filt) small = filter_small_row(ra, rc, p.filter_eps);
 #pragma unroll
         for (int i2 = 0; i2 < 32; ++i2) pk0[i2] = pack_bf16x2(__uint_as_float(ra[2 * i2]), __uint_as_float(ra[2 * i2 + 1]));
-        ds_chunk64<kVocabRows>(rb, col0 + 64, rc, general, p.bias == nullptr && col0 + 128 <= p.V, p.colb2,
-                               tstats + 64, gbias, fge, fov);
+        if (kOnline)
+          online_chunk64(rb, col0 + 64, -on_ref, p.bias == nullptr && col0 + 128 <= p.V, p.colb2, p.bias, rc.y,
+                         on_lsum, on_zy);
+        else
+          ds_chunk64<kVocabRows>(rb, col0 + 64, rc, general, p.bias == nullptr && col0 + 128 <= p.V, p.colb2,
+                                 tstats + 64, gbias, fge, fov);
         if (!kVocabRows && filt) small = filter_small_row(rb, rc, p.filter_eps) && small;
         if (kVocabRows && filt) small = (over == 0);
 #pragma unroll
@@ -723,6 +826,60 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
     }
 
+    // online form: every pair's partial sums of this row combined, the row's statistics for the grad_W pass
+    // and loss, and the two coefficients of grad_input[row] = c1 O[row] + c2 W[y]:
+    //   L = sum_n 2^(z_n log2 e - ref), LSE = (ref + log2 L) ln 2, f = 1 + 2 z_loss LSE,
+    //   c1 = G u f / L (O holds sum over n != y of 2^(..) W[n]),  c2 = G u (f p_y - 1)
+    float on_c1 = 0.f, on_c2 = 0.f;
+    if (kOnline) {
+      if (ok && !on_have_ref) {
+        // a pair that owned no block still needs the reference
+        if (!mbar_wait_cluster(&sm.mref_ready, 0, abort)) {
+          ok = false;
+        } else {
+          on_ref = __ldcg(p.mref_g + row);
+          on_have_ref = true;
+        }
+      }
+      if (ok) {
+        p.part_g[(static_cast<size_t>(row) * kMaxPairs + pr) * 2 + hh] = make_float2(on_lsum, on_zy);
+        __syncwarp();
+        if (lane == 0)
+          for (int pp = 0; pp < P; ++pp)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&sm.part_ready), static_cast<uint32_t>(2 * pp) + q));
+        if (!mbar_wait_cluster(&sm.part_ready, 0, abort)) ok = false;
+      }
+      if (ok) {
+        float L = 0.f, zy = -INFINITY;
+        for (int pp = 0; pp < P; ++pp)
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float2 v = __ldcg(p.part_g + (static_cast<size_t>(row) * kMaxPairs + pp) * 2 + h2);
+            L += v.x;
+            zy = fmaxf(zy, v.y);
+          }
+        const float lse2 = on_ref + log2f(L);
+        const float lse = lse2 * kLn2;
+        const bool valid = rc.y >= 0;
+        const float f = 1.0f + 2.0f * p.z_loss * lse;
+        if (valid) {
+          on_c1 = scale * on_u * f / L;
+          on_c2 = scale * on_u * (f * ex2_approx(fmaf(zy, kLog2e, -lse2)) - 1.0f);
+        }
+        if (pr == 0 && hh == 0 && row < p.BT) {
+          const float lt = valid ? (lse - zy) + p.z_loss * lse * lse : 0.f;
+          p.row_loss[row] = lt;
+          if (p.loss_tok != nullptr) p.loss_tok[row] = lt;
+          const float uf = on_u * f;
+          if (valid && on_u != 0.f && !(uf > 0.f)) atomicOr(p.zf_neg_out, 1u);
+          p.stats_out[row] = make_float4(valid && uf > 0.f ? log2f(uf) - lse2 : -INFINITY, valid ? on_u : 0.f, lse2,
+                                         __int_as_float(valid ? rc.y : -1));
+        }
+        // 2^115 leaves room for the accumulator's sums over the vocabulary; beyond it (or for a sum that is
+        // not finite) the classic passes redo the call
+        if (row < p.BT && !(L < 0x1p115f)) atomicOr(p.fallback, 1u);
+      }
+    }
+
     if (ok && mbar_wait(&sm.o_full, 0, abort)) {
       tc_fence_after();
       const int n_chunks = (hc + 31) / 32;
@@ -740,6 +897,21 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
                 float o[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(vv[8 * g8 + e]);
+                if (kOnline) {
+                  float wy[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                  if (on_c2 != 0.f) {
+                    const uint4 wv = *reinterpret_cast<const uint4*>(p.Wmat + static_cast<size_t>(rc.y) * p.H + h0 + cb +
+                                                                     8 * g8);
+                    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      wy[2 * e] = bf16_lo(ww[e]);
+                      wy[2 * e + 1] = bf16_hi(ww[e]);
+                    }
+                  }
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) o[e] = fmaf(on_c1, o[e], on_c2 * wy[e]);
+                }
                 if (p.accumulate) {
                   const uint4 old = *reinterpret_cast<const uint4*>(out + 8 * g8);
                   const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
@@ -813,6 +985,14 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
                                        static_cast<int>(blockIdx.y));
 }
 
+// The grad_input pass without a prior LSE pass: the same cluster layout as dgrad_pair_kernel<false>.
+__global__ void __launch_bounds__(kThreads, 1)
+dgrad_online_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
+                    const PairParams p, uint32_t* __restrict__ status) {
+  dgrad_pair_body<false, false, true>(tm_rows, tm_cols, p, status, static_cast<int>(blockIdx.x) / (2 * p.P),
+                                      static_cast<int>(blockIdx.y));
+}
+
 // Both gradient passes in one grid, so that the grad_W pass's clusters take the SMs the grad_input pass's
 // last wave leaves idle: clusters 0 .. n_in-1 (in the grad_input pass's own order, row pairs fastest) run
 // the grad_input pass, the rest the grad_W pass.  Both passes have the same number of pairs per cluster.
@@ -861,6 +1041,18 @@ PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
   p.grad_input = a.grad_input;
   p.grad_W = a.grad_W;
   p.grad_bias = a.grad_bias;
+  p.gate = a.gate;
+  p.target = a.target;
+  p.ignore_index = a.ignore_index;
+  p.grad_tok = a.grad_tok;
+  p.Wmat = a.Wmat;
+  p.mref_g = a.mref_g;
+  p.part_g = a.part_g;
+  p.stats_out = a.stats_out;
+  p.row_loss = a.row_loss;
+  p.loss_tok = a.loss_tok;
+  p.zf_neg_out = a.zf_neg_out;
+  p.fallback = a.fallback;
   // with only grad_bias requested one H chunk suffices (the GEMM2 result is not stored)
   *h_chunks = (kVocabRows && p.grad_W == nullptr) ? 1 : (p.H + kHc - 1) / kHc;
   p.P = pairs_per_cluster(*h_chunks);
@@ -898,6 +1090,21 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * row_pairs_of(p), h_chunks / p.P, 1), smem, p.P, stream, attr);
   e = cudaLaunchKernelEx(&cfg, kern, rows, cols, p, a.status);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap& w_map, const DgPairArgs& a,
+                                cudaStream_t stream) {
+  int h_chunks = 0;
+  const PairParams p = make_pair_params<false>(a, &h_chunks);
+  constexpr size_t smem = pair_smem_bytes<false>();
+  cudaError_t e =
+      cudaFuncSetAttribute(dgrad_online_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * row_pairs_of(p), h_chunks / p.P, 1), smem, p.P, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, dgrad_online_kernel, hidden_map, w_map, p, a.status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

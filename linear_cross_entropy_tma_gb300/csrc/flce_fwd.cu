@@ -74,7 +74,9 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constan
                 const float* __restrict__ bias, const int64_t* __restrict__ target, int BT, int V,
                 int64_t ignore_index, int num_kb, int tiles_per_split, int n_tiles, int BTp,
                 float2* __restrict__ part, float* __restrict__ part_t, float* __restrict__ zy_out,
-                uint32_t* __restrict__ status) {
+                uint32_t* __restrict__ status, const uint32_t* __restrict__ gate) {
+  // behind an online grad_input pass this launch runs only when that pass asked for it
+  if (gate != nullptr && *reinterpret_cast<const volatile uint32_t*>(gate) == 0u) return;
   extern __shared__ uint8_t smem_raw[];
   LsePairSmem& sm =
       *reinterpret_cast<LsePairSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -276,7 +278,9 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
                                  float z_loss, const float* __restrict__ bias, const float* __restrict__ grad_tok,
                                  float4* __restrict__ stats, float* __restrict__ row_loss,
                                  float* __restrict__ loss_tok, float* __restrict__ colb2,
-                                 uint32_t* __restrict__ zf_neg, uint32_t* __restrict__ status) {
+                                 uint32_t* __restrict__ zf_neg, uint32_t* __restrict__ status,
+                                 const uint32_t* __restrict__ gate) {
+  if (gate != nullptr && *reinterpret_cast<const volatile uint32_t*>(gate) == 0u) return;
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   // per-column bias in log2 units for the gradient passes; -inf masks the columns past V
   if (t < ((V + 255) & ~255)) colb2[t] = t < V ? (bias != nullptr ? bias[t] * kLog2e : 0.f) : -INFINITY;
@@ -321,7 +325,9 @@ constexpr int kReduceThreads = 1024;
 __global__ void __launch_bounds__(kReduceThreads)
 loss_reduce_kernel(const float* __restrict__ row_loss, const float4* __restrict__ stats, int BT, int reduction,
                    float grad_scale, float* __restrict__ scale_ws, int64_t* __restrict__ n_valid_ws,
-                   uint32_t* __restrict__ zf_neg, float* __restrict__ loss, int64_t* __restrict__ n_valid_out) {
+                   uint32_t* __restrict__ zf_neg, float* __restrict__ loss, int64_t* __restrict__ n_valid_out,
+                   const uint32_t* __restrict__ gate) {
+  if (gate != nullptr && *reinterpret_cast<const volatile uint32_t*>(gate) == 0u) return;
   __shared__ double s_sum[kReduceThreads / 32];
   __shared__ long long s_cnt[kReduceThreads / 32];
   double acc = 0.0;
@@ -355,6 +361,45 @@ loss_reduce_kernel(const float* __restrict__ row_loss, const float4* __restrict_
     if (!(G > 0.f)) *zf_neg |= 1u;
     *n_valid_ws = n;
     if (n_valid_out != nullptr) *n_valid_out = n;
+  }
+}
+
+// Before an online grad_input pass: the per-column bias table (as lse_merge_kernel writes it) and the
+// statistics of the padding rows past BT.
+__global__ void online_prep_kernel(const float* __restrict__ bias, int V, int BT, float* __restrict__ colb2,
+                                   float4* __restrict__ stats) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < ((V + 255) & ~255)) colb2[t] = t < V ? (bias != nullptr ? bias[t] * kLog2e : 0.f) : -INFINITY;
+  if (t >= BT && t < ((BT + 255) & ~255)) stats[t] = make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
+}
+
+// Before an online grad_input pass (one CTA): the valid count, the gradient scale G and the bad-target
+// flag, from the targets alone (the loss reduction after the pass computes the same count and G again).
+__global__ void __launch_bounds__(kReduceThreads)
+online_count_kernel(const int64_t* __restrict__ target, int BT, int V, int64_t ignore_index, int reduction,
+                    float grad_scale, float* __restrict__ scale_ws, uint32_t* __restrict__ zf_neg,
+                    uint32_t* __restrict__ status) {
+  __shared__ long long s_cnt[kReduceThreads / 32];
+  long long cnt = 0;
+  bool bad = false;
+  for (int t = threadIdx.x; t < BT; t += kReduceThreads) {
+    const int64_t y = target[t];
+    const bool valid = (y != ignore_index) && (y >= 0) && (y < V);
+    cnt += valid ? 1 : 0;
+    bad |= !valid && y != ignore_index;
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusBadTarget);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+  if ((threadIdx.x & 31) == 0) s_cnt[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long n = 0;
+    for (int w = 0; w < kReduceThreads / 32; ++w) n += s_cnt[w];
+    const double scale = (reduction == 0) ? 1.0 / static_cast<double>(n > 0 ? n : 1) : 1.0;
+    const float G = static_cast<float>(scale * static_cast<double>(grad_scale));
+    *scale_ws = G;
+    if (!(G > 0.f)) *zf_neg |= 1u;
   }
 }
 
@@ -406,6 +451,7 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   w.n_valid = reinterpret_cast<int64_t*>(p + 8);
   w.zf_neg = reinterpret_cast<uint32_t*>(p + 16);
   w.skipped = reinterpret_cast<uint32_t*>(p + 20);
+  w.fallback = reinterpret_cast<uint32_t*>(p + 24);
   size_t off = 256;
   w.part = reinterpret_cast<float2*>(p + off);
   off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
@@ -424,7 +470,7 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
 }
 
 cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int num_sms, cudaStream_t stream,
-                              char* err, size_t err_len, cudaEvent_t const* events) {
+                              char* err, size_t err_len, cudaEvent_t const* events, const uint32_t* gate) {
   const int BT = static_cast<int>(a.BT);
   const int V = static_cast<int>(a.V);
   const int BTp = static_cast<int>(align_up(static_cast<size_t>(BT), kTileM));
@@ -444,20 +490,40 @@ cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int 
     if (e != cudaSuccess) return e;
     kern<<<dim3(2 * pairs, splits), kThreads, kLsePairSmemBytes, stream>>>(
         tm_h, tm_w, a.bias, a.target, BT, V, a.ignore_index, num_kb, tps, n_tiles, BTp, ws.part, ws.part_t, ws.zy,
-        ws.status);
+        ws.status, gate);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) return e;
     const int merge_threads = max((BT + 255) & ~255, (V + 255) & ~255);
     lse_merge_kernel<<<merge_threads / 256, 256, 0, stream>>>(ws.part, ws.part_t, splits, BTp, a.entropy, ws.zy,
                                                             a.target, BT, V,
                                                             a.ignore_index, a.z_loss, a.bias, a.grad_tok, ws.stats,
-                                                            ws.row_loss, a.loss_tok, ws.colb2, ws.zf_neg, ws.status);
+                                                            ws.row_loss, a.loss_tok, ws.colb2, ws.zf_neg, ws.status,
+                                                            gate);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) {
     return e;
   }
   loss_reduce_kernel<<<1, kReduceThreads, 0, stream>>>(ws.row_loss, ws.stats, BT, a.reduction, a.grad_scale, ws.scale,
-                                                      ws.n_valid, ws.zf_neg, a.loss, a.n_valid_out);
+                                                      ws.n_valid, ws.zf_neg, a.loss, a.n_valid_out, gate);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_online_prep(const FusedArgs& a, const FusedWorkspace& ws, cudaStream_t stream) {
+  const int BT = static_cast<int>(a.BT);
+  const int V = static_cast<int>(a.V);
+  const int n = max((BT + 255) & ~255, (V + 255) & ~255);
+  online_prep_kernel<<<n / 256, 256, 0, stream>>>(a.bias, V, BT, ws.colb2, ws.stats);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  online_count_kernel<<<1, kReduceThreads, 0, stream>>>(a.target, BT, V, a.ignore_index, a.reduction, a.grad_scale,
+                                                       ws.scale, ws.zf_neg, ws.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_reduce(const FusedArgs& a, const FusedWorkspace& ws, cudaStream_t stream) {
+  loss_reduce_kernel<<<1, kReduceThreads, 0, stream>>>(ws.row_loss, ws.stats, static_cast<int>(a.BT), a.reduction,
+                                                      a.grad_scale, ws.scale, ws.n_valid, ws.zf_neg, a.loss,
+                                                      a.n_valid_out, nullptr);
   return cudaGetLastError();
 }
 

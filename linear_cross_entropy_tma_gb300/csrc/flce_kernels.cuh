@@ -35,6 +35,7 @@ struct FusedWorkspace {
   float* scale;      // header: gradient scale G = grad_scale / max(n_valid, 1) (mean) or grad_scale
   int64_t* n_valid;  // header: valid count
   uint32_t* skipped; // header: dS halves whose GEMM2 the gradient filter skipped (both passes)
+  uint32_t* fallback; // header: non-zero when the online grad_input pass handed the call to the classic passes
   uint32_t* zf_neg;  // header: non-zero when the log form of dS does not apply (some valid row has
                      // f u <= 0 with u its upstream gradient, or the gradient scale is <= 0)
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
@@ -91,6 +92,7 @@ struct FusedArgs {
   bool sort_vocab;            // run the passes on the vocabulary sorted by average logit
   float* logit_avg_out;       // [V] average logit per vocabulary entry out, or NULL (needs sort_vocab)
   int32_t* vocab_order_out;   // [V] sorted order out, or NULL (needs sort_vocab)
+  bool separate_lse;          // always the classic flow (LSE tiles first)
 };
 
 // The vocabulary sort: logit_avg, the sorted order (in w.vals[0]), the sorted copies of W, the bias and
@@ -116,6 +118,19 @@ struct DgPairArgs {
   float* grad_W;
   float* grad_bias;
   uint32_t* status;
+  const uint32_t* gate;      // non-NULL: the launch does nothing unless *gate != 0
+  // grad_input pass without a prior LSE pass (launch_dgrad_online)
+  const int64_t* target;
+  int64_t ignore_index;
+  const float* grad_tok;
+  const uint16_t* Wmat;
+  float* mref_g;             // [BT rounded up to 256]
+  float2* part_g;            // [BT rounded up to 256][4][2]
+  float4* stats_out;
+  float* row_loss;
+  float* loss_tok;
+  uint32_t* zf_neg_out;
+  uint32_t* fallback;
 };
 
 // kVocabRows = false: grad_input pass (rows = tokens, reduction over the vocabulary);
@@ -124,6 +139,14 @@ struct DgPairArgs {
 template <bool kVocabRows>
 cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, const DgPairArgs& a,
                               cudaStream_t stream);
+
+// The grad_input pass without a prior LSE pass: online softmax over the vocabulary against a fixed per-row
+// reference (the row's largest logit in the first 128 columns), which also produces the per-token
+// statistics, the loss terms and zf_neg for the grad_W pass and the loss reduction.  Needs the gradient
+// scale (ws.scale) and the bias table (colb2) in place.  Sets *fallback when some row's sum leaves the safe
+// range; the classic passes, gated on it, then redo the call.
+cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap& w_map, const DgPairArgs& a,
+                                cudaStream_t stream);
 
 // Both gradient passes, as one launch when they have the same cluster shape (the grad_W pass's clusters
 // then fill the SMs the grad_input pass's last wave leaves idle), else as two.  hidden_map / w_map: the

@@ -1,13 +1,21 @@
-// flce_launch.cu -- enqueues every pass of one flce_fwd_bwd call on the caller's stream:
-//   header clear -> [vocabulary sort (vocab_sort.cu)] -> LSE tiles (flce_fwd.cu) -> split merge
-//   -> loss reduction -> grad_input pass -> grad_W / grad_bias pass (flce_bwd.cu)
-// with optional caller events at the pass boundaries.  No host synchronisation, no allocation.
+// flce_launch.cu -- enqueues every pass of one flce_fwd_bwd call on the caller's stream, no host
+// synchronisation, no allocation, optional caller events at the pass boundaries:
+//   header clear -> [vocabulary sort (vocab_sort.cu)] -> then either
+//   online flow (grad_input requested, no accumulation, filter or entropy):
+//     bias table + valid count -> grad_input pass that also finds the LSE (flce_bwd.cu, online form)
+//     -> loss reduction -> [LSE tiles, merge, reduction, classic grad_input pass: gated, they run only when
+//     the online pass reported a row outside its safe range] -> grad_W / grad_bias pass
+//   or classic flow:
+//     LSE tiles (flce_fwd.cu) -> split merge -> loss reduction -> grad_input and grad_W passes (one launch
+//     when both run)
 #include "flce_kernels.cuh"
 
 namespace flce {
 
 cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int num_sms, cudaStream_t stream,
-                              char* err, size_t err_len, cudaEvent_t const* events);
+                              char* err, size_t err_len, cudaEvent_t const* events, const uint32_t* gate);
+cudaError_t launch_online_prep(const FusedArgs& a, const FusedWorkspace& ws, cudaStream_t stream);
+cudaError_t launch_loss_reduce(const FusedArgs& a, const FusedWorkspace& ws, cudaStream_t stream);
 
 cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cudaStream_t stream, char* err,
                          size_t err_len, cudaEvent_t const* events) {
@@ -37,21 +45,9 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     a.ignore_index = -1;
     row_perm = vs.vals[0];
   }
-  if ((e = launch_lse_passes(a, ws, num_sms, stream, err, err_len, events)) != cudaSuccess) return e;
-  if ((e = mark(2)) != cudaSuccess) return e;
-
   const bool want_dw = (a.grad_W != nullptr) || (a.grad_bias != nullptr);
-  if (a.BT == 0) {
-    // no tokens: every gradient is zero (unchanged when accumulating)
-    if (!a.accumulate && a.grad_W != nullptr &&
-        (e = cudaMemsetAsync(a.grad_W, 0, sizeof(float) * a.V * a.H, stream)) != cudaSuccess)
-      return e;
-    if (!a.accumulate && a.grad_bias != nullptr &&
-        (e = cudaMemsetAsync(a.grad_bias, 0, sizeof(float) * a.V, stream)) != cudaSuccess)
-      return e;
-    if ((e = mark(3)) != cudaSuccess) return e;
-    return mark(4);
-  }
+  const bool online = a.BT > 0 && a.grad_input != nullptr && !a.accumulate && !(a.filter_eps > 0.f) &&
+                      a.entropy == nullptr && !a.separate_lse;
   DgPairArgs pa{};
   pa.bias = a.bias;
   pa.stats = ws.stats;
@@ -71,6 +67,52 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
   pa.grad_W = a.grad_W;
   pa.grad_bias = a.grad_bias;
   pa.status = ws.status;
+  if (online) {
+    // events: 1 after the bias table and count, 2 after the online grad_input pass, 3 after the loss
+    // reduction and the gated classic passes, 4 after the grad_W pass
+    if ((e = launch_online_prep(a, ws, stream)) != cudaSuccess) return e;
+    if ((e = mark(1)) != cudaSuccess) return e;
+    CUtensorMap tm_h, tm_w;
+    if (!make_tmap_bf16(&tm_h, a.hidden, a.BT, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&tm_w, a.W, a.V, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;
+    DgPairArgs po = pa;
+    po.target = a.target;
+    po.ignore_index = a.ignore_index;
+    po.grad_tok = a.grad_tok;
+    po.Wmat = a.W;
+    po.mref_g = ws.part_t;                      // the split partials are free in this flow
+    po.part_g = ws.part;
+    po.stats_out = ws.stats;
+    po.row_loss = ws.row_loss;
+    po.loss_tok = a.loss_tok;
+    po.zf_neg_out = ws.zf_neg;
+    po.fallback = ws.fallback;
+    if ((e = launch_dgrad_online(tm_h, tm_w, po, stream)) != cudaSuccess) return e;
+    if ((e = mark(2)) != cudaSuccess) return e;
+    if ((e = launch_loss_reduce(a, ws, stream)) != cudaSuccess) return e;
+    // the classic passes, run only if the online pass set the fallback flag
+    if ((e = launch_lse_passes(a, ws, num_sms, stream, err, err_len, nullptr, ws.fallback)) != cudaSuccess) return e;
+    DgPairArgs pg = pa;
+    pg.gate = ws.fallback;
+    if ((e = launch_dgrad_pair<false>(tm_h, tm_w, pg, stream)) != cudaSuccess) return e;
+    if ((e = mark(3)) != cudaSuccess) return e;
+    if (want_dw && (e = launch_dgrad_pair<true>(tm_w, tm_h, pa, stream)) != cudaSuccess) return e;
+    return mark(4);
+  }
+  if ((e = launch_lse_passes(a, ws, num_sms, stream, err, err_len, events, nullptr)) != cudaSuccess) return e;
+  if ((e = mark(2)) != cudaSuccess) return e;
+
+  if (a.BT == 0) {
+    // no tokens: every gradient is zero (unchanged when accumulating)
+    if (!a.accumulate && a.grad_W != nullptr &&
+        (e = cudaMemsetAsync(a.grad_W, 0, sizeof(float) * a.V * a.H, stream)) != cudaSuccess)
+      return e;
+    if (!a.accumulate && a.grad_bias != nullptr &&
+        (e = cudaMemsetAsync(a.grad_bias, 0, sizeof(float) * a.V, stream)) != cudaSuccess)
+      return e;
+    if ((e = mark(3)) != cudaSuccess) return e;
+    return mark(4);
+  }
   CUtensorMap tm_h128, tm_w128;
   if (a.grad_input != nullptr || want_dw) {
     if (!make_tmap_bf16(&tm_h128, a.hidden, a.BT, a.H, kTileM, err, err_len)) return cudaErrorInvalidValue;

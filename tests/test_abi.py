@@ -52,8 +52,8 @@ def test_workspace_sizes(lib):
     assert lib.flce_workspace_size(65535, 64, 176245) - lib.flce_workspace_size(65535, 64, 8) == 4 * (176384 - 256)
     assert lib.ce_workspace_size(8192, 128256) == 256 + 16 * 8192
     # the vocabulary sort adds a sorted copy of W (V x H bf16) and O(V + BT + H) scratch
-    plain = _lib.FwdBwdOptions(1.0, None, None, 0, None, 0.0, 0, None, None)
-    sort = _lib.FwdBwdOptions(1.0, None, None, 0, None, 0.0, 1, None, None)
+    plain = _lib.FwdBwdOptions(1.0, None, None, 0, None, 0.0, 0, None, None, 0)
+    sort = _lib.FwdBwdOptions(1.0, None, None, 0, None, 0.0, 1, None, None, 0)
     assert lib.flce_workspace_size_ex(128, 64, 512, None) == a
     assert lib.flce_workspace_size_ex(128, 64, 512, ctypes.byref(plain)) == a
     extra = lib.flce_workspace_size_ex(65535, 1024, 176245, ctypes.byref(sort)) - b
@@ -86,7 +86,7 @@ def test_fwd_bwd_argument_errors(lib):
 
 def _fwd_ex(lib, red=2, loss=None, grad_scale=1.0, gtok=None, ltok=None, acc=0, gi=0x5000, ent=None, eps=0.0,
             sort=0, la=None, vo=None, wsb=1 << 30):
-    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent, eps, sort, la, vo)
+    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent, eps, sort, la, vo, 0)
     return lib.flce_fwd_bwd_ex(0x1000, 0x2000, None, 0x3000, 128, 64, 512, -100, red, 0.0, loss, gi, 0x6000, None,
                                None, 0x7000, wsb, ctypes.byref(opts), None)
 

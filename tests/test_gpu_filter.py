@@ -86,11 +86,11 @@ def test_filter_within_stated_bound(flce, name):
 def test_filter_threshold_below_every_entry_is_exact(flce):
     # a threshold below every nonzero |dS| skips only all-zero blocks (the token padding of the last
     # block of the grad_W pass: 24 halves here): the result must equal the unfiltered call bit for bit
-    # (the filtered path starts O from zeros and always accumulates)
+    # (the filtered path starts O from zeros and always accumulates; both compute the LSE in its own pass)
     import torch
     d = _inputs(260, 512, 3000, 1.0, True, 1e-4, "mean", seed=33)
     hidden, W, target, b = _upload(d)
-    a = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction="mean", z_loss=1e-4)
+    a = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction="mean", z_loss=1e-4, separate_lse_pass=True)
     c = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction="mean", z_loss=1e-4, filter_eps=1e-30)
     torch.cuda.synchronize()
     assert flce.read_filter_skips(c["workspace"]) == 24

@@ -86,11 +86,12 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("separate_lse", [False, True], ids=["lse-in-grad-input-pass", "separate-lse-pass"])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_flce_matches_oracle(flce, name):
+def test_flce_matches_oracle(flce, name, separate_lse):
     BT, H, V, bias, zl, red, ign = CASES[name]
     d = _synthetic(BT, H, V, bias, zl, red, ignore=ign, seed=BT * 7 + V)
-    out = _run(flce, d)
+    out = _run(flce, d, separate_lse_pass=separate_lse)
     assert out["status"] == 0
     _check_full(out, d)
 
@@ -103,10 +104,27 @@ def test_flce_tiny_workload(flce):
     assert ref["n_valid"] == 122
 
 
-def test_flce_peaked_logits(flce):
+@pytest.mark.parametrize("separate_lse", [False, True], ids=["lse-in-grad-input-pass", "separate-lse-pass"])
+def test_flce_peaked_logits(flce, separate_lse):
     # logits std ~8: the online max matters and the softmax is far from uniform
     d = _synthetic(200, 256, 3000, True, 1e-4, "mean", ignore=(7,), seed=3, w_std=0.5)
+    out = _run(flce, d, separate_lse_pass=separate_lse)
+    _check_full(out, d)
+
+
+def test_flce_confident_rows(flce):
+    # rows whose target holds almost all of the probability (p_y near 1): grad_input is a small difference
+    # (p_y f - 1) W_y + ...; the online pass adds the target term exactly at the end
+    d = _synthetic(260, 512, 2000, False, 0.0, "sum", ignore=(3,), seed=23, w_std=0.02)
+    W = oracle.widen(d["W"])
+    h = oracle.widen(d["hidden"])
+    for r in range(0, 260, 2):   # make half of the rows confident: hidden aligned with its target's W row
+        y = int(d["target"][r])
+        if y >= 0:
+            v = (W[y] / np.linalg.norm(W[y]) * 40.0).astype(np.float32)
+            d["hidden"][r] = wl.f32_to_bf16_bits(v)
     out = _run(flce, d)
+    assert out["status"] == 0
     _check_full(out, d)
 
 
@@ -162,6 +180,31 @@ def test_flce_output_subsets(flce):
                                         ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
     assert_grad_close(gb.cpu().numpy(), ref["grad_bias"], "grad_bias only")
+
+
+def _fallback_flag(ws) -> int:
+    # word 6 of the workspace header: set when the grad_input pass that finds the LSE itself handed the
+    # call to the classic passes
+    return int(ws[24:28].cpu().view(__import__("torch").int32).item())
+
+
+@pytest.mark.parametrize("H", [128, 512])
+def test_flce_online_fallback(flce, H):
+    # a bias of -200 on the first 128 columns puts every row's reference far below its other logits: the
+    # sums overflow the online pass's safe range, and the classic passes must produce the exact result
+    d = _synthetic(260, H, 1200, True, 1e-4, "mean", ignore=(1, 200), seed=17)
+    d["bias"] = d["bias"].copy()
+    d["bias"][:128] = -200.0
+    d["target"][d["target"] < 128] = 300
+    out = _run(flce, d)
+    assert out["status"] == 0
+    assert _fallback_flag(out["workspace"]) == 1
+    _check_full(out, d)
+    # and ordinary inputs stay on the online pass
+    d2 = _synthetic(260, H, 1200, True, 1e-4, "mean", ignore=(1, 200), seed=18)
+    out2 = _run(flce, d2)
+    assert _fallback_flag(out2["workspace"]) == 0
+    _check_full(out2, d2)
 
 
 def test_flce_grad_input_and_bias_without_grad_W(flce):
