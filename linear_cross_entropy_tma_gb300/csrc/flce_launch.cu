@@ -1,7 +1,7 @@
 // flce_launch.cu -- enqueues every pass of one flce_fwd_bwd call on the caller's stream, no host
 // synchronisation, no allocation, optional caller events at the pass boundaries:
 //   header clear -> [vocabulary sort (vocab_sort.cu)] -> then either
-//   online flow (grad_input requested, no accumulation, filter or entropy):
+//   online flow (grad_input requested, no accumulation or entropy):
 //     bias table + valid count -> grad_input pass that also finds the LSE (flce_bwd.cu, online form)
 //     -> loss reduction -> [LSE tiles, merge, reduction, classic grad_input pass: gated, they run only when
 //     the online pass reported a row outside its safe range] -> grad_W / grad_bias pass
@@ -46,8 +46,9 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     row_perm = vs.vals[0];
   }
   const bool want_dw = (a.grad_W != nullptr) || (a.grad_bias != nullptr);
-  const bool online = a.BT > 0 && a.grad_input != nullptr && !a.accumulate && !(a.filter_eps > 0.f) &&
-                      a.entropy == nullptr && !a.separate_lse;
+  // (with gradient filtering the online grad_input pass is exact and only the grad_W pass filters)
+  const bool online = a.BT > 0 && a.grad_input != nullptr && !a.accumulate && a.entropy == nullptr &&
+                      !a.separate_lse;
   DgPairArgs pa{};
   pa.bias = a.bias;
   pa.stats = ws.stats;

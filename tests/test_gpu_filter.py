@@ -53,13 +53,16 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("separate_lse", [False, True], ids=["lse-in-grad-input-pass", "separate-lse-pass"])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_filter_within_stated_bound(flce, name):
+def test_filter_within_stated_bound(flce, name, separate_lse):
+    # (by default the grad_input pass finds the LSE itself and is exact; only the grad_W pass filters)
     import torch
     BT, H, V, hs, bias, zl, red, eps, ign = CASES[name]
     d = _inputs(BT, H, V, hs, bias, zl, red, seed=BT + V, ignore=ign)
     hidden, W, target, b = _upload(d)
-    out = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction=red, z_loss=zl, filter_eps=eps)
+    out = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction=red, z_loss=zl, filter_eps=eps,
+                            separate_lse_pass=separate_lse)
     torch.cuda.synchronize()
     assert flce.read_device_status(out["workspace"]) == 0
     skips = flce.read_filter_skips(out["workspace"])
@@ -91,7 +94,8 @@ def test_filter_threshold_below_every_entry_is_exact(flce):
     d = _inputs(260, 512, 3000, 1.0, True, 1e-4, "mean", seed=33)
     hidden, W, target, b = _upload(d)
     a = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction="mean", z_loss=1e-4, separate_lse_pass=True)
-    c = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction="mean", z_loss=1e-4, filter_eps=1e-30)
+    c = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction="mean", z_loss=1e-4, filter_eps=1e-30,
+                          separate_lse_pass=True)
     torch.cuda.synchronize()
     assert flce.read_filter_skips(c["workspace"]) == 24
     assert torch.equal(a["grad_input"].view(torch.int16), c["grad_input"].view(torch.int16))

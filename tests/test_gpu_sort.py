@@ -119,8 +119,9 @@ def test_sort_raises_filter_skips(flce):
     BT, H, V, eps = 520, 512, 4096, 2.0 ** -12
     hidden, W, target, bias = _popular_case(BT, H, V, 64, seed=41)
     h, w_, t, b = _upload(hidden, W, target, bias)
-    plain = flce.flce_fwd_bwd(h, w_, t, bias=b, filter_eps=eps)
-    srt = flce.flce_fwd_bwd(h, w_, t, bias=b, filter_eps=eps, sort_vocab=True)
+    # (the separate LSE pass keeps both gradient passes filtering; by default only the grad_W pass does)
+    plain = flce.flce_fwd_bwd(h, w_, t, bias=b, filter_eps=eps, separate_lse_pass=True)
+    srt = flce.flce_fwd_bwd(h, w_, t, bias=b, filter_eps=eps, sort_vocab=True, separate_lse_pass=True)
     torch.cuda.synchronize()
     assert flce.read_device_status(srt["workspace"]) == 0
     skips_plain = flce.read_filter_skips(plain["workspace"])
