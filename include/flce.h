@@ -115,6 +115,10 @@ flce_status flce_fwd_bwd(const uint16_t* hidden, const uint16_t* W, const float*
  *   events[0] before the LSE pass        events[1] after the LSE tile kernel
  *   events[2] after the merge + loss reduction
  *   events[3] after the grad_input pass  events[4] after the grad_W pass
+ * in the classic flow; when the grad_input pass finds the LSE itself (the default whenever grad_input is
+ * requested, see flce_fwd_bwd_options.separate_lse_pass, which this call does not take):
+ *   events[1] after the bias table and the valid count   events[2] after that grad_input pass
+ *   events[3] after the loss reduction and the gated classic kernels   events[4] after the grad_W pass
  * (a skipped pass records its two events back to back; when both gradient passes run as one launch,
  * which they do whenever both are requested and have the same cluster shape, events[3] is recorded
  * together with events[4], after that launch).  n_events must be 0 or 5; events may be
