@@ -83,6 +83,9 @@ CASES = {
     "wide-H-bias": (96, 576, 513, True, 1e-4, "mean", (1, 2)),
     "V-equals-1": (130, 64, 1, True, 1e-2, "sum", (3,)),
     "many-vocab-tiles": (40, 64, 5000, False, 0.0, "mean", ()),
+    # fewer vocabulary blocks than pairs per cluster: pairs that own no block (two and three pairs)
+    "one-block-two-pairs": (64, 512, 100, True, 1e-3, "mean", (3,)),
+    "one-block-three-pairs": (70, 768, 200, False, 0.0, "sum", ()),
 }
 
 
