@@ -161,7 +161,9 @@ struct PairParams {
   const float* grad_tok;    // per-token upstream gradient, or null (ones)
   const uint16_t* Wmat;     // W, for the target-row term
   float* mref_g;            // [BT rounded up to 256] per-row reference, log2 units
-  float2* part_g;           // [BT rounded up to 256][kMaxPairs][2]: (sum of 2^(x - ref), z_y or -inf)
+  float4* part_g;           // [BT rounded up to 256][kMaxPairs][2]: (sum of 2^(x - ref), z_y or -inf,
+                            //  sum of 2^(x - ref) z, 0)
+  float* entropy_out;       // per-row entropy of softmax(z), or null
   float4* stats_out;        // per-token statistics for the grad_W pass
   float* row_loss;
   float* loss_tok;
@@ -279,24 +281,27 @@ __device__ __forceinline__ bool filter_small_row(const uint32_t (&r)[64], const 
 }
 
 // Online grad_input pass: 64 consecutive logits of one row (fp32 bits in) -> 2^(S log2 e + b log2 e - ref)
-// (fp32 bits out), with c = -ref, and their sum added to lsum; the target column's logit (+ bias) goes to
-// zy and its entry to 0 (its gradient term is added exactly at the end; it stays in the sum).
+// (fp32 bits out), with c = -ref, and their sum added to lsum (with ent, the sum of each times its logit
+// z = S + b to tsum); the target column's logit (+ bias) goes to zy and its entry to 0 (its gradient term
+// is added exactly at the end; it stays in the sums).
 __device__ __forceinline__ void online_chunk64(uint32_t (&r)[64], int col0, float c, bool plain,
                                                const float* __restrict__ colb2, const float* __restrict__ bias, int y,
-                                               float& lsum, float& zy) {
+                                               float& lsum, float& zy, bool ent, float& tsum) {
   const bool has_y = static_cast<unsigned>(y - col0) < 64u;
   if (has_y) {
 #pragma unroll
     for (int i = 0; i < 64; ++i)
       if (col0 + i == y) zy = __uint_as_float(r[i]) + (bias != nullptr ? __ldg(bias + y) : 0.f);
   }
-  float sum = 0.f;
+  float sum = 0.f, tz = 0.f;
   if (plain) {
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
-      const float v = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, c));
+      const float z = __uint_as_float(r[i]);
+      const float v = ex2_approx(fmaf(z, kLog2e, c));
       r[i] = __float_as_uint(v);
       sum += v;
+      if (ent) tz = fmaf(v, z, tz);
     }
   } else {
 #pragma unroll
@@ -305,12 +310,16 @@ __device__ __forceinline__ void online_chunk64(uint32_t (&r)[64], int col0, floa
       const float bb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float v = ex2_approx(fmaf(__uint_as_float(r[4 * i4 + k]), kLog2e, c + bb[k]));
+        const float z = __uint_as_float(r[4 * i4 + k]);
+        const float v = ex2_approx(fmaf(z, kLog2e, c + bb[k]));
         r[4 * i4 + k] = __float_as_uint(v);
         sum += v;
+        // (columns past V carry b = -inf and v = 0: no term)
+        if (ent && bb[k] != -INFINITY) tz = fmaf(v, fmaf(bb[k], kLn2, z), tz);
       }
     }
   }
+  if (ent) tsum += tz;
   if (has_y) {
 #pragma unroll
     for (int i = 0; i < 64; ++i)
@@ -624,7 +633,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     DsRow rc{-INFINITY, 0.f, 0.f, 0.f, 0.f, scale, 2.0f * p.z_loss * kLn2, -1};
     // online form: no statistics yet; this row's target and upstream gradient, its reference (from the first
     // block, once pair 0 has published it), and the running sum / target logit of the columns it owns
-    float on_ref = 0.f, on_lsum = 0.f, on_zy = -INFINITY, on_u = 0.f;
+    float on_ref = 0.f, on_lsum = 0.f, on_zy = -INFINITY, on_u = 0.f, on_tsum = 0.f;
+    const bool on_ent = kOnline && p.entropy_out != nullptr;
     bool on_have_ref = false;
     if (kOnline) {
       if (row < p.BT) {
@@ -726,7 +736,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         const float fge = (kVocabRows && filt) ? p.filter_eps * fabsf(scale) : 0.f;
         int* const fov = (kVocabRows && filt) ? &over : nullptr;
         if (kOnline)
-          online_chunk64(ra, col0, -on_ref, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, p.bias, rc.y, on_lsum, on_zy);
+          online_chunk64(ra, col0, -on_ref, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, p.bias, rc.y, on_lsum, on_zy,
+                         on_ent, on_tsum);
         else
           ds_chunk64<kVocabRows>(ra, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gbias,
                                  fge, fov);
@@ -735,7 +746,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         for (int i2 = 0; i2 < 32; ++i2) pk0[i2] = pack_bf16x2(__uint_as_float(ra[2 * i2]), __uint_as_float(ra[2 * i2 + 1]));
         if (kOnline)
           online_chunk64(rb, col0 + 64, -on_ref, p.bias == nullptr && col0 + 128 <= p.V, p.colb2, p.bias, rc.y,
-                         on_lsum, on_zy);
+                         on_lsum, on_zy, on_ent, on_tsum);
         else
           ds_chunk64<kVocabRows>(rb, col0 + 64, rc, general, p.bias == nullptr && col0 + 128 <= p.V, p.colb2,
                                  tstats + 64, gbias, fge, fov);
@@ -842,7 +853,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         }
       }
       if (ok) {
-        p.part_g[(static_cast<size_t>(row) * kMaxPairs + pr) * 2 + hh] = make_float2(on_lsum, on_zy);
+        p.part_g[(static_cast<size_t>(row) * kMaxPairs + pr) * 2 + hh] = make_float4(on_lsum, on_zy, on_tsum, 0.f);
         __syncwarp();
         if (lane == 0)
           for (int pp = 0; pp < P; ++pp)
@@ -850,12 +861,13 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         if (!mbar_wait_cluster(&sm.part_ready, 0, abort)) ok = false;
       }
       if (ok) {
-        float L = 0.f, zy = -INFINITY;
+        float L = 0.f, zy = -INFINITY, T = 0.f;
         for (int pp = 0; pp < P; ++pp)
           for (int h2 = 0; h2 < 2; ++h2) {
-            const float2 v = __ldcg(p.part_g + (static_cast<size_t>(row) * kMaxPairs + pp) * 2 + h2);
+            const float4 v = __ldcg(p.part_g + (static_cast<size_t>(row) * kMaxPairs + pp) * 2 + h2);
             L += v.x;
             zy = fmaxf(zy, v.y);
+            T += v.z;
           }
         const float lse2 = on_ref + log2f(L);
         const float lse = lse2 * kLn2;
@@ -873,6 +885,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
           if (valid && on_u != 0.f && !(uf > 0.f)) atomicOr(p.zf_neg_out, 1u);
           p.stats_out[row] = make_float4(valid && uf > 0.f ? log2f(uf) - lse2 : -INFINITY, valid ? on_u : 0.f, lse2,
                                          __int_as_float(valid ? rc.y : -1));
+          // entropy of softmax(z) = LSE - sum_n p_n z_n, for every row
+          if (on_ent) p.entropy_out[row] = lse - T / L;
         }
         // 2^115 leaves room for the accumulator's sums over the vocabulary; beyond it (or for a sum that is
         // not finite) the classic passes redo the call
@@ -1048,6 +1062,7 @@ PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
   p.Wmat = a.Wmat;
   p.mref_g = a.mref_g;
   p.part_g = a.part_g;
+  p.entropy_out = a.entropy_out;
   p.stats_out = a.stats_out;
   p.row_loss = a.row_loss;
   p.loss_tok = a.loss_tok;

@@ -125,7 +125,8 @@ struct DgPairArgs {
   const float* grad_tok;
   const uint16_t* Wmat;
   float* mref_g;             // [BT rounded up to 256]
-  float2* part_g;            // [BT rounded up to 256][4][2]
+  float4* part_g;            // [BT rounded up to 256][4][2]
+  float* entropy_out;        // per-row entropy out, or NULL
   float4* stats_out;
   float* row_loss;
   float* loss_tok;

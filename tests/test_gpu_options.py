@@ -139,15 +139,17 @@ def test_unreduced_empty_batch_leaves_accumulators(flce):
     assert res["loss"].item() == 0.0
 
 
+@pytest.mark.parametrize("separate_lse", [False, True], ids=["lse-in-grad-input-pass", "separate-lse-pass"])
 @pytest.mark.parametrize("shape", sorted(SHAPES))
-def test_entropy(flce, shape):
+def test_entropy(flce, shape, separate_lse):
     # per-row entropy of softmax(z); tolerance: H = LSE - sum p z is a difference of two fp32 quantities of
     # size about LSE, so each row is held to the loss bar relative to max(1, LSE)
     import torch
     BT, H, V, bias, zl, ign = SHAPES[shape]
     d = _inputs(BT, H, V, bias, zl, seed=7 * BT + H, ignore=ign)
     hidden, W, target, b = _upload(d)
-    out = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction="mean", z_loss=zl, want_entropy=True)
+    out = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction="mean", z_loss=zl, want_entropy=True,
+                            separate_lse_pass=separate_lse)
     torch.cuda.synchronize()
     assert flce.read_device_status(out["workspace"]) == 0
     ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], reduction="mean", z_loss=zl)
@@ -159,14 +161,16 @@ def test_entropy(flce, shape):
     _compare(out, ref)
 
 
-def test_entropy_peaked(flce):
+@pytest.mark.parametrize("separate_lse", [False, True], ids=["lse-in-grad-input-pass", "separate-lse-pass"])
+def test_entropy_peaked(flce, separate_lse):
     # logits with a standard deviation near 5 (hidden scaled): low-entropy rows
     import torch
     w = wl.FusedWorkload("peaked", BT=130, H=64, V=700, hidden_std=31.0, w_std=0.02, bias_std=None,
                          ignore_frac=0.0, z_loss=0.0, reduction="sum", seed=21)
     d = wl.make_fused_inputs(w)
     hidden, W, target, b = _upload(d)
-    out = flce.flce_fwd_bwd(hidden, W, target, reduction="sum", want_entropy=True, need_grad_W=False)
+    out = flce.flce_fwd_bwd(hidden, W, target, reduction="sum", want_entropy=True, need_grad_W=False,
+                            separate_lse_pass=separate_lse)
     torch.cuda.synchronize()
     ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], reduction="sum", want_grads=False)
     got = out["entropy"].cpu().numpy().astype(np.float64)
