@@ -175,11 +175,11 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        index at sorted position k (requires sort_vocab).
  *   separate_lse_pass    non-zero: compute every row's LSE in a pass of its own before the gradient passes
  *                        (the two-pass scheme of "Cut Cross Entropy visualized", "Backward pass").  By
- *                        default, when grad_input is requested without accumulate, the grad_input pass
- *                        finds the LSE itself (and the entropy, when requested) (online softmax against a per-row
+ *                        default, when grad_input is requested, the grad_input pass finds the LSE itself
+ *                        (and the entropy, when requested) (online softmax against a per-row
  *                        reference, "Fused Linear Cross-Entropy", "Strategy 2"), one GEMM over the logits
- *                        fewer; rows whose sums leave that pass's safe range make the call redo the work
- *                        with the separate pass, on the device.  Both give the same results up to rounding.
+ *                        fewer; rows whose sums leave that pass's safe range are redone with the separate
+ *                        pass, on the device.  Both give the same results up to rounding.
  *                        With filter_eps > 0 that grad_input pass is exact and only the grad_W pass
  *                        filters (a result within the same bound).
  */

@@ -164,6 +164,8 @@ struct PairParams {
   float4* part_g;           // [BT rounded up to 256][kMaxPairs][2]: (sum of 2^(x - ref), z_y or -inf,
                             //  sum of 2^(x - ref) z, 0)
   float* entropy_out;       // per-row entropy of softmax(z), or null
+  uint32_t* row_redo;       // online pass: per row, 1 when its sum left the safe range (row not written);
+                            // classic grad_input pass behind it: write only those rows
   float4* stats_out;        // per-token statistics for the grad_W pass
   float* row_loss;
   float* loss_tok;
@@ -842,6 +844,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     //   L = sum_n 2^(z_n log2 e - ref), LSE = (ref + log2 L) ln 2, f = 1 + 2 z_loss LSE,
     //   c1 = G u f / L (O holds sum over n != y of 2^(..) W[n]),  c2 = G u (f p_y - 1)
     float on_c1 = 0.f, on_c2 = 0.f;
+    bool on_row_ok = true;
     if (kOnline) {
       if (ok && !on_have_ref) {
         // a pair that owned no block still needs the reference
@@ -889,8 +892,10 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
           if (on_ent) p.entropy_out[row] = lse - T / L;
         }
         // 2^115 leaves room for the accumulator's sums over the vocabulary; beyond it (or for a sum that is
-        // not finite) the classic passes redo the call
-        if (row < p.BT && !(L < 0x1p115f)) atomicOr(p.fallback, 1u);
+        // not finite) this row is left unwritten and the classic passes redo it
+        on_row_ok = L < 0x1p115f;
+        if (pr == 0 && hh == 0 && row < p.BT) p.row_redo[row] = on_row_ok ? 0u : 1u;
+        if (row < p.BT && !on_row_ok) atomicOr(p.fallback, 1u);
       }
     }
 
@@ -903,7 +908,10 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         tmem_wait_ld();
         const int cb = 32 * c;
         if (!kVocabRows) {
-          if (row < p.BT) {
+          // (online: a row outside the safe range is left to the classic pass; classic behind an online
+          // pass: only such rows)
+          const bool write_row = kOnline ? on_row_ok : (p.row_redo == nullptr || (row < p.BT && p.row_redo[row] != 0u));
+          if (row < p.BT && write_row) {
             uint16_t* out = p.grad_input + static_cast<size_t>(row) * p.H + h0 + cb;
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
@@ -1063,6 +1071,7 @@ PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
   p.mref_g = a.mref_g;
   p.part_g = a.part_g;
   p.entropy_out = a.entropy_out;
+  p.row_redo = a.row_redo;
   p.stats_out = a.stats_out;
   p.row_loss = a.row_loss;
   p.loss_tok = a.loss_tok;

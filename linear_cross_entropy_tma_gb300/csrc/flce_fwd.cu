@@ -437,6 +437,7 @@ size_t fused_workspace_bytes(int64_t BT, int64_t V) {
   off += align_up(sizeof(float4) * align_up(btp, 256), 256);
   off += align_up(sizeof(float) * btp, 256);
   off += align_up(sizeof(float) * vp, 256);
+  off += align_up(sizeof(uint32_t) * btp, 256);
   off += kDsL2Slots * kDsL2SlotBytes;
   return off;
 }
@@ -465,6 +466,8 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   off += align_up(sizeof(float) * btp, 256);
   w.colb2 = reinterpret_cast<float*>(p + off);
   off += align_up(sizeof(float) * vp, 256);
+  w.row_redo = reinterpret_cast<uint32_t*>(p + off);
+  off += align_up(sizeof(uint32_t) * btp, 256);
   w.ds_l2 = p + off;
   return w;
 }

@@ -47,6 +47,7 @@ struct FusedWorkspace {
                      //   z = LSE2, w = target as int bits (-1 for ignored rows); rows past BT: (-inf, 0, 0, -1)
   float* row_loss;   // [BTp] valid * (LSE - z_y + z_loss LSE^2)
   float* colb2;      // [V rounded up to 256] bias * log2 e (0 without bias); -inf past V
+  uint32_t* row_redo; // [BTp] online flow: 1 for a row the grad_input pass left to the classic passes
   uint8_t* ds_l2;    // [kDsL2Slots][kDsL2SlotBytes] per-SM staging of dS blocks handed to the other pairs
 };
 
@@ -127,6 +128,7 @@ struct DgPairArgs {
   float* mref_g;             // [BT rounded up to 256]
   float4* part_g;            // [BT rounded up to 256][4][2]
   float* entropy_out;        // per-row entropy out, or NULL
+  uint32_t* row_redo;        // [BTp] rows the online pass left to the classic one (see flce_bwd.cu)
   float4* stats_out;
   float* row_loss;
   float* loss_tok;

@@ -1,7 +1,7 @@
 // flce_launch.cu -- enqueues every pass of one flce_fwd_bwd call on the caller's stream, no host
 // synchronisation, no allocation, optional caller events at the pass boundaries:
 //   header clear -> [vocabulary sort (vocab_sort.cu)] -> then either
-//   online flow (grad_input requested, no accumulation):
+//   online flow (grad_input requested):
 //     bias table + valid count -> grad_input pass that also finds the LSE (flce_bwd.cu, online form)
 //     -> loss reduction -> [LSE tiles, merge, reduction, classic grad_input pass: gated, they run only when
 //     the online pass reported a row outside its safe range] -> grad_W / grad_bias pass
@@ -47,7 +47,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
   }
   const bool want_dw = (a.grad_W != nullptr) || (a.grad_bias != nullptr);
   // (with gradient filtering the online grad_input pass is exact and only the grad_W pass filters)
-  const bool online = a.BT > 0 && a.grad_input != nullptr && !a.accumulate && !a.separate_lse;
+  const bool online = a.BT > 0 && a.grad_input != nullptr && !a.separate_lse;
   DgPairArgs pa{};
   pa.bias = a.bias;
   pa.stats = ws.stats;
@@ -83,6 +83,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     po.mref_g = ws.part_t;                      // the split partials are free in this flow
     po.part_g = reinterpret_cast<float4*>(ws.part);   // [BT up to 256][4][2] float4 fits its 32 x BTp float2
     po.entropy_out = a.entropy;
+    po.row_redo = ws.row_redo;
     po.stats_out = ws.stats;
     po.row_loss = ws.row_loss;
     po.loss_tok = a.loss_tok;
@@ -95,6 +96,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     if ((e = launch_lse_passes(a, ws, num_sms, stream, err, err_len, nullptr, ws.fallback)) != cudaSuccess) return e;
     DgPairArgs pg = pa;
     pg.gate = ws.fallback;
+    pg.row_redo = ws.row_redo;   // only the rows the online pass left
     if ((e = launch_dgrad_pair<false>(tm_h, tm_w, pg, stream)) != cudaSuccess) return e;
     if ((e = mark(3)) != cudaSuccess) return e;
     if (want_dw && (e = launch_dgrad_pair<true>(tm_w, tm_h, pa, stream)) != cudaSuccess) return e;

@@ -203,6 +203,21 @@ def test_flce_online_fallback(flce, H):
     assert out["status"] == 0
     assert _fallback_flag(out["workspace"]) == 1
     _check_full(out, d)
+    # the same with accumulation: rows the online pass left are written once, by the classic pass
+    import torch
+    rng = np.random.Generator(np.random.PCG64(5))
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], reduction="mean", z_loss=1e-4)
+    gi0 = wl.f32_to_bf16_bits((rng.standard_normal((260, H)) * np.std(ref["grad_input"])).astype(np.float32))
+    gw0 = (rng.standard_normal((1200, H)) * np.std(ref["grad_W"])).astype(np.float32)
+    gb0 = (rng.standard_normal(1200) * np.std(ref["grad_bias"])).astype(np.float32)
+    acc = {"grad_input": bf16_tensor(gi0), "grad_W": torch.from_numpy(gw0.copy()).cuda(),
+           "grad_bias": torch.from_numpy(gb0.copy()).cuda()}
+    out3 = _run(flce, d, accumulate=True, out=acc)
+    assert out3["status"] == 0 and _fallback_flag(out3["workspace"]) == 1
+    assert_grad_close(bf16_to_numpy_f32(out3["grad_input"]),
+                      ref["grad_input"] + (gi0.astype(np.uint32) << 16).view(np.float32), "grad_input (accumulated)")
+    assert_grad_close(out3["grad_W"].cpu().numpy(), ref["grad_W"] + gw0, "grad_W (accumulated)")
+    assert_grad_close(out3["grad_bias"].cpu().numpy(), ref["grad_bias"] + gb0, "grad_bias (accumulated)")
     # and ordinary inputs stay on the online pass
     d2 = _synthetic(260, H, 1200, True, 1e-4, "mean", ignore=(1, 200), seed=18)
     out2 = _run(flce, d2)
