@@ -37,6 +37,13 @@
 //     can never be two phases behind or ahead.
 //   * grad_bias (vocabulary rows) is each CTA's fp32 row sum of dS over the blocks it owns, gathered
 //     across the pairs in distributed shared memory and added in pair order (deterministic).
+//   * Online form of the grad_input pass (dgrad_online_kernel): no row statistics beforehand.  The tile
+//     carries P = 2^(z log2 e - ref) against a per-row reference fixed by the first block (the same in
+//     every pair, so the accumulators share one scale and nothing is rescaled; "Fused Linear
+//     Cross-Entropy", "Strategy 2" keeps a running max instead), the target column is left out of O, the
+//     owners keep the row sums and the target logit, and at the end the pairs combine them into the LSE,
+//     the statistics and loss terms the rest of the call needs, and grad_input = G u (f O / L + (f p_y - 1)
+//     W[y]).  Rows whose sums leave the safe range are left to the classic passes.
 // All waits are bounded; a wait that gives up flags the status word and the kernel winds down.
 #include "flce_kernels.cuh"
 #include "sm100.cuh"

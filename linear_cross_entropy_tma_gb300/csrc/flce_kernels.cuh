@@ -1,6 +1,7 @@
 // flce_kernels.cuh -- workspace layout and launchers of the fused linear cross-entropy kernels.
 //
-// Pass structure of one flce_fwd_bwd call (all on one stream, no host synchronisation):
+// Pass structure of one flce_fwd_bwd call in the classic flow (all on one stream, no host
+// synchronisation; the default flow replaces steps 1-4 by the online grad_input pass, see flce_launch.cu):
 //   1. lse_partial   logits tile GEMM (tcgen05, TMEM accumulators, TMA-fed) per (128-token tile,
 //                    vocabulary split); the epilogue keeps an online per-row (max, sum-exp) over the
 //                    split's 256-wide vocabulary tiles and picks up the target logit z_y.
