@@ -182,6 +182,16 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        pass, on the device.  Both give the same results up to rounding.
  *                        With filter_eps > 0 that grad_input pass is exact and only the grad_W pass
  *                        filters (a result within the same bound).
+ *   vocab_splits         work split of that grad_input pass (default flow only).  0: automatic -- the
+ *                        row blocks of its last, partly filled wave of clusters are each split into
+ *                        vocabulary ranges processed by separate clusters, whose partial sums (against
+ *                        their own references) a merge kernel rescales and adds ("Cut Cross Entropy
+ *                        visualized", "Triton kernel, online softmax across vocab splits"); 1: never
+ *                        split; k >= 2: split every row block into up to k ranges (fewer when the
+ *                        scratch, 64 split clusters, or ranges of at least 4 x 256 columns do not
+ *                        allow k; at most 8).  Results are the same up to rounding order.  Negative:
+ *                        FLCE_ERR_INVALID_ARG.  The number of vocabulary-split clusters the call ran is
+ *                        the 32-bit word at byte 28 of the workspace.
  */
 typedef struct flce_fwd_bwd_options {
   float grad_scale;
@@ -194,6 +204,7 @@ typedef struct flce_fwd_bwd_options {
   float* logit_avg;
   int32_t* vocab_order;
   int separate_lse_pass;
+  int vocab_splits;
 } flce_fwd_bwd_options;
 
 /* Bytes of workspace flce_fwd_bwd_ex needs with these options (NULL: flce_workspace_size). */

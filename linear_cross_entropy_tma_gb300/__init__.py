@@ -14,5 +14,6 @@ from ._lib import (  # noqa: F401
     load,
     read_device_status,
     read_filter_skips,
+    read_vocab_split_units,
     workspace_size,
 )

@@ -45,6 +45,8 @@
 //     the statistics and loss terms the rest of the call needs, and grad_input = G u (f O / L + (f p_y - 1)
 //     W[y]).  Rows whose sums leave the safe range are left to the classic passes.
 // All waits are bounded; a wait that gives up flags the status word and the kernel winds down.
+#include <algorithm>
+
 #include "flce_kernels.cuh"
 #include "sm100.cuh"
 
@@ -178,6 +180,13 @@ struct PairParams {
   float* loss_tok;
   uint32_t* zf_neg_out;
   uint32_t* fallback;       // set when a row's sum left the safe range: the classic passes redo the work
+  // online pass, vocabulary-split work units (unit su covers column blocks [jb, je) of its 256 rows and
+  // writes partial results instead of the row outputs; online_vmerge_kernel combines them):
+  float* vs_mref;           // [su][256] the unit's per-row reference
+  float4* vs_part;          // [su][256][kMaxPairs][2] its pairs' partial sums (as part_g)
+  float4* vs_stat;          // [su][256] (L, z_y or -inf, T, reference) over the unit's columns
+  float* vs_o;              // [su][256][P * 256] its unnormalised accumulator O
+  uint32_t* vs_count;       // receives the number of vocabulary-split units (workspace header)
 };
 
 // The block whose GEMM1 pair `pr` works on in step s (the one it owns in [s+P+1, s+2P]) and which
@@ -337,14 +346,56 @@ __device__ __forceinline__ void online_chunk64(uint32_t (&r)[64], int col0, floa
   lsum += sum;
 }
 
+// Online grad_input pass: one row's outputs from its sums over the whole vocabulary against the reference
+// ref (log2 units): L = sum_n 2^(z_n log2 e - ref), zy = the target logit (-inf if none), T = sum_n
+// 2^(z_n log2 e - ref) z_n.  With `write` (one thread per row) stores the loss terms, the statistics the
+// grad_W pass reads, zf_neg, the entropy and the redo flag.  Returns the coefficients of
+// grad_input[row] = c1 O[row] + c2 W[y] and whether the row is in the safe range:
+//   LSE = (ref + log2 L) ln 2, f = 1 + 2 z_loss LSE, c1 = G u f / L (O holds sum over n != y of
+//   2^(..) W[n]), c2 = G u (f p_y - 1).
+struct OnlineRow {
+  float c1, c2;
+  bool ok;
+};
+__device__ __forceinline__ OnlineRow online_row_finish(const PairParams& p, int row, float ref, float L, float zy,
+                                                       float T, int y, float u, float scale, bool write) {
+  OnlineRow r{0.f, 0.f, true};
+  const float lse2 = ref + log2f(L);
+  const float lse = lse2 * kLn2;
+  const bool valid = y >= 0;
+  const float f = 1.0f + 2.0f * p.z_loss * lse;
+  if (valid) {
+    r.c1 = scale * u * f / L;
+    r.c2 = scale * u * (f * ex2_approx(fmaf(zy, kLog2e, -lse2)) - 1.0f);
+  }
+  // 2^115 leaves room for the accumulator's sums over the vocabulary; beyond it (or for a sum that is
+  // not finite) the row is left unwritten and the classic passes redo it
+  r.ok = L < 0x1p115f;
+  if (write && row < p.BT) {
+    const float lt = valid ? (lse - zy) + p.z_loss * lse * lse : 0.f;
+    p.row_loss[row] = lt;
+    if (p.loss_tok != nullptr) p.loss_tok[row] = lt;
+    const float uf = u * f;
+    if (valid && u != 0.f && !(uf > 0.f)) atomicOr(p.zf_neg_out, 1u);
+    p.stats_out[row] = make_float4(valid && uf > 0.f ? log2f(uf) - lse2 : -INFINITY, valid ? u : 0.f, lse2,
+                                   __int_as_float(valid ? y : -1));
+    // entropy of softmax(z) = LSE - sum_n p_n z_n, for every row
+    if (p.entropy_out != nullptr) p.entropy_out[row] = lse - T / L;
+    p.row_redo[row] = r.ok ? 0u : 1u;
+    if (!r.ok) atomicOr(p.fallback, 1u);
+  }
+  return r;
+}
+
 // kFilter: the gradient-filtering variant (a separate instantiation, so the exact path carries none of
 // its checks).
 // One cluster's work: rows [256 row_pair, +256) (128 per CTA of each pair) and the H chunks of
 // group hgroup (P consecutive 256-wide chunks, one per pair).
+// Columns: blocks [jb, je) of 256 (all of them except for a vocabulary-split unit of the online pass, su >= 0).
 template <bool kVocabRows, bool kFilter, bool kOnline = false>
 __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols,
                                                 const PairParams& p, uint32_t* __restrict__ status, int row_pair,
-                                                int hgroup) {
+                                                int hgroup, int jb = 0, int je = -1, int su = -1) {
   static_assert(!kOnline || (!kVocabRows && !kFilter), "the online form is a grad_input pass without the filter");
   constexpr int kStages = PairCfg<kVocabRows>::kStages;
   // the classic passes behind an online grad_input pass run only when it asked for them
@@ -366,7 +417,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
   const int hc = min(kHc, p.H - h0);
   const uint32_t n2 = hc > 128 ? 256u : 128u;   // GEMM2 N; columns past H are zero-filled by TMA
   const int nbox2 = static_cast<int>(n2) / 128; // 64-column boxes per CTA per GEMM2 stage
-  const int nt = (p.n_cols + kPN - 1) / kPN;
+  if (je < 0) je = (p.n_cols + kPN - 1) / kPN;
+  const int nt = je - jb;   // column blocks of this unit; j below counts from jb
   const int nkb = p.num_kb;
   constexpr bool filt = kFilter;
 
@@ -442,7 +494,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2u * nbox2 * kBox);
         for (int b = 0; b < nbox2; ++b)
           tma_load_2d_pair(sm.stage[stage] + b * kBox, &tm_cols, fb,
-                           h0 + static_cast<int>(q * (n2 / 2)) + 64 * b, j * kPN + half * kTileM);
+                           h0 + static_cast<int>(q * (n2 / 2)) + 64 * b, (jb + j) * kPN + half * kTileM);
         next();
       };
       int u = 0;   // owned blocks whose GEMM1 has been fully loaded
@@ -457,7 +509,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
             break;
           }
           mbar_arrive_expect_tx(&sm.st_full[sb], kPN * sizeof(float4));
-          bulk_load_1d(sm.colstats[sb], p.stats + static_cast<size_t>(g.block) * kPN, kPN * sizeof(float4),
+          bulk_load_1d(sm.colstats[sb], p.stats + static_cast<size_t>(jb + g.block) * kPN, kPN * sizeof(float4),
                        &sm.st_full[sb]);
         }
         const int kb0 = has_g1 ? share_begin(g.prog, nkb, P) : 0;
@@ -473,7 +525,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
             if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * kStage);
             tma_load_2d_pair(sm.stage[stage], &tm_rows, fb, kb * kBK, r0);
             tma_load_2d_pair(sm.stage[stage] + kBox, &tm_cols, fb, kb * kBK,
-                             g.block * kPN + static_cast<int>(q) * kTileM);
+                             (jb + g.block) * kPN + static_cast<int>(q) * kTileM);
             next();
           }
         };
@@ -645,6 +697,15 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     float on_ref = 0.f, on_lsum = 0.f, on_zy = -INFINITY, on_u = 0.f, on_tsum = 0.f;
     const bool on_ent = kOnline && p.entropy_out != nullptr;
     bool on_have_ref = false;
+    // where this row's reference and partial sums go (a vocabulary-split unit has its own; rloc = the row
+    // within the unit's 256)
+    const int rloc = static_cast<int>(q) * kTileM + rl;
+    float* const on_mref = !kOnline ? nullptr
+                           : su < 0 ? p.mref_g + row
+                                    : p.vs_mref + static_cast<size_t>(su) * 256 + rloc;
+    float4* const on_part = !kOnline ? nullptr
+                            : su < 0 ? p.part_g + static_cast<size_t>(row) * kMaxPairs * 2
+                                     : p.vs_part + (static_cast<size_t>(su) * 256 + rloc) * kMaxPairs * 2;
     if (kOnline) {
       if (row < p.BT) {
         const int64_t y = p.target[row];
@@ -700,7 +761,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         break;
       }
       const float4* tstats = sm.colstats[kVocabRows ? sb : 0] + (kVocabRows ? hh * 128 : 0);
-      const int col0 = j * kPN + hh * 128;
+      const int col0 = (jb + j) * kPN + hh * 128;
       // dS of this row's 128 columns in two chunks of 64, packed to bf16 pairs
       uint32_t pk0[32], pk1[32];
       {
@@ -724,7 +785,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
               m = fmaxf(m, fmaf(__uint_as_float(ra[i]), kLog2e, __ldg(p.colb2 + col0 + i)));
               m = fmaxf(m, fmaf(__uint_as_float(rb[i]), kLog2e, __ldg(p.colb2 + col0 + 64 + i)));
             }
-            p.mref_g[row] = m;
+            *on_mref = m;
             __syncwarp();
             if (lane == 0)
               for (int pp = 0; pp < P; ++pp)
@@ -734,7 +795,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
             ok = false;
             break;
           }
-          on_ref = __ldcg(p.mref_g + row);
+          on_ref = __ldcg(on_mref);
           on_have_ref = true;
         }
         // with the filter: is every entry of this row's half small, |dS| <= eps |w| with w the entry's
@@ -846,10 +907,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
     }
 
-    // online form: every pair's partial sums of this row combined, the row's statistics for the grad_W pass
-    // and loss, and the two coefficients of grad_input[row] = c1 O[row] + c2 W[y]:
-    //   L = sum_n 2^(z_n log2 e - ref), LSE = (ref + log2 L) ln 2, f = 1 + 2 z_loss LSE,
-    //   c1 = G u f / L (O holds sum over n != y of 2^(..) W[n]),  c2 = G u (f p_y - 1)
+    // online form: every pair's partial sums of this row combined into the row's outputs (online_row_finish),
+    // or, in a vocabulary-split unit, into the unit's partial statistics
     float on_c1 = 0.f, on_c2 = 0.f;
     bool on_row_ok = true;
     if (kOnline) {
@@ -858,12 +917,12 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         if (!mbar_wait_cluster(&sm.mref_ready, 0, abort)) {
           ok = false;
         } else {
-          on_ref = __ldcg(p.mref_g + row);
+          on_ref = __ldcg(on_mref);
           on_have_ref = true;
         }
       }
       if (ok) {
-        p.part_g[(static_cast<size_t>(row) * kMaxPairs + pr) * 2 + hh] = make_float4(on_lsum, on_zy, on_tsum, 0.f);
+        on_part[pr * 2 + hh] = make_float4(on_lsum, on_zy, on_tsum, 0.f);
         __syncwarp();
         if (lane == 0)
           for (int pp = 0; pp < P; ++pp)
@@ -874,35 +933,19 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         float L = 0.f, zy = -INFINITY, T = 0.f;
         for (int pp = 0; pp < P; ++pp)
           for (int h2 = 0; h2 < 2; ++h2) {
-            const float4 v = __ldcg(p.part_g + (static_cast<size_t>(row) * kMaxPairs + pp) * 2 + h2);
+            const float4 v = __ldcg(on_part + pp * 2 + h2);
             L += v.x;
             zy = fmaxf(zy, v.y);
             T += v.z;
           }
-        const float lse2 = on_ref + log2f(L);
-        const float lse = lse2 * kLn2;
-        const bool valid = rc.y >= 0;
-        const float f = 1.0f + 2.0f * p.z_loss * lse;
-        if (valid) {
-          on_c1 = scale * on_u * f / L;
-          on_c2 = scale * on_u * (f * ex2_approx(fmaf(zy, kLog2e, -lse2)) - 1.0f);
+        if (su >= 0) {
+          if (pr == 0 && hh == 0) p.vs_stat[static_cast<size_t>(su) * 256 + rloc] = make_float4(L, zy, T, on_ref);
+        } else {
+          const OnlineRow fr = online_row_finish(p, row, on_ref, L, zy, T, rc.y, on_u, scale, pr == 0 && hh == 0);
+          on_c1 = fr.c1;
+          on_c2 = fr.c2;
+          on_row_ok = fr.ok;
         }
-        if (pr == 0 && hh == 0 && row < p.BT) {
-          const float lt = valid ? (lse - zy) + p.z_loss * lse * lse : 0.f;
-          p.row_loss[row] = lt;
-          if (p.loss_tok != nullptr) p.loss_tok[row] = lt;
-          const float uf = on_u * f;
-          if (valid && on_u != 0.f && !(uf > 0.f)) atomicOr(p.zf_neg_out, 1u);
-          p.stats_out[row] = make_float4(valid && uf > 0.f ? log2f(uf) - lse2 : -INFINITY, valid ? on_u : 0.f, lse2,
-                                         __int_as_float(valid ? rc.y : -1));
-          // entropy of softmax(z) = LSE - sum_n p_n z_n, for every row
-          if (on_ent) p.entropy_out[row] = lse - T / L;
-        }
-        // 2^115 leaves room for the accumulator's sums over the vocabulary; beyond it (or for a sum that is
-        // not finite) this row is left unwritten and the classic passes redo it
-        on_row_ok = L < 0x1p115f;
-        if (pr == 0 && hh == 0 && row < p.BT) p.row_redo[row] = on_row_ok ? 0u : 1u;
-        if (row < p.BT && !on_row_ok) atomicOr(p.fallback, 1u);
       }
     }
 
@@ -914,7 +957,16 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         tmem_ld_32cols(tmem + (static_cast<uint32_t>(qq * 32) << 16) + kTmemO + 32u * c, vv);
         tmem_wait_ld();
         const int cb = 32 * c;
-        if (!kVocabRows) {
+        if (kOnline && su >= 0) {
+          // vocabulary-split unit: the raw accumulator columns of this pair, for online_vmerge_kernel
+          float* out = p.vs_o + (static_cast<size_t>(su) * 256 + rloc) * (P * kHc) + pr * kHc + cb;
+#pragma unroll
+          for (int g4 = 0; g4 < 8; ++g4)
+            if (cb + 4 * g4 + 4 <= hc)
+              *reinterpret_cast<float4*>(out + 4 * g4) =
+                  make_float4(__uint_as_float(vv[4 * g4 + 0]), __uint_as_float(vv[4 * g4 + 1]),
+                              __uint_as_float(vv[4 * g4 + 2]), __uint_as_float(vv[4 * g4 + 3]));
+        } else if (!kVocabRows) {
           // (online: a row outside the safe range is left to the classic pass; classic behind an online
           // pass: only such rows)
           const bool write_row = kOnline ? on_row_ok : (p.row_redo == nullptr || (row < p.BT && p.row_redo[row] != 0u));
@@ -1014,12 +1066,121 @@ dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_cons
                                        static_cast<int>(blockIdx.y));
 }
 
+// Work units of the online grad_input pass, in launch order: n_whole clusters over the whole vocabulary (row
+// pair u / groups, H group u % groups), then for the last row pairs, from rp_tail0 on, groups x nsplit
+// clusters each over one of nsplit consecutive ranges of the nt column blocks (vocabulary-split units,
+// numbered su = (tail row pair x groups + group) x nsplit + part), which online_vmerge_kernel combines.
+// Splitting the row pairs of a partly filled last wave shortens that wave.
+struct OnlinePlan {
+  int groups, n_whole, rp_tail0, nsplit, nt;
+};
+
 // The grad_input pass without a prior LSE pass: the same cluster layout as dgrad_pair_kernel<false>.
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_online_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
-                    const PairParams p, uint32_t* __restrict__ status) {
-  dgrad_pair_body<false, false, true>(tm_rows, tm_cols, p, status, static_cast<int>(blockIdx.x) / (2 * p.P),
-                                      static_cast<int>(blockIdx.y));
+                    const PairParams p, uint32_t* __restrict__ status, const OnlinePlan plan) {
+  const int c = static_cast<int>(blockIdx.x) / (2 * p.P);
+  int row_pair = c / plan.groups, hgroup = c % plan.groups, jb = 0, je = plan.nt, su = -1;
+  if (c >= plan.n_whole) {
+    su = c - plan.n_whole;
+    const int part = su % plan.nsplit, ug = su / plan.nsplit;
+    row_pair = plan.rp_tail0 + ug / plan.groups;
+    hgroup = ug % plan.groups;
+    jb = (part * plan.nt) / plan.nsplit;
+    je = ((part + 1) * plan.nt) / plan.nsplit;
+  }
+  dgrad_pair_body<false, false, true>(tm_rows, tm_cols, p, status, row_pair, hgroup, jb, je, su);
+}
+
+constexpr int kMaxVocabSplits = 8;
+
+// The rows of vocabulary-split units: per row, the units' partial sums rescaled to the largest of their
+// references R and added (L = sum_v 2^(ref_v - R) L_v, the same for T; z_y from the unit that saw the
+// target), then the row's outputs as in the pass itself (online_row_finish) and
+// grad_input[row] = c1 sum_v 2^(ref_v - R) O_v[row] + c2 W[y].  One CTA of 128 threads per row.
+__global__ void __launch_bounds__(128) online_vmerge_kernel(const PairParams p, const OnlinePlan plan) {
+  const int t = static_cast<int>(blockIdx.x) / 256, rloc = static_cast<int>(blockIdx.x) % 256;
+  const int row = (plan.rp_tail0 + t) * 256 + rloc;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.vs_count != nullptr)
+    *p.vs_count = static_cast<uint32_t>(gridDim.x / 256 * plan.groups * plan.nsplit);
+  if (row >= p.BT) return;
+  const int ns = plan.nsplit;
+  float ref[kMaxVocabSplits], w[kMaxVocabSplits];
+  float R = -INFINITY;
+#pragma unroll
+  for (int v = 0; v < kMaxVocabSplits; ++v) {
+    ref[v] = -INFINITY;
+    if (v < ns) {
+      // (group 0's units: every group sees the same logits)
+      ref[v] = __ldcg(&p.vs_stat[static_cast<size_t>(t * plan.groups * ns + v) * 256 + rloc].w);
+      R = fmaxf(R, ref[v]);
+    }
+  }
+  float L = 0.f, zy = -INFINITY, T = 0.f;
+  bool fin = true;
+#pragma unroll
+  for (int v = 0; v < kMaxVocabSplits; ++v) {
+    w[v] = 0.f;
+    if (v < ns) {
+      const float4 st = __ldcg(&p.vs_stat[static_cast<size_t>(t * plan.groups * ns + v) * 256 + rloc]);
+      w[v] = ex2_approx(ref[v] - R);
+      L = fmaf(st.x, w[v], L);
+      T = fmaf(st.z, w[v], T);
+      zy = fmaxf(zy, st.y);
+      fin = fin && st.x < 0x1p115f;   // each part's accumulator stayed in the safe range
+    }
+  }
+  if (!fin) L = INFINITY;
+  const int64_t yy = p.target[row];
+  const int y = (yy != p.ignore_index && yy >= 0 && yy < p.V) ? static_cast<int>(yy) : -1;
+  const float u = p.grad_tok != nullptr ? p.grad_tok[row] : 1.0f;
+  const OnlineRow fr = online_row_finish(p, row, R, L, zy, T, y, u, *p.scale, threadIdx.x == 0);
+  if (!fr.ok) return;
+  const int span = p.P * kHc;   // columns of one unit
+  for (int h = 8 * static_cast<int>(threadIdx.x); h < p.H; h += 8 * 128) {
+    const int g = h / span, col = h - g * span;
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int v = 0; v < kMaxVocabSplits; ++v) {
+      if (v < ns) {
+        const float* src = p.vs_o + (static_cast<size_t>((t * plan.groups + g) * ns + v) * 256 + rloc) * span + col;
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(src + 4));
+        o[0] = fmaf(w[v], a.x, o[0]);
+        o[1] = fmaf(w[v], a.y, o[1]);
+        o[2] = fmaf(w[v], a.z, o[2]);
+        o[3] = fmaf(w[v], a.w, o[3]);
+        o[4] = fmaf(w[v], b.x, o[4]);
+        o[5] = fmaf(w[v], b.y, o[5]);
+        o[6] = fmaf(w[v], b.z, o[6]);
+        o[7] = fmaf(w[v], b.w, o[7]);
+      }
+    }
+    float wy[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (fr.c2 != 0.f) {
+      const uint4 wv = *reinterpret_cast<const uint4*>(p.Wmat + static_cast<size_t>(y) * p.H + h);
+      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        wy[2 * e] = bf16_lo(ww[e]);
+        wy[2 * e + 1] = bf16_hi(ww[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = fmaf(fr.c1, o[e], fr.c2 * wy[e]);
+    uint16_t* out = p.grad_input + static_cast<size_t>(row) * p.H + h;
+    if (p.accumulate) {
+      const uint4 old = *reinterpret_cast<const uint4*>(out);
+      const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        o[2 * e] += bf16_lo(ow[e]);
+        o[2 * e + 1] += bf16_hi(ow[e]);
+      }
+    }
+    *reinterpret_cast<uint4*>(out) =
+        make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+  }
 }
 
 // Both gradient passes in one grid, so that the grad_W pass's clusters take the SMs the grad_input pass's
@@ -1128,15 +1289,63 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
 cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap& w_map, const DgPairArgs& a,
                                 cudaStream_t stream) {
   int h_chunks = 0;
-  const PairParams p = make_pair_params<false>(a, &h_chunks);
+  PairParams p = make_pair_params<false>(a, &h_chunks);
+  p.vs_mref = a.vs_mref;
+  p.vs_part = a.vs_part;
+  p.vs_stat = a.vs_stat;
+  p.vs_o = a.vs_o;
+  p.vs_count = a.vs_count;
   constexpr size_t smem = pair_smem_bytes<false>();
   cudaError_t e =
       cudaFuncSetAttribute(dgrad_online_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  OnlinePlan plan{};
+  plan.groups = h_chunks / p.P;
+  plan.nt = (p.n_cols + kPN - 1) / kPN;
+  const int rp = row_pairs_of(p);
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * row_pairs_of(p), h_chunks / p.P, 1), smem, p.P, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, dgrad_online_kernel, hidden_map, w_map, p, a.status);
+  // clusters of this shape resident at once (queried once per shape; 0 if the query fails)
+  static int slots_of[kMaxPairs + 1] = {};
+  if (slots_of[p.P] == 0) {
+    cudaLaunchConfig_t q = cluster_config(dim3(2 * p.P, 1, 1), smem, p.P, stream, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dgrad_online_kernel, &q) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = -1;
+    }
+    slots_of[p.P] = n;
+  }
+  const int slots = slots_of[p.P];
+  // vocabulary-split tail: the row pairs of the last, partly filled wave (or every row pair when the caller
+  // asks for a fixed number of parts), each part at least 4 column blocks, within the scratch
+  const int units = rp * plan.groups;
+  const int su_cap = static_cast<int>(std::min<size_t>(
+      kMaxSplitUnits, (static_cast<size_t>(kDsL2Slots) * kDsL2SlotBytes) / (sizeof(float) * 256 * p.P * kHc)));
+  int tail_rp = 0, nsplit = 1;
+  if (a.vocab_splits >= 2) {
+    tail_rp = rp;
+    nsplit = a.vocab_splits;
+  } else if (a.vocab_splits == 0 && slots > 0 && units % slots != 0) {
+    tail_rp = std::min(rp, (units % slots + plan.groups - 1) / plan.groups);
+    nsplit = slots / (tail_rp * plan.groups);
+  }
+  if (tail_rp > 0)
+    nsplit = std::min({nsplit, kMaxVocabSplits, plan.nt / 4, su_cap / (tail_rp * plan.groups)});
+  if (tail_rp == 0 || nsplit < 2 || a.vs_o == nullptr) {
+    tail_rp = 0;
+    nsplit = 1;
+  }
+  plan.nsplit = nsplit;
+  plan.rp_tail0 = rp - tail_rp;
+  plan.n_whole = (rp - tail_rp) * plan.groups;
+  const int n_clusters = plan.n_whole + tail_rp * plan.groups * nsplit;
+  cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * n_clusters, 1, 1), smem, p.P, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, dgrad_online_kernel, hidden_map, w_map, p, a.status, plan);
   if (e != cudaSuccess) return e;
+  if (tail_rp > 0) {
+    online_vmerge_kernel<<<tail_rp * 256, 128, 0, stream>>>(p, plan);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 

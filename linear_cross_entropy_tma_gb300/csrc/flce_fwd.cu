@@ -438,6 +438,9 @@ size_t fused_workspace_bytes(int64_t BT, int64_t V) {
   off += align_up(sizeof(float) * btp, 256);
   off += align_up(sizeof(float) * vp, 256);
   off += align_up(sizeof(uint32_t) * btp, 256);
+  off += sizeof(float) * kMaxSplitUnits * 256;
+  off += sizeof(float4) * kMaxSplitUnits * 256 * 8;
+  off += sizeof(float4) * kMaxSplitUnits * 256;
   off += kDsL2Slots * kDsL2SlotBytes;
   return off;
 }
@@ -453,6 +456,7 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   w.zf_neg = reinterpret_cast<uint32_t*>(p + 16);
   w.skipped = reinterpret_cast<uint32_t*>(p + 20);
   w.fallback = reinterpret_cast<uint32_t*>(p + 24);
+  w.vs_count = reinterpret_cast<uint32_t*>(p + 28);
   size_t off = 256;
   w.part = reinterpret_cast<float2*>(p + off);
   off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
@@ -468,6 +472,12 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   off += align_up(sizeof(float) * vp, 256);
   w.row_redo = reinterpret_cast<uint32_t*>(p + off);
   off += align_up(sizeof(uint32_t) * btp, 256);
+  w.vs_mref = reinterpret_cast<float*>(p + off);
+  off += sizeof(float) * kMaxSplitUnits * 256;
+  w.vs_part = reinterpret_cast<float4*>(p + off);
+  off += sizeof(float4) * kMaxSplitUnits * 256 * 8;
+  w.vs_stat = reinterpret_cast<float4*>(p + off);
+  off += sizeof(float4) * kMaxSplitUnits * 256;
   w.ds_l2 = p + off;
   return w;
 }

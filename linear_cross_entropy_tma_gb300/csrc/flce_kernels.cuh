@@ -30,6 +30,9 @@ constexpr int kTileM = 128;        // rows of every MMA tile (tokens or vocabula
 // passes occupies its SM alone); CTAs on SM ids past the table use shared-memory copies instead.
 constexpr int kDsL2Slots = 256;
 constexpr size_t kDsL2SlotBytes = 65536;
+// Vocabulary-split work units of the online grad_input pass (see launch_dgrad_online): at most this many,
+// their accumulators in the dS staging area (free until the grad_W pass), their row sums in vs_*.
+constexpr int kMaxSplitUnits = 64;
 
 struct FusedWorkspace {
   uint32_t* status;  // header: status word
@@ -37,6 +40,7 @@ struct FusedWorkspace {
   int64_t* n_valid;  // header: valid count
   uint32_t* skipped; // header: dS halves whose GEMM2 the gradient filter skipped (both passes)
   uint32_t* fallback; // header: non-zero when the online grad_input pass handed the call to the classic passes
+  uint32_t* vs_count; // header: vocabulary-split clusters of the online grad_input pass
   uint32_t* zf_neg;  // header: non-zero when the log form of dS does not apply (some valid row has
                      // f u <= 0 with u its upstream gradient, or the gradient scale is <= 0)
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
@@ -49,7 +53,11 @@ struct FusedWorkspace {
   float* row_loss;   // [BTp] valid * (LSE - z_y + z_loss LSE^2)
   float* colb2;      // [V rounded up to 256] bias * log2 e (0 without bias); -inf past V
   uint32_t* row_redo; // [BTp] online flow: 1 for a row the grad_input pass left to the classic passes
-  uint8_t* ds_l2;    // [kDsL2Slots][kDsL2SlotBytes] per-SM staging of dS blocks handed to the other pairs
+  float* vs_mref;    // [kMaxSplitUnits][256] online pass, vocabulary-split units: per-row reference
+  float4* vs_part;   // [kMaxSplitUnits][256][4][2] their pairs' partial sums
+  float4* vs_stat;   // [kMaxSplitUnits][256] their row sums
+  uint8_t* ds_l2;    // [kDsL2Slots][kDsL2SlotBytes] per-SM staging of dS blocks handed to the other pairs;
+                     // before the grad_W pass, the split units' accumulators
 };
 
 size_t fused_workspace_bytes(int64_t BT, int64_t V);
@@ -95,6 +103,7 @@ struct FusedArgs {
   float* logit_avg_out;       // [V] average logit per vocabulary entry out, or NULL (needs sort_vocab)
   int32_t* vocab_order_out;   // [V] sorted order out, or NULL (needs sort_vocab)
   bool separate_lse;          // always the classic flow (LSE tiles first)
+  int vocab_splits;           // online grad_input pass: 0 automatic, 1 never, k >= 2 every row block in k parts
 };
 
 // The vocabulary sort: logit_avg, the sorted order (in w.vals[0]), the sorted copies of W, the bias and
@@ -135,6 +144,14 @@ struct DgPairArgs {
   float* loss_tok;
   uint32_t* zf_neg_out;
   uint32_t* fallback;
+  // vocabulary-split units of the online pass: 0 = split the last, partly filled wave automatically,
+  // 1 = never, k >= 2 = every row block into (up to) k parts; their scratch (null: no splitting)
+  int vocab_splits;
+  float* vs_mref;
+  float4* vs_part;
+  float4* vs_stat;
+  float* vs_o;
+  uint32_t* vs_count;
 };
 
 // kVocabRows = false: grad_input pass (rows = tokens, reduction over the vocabulary);

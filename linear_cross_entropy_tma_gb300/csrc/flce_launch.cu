@@ -89,6 +89,12 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     po.loss_tok = a.loss_tok;
     po.zf_neg_out = ws.zf_neg;
     po.fallback = ws.fallback;
+    po.vocab_splits = a.vocab_splits;
+    po.vs_mref = ws.vs_mref;
+    po.vs_part = ws.vs_part;
+    po.vs_stat = ws.vs_stat;
+    po.vs_o = reinterpret_cast<float*>(ws.ds_l2);
+    po.vs_count = ws.vs_count;
     if ((e = launch_dgrad_online(tm_h, tm_w, po, stream)) != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
     if ((e = launch_loss_reduce(a, ws, stream)) != cudaSuccess) return e;

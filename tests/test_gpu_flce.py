@@ -89,14 +89,72 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("separate_lse", [False, True], ids=["lse-in-grad-input-pass", "separate-lse-pass"])
+FLOWS = {
+    # the default: LSE inside the grad_input pass, vocabulary-split clusters where the plan puts them
+    "online": {},
+    # the same pass with every cluster over the whole vocabulary
+    "online-whole-vocab": {"vocab_splits": 1},
+    "separate-lse-pass": {"separate_lse_pass": True},
+}
+
+
+@pytest.mark.parametrize("flow", sorted(FLOWS))
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_flce_matches_oracle(flce, name, separate_lse):
+def test_flce_matches_oracle(flce, name, flow):
     BT, H, V, bias, zl, red, ign = CASES[name]
     d = _synthetic(BT, H, V, bias, zl, red, ignore=ign, seed=BT * 7 + V)
-    out = _run(flce, d, separate_lse_pass=separate_lse)
+    out = _run(flce, d, **FLOWS[flow])
     assert out["status"] == 0
     _check_full(out, d)
+    if flow != "online":
+        assert flce.read_vocab_split_units(out["workspace"]) == 0
+
+
+# vocabulary-split clusters of the grad_input pass, forced: (BT, H, V, bias, z_loss, reduction, ignored rows,
+# parts asked for).  Two and three pairs per cluster, ragged BT / V / H, parts of unequal length.
+SPLIT_CASES = {
+    "H1024-two-parts": (600, 1024, 9000, True, 1e-4, "mean", (0, 599), 2),
+    "H1024-max-parts": (300, 1024, 12000, False, 0.0, "sum", (7,), 8),
+    "H768-three-pairs": (260, 768, 5000, True, 1e-3, "mean", (1,), 3),
+    "H200-one-pair-ragged": (513, 200, 4100, True, 0.0, "mean", (), 5),
+    "H2304-three-groups": (100, 2304, 3333, False, 1e-4, "mean", (50,), 3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SPLIT_CASES))
+def test_flce_vocab_split_units(flce, name):
+    BT, H, V, bias, zl, red, ign, k = SPLIT_CASES[name]
+    d = _synthetic(BT, H, V, bias, zl, red, ignore=ign, seed=BT + V + k)
+    out = _run(flce, d, vocab_splits=k)
+    assert out["status"] == 0
+    assert flce.read_vocab_split_units(out["workspace"]) > 0, "the pass did not split the vocabulary"
+    _check_full(out, d)
+
+
+def test_flce_vocab_split_options(flce):
+    # per-token upstream gradients, per-token losses, entropy and accumulation through the merge kernel
+    import torch
+    BT, H, V = 400, 1024, 7000
+    d = _synthetic(BT, H, V, True, 1e-4, "none", ignore=(3, 399), seed=77)
+    rng = np.random.Generator(np.random.PCG64(9))
+    gtok = rng.standard_normal(BT).astype(np.float32)
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], reduction="none", z_loss=1e-4,
+                                grad_loss_per_token=gtok)
+    gi0 = wl.f32_to_bf16_bits((rng.standard_normal((BT, H)) * np.std(ref["grad_input"])).astype(np.float32))
+    gw0 = (rng.standard_normal((V, H)) * np.std(ref["grad_W"])).astype(np.float32)
+    gb0 = (rng.standard_normal(V) * np.std(ref["grad_bias"])).astype(np.float32)
+    acc = {"grad_input": bf16_tensor(gi0), "grad_W": torch.from_numpy(gw0.copy()).cuda(),
+           "grad_bias": torch.from_numpy(gb0.copy()).cuda()}
+    out = _run(flce, d, vocab_splits=4, grad_loss_per_token=torch.from_numpy(gtok).cuda(), want_entropy=True,
+               accumulate=True, out=acc)
+    assert out["status"] == 0
+    assert flce.read_vocab_split_units(out["workspace"]) > 0
+    assert_grad_close(out["loss_per_token"].cpu().numpy(), ref["loss_per_token"], "loss_per_token")
+    assert_grad_close(out["entropy"].cpu().numpy(), ref["entropy"], "entropy")
+    assert_grad_close(bf16_to_numpy_f32(out["grad_input"]),
+                      ref["grad_input"] + (gi0.astype(np.uint32) << 16).view(np.float32), "grad_input (accumulated)")
+    assert_grad_close(out["grad_W"].cpu().numpy(), ref["grad_W"] + gw0, "grad_W (accumulated)")
+    assert_grad_close(out["grad_bias"].cpu().numpy(), ref["grad_bias"] + gb0, "grad_bias (accumulated)")
 
 
 def test_flce_tiny_workload(flce):
@@ -223,6 +281,20 @@ def test_flce_online_fallback(flce, H):
     out2 = _run(flce, d2)
     assert _fallback_flag(out2["workspace"]) == 0
     _check_full(out2, d2)
+
+
+def test_flce_online_fallback_vocab_split(flce):
+    # as above, with the vocabulary split: only the part whose reference comes from the -200 columns leaves
+    # the safe range, and its rows go to the classic passes
+    d = _synthetic(260, 512, 3000, True, 1e-4, "mean", ignore=(1, 200), seed=19)
+    d["bias"] = d["bias"].copy()
+    d["bias"][:128] = -200.0
+    d["target"][d["target"] < 128] = 300
+    out = _run(flce, d, vocab_splits=3)
+    assert out["status"] == 0
+    assert flce.read_vocab_split_units(out["workspace"]) > 0
+    assert _fallback_flag(out["workspace"]) == 1
+    _check_full(out, d)
 
 
 def test_flce_grad_input_and_bias_without_grad_W(flce):
