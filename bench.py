@@ -37,7 +37,8 @@ PAGES_TOKENS_PER_S = {"long": 65535 / 0.356}
 KERNELS_PER_STEP = 5  # lse_partial, lse_merge, loss_reduce, dgrad(grad_input), dgrad(grad_W); the two dgrad passes are one launch when both run
 # online flow: bias table, count, grad_input pass with the LSE, loss reduction, four gated classic kernels
 # (launched, exit at once unless the online pass asked for them), grad_W pass; plus the merge of the
-# vocabulary-split clusters when the grad_input pass splits its last wave
+# vocabulary-split clusters when the grad_input pass splits its last wave (and the same for the grad_W
+# pass's token-split clusters)
 KERNELS_PER_STEP_ONLINE = 9
 
 
@@ -207,6 +208,7 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
     loss = out["loss"].item()
     # vocabulary-split clusters the grad_input pass ran (its merge kernel is one more launch per step)
     split_units = flce.read_vocab_split_units(ws)
+    token_split_units = flce.read_token_split_units(ws)
 
     # end to end through the same public call from pinned host buffers: every step copies its inputs
     # host -> device, runs the call and copies the loss and both gradients device -> host.  The copies run
@@ -345,7 +347,7 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
         del ws_sort
     return dict(elapsed_ms=elapsed_ms, passes=passes, clocks=clocks, peak_mem=peak_mem, loss=loss, e2e_ms=e2e_ms,
                 e2e_serial_ms=e2e_serial_ms, h2d=h2d, d2h=d2h, workspace_bytes=ws.numel(), filter=filt,
-                split_units=split_units)
+                split_units=split_units, token_split_units=token_split_units)
 
 
 def bench_ce(steps: int, warmup: int, local: int, peaks: dict):
@@ -521,8 +523,10 @@ def main():
                           "convention": "8*BT*V*H per fused forward+backward"},
         "pass_ms": passes,
         "gpu_launches": ((KERNELS_PER_STEP_ONLINE + (1 if r["split_units"] else 0)) if online
-                         else KERNELS_PER_STEP - 1 if merged else KERNELS_PER_STEP) * args.steps,
+                         else KERNELS_PER_STEP - 1 if merged else KERNELS_PER_STEP)
+                        * args.steps + (args.steps if r["token_split_units"] else 0),
         "vocab_split_clusters": r["split_units"],
+        "token_split_clusters": r["token_split_units"],
         "clocks": r["clocks"],
         "e2e": {"value": world * w.BT / (r["e2e_ms"] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],

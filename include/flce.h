@@ -192,6 +192,12 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        allow k; at most 8).  Results are the same up to rounding order.  Negative:
  *                        FLCE_ERR_INVALID_ARG.  The number of vocabulary-split clusters the call ran is
  *                        the 32-bit word at byte 28 of the workspace.
+ *   token_splits         the same for the grad_W pass, whose clusters own vocabulary rows and run over
+ *                        the tokens: 0 splits the row blocks of its last, partly filled wave into token
+ *                        ranges (partial grad_W / grad_bias rows, added in order by a merge kernel), 1
+ *                        never, k >= 2 every row block into up to k ranges (within the workspace's
+ *                        scratch: fewer at small BT).  The number of token-split clusters is the word
+ *                        at byte 32 of the workspace.
  */
 typedef struct flce_fwd_bwd_options {
   float grad_scale;
@@ -205,6 +211,7 @@ typedef struct flce_fwd_bwd_options {
   int32_t* vocab_order;
   int separate_lse_pass;
   int vocab_splits;
+  int token_splits;
 } flce_fwd_bwd_options;
 
 /* Bytes of workspace flce_fwd_bwd_ex needs with these options (NULL: flce_workspace_size). */

@@ -34,7 +34,8 @@ class FwdBwdOptions(ctypes.Structure):
     _fields_ = [("grad_scale", ctypes.c_float), ("grad_loss_per_token", c_p), ("loss_per_token", c_p),
                 ("accumulate", ctypes.c_int), ("entropy", c_p), ("filter_eps", ctypes.c_float),
                 ("sort_vocab", ctypes.c_int), ("logit_avg", c_p), ("vocab_order", c_p),
-                ("separate_lse_pass", ctypes.c_int), ("vocab_splits", ctypes.c_int)]
+                ("separate_lse_pass", ctypes.c_int), ("vocab_splits", ctypes.c_int),
+                ("token_splits", ctypes.c_int)]
 
 
 def load() -> ctypes.CDLL:
@@ -115,7 +116,7 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
                  out=None, stream=None, pass_events=None, grad_scale: float = 1.0, grad_loss_per_token=None,
                  accumulate: bool = False, want_loss_per_token: bool = False, want_entropy: bool = False,
                  filter_eps: float = 0.0, sort_vocab: bool = False, separate_lse_pass: bool = False,
-                 vocab_splits: int = 0) -> dict:
+                 vocab_splits: int = 0, token_splits: int = 0) -> dict:
     """Fused linear cross-entropy forward + backward on the current CUDA device.
 
     hidden [BT, H] bf16, W [V, H] bf16, target [BT] int64, bias [V] fp32 or None.  Returns a dict with
@@ -133,7 +134,8 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     bound); ``sort_vocab`` runs every pass on the vocabulary sorted by average logit (adds ``logit_avg``,
     fp32 [V], and ``vocab_order``, int32 [V], to the result); ``separate_lse_pass`` computes the LSE in a
     pass of its own first instead of inside the grad_input pass; ``vocab_splits`` sets how that pass splits
-    the vocabulary of its row blocks (0 automatic, 1 never, k >= 2 up to k parts each) (flce_fwd_bwd_ex).
+    the vocabulary of its row blocks (0 automatic, 1 never, k >= 2 up to k parts each), ``token_splits`` the
+    same for the grad_W pass over token ranges (flce_fwd_bwd_ex).
     ``pass_events``: five
     recorded ``torch.cuda.Event(enable_timing=True)`` objects; the library re-records them at the pass
     boundaries (flce_fwd_bwd_timed) for per-kernel timing; only with the default options.
@@ -190,7 +192,7 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
             _ptr(o["loss"]), _ptr(gi), _ptr(gw), _ptr(gb), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel())
     plain = (red != 2 and grad_scale == 1.0 and grad_loss_per_token is None and not accumulate and lt is None
              and ent is None and filter_eps == 0.0 and not sort_vocab and not separate_lse_pass
-             and vocab_splits == 0)
+             and vocab_splits == 0 and token_splits == 0)
     if pass_events is not None:
         if not plain:
             raise ValueError("pass_events only with the default options")
@@ -203,7 +205,7 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     else:
         opts = FwdBwdOptions(float(grad_scale), _ptr(grad_loss_per_token), _ptr(lt), 1 if accumulate else 0, _ptr(ent),
                              float(filter_eps), 1 if sort_vocab else 0, _ptr(la), _ptr(vo),
-                             1 if separate_lse_pass else 0, int(vocab_splits))
+                             1 if separate_lse_pass else 0, int(vocab_splits), int(token_splits))
         check(load().flce_fwd_bwd_ex(*args, ctypes.byref(opts), _stream_ptr(stream)))
     res = dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, loss_per_token=lt,
                entropy=ent, workspace=workspace)
@@ -287,6 +289,14 @@ def read_vocab_split_units(workspace) -> int:
     import torch
     torch.cuda.synchronize(workspace.device)
     return int(workspace[28:32].cpu().view(torch.int32).item())
+
+
+def read_token_split_units(workspace) -> int:
+    """Token-split clusters the grad_W pass of the last flce_fwd_bwd on this workspace ran (the 32-bit
+    word at byte 32; synchronises the device)."""
+    import torch
+    torch.cuda.synchronize(workspace.device)
+    return int(workspace[32:36].cpu().view(torch.int32).item())
 
 
 def read_device_status(workspace, stream=None) -> int:

@@ -113,7 +113,7 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
                                 void* stream, void* const* events, int n_events) {
   g_last_error[0] = '\0';
   const flce_fwd_bwd_options opt =
-      options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0, nullptr, 0.0f, 0, nullptr, nullptr, 0, 0};
+      options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0, nullptr, 0.0f, 0, nullptr, nullptr, 0, 0, 0};
   if (n_events != 0 && (n_events != 5 || events == nullptr)) {
     set_error("n_events must be 0 or 5 (with a non-NULL event array)");
     return FLCE_ERR_INVALID_ARG;
@@ -144,8 +144,8 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
     set_error("filter_eps must be finite and >= 0");
     return FLCE_ERR_INVALID_ARG;
   }
-  if (opt.vocab_splits < 0) {
-    set_error("vocab_splits must be >= 0, got %d", opt.vocab_splits);
+  if (opt.vocab_splits < 0 || opt.token_splits < 0) {
+    set_error("vocab_splits and token_splits must be >= 0, got %d and %d", opt.vocab_splits, opt.token_splits);
     return FLCE_ERR_INVALID_ARG;
   }
   if (opt.sort_vocab == 0 && (opt.logit_avg != nullptr || opt.vocab_order != nullptr)) {
@@ -210,6 +210,7 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   a.vocab_order_out = opt.vocab_order;
   a.separate_lse = opt.separate_lse_pass != 0;
   a.vocab_splits = opt.vocab_splits;
+  a.token_splits = opt.token_splits;
   char err[256] = "";
   const cudaError_t e = flce::launch_fused(a, workspace, num_sms, static_cast<cudaStream_t>(stream), err, sizeof(err),
                                            n_events ? reinterpret_cast<cudaEvent_t const*>(events) : nullptr);

@@ -185,8 +185,10 @@ struct PairParams {
   float* vs_mref;           // [su][256] the unit's per-row reference
   float4* vs_part;          // [su][256][kMaxPairs][2] its pairs' partial sums (as part_g)
   float4* vs_stat;          // [su][256] (L, z_y or -inf, T, reference) over the unit's columns
-  float* vs_o;              // [su][256][P * 256] its unnormalised accumulator O
-  uint32_t* vs_count;       // receives the number of vocabulary-split units (workspace header)
+  float* vs_o;              // [su][256][P * 256] its unnormalised accumulator O (grad_W pass: its partial
+                            // grad_W rows, the units then covering token ranges)
+  float* vs_gb;             // grad_W pass: [su][256] partial grad_bias
+  uint32_t* vs_count;       // receives the number of split units (workspace header)
 };
 
 // The block whose GEMM1 pair `pr` works on in step s (the one it owns in [s+P+1, s+2P]) and which
@@ -957,8 +959,10 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         tmem_ld_32cols(tmem + (static_cast<uint32_t>(qq * 32) << 16) + kTmemO + 32u * c, vv);
         tmem_wait_ld();
         const int cb = 32 * c;
-        if (kOnline && su >= 0) {
-          // vocabulary-split unit: the raw accumulator columns of this pair, for online_vmerge_kernel
+        if (su >= 0) {
+          // split unit: the raw accumulator columns of this pair, for the merge kernel (grad_W pass: not
+          // needed when only grad_bias is asked for)
+          if (kVocabRows && p.grad_W == nullptr) continue;
           float* out = p.vs_o + (static_cast<size_t>(su) * 256 + rloc) * (P * kHc) + pr * kHc + cb;
 #pragma unroll
           for (int g4 = 0; g4 < 8; ++g4)
@@ -1046,8 +1050,12 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     if (row < p.V) {
       float acc = 0.f;
       for (int pp = 0; pp < P; ++pp) acc += sm.gb_gather[pp][rl];
-      const int orow = p.row_perm != nullptr ? p.row_perm[row] : row;
-      p.grad_bias[orow] = p.accumulate ? p.grad_bias[orow] + acc : acc;
+      if (su >= 0) {
+        p.vs_gb[static_cast<size_t>(su) * 256 + static_cast<int>(q) * kTileM + rl] = acc;   // for dw_vmerge_kernel
+      } else {
+        const int orow = p.row_perm != nullptr ? p.row_perm[row] : row;
+        p.grad_bias[orow] = p.accumulate ? p.grad_bias[orow] + acc : acc;
+      }
     }
   }
   if (warp == kMmaWarp) {
@@ -1057,39 +1065,89 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
   if (threadIdx.x == 0 && sm.abort) atomicOr(status, kStatusTimeout);
 }
 
-// One gradient pass: cluster (blockIdx.x / 2P, blockIdx.y).
+// Work units of a gradient pass, in launch order: n_whole clusters over all column blocks (row pair
+// u / groups, H group u % groups), then for the last row pairs, from rp_tail0 on, groups x nsplit clusters,
+// each over one of nsplit consecutive ranges of the nt column blocks (split units, numbered
+// su = (tail row pair x groups + group) x nsplit + part), which a merge kernel combines (online_vmerge_kernel
+// for the online grad_input pass, dw_vmerge_kernel for the grad_W pass).  Splitting the row pairs of a
+// partly filled last wave shortens that wave.
+struct UnitPlan {
+  int groups, n_whole, rp_tail0, nsplit, nt;
+};
+struct Unit {
+  int row_pair, hgroup, jb, je, su;
+};
+__device__ __forceinline__ Unit unit_of(const UnitPlan& plan, int c) {
+  Unit u{c / plan.groups, c % plan.groups, 0, plan.nt, -1};
+  if (c >= plan.n_whole) {
+    u.su = c - plan.n_whole;
+    const int part = u.su % plan.nsplit, ug = u.su / plan.nsplit;
+    u.row_pair = plan.rp_tail0 + ug / plan.groups;
+    u.hgroup = ug % plan.groups;
+    u.jb = (part * plan.nt) / plan.nsplit;
+    u.je = ((part + 1) * plan.nt) / plan.nsplit;
+  }
+  return u;
+}
+
+// One gradient pass: cluster blockIdx.x / 2P is work unit unit_of(plan, .).
 template <bool kVocabRows, bool kFilter>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
-                  const PairParams p, uint32_t* __restrict__ status) {
-  dgrad_pair_body<kVocabRows, kFilter>(tm_rows, tm_cols, p, status, static_cast<int>(blockIdx.x) / (2 * p.P),
-                                       static_cast<int>(blockIdx.y));
+                  const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan) {
+  const Unit u = unit_of(plan, static_cast<int>(blockIdx.x) / (2 * p.P));
+  dgrad_pair_body<kVocabRows, kFilter>(tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je, u.su);
 }
-
-// Work units of the online grad_input pass, in launch order: n_whole clusters over the whole vocabulary (row
-// pair u / groups, H group u % groups), then for the last row pairs, from rp_tail0 on, groups x nsplit
-// clusters each over one of nsplit consecutive ranges of the nt column blocks (vocabulary-split units,
-// numbered su = (tail row pair x groups + group) x nsplit + part), which online_vmerge_kernel combines.
-// Splitting the row pairs of a partly filled last wave shortens that wave.
-struct OnlinePlan {
-  int groups, n_whole, rp_tail0, nsplit, nt;
-};
 
 // The grad_input pass without a prior LSE pass: the same cluster layout as dgrad_pair_kernel<false>.
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_online_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
-                    const PairParams p, uint32_t* __restrict__ status, const OnlinePlan plan) {
-  const int c = static_cast<int>(blockIdx.x) / (2 * p.P);
-  int row_pair = c / plan.groups, hgroup = c % plan.groups, jb = 0, je = plan.nt, su = -1;
-  if (c >= plan.n_whole) {
-    su = c - plan.n_whole;
-    const int part = su % plan.nsplit, ug = su / plan.nsplit;
-    row_pair = plan.rp_tail0 + ug / plan.groups;
-    hgroup = ug % plan.groups;
-    jb = (part * plan.nt) / plan.nsplit;
-    je = ((part + 1) * plan.nt) / plan.nsplit;
+                    const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan) {
+  const Unit u = unit_of(plan, static_cast<int>(blockIdx.x) / (2 * p.P));
+  dgrad_pair_body<false, false, true>(tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je, u.su);
+}
+
+// The vocabulary rows of token-split units of the grad_W pass: grad_W[row] = sum over parts, in order, of
+// their partial rows (plus the old value when accumulating), the same for grad_bias.  One CTA of 128
+// threads per row.
+__global__ void __launch_bounds__(128) dw_vmerge_kernel(const PairParams p, const UnitPlan plan) {
+  const int t = static_cast<int>(blockIdx.x) / 256, rloc = static_cast<int>(blockIdx.x) % 256;
+  const int row = (plan.rp_tail0 + t) * 256 + rloc;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.vs_count != nullptr)
+    *p.vs_count = static_cast<uint32_t>(gridDim.x / 256 * plan.groups * plan.nsplit);
+  if (row >= p.V) return;
+  const int ns = plan.nsplit;
+  const int orow = p.row_perm != nullptr ? p.row_perm[row] : row;
+  const int span = p.P * kHc;
+  if (p.grad_W != nullptr) {
+    for (int h = 4 * static_cast<int>(threadIdx.x); h < p.H; h += 4 * 128) {
+      const int g = h / span, col = h - g * span;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int v = 0; v < ns; ++v) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(
+            p.vs_o + (static_cast<size_t>((t * plan.groups + g) * ns + v) * 256 + rloc) * span + col));
+        acc.x += x.x;
+        acc.y += x.y;
+        acc.z += x.z;
+        acc.w += x.w;
+      }
+      float4* out = reinterpret_cast<float4*>(p.grad_W + static_cast<size_t>(orow) * p.H + h);
+      if (p.accumulate) {
+        const float4 old = *out;
+        acc.x += old.x;
+        acc.y += old.y;
+        acc.z += old.z;
+        acc.w += old.w;
+      }
+      *out = acc;
+    }
   }
-  dgrad_pair_body<false, false, true>(tm_rows, tm_cols, p, status, row_pair, hgroup, jb, je, su);
+  if (threadIdx.x == 0 && p.grad_bias != nullptr) {
+    float acc = 0.f;
+    // (group 0's units carry grad_bias)
+    for (int v = 0; v < ns; ++v) acc += __ldcg(p.vs_gb + static_cast<size_t>(t * plan.groups * ns + v) * 256 + rloc);
+    p.grad_bias[orow] = p.accumulate ? p.grad_bias[orow] + acc : acc;
+  }
 }
 
 constexpr int kMaxVocabSplits = 8;
@@ -1098,7 +1156,7 @@ constexpr int kMaxVocabSplits = 8;
 // references R and added (L = sum_v 2^(ref_v - R) L_v, the same for T; z_y from the unit that saw the
 // target), then the row's outputs as in the pass itself (online_row_finish) and
 // grad_input[row] = c1 sum_v 2^(ref_v - R) O_v[row] + c2 W[y].  One CTA of 128 threads per row.
-__global__ void __launch_bounds__(128) online_vmerge_kernel(const PairParams p, const OnlinePlan plan) {
+__global__ void __launch_bounds__(128) online_vmerge_kernel(const PairParams p, const UnitPlan plan) {
   const int t = static_cast<int>(blockIdx.x) / 256, rloc = static_cast<int>(blockIdx.x) % 256;
   const int row = (plan.rp_tail0 + t) * 256 + rloc;
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.vs_count != nullptr)
@@ -1268,21 +1326,80 @@ cudaLaunchConfig_t cluster_config(dim3 grid, size_t smem, int P, cudaStream_t st
   return cfg;
 }
 
+// Clusters of 2P CTAs of this kernel resident at once (-1 if the query fails).
+template <class Kernel>
+int resident_clusters(Kernel kern, size_t smem, int P, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t q = cluster_config(dim3(2 * P, 1, 1), smem, P, stream, attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = -1;
+  }
+  return n;
+}
+
+// Split plan of a pass over row_pairs x groups clusters of nt column blocks (see UnitPlan).  forced: 0 =
+// split the row pairs of a partly filled last wave of `slots` resident clusters, each into
+// slots / (their clusters) parts; 1 = never; k >= 2 = every row pair into k parts.  Parts hold at least 4
+// column blocks; at most kMaxVocabSplits parts and su_cap split units.
+UnitPlan make_plan(int row_pairs, int groups, int nt, int slots, int forced, int su_cap) {
+  UnitPlan plan{groups, row_pairs * groups, row_pairs, 1, nt};
+  const int units = row_pairs * groups;
+  int tail_rp = 0, nsplit = 1;
+  if (forced >= 2) {
+    tail_rp = row_pairs;
+    nsplit = forced;
+  } else if (forced == 0 && slots > 0 && units % slots != 0) {
+    tail_rp = std::min(row_pairs, (units % slots + groups - 1) / groups);
+    nsplit = slots / (tail_rp * groups);
+  }
+  if (tail_rp > 0) nsplit = std::min({nsplit, kMaxVocabSplits, nt / 4, su_cap / (tail_rp * groups)});
+  if (tail_rp == 0 || nsplit < 2) return plan;
+  plan.nsplit = nsplit;
+  plan.rp_tail0 = row_pairs - tail_rp;
+  plan.n_whole = plan.rp_tail0 * groups;
+  return plan;
+}
+int clusters_of(const UnitPlan& plan, int row_pairs) {
+  return plan.n_whole + (row_pairs - plan.rp_tail0) * plan.groups * plan.nsplit;
+}
+
 }  // namespace
 
 template <bool kVocabRows>
 cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, const DgPairArgs& a,
                               cudaStream_t stream) {
   int h_chunks = 0;
-  const PairParams p = make_pair_params<kVocabRows>(a, &h_chunks);
+  PairParams p = make_pair_params<kVocabRows>(a, &h_chunks);
   constexpr size_t smem = pair_smem_bytes<kVocabRows>();
-  auto kern = p.filter_eps > 0.f ? dgrad_pair_kernel<kVocabRows, true> : dgrad_pair_kernel<kVocabRows, false>;
+  const bool filt = p.filter_eps > 0.f;
+  auto kern = filt ? dgrad_pair_kernel<kVocabRows, true> : dgrad_pair_kernel<kVocabRows, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  const int rp = row_pairs_of(p);
+  const int nt = (p.n_cols + kPN - 1) / kPN;
+  UnitPlan plan = make_plan(rp, h_chunks / p.P, nt, 0, 1, 0);
+  if (kVocabRows && a.split_scratch != nullptr) {
+    // token-split tail of the grad_W pass: partial rows in the caller's scratch
+    static int slots_of[2][kMaxPairs + 1] = {};
+    int& slots = slots_of[filt ? 1 : 0][p.P];
+    if (slots == 0) slots = resident_clusters(kern, smem, p.P, stream);
+    const size_t per_su = sizeof(float) * 256 * (static_cast<size_t>(p.P) * kHc + 1);
+    const int su_cap = static_cast<int>(std::min<size_t>(kMaxSplitUnits, a.split_scratch_bytes / per_su));
+    plan = make_plan(rp, h_chunks / p.P, nt, slots, a.token_splits, su_cap);
+    p.vs_o = a.split_scratch;
+    p.vs_gb = a.split_scratch + static_cast<size_t>(su_cap) * 256 * p.P * kHc;
+    p.vs_count = a.split_count;
+  }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * row_pairs_of(p), h_chunks / p.P, 1), smem, p.P, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, kern, rows, cols, p, a.status);
+  cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * clusters_of(plan, rp), 1, 1), smem, p.P, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, kern, rows, cols, p, a.status, plan);
   if (e != cudaSuccess) return e;
+  if (kVocabRows && plan.nsplit > 1) {
+    dw_vmerge_kernel<<<(rp - plan.rp_tail0) * 256, 128, 0, stream>>>(p, plan);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -1299,51 +1416,19 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   cudaError_t e =
       cudaFuncSetAttribute(dgrad_online_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  OnlinePlan plan{};
-  plan.groups = h_chunks / p.P;
-  plan.nt = (p.n_cols + kPN - 1) / kPN;
   const int rp = row_pairs_of(p);
-  cudaLaunchAttribute attr[1];
-  // clusters of this shape resident at once (queried once per shape; 0 if the query fails)
   static int slots_of[kMaxPairs + 1] = {};
-  if (slots_of[p.P] == 0) {
-    cudaLaunchConfig_t q = cluster_config(dim3(2 * p.P, 1, 1), smem, p.P, stream, attr);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, dgrad_online_kernel, &q) != cudaSuccess) {
-      (void)cudaGetLastError();
-      n = -1;
-    }
-    slots_of[p.P] = n;
-  }
-  const int slots = slots_of[p.P];
-  // vocabulary-split tail: the row pairs of the last, partly filled wave (or every row pair when the caller
-  // asks for a fixed number of parts), each part at least 4 column blocks, within the scratch
-  const int units = rp * plan.groups;
-  const int su_cap = static_cast<int>(std::min<size_t>(
+  if (slots_of[p.P] == 0) slots_of[p.P] = resident_clusters(dgrad_online_kernel, smem, p.P, stream);
+  // vocabulary-split tail: the accumulators go to the dS staging area (16 MiB, idle until the grad_W pass)
+  const int su_cap = a.vs_o == nullptr ? 0 : static_cast<int>(std::min<size_t>(
       kMaxSplitUnits, (static_cast<size_t>(kDsL2Slots) * kDsL2SlotBytes) / (sizeof(float) * 256 * p.P * kHc)));
-  int tail_rp = 0, nsplit = 1;
-  if (a.vocab_splits >= 2) {
-    tail_rp = rp;
-    nsplit = a.vocab_splits;
-  } else if (a.vocab_splits == 0 && slots > 0 && units % slots != 0) {
-    tail_rp = std::min(rp, (units % slots + plan.groups - 1) / plan.groups);
-    nsplit = slots / (tail_rp * plan.groups);
-  }
-  if (tail_rp > 0)
-    nsplit = std::min({nsplit, kMaxVocabSplits, plan.nt / 4, su_cap / (tail_rp * plan.groups)});
-  if (tail_rp == 0 || nsplit < 2 || a.vs_o == nullptr) {
-    tail_rp = 0;
-    nsplit = 1;
-  }
-  plan.nsplit = nsplit;
-  plan.rp_tail0 = rp - tail_rp;
-  plan.n_whole = (rp - tail_rp) * plan.groups;
-  const int n_clusters = plan.n_whole + tail_rp * plan.groups * nsplit;
-  cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * n_clusters, 1, 1), smem, p.P, stream, attr);
+  const UnitPlan plan = make_plan(rp, h_chunks / p.P, (p.n_cols + kPN - 1) / kPN, slots_of[p.P], a.vocab_splits, su_cap);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * clusters_of(plan, rp), 1, 1), smem, p.P, stream, attr);
   e = cudaLaunchKernelEx(&cfg, dgrad_online_kernel, hidden_map, w_map, p, a.status, plan);
   if (e != cudaSuccess) return e;
-  if (tail_rp > 0) {
-    online_vmerge_kernel<<<tail_rp * 256, 128, 0, stream>>>(p, plan);
+  if (plan.nsplit > 1) {
+    online_vmerge_kernel<<<(rp - plan.rp_tail0) * 256, 128, 0, stream>>>(p, plan);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaGetLastError();

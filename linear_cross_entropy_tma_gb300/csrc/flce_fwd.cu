@@ -457,9 +457,11 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   w.skipped = reinterpret_cast<uint32_t*>(p + 20);
   w.fallback = reinterpret_cast<uint32_t*>(p + 24);
   w.vs_count = reinterpret_cast<uint32_t*>(p + 28);
+  w.ts_count = reinterpret_cast<uint32_t*>(p + 32);
   size_t off = 256;
   w.part = reinterpret_cast<float2*>(p + off);
-  off += align_up(sizeof(float2) * kMaxSplits * btp, 256);
+  w.part_bytes = align_up(sizeof(float2) * kMaxSplits * btp, 256);
+  off += w.part_bytes;
   w.part_t = reinterpret_cast<float*>(p + off);
   off += align_up(sizeof(float) * kMaxSplits * btp, 256);
   w.zy = reinterpret_cast<float*>(p + off);

@@ -41,9 +41,12 @@ struct FusedWorkspace {
   uint32_t* skipped; // header: dS halves whose GEMM2 the gradient filter skipped (both passes)
   uint32_t* fallback; // header: non-zero when the online grad_input pass handed the call to the classic passes
   uint32_t* vs_count; // header: vocabulary-split clusters of the online grad_input pass
+  uint32_t* ts_count; // header: token-split clusters of the grad_W pass
   uint32_t* zf_neg;  // header: non-zero when the log form of dS does not apply (some valid row has
                      // f u <= 0 with u its upstream gradient, or the gradient scale is <= 0)
-  float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max))
+  float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max)); free again by the
+                     // grad_W pass, which keeps the partial rows of its token-split units there
+  size_t part_bytes;
   float* part_t;     // [kMaxSplits][BTp] sum of 2^(x - max) z (only when the entropy is requested)
   float* zy;         // [BTp] target logit
   float4* stats;     // [BT rounded up to 256] per row t, with LSE2 = LSE log2 e, f = 1 + 2 z_loss LSE and u
@@ -104,6 +107,7 @@ struct FusedArgs {
   int32_t* vocab_order_out;   // [V] sorted order out, or NULL (needs sort_vocab)
   bool separate_lse;          // always the classic flow (LSE tiles first)
   int vocab_splits;           // online grad_input pass: 0 automatic, 1 never, k >= 2 every row block in k parts
+  int token_splits;           // grad_W pass: the same over token ranges
 };
 
 // The vocabulary sort: logit_avg, the sorted order (in w.vals[0]), the sorted copies of W, the bias and
@@ -152,6 +156,12 @@ struct DgPairArgs {
   float4* vs_stat;
   float* vs_o;
   uint32_t* vs_count;
+  // token-split units of the grad_W pass (same meaning as vocab_splits); their partial rows go to
+  // split_scratch (null: no splitting)
+  int token_splits;
+  float* split_scratch;
+  size_t split_scratch_bytes;
+  uint32_t* split_count;
 };
 
 // kVocabRows = false: grad_input pass (rows = tokens, reduction over the vocabulary);

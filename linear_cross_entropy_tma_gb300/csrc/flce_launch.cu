@@ -67,6 +67,11 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
   pa.grad_W = a.grad_W;
   pa.grad_bias = a.grad_bias;
   pa.status = ws.status;
+  // (read by the grad_W pass only)
+  pa.token_splits = a.token_splits;
+  pa.split_scratch = reinterpret_cast<float*>(ws.part);
+  pa.split_scratch_bytes = ws.part_bytes;
+  pa.split_count = ws.ts_count;
   if (online) {
     // events: 1 after the bias table and count, 2 after the online grad_input pass, 3 after the loss
     // reduction and the gated classic passes, 4 after the grad_W pass

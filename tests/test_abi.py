@@ -85,8 +85,8 @@ def test_fwd_bwd_argument_errors(lib):
 
 
 def _fwd_ex(lib, red=2, loss=None, grad_scale=1.0, gtok=None, ltok=None, acc=0, gi=0x5000, ent=None, eps=0.0,
-            sort=0, la=None, vo=None, wsb=1 << 30, splits=0):
-    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent, eps, sort, la, vo, 0, splits)
+            sort=0, la=None, vo=None, wsb=1 << 30, splits=0, tsplits=0):
+    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent, eps, sort, la, vo, 0, splits, tsplits)
     return lib.flce_fwd_bwd_ex(0x1000, 0x2000, None, 0x3000, 128, 64, 512, -100, red, 0.0, loss, gi, 0x6000, None,
                                None, 0x7000, wsb, ctypes.byref(opts), None)
 
@@ -102,6 +102,8 @@ def test_fwd_bwd_ex_argument_errors(lib):
     assert _fwd_ex(lib, splits=-1) == INVALID_ARG
     assert _fwd_ex(lib, splits=3) == NO_DEVICE
     assert _fwd_ex(lib, splits=1000) == NO_DEVICE                         # (clamped, not an error)
+    assert _fwd_ex(lib, tsplits=-2) == INVALID_ARG
+    assert _fwd_ex(lib, tsplits=4) == NO_DEVICE
     assert _fwd_ex(lib, ltok=0x9002) == MISALIGNED
     assert _fwd_ex(lib, gtok=0x9001) == MISALIGNED
     assert _fwd_ex(lib, ent=0x9003) == MISALIGNED

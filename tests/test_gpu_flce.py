@@ -131,6 +131,45 @@ def test_flce_vocab_split_units(flce, name):
     _check_full(out, d)
 
 
+# token-split clusters of the grad_W pass, forced: (BT, H, V, bias, z_loss, reduction, ignored rows, parts).
+# Their partial rows live in the workspace's LSE-partials area (256 bytes per token), so BT must be large
+# enough for two or three units' rows of P x 256 fp32 columns (and V at most 256: one row block).
+DW_SPLIT_CASES = {
+    "H256-one-pair": (4096, 256, 250, True, 1e-4, "mean", (5,), 3),
+    "H512-two-pairs": (4500, 512, 200, True, 0.0, "sum", (), 2),
+    "H768-three-pairs": (6200, 768, 250, False, 1e-3, "mean", (1, 6199), 2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DW_SPLIT_CASES))
+def test_flce_token_split_units(flce, name):
+    BT, H, V, bias, zl, red, ign, k = DW_SPLIT_CASES[name]
+    d = _synthetic(BT, H, V, bias, zl, red, ignore=ign, seed=BT + V + 3 * k)
+    out = _run(flce, d, token_splits=k)
+    assert out["status"] == 0
+    assert flce.read_token_split_units(out["workspace"]) > 0, "the grad_W pass did not split the tokens"
+    _check_full(out, d)
+
+
+def test_flce_token_split_accumulate_sorted(flce):
+    # accumulation and the vocabulary sort's row permutation through the grad_W merge kernel
+    import torch
+    BT, H, V = 4096, 256, 250
+    d = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(9,), seed=31)
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], reduction="mean", z_loss=1e-4)
+    rng = np.random.Generator(np.random.PCG64(4))
+    gw0 = (rng.standard_normal((V, H)) * np.std(ref["grad_W"])).astype(np.float32)
+    gb0 = (rng.standard_normal(V) * np.std(ref["grad_bias"])).astype(np.float32)
+    gi0 = wl.f32_to_bf16_bits((rng.standard_normal((BT, H)) * np.std(ref["grad_input"])).astype(np.float32))
+    acc = {"grad_input": bf16_tensor(gi0), "grad_W": torch.from_numpy(gw0.copy()).cuda(),
+           "grad_bias": torch.from_numpy(gb0.copy()).cuda()}
+    out = _run(flce, d, token_splits=3, sort_vocab=True, accumulate=True, out=acc)
+    assert out["status"] == 0
+    assert flce.read_token_split_units(out["workspace"]) > 0
+    assert_grad_close(out["grad_W"].cpu().numpy(), ref["grad_W"] + gw0, "grad_W (accumulated)")
+    assert_grad_close(out["grad_bias"].cpu().numpy(), ref["grad_bias"] + gb0, "grad_bias (accumulated)")
+
+
 def test_flce_vocab_split_options(flce):
     # per-token upstream gradients, per-token losses, entropy and accumulation through the merge kernel
     import torch
