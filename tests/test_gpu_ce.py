@@ -50,6 +50,10 @@ def _run(flce, x, lab, z_loss):
     (5, 1, 1e-2, (2,)),              # V = 1: the CE part vanishes
     (300, 4101, 1e-4, (7, 299)),     # more rows than a few CTAs, ragged
     (3, 200003, 1e-4, ()),           # long rows: many iterations per thread
+    # aligned rows longer than the shared-memory head (the rest of each row re-read in pass 2)
+    (40, 65536, 0.0, ()),
+    (300, 50000, 1e-4, (5, 299)),    # many rows per CTA
+    (7, 131064, 1e-3, (2,)),
 ])
 def test_ce_matches_oracle(flce, B, V, z_loss, ignore):
     x, lab = _case(B, V, ignore=ignore, seed=B + V)
@@ -69,13 +73,14 @@ def test_ce_all_ignored_and_bad_labels(flce):
     assert int(out["n_valid"].item()) == 0 and out["ce_sum"].item() == 0.0 and out["z_sum"].item() == 0.0
     assert np.all(bf16_to_numpy_f32(logits) == 0.0)
     # a label outside [0, V) that is not ignore_index: the row is treated as ignored and flagged
-    x, lab = _case(12, 500, ignore=(1,), bad=(4, 9))
-    out, logits, status = _run(flce, x, lab, 1e-4)
-    assert status & flce.STATUS_BAD_TARGET
-    ref = oracle.ce_reference(x, lab, z_loss=1e-4)
-    assert int(out["n_valid"].item()) == ref["n_valid"] == 9
-    assert_scalar_close(out["ce_sum"].item(), ref["ce_sum"], "ce_sum")
-    assert_grad_close(bf16_to_numpy_f32(logits), ref["dlogits"], "dlogits")
+    for V in (500, 48000):   # (the second with rows longer than the shared-memory head)
+        x, lab = _case(12, V, ignore=(1,), bad=(4, 9))
+        out, logits, status = _run(flce, x, lab, 1e-4)
+        assert status & flce.STATUS_BAD_TARGET
+        ref = oracle.ce_reference(x, lab, z_loss=1e-4)
+        assert int(out["n_valid"].item()) == ref["n_valid"] == 9
+        assert_scalar_close(out["ce_sum"].item(), ref["ce_sum"], "ce_sum")
+        assert_grad_close(bf16_to_numpy_f32(logits), ref["dlogits"], "dlogits")
 
 
 def test_ce_empty(flce):
@@ -111,7 +116,8 @@ def test_ce_full_size(flce):
 
 @pytest.mark.parametrize("dtype", ["float16", "float32", "bfloat16"])
 @pytest.mark.parametrize("mode", ["inplace", "separate", "nograd"])
-@pytest.mark.parametrize("B,V,z_loss,ignore", [(300, 4101, 1e-4, (7, 299)), (37, 1003, 0.0, (0,)), (4, 130001, 1e-3, (1,))])
+@pytest.mark.parametrize("B,V,z_loss,ignore", [(300, 4101, 1e-4, (7, 299)), (37, 1003, 0.0, (0,)), (4, 130001, 1e-3, (1,)),
+                                                (6, 65536, 1e-3, (1,))])
 def test_ce_dtypes_and_modes(flce, dtype, mode, B, V, z_loss, ignore):
     import torch
     tdt = getattr(torch, dtype)
@@ -148,12 +154,13 @@ def test_ce_dtypes_and_modes(flce, dtype, mode, B, V, z_loss, ignore):
 def test_ce_separate_equals_inplace_bitwise(flce):
     # the non-mutating form runs the same arithmetic: its dlogits must equal the in-place result bit for bit
     import torch
-    x, lab = _case(96, 5003, ignore=(3,), seed=11)
-    a = bf16_tensor(x)
-    labels = torch.from_numpy(lab).cuda()
-    r = flce.cross_entropy(a, labels, z_loss=1e-4)
-    b = bf16_tensor(x)
-    flce.ce_with_grad(b, labels, z_loss=1e-4)
-    torch.cuda.synchronize()
-    assert torch.equal(r["dlogits"].view(torch.int16), b.view(torch.int16))
-    assert torch.equal(a.view(torch.int16), bf16_tensor(x).view(torch.int16))
+    for B, V in ((96, 5003), (33, 60000)):   # (the second with rows longer than the shared-memory head)
+        x, lab = _case(B, V, ignore=(3,), seed=11)
+        a = bf16_tensor(x)
+        labels = torch.from_numpy(lab).cuda()
+        r = flce.cross_entropy(a, labels, z_loss=1e-4)
+        b = bf16_tensor(x)
+        flce.ce_with_grad(b, labels, z_loss=1e-4)
+        torch.cuda.synchronize()
+        assert torch.equal(r["dlogits"].view(torch.int16), b.view(torch.int16))
+        assert torch.equal(a.view(torch.int16), bf16_tensor(x).view(torch.int16))
