@@ -196,8 +196,9 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        the tokens: 0 splits the row blocks of its last, partly filled wave into token
  *                        ranges (partial grad_W / grad_bias rows, added in order by a merge kernel), 1
  *                        never, k >= 2 every row block into up to k ranges (within the workspace's
- *                        scratch: fewer at small BT).  The number of token-split clusters is the word
- *                        at byte 32 of the workspace.
+ *                        scratch: fewer at small BT).  The classic flow's single launch of both passes
+ *                        (separate_lse_pass with grad_input and grad_W) does not split.  The number of
+ *                        token-split clusters is the word at byte 32 of the workspace.
  */
 typedef struct flce_fwd_bwd_options {
   float grad_scale;

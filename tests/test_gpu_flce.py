@@ -151,6 +151,18 @@ def test_flce_token_split_units(flce, name):
     _check_full(out, d)
 
 
+def test_flce_token_split_classic_flow(flce):
+    # without grad_input the call takes the classic flow: the LSE pass's partials occupy the scratch the
+    # grad_W pass's split clusters reuse once the merge has read them
+    BT, H, V, bias, zl, red, ign, k = DW_SPLIT_CASES["H512-two-pairs"]
+    d = _synthetic(BT, H, V, bias, zl, red, ignore=ign, seed=BT + V + 1)
+    out = _run(flce, d, token_splits=k, need_grad_input=False)
+    assert out["status"] == 0
+    assert flce.read_token_split_units(out["workspace"]) > 0
+    assert out["grad_input"] is None
+    _check_full(out, d)
+
+
 def test_flce_token_split_accumulate_sorted(flce):
     # accumulation and the vocabulary sort's row permutation through the grad_W merge kernel
     import torch
