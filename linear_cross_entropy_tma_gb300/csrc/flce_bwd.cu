@@ -44,6 +44,10 @@
 //     owners keep the row sums and the target logit, and at the end the pairs combine them into the LSE,
 //     the statistics and loss terms the rest of the call needs, and grad_input = G u (f O / L + (f p_y - 1)
 //     W[y]).  Rows whose sums leave the safe range are left to the classic passes.
+//   * Work units: a 1-D grid of clusters, row pair x H group.  When they do not fill their last wave, the
+//     row pairs of that wave are split over column ranges (the vocabulary in the grad_input pass, the
+//     tokens in the grad_W pass), one cluster per range, and the partial results of those clusters are
+//     combined by online_vmerge_kernel / dw_vmerge_kernel.
 // All waits are bounded; a wait that gives up flags the status word and the kernel winds down.
 #include <algorithm>
 
