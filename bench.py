@@ -210,6 +210,24 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
     split_units = flce.read_vocab_split_units(ws)
     token_split_units = flce.read_token_split_units(ws)
 
+    # the same call captured once into a CUDA graph and replayed (what a training loop that captures its
+    # step sees: no per-launch host overhead); same buffers, same inputs
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        flce.flce_fwd_bwd(hidden, W, target, **kw)
+    graph.replay()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record()
+    for _ in range(steps):
+        graph.replay()
+    g1.record()
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1), world) / steps
+    assert flce.read_device_status(ws) == 0, "device status word non-zero after the graph replays"
+    del graph
+
     # end to end through the same public call from pinned host buffers: every step copies its inputs
     # host -> device, runs the call and copies the loss and both gradients device -> host.  The copies run
     # on two copy streams with double-buffered device inputs and outputs, so step k's copies overlap the
@@ -347,7 +365,7 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
         del ws_sort
     return dict(elapsed_ms=elapsed_ms, passes=passes, clocks=clocks, peak_mem=peak_mem, loss=loss, e2e_ms=e2e_ms,
                 e2e_serial_ms=e2e_serial_ms, h2d=h2d, d2h=d2h, workspace_bytes=ws.numel(), filter=filt,
-                split_units=split_units, token_split_units=token_split_units)
+                split_units=split_units, token_split_units=token_split_units, graph_ms=graph_ms)
 
 
 def bench_ce(steps: int, warmup: int, local: int, peaks: dict):
@@ -525,6 +543,8 @@ def main():
         "gpu_launches": ((KERNELS_PER_STEP_ONLINE + (1 if r["split_units"] else 0)) if online
                          else KERNELS_PER_STEP - 1 if merged else KERNELS_PER_STEP)
                         * args.steps + (args.steps if r["token_split_units"] else 0),
+        "graph_replay": {"ms_per_step": r["graph_ms"], "tokens_per_s": world * w.BT / (r["graph_ms"] * 1e-3),
+                         "note": "the same call captured once into a CUDA graph, replayed steps times"},
         "vocab_split_clusters": r["split_units"],
         "token_split_clusters": r["token_split_units"],
         "clocks": r["clocks"],

@@ -348,6 +348,46 @@ def test_flce_online_fallback_vocab_split(flce):
     _check_full(out, d)
 
 
+@pytest.mark.parametrize("shape", [(600, 1024, 9000), (128, 64, 512)])
+def test_flce_cuda_graph_replay(flce, shape):
+    # the call captures into a CUDA graph (no host synchronisation, no allocation inside): a replay gives
+    # the eager call's results bit for bit, and replays on new inputs in the same buffers match the oracle
+    import torch
+    from linear_cross_entropy_tma_gb300 import _lib
+    BT, H, V = shape
+    d = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(0,), seed=5)
+    hidden, W, target, bias = _upload(d)
+    ws = torch.empty(_lib.workspace_size(BT, H, V), dtype=torch.uint8, device="cuda")
+    out = {"loss": torch.empty(1, device="cuda"), "n_valid": torch.empty(1, dtype=torch.int64, device="cuda"),
+           "grad_input": torch.empty((BT, H), dtype=torch.bfloat16, device="cuda"),
+           "grad_W": torch.empty((V, H), device="cuda"), "grad_bias": torch.empty(V, device="cuda")}
+    kw = dict(bias=bias, z_loss=1e-4, workspace=ws, out=out)
+    flce.flce_fwd_bwd(hidden, W, target, **kw)   # (one-time queries run outside the capture)
+    torch.cuda.synchronize()
+    eager = {k: v.clone() for k, v in out.items()}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        flce.flce_fwd_bwd(hidden, W, target, **kw)
+    for v in out.values():
+        v.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert flce.read_device_status(ws) == 0
+    for k in out:
+        assert torch.equal(out[k], eager[k]), f"graph replay differs from the eager call in {k}"
+    d2 = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(1, BT - 1), seed=6)
+    h2, w2, t2, b2 = _upload(d2)
+    hidden.copy_(h2)
+    W.copy_(w2)
+    target.copy_(t2)
+    bias.copy_(b2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert flce.read_device_status(ws) == 0
+    _check_full(dict(loss=out["loss"], n_valid=out["n_valid"], grad_input=out["grad_input"], grad_W=out["grad_W"],
+                     grad_bias=out["grad_bias"]), d2)
+
+
 def test_flce_grad_input_and_bias_without_grad_W(flce):
     # grad_W NULL with a bias: the grad_W pass covers one H chunk (one pair per cluster) while the
     # grad_input pass at H = 512 has two, so the two passes run as separate launches
