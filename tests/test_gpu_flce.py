@@ -438,3 +438,35 @@ def test_flce_full_size_sampled(flce, key):
     del out
     again = _run(flce, d, need_grad_input=False, need_grad_W=False)
     assert again["loss"].item() == first, "loss is not deterministic"
+
+
+@pytest.mark.parametrize("key", ["gemma2", "long"])
+def test_flce_full_size_split_tails(flce, key):
+    """The automatic split tails at the full sizes: every row of the split row pairs (grad_input) and every
+    vocabulary row of the split vocabulary row pairs (grad_W, grad_bias) against the same call with no
+    splitting (whose rows the sampled test above checks against the oracle), within the parity bounds."""
+    import torch
+    d = _full_inputs(key)
+    a = _run(flce, d)
+    assert a["status"] == 0
+    vs, ts = flce.read_vocab_split_units(a["workspace"]), flce.read_token_split_units(a["workspace"])
+    assert vs > 0, "the grad_input pass did not split its last wave"
+    b = _run(flce, d, vocab_splits=1, token_splits=1)
+    assert b["status"] == 0
+    assert flce.read_vocab_split_units(b["workspace"]) == 0 and flce.read_token_split_units(b["workspace"]) == 0
+    assert_scalar_close(a["loss"].item(), b["loss"].item(), "loss")
+    w = wl.FUSED_WORKLOADS[key]
+    # the split row pairs are the last ones: at least the last vs / (groups x parts) row pairs; compare the
+    # last 1024 rows (4 row pairs) and the last 1280 vocabulary rows (5 vocabulary row pairs)
+    r0 = max(0, w.BT - 1024)
+    assert_grad_close(bf16_to_numpy_f32(a["grad_input"][r0:]), bf16_to_numpy_f32(b["grad_input"][r0:]).astype(np.float64),
+                      "grad_input (split rows)")
+    v0 = max(0, w.V - 1280)
+    assert_grad_close(a["grad_W"][v0:].cpu().numpy(), b["grad_W"][v0:].cpu().numpy().astype(np.float64),
+                      "grad_W (split vocabulary rows)")
+    if a["grad_bias"] is not None:
+        assert_grad_close(a["grad_bias"][v0:].cpu().numpy(), b["grad_bias"][v0:].cpu().numpy().astype(np.float64),
+                          "grad_bias (split vocabulary rows)")
+    if key == "long":
+        assert ts > 0, "the grad_W pass did not split its last wave"
+
