@@ -75,10 +75,11 @@ constexpr int kStepOrder = 0;
 // multicast bulk load into the other pairs' CTAs; clear = shared-memory to shared-memory bulk copies
 // (also the fallback of a CTA whose SM id is past the staging table).
 // Measured on the 65535 x 1024 x 176245 workload: L2 for half 0 costs the grad_input pass ~3.5 ms (its
-// hand-over window is shorter than the store + load latency), half 1 is neutral there and saves ~0.6 ms
-// in the grad_W pass (fewer bulk copies competing with the operand loads).
+// hand-over window is shorter than the store + load latency), half 1 is neutral there.  In the grad_W
+// pass L2 for half 1 saves ~0.6 ms (fewer bulk copies competing with the operand loads), and for both
+// halves another ~0.4 ms (47.2-47.5 against 47.5-48.1 ms in one session).
 constexpr int kDsL2HalvesInput = 0;
-constexpr int kDsL2HalvesVocab = 2;
+constexpr int kDsL2HalvesVocab = 3;
 constexpr uint32_t kBox = kTileM * kBK * 2;   // 16 KiB: a 128-row x 64-column bf16 box
 constexpr uint32_t kStage = 2 * kBox;
 constexpr uint32_t kHalfBytes = 2 * kBox;     // one 128-column half of a dS block (per CTA)
