@@ -1155,7 +1155,7 @@ __global__ void __launch_bounds__(128) dw_vmerge_kernel(const PairParams p, cons
   }
 }
 
-constexpr int kMaxVocabSplits = 8;
+constexpr int kMaxSplitParts = 8;
 
 // The rows of vocabulary-split units: per row, the units' partial sums rescaled to the largest of their
 // references R and added (L = sum_v 2^(ref_v - R) L_v, the same for T; z_y from the unit that saw the
@@ -1168,10 +1168,10 @@ __global__ void __launch_bounds__(128) online_vmerge_kernel(const PairParams p, 
     *p.vs_count = static_cast<uint32_t>(gridDim.x / 256 * plan.groups * plan.nsplit);
   if (row >= p.BT) return;
   const int ns = plan.nsplit;
-  float ref[kMaxVocabSplits], w[kMaxVocabSplits];
+  float ref[kMaxSplitParts], w[kMaxSplitParts];
   float R = -INFINITY;
 #pragma unroll
-  for (int v = 0; v < kMaxVocabSplits; ++v) {
+  for (int v = 0; v < kMaxSplitParts; ++v) {
     ref[v] = -INFINITY;
     if (v < ns) {
       // (group 0's units: every group sees the same logits)
@@ -1182,7 +1182,7 @@ __global__ void __launch_bounds__(128) online_vmerge_kernel(const PairParams p, 
   float L = 0.f, zy = -INFINITY, T = 0.f;
   bool fin = true;
 #pragma unroll
-  for (int v = 0; v < kMaxVocabSplits; ++v) {
+  for (int v = 0; v < kMaxSplitParts; ++v) {
     w[v] = 0.f;
     if (v < ns) {
       const float4 st = __ldcg(&p.vs_stat[static_cast<size_t>(t * plan.groups * ns + v) * 256 + rloc]);
@@ -1204,7 +1204,7 @@ __global__ void __launch_bounds__(128) online_vmerge_kernel(const PairParams p, 
     const int g = h / span, col = h - g * span;
     float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int v = 0; v < kMaxVocabSplits; ++v) {
+    for (int v = 0; v < kMaxSplitParts; ++v) {
       if (v < ns) {
         const float* src = p.vs_o + (static_cast<size_t>((t * plan.groups + g) * ns + v) * 256 + rloc) * span + col;
         const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
@@ -1347,7 +1347,7 @@ int resident_clusters(Kernel kern, size_t smem, int P, cudaStream_t stream) {
 // Split plan of a pass over row_pairs x groups clusters of nt column blocks (see UnitPlan).  forced: 0 =
 // split the row pairs of a partly filled last wave of `slots` resident clusters, each into
 // slots / (their clusters) parts; 1 = never; k >= 2 = every row pair into k parts.  Parts hold at least 4
-// column blocks; at most kMaxVocabSplits parts and su_cap split units.
+// column blocks; at most kMaxSplitParts parts and su_cap split units.
 UnitPlan make_plan(int row_pairs, int groups, int nt, int slots, int forced, int su_cap) {
   UnitPlan plan{groups, row_pairs * groups, row_pairs, 1, nt};
   const int units = row_pairs * groups;
@@ -1359,7 +1359,7 @@ UnitPlan make_plan(int row_pairs, int groups, int nt, int slots, int forced, int
     tail_rp = std::min(row_pairs, (units % slots + groups - 1) / groups);
     nsplit = slots / (tail_rp * groups);
   }
-  if (tail_rp > 0) nsplit = std::min({nsplit, kMaxVocabSplits, nt / 4, su_cap / (tail_rp * groups)});
+  if (tail_rp > 0) nsplit = std::min({nsplit, kMaxSplitParts, nt / 4, su_cap / (tail_rp * groups)});
   if (tail_rp == 0 || nsplit < 2) return plan;
   plan.nsplit = nsplit;
   plan.rp_tail0 = row_pairs - tail_rp;
