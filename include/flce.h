@@ -183,13 +183,14 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        With filter_eps > 0 that grad_input pass is exact and only the grad_W pass
  *                        filters (a result within the same bound).
  *   vocab_splits         work split of that grad_input pass (default flow only).  0: automatic -- the
- *                        row blocks of its last, partly filled wave of clusters are each split into
- *                        vocabulary ranges processed by separate clusters, whose partial sums (against
- *                        their own references) a merge kernel rescales and adds ("Cut Cross Entropy
- *                        visualized", "Triton kernel, online softmax across vocab splits"); 1: never
- *                        split; k >= 2: split every row block into up to k ranges (fewer when the
- *                        scratch, 64 split clusters, or ranges of at least 4 x 256 columns do not
- *                        allow k; at most 8).  Results are the same up to rounding order.  Negative:
+ *                        row blocks of its last, partly filled wave of clusters (all of them when
+ *                        they fill less than a wave: small BT) are each split into vocabulary ranges
+ *                        processed by separate clusters, whose partial sums (against their own
+ *                        references) a merge kernel rescales and adds ("Cut Cross Entropy visualized",
+ *                        "Triton kernel, online softmax across vocab splits"); 1: never split; k >= 2:
+ *                        split every row block into up to k ranges (fewer when the scratch, 64 split
+ *                        clusters, or ranges of at least 4 x 256 columns do not allow k; at most 16).
+ *                        Results are the same up to rounding order.  Negative:
  *                        FLCE_ERR_INVALID_ARG.  The number of vocabulary-split clusters the call ran is
  *                        the 32-bit word at byte 28 of the workspace.
  *   token_splits         the same for the grad_W pass, whose clusters own vocabulary rows and run over

@@ -1155,7 +1155,7 @@ __global__ void __launch_bounds__(128) dw_vmerge_kernel(const PairParams p, cons
   }
 }
 
-constexpr int kMaxSplitParts = 8;
+constexpr int kMaxSplitParts = 16;
 
 // The rows of vocabulary-split units: per row, the units' partial sums rescaled to the largest of their
 // references R and added (L = sum_v 2^(ref_v - R) L_v, the same for T; z_y from the unit that saw the

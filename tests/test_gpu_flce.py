@@ -118,6 +118,7 @@ SPLIT_CASES = {
     "H768-three-pairs": (260, 768, 5000, True, 1e-3, "mean", (1,), 3),
     "H200-one-pair-ragged": (513, 200, 4100, True, 0.0, "mean", (), 5),
     "H2304-three-groups": (100, 2304, 3333, False, 1e-4, "mean", (50,), 3),
+    "H256-sixteen-parts": (300, 256, 20000, True, 1e-4, "mean", (3,), 16),
 }
 
 
