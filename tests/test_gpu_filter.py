@@ -53,16 +53,12 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("separate_lse", [False, True], ids=["lse-in-grad-input-pass", "separate-lse-pass"])
-@pytest.mark.parametrize("name", sorted(CASES))
-def test_filter_within_stated_bound(flce, name, separate_lse):
-    # (by default the grad_input pass finds the LSE itself and is exact; only the grad_W pass filters)
+def _check_filtered(flce, d, red, zl, eps, **kw):
+    """One filtered call against the oracle within the stated bound; returns the workspace."""
     import torch
-    BT, H, V, hs, bias, zl, red, eps, ign = CASES[name]
-    d = _inputs(BT, H, V, hs, bias, zl, red, seed=BT + V, ignore=ign)
+    V = d["W"].shape[0]
     hidden, W, target, b = _upload(d)
-    out = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction=red, z_loss=zl, filter_eps=eps,
-                            separate_lse_pass=separate_lse)
+    out = flce.flce_fwd_bwd(hidden, W, target, bias=b, reduction=red, z_loss=zl, filter_eps=eps, **kw)
     torch.cuda.synchronize()
     assert flce.read_device_status(out["workspace"]) == 0
     skips = flce.read_filter_skips(out["workspace"])
@@ -79,11 +75,29 @@ def test_filter_within_stated_bound(flce, name, separate_lse):
     assert_scalar_close(out["loss"].item(), ref["loss"], "loss")
     assert_within_bound(bf16_to_numpy_f32(out["grad_input"]), ref["grad_input"], small @ Wf, "grad_input")
     assert_within_bound(out["grad_W"].cpu().numpy(), ref["grad_W"], small.T @ hf, "grad_W")
-    if bias:
+    if d["bias"] is not None:
         gb = out["grad_bias"].cpu().numpy()
         assert np.max(np.abs(gb - ref["grad_bias"])) <= GRAD_MAXABS * np.max(np.abs(ref["grad_bias"]))
     # the filter must actually have skipped blocks here (both passes counted)
     assert skips > 0, "no dS block was skipped"
+    return out["workspace"]
+
+
+@pytest.mark.parametrize("separate_lse", [False, True], ids=["lse-in-grad-input-pass", "separate-lse-pass"])
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_filter_within_stated_bound(flce, name, separate_lse):
+    # (by default the grad_input pass finds the LSE itself and is exact; only the grad_W pass filters)
+    BT, H, V, hs, bias, zl, red, eps, ign = CASES[name]
+    d = _inputs(BT, H, V, hs, bias, zl, red, seed=BT + V, ignore=ign)
+    _check_filtered(flce, d, red, zl, eps, separate_lse_pass=separate_lse)
+
+
+def test_filter_with_split_tails(flce):
+    # the filtering grad_W pass with token-split clusters (its partial rows merged in order) within the
+    # same bound; BT large enough for the split scratch, 8 vocabulary blocks so that blocks are skippable
+    d = _inputs(20000, 256, 2000, 25.0, True, 1e-4, "mean", seed=41, ignore=(5, 19999))
+    ws = _check_filtered(flce, d, "mean", 1e-4, 2.0 ** -12, token_splits=2)
+    assert flce.read_token_split_units(ws) > 0
 
 
 def test_filter_threshold_below_every_entry_is_exact(flce):
