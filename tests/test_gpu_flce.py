@@ -139,6 +139,7 @@ DW_SPLIT_CASES = {
     "H256-one-pair": (4096, 256, 250, True, 1e-4, "mean", (5,), 3),
     "H512-two-pairs": (4500, 512, 200, True, 0.0, "sum", (), 2),
     "H768-three-pairs": (6200, 768, 250, False, 1e-3, "mean", (1, 6199), 2),
+    "H2304-three-groups": (20000, 2304, 250, True, 1e-4, "mean", (7,), 2),
 }
 
 
