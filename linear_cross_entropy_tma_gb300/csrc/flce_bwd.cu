@@ -1076,8 +1076,12 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
 // su = (tail row pair x groups + group) x nsplit + part), which a merge kernel combines (online_vmerge_kernel
 // for the online grad_input pass, dw_vmerge_kernel for the grad_W pass).  Splitting the row pairs of a
 // partly filled last wave shortens that wave.
+// Uneven form (jsplit > 0, nsplit = 2): each of the n_tail split row-pair clusters has a large part over
+// blocks [0, jsplit) and a small part over [jsplit, nt); all large parts are launched first, so that the
+// free slots of the last wave take the small parts (n_tail / (slots - n_tail) of them each).
 struct UnitPlan {
   int groups, n_whole, rp_tail0, nsplit, nt;
+  int jsplit, n_tail;
 };
 struct Unit {
   int row_pair, hgroup, jb, je, su;
@@ -1085,12 +1089,22 @@ struct Unit {
 __device__ __forceinline__ Unit unit_of(const UnitPlan& plan, int c) {
   Unit u{c / plan.groups, c % plan.groups, 0, plan.nt, -1};
   if (c >= plan.n_whole) {
-    u.su = c - plan.n_whole;
-    const int part = u.su % plan.nsplit, ug = u.su / plan.nsplit;
+    const int k = c - plan.n_whole;
+    int part, ug;
+    if (plan.jsplit > 0) {
+      part = k / plan.n_tail;
+      ug = k % plan.n_tail;
+      u.jb = part == 0 ? 0 : plan.jsplit;
+      u.je = part == 0 ? plan.jsplit : plan.nt;
+    } else {
+      part = k % plan.nsplit;
+      ug = k / plan.nsplit;
+      u.jb = (part * plan.nt) / plan.nsplit;
+      u.je = ((part + 1) * plan.nt) / plan.nsplit;
+    }
+    u.su = ug * plan.nsplit + part;
     u.row_pair = plan.rp_tail0 + ug / plan.groups;
     u.hgroup = ug % plan.groups;
-    u.jb = (part * plan.nt) / plan.nsplit;
-    u.je = ((part + 1) * plan.nt) / plan.nsplit;
   }
   return u;
 }
@@ -1348,8 +1362,11 @@ int resident_clusters(Kernel kern, size_t smem, int P, cudaStream_t stream) {
 // split the row pairs of a partly filled last wave of `slots` resident clusters, each into
 // slots / (their clusters) parts; 1 = never; k >= 2 = every row pair into k parts.  Parts hold at least 4
 // column blocks; at most kMaxSplitParts parts and su_cap split units.
-UnitPlan make_plan(int row_pairs, int groups, int nt, int slots, int forced, int su_cap) {
-  UnitPlan plan{groups, row_pairs * groups, row_pairs, 1, nt};
+//   With `uneven`, a last wave whose row pairs fill more than half of the slots (too many for equal
+// parts) is split unevenly instead: each of its n_tail clusters into a part of jsplit blocks and the
+// rest, so that the slots - n_tail free slots take the rests side by side and finish with the large parts.
+UnitPlan make_plan(int row_pairs, int groups, int nt, int slots, int forced, int su_cap, bool uneven) {
+  UnitPlan plan{groups, row_pairs * groups, row_pairs, 1, nt, 0, 0};
   const int units = row_pairs * groups;
   int tail_rp = 0, nsplit = 1;
   if (forced >= 2) {
@@ -1360,8 +1377,26 @@ UnitPlan make_plan(int row_pairs, int groups, int nt, int slots, int forced, int
     nsplit = slots / (tail_rp * groups);
   }
   if (tail_rp > 0) nsplit = std::min({nsplit, kMaxSplitParts, nt / 4, su_cap / (tail_rp * groups)});
+  if (tail_rp > 0 && nsplit < 2 && uneven && forced == 0 && tail_rp * groups < slots) {
+    // m small parts run back to back on each free slot; a split cluster also costs a fixed ~7 block steps
+    // (measured ~30 us at H = 1024: pipeline fill, reference, partial write-out), so the split point
+    // balances jsplit + c against m (nt - jsplit + c): jsplit = (m nt + (m - 1) c) / (m + 1)
+    constexpr int kPartCostBlocks = 7;
+    const int n_tail = tail_rp * groups;
+    const int m = (n_tail + (slots - n_tail) - 1) / (slots - n_tail);
+    const int jsplit = (m * nt + (m - 1) * kPartCostBlocks) / (m + 1);
+    if (2 * n_tail <= su_cap && jsplit >= 4 && nt - jsplit >= 4) {
+      plan.nsplit = 2;
+      plan.jsplit = jsplit;
+      plan.n_tail = n_tail;
+      plan.rp_tail0 = row_pairs - tail_rp;
+      plan.n_whole = plan.rp_tail0 * groups;
+    }
+    return plan;
+  }
   if (tail_rp == 0 || nsplit < 2) return plan;
   plan.nsplit = nsplit;
+  plan.n_tail = tail_rp * groups;
   plan.rp_tail0 = row_pairs - tail_rp;
   plan.n_whole = plan.rp_tail0 * groups;
   return plan;
@@ -1384,7 +1419,7 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   if (e != cudaSuccess) return e;
   const int rp = row_pairs_of(p);
   const int nt = (p.n_cols + kPN - 1) / kPN;
-  UnitPlan plan = make_plan(rp, h_chunks / p.P, nt, 0, 1, 0);
+  UnitPlan plan = make_plan(rp, h_chunks / p.P, nt, 0, 1, 0, false);
   if (kVocabRows && a.split_scratch != nullptr) {
     // token-split tail of the grad_W pass: partial rows in the caller's scratch
     static int slots_of[2][kMaxPairs + 1] = {};
@@ -1392,7 +1427,7 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
     if (slots == 0) slots = resident_clusters(kern, smem, p.P, stream);
     const size_t per_su = sizeof(float) * 256 * (static_cast<size_t>(p.P) * kHc + 1);
     const int su_cap = static_cast<int>(std::min<size_t>(kMaxSplitUnits, a.split_scratch_bytes / per_su));
-    plan = make_plan(rp, h_chunks / p.P, nt, slots, a.token_splits, su_cap);
+    plan = make_plan(rp, h_chunks / p.P, nt, slots, a.token_splits, su_cap, false);
     p.vs_o = a.split_scratch;
     p.vs_gb = a.split_scratch + static_cast<size_t>(su_cap) * 256 * p.P * kHc;
     p.vs_count = a.split_count;
@@ -1424,10 +1459,18 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   const int rp = row_pairs_of(p);
   static int slots_of[kMaxPairs + 1] = {};
   if (slots_of[p.P] == 0) slots_of[p.P] = resident_clusters(dgrad_online_kernel, smem, p.P, stream);
-  // vocabulary-split tail: the accumulators go to the dS staging area (16 MiB, idle until the grad_W pass)
-  const int su_cap = a.vs_o == nullptr ? 0 : static_cast<int>(std::min<size_t>(
-      kMaxSplitUnits, (static_cast<size_t>(kDsL2Slots) * kDsL2SlotBytes) / (sizeof(float) * 256 * p.P * kHc)));
-  const UnitPlan plan = make_plan(rp, h_chunks / p.P, (p.n_cols + kPN - 1) / kPN, slots_of[p.P], a.vocab_splits, su_cap);
+  // vocabulary-split tail: the accumulators go to the dS staging area (16 MiB, idle until the grad_W pass),
+  // or to grad_W when it is larger and holds nothing yet (written only by the grad_W pass, after the merge)
+  const size_t per_su = sizeof(float) * 256 * p.P * kHc;
+  size_t scratch = a.vs_o == nullptr ? 0 : static_cast<size_t>(kDsL2Slots) * kDsL2SlotBytes;
+  if (a.vs_o != nullptr && a.grad_W != nullptr && !a.accumulate &&
+      sizeof(float) * static_cast<size_t>(a.V) * a.H > scratch) {
+    scratch = sizeof(float) * static_cast<size_t>(a.V) * a.H;
+    p.vs_o = a.grad_W;
+  }
+  const int su_cap = static_cast<int>(std::min<size_t>(kMaxSplitUnits, scratch / per_su));
+  const UnitPlan plan =
+      make_plan(rp, h_chunks / p.P, (p.n_cols + kPN - 1) / kPN, slots_of[p.P], a.vocab_splits, su_cap, true);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * clusters_of(plan, rp), 1, 1), smem, p.P, stream, attr);
   e = cudaLaunchKernelEx(&cfg, dgrad_online_kernel, hidden_map, w_map, p, a.status, plan);
