@@ -1345,9 +1345,17 @@ cudaLaunchConfig_t cluster_config(dim3 grid, size_t smem, int P, cudaStream_t st
   return cfg;
 }
 
-// Clusters of 2P CTAs of this kernel resident at once (-1 if the query fails).
+// Clusters of 2P CTAs of this kernel resident at once (-1 if the query fails).  While the stream is being
+// captured into a CUDA graph the query is not made: 0, so that call plans no split tail and a later call
+// asks again.
 template <class Kernel>
 int resident_clusters(Kernel kern, size_t smem, int P, cudaStream_t stream) {
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  if (capture != cudaStreamCaptureStatusNone) return 0;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t q = cluster_config(dim3(2 * P, 1, 1), smem, P, stream, attr);
   int n = 0;

@@ -390,6 +390,43 @@ def test_flce_cuda_graph_replay(flce, shape):
                      grad_bias=out["grad_bias"]), d2)
 
 
+def test_flce_cuda_graph_capture_of_the_first_call(flce):
+    # in a fresh process the very first call is the captured one (its one-time occupancy queries are then
+    # skipped, not made inside the capture): the replay must match an eager call made afterwards
+    import subprocess
+    import sys
+    code = r"""
+import sys, torch
+sys.path.insert(0, %r)
+import linear_cross_entropy_tma_gb300 as flce
+from linear_cross_entropy_tma_gb300 import _lib
+torch.manual_seed(0)
+BT, H, V = 1000, 1024, 9000
+h = torch.randn(BT, H, device="cuda").bfloat16()
+W = (torch.randn(V, H, device="cuda") * 0.02).bfloat16()
+t = torch.randint(0, V, (BT,), device="cuda")
+ws = torch.empty(_lib.workspace_size(BT, H, V), dtype=torch.uint8, device="cuda")
+out = {"loss": torch.empty(1, device="cuda"), "grad_input": torch.empty((BT, H), dtype=torch.bfloat16, device="cuda"),
+       "grad_W": torch.empty((V, H), device="cuda")}
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g):
+    flce.flce_fwd_bwd(h, W, t, workspace=ws, out=out)
+g.replay()
+torch.cuda.synchronize()
+assert flce.read_device_status(ws) == 0
+first = {k: v.clone() for k, v in out.items()}
+r = flce.flce_fwd_bwd(h, W, t)   # eager, with the queries (and possibly a split plan) this time
+torch.cuda.synchronize()
+assert abs(r["loss"].item() - first["loss"].item()) <= 2e-4 * abs(first["loss"].item())
+for k in ("grad_input", "grad_W"):
+    a, b = first[k].float(), r[k].float()
+    assert ((a - b).norm() / b.norm()).item() < 5e-3, k
+print("ok")
+""" % (os.path.dirname(os.path.dirname(os.path.abspath(__file__))),)
+    p = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0 and p.stdout.strip().endswith("ok"), p.stdout + p.stderr
+
+
 def test_flce_grad_input_and_bias_without_grad_W(flce):
     # grad_W NULL with a bias: the grad_W pass covers one H chunk (one pair per cluster) while the
     # grad_input pass at H = 512 has two, so the two passes run as separate launches
