@@ -1,0 +1,71 @@
+"""Seeded randomised shapes and option combinations of flce_fwd_bwd against the fp64 oracle, through the
+C ABI: ragged BT / V / H (H a multiple of 8), bias, z-loss, the three reductions with per-token upstream
+gradients, ignored rows, both flows and forced vocabulary splits.  Element-wise bars as in the other
+parity tests."""
+import numpy as np
+import pytest
+
+import oracle
+from linear_cross_entropy_tma_gb300 import workloads as wl
+from parity import assert_grad_close, assert_scalar_close, bf16_tensor, bf16_to_numpy_f32
+
+pytestmark = pytest.mark.gpu
+N_CASES = 24
+
+
+@pytest.fixture(scope="module")
+def flce():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for -m gpu tests")
+    import linear_cross_entropy_tma_gb300 as m
+    m.load()
+    return m
+
+
+def _case(i):
+    rng = np.random.Generator(np.random.PCG64(1000 + i))
+    BT = int(rng.integers(1, 700))
+    H = 8 * int(rng.integers(1, 145))          # 8 .. 1152
+    V = int(rng.integers(1, 5000))
+    opts = dict(
+        bias=bool(rng.integers(0, 2)),
+        z_loss=float(rng.choice([0.0, 1e-4, 1e-2])),
+        reduction=str(rng.choice(["mean", "sum", "none"])),
+        separate_lse_pass=bool(rng.integers(0, 4) == 0),
+        vocab_splits=int(rng.choice([0, 1, 2, 3])),
+        ignore=int(rng.integers(0, 3)),
+        hidden_std=float(rng.choice([1.0, 4.0])),
+    )
+    return BT, H, V, opts, rng
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_case(flce, i):
+    import torch
+    BT, H, V, o, rng = _case(i)
+    w = wl.FusedWorkload("random", BT=BT, H=H, V=V, hidden_std=o["hidden_std"], w_std=0.02,
+                         bias_std=0.1 if o["bias"] else None, ignore_frac=0.0, z_loss=o["z_loss"],
+                         reduction=o["reduction"], seed=2000 + i)
+    d = wl.make_fused_inputs(w)
+    for r in rng.choice(BT, size=min(o["ignore"], BT), replace=False):
+        d["target"][r] = -100
+    gtok = (rng.standard_normal(BT).astype(np.float32) if o["reduction"] == "none" else None)
+    hidden, W = bf16_tensor(d["hidden"]), bf16_tensor(d["W"])
+    target = torch.from_numpy(d["target"]).cuda()
+    bias = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
+    out = flce.flce_fwd_bwd(hidden, W, target, bias=bias, reduction=o["reduction"], z_loss=o["z_loss"],
+                            grad_loss_per_token=torch.from_numpy(gtok).cuda() if gtok is not None else None,
+                            separate_lse_pass=o["separate_lse_pass"], vocab_splits=o["vocab_splits"])
+    torch.cuda.synchronize()
+    assert flce.read_device_status(out["workspace"]) == 0, f"case {i}: {BT}x{H}x{V} {o}"
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], reduction=o["reduction"],
+                                z_loss=o["z_loss"], grad_loss_per_token=gtok)
+    assert int(out["n_valid"].item()) == ref["n_valid"]
+    assert_scalar_close(out["loss"].item(), ref["loss"], f"loss (case {i})")
+    if o["reduction"] == "none":
+        assert_grad_close(out["loss_per_token"].cpu().numpy(), ref["loss_per_token"], f"loss_per_token (case {i})")
+    assert_grad_close(bf16_to_numpy_f32(out["grad_input"]), ref["grad_input"], f"grad_input (case {i})")
+    assert_grad_close(out["grad_W"].cpu().numpy(), ref["grad_W"], f"grad_W (case {i})")
+    if d["bias"] is not None:
+        assert_grad_close(out["grad_bias"].cpu().numpy(), ref["grad_bias"], f"grad_bias (case {i})")
