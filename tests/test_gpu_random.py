@@ -1,4 +1,5 @@
-"""Seeded randomised shapes and option combinations of flce_fwd_bwd against the fp64 oracle, through the
+"""Seeded randomised shapes and option combinations of flce_fwd_bwd and the standalone CE kernel against the
+fp64 oracle, through the
 C ABI: ragged BT / V / H (H a multiple of 8), bias, z-loss, the three reductions with per-token upstream
 gradients, ignored rows, both flows and forced vocabulary splits.  Element-wise bars as in the other
 parity tests."""
@@ -69,3 +70,42 @@ def test_random_case(flce, i):
     assert_grad_close(out["grad_W"].cpu().numpy(), ref["grad_W"], f"grad_W (case {i})")
     if d["bias"] is not None:
         assert_grad_close(out["grad_bias"].cpu().numpy(), ref["grad_bias"], f"grad_bias (case {i})")
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_ce_case(flce, i):
+    # the standalone CE kernel: random rows / vocabulary (aligned or not), dtype, in place / separate /
+    # loss only, ignored and out-of-range labels
+    import torch
+    rng = np.random.Generator(np.random.PCG64(3000 + i))
+    B = int(rng.integers(1, 400))
+    V = int(rng.integers(1, 60000)) if rng.integers(0, 2) else 8 * int(rng.integers(1, 8000))
+    dtype = str(rng.choice(["bfloat16", "float16", "float32"]))
+    mode = str(rng.choice(["inplace", "separate", "nograd"]))
+    z_loss = float(rng.choice([0.0, 1e-4, 1e-2]))
+    x32 = (rng.standard_normal((B, V)) * float(rng.choice([1.0, 3.0]))).astype(np.float32)
+    lab = rng.integers(0, V, B).astype(np.int64)
+    n_ign = int(rng.integers(0, 3))
+    for r in rng.choice(B, size=min(n_ign, B), replace=False):
+        lab[r] = -100
+    bad = bool(rng.integers(0, 4) == 0) and B > 1
+    if bad:
+        lab[B - 1] = V + 7
+    logits = torch.from_numpy(x32).to(getattr(torch, dtype)).cuda()
+    xin = logits.float().cpu().numpy().astype(np.float64)
+    labels = torch.from_numpy(lab).cuda()
+    if mode == "inplace":
+        r = flce.ce_with_grad(logits, labels, z_loss=z_loss)
+        dl = logits
+    else:
+        r = flce.cross_entropy(logits, labels, z_loss=z_loss, want_grad=(mode == "separate"))
+        dl = r["dlogits"]
+    torch.cuda.synchronize()
+    status = flce.read_device_status(r["workspace"])
+    assert status == (flce.STATUS_BAD_TARGET if bad else 0), f"case {i}: B={B} V={V} {dtype} {mode}"
+    ref = oracle.ce_reference(xin, lab, z_loss=z_loss)
+    assert int(r["n_valid"].item()) == ref["n_valid"]
+    assert_scalar_close(r["ce_sum"].item(), ref["ce_sum"], f"ce_sum (case {i})")
+    assert_scalar_close(r["z_sum"].item(), ref["z_sum"], f"z_sum (case {i})")
+    if mode != "nograd":
+        assert_grad_close(dl.float().cpu().numpy(), ref["dlogits"], f"dlogits (case {i})")
