@@ -1,8 +1,9 @@
-"""Seeded randomised shapes and option combinations of flce_fwd_bwd and the standalone CE kernel against the
-fp64 oracle, through the
-C ABI: ragged BT / V / H (H a multiple of 8), bias, z-loss, the three reductions with per-token upstream
-gradients, ignored rows, both flows and forced vocabulary splits.  Element-wise bars as in the other
-parity tests."""
+"""Seeded randomised shapes and option combinations against the fp64 oracle, through the C ABI.
+
+flce_fwd_bwd: ragged BT / V / H (H a multiple of 8), bias, z-loss, the three reductions with per-token
+upstream gradients, ignored rows, both flows and forced vocabulary splits.  The standalone CE kernel:
+aligned and ragged rows, the three logits types, in place / separate / loss only, ignored and
+out-of-range labels.  Element-wise bars as in the other parity tests."""
 import numpy as np
 import pytest
 
