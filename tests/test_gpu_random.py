@@ -1,7 +1,8 @@
 """Seeded randomised shapes and option combinations against the fp64 oracle, through the C ABI.
 
 flce_fwd_bwd: ragged BT / V / H (H a multiple of 8), bias, z-loss, the three reductions with per-token
-upstream gradients, ignored rows, both flows and forced vocabulary splits.  The standalone CE kernel:
+upstream gradients, ignored rows, both flows, forced vocabulary / token splits, accumulation and the
+vocabulary sort.  The standalone CE kernel:
 aligned and ragged rows, the three logits types, in place / separate / loss only, ignored and
 out-of-range labels.  Element-wise bars as in the other parity tests."""
 import numpy as np
@@ -39,6 +40,10 @@ def _case(i):
         ignore=int(rng.integers(0, 3)),
         hidden_std=float(rng.choice([1.0, 4.0])),
     )
+    # drawn after the above, so that adding them left the earlier draws of each case unchanged
+    opts["accumulate"] = bool(rng.integers(0, 4) == 0)
+    opts["sort_vocab"] = bool(rng.integers(0, 4) == 0)
+    opts["token_splits"] = int(rng.choice([0, 0, 1, 2]))
     return BT, H, V, opts, rng
 
 
@@ -56,21 +61,33 @@ def test_random_case(flce, i):
     hidden, W = bf16_tensor(d["hidden"]), bf16_tensor(d["W"])
     target = torch.from_numpy(d["target"]).cuda()
     bias = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
-    out = flce.flce_fwd_bwd(hidden, W, target, bias=bias, reduction=o["reduction"], z_loss=o["z_loss"],
-                            grad_loss_per_token=torch.from_numpy(gtok).cuda() if gtok is not None else None,
-                            separate_lse_pass=o["separate_lse_pass"], vocab_splits=o["vocab_splits"])
-    torch.cuda.synchronize()
-    assert flce.read_device_status(out["workspace"]) == 0, f"case {i}: {BT}x{H}x{V} {o}"
     ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], reduction=o["reduction"],
                                 z_loss=o["z_loss"], grad_loss_per_token=gtok)
+    acc, gi0, gw0, gb0 = None, 0.0, 0.0, 0.0
+    if o["accumulate"]:
+        # existing gradients of the same magnitude to add to
+        gi0b = wl.f32_to_bf16_bits((rng.standard_normal((BT, H)) * (np.std(ref["grad_input"]) + 1e-6)).astype(np.float32))
+        gi0 = (gi0b.astype(np.uint32) << 16).view(np.float32)
+        gw0 = (rng.standard_normal((V, H)) * (np.std(ref["grad_W"]) + 1e-6)).astype(np.float32)
+        acc = {"grad_input": bf16_tensor(gi0b), "grad_W": torch.from_numpy(gw0.copy()).cuda()}
+        if d["bias"] is not None:
+            gb0 = (rng.standard_normal(V) * (np.std(ref["grad_bias"]) + 1e-6)).astype(np.float32)
+            acc["grad_bias"] = torch.from_numpy(gb0.copy()).cuda()
+    out = flce.flce_fwd_bwd(hidden, W, target, bias=bias, reduction=o["reduction"], z_loss=o["z_loss"],
+                            grad_loss_per_token=torch.from_numpy(gtok).cuda() if gtok is not None else None,
+                            separate_lse_pass=o["separate_lse_pass"], vocab_splits=o["vocab_splits"],
+                            token_splits=o["token_splits"], sort_vocab=o["sort_vocab"],
+                            accumulate=o["accumulate"], out=acc)
+    torch.cuda.synchronize()
+    assert flce.read_device_status(out["workspace"]) == 0, f"case {i}: {BT}x{H}x{V} {o}"
     assert int(out["n_valid"].item()) == ref["n_valid"]
     assert_scalar_close(out["loss"].item(), ref["loss"], f"loss (case {i})")
     if o["reduction"] == "none":
         assert_grad_close(out["loss_per_token"].cpu().numpy(), ref["loss_per_token"], f"loss_per_token (case {i})")
-    assert_grad_close(bf16_to_numpy_f32(out["grad_input"]), ref["grad_input"], f"grad_input (case {i})")
-    assert_grad_close(out["grad_W"].cpu().numpy(), ref["grad_W"], f"grad_W (case {i})")
+    assert_grad_close(bf16_to_numpy_f32(out["grad_input"]), ref["grad_input"] + gi0, f"grad_input (case {i})")
+    assert_grad_close(out["grad_W"].cpu().numpy(), ref["grad_W"] + gw0, f"grad_W (case {i})")
     if d["bias"] is not None:
-        assert_grad_close(out["grad_bias"].cpu().numpy(), ref["grad_bias"], f"grad_bias (case {i})")
+        assert_grad_close(out["grad_bias"].cpu().numpy(), ref["grad_bias"] + gb0, f"grad_bias (case {i})")
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
