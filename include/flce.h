@@ -27,10 +27,14 @@
  *   - All tensor pointers are DEVICE pointers of the current CUDA device, row-major and contiguous.
  *     bf16 tensors are passed as uint16_t (raw bfloat16 bit patterns).
  *   - The caller owns and allocates every buffer, including the workspace.  The library keeps no
- *     state between calls and touches no memory other than the buffers it is given.
+ *     state between calls (beyond a per-process cache of how many clusters of each shape the device
+ *     holds at once) and touches no memory other than the buffers it is given.  (flce_fwd_bwd may use
+ *     grad_W as scratch before writing it, when the call does not accumulate.)
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and the call
- *     returns without synchronising.  Only flce_read_device_status synchronises the stream.
- *   - Outputs are overwritten, never accumulated into.
+ *     returns without synchronising.  Only flce_read_device_status synchronises the stream.  A call
+ *     can be captured into a CUDA graph and replayed; the occupancy query behind the cache is not made
+ *     while the stream is capturing (that call then plans no split tails, see vocab_splits).
+ *   - Outputs are overwritten (flce_fwd_bwd_ex can accumulate into them instead).
  *   - Argument errors are reported synchronously by the return code before anything is enqueued.
  *     Data errors (a target outside [0, V) that is not ignore_index) are found on the device: the
  *     row is treated as ignored and bit FLCE_STATUS_BAD_TARGET is set in the workspace status word.
