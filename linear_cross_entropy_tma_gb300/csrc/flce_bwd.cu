@@ -16,10 +16,9 @@
 //       GEMM1   S[256, 256] = rows[256, H] . cols[256, H]^T          (TMEM, 256 columns)
 //       epi     dS = f(S, statistics) in registers -> bf16 in shared memory, in the 128-byte-swizzled
 //               K-major layout of the next MMA's A operand; each epilogue warp hands its 32 rows to
-//               the same buffer of the other P-1 pairs' CTAs, either by cp.async.bulk copies between
-//               shared memories or through a 64 KiB per-SM staging block in L2 (a bulk store, then
-//               one multicast bulk load); never through HBM.  (Stores by the threads themselves,
-//               st.shared::cluster, measured about four times slower.)
+//               the same buffer of the other P-1 pairs' CTAs by cp.async.bulk copies between shared
+//               memories; never through HBM.  (Stores by the threads themselves, st.shared::cluster,
+//               measured about four times slower.)
 //     and every pair accumulates its own H chunk:
 //       GEMM2   O[256, 256] += dS[256, 256] . cols[256, chunk]      (TMEM, 256 columns, fp32)
 //     So the logits of each (row block, column block) are computed ceil(H / (256 P)) times instead of
@@ -70,16 +69,6 @@ static_assert(kFlagRing >= kMaxPairs + 2, "the skip-verdict ring must outlast P 
 // Order of a step's tensor work: 0 = GEMM2 half 0, half 1, then the GEMM1 share; 1 = the GEMM1 share
 // first; 2 = GEMM2 half 0, half of the share, GEMM2 half 1, the rest of the share.
 constexpr int kStepOrder = 0;
-// Hand-over of dS to the other pairs, per 128-column half (bit h of the mask of the grad_input pass,
-// resp. the grad_W pass): set = bulk store of the owner's rows to a per-SM staging block in L2, then one
-// multicast bulk load into the other pairs' CTAs; clear = shared-memory to shared-memory bulk copies
-// (also the fallback of a CTA whose SM id is past the staging table).
-// Measured on the 65535 x 1024 x 176245 workload: L2 for half 0 costs the grad_input pass ~3.5 ms (its
-// hand-over window is shorter than the store + load latency), half 1 is neutral there.  In the grad_W
-// pass L2 for half 1 saves ~0.6 ms (fewer bulk copies competing with the operand loads), and for both
-// halves another ~0.4 ms (47.2-47.5 against 47.5-48.1 ms in one session).
-constexpr int kDsL2HalvesInput = 0;
-constexpr int kDsL2HalvesVocab = 3;
 constexpr uint32_t kBox = kTileM * kBK * 2;   // 16 KiB: a 128-row x 64-column bf16 box
 constexpr uint32_t kStage = 2 * kBox;
 constexpr uint32_t kHalfBytes = 2 * kBox;     // one 128-column half of a dS block (per CTA)
@@ -134,7 +123,6 @@ template <bool kVocabRows>
 constexpr size_t pair_smem_bytes() { return sizeof(PairSmem<kVocabRows>) + 1024; }
 static_assert(pair_smem_bytes<false>() <= 232448, "shared memory budget of one CTA exceeded");
 static_assert(pair_smem_bytes<true>() <= 232448, "shared memory budget of one CTA exceeded");
-static_assert(kDsBytes == kDsL2SlotBytes, "an L2 staging block holds one CTA's dS block");
 
 // Gradient filter: the verdict on half `half` of block j, once the 8 epilogue warps of its owner pair that
 // hold the half (4 per CTA) have published theirs: 1 = every pair skips it (no operand stage, no MMA, no
@@ -160,7 +148,6 @@ struct PairParams {
   int accumulate;
   float filter_eps;         // > 0: skip GEMM2 of dS halves whose entries are all below it
   uint32_t* skip_count;     // halves skipped (filter statistics)
-  uint8_t* ds_l2;           // per-SM dS staging blocks (kDsL2Slots x kDsL2SlotBytes), or null
   const int32_t* row_perm;  // grad_W pass: output row of each vocabulary row (vocabulary sort), or null
   int BT, V, H;
   int n_rows, n_cols, num_kb;
@@ -735,14 +722,6 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     }
     float gbias = 0.f;
     bool ok = true;
-    // this CTA's L2 staging block for the dS it hands to the other pairs (null: shared-memory copies)
-    uint8_t* l2_stage = nullptr;
-    if (((kVocabRows ? kDsL2HalvesVocab : kDsL2HalvesInput) >> hh) & 1) {
-      if (P > 1 && p.ds_l2 != nullptr) {
-        const uint32_t sid = sm_id();
-        if (sid < static_cast<uint32_t>(kDsL2Slots)) l2_stage = p.ds_l2 + static_cast<size_t>(sid) * kDsL2SlotBytes;
-      }
-    }
     uint8_t* const ds_row = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(rl) * 128u;
     if (filt) {
       // O starts at zero (GEMM2 then always accumulates, whichever halves are skipped): this warp's 32
@@ -871,7 +850,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       // A verdict wait that gave up sends the data (the kernel is winding down by then).
       bool send = true;
       if (filt && lane == 0) send = filter_verdict(sm, j, hh, abort) != 1;
-      if (lane == 0 && l2_stage == nullptr) {
+      if (lane == 0) {
         // this warp's 32 rows of both 64-column boxes to the other pairs' CTAs with the same rows
         uint8_t* const src = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
         for (int pp = 0; pp < P; ++pp) {
@@ -888,30 +867,6 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
       named_barrier_sync(1 + hh, 4 * 32);
       if (qq == 0 && lane == 0) mbar_arrive_cluster(ds_full_c);
-      if (l2_stage != nullptr && lane == 0 && !send) {
-        for (int pp = 0; pp < P; ++pp) {
-          if (pp == pr) continue;
-          mbar_complete_tx_cluster(mapa_shared(smem_u32(&sm.rx_full[hh]), static_cast<uint32_t>(2 * pp) + q), 2u * 4096u);
-        }
-      }
-      if (l2_stage != nullptr && lane == 0 && send) {
-        // this warp's 32 rows of both 64-column boxes through L2: store, wait until the writes are done,
-        // then one multicast load into the other pairs' CTAs with the same rows (completing on their
-        // rx_full[hh]).  The staging block is rewritten only for this CTA's next block, after every pair
-        // has finished GEMM2 with this one (ds_free), so after these loads have landed.
-        const uint32_t off = static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
-        uint8_t* const src = sm.ds + off;
-        bulk_store_1d(l2_stage + off, src, 4096u);
-        bulk_store_1d(l2_stage + off + kBox, src + kBox, 4096u);
-        bulk_commit_group();
-        bulk_wait_group_all();
-        fence_proxy_async_global();
-        uint16_t mask = 0;
-        for (int pp = 0; pp < P; ++pp)
-          if (pp != pr) mask |= static_cast<uint16_t>(1u << (2 * pp + static_cast<int>(q)));
-        bulk_load_1d_multicast(src, l2_stage + off, 4096u, &sm.rx_full[hh], mask);
-        bulk_load_1d_multicast(src + kBox, l2_stage + off + kBox, 4096u, &sm.rx_full[hh], mask);
-      }
     }
 
     // online form: every pair's partial sums of this row combined into the row's outputs (online_row_finish),
@@ -1297,7 +1252,6 @@ PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
   p.accumulate = a.accumulate ? 1 : 0;
   p.filter_eps = a.filter_eps;
   p.skip_count = a.skip_count;
-  p.ds_l2 = a.ds_l2;
   p.row_perm = a.row_perm;
   p.BT = a.BT;
   p.V = a.V;
@@ -1467,10 +1421,10 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   const int rp = row_pairs_of(p);
   static int slots_of[kMaxPairs + 1] = {};
   if (slots_of[p.P] == 0) slots_of[p.P] = resident_clusters(dgrad_online_kernel, smem, p.P, stream);
-  // vocabulary-split tail: the accumulators go to the dS staging area (16 MiB, idle until the grad_W pass),
+  // vocabulary-split tail: the accumulators go to the split scratch (16 MiB),
   // or to grad_W when it is larger and holds nothing yet (written only by the grad_W pass, after the merge)
   const size_t per_su = sizeof(float) * 256 * p.P * kHc;
-  size_t scratch = a.vs_o == nullptr ? 0 : static_cast<size_t>(kDsL2Slots) * kDsL2SlotBytes;
+  size_t scratch = a.vs_o == nullptr ? 0 : kSplitAccBytes;
   if (a.vs_o != nullptr && a.grad_W != nullptr && !a.accumulate &&
       sizeof(float) * static_cast<size_t>(a.V) * a.H > scratch) {
     scratch = sizeof(float) * static_cast<size_t>(a.V) * a.H;

@@ -441,7 +441,7 @@ size_t fused_workspace_bytes(int64_t BT, int64_t V) {
   off += sizeof(float) * kMaxSplitUnits * 256;
   off += sizeof(float4) * kMaxSplitUnits * 256 * 8;
   off += sizeof(float4) * kMaxSplitUnits * 256;
-  off += kDsL2Slots * kDsL2SlotBytes;
+  off += kSplitAccBytes;
   return off;
 }
 
@@ -480,7 +480,7 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   off += sizeof(float4) * kMaxSplitUnits * 256 * 8;
   w.vs_stat = reinterpret_cast<float4*>(p + off);
   off += sizeof(float4) * kMaxSplitUnits * 256;
-  w.ds_l2 = p + off;
+  w.split_acc = reinterpret_cast<float*>(p + off);
   return w;
 }
 

@@ -26,12 +26,10 @@ namespace flce {
 constexpr int kMaxSplits = 32;     // vocabulary splits of the LSE pass
 constexpr int kTileM = 128;        // rows of every MMA tile (tokens or vocabulary rows)
 
-// dS hand-over through L2 in the gradient passes: one 64 KiB staging block per SM id (a CTA of those
-// passes occupies its SM alone); CTAs on SM ids past the table use shared-memory copies instead.
-constexpr int kDsL2Slots = 256;
-constexpr size_t kDsL2SlotBytes = 65536;
+// Accumulator scratch of the vocabulary-split units of the online grad_input pass (16 MiB).
+constexpr size_t kSplitAccBytes = size_t(16) << 20;
 // Vocabulary-split work units of the online grad_input pass (see launch_dgrad_online): at most this many,
-// their accumulators in the dS staging area (free until the grad_W pass), their row sums in vs_*.
+// their accumulators in the split scratch (or in grad_W, see launch_dgrad_online), their row sums in vs_*.
 constexpr int kMaxSplitUnits = 64;
 
 struct FusedWorkspace {
@@ -59,8 +57,7 @@ struct FusedWorkspace {
   float* vs_mref;    // [kMaxSplitUnits][256] online pass, vocabulary-split units: per-row reference
   float4* vs_part;   // [kMaxSplitUnits][256][4][2] their pairs' partial sums
   float4* vs_stat;   // [kMaxSplitUnits][256] their row sums
-  uint8_t* ds_l2;    // [kDsL2Slots][kDsL2SlotBytes] per-SM staging of dS blocks handed to the other pairs;
-                     // before the grad_W pass, the split units' accumulators
+  float* split_acc;  // [kSplitAccBytes] accumulators of the online pass's vocabulary-split units
 };
 
 size_t fused_workspace_bytes(int64_t BT, int64_t V);
@@ -126,7 +123,6 @@ struct DgPairArgs {
   bool accumulate;
   float filter_eps;
   uint32_t* skip_count;
-  uint8_t* ds_l2;
   const int32_t* row_perm;   // grad_W pass: output row of each (sorted) vocabulary row, or NULL
   int BT, V, H;
   uint16_t* grad_input;

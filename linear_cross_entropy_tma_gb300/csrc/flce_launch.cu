@@ -58,7 +58,6 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
   pa.accumulate = a.accumulate;
   pa.filter_eps = a.filter_eps;
   pa.skip_count = ws.skipped;
-  pa.ds_l2 = ws.ds_l2;
   pa.row_perm = row_perm;
   pa.BT = static_cast<int>(a.BT);
   pa.V = static_cast<int>(a.V);
@@ -98,7 +97,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     po.vs_mref = ws.vs_mref;
     po.vs_part = ws.vs_part;
     po.vs_stat = ws.vs_stat;
-    po.vs_o = reinterpret_cast<float*>(ws.ds_l2);
+    po.vs_o = ws.split_acc;
     po.vs_count = ws.vs_count;
     if ((e = launch_dgrad_online(tm_h, tm_w, po, stream)) != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;

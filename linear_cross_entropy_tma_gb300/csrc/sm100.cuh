@@ -27,11 +27,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t sm_id() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
-  return r;
-}
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 // ------------------------------------------------------------------------------------------ mbarrier
@@ -135,40 +130,6 @@ __device__ __forceinline__ void bulk_load_1d_hint(void* smem_dst, const void* gs
       ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-
-// 1-D bulk copy this CTA's shared memory -> global, tracked by bulk async-groups of the issuing thread.
-__device__ __forceinline__ void bulk_store_1d_hint(void* gdst, const void* smem_src, uint32_t bytes, uint64_t policy) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
-               ::"l"(reinterpret_cast<uint64_t>(gdst)), "r"(smem_u32(smem_src)), "r"(bytes), "l"(policy)
-               : "memory");
-}
-// 1-D bulk copy this CTA's shared memory -> global, tracked by bulk async-groups of the issuing thread.
-__device__ __forceinline__ void bulk_store_1d(void* gdst, const void* smem_src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-               ::"l"(reinterpret_cast<uint64_t>(gdst)), "r"(smem_u32(smem_src)), "r"(bytes)
-               : "memory");
-}
-// 1-D bulk copy global -> the same shared-memory offset in every CTA of `cta_mask` (cluster ranks);
-// the byte count completes on the mbarrier at `bar`'s offset in each of those CTAs.
-__device__ __forceinline__ void bulk_load_1d_multicast(const void* smem_dst_offset, const void* gsrc, uint32_t bytes,
-                                                       const uint64_t* bar_offset, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;"
-      ::"r"(smem_u32(smem_dst_offset)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar_offset)),
-        "h"(cta_mask)
-      : "memory");
-}
-// Orders this thread's completed async-proxy global writes before its later async-proxy reads (and
-// generic accesses) of global memory.
-__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until at most N committed bulk groups of this thread still have to read their shared-memory source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Wait until every committed bulk group of this thread has completed (writes visible).
-__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
