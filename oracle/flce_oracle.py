@@ -25,7 +25,7 @@ Definitions followed (page, section):
                                                                                  gradient together"
   * loss = ce_sum / max(n_valid, 1)                                           p3 "Usage" (raw helper)
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent:
   * with z-loss in the fused loss, l_t = LSE_t - z_y + z_loss * LSE_t^2, so the gradient row is
     p * (1 + 2 z_loss LSE_t) - onehot(y_t);
   * n_valid = 0 gives loss 0 and all-zero gradients (the clamp of p3 "Usage");

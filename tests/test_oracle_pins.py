@@ -9,7 +9,10 @@
   * the unreduced loss with an upstream gradient against finite differences and torch autograd;
   * the per-row entropy against torch, plain loops, closed forms and its bounds;
   * the average logit per vocabulary entry against loops, closed forms and the linearity identity, and
-    the vocabulary order against a hand-evaluated case and brute force.
+    the vocabulary order against a hand-evaluated case and brute force;
+  * the widening of bf16 bit patterns against hand-evaluated values (zeros, subnormals, infinities, the
+    largest finite values) and torch's bfloat16 decoding of all 65536 patterns, and the loss and
+    gradients from bit patterns against torch.
 
 The same checks run against deliberately broken copies of the oracle (test_planted_mistakes) to show
 that a dropped term, a wrong sign, a wrong index or a wrong scale fails at least one of them.
@@ -326,6 +329,51 @@ def pin_dlogits_matrix(orc):
         assert _rel(d.T @ hidden, g["grad_W"]) < 1e-12
 
 
+def pin_widen_bf16_bits(orc):
+    # bf16 bit patterns (uint16) widen to the exact value they encode: against hand-evaluated values
+    # (sign, exponent field e, fraction f: (-1)^s 2^(e-127) (1 + f/128), subnormals 2^-126 f/128) and
+    # against torch's own bfloat16 decoding
+    cases = {
+        0x0000: 0.0, 0x8000: -0.0, 0x0001: math.ldexp(1.0, -133), 0x8001: -math.ldexp(1.0, -133),
+        0x007F: math.ldexp(127.0, -133), 0x0080: math.ldexp(1.0, -126), 0x3F80: 1.0, 0xBF80: -1.0,
+        0x3FC0: 1.5, 0xC000: -2.0, 0x4049: 3.140625, 0x3DCD: 0.10009765625, 0x477F: 65280.0,
+        0x4780: 65536.0, 0x7F7F: math.ldexp(255.0, 120), 0xFF7F: -math.ldexp(255.0, 120),
+        0x7F80: math.inf, 0xFF80: -math.inf,
+    }
+    bits = np.array(sorted(cases), dtype=np.uint16)
+    got = orc.widen(bits)
+    assert got.dtype == np.float64 and got.shape == bits.shape
+    for b_, v in zip(bits.tolist(), got.tolist()):
+        assert v == cases[b_] and math.copysign(1.0, v) == math.copysign(1.0, cases[b_]), (hex(b_), v, cases[b_])
+    assert np.isnan(orc.widen(np.array([0x7FC0, 0xFFC1], dtype=np.uint16))).all()
+    rng = np.random.default_rng(29)
+    every = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(every.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    with np.errstate(invalid="ignore"):   # (the NaN patterns)
+        w = orc.widen(every)
+    fin = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(w), ~fin)
+    assert np.array_equal(w[fin], ref[fin]) and np.array_equal(np.signbit(w[fin]), np.signbit(ref[fin]))
+    # the fused loss from bf16 bit patterns equals the loss from the values they encode (torch, float64)
+    hb = rng.integers(0x3C00, 0x4000, (9, 8)).astype(np.uint16) ^ (rng.integers(0, 2, (9, 8)).astype(np.uint16) << 15)
+    wb = rng.integers(0x3A00, 0x3E00, (13, 8)).astype(np.uint16) ^ (rng.integers(0, 2, (13, 8)).astype(np.uint16) << 15)
+    t = rng.integers(0, 13, 9)
+    got = orc.flce_reference(hb, wb, t, row_block=4)
+    th = torch.from_numpy(hb.view(np.int16).copy()).view(torch.bfloat16).double().requires_grad_(True)
+    tw = torch.from_numpy(wb.view(np.int16).copy()).view(torch.bfloat16).double().requires_grad_(True)
+    loss = torch.nn.functional.cross_entropy(th @ tw.T, torch.tensor(t))
+    loss.backward()
+    assert abs(got["loss"] - loss.item()) <= 1e-12 * abs(loss.item())
+    assert _rel(got["grad_input"], th.grad.numpy()) < 1e-10
+    assert _rel(got["grad_W"], tw.grad.numpy()) < 1e-10
+    cb = rng.integers(0x3F00, 0x4100, (5, 11)).astype(np.uint16)
+    lab = rng.integers(0, 11, 5)
+    gce = orc.ce_reference(cb, lab)
+    tx = torch.from_numpy(cb.view(np.int16).copy()).view(torch.bfloat16).double()
+    assert abs(gce["ce_sum"] - torch.nn.functional.cross_entropy(tx, torch.tensor(lab), reduction="sum").item()) \
+        <= 1e-12 * abs(gce["ce_sum"])
+
+
 def pin_logit_avg_and_order(orc):
     # logit_avg: plain loops with exactly rounded sums; closed forms (W = 0 gives the bias, equal rows
     # give one matrix-vector product); the linearity identity mean_t z[t, n] = W[n] . mean_t hidden[t]
@@ -353,7 +401,7 @@ def pin_logit_avg_and_order(orc):
 
 PINS = [pin_loops_vs_vectorised, pin_finite_differences, pin_torch_fp64, pin_closed_forms,
         pin_invariants, pin_ce, pin_sampled_matches_full, pin_unreduced_and_upstream, pin_entropy,
-        pin_dlogits_matrix, pin_logit_avg_and_order]
+        pin_dlogits_matrix, pin_logit_avg_and_order, pin_widen_bf16_bits]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -384,6 +432,8 @@ MUTATIONS = {
     "vocabulary order ascending": ('np.argsort(-a, kind="stable")', 'np.argsort(a, kind="stable")'),
     "vocabulary ties in reverse index order": ('np.argsort(-a, kind="stable")',
                                                '(len(a) - 1 - np.argsort(-a[::-1], kind="stable"))'),
+    "bf16 bits widened with a 15-bit shift": ("(a.astype(np.uint32) << 16)", "(a.astype(np.uint32) << 15)"),
+    "bf16 bit patterns read as integers": ("    if a.dtype == np.uint16:\n", "    if False:\n"),
     "grad_input uses transposed product": ("grad_input[r0:r1] = d @ w", "grad_input[r0:r1] = (w.T @ d.T).T * 0 + d @ w[::-1]"),
 }
 
