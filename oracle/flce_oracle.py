@@ -60,11 +60,11 @@ __all__ = [
 
 
 def widen(x) -> np.ndarray:
-    """bf16 bit patterns (uint16) or any float array -> float64, exactly."""
+    """bf16 bit patterns (uint16) or any float array -> float64, exactly (a float64 array is used as is)."""
     a = np.asarray(x)
     if a.dtype == np.uint16:
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    return a.astype(np.float64)
+    return np.asarray(a, dtype=np.float64)
 
 
 def logits(hidden, W, bias=None) -> np.ndarray:
@@ -202,7 +202,9 @@ def flce_sampled(hidden, W, target, lse_all, rows, vocab_rows, bias=None, ignore
     * ``grad_input[rows]``: dlogits rows times W,
     * ``grad_W[vocab_rows]`` and ``grad_bias[vocab_rows]``: the dlogits columns of those vocabulary
       entries (over every token) times hidden.
-    All from the same definitions as ``flce_reference``.
+    All from the same definitions as ``flce_reference``.  The ``*_softmax`` entries are the same rows with
+    the onehot term of dlogits left out (only s [y_t valid] softmax(z_t) (1 + 2 z_loss LSE_t)), so that a
+    test can tell the softmax part of a gradient row from its target part.
     """
     h = widen(hidden)
     w = widen(W)
@@ -227,6 +229,7 @@ def flce_sampled(hidden, W, target, lse_all, rows, vocab_rows, bias=None, ignore
     if b is not None:
         z += b[None, :]
     d = np.exp(z - L[rows][:, None]) * (1.0 + 2.0 * z_loss * L[rows])[:, None]
+    gi_soft = (d * (s * valid[rows])[:, None]) @ w
     d[np.arange(len(rows)), y[rows]] -= 1.0
     d *= (s * valid[rows])[:, None]
     gi = d @ w
@@ -236,11 +239,14 @@ def flce_sampled(hidden, W, target, lse_all, rows, vocab_rows, bias=None, ignore
     if b is not None:
         zc += b[vr][None, :]
     dc = np.exp(zc - L[:, None]) * (1.0 + 2.0 * z_loss * L)[:, None]
+    dc_soft = dc * (s * valid)[:, None]
     dc -= ((y[:, None] == vr[None, :]) & valid[:, None]).astype(np.float64)
     dc *= (s * valid)[:, None]
     gw = dc.T @ h
     gb = dc.sum(axis=0) if b is not None else None
-    return dict(loss=loss, n_valid=n_valid, grad_input_rows=gi, grad_W_rows=gw, grad_bias_rows=gb)
+    return dict(loss=loss, n_valid=n_valid, grad_input_rows=gi, grad_W_rows=gw, grad_bias_rows=gb,
+                grad_input_rows_softmax=gi_soft, grad_W_rows_softmax=dc_soft.T @ h,
+                grad_bias_rows_softmax=dc_soft.sum(axis=0) if b is not None else None)
 
 
 def flce_reference_loops(hidden, W, target, bias=None, ignore_index: int = -100,

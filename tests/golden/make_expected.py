@@ -7,6 +7,14 @@ grad_input rows for sampled tokens, grad_W / grad_bias rows for sampled vocabula
 need the float64 LSE of every token, which this script computes), and for the standalone CE
 workload ce_sum, z_sum, n_valid and the dlogits of sampled rows.
 
+The samples: tokens 0, BT - 1, the first ignored token, random tokens, and 8 tokens among the last 512
+(the row blocks that the grad_input pass splits over the vocabulary when its last wave is partly
+filled); vocabulary entries 0, V - 1, the most frequent target, the first token's target, random
+entries, 16 entries that no token targets (their grad_W rows are the softmax part alone), and 8 entries
+among the last 512 (the rows the grad_W pass splits over the tokens).  Besides the full rows the file
+holds the oracle's softmax parts (the rows without the onehot term of dlogits), in float64, and each
+sampled entry's target count.
+
 Usage:  python tests/golden/make_expected.py [name ...]     (names: qwen3 gemma2 long ce)
 """
 from __future__ import annotations
@@ -25,6 +33,9 @@ from linear_cross_entropy_tma_gb300 import workloads as wl  # noqa: E402
 
 N_ROWS = 32
 N_VOCAB = 16
+N_UNTARGETED = 16
+N_TAIL = 8
+TAIL = 512
 
 
 def sample_rows(BT: int, target: np.ndarray, seed: int) -> np.ndarray:
@@ -33,6 +44,8 @@ def sample_rows(BT: int, target: np.ndarray, seed: int) -> np.ndarray:
     rows = {0, BT - 1, int(ign[0])} if ign.size else {0, BT - 1}
     while len(rows) < N_ROWS:
         rows.add(int(rng.integers(0, BT)))
+    tail = rng.choice(np.arange(max(0, BT - TAIL), BT), size=min(N_TAIL, BT), replace=False)
+    rows.update(int(r) for r in tail)
     return np.array(sorted(rows), dtype=np.int64)
 
 
@@ -43,6 +56,14 @@ def sample_vocab(V: int, target: np.ndarray, seed: int) -> np.ndarray:
     vs = {0, V - 1, int(counts.argmax()), int(t[0])}
     while len(vs) < N_VOCAB:
         vs.add(int(rng.integers(0, V)))
+    free = np.flatnonzero(counts == 0)
+    vs.update(int(v) for v in rng.choice(free, size=min(N_UNTARGETED, free.size), replace=False))
+    tail = np.arange(max(0, V - TAIL), V)
+    tail_free = tail[counts[tail] == 0]
+    tail_hit = tail[counts[tail] > 0]
+    # tail entries: untargeted ones and targeted ones
+    vs.update(int(v) for v in rng.choice(tail_free, size=min(N_TAIL // 2, tail_free.size), replace=False))
+    vs.update(int(v) for v in rng.choice(tail_hit, size=min(N_TAIL - N_TAIL // 2, tail_hit.size), replace=False))
     return np.array(sorted(vs), dtype=np.int64)
 
 
@@ -56,12 +77,16 @@ def make_fused(key: str) -> None:
     vocab = sample_vocab(w.V, d["target"], w.seed)
     smp = oracle.flce_sampled(d["hidden"], d["W"], d["target"], L, rows, vocab, bias=d["bias"],
                               reduction=w.reduction, z_loss=w.z_loss)
+    t = d["target"]
+    counts = np.bincount(t[(t >= 0) & (t < w.V)], minlength=w.V)
     out = dict(digest=np.array(dig), loss=np.float64(smp["loss"]), n_valid=np.int64(smp["n_valid"]),
-               rows=rows, vocab_rows=vocab, lse_rows=L[rows],
-               grad_input_rows=smp["grad_input_rows"].astype(np.float32),
-               grad_W_rows=smp["grad_W_rows"].astype(np.float32))
+               rows=rows, vocab_rows=vocab, lse_rows=L[rows], vocab_target_count=counts[vocab].astype(np.int64),
+               grad_input_rows=smp["grad_input_rows"], grad_W_rows=smp["grad_W_rows"],
+               grad_input_rows_softmax=smp["grad_input_rows_softmax"],
+               grad_W_rows_softmax=smp["grad_W_rows_softmax"])
     if smp["grad_bias_rows"] is not None:
         out["grad_bias_rows"] = smp["grad_bias_rows"]
+        out["grad_bias_rows_softmax"] = smp["grad_bias_rows_softmax"]
     np.savez_compressed(os.path.join(HERE, f"expected_{key}.npz"), **out)
     print(f"{key}: loss={smp['loss']:.12f} n_valid={smp['n_valid']} ({time.time() - t0:.1f} s)")
 

@@ -59,3 +59,28 @@ def bf16_to_numpy_f32(t) -> np.ndarray:
     import torch
     u = t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
     return (u.astype(np.uint32) << 16).view(np.float32)
+
+
+def check_full_size_rows(exp, gi_rows, gw_rows, gb_rows=None) -> None:
+    """Sampled rows of a full-size fused call against the stored oracle rows (tests/golden/expected_*.npz).
+
+    Every sampled row is checked on its own (the gradient bars against that row's own max |ref| and
+    norm), so that no row hides behind a larger one.  grad_W rows of vocabulary entries that no token
+    targets are the softmax part of the gradient alone, so those rows check the logits recompute, the
+    exponentials and the gradient GEMM of the grad_W pass without the onehot term around them; they are
+    also checked jointly.  grad_bias: the joint bars over all sampled entries and over the untargeted ones.
+    """
+    gi_rows = np.asarray(gi_rows, dtype=np.float64)
+    gw_rows = np.asarray(gw_rows, dtype=np.float64)
+    for i, r in enumerate(exp["rows"]):
+        assert_grad_close(gi_rows[i], exp["grad_input_rows"][i], f"grad_input row {int(r)}")
+    for i, n in enumerate(exp["vocab_rows"]):
+        assert_grad_close(gw_rows[i], exp["grad_W_rows"][i], f"grad_W row {int(n)}")
+    free = np.asarray(exp["vocab_target_count"]) == 0
+    assert free.sum() >= 8, "the sample needs untargeted vocabulary entries"
+    assert np.array_equal(exp["grad_W_rows"][free], exp["grad_W_rows_softmax"][free])
+    assert_grad_close(gw_rows[free], exp["grad_W_rows_softmax"][free], "grad_W rows of untargeted entries")
+    if gb_rows is not None:
+        gb_rows = np.asarray(gb_rows, dtype=np.float64)
+        assert_grad_close(gb_rows, exp["grad_bias_rows"], "grad_bias rows")
+        assert_grad_close(gb_rows[free], exp["grad_bias_rows_softmax"][free], "grad_bias rows of untargeted entries")

@@ -3,7 +3,8 @@
 Element-by-element parity at sizes the oracle finishes in seconds (several tiles, ragged tails in
 BT, V and H, bias, z-loss, both reductions, degenerate cases), and at the full benchmark sizes on
 sampled outputs: the loss and n_valid, grad_input rows of sampled tokens and grad_W / grad_bias rows
-of sampled vocabulary entries (stored by tests/golden/make_expected.py, which calls only the oracle).
+of sampled vocabulary entries (stored by tests/golden/make_expected.py, which calls only the oracle),
+each row checked on its own, the rows of untargeted vocabulary entries against the softmax part alone.
 """
 import functools
 import os
@@ -13,7 +14,7 @@ import pytest
 
 import oracle
 from linear_cross_entropy_tma_gb300 import workloads as wl
-from parity import assert_grad_close, assert_scalar_close, bf16_tensor, bf16_to_numpy_f32
+from parity import assert_grad_close, assert_scalar_close, bf16_tensor, bf16_to_numpy_f32, check_full_size_rows
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -465,12 +466,15 @@ def test_flce_full_size_sampled(flce, key):
     assert out["status"] == 0
     assert int(out["n_valid"].item()) == int(exp["n_valid"]) == w.n_valid
     assert_scalar_close(out["loss"].item(), float(exp["loss"]), "loss")
+    # the automatic split tails ran (their row blocks are the last ones; the sample holds tokens and
+    # vocabulary entries among the last 512)
+    assert flce.read_vocab_split_units(out["workspace"]) > 0
+    if key == "long":
+        assert flce.read_token_split_units(out["workspace"]) > 0
     rows = torch.from_numpy(exp["rows"]).cuda()
-    assert_grad_close(bf16_to_numpy_f32(out["grad_input"][rows]), exp["grad_input_rows"], "grad_input rows")
     vr = torch.from_numpy(exp["vocab_rows"]).cuda()
-    assert_grad_close(out["grad_W"][vr].cpu().numpy(), exp["grad_W_rows"], "grad_W rows")
-    if "grad_bias_rows" in exp.files:
-        assert_grad_close(out["grad_bias"][vr].cpu().numpy(), exp["grad_bias_rows"], "grad_bias rows")
+    check_full_size_rows(exp, bf16_to_numpy_f32(out["grad_input"][rows]), out["grad_W"][vr].cpu().numpy(),
+                         out["grad_bias"][vr].cpu().numpy() if "grad_bias_rows" in exp.files else None)
     # no (BT, V) buffer: the workspace is O(BT)
     assert out["workspace"].numel() < 64 * 2**20
     first = out["loss"].item()

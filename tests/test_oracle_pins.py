@@ -235,6 +235,23 @@ def pin_sampled_matches_full(orc):
     assert _rel(smp["grad_input_rows"], full["grad_input"][rows]) < 1e-12
     assert _rel(smp["grad_W_rows"], full["grad_W"][vrows]) < 1e-12
     assert _rel(smp["grad_bias_rows"], full["grad_bias"][vrows]) < 1e-12
+    # the softmax parts: the full rows minus the onehot term, written out with loops from the targets
+    # (grad_input: -s W[y_t] on valid rows; grad_W[n]: -s sum of hidden[t] over valid t with y_t = n;
+    # grad_bias[n]: -s times that count)
+    s = 1.0 / full["n_valid"]
+    for i, r in enumerate(rows):
+        one = -s * W[t[r]] if t[r] != -100 else np.zeros(W.shape[1])
+        assert np.allclose(smp["grad_input_rows"][i] - smp["grad_input_rows_softmax"][i], one, rtol=0, atol=1e-13)
+    for i, n in enumerate(vrows):
+        one = np.zeros(hidden.shape[1])
+        cnt = 0
+        for tt in range(len(t)):
+            if t[tt] == n:
+                one -= s * hidden[tt]
+                cnt += 1
+        assert np.allclose(smp["grad_W_rows"][i] - smp["grad_W_rows_softmax"][i], one, rtol=0, atol=1e-13)
+        assert abs(smp["grad_bias_rows"][i] - smp["grad_bias_rows_softmax"][i] + s * cnt) < 1e-13
+    assert (t[:, None] == np.array(vrows)[None, :]).any(axis=0).any(), "the sample must hold a targeted entry"
 
 
 def pin_unreduced_and_upstream(orc):
@@ -434,6 +451,9 @@ MUTATIONS = {
                                                '(len(a) - 1 - np.argsort(-a[::-1], kind="stable"))'),
     "bf16 bits widened with a 15-bit shift": ("(a.astype(np.uint32) << 16)", "(a.astype(np.uint32) << 15)"),
     "bf16 bit patterns read as integers": ("    if a.dtype == np.uint16:\n", "    if False:\n"),
+    "sampled softmax part keeps the target column": (
+        "    dc_soft = dc * (s * valid)[:, None]\n",
+        "    dc_soft = (dc - (y[:, None] == vr[None, :])) * (s * valid)[:, None]\n"),
     "grad_input uses transposed product": ("grad_input[r0:r1] = d @ w", "grad_input[r0:r1] = (w.T @ d.T).T * 0 + d @ w[::-1]"),
 }
 
