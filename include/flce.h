@@ -75,7 +75,7 @@ typedef enum flce_status {
 /*
  * Bytes of workspace flce_fwd_bwd needs for these sizes (O(BT + V) floats: per-row LSE statistics,
  * per-row loss terms, the per-column bias in log2 units, the status word and the valid count; plus a
- * fixed 16 MiB of per-SM staging blocks through which the gradient passes hand dS tiles between SMs).
+ * fixed 16 MiB for the accumulators of the grad_input pass's vocabulary-split clusters).
  * Returns 0 for negative sizes.
  */
 size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V);
@@ -204,6 +204,16 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        scratch: fewer at small BT).  The classic flow's single launch of both passes
  *                        (separate_lse_pass with grad_input and grad_W) does not split.  The number of
  *                        token-split clusters is the word at byte 32 of the workspace.
+ *   debug_stall_us       test-only; 0 in normal use.  When > 0 (at most 1000000, else
+ *                        FLCE_ERR_INVALID_ARG), the TMA producer of every CTA of the gradient passes first
+ *                        waits this many microseconds for an mbarrier phase that nothing completes, before
+ *                        it issues any copy.  That wait gives up as any bounded wait in the kernels does:
+ *                        it raises the CTA's abort flag, every role of the cluster winds down (nothing is
+ *                        in flight), TMEM is freed, the kernel sets FLCE_STATUS_TIMEOUT in the status word
+ *                        and returns.  The rest of the call still runs; its results are invalid.  This is
+ *                        how the timeout path (the bounded replacement of the spin lock in "Cut Cross
+ *                        Entropy visualized", "Forward kernel") is exercised without faulting or hanging
+ *                        a GPU; the next call on the same stream and workspace is unaffected.
  */
 typedef struct flce_fwd_bwd_options {
   float grad_scale;
@@ -218,6 +228,7 @@ typedef struct flce_fwd_bwd_options {
   int separate_lse_pass;
   int vocab_splits;
   int token_splits;
+  uint32_t debug_stall_us;
 } flce_fwd_bwd_options;
 
 /* Bytes of workspace flce_fwd_bwd_ex needs with these options (NULL: flce_workspace_size). */
@@ -296,7 +307,10 @@ flce_status ce_with_grad_ex(const void* logits, void* dlogits, int dtype, const 
  *   Memory: every GPU that loads the library holds the array (256 + 16 * FLCE_CE_NOALLOC_MAX_ROWS
  *   bytes, 4 MiB) until the process exits.
  *   The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
- *   that device current) and remembers it; make that first call before any stream capture.
+ *   that device current) and remembers it; make that first call before any stream capture.  The remembered address belongs
+ *   to the device's context of that moment: a caller that resets the device (cudaDeviceReset) or
+ *   otherwise recreates its primary context must not call this entry point on that device again in
+ *   the same process.
  *   All calls share the one array, which keeps the previous call's contents; each call clears what
  *   must start at zero.  Calls whose kernels can overlap on the GPU (e.g. on two streams without
  *   ordering between them, or from two host threads) race on the array: serialise them.
@@ -307,6 +321,34 @@ flce_status ce_with_grad_ex(const void* logits, void* dlogits, int dtype, const 
 flce_status ce_with_grad_noalloc(uint16_t* logits, const int64_t* labels, int64_t B, int64_t V,
                                  int64_t ignore_index, float z_loss, float* ce_sum, float* z_sum,
                                  int64_t* n_valid, void* stream);
+
+/*
+ * The reduced loss of the standalone CE from the device sums of ce_with_grad / ce_with_grad_ex, without
+ * a host round trip (the loss a framework's autograd function returns):
+ *   *loss = (*ce_sum + z_loss * *z_sum) / max(*n_valid, 1)   for FLCE_REDUCTION_MEAN ("Greyhound --
+ *           Cross-Entropy", "Usage": ce_sum over the clamped valid count), or
+ *   *loss = *ce_sum + z_loss * *z_sum                         for FLCE_REDUCTION_SUM.
+ * With this z_loss the loss is the one whose gradient ce_with_grad writes (scaled by 1 / max(n_valid, 1)
+ * for the mean).  All pointers are device pointers (n_valid 8-byte aligned, the others 4); one thread
+ * of one kernel on `stream`.  FLCE_ERR_INVALID_ARG for a NULL pointer or another reduction.
+ */
+flce_status ce_reduce_loss(const float* ce_sum, const float* z_sum, const int64_t* n_valid, float z_loss,
+                           int reduction, float* loss, void* stream);
+
+/*
+ * Multiplies a contiguous gradient buffer in place by an upstream gradient that lives on the device:
+ *   grad[i] *= *upstream / (divisor != NULL ? max(*divisor, 1) : 1),   i in [0, n)
+ * rounding to nearest-even in the buffer's type (dtype: FLCE_DTYPE_BF16, _F16 or _F32).  This is the
+ * d_out factor of "Cut Cross Entropy visualized", "Breakdown: Backward Pass", step 4, applied after the
+ * fact to gradients computed with an upstream gradient of 1 (flce_fwd_bwd, ce_with_grad): the backward
+ * pass of an autograd function calls it with the incoming gradient, and for the standalone CE's mean
+ * reduction with divisor = n_valid.  When the factor is exactly 1 the buffer is not touched.
+ *   grad      device, 16-byte aligned (may be NULL when n == 0).
+ *   upstream  [1] fp32, device.   divisor  [1] int64, device, or NULL.
+ * FLCE_ERR_INVALID_ARG for a bad dtype, n < 0 or a NULL pointer; FLCE_ERR_MISALIGNED.
+ */
+flce_status flce_scale_gradient(void* grad, int dtype, int64_t n, const float* upstream, const int64_t* divisor,
+                                void* stream);
 
 /*
  * Copy the device status word of a workspace used by a previous call to *host_status, after

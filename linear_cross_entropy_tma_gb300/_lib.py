@@ -19,7 +19,7 @@ STATUS_TIMEOUT = 0x2
 STATUS_INTERNAL = 0x4
 EXPORTED = ("flce_workspace_size", "flce_workspace_size_ex", "flce_fwd_bwd", "flce_fwd_bwd_timed", "flce_fwd_bwd_ex", "ce_workspace_size",
             "ce_with_grad", "ce_with_grad_ex", "flce_read_device_status", "flce_status_string", "flce_last_error",
-            "ce_with_grad_noalloc")
+            "ce_with_grad_noalloc", "ce_reduce_loss", "flce_scale_gradient")
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 _lib = None
@@ -35,7 +35,7 @@ class FwdBwdOptions(ctypes.Structure):
                 ("accumulate", ctypes.c_int), ("entropy", c_p), ("filter_eps", ctypes.c_float),
                 ("sort_vocab", ctypes.c_int), ("logit_avg", c_p), ("vocab_order", c_p),
                 ("separate_lse_pass", ctypes.c_int), ("vocab_splits", ctypes.c_int),
-                ("token_splits", ctypes.c_int)]
+                ("token_splits", ctypes.c_int), ("debug_stall_us", ctypes.c_uint32)]
 
 
 def load() -> ctypes.CDLL:
@@ -67,6 +67,10 @@ def load() -> ctypes.CDLL:
                                     c_p, c_sz, c_p]
     lib.ce_with_grad_noalloc.restype = ctypes.c_int
     lib.ce_with_grad_noalloc.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, ctypes.c_float, c_p, c_p, c_p, c_p]
+    lib.ce_reduce_loss.restype = ctypes.c_int
+    lib.ce_reduce_loss.argtypes = [c_p, c_p, c_p, ctypes.c_float, ctypes.c_int, c_p, c_p]
+    lib.flce_scale_gradient.restype = ctypes.c_int
+    lib.flce_scale_gradient.argtypes = [c_p, ctypes.c_int, c_i64, c_p, c_p, c_p]
     lib.flce_read_device_status.restype = ctypes.c_int
     lib.flce_read_device_status.argtypes = [c_p, ctypes.POINTER(ctypes.c_uint32), c_p]
     lib.flce_status_string.restype = ctypes.c_char_p
@@ -116,7 +120,7 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
                  out=None, stream=None, pass_events=None, grad_scale: float = 1.0, grad_loss_per_token=None,
                  accumulate: bool = False, want_loss_per_token: bool = False, want_entropy: bool = False,
                  filter_eps: float = 0.0, sort_vocab: bool = False, separate_lse_pass: bool = False,
-                 vocab_splits: int = 0, token_splits: int = 0) -> dict:
+                 vocab_splits: int = 0, token_splits: int = 0, debug_stall_us: int = 0) -> dict:
     """Fused linear cross-entropy forward + backward on the current CUDA device.
 
     hidden [BT, H] bf16, W [V, H] bf16, target [BT] int64, bias [V] fp32 or None.  Returns a dict with
@@ -135,7 +139,8 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     fp32 [V], and ``vocab_order``, int32 [V], to the result); ``separate_lse_pass`` computes the LSE in a
     pass of its own first instead of inside the grad_input pass; ``vocab_splits`` sets how that pass splits
     the vocabulary of its row blocks (0 automatic, 1 never, k >= 2 up to k parts each), ``token_splits`` the
-    same for the grad_W pass over token ranges (flce_fwd_bwd_ex).
+    same for the grad_W pass over token ranges (flce_fwd_bwd_ex).  ``debug_stall_us`` (test-only) makes the
+    gradient passes' bounded waits give up on purpose (FLCE_STATUS_TIMEOUT; results invalid).
     ``pass_events``: five
     recorded ``torch.cuda.Event(enable_timing=True)`` objects; the library re-records them at the pass
     boundaries (flce_fwd_bwd_timed) for per-kernel timing; only with the default options.
@@ -192,7 +197,7 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
             _ptr(o["loss"]), _ptr(gi), _ptr(gw), _ptr(gb), _ptr(o["n_valid"]), _ptr(workspace), workspace.numel())
     plain = (red != 2 and grad_scale == 1.0 and grad_loss_per_token is None and not accumulate and lt is None
              and ent is None and filter_eps == 0.0 and not sort_vocab and not separate_lse_pass
-             and vocab_splits == 0 and token_splits == 0)
+             and vocab_splits == 0 and token_splits == 0 and debug_stall_us == 0)
     if pass_events is not None:
         if not plain:
             raise ValueError("pass_events only with the default options")
@@ -205,7 +210,8 @@ def flce_fwd_bwd(hidden, W, target, bias=None, ignore_index: int = -100, reducti
     else:
         opts = FwdBwdOptions(float(grad_scale), _ptr(grad_loss_per_token), _ptr(lt), 1 if accumulate else 0, _ptr(ent),
                              float(filter_eps), 1 if sort_vocab else 0, _ptr(la), _ptr(vo),
-                             1 if separate_lse_pass else 0, int(vocab_splits), int(token_splits))
+                             1 if separate_lse_pass else 0, int(vocab_splits), int(token_splits),
+                             int(debug_stall_us))
         check(load().flce_fwd_bwd_ex(*args, ctypes.byref(opts), _stream_ptr(stream)))
     res = dict(loss=o["loss"], n_valid=o["n_valid"], grad_input=gi, grad_W=gw, grad_bias=gb, loss_per_token=lt,
                entropy=ent, workspace=workspace)
@@ -273,6 +279,39 @@ def cross_entropy(logits, labels, ignore_index: int = -100, z_loss: float = 0.0,
     r = _ce_call(logits, dl, labels, ignore_index, z_loss, workspace, o, stream)
     r["dlogits"] = dl
     return r
+
+
+def ce_reduce_loss(ce_sum, z_sum, n_valid, z_loss: float = 0.0, reduction: str = "mean", loss=None,
+                   stream=None):
+    """The reduced loss of the standalone CE from its device sums (ce_reduce_loss of include/flce.h):
+    (ce_sum + z_loss z_sum) / max(n_valid, 1) for "mean", ce_sum + z_loss z_sum for "sum".  Returns a
+    fp32 [1] CUDA tensor (``loss`` if given)."""
+    import torch
+    if reduction not in ("mean", "sum"):
+        raise ValueError("reduction must be 'mean' or 'sum'")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=ce_sum.device)
+    check(load().ce_reduce_loss(_ptr(ce_sum), _ptr(z_sum), _ptr(n_valid), float(z_loss), REDUCTIONS[reduction],
+                                _ptr(loss), _stream_ptr(stream)))
+    return loss
+
+
+def scale_gradient_(grad, upstream, divisor=None, stream=None):
+    """grad *= upstream / max(divisor, 1) in place, with ``upstream`` a fp32 CUDA scalar tensor and
+    ``divisor`` an int64 CUDA scalar tensor or None (flce_scale_gradient of include/flce.h).  ``grad``:
+    a contiguous CUDA bf16, fp16 or fp32 tensor.  Returns ``grad``."""
+    import torch
+    codes = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
+    if grad.dtype not in codes or not grad.is_cuda or not grad.is_contiguous():
+        raise ValueError("grad must be a contiguous CUDA bfloat16, float16 or float32 tensor")
+    if upstream.dtype != torch.float32 or upstream.numel() != 1 or not upstream.is_cuda:
+        raise ValueError("upstream must be a CUDA float32 scalar tensor")
+    if divisor is not None and (divisor.dtype != torch.int64 or divisor.numel() != 1 or not divisor.is_cuda):
+        raise ValueError("divisor must be a CUDA int64 scalar tensor")
+    up = upstream.contiguous()
+    check(load().flce_scale_gradient(_ptr(grad), codes[grad.dtype], grad.numel(), _ptr(up), _ptr(divisor),
+                                     _stream_ptr(stream)))
+    return grad
 
 
 def read_filter_skips(workspace) -> int:

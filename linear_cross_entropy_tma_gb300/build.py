@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libflce.so")
-SOURCES = ["api.cu", "ce_kernel.cu", "flce_fwd.cu", "flce_bwd.cu", "flce_launch.cu", "ce_noalloc.cu", "vocab_sort.cu"]
+SOURCES = ["api.cu", "ce_kernel.cu", "flce_fwd.cu", "flce_bwd.cu", "flce_launch.cu", "ce_noalloc.cu", "vocab_sort.cu", "grad_ops.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=default",
            "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

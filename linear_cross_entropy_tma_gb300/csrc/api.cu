@@ -8,6 +8,7 @@
 #include "../../include/flce.h"
 #include "ce_kernel.cuh"
 #include "flce_kernels.cuh"
+#include "grad_ops.cuh"
 
 namespace {
 
@@ -113,7 +114,7 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
                                 void* stream, void* const* events, int n_events) {
   g_last_error[0] = '\0';
   const flce_fwd_bwd_options opt =
-      options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0, nullptr, 0.0f, 0, nullptr, nullptr, 0, 0, 0};
+      options != nullptr ? *options : flce_fwd_bwd_options{1.0f, nullptr, nullptr, 0, nullptr, 0.0f, 0, nullptr, nullptr, 0, 0, 0, 0u};
   if (n_events != 0 && (n_events != 5 || events == nullptr)) {
     set_error("n_events must be 0 or 5 (with a non-NULL event array)");
     return FLCE_ERR_INVALID_ARG;
@@ -142,6 +143,10 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   }
   if (!(opt.filter_eps >= 0.0f) || !std::isfinite(opt.filter_eps)) {
     set_error("filter_eps must be finite and >= 0");
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (opt.debug_stall_us > 1000000u) {
+    set_error("debug_stall_us must be at most 1000000 (1 s), got %u", opt.debug_stall_us);
     return FLCE_ERR_INVALID_ARG;
   }
   if (opt.vocab_splits < 0 || opt.token_splits < 0) {
@@ -211,6 +216,7 @@ static flce_status fwd_bwd_impl(const uint16_t* hidden, const uint16_t* W, const
   a.separate_lse = opt.separate_lse_pass != 0;
   a.vocab_splits = opt.vocab_splits;
   a.token_splits = opt.token_splits;
+  a.debug_stall_us = opt.debug_stall_us;
   char err[256] = "";
   const cudaError_t e = flce::launch_fused(a, workspace, num_sms, static_cast<cudaStream_t>(stream), err, sizeof(err),
                                            n_events ? reinterpret_cast<cudaEvent_t const*>(events) : nullptr);
@@ -311,6 +317,51 @@ flce_status ce_with_grad_ex(const void* logits, void* dlogits, int dtype, const 
                             void* workspace, size_t workspace_bytes, void* stream) {
   return ce_impl(logits, dlogits, dtype, labels, B, V, ignore_index, z_loss, ce_sum, z_sum, n_valid, workspace,
                  workspace_bytes, stream, "ce_with_grad_ex launch");
+}
+
+flce_status flce_scale_gradient(void* grad, int dtype, int64_t n, const float* upstream, const int64_t* divisor,
+                                void* stream) {
+  g_last_error[0] = '\0';
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_F16 && dtype != FLCE_DTYPE_F32) {
+    set_error("dtype must be FLCE_DTYPE_BF16, FLCE_DTYPE_F16 or FLCE_DTYPE_F32, got %d", dtype);
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (n < 0 || upstream == nullptr || (n > 0 && grad == nullptr)) {
+    set_error("need n >= 0 and non-NULL grad and upstream (got n = %lld)", (long long)n);
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (!aligned(grad, 16) || !aligned(upstream, 4) || !aligned(divisor, 8)) {
+    set_error("misaligned pointer (grad needs 16 bytes, upstream 4, divisor 8)");
+    return FLCE_ERR_MISALIGNED;
+  }
+  int num_sms = 0;
+  const flce_status ds = check_device(&num_sms);
+  if (ds != FLCE_OK) return ds;
+  return from_cuda(flce::launch_scale(grad, n, dtype, upstream, divisor, num_sms, static_cast<cudaStream_t>(stream)),
+                   "flce_scale_gradient launch");
+}
+
+flce_status ce_reduce_loss(const float* ce_sum, const float* z_sum, const int64_t* n_valid, float z_loss,
+                           int reduction, float* loss, void* stream) {
+  g_last_error[0] = '\0';
+  if (reduction != FLCE_REDUCTION_MEAN && reduction != FLCE_REDUCTION_SUM) {
+    set_error("reduction must be 0 (mean) or 1 (sum), got %d", reduction);
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (ce_sum == nullptr || z_sum == nullptr || n_valid == nullptr || loss == nullptr) {
+    set_error("ce_sum, z_sum, n_valid and loss must not be NULL");
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (!aligned(ce_sum, 4) || !aligned(z_sum, 4) || !aligned(n_valid, 8) || !aligned(loss, 4)) {
+    set_error("misaligned pointer (n_valid needs 8 bytes, the others 4)");
+    return FLCE_ERR_MISALIGNED;
+  }
+  int num_sms = 0;
+  const flce_status ds = check_device(&num_sms);
+  if (ds != FLCE_OK) return ds;
+  return from_cuda(flce::launch_ce_reduce_loss(ce_sum, z_sum, n_valid, z_loss, reduction == FLCE_REDUCTION_MEAN, loss,
+                                               static_cast<cudaStream_t>(stream)),
+                   "ce_reduce_loss launch");
 }
 
 flce_status flce_read_device_status(const void* workspace, uint32_t* host_status, void* stream) {

@@ -61,9 +61,17 @@ flce_status ce_with_grad_noalloc(uint16_t* logits, const int64_t* labels, int64_
   flce::set_last_error_message("");
   if (B < 0 || V <= 0 || ce_sum == nullptr || z_sum == nullptr || n_valid == nullptr ||
       (B > 0 && (logits == nullptr || labels == nullptr))) {
+    snprintf(msg, sizeof(msg), "ce_with_grad_noalloc: need B >= 0 and V > 0 (got %lld, %lld) and non-NULL logits, "
+             "labels, ce_sum, z_sum and n_valid", static_cast<long long>(B), static_cast<long long>(V));
+    flce::set_last_error_message(msg);
     return FLCE_ERR_INVALID_ARG;
   }
-  if (B > kNoAllocMaxRows || V > (int64_t(1) << 31) - 1) {
+  if (V > (int64_t(1) << 31) - 1) {
+    snprintf(msg, sizeof(msg), "ce_with_grad_noalloc: V must be below 2^31 (got %lld)", static_cast<long long>(V));
+    flce::set_last_error_message(msg);
+    return FLCE_ERR_UNSUPPORTED;
+  }
+  if (B > kNoAllocMaxRows) {
     snprintf(msg, sizeof(msg),
              "ce_with_grad_noalloc handles at most %lld rows (got %lld); use ce_with_grad with a workspace",
              static_cast<long long>(kNoAllocMaxRows), static_cast<long long>(B));
@@ -73,6 +81,8 @@ flce_status ce_with_grad_noalloc(uint16_t* logits, const int64_t* labels, int64_
   if ((reinterpret_cast<uintptr_t>(logits) & 15u) != 0 || (reinterpret_cast<uintptr_t>(labels) & 7u) != 0 ||
       (reinterpret_cast<uintptr_t>(ce_sum) & 3u) != 0 || (reinterpret_cast<uintptr_t>(z_sum) & 3u) != 0 ||
       (reinterpret_cast<uintptr_t>(n_valid) & 7u) != 0) {
+    flce::set_last_error_message("ce_with_grad_noalloc: misaligned pointer (logits need 16 bytes, labels and n_valid "
+                                 "8, ce_sum and z_sum 4)");
     return FLCE_ERR_MISALIGNED;
   }
   int dev = 0, major = 0, minor = 0, num_sms = 0;
@@ -81,6 +91,10 @@ flce_status ce_with_grad_noalloc(uint16_t* logits, const int64_t* labels, int64_
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || major != 10 ||
       minor != 3) {
+    (void)cudaGetLastError();
+    snprintf(msg, sizeof(msg), "ce_with_grad_noalloc: the current device (%d) is not a compute capability 10.3 GPU "
+             "(or the query failed)", dev);
+    flce::set_last_error_message(msg);
     return FLCE_ERR_NO_DEVICE;
   }
   void* scratch = nullptr;

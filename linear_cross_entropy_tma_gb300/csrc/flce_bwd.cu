@@ -49,6 +49,7 @@
 //     combined by online_vmerge_kernel / dw_vmerge_kernel.
 // All waits are bounded; a wait that gives up flags the status word and the kernel winds down.
 #include <algorithm>
+#include <type_traits>
 
 #include "flce_kernels.cuh"
 #include "sm100.cuh"
@@ -69,6 +70,9 @@ static_assert(kFlagRing >= kMaxPairs + 2, "the skip-verdict ring must outlast P 
 // Order of a step's tensor work: 0 = GEMM2 half 0, half 1, then the GEMM1 share; 1 = the GEMM1 share
 // first; 2 = GEMM2 half 0, half of the share, GEMM2 half 1, the rest of the share.
 constexpr int kStepOrder = 0;
+// dS hand-over to the other pairs: 0 = one lane per warp issues cp.async.bulk copies shared -> peer shared
+// (TMA unit), 1 = every lane stores 16-byte pieces with st.async (load/store path), coalesced.
+constexpr int kDsHandOver = 1;
 constexpr uint32_t kBox = kTileM * kBK * 2;   // 16 KiB: a 128-row x 64-column bf16 box
 constexpr uint32_t kStage = 2 * kBox;
 constexpr uint32_t kHalfBytes = 2 * kBox;     // one 128-column half of a dS block (per CTA)
@@ -82,27 +86,30 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
 
-// Shared memory per CTA: an operand ring (5 stages of 32 KiB for the grad_input pass, 4 for the grad_W
-// pass, which also stages each owned block's 256 per-token statistics in a two-slot ring) and the dS
-// block (two 32 KiB half slots).
-template <bool kVocabRows>
+// Shared memory per CTA: an operand ring of 32 KiB stages, the dS block (two 32 KiB half slots) and, in the
+// grad_W pass, one slot with the per-token statistics of the owned block whose dS the epilogue computes
+// next (loaded by the producer with that block's last GEMM1 share): the (exponent constant, target) pairs,
+// 2 KiB, in the exact pass; the four-word statistics, 4 KiB, in the filtering pass, which also keeps a
+// ring of skip verdicts and has one stage fewer (4).  The other passes have 5 stages.  After the main
+// loop the dS block gathers the grad_bias partials.
+template <bool kVocabRows, bool kFilter>
 struct PairCfg {
-  static constexpr int kStages = kVocabRows ? 4 : 5;
-  static constexpr int kStatSlots = kVocabRows ? 2 : 1;
-  static constexpr int kStatCols = kVocabRows ? kPN : 4;
-  static constexpr int kGather = kVocabRows ? kMaxPairs : 1;
+  static constexpr int kStages = (kVocabRows && kFilter) ? 4 : 5;
+  static constexpr int kStatCols = kVocabRows ? kPN : 1;
+  static constexpr int kRing = kFilter ? kFlagRing : 1;
+  using Stat = typename std::conditional<kFilter, float4, float2>::type;
 };
 
-template <bool kVocabRows>
+template <bool kVocabRows, bool kFilter>
 struct PairSmem {
-  uint8_t stage[PairCfg<kVocabRows>::kStages][kStage];
+  using Cfg = PairCfg<kVocabRows, kFilter>;
+  uint8_t stage[Cfg::kStages][kStage];
   uint8_t ds[kDsBytes];
-  float4 colstats[PairCfg<kVocabRows>::kStatSlots][PairCfg<kVocabRows>::kStatCols];
-  float gb_gather[PairCfg<kVocabRows>::kGather][kTileM];
-  uint64_t full[PairCfg<kVocabRows>::kStages];
-  uint64_t empty[PairCfg<kVocabRows>::kStages];
-  uint64_t st_full[2];
-  uint64_t st_empty[2];
+  typename Cfg::Stat colstats[Cfg::kStatCols];
+  uint64_t full[Cfg::kStages];
+  uint64_t empty[Cfg::kStages];
+  uint64_t st_full;
+  uint64_t st_empty;
   uint64_t s_full;
   uint64_t s_empty;
   uint64_t ds_full[2];
@@ -111,24 +118,36 @@ struct PairSmem {
   uint64_t o_full;
   uint64_t o_zero;
   uint64_t drain;
+  uint64_t never;             // test-only stall (debug_stall_us): a phase nothing completes
   uint64_t mref_ready;        // online grad_input pass: the per-row reference is in
   uint64_t part_ready;        // online grad_input pass: every pair's per-row partial sums are in
-  uint64_t flag_full[kFlagRing][2];   // filter: the 8 owner warps' verdicts of [block mod ring][half] are in
-  uint32_t skipf[kFlagRing][2][8];    // filter: [block mod ring][half][4 x owner CTA + warp] 1 = all small
+  uint64_t flag_full[Cfg::kRing][2];  // filter: the 8 owner warps' verdicts of [block mod ring][half] are in
+  uint32_t skipf[Cfg::kRing][2][8];   // filter: [block mod ring][half][4 x owner CTA + warp] 1 = all small
   uint32_t tmem_base;
   int abort;
-  float half_bias[kTileM];
 };
-template <bool kVocabRows>
-constexpr size_t pair_smem_bytes() { return sizeof(PairSmem<kVocabRows>) + 1024; }
-static_assert(pair_smem_bytes<false>() <= 232448, "shared memory budget of one CTA exceeded");
-static_assert(pair_smem_bytes<true>() <= 232448, "shared memory budget of one CTA exceeded");
+constexpr size_t kSmemBudget = 232448;
+// The stage ring and the dS block need 1024-byte alignment (128-byte swizzle atoms).  A layout that fits
+// with 1023 bytes of slack is placed at the next 1024-byte boundary; the exact grad_W pass's layout does
+// not fit with the slack, so it is placed at the start of the dynamic shared memory, which the kernel
+// checks is on a 1024-byte boundary (FLCE_STATUS_INTERNAL and an early return otherwise).
+template <bool kVocabRows, bool kFilter>
+constexpr size_t pair_smem_slack() {
+  return sizeof(PairSmem<kVocabRows, kFilter>) + 1024 <= kSmemBudget ? 1024 : 0;
+}
+template <bool kVocabRows, bool kFilter>
+constexpr size_t pair_smem_bytes() { return sizeof(PairSmem<kVocabRows, kFilter>) + pair_smem_slack<kVocabRows, kFilter>(); }
+static_assert(pair_smem_bytes<false, false>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
+static_assert(pair_smem_bytes<true, false>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
+static_assert(pair_smem_bytes<false, true>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
+static_assert(pair_smem_bytes<true, true>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
+static_assert(sizeof(float) * kMaxPairs * 2 * kTileM <= kDsBytes, "the dS block gathers the grad_bias partials");
 
 // Gradient filter: the verdict on half `half` of block j, once the 8 epilogue warps of its owner pair that
 // hold the half (4 per CTA) have published theirs: 1 = every pair skips it (no operand stage, no MMA, no
 // dS hand-over), 0 = keep, -1 = the bounded wait gave up.
-template <bool kVocabRows>
-__device__ __forceinline__ int filter_verdict(PairSmem<kVocabRows>& sm, int j, int half, volatile int* abort) {
+template <class Smem>
+__device__ __forceinline__ int filter_verdict(Smem& sm, int j, int half, volatile int* abort) {
   const int r = j % kFlagRing;
   if (!mbar_wait_cluster(&sm.flag_full[r][half], static_cast<uint32_t>(j / kFlagRing) & 1u, abort)) return -1;
   const volatile uint32_t* f = sm.skipf[r][half];
@@ -141,6 +160,7 @@ __device__ __forceinline__ int filter_verdict(PairSmem<kVocabRows>& sm, int j, i
 struct PairParams {
   const float* bias;
   const float4* stats;
+  const float2* stats_ct;   // (x, y) of stats: what the exact grad_W pass stages per block
   const float* colb2;
   const float* scale;
   const uint32_t* zf_neg;
@@ -168,6 +188,7 @@ struct PairParams {
   uint32_t* row_redo;       // online pass: per row, 1 when its sum left the safe range (row not written);
                             // classic grad_input pass behind it: write only those rows
   float4* stats_out;        // per-token statistics for the grad_W pass
+  float2* stats_ct_out;     // their compact (x, y) copy
   float* row_loss;
   float* loss_tok;
   uint32_t* zf_neg_out;
@@ -181,6 +202,7 @@ struct PairParams {
                             // grad_W rows, the units then covering token ranges)
   float* vs_gb;             // grad_W pass: [su][256] partial grad_bias
   uint32_t* vs_count;       // receives the number of split units (workspace header)
+  uint32_t debug_stall_us;  // test-only: the producer first waits this long on `never`, then gives up
 };
 
 // The block whose GEMM1 pair `pr` works on in step s (the one it owns in [s+P+1, s+2P]) and which
@@ -213,16 +235,28 @@ struct DsRow {
   int y;        // grad_input pass: target column (-1 if none); grad_W pass: this row's vocabulary index
 };
 
+// Per-token statistics of the grad_W pass's columns: the staged (x, y) pairs of the exact pass (the other
+// two words from global memory, where needed: the rare target column and the general form), or the staged
+// four words of the filtering pass.
+__device__ __forceinline__ float2 stat_xy(const float2& s) { return s; }
+__device__ __forceinline__ float2 stat_xy(const float4& s) { return make_float2(s.x, s.y); }
+__device__ __forceinline__ float4 stat_full(const float2* /*staged*/, const float4* __restrict__ g, int i) {
+  return __ldg(g + i);
+}
+__device__ __forceinline__ float4 stat_full(const float4* s, const float4* /*global*/, int i) { return s[i]; }
+
 // dS of 64 consecutive logits of one row, in place (fp32 bits in, fp32 bits out).
 //   grad_input pass (rows = tokens): columns col0.. are vocabulary entries; colb2 holds the bias in
 //     log2 units (-inf past V); `plain` means no bias and no column past V in this chunk.
-//   grad_W pass (rows = vocabulary): columns are tokens; tstats holds their statistics.
+//   grad_W pass (rows = vocabulary): columns are tokens; tstats holds their staged statistics, gst the
+//     same columns' four-word statistics in global memory.
 //   fge > 0 (gradient filter, grad_W pass): fover is set when some |dS| exceeds fge |w| (w the column's
 //   gradient weight), checked where each column's statistics are loaded anyway.
-template <bool kVocabRows>
+template <bool kVocabRows, class St>
 __device__ __forceinline__ void ds_chunk64(uint32_t (&r)[64], int col0, const DsRow& rc, bool general, bool plain,
-                                           const float* __restrict__ colb2, const float4* tstats, float& gbias,
-                                           float fge = 0.f, int* fover = nullptr) {
+                                           const float* __restrict__ colb2, const St* tstats,
+                                           const float4* __restrict__ gst, float& gbias, float fge = 0.f,
+                                           int* fover = nullptr) {
   if (!kVocabRows) {
     if (general) {
 #pragma unroll
@@ -261,22 +295,23 @@ __device__ __forceinline__ void ds_chunk64(uint32_t (&r)[64], int col0, const Ds
     if (general) {
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float4 st = tstats[i];
-        const int yt = __float_as_int(st.w);
-        const float e = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.bias2 - st.z)) * fmaf(rc.zl2, st.z, 1.0f);
-        const float g = (rc.scale * st.y) * (yt == rc.y ? e - 1.0f : e);
+        const float4 st = stat_full(tstats, gst, i);
+        const int yt = __float_as_int(st.y);
+        const float e = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.bias2 - st.w)) * fmaf(rc.zl2, st.w, 1.0f);
+        const float g = (rc.scale * st.z) * (yt == rc.y ? e - 1.0f : e);
         gbias += g;
-        if (fover != nullptr) *fover |= fabsf(g) > fge * fabsf(st.y) ? 1 : 0;
+        if (fover != nullptr) *fover |= fabsf(g) > fge * fabsf(st.z) ? 1 : 0;
         r[i] = __float_as_uint(g);
       }
     } else {
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float4 st = tstats[i];
+        // (exponent constant and target of the token; its gradient weight only where needed)
+        const float2 st = stat_xy(tstats[i]);
         float g = ex2_approx(fmaf(__uint_as_float(r[i]), kLog2e, rc.c + st.x));
-        if (__float_as_int(st.w) == rc.y) g -= rc.scale * st.y;
+        if (__float_as_int(st.y) == rc.y) g -= rc.scale * stat_full(tstats, gst, i).z;
         gbias += g;
-        if (fover != nullptr) *fover |= fabsf(g) > fge * fabsf(st.y) ? 1 : 0;
+        if (fover != nullptr) *fover |= fabsf(g) > fge * fabsf(stat_full(tstats, gst, i).z) ? 1 : 0;
         r[i] = __float_as_uint(g);
       }
     }
@@ -371,8 +406,9 @@ __device__ __forceinline__ OnlineRow online_row_finish(const PairParams& p, int 
     if (p.loss_tok != nullptr) p.loss_tok[row] = lt;
     const float uf = u * f;
     if (valid && u != 0.f && !(uf > 0.f)) atomicOr(p.zf_neg_out, 1u);
-    p.stats_out[row] = make_float4(valid && uf > 0.f ? log2f(uf) - lse2 : -INFINITY, valid ? u : 0.f, lse2,
-                                   __int_as_float(valid ? y : -1));
+    const float2 ct = make_float2(valid && uf > 0.f ? log2f(uf) - lse2 : -INFINITY, __int_as_float(valid ? y : -1));
+    p.stats_out[row] = make_float4(ct.x, ct.y, valid ? u : 0.f, lse2);
+    p.stats_ct_out[row] = ct;
     // entropy of softmax(z) = LSE - sum_n p_n z_n, for every row
     if (p.entropy_out != nullptr) p.entropy_out[row] = lse - T / L;
     p.row_redo[row] = r.ok ? 0u : 1u;
@@ -391,12 +427,20 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
                                                 const PairParams& p, uint32_t* __restrict__ status, int row_pair,
                                                 int hgroup, int jb = 0, int je = -1, int su = -1) {
   static_assert(!kOnline || (!kVocabRows && !kFilter), "the online form is a grad_input pass without the filter");
-  constexpr int kStages = PairCfg<kVocabRows>::kStages;
+  using Smem = PairSmem<kVocabRows, kFilter>;
+  constexpr int kStages = Smem::Cfg::kStages;
   // the classic passes behind an online grad_input pass run only when it asked for them
   if (p.gate != nullptr && *reinterpret_cast<const volatile uint32_t*>(p.gate) == 0u) return;
-  extern __shared__ uint8_t smem_raw[];
-  PairSmem<kVocabRows>& sm =
-      *reinterpret_cast<PairSmem<kVocabRows>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uintptr_t smem_base = reinterpret_cast<uintptr_t>(smem_raw);
+  if (pair_smem_slack<kVocabRows, kFilter>() != 0) {
+    smem_base = (smem_base + 1023) & ~uintptr_t(1023);
+  } else if ((smem_u32(smem_raw) & 1023u) != 0u) {
+    // (every CTA of the launch sees the same offset, so all of them return here, before any barrier)
+    if (threadIdx.x == 0) atomicOr(status, kStatusInternal);
+    return;
+  }
+  Smem& sm = *reinterpret_cast<Smem*>(smem_base);
   const uint32_t rank = cluster_ctarank();
   const int P = p.P;
   const int pr = static_cast<int>(rank >> 1);       // pair index within the cluster
@@ -421,9 +465,11 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
+    if (kVocabRows) {
+      mbar_init(&sm.st_full, 1);
+      mbar_init(&sm.st_empty, kEpiWarps);
+    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.st_full[b], 1);
-      mbar_init(&sm.st_empty[b], kEpiWarps);
       mbar_init(&sm.ds_full[b], 2);
       mbar_init(&sm.ds_free[b], static_cast<uint32_t>(P));
       mbar_init(&sm.rx_full[b], 1);
@@ -437,6 +483,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.o_zero, 2 * kEpiWarps);
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.never, 1);
     if (kOnline) {
       mbar_init(&sm.mref_ready, 4);       // the 4 warps of pair 0's CTA with these rows that hold half 0
       mbar_init(&sm.part_ready, 8 * P);   // the 8 epilogue warps of every pair's CTA with these rows
@@ -457,6 +504,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
+  float gbias_out = 0.f;   // grad_W pass: this epilogue thread's grad_bias partial (its row, its half)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------------------ TMA producer
@@ -464,6 +512,10 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // test-only (debug_stall_us): wait for a phase that nothing completes, before any copy is issued; the
+      // wait gives up like any other and the whole cluster winds down with nothing in flight
+      if (p.debug_stall_us != 0u) ok = mbar_wait(&sm.never, 0, abort, 1000ull * p.debug_stall_us);
+      int us = 0;   // grad_W pass: owned blocks whose statistics have been loaded
       auto next = [&]() {
         if (++stage == kStages) {
           stage = 0;
@@ -491,24 +543,27 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
                            h0 + static_cast<int>(q * (n2 / 2)) + 64 * b, (jb + j) * kPN + half * kTileM);
         next();
       };
-      int u = 0;   // owned blocks whose GEMM1 has been fully loaded
       for (int s = -2 * P; s < nt && ok; ++s) {
         const G1Share g = g1_share(s, pr, P);
         const bool has_g1 = g.block >= 0 && g.block < nt;
-        if (kVocabRows && has_g1 && g.prog == 0) {
-          // this block's per-token statistics (stats is padded to a multiple of 256 tokens)
-          const int sb = u & 1;
-          if (!mbar_wait(&sm.st_empty[sb], ((u >> 1) & 1) ^ 1, abort)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.st_full[sb], kPN * sizeof(float4));
-          bulk_load_1d(sm.colstats[sb], p.stats + static_cast<size_t>(jb + g.block) * kPN, kPN * sizeof(float4),
-                       &sm.st_full[sb]);
-        }
         const int kb0 = has_g1 ? share_begin(g.prog, nkb, P) : 0;
         const int kb1 = has_g1 ? share_begin(g.prog + 1, nkb, P) : 0;
         const int kbm = kStepOrder == 2 ? (kb0 + kb1) / 2 : kb1;
+        auto load_stats = [&]() {
+          // grad_W pass: the statistics of the owned block whose last GEMM1 share this step loads, into the
+          // single slot once the epilogue has turned the previous owned block into dS (stats are padded to a
+          // multiple of 256 tokens)
+          if (!kVocabRows || !ok || !has_g1 || g.prog != P - 1) return;
+          if (!mbar_wait(&sm.st_empty, (us & 1) ^ 1, abort)) {
+            ok = false;
+            return;
+          }
+          const size_t col = static_cast<size_t>(jb + g.block) * kPN;
+          const void* src = kFilter ? static_cast<const void*>(p.stats + col) : static_cast<const void*>(p.stats_ct + col);
+          mbar_arrive_expect_tx(&sm.st_full, static_cast<uint32_t>(sizeof(sm.colstats)));
+          bulk_load_1d(sm.colstats, src, static_cast<uint32_t>(sizeof(sm.colstats)), &sm.st_full);
+          ++us;
+        };
         auto load_gemm1 = [&](int kb_begin, int kb_end) {
           for (int kb = kb_begin; kb < kb_end && ok; ++kb) {
             if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
@@ -527,9 +582,9 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         load_gemm2(s, 0);
         if (kStepOrder == 2) load_gemm1(kb0, kbm);
         load_gemm2(s, 1);
+        load_stats();
         if (kStepOrder == 0) load_gemm1(kb0, kb1);
         if (kStepOrder == 2) load_gemm1(kbm, kb1);
-        if (has_g1 && g.prog == P - 1) ++u;
       }
       if (!ok) {
         // let copies already issued land before the CTA can finish
@@ -665,6 +720,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
             ok = false;
             break;
           }
+          // (the half was written by the other pair's stores; order them before the MMAs that read it)
+          fence_proxy_async_smem();
           mbar_arrive_cluster(half ? ds_full_c1 : ds_full_c0);
         }
         ++v;
@@ -710,10 +767,10 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       if (row < p.BT) {
         const float4 st = p.stats[row];
         rc.c = st.x + log2s;
-        rc.lse2 = st.z;
-        rc.f = fmaf(rc.zl2, st.z, 1.0f);
-        rc.y = __float_as_int(st.w);
-        rc.coef = scale * st.y;
+        rc.lse2 = st.w;
+        rc.f = fmaf(rc.zl2, st.w, 1.0f);
+        rc.y = __float_as_int(st.y);
+        rc.coef = scale * st.z;
       }
     } else {
       if (p.bias != nullptr && row < p.V) rc.bias2 = __ldg(p.bias + row) * kLog2e;
@@ -741,12 +798,13 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(qq * 32) << 16) + kTmemS + static_cast<uint32_t>(hh * 128);
-      const int sb = u & 1;
-      if (kVocabRows && !mbar_wait(&sm.st_full[sb], (u >> 1) & 1, abort)) {
+      // grad_W pass: the statistics of this half's 128 token columns (staged in the slot, and in global memory)
+      if (kVocabRows && !mbar_wait(&sm.st_full, u & 1, abort)) {
         ok = false;
         break;
       }
-      const float4* tstats = sm.colstats[kVocabRows ? sb : 0] + (kVocabRows ? hh * 128 : 0);
+      const typename Smem::Cfg::Stat* tstats = sm.colstats + (kVocabRows ? hh * 128 : 0);
+      const float4* gst = kVocabRows ? p.stats + static_cast<size_t>(jb + j) * kPN + hh * 128 : nullptr;
       const int col0 = (jb + j) * kPN + hh * 128;
       // dS of this row's 128 columns in two chunks of 64, packed to bf16 pairs
       uint32_t pk0[32], pk1[32];
@@ -795,8 +853,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
           online_chunk64(ra, col0, -on_ref, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, p.bias, rc.y, on_lsum, on_zy,
                          on_ent, on_tsum);
         else
-          ds_chunk64<kVocabRows>(ra, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gbias,
-                                 fge, fov);
+          ds_chunk64<kVocabRows>(ra, col0, rc, general, p.bias == nullptr && col0 + 64 <= p.V, p.colb2, tstats, gst,
+                                 gbias, fge, fov);
         if (!kVocabRows && filt) small = filter_small_row(ra, rc, p.filter_eps);
 #pragma unroll
         for (int i2 = 0; i2 < 32; ++i2) pk0[i2] = pack_bf16x2(__uint_as_float(ra[2 * i2]), __uint_as_float(ra[2 * i2 + 1]));
@@ -805,11 +863,16 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
                          on_lsum, on_zy, on_ent, on_tsum);
         else
           ds_chunk64<kVocabRows>(rb, col0 + 64, rc, general, p.bias == nullptr && col0 + 128 <= p.V, p.colb2,
-                                 tstats + 64, gbias, fge, fov);
+                                 tstats + 64, kVocabRows ? gst + 64 : nullptr, gbias, fge, fov);
         if (!kVocabRows && filt) small = filter_small_row(rb, rc, p.filter_eps) && small;
         if (kVocabRows && filt) small = (over == 0);
 #pragma unroll
         for (int i2 = 0; i2 < 32; ++i2) pk1[i2] = pack_bf16x2(__uint_as_float(rb[2 * i2]), __uint_as_float(rb[2 * i2 + 1]));
+        if (kVocabRows) {
+          // the statistics slot is free for the producer's next owned block
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.st_empty);
+        }
         if (filt) {
           // this warp's verdict on its 32 rows of half hh of block j, published at once to every CTA of the
           // cluster: their producers and MMA threads skip the half when all 8 owner warps say "small"
@@ -839,10 +902,6 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       for (int ch = 0; ch < 8; ++ch)
         *reinterpret_cast<uint4*>(ds_row + kBox + ((ch ^ (rl & 7)) << 4)) =
             make_uint4(pk1[4 * ch + 0], pk1[4 * ch + 1], pk1[4 * ch + 2], pk1[4 * ch + 3]);
-      if (kVocabRows) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.st_empty[sb]);
-      }
       fence_proxy_async_smem();
       __syncwarp();
       // with the filter, a half every pair skips is not sent: the other pairs' receivers get its byte count
@@ -850,7 +909,28 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       // A verdict wait that gave up sends the data (the kernel is winding down by then).
       bool send = true;
       if (filt && lane == 0) send = filter_verdict(sm, j, hh, abort) != 1;
-      if (lane == 0) {
+      if (kDsHandOver == 1) {
+        // the warp's 32 rows are two contiguous 4 KB runs (one per 64-column box); each lane moves 16-byte
+        // pieces of them, so that every store instruction writes 512 consecutive bytes of the peer's slot
+        send = __shfl_sync(0xffffffffu, send, 0);
+        const uint8_t* const src = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
+        for (int pp = 0; pp < P; ++pp) {
+          if (pp == pr) continue;
+          const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
+          const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[hh]), dst_rank);
+          if (send) {
+            const uint32_t dst = mapa_shared(smem_u32(src), dst_rank);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t off = static_cast<uint32_t>(i >> 3) * kBox + static_cast<uint32_t>(i & 7) * 512u +
+                                   static_cast<uint32_t>(lane) * 16u;
+              st_async_v4(dst + off, *reinterpret_cast<const uint4*>(src + off), bar);
+            }
+          } else if (lane == 0) {
+            mbar_complete_tx_cluster(bar, 2u * 4096u);
+          }
+        }
+      } else if (lane == 0) {
         // this warp's 32 rows of both 64-column boxes to the other pairs' CTAs with the same rows
         uint8_t* const src = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
         for (int pp = 0; pp < P; ++pp) {
@@ -994,22 +1074,28 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         }
       }
     }
-    if (kVocabRows) {
-      // this CTA's share of grad_bias (its owned blocks) -> pair 0's CTA with the same rows
-      if (hh == 1) sm.half_bias[rl] = gbias;
-      named_barrier_sync(3, kEpiWarps * 32);
-      if (hh == 0) st_shared_cluster_f32(mapa_shared(smem_u32(&sm.gb_gather[pr][rl]), q), gbias + sm.half_bias[rl]);
-    }
+    gbias_out = gbias;
   }
 
   tc_fence_before();
   cluster_sync();
+  // grad_W pass: every MMA of the cluster has completed by now (each MMA thread waited for its drain, each
+  // epilogue for o_full, before the barrier), so the dS blocks are free and gather the grad_bias partials:
+  // [pair][half][row] in pair 0's CTA with the same rows, added there in pair and half order
+  float* const gb_gather = reinterpret_cast<float*>(sm.ds);
+  if (kVocabRows) {
+    if (warp < kEpiWarps) {
+      const int rl = (warp & 3) * 32 + lane;
+      st_shared_cluster_f32(mapa_shared(smem_u32(gb_gather + (pr * 2 + (warp >> 2)) * kTileM + rl), q), gbias_out);
+    }
+    cluster_sync();
+  }
   if (kVocabRows && pr == 0 && warp < 4 && hgroup == 0 && p.grad_bias != nullptr && !sm.abort) {
     const int rl = warp * 32 + lane;
     const int row = r0 + rl;
     if (row < p.V) {
       float acc = 0.f;
-      for (int pp = 0; pp < P; ++pp) acc += sm.gb_gather[pp][rl];
+      for (int pp = 0; pp < P; ++pp) acc += gb_gather[(pp * 2) * kTileM + rl] + gb_gather[(pp * 2 + 1) * kTileM + rl];
       if (su >= 0) {
         p.vs_gb[static_cast<size_t>(su) * 256 + static_cast<int>(q) * kTileM + rl] = acc;   // for dw_vmerge_kernel
       } else {
@@ -1245,6 +1331,7 @@ PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
   PairParams p{};
   p.bias = a.bias;
   p.stats = a.stats;
+  p.stats_ct = a.stats_ct;
   p.colb2 = a.colb2;
   p.scale = a.scale;
   p.zf_neg = a.zf_neg;
@@ -1253,6 +1340,7 @@ PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
   p.filter_eps = a.filter_eps;
   p.skip_count = a.skip_count;
   p.row_perm = a.row_perm;
+  p.debug_stall_us = a.debug_stall_us;
   p.BT = a.BT;
   p.V = a.V;
   p.H = a.H;
@@ -1272,6 +1360,7 @@ PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
   p.entropy_out = a.entropy_out;
   p.row_redo = a.row_redo;
   p.stats_out = a.stats_out;
+  p.stats_ct_out = a.stats_ct_out;
   p.row_loss = a.row_loss;
   p.loss_tok = a.loss_tok;
   p.zf_neg_out = a.zf_neg_out;
@@ -1374,8 +1463,8 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
                               cudaStream_t stream) {
   int h_chunks = 0;
   PairParams p = make_pair_params<kVocabRows>(a, &h_chunks);
-  constexpr size_t smem = pair_smem_bytes<kVocabRows>();
   const bool filt = p.filter_eps > 0.f;
+  const size_t smem = filt ? pair_smem_bytes<kVocabRows, true>() : pair_smem_bytes<kVocabRows, false>();
   auto kern = filt ? dgrad_pair_kernel<kVocabRows, true> : dgrad_pair_kernel<kVocabRows, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -1414,7 +1503,7 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   p.vs_stat = a.vs_stat;
   p.vs_o = a.vs_o;
   p.vs_count = a.vs_count;
-  constexpr size_t smem = pair_smem_bytes<false>();
+  constexpr size_t smem = pair_smem_bytes<false, false>();
   cudaError_t e =
       cudaFuncSetAttribute(dgrad_online_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -1455,9 +1544,10 @@ cudaError_t launch_dgrad_both(const CUtensorMap& hidden_map, const CUtensorMap& 
     if (e != cudaSuccess) return e;
     return launch_dgrad_pair<true>(w_map, hidden_map, a, stream);
   }
-  constexpr size_t smem = pair_smem_bytes<false>() > pair_smem_bytes<true>() ? pair_smem_bytes<false>()
-                                                                               : pair_smem_bytes<true>();
-  auto kern = a.filter_eps > 0.f ? dgrad_both_kernel<true> : dgrad_both_kernel<false>;
+  const bool filt = a.filter_eps > 0.f;
+  const size_t smem = filt ? std::max(pair_smem_bytes<false, true>(), pair_smem_bytes<true, true>())
+                           : std::max(pair_smem_bytes<false, false>(), pair_smem_bytes<true, false>());
+  auto kern = filt ? dgrad_both_kernel<true> : dgrad_both_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int in_rp = row_pairs_of(p_in), w_rp = row_pairs_of(p_w);

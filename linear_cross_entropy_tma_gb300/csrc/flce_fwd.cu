@@ -276,8 +276,8 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
                                  float* __restrict__ entropy, const float* __restrict__ zy,
                                  const int64_t* __restrict__ target, int BT, int V, int64_t ignore_index,
                                  float z_loss, const float* __restrict__ bias, const float* __restrict__ grad_tok,
-                                 float4* __restrict__ stats, float* __restrict__ row_loss,
-                                 float* __restrict__ loss_tok, float* __restrict__ colb2,
+                                 float4* __restrict__ stats, float2* __restrict__ stats_ct,
+                                 float* __restrict__ row_loss, float* __restrict__ loss_tok, float* __restrict__ colb2,
                                  uint32_t* __restrict__ zf_neg, uint32_t* __restrict__ status,
                                  const uint32_t* __restrict__ gate) {
   if (gate != nullptr && *reinterpret_cast<const volatile uint32_t*>(gate) == 0u) return;
@@ -286,7 +286,10 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
   if (t < ((V + 255) & ~255)) colb2[t] = t < V ? (bias != nullptr ? bias[t] * kLog2e : 0.f) : -INFINITY;
   if (t >= BT) {
     // padding rows (up to a multiple of 256 tokens) read by the gradient passes: no contribution
-    if (t < ((BT + 255) & ~255)) stats[t] = make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
+    if (t < ((BT + 255) & ~255)) {
+      stats[t] = make_float4(-INFINITY, __int_as_float(-1), 0.f, 0.f);
+      stats_ct[t] = make_float2(-INFINITY, __int_as_float(-1));
+    }
     return;
   }
   float M = -INFINITY;
@@ -316,8 +319,10 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
   const float f = 1.0f + 2.0f * z_loss * lse;
   const float uf = u * f;
   if (valid && u != 0.f && !(uf > 0.f)) atomicOr(zf_neg, 1u);
-  stats[t] = make_float4(valid && uf > 0.f ? log2f(uf) - lse2 : -INFINITY, valid ? u : 0.f, lse2,
-                         __int_as_float(valid ? static_cast<int>(y) : -1));
+  const float2 ct = make_float2(valid && uf > 0.f ? log2f(uf) - lse2 : -INFINITY,
+                                __int_as_float(valid ? static_cast<int>(y) : -1));
+  stats[t] = make_float4(ct.x, ct.y, valid ? u : 0.f, lse2);
+  stats_ct[t] = ct;
 }
 
 constexpr int kReduceThreads = 1024;
@@ -334,7 +339,7 @@ loss_reduce_kernel(const float* __restrict__ row_loss, const float4* __restrict_
   long long cnt = 0;
   for (int t = threadIdx.x; t < BT; t += kReduceThreads) {
     acc += static_cast<double>(row_loss[t]);
-    cnt += (__float_as_int(stats[t].w) >= 0) ? 1 : 0;
+    cnt += (__float_as_int(stats[t].y) >= 0) ? 1 : 0;
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -367,10 +372,13 @@ loss_reduce_kernel(const float* __restrict__ row_loss, const float4* __restrict_
 // Before an online grad_input pass: the per-column bias table (as lse_merge_kernel writes it) and the
 // statistics of the padding rows past BT.
 __global__ void online_prep_kernel(const float* __restrict__ bias, int V, int BT, float* __restrict__ colb2,
-                                   float4* __restrict__ stats) {
+                                   float4* __restrict__ stats, float2* __restrict__ stats_ct) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t < ((V + 255) & ~255)) colb2[t] = t < V ? (bias != nullptr ? bias[t] * kLog2e : 0.f) : -INFINITY;
-  if (t >= BT && t < ((BT + 255) & ~255)) stats[t] = make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
+  if (t >= BT && t < ((BT + 255) & ~255)) {
+    stats[t] = make_float4(-INFINITY, __int_as_float(-1), 0.f, 0.f);
+    stats_ct[t] = make_float2(-INFINITY, __int_as_float(-1));
+  }
 }
 
 // Before an online grad_input pass (one CTA): the valid count, the gradient scale G and the bad-target
@@ -435,6 +443,7 @@ size_t fused_workspace_bytes(int64_t BT, int64_t V) {
   off += align_up(sizeof(float) * kMaxSplits * btp, 256);
   off += align_up(sizeof(float) * btp, 256);
   off += align_up(sizeof(float4) * align_up(btp, 256), 256);
+  off += align_up(sizeof(float2) * align_up(btp, 256), 256);
   off += align_up(sizeof(float) * btp, 256);
   off += align_up(sizeof(float) * vp, 256);
   off += align_up(sizeof(uint32_t) * btp, 256);
@@ -468,6 +477,8 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   off += align_up(sizeof(float) * btp, 256);
   w.stats = reinterpret_cast<float4*>(p + off);
   off += align_up(sizeof(float4) * align_up(btp, 256), 256);
+  w.stats_ct = reinterpret_cast<float2*>(p + off);
+  off += align_up(sizeof(float2) * align_up(btp, 256), 256);
   w.row_loss = reinterpret_cast<float*>(p + off);
   off += align_up(sizeof(float) * btp, 256);
   w.colb2 = reinterpret_cast<float*>(p + off);
@@ -512,7 +523,7 @@ cudaError_t launch_lse_passes(const FusedArgs& a, const FusedWorkspace& ws, int 
     lse_merge_kernel<<<merge_threads / 256, 256, 0, stream>>>(ws.part, ws.part_t, splits, BTp, a.entropy, ws.zy,
                                                             a.target, BT, V,
                                                             a.ignore_index, a.z_loss, a.bias, a.grad_tok, ws.stats,
-                                                            ws.row_loss, a.loss_tok, ws.colb2, ws.zf_neg, ws.status,
+                                                            ws.stats_ct, ws.row_loss, a.loss_tok, ws.colb2, ws.zf_neg, ws.status,
                                                             gate);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else if (events != nullptr && (e = cudaEventRecord(events[1], stream)) != cudaSuccess) {
@@ -527,7 +538,7 @@ cudaError_t launch_online_prep(const FusedArgs& a, const FusedWorkspace& ws, cud
   const int BT = static_cast<int>(a.BT);
   const int V = static_cast<int>(a.V);
   const int n = max((BT + 255) & ~255, (V + 255) & ~255);
-  online_prep_kernel<<<n / 256, 256, 0, stream>>>(a.bias, V, BT, ws.colb2, ws.stats);
+  online_prep_kernel<<<n / 256, 256, 0, stream>>>(a.bias, V, BT, ws.colb2, ws.stats, ws.stats_ct);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   online_count_kernel<<<1, kReduceThreads, 0, stream>>>(a.target, BT, V, a.ignore_index, a.reduction, a.grad_scale,

@@ -49,8 +49,10 @@ struct FusedWorkspace {
   float* zy;         // [BTp] target logit
   float4* stats;     // [BT rounded up to 256] per row t, with LSE2 = LSE log2 e, f = 1 + 2 z_loss LSE and u
                      // the row's upstream gradient (1 unless reduction none):
-                     //   x = log2(f u) - LSE2 (-inf for ignored rows and when f u <= 0), y = valid ? u : 0,
-                     //   z = LSE2, w = target as int bits (-1 for ignored rows); rows past BT: (-inf, 0, 0, -1)
+                     //   x = log2(f u) - LSE2 (-inf for ignored rows and when f u <= 0), y = target as int bits
+                     //   (-1 for ignored rows), z = valid ? u : 0, w = LSE2; rows past BT: (-inf, -1, 0, 0)
+  float2* stats_ct;  // [BT rounded up to 256] the first two words of stats (x, y): what the exact grad_W pass
+                     // stages per block
   float* row_loss;   // [BTp] valid * (LSE - z_y + z_loss LSE^2)
   float* colb2;      // [V rounded up to 256] bias * log2 e (0 without bias); -inf past V
   uint32_t* row_redo; // [BTp] online flow: 1 for a row the grad_input pass left to the classic passes
@@ -105,6 +107,7 @@ struct FusedArgs {
   bool separate_lse;          // always the classic flow (LSE tiles first)
   int vocab_splits;           // online grad_input pass: 0 automatic, 1 never, k >= 2 every row block in k parts
   int token_splits;           // grad_W pass: the same over token ranges
+  uint32_t debug_stall_us;    // test-only: the gradient passes' producers first wait this long on nothing
 };
 
 // The vocabulary sort: logit_avg, the sorted order (in w.vals[0]), the sorted copies of W, the bias and
@@ -116,6 +119,7 @@ cudaError_t launch_vocab_sort(const FusedArgs& a, const VocabSortWorkspace& w, u
 struct DgPairArgs {
   const float* bias;
   const float4* stats;
+  const float2* stats_ct;    // (x, y) of stats, compact
   const float* colb2;
   const float* scale;
   const uint32_t* zf_neg;
@@ -140,6 +144,7 @@ struct DgPairArgs {
   float* entropy_out;        // per-row entropy out, or NULL
   uint32_t* row_redo;        // [BTp] rows the online pass left to the classic one (see flce_bwd.cu)
   float4* stats_out;
+  float2* stats_ct_out;
   float* row_loss;
   float* loss_tok;
   uint32_t* zf_neg_out;
@@ -158,6 +163,7 @@ struct DgPairArgs {
   float* split_scratch;
   size_t split_scratch_bytes;
   uint32_t* split_count;
+  uint32_t debug_stall_us;   // test-only (flce_fwd_bwd_options.debug_stall_us)
 };
 
 // kVocabRows = false: grad_input pass (rows = tokens, reduction over the vocabulary);

@@ -51,6 +51,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
   DgPairArgs pa{};
   pa.bias = a.bias;
   pa.stats = ws.stats;
+  pa.stats_ct = ws.stats_ct;
   pa.colb2 = ws.colb2;
   pa.scale = ws.scale;
   pa.zf_neg = ws.zf_neg;
@@ -68,6 +69,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
   pa.status = ws.status;
   // (read by the grad_W pass only)
   pa.token_splits = a.token_splits;
+  pa.debug_stall_us = a.debug_stall_us;
   pa.split_scratch = reinterpret_cast<float*>(ws.part);
   pa.split_scratch_bytes = ws.part_bytes;
   pa.split_count = ws.ts_count;
@@ -89,6 +91,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     po.entropy_out = a.entropy;
     po.row_redo = ws.row_redo;
     po.stats_out = ws.stats;
+    po.stats_ct_out = ws.stats_ct;
     po.row_loss = ws.row_loss;
     po.loss_tok = a.loss_tok;
     po.zf_neg_out = ws.zf_neg;
