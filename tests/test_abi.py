@@ -85,8 +85,8 @@ def test_fwd_bwd_argument_errors(lib):
 
 
 def _fwd_ex(lib, red=2, loss=None, grad_scale=1.0, gtok=None, ltok=None, acc=0, gi=0x5000, ent=None, eps=0.0,
-            sort=0, la=None, vo=None, wsb=1 << 30, splits=0, tsplits=0):
-    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent, eps, sort, la, vo, 0, splits, tsplits)
+            sort=0, la=None, vo=None, wsb=1 << 30, splits=0, tsplits=0, stall=0):
+    opts = _lib.FwdBwdOptions(grad_scale, gtok, ltok, acc, ent, eps, sort, la, vo, 0, splits, tsplits, stall)
     return lib.flce_fwd_bwd_ex(0x1000, 0x2000, None, 0x3000, 128, 64, 512, -100, red, 0.0, loss, gi, 0x6000, None,
                                None, 0x7000, wsb, ctypes.byref(opts), None)
 
@@ -122,6 +122,47 @@ def test_fwd_bwd_ex_argument_errors(lib):
     assert _fwd_ex(lib, red=0, loss=0x4000, eps=2.0 ** -12) == NO_DEVICE
     # the plain entry points do not take reduction none
     assert _fwd(lib, red=2) == INVALID_ARG
+    # the test-only stall of the bounded waits: at most one second
+    assert _fwd_ex(lib, stall=1000001) == INVALID_ARG
+    assert b"debug_stall_us" in lib.flce_last_error()
+    assert _fwd_ex(lib, stall=1000) == NO_DEVICE
+
+
+def test_scale_and_reduce_argument_errors(lib):
+    def scale(g=0x1000, dtype=0, n=100, up=0x2000, div=None):
+        return lib.flce_scale_gradient(g, dtype, n, up, div, None)
+
+    assert scale(dtype=3) == INVALID_ARG
+    assert scale(n=-1) == INVALID_ARG
+    assert scale(up=None) == INVALID_ARG
+    assert scale(g=None) == INVALID_ARG
+    assert scale(g=0x1008) == MISALIGNED
+    assert scale(up=0x2002) == MISALIGNED
+    assert scale(div=0x3004) == MISALIGNED
+    assert scale() == NO_DEVICE
+    assert scale(g=None, n=0, div=0x3000, dtype=2) == NO_DEVICE
+
+    def red(cs=0x1000, zs=0x1004, nv=0x1008, reduction=0, loss=0x1010):
+        return lib.ce_reduce_loss(cs, zs, nv, 1e-4, reduction, loss, None)
+
+    assert red(reduction=2) == INVALID_ARG
+    assert red(loss=None) == INVALID_ARG
+    assert red(nv=None) == INVALID_ARG
+    assert red(nv=0x100C) == MISALIGNED
+    assert red() == NO_DEVICE
+    assert red(reduction=1) == NO_DEVICE
+
+
+def test_ce_noalloc_argument_errors(lib):
+    def na(logits=0x1000, labels=0x2000, B=8, V=16, cs=0x3000, zs=0x3004, nv=0x3008):
+        return lib.ce_with_grad_noalloc(logits, labels, B, V, -100, 0.0, cs, zs, nv, None)
+
+    assert na(logits=None) == INVALID_ARG and b"non-NULL" in lib.flce_last_error()
+    assert na(V=0) == INVALID_ARG and b"V > 0" in lib.flce_last_error()
+    assert na(V=1 << 31) == UNSUPPORTED and b"V must be below 2^31" in lib.flce_last_error()
+    assert na(B=262145) == UNSUPPORTED and b"at most 262144 rows" in lib.flce_last_error()
+    assert na(logits=0x1008) == MISALIGNED and b"misaligned" in lib.flce_last_error()
+    assert na() == NO_DEVICE and b"10.3" in lib.flce_last_error()
 
 
 def test_ce_argument_errors(lib):

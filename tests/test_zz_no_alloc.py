@@ -1,14 +1,15 @@
 """ce_with_grad_noalloc: the standalone CE entry point for callers that cannot allocate device memory
 (for example a plugin that receives only its input and output buffers from an engine that plans all
 device memory ahead).  It takes its scratch from a fixed array inside the library instead of a
-workspace.  Checked through the C ABI against ce_with_grad on the same inputs, on two calls in a row
-(the second call finds the first call's leftovers in the shared array).  This file is collected last
+workspace.  Checked through the C ABI against ce_with_grad on the same inputs and against the fp64
+oracle, on two calls in a row (the second call finds the first call's leftovers in the shared array).  This file is collected last
 so that a run stopping at the first failure has run every other test before it."""
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 from linear_cross_entropy_tma_gb300 import _lib
 from linear_cross_entropy_tma_gb300 import workloads as wl
 from parity import assert_grad_close, assert_scalar_close, bf16_tensor, bf16_to_numpy_f32
@@ -69,6 +70,11 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert_scalar_close(got[0], ref[0], f"call {call}: ce_sum")
         assert_scalar_close(got[1], ref[1], f"call {call}: z_sum")
         assert_grad_close(bf16_to_numpy_f32(a), bf16_to_numpy_f32(b), f"call {call}: dlogits")
+        orc = oracle.ce_reference(x, lab, z_loss=1e-4)
+        assert got[2] == orc["n_valid"], f"call {call}: n_valid {got[2]} vs oracle {orc['n_valid']}"
+        assert_scalar_close(got[0], orc["ce_sum"], f"call {call}: ce_sum vs oracle")
+        assert_scalar_close(got[1], orc["z_sum"], f"call {call}: z_sum vs oracle")
+        assert_grad_close(bf16_to_numpy_f32(a), orc["dlogits"], f"call {call}: dlogits vs oracle")
 
 
 def test_noalloc_rejects_too_many_rows():
