@@ -368,6 +368,56 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
                 split_units=split_units, token_split_units=token_split_units, graph_ms=graph_ms)
 
 
+def bench_workload(w: wl.FusedWorkload, steps: int, warmup: int, local: int, peaks: dict, oracle_rows: int | None):
+    """One more fused workload, timed like the headline (same call, W warm-up steps, K steps between two
+    CUDA events on the launching stream, clocks sampled), and the fp64 oracle's rate on it: all BT tokens
+    when oracle_rows is None, else a sample of that many tokens (labelled row-sampled)."""
+    import torch
+    import linear_cross_entropy_tma_gb300 as flce
+    dev = torch.device("cuda", local)
+    d = wl.make_fused_inputs(w)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats(dev)
+    hidden = to_device_bf16(d["hidden"], dev)
+    W = to_device_bf16(d["W"], dev)
+    target = torch.from_numpy(d["target"]).to(dev)
+    bias = torch.from_numpy(d["bias"]).to(dev) if d["bias"] is not None else None
+    res = flce.flce_fwd_bwd(hidden, W, target, bias=bias, reduction=w.reduction, z_loss=w.z_loss)
+    kw = dict(bias=bias, reduction=w.reduction, z_loss=w.z_loss, workspace=res["workspace"],
+              out={k: v for k, v in res.items() if k in ("loss", "n_valid", "grad_input", "grad_W", "grad_bias")
+                   and v is not None})
+    for _ in range(warmup):
+        flce.flce_fwd_bwd(hidden, W, target, **kw)
+    torch.cuda.synchronize()
+    assert flce.read_device_status(res["workspace"]) == 0, f"device status word non-zero ({w.name})"
+    sampler = ClockSampler(local)
+    sampler.start()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        flce.flce_fwd_bwd(hidden, W, target, **kw)
+    b.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = a.elapsed_time(b) / steps
+    peak = torch.cuda.max_memory_allocated(dev)
+    tf = w.flops() / (ms * 1e-3) / 1e12
+    del hidden, W, target, bias, res, kw
+    torch.cuda.empty_cache()
+    dw = widened(d)
+    n = w.BT if oracle_rows is None else min(oracle_rows, w.BT)
+    t = time_oracle_tokens(w, dw, n)
+    return {"workload": w.name, "ms_per_step": ms, "tokens_per_s": w.BT / (ms * 1e-3), "tflops": tf,
+            "frac_of_burst": tf / peaks["bf16_tflops"], "frac_of_sustained": tf / peaks["bf16_tflops_sustained"],
+            "flops_per_step": w.flops(), "peak_allocated_bytes": peak, "avoided_fp32_logits_bytes": 4 * w.BT * w.V,
+            "clocks": clocks,
+            "oracle": {"tokens_per_s": n / t, "cores": cpu_cores(), "seconds": t,
+                       "sample": "full: every token" if n == w.BT else
+                                 f"row-sampled: the first {n} of {w.BT} tokens (full V and H per token)"}}
+
+
 def bench_ce(steps: int, warmup: int, local: int, peaks: dict):
     import torch
     import linear_cross_entropy_tma_gb300 as flce
@@ -401,7 +451,18 @@ def bench_ce(steps: int, warmup: int, local: int, peaks: dict):
 
 
 # ----------------------------------------------------------------------------------- oracle timing
+def widened(d: dict) -> dict:
+    """The inputs with W (and the bias) widened to float64 once, outside any timed region: the oracle then
+    uses them as they are, so a timed call does the method's work and not a 1.4 GB conversion of W."""
+    import oracle
+    e = dict(d)
+    e["W"] = oracle.widen(d["W"])
+    e["bias"] = None if d["bias"] is None else oracle.widen(d["bias"])
+    return e
+
+
 def time_oracle_tokens(w: wl.FusedWorkload, d: dict, n_rows: int, offset: int = 0):
+    """Seconds the fp64 oracle takes for the full loss + gradient work of n_rows tokens (d from widened())."""
     import oracle
     rows = slice(offset, offset + n_rows)
     t = time.perf_counter()
@@ -419,21 +480,22 @@ def cpu_cores():
 
 
 def cpu_baseline(w: wl.FusedWorkload, target_s: float = 12.0):
-    d = wl.make_fused_inputs(w)
+    d = widened(wl.make_fused_inputs(w))
     time_oracle_tokens(w, d, 32)
     t256 = time_oracle_tokens(w, d, 256)
     n = int(max(256, min(w.BT - 64, 256 * target_s / max(t256, 1e-3))))
     t = time_oracle_tokens(w, d, n, offset=64)
     return {"value": n / t, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
             "sample": f"fp64 oracle, full loss + grad_input + grad_W work for {n} of the {w.BT} tokens "
-                      f"(rows 64..{64 + n - 1}), full V={w.V} and H={w.H}; {t:.1f} s"}
+                      f"(rows 64..{64 + n - 1}), full V={w.V} and H={w.H}; {t:.1f} s (W widened to fp64 once, "
+                      f"before timing)"}
 
 
 def run_reference(args, w):
     rank, world, local = dist_info()
     if rank != 0:
         return 0
-    d = wl.make_fused_inputs(w)
+    d = widened(wl.make_fused_inputs(w))
     per_step = 64
     for k in range(args.warmup):
         time_oracle_tokens(w, d, per_step, offset=(k * per_step) % max(1, w.BT - per_step))
@@ -473,6 +535,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(wl.FUSED_WORKLOADS), default="long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ce", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other fused workloads")
     ap.add_argument("--filter-eps", type=float, default=2.0 ** -12,
                     help="also time the gradient-filtering variant at this threshold (0: skip)")
     args = ap.parse_args()
@@ -559,6 +622,12 @@ def main():
     }
     if not args.no_ce and world == 1:
         line["ce_standalone"] = bench_ce(args.steps, args.warmup, local, peaks)
+    if not args.no_workloads and world == 1:
+        # the other fused workloads in the same run (the headline value stays on this one); the oracle in
+        # full for the two small ones, row-sampled for the large ones
+        others = {"tiny": None, "qwen3": None, "gemma2": 256, "long": 256}
+        line["workloads"] = {k: bench_workload(wl.FUSED_WORKLOADS[k], args.steps, args.warmup, local, peaks, rows)
+                             for k, rows in others.items() if k != args.workload}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
