@@ -92,19 +92,20 @@ constexpr uint32_t kTmemO = 256;
 // 2 KiB, in the exact pass; the four-word statistics, 4 KiB, in the filtering pass, which also keeps a
 // ring of skip verdicts and has one stage fewer (4).  The other passes have 5 stages.  After the main
 // loop the dS block gathers the grad_bias partials.
-template <bool kVocabRows, bool kFilter>
+template <bool kVocabRows, bool kFilter, int kSlots = 2>
 struct PairCfg {
-  static constexpr int kStages = (kVocabRows && kFilter) ? 4 : 5;
+  static_assert(kSlots == 2 || (kSlots == 4 && !kFilter), "dS slots: 2, or 4 for the exact passes");
+  static constexpr int kStages = kSlots == 4 ? 3 : (kVocabRows && kFilter) ? 4 : 5;
   static constexpr int kStatCols = kVocabRows ? kPN : 1;
   static constexpr int kRing = kFilter ? kFlagRing : 1;
   using Stat = typename std::conditional<kFilter, float4, float2>::type;
 };
 
-template <bool kVocabRows, bool kFilter>
+template <bool kVocabRows, bool kFilter, int kSlots = 2>
 struct PairSmem {
-  using Cfg = PairCfg<kVocabRows, kFilter>;
+  using Cfg = PairCfg<kVocabRows, kFilter, kSlots>;
   uint8_t stage[Cfg::kStages][kStage];
-  uint8_t ds[kDsBytes];
+  uint8_t ds[kSlots][kHalfBytes];
   typename Cfg::Stat colstats[Cfg::kStatCols];
   uint64_t full[Cfg::kStages];
   uint64_t empty[Cfg::kStages];
@@ -112,9 +113,9 @@ struct PairSmem {
   uint64_t st_empty;
   uint64_t s_full;
   uint64_t s_empty;
-  uint64_t ds_full[2];
-  uint64_t ds_free[2];
-  uint64_t rx_full[2];
+  uint64_t ds_full[kSlots];
+  uint64_t ds_free[kSlots][kMaxPairs];   // [slot][pair that consumed the slot's previous content]
+  uint64_t rx_full[kSlots];
   uint64_t o_full;
   uint64_t o_zero;
   uint64_t drain;
@@ -131,16 +132,20 @@ constexpr size_t kSmemBudget = 232448;
 // with 1023 bytes of slack is placed at the next 1024-byte boundary; the exact grad_W pass's layout does
 // not fit with the slack, so it is placed at the start of the dynamic shared memory, which the kernel
 // checks is on a 1024-byte boundary (FLCE_STATUS_INTERNAL and an early return otherwise).
-template <bool kVocabRows, bool kFilter>
+template <bool kVocabRows, bool kFilter, int kSlots = 2>
 constexpr size_t pair_smem_slack() {
-  return sizeof(PairSmem<kVocabRows, kFilter>) + 1024 <= kSmemBudget ? 1024 : 0;
+  return sizeof(PairSmem<kVocabRows, kFilter, kSlots>) + 1024 <= kSmemBudget ? 1024 : 0;
 }
-template <bool kVocabRows, bool kFilter>
-constexpr size_t pair_smem_bytes() { return sizeof(PairSmem<kVocabRows, kFilter>) + pair_smem_slack<kVocabRows, kFilter>(); }
+template <bool kVocabRows, bool kFilter, int kSlots = 2>
+constexpr size_t pair_smem_bytes() {
+  return sizeof(PairSmem<kVocabRows, kFilter, kSlots>) + pair_smem_slack<kVocabRows, kFilter, kSlots>();
+}
 static_assert(pair_smem_bytes<false, false>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
 static_assert(pair_smem_bytes<true, false>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
 static_assert(pair_smem_bytes<false, true>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
 static_assert(pair_smem_bytes<true, true>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
+static_assert(pair_smem_bytes<false, false, 4>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
+static_assert(pair_smem_bytes<true, false, 4>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
 static_assert(sizeof(float) * kMaxPairs * 2 * kTileM <= kDsBytes, "the dS block gathers the grad_bias partials");
 
 // Gradient filter: the verdict on half `half` of block j, once the 8 epilogue warps of its owner pair that
@@ -422,18 +427,18 @@ __device__ __forceinline__ OnlineRow online_row_finish(const PairParams& p, int 
 // One cluster's work: rows [256 row_pair, +256) (128 per CTA of each pair) and the H chunks of
 // group hgroup (P consecutive 256-wide chunks, one per pair).
 // Columns: blocks [jb, je) of 256 (all of them except for a vocabulary-split unit of the online pass, su >= 0).
-template <bool kVocabRows, bool kFilter, bool kOnline = false>
+template <bool kVocabRows, bool kFilter, bool kOnline = false, int kSlots = 2>
 __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols,
                                                 const PairParams& p, uint32_t* __restrict__ status, int row_pair,
                                                 int hgroup, int jb = 0, int je = -1, int su = -1) {
   static_assert(!kOnline || (!kVocabRows && !kFilter), "the online form is a grad_input pass without the filter");
-  using Smem = PairSmem<kVocabRows, kFilter>;
+  using Smem = PairSmem<kVocabRows, kFilter, kSlots>;
   constexpr int kStages = Smem::Cfg::kStages;
   // the classic passes behind an online grad_input pass run only when it asked for them
   if (p.gate != nullptr && *reinterpret_cast<const volatile uint32_t*>(p.gate) == 0u) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uintptr_t smem_base = reinterpret_cast<uintptr_t>(smem_raw);
-  if (pair_smem_slack<kVocabRows, kFilter>() != 0) {
+  if (pair_smem_slack<kVocabRows, kFilter, kSlots>() != 0) {
     smem_base = (smem_base + 1023) & ~uintptr_t(1023);
   } else if ((smem_u32(smem_raw) & 1023u) != 0u) {
     // (every CTA of the launch sees the same offset, so all of them return here, before any barrier)
@@ -469,9 +474,10 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       mbar_init(&sm.st_full, 1);
       mbar_init(&sm.st_empty, kEpiWarps);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.ds_full[b], 2);
-      mbar_init(&sm.ds_free[b], static_cast<uint32_t>(P));
+    for (int b = 0; b < kSlots; ++b) {
+      // 8 arrivals per content: the owner pair's 8 epilogue warps (4 per CTA), or 4 from each CTA's receiver
+      mbar_init(&sm.ds_full[b], 8);
+      for (int pp = 0; pp < kMaxPairs; ++pp) mbar_init(&sm.ds_free[b][pp], 1);
       mbar_init(&sm.rx_full[b], 1);
     }
     if (filt) {
@@ -609,8 +615,12 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       };
       auto gemm2 = [&](int j, int half) {
         if (!ok || j < 0) return;
-        // the pair that writes block j+1 reuses both dS halves once every pair is done with block j
-        const uint16_t next_owner = static_cast<uint16_t>(3u << (2 * ((j + 1) % P)));
+        // content n = 2j + half of the dS slots sits in slot n mod kSlots; the pair that writes that slot's
+        // next content (n + kSlots) reuses it once every pair is done with this one
+        const int n_ds = 2 * j + half;
+        const int slot = n_ds % kSlots;
+        const int j_next = (n_ds + kSlots) >> 1;
+        const uint16_t next_owner = static_cast<uint16_t>(3u << (2 * (j_next % P)));
         if (filt && j == 0 && half == 0) {
           // with the filter O starts from the epilogue's zeros and every GEMM2 accumulates
           if (!mbar_wait_cluster(&sm.o_zero, 0, abort)) {
@@ -620,7 +630,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         }
         {
           // (also for a skipped half: its slot may be rewritten only after anything sent into it landed)
-          if (!mbar_wait_cluster(&sm.ds_full[half], static_cast<uint32_t>(j) & 1u, abort)) {
+          if (!mbar_wait_cluster(&sm.ds_full[slot], static_cast<uint32_t>(n_ds / kSlots) & 1u, abort)) {
             ok = false;
             return;
           }
@@ -639,7 +649,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
               return;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(sm.ds) + static_cast<uint32_t>(half) * kHalfBytes;
+            const uint32_t a_base = smem_u32(sm.ds[slot]);
             const uint32_t b_base = smem_u32(sm.stage[stage]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -652,7 +662,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
           } else if (p.skip_count != nullptr) {
             atomicAdd(p.skip_count, 1u);
           }
-          if (j + 1 < nt) mma_commit_mc(&sm.ds_free[half], next_owner);
+          if (j_next < nt) mma_commit_mc(&sm.ds_free[slot][pr], next_owner);
         }
       };
       int u = 0;   // owned blocks whose GEMM1 has been issued in full
@@ -708,21 +718,21 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
   } else if (warp == kRecvWarp) {
     // ---------------------------------------- dS halves of blocks computed by the other pairs
     if (lane == 0 && P > 1) {
-      const uint32_t ds_full_c0 = mapa_shared(smem_u32(&sm.ds_full[0]), lead_rank);
-      const uint32_t ds_full_c1 = mapa_shared(smem_u32(&sm.ds_full[1]), lead_rank);
       int v = 0;   // blocks received so far
+      int recv[kSlots] = {};   // contents received into each slot so far
       bool ok = true;
       for (int j = 0; j < nt && ok; ++j) {
         if (j % P == pr) continue;
         for (int half = 0; half < 2; ++half) {
-          mbar_arrive_expect_tx(&sm.rx_full[half], kHalfBytes);
-          if (!mbar_wait_cluster(&sm.rx_full[half], static_cast<uint32_t>(v) & 1u, abort)) {
+          const int slot = (2 * j + half) % kSlots;
+          mbar_arrive_expect_tx(&sm.rx_full[slot], kHalfBytes);
+          if (!mbar_wait_cluster(&sm.rx_full[slot], static_cast<uint32_t>(recv[slot]++) & 1u, abort)) {
             ok = false;
             break;
           }
           // (the half was written by the other pair's stores; order them before the MMAs that read it)
           fence_proxy_async_smem();
-          mbar_arrive_cluster(half ? ds_full_c1 : ds_full_c0);
+          mbar_arrive_cluster_cnt(mapa_shared(smem_u32(&sm.ds_full[slot]), lead_rank), 4);
         }
         ++v;
       }
@@ -735,7 +745,6 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     const int row = r0 + rl;
     const float scale = *p.scale;
     const uint32_t s_empty_c = mapa_shared(smem_u32(&sm.s_empty), lead_rank);
-    const uint32_t ds_full_c = mapa_shared(smem_u32(&sm.ds_full[hh]), lead_rank);
     // dS[m, n] = s [m valid] f_m 2^(S log2 e + b_n log2 e - LSE2_m) - s [n = y_m], with f = 1 + 2 z_loss LSE,
     // evaluated as 2^(S log2 e + c) with c = log2(s f) - LSE2 + b log2 e gathered per row or column.
     // When some valid row has f <= 0 (LSE <= -1/(2 z_loss)) the log form does not apply and every tile
@@ -779,7 +788,9 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     }
     float gbias = 0.f;
     bool ok = true;
-    uint8_t* const ds_row = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(rl) * 128u;
+    // this warp's writes into each of its slots (half hh's contents go to the slots of parity hh) that had
+    // to wait for the slot's previous content to be consumed
+    int waited[kSlots / 2] = {};
     if (filt) {
       // O starts at zero (GEMM2 then always accumulates, whichever halves are skipped): this warp's 32
       // lanes of its 128 of the 256 accumulator columns
@@ -792,14 +803,14 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     }
     int u = 0;
     for (int j = pr; j < nt && ok; j += P, ++u) {
-      if (!mbar_wait(&sm.s_full, u & 1, abort)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full, u & 1, abort))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(qq * 32) << 16) + kTmemS + static_cast<uint32_t>(hh * 128);
       // grad_W pass: the statistics of this half's 128 token columns (staged in the slot, and in global memory)
-      if (kVocabRows && !mbar_wait(&sm.st_full, u & 1, abort)) {
+      if (kVocabRows && !__all_sync(0xffffffffu, mbar_wait(&sm.st_full, u & 1, abort))) {
         ok = false;
         break;
       }
@@ -835,7 +846,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
               for (int pp = 0; pp < P; ++pp)
                 mbar_arrive_cluster(mapa_shared(smem_u32(&sm.mref_ready), static_cast<uint32_t>(2 * pp) + q));
           }
-          if (!mbar_wait_cluster(&sm.mref_ready, 0, abort)) {
+          if (!__all_sync(0xffffffffu, mbar_wait_cluster(&sm.mref_ready, 0, abort))) {
             ok = false;
             break;
           }
@@ -888,20 +899,27 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
           }
         }
       }
-      // every pair must be done with block j-1 in this half slot before it is overwritten here and
-      // in the other pairs' CTAs (phase = blocks this pair wrote after block 0)
-      if (j >= 1 && !mbar_wait_cluster(&sm.ds_free[hh], static_cast<uint32_t>(u - (pr == 0 ? 1 : 0)) & 1u, abort)) {
-        ok = false;
-        break;
+      // content 2j + hh goes to slot (2j + hh) mod kSlots.  Unless it is the slot's first content, each pair
+      // must be done with the slot's previous content before this content overwrites that pair's copy:
+      // ds_free[slot][pp] completes when pair pp is (phase = this warp's earlier writes into the slot that
+      // waited).  A wait that gives up skips the writes but still reaches the named barrier below.
+      const int n_ds = 2 * j + hh;
+      const int slot = n_ds % kSlots;
+      const bool must_wait = n_ds >= kSlots;
+      const uint32_t fpar = must_wait ? static_cast<uint32_t>(waited[slot >> 1]++) & 1u : 0u;
+      const bool own_free = __all_sync(0xffffffffu, !must_wait || mbar_wait_cluster(&sm.ds_free[slot][pr], fpar, abort));
+      ok = ok && own_free;
+      if (own_free) {
+        uint8_t* const ds_row = sm.ds[slot] + static_cast<uint32_t>(rl) * 128u;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(ds_row + ((ch ^ (rl & 7)) << 4)) =
+              make_uint4(pk0[4 * ch + 0], pk0[4 * ch + 1], pk0[4 * ch + 2], pk0[4 * ch + 3]);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(ds_row + kBox + ((ch ^ (rl & 7)) << 4)) =
+              make_uint4(pk1[4 * ch + 0], pk1[4 * ch + 1], pk1[4 * ch + 2], pk1[4 * ch + 3]);
       }
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (rl & 7)) << 4)) =
-            make_uint4(pk0[4 * ch + 0], pk0[4 * ch + 1], pk0[4 * ch + 2], pk0[4 * ch + 3]);
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(ds_row + kBox + ((ch ^ (rl & 7)) << 4)) =
-            make_uint4(pk1[4 * ch + 0], pk1[4 * ch + 1], pk1[4 * ch + 2], pk1[4 * ch + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       // with the filter, a half every pair skips is not sent: the other pairs' receivers get its byte count
@@ -913,11 +931,15 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         // the warp's 32 rows are two contiguous 4 KB runs (one per 64-column box); each lane moves 16-byte
         // pieces of them, so that every store instruction writes 512 consecutive bytes of the peer's slot
         send = __shfl_sync(0xffffffffu, send, 0);
-        const uint8_t* const src = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
-        for (int pp = 0; pp < P; ++pp) {
+        const uint8_t* const src = sm.ds[slot] + static_cast<uint32_t>(qq) * 4096u;
+        for (int pp = 0; pp < P && ok; ++pp) {
           if (pp == pr) continue;
           const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
-          const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[hh]), dst_rank);
+          const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[slot]), dst_rank);
+          if (must_wait && !__all_sync(0xffffffffu, mbar_wait_cluster(&sm.ds_free[slot][pp], fpar, abort))) {
+            ok = false;
+            break;
+          }
           if (send) {
             const uint32_t dst = mapa_shared(smem_u32(src), dst_rank);
 #pragma unroll
@@ -932,11 +954,15 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         }
       } else if (lane == 0) {
         // this warp's 32 rows of both 64-column boxes to the other pairs' CTAs with the same rows
-        uint8_t* const src = sm.ds + static_cast<uint32_t>(hh) * kHalfBytes + static_cast<uint32_t>(qq) * 4096u;
-        for (int pp = 0; pp < P; ++pp) {
+        uint8_t* const src = sm.ds[slot] + static_cast<uint32_t>(qq) * 4096u;
+        for (int pp = 0; pp < P && ok; ++pp) {
           if (pp == pr) continue;
           const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
-          const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[hh]), dst_rank);
+          const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[slot]), dst_rank);
+          if (must_wait && !mbar_wait_cluster(&sm.ds_free[slot][pp], fpar, abort)) {
+            ok = false;
+            break;
+          }
           if (send) {
             bulk_copy_to_peer(mapa_shared(smem_u32(src), dst_rank), src, 4096u, bar);
             bulk_copy_to_peer(mapa_shared(smem_u32(src + kBox), dst_rank), src + kBox, 4096u, bar);
@@ -945,8 +971,13 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
           }
         }
       }
-      named_barrier_sync(1 + hh, 4 * 32);
-      if (qq == 0 && lane == 0) mbar_arrive_cluster(ds_full_c);
+      // (lane 0 alone may have given up in the bulk-copy form: every lane takes the same exit)
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      // this warp's rows of the slot are written here and on their way to the other pairs: one of the 8
+      // arrivals the MMA issuer waits for (no barrier between the epilogue warps, so none can be left
+      // waiting for a warp that gave up)
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.ds_full[slot]), lead_rank));
     }
 
     // online form: every pair's partial sums of this row combined into the row's outputs (online_row_finish),
@@ -956,7 +987,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     if (kOnline) {
       if (ok && !on_have_ref) {
         // a pair that owned no block still needs the reference
-        if (!mbar_wait_cluster(&sm.mref_ready, 0, abort)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&sm.mref_ready, 0, abort))) {
           ok = false;
         } else {
           on_ref = __ldcg(on_mref);
@@ -969,7 +1000,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         if (lane == 0)
           for (int pp = 0; pp < P; ++pp)
             mbar_arrive_cluster(mapa_shared(smem_u32(&sm.part_ready), static_cast<uint32_t>(2 * pp) + q));
-        if (!mbar_wait_cluster(&sm.part_ready, 0, abort)) ok = false;
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&sm.part_ready, 0, abort))) ok = false;
       }
       if (ok) {
         float L = 0.f, zy = -INFINITY, T = 0.f;
@@ -991,7 +1022,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
     }
 
-    if (ok && mbar_wait(&sm.o_full, 0, abort)) {
+    if (ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_full, 0, abort))) {
       tc_fence_after();
       const int n_chunks = (hc + 31) / 32;
       for (int c = hh; c < n_chunks; c += 2) {
@@ -1082,7 +1113,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
   // grad_W pass: every MMA of the cluster has completed by now (each MMA thread waited for its drain, each
   // epilogue for o_full, before the barrier), so the dS blocks are free and gather the grad_bias partials:
   // [pair][half][row] in pair 0's CTA with the same rows, added there in pair and half order
-  float* const gb_gather = reinterpret_cast<float*>(sm.ds);
+  float* const gb_gather = reinterpret_cast<float*>(&sm.ds[0][0]);
   if (kVocabRows) {
     if (warp < kEpiWarps) {
       const int rl = (warp & 3) * 32 + lane;
@@ -1151,20 +1182,22 @@ __device__ __forceinline__ Unit unit_of(const UnitPlan& plan, int c) {
 }
 
 // One gradient pass: cluster blockIdx.x / 2P is work unit unit_of(plan, .).
-template <bool kVocabRows, bool kFilter>
+template <bool kVocabRows, bool kFilter, int kSlots>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
                   const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan) {
   const Unit u = unit_of(plan, static_cast<int>(blockIdx.x) / (2 * p.P));
-  dgrad_pair_body<kVocabRows, kFilter>(tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je, u.su);
+  dgrad_pair_body<kVocabRows, kFilter, false, kSlots>(tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je,
+                                                      u.su);
 }
 
 // The grad_input pass without a prior LSE pass: the same cluster layout as dgrad_pair_kernel<false>.
+template <int kSlots>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_online_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
                     const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan) {
   const Unit u = unit_of(plan, static_cast<int>(blockIdx.x) / (2 * p.P));
-  dgrad_pair_body<false, false, true>(tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je, u.su);
+  dgrad_pair_body<false, false, true, kSlots>(tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je, u.su);
 }
 
 // The vocabulary rows of token-split units of the grad_W pass: grad_W[row] = sum over parts, in order, of
@@ -1304,22 +1337,31 @@ __global__ void __launch_bounds__(128) online_vmerge_kernel(const PairParams p, 
 // Both gradient passes in one grid, so that the grad_W pass's clusters take the SMs the grad_input pass's
 // last wave leaves idle: clusters 0 .. n_in-1 (in the grad_input pass's own order, row pairs fastest) run
 // the grad_input pass, the rest the grad_W pass.  Both passes have the same number of pairs per cluster.
-template <bool kFilter>
+template <bool kFilter, int kSlots>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_both_kernel(const __grid_constant__ CUtensorMap tm_hidden, const __grid_constant__ CUtensorMap tm_w,
                   const PairParams p_in, const PairParams p_w, uint32_t* __restrict__ status, int n_in,
                   int in_row_pairs, int w_row_pairs) {
   const int c = static_cast<int>(blockIdx.x) / (2 * p_in.P);
   if (c < n_in) {
-    dgrad_pair_body<false, kFilter>(tm_hidden, tm_w, p_in, status, c % in_row_pairs, c / in_row_pairs);
+    dgrad_pair_body<false, kFilter, false, kSlots>(tm_hidden, tm_w, p_in, status, c % in_row_pairs, c / in_row_pairs);
   } else {
     const int cw = c - n_in;
-    dgrad_pair_body<true, kFilter>(tm_w, tm_hidden, p_w, status, cw % w_row_pairs, cw / w_row_pairs);
+    dgrad_pair_body<true, kFilter, false, kSlots>(tm_w, tm_hidden, p_w, status, cw % w_row_pairs, cw / w_row_pairs);
   }
 }
 
-// Pairs per cluster: 2 when the number of 256-wide H chunks is even, else 3 when it divides, else 1.
-int pairs_per_cluster(int h_chunks) {
+// Four pairs per cluster (clusters of 8 CTAs, every logits tile computed once per pass when H is a
+// multiple of 1024; four dS half-slots per CTA and three operand stages), for the exact passes whose
+// units run over at least kFourPairsMinBlocks column blocks: the pipeline fill of 2P steps per unit costs
+// too much on shorter units (a grad_W pass over 4096 tokens has 16 blocks per unit).  Measured at
+// BT = 65535, H = 1024, V = 176245: 83.9 ms per step against 91.7 with two pairs.
+constexpr int kFourPairsMinBlocks = 64;
+
+// Pairs per cluster: 4 when allowed (see above) and the number of 256-wide H chunks divides by 4, else 2
+// when it is even, else 3 when it divides by 3, else 1.
+int pairs_per_cluster(int h_chunks, bool four_ok) {
+  if (four_ok && h_chunks % 4 == 0) return 4;
   if (h_chunks % 2 == 0) return 2;
   if (h_chunks % 3 == 0) return 3;
   return 1;
@@ -1367,7 +1409,8 @@ PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
   p.fallback = a.fallback;
   // with only grad_bias requested one H chunk suffices (the GEMM2 result is not stored)
   *h_chunks = (kVocabRows && p.grad_W == nullptr) ? 1 : (p.H + kHc - 1) / kHc;
-  p.P = pairs_per_cluster(*h_chunks);
+  const int n_blocks = (p.n_cols + kPN - 1) / kPN;
+  p.P = pairs_per_cluster(*h_chunks, !(p.filter_eps > 0.f) && n_blocks >= kFourPairsMinBlocks);
   return p;
 }
 
@@ -1464,8 +1507,13 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   int h_chunks = 0;
   PairParams p = make_pair_params<kVocabRows>(a, &h_chunks);
   const bool filt = p.filter_eps > 0.f;
-  const size_t smem = filt ? pair_smem_bytes<kVocabRows, true>() : pair_smem_bytes<kVocabRows, false>();
-  auto kern = filt ? dgrad_pair_kernel<kVocabRows, true> : dgrad_pair_kernel<kVocabRows, false>;
+  const bool four = p.P == 4;   // (exact passes only)
+  const size_t smem = filt   ? pair_smem_bytes<kVocabRows, true>()
+                      : four ? pair_smem_bytes<kVocabRows, false, 4>()
+                             : pair_smem_bytes<kVocabRows, false>();
+  auto kern = filt   ? dgrad_pair_kernel<kVocabRows, true, 2>
+              : four ? dgrad_pair_kernel<kVocabRows, false, 4>
+                     : dgrad_pair_kernel<kVocabRows, false, 2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int rp = row_pairs_of(p);
@@ -1503,13 +1551,14 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   p.vs_stat = a.vs_stat;
   p.vs_o = a.vs_o;
   p.vs_count = a.vs_count;
-  constexpr size_t smem = pair_smem_bytes<false, false>();
-  cudaError_t e =
-      cudaFuncSetAttribute(dgrad_online_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const bool four = p.P == 4;
+  const size_t smem = four ? pair_smem_bytes<false, false, 4>() : pair_smem_bytes<false, false>();
+  auto kern = four ? dgrad_online_kernel<4> : dgrad_online_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int rp = row_pairs_of(p);
   static int slots_of[kMaxPairs + 1] = {};
-  if (slots_of[p.P] == 0) slots_of[p.P] = resident_clusters(dgrad_online_kernel, smem, p.P, stream);
+  if (slots_of[p.P] == 0) slots_of[p.P] = resident_clusters(kern, smem, p.P, stream);
   // vocabulary-split tail: the accumulators go to the split scratch (16 MiB),
   // or to grad_W when it is larger and holds nothing yet (written only by the grad_W pass, after the merge)
   const size_t per_su = sizeof(float) * 256 * p.P * kHc;
@@ -1524,7 +1573,7 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
       make_plan(rp, h_chunks / p.P, (p.n_cols + kPN - 1) / kPN, slots_of[p.P], a.vocab_splits, su_cap, true);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * clusters_of(plan, rp), 1, 1), smem, p.P, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, dgrad_online_kernel, hidden_map, w_map, p, a.status, plan);
+  e = cudaLaunchKernelEx(&cfg, kern, hidden_map, w_map, p, a.status, plan);
   if (e != cudaSuccess) return e;
   if (plan.nsplit > 1) {
     online_vmerge_kernel<<<(rp - plan.rp_tail0) * 256, 128, 0, stream>>>(p, plan);
@@ -1545,9 +1594,11 @@ cudaError_t launch_dgrad_both(const CUtensorMap& hidden_map, const CUtensorMap& 
     return launch_dgrad_pair<true>(w_map, hidden_map, a, stream);
   }
   const bool filt = a.filter_eps > 0.f;
-  const size_t smem = filt ? std::max(pair_smem_bytes<false, true>(), pair_smem_bytes<true, true>())
-                           : std::max(pair_smem_bytes<false, false>(), pair_smem_bytes<true, false>());
-  auto kern = filt ? dgrad_both_kernel<true> : dgrad_both_kernel<false>;
+  const bool four = p_in.P == 4;
+  const size_t smem = filt   ? std::max(pair_smem_bytes<false, true>(), pair_smem_bytes<true, true>())
+                      : four ? std::max(pair_smem_bytes<false, false, 4>(), pair_smem_bytes<true, false, 4>())
+                             : std::max(pair_smem_bytes<false, false>(), pair_smem_bytes<true, false>());
+  auto kern = filt ? dgrad_both_kernel<true, 2> : four ? dgrad_both_kernel<false, 4> : dgrad_both_kernel<false, 2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int in_rp = row_pairs_of(p_in), w_rp = row_pairs_of(p_w);

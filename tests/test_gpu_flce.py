@@ -87,6 +87,12 @@ CASES = {
     # fewer vocabulary blocks than pairs per cluster: pairs that own no block (two and three pairs)
     "one-block-two-pairs": (64, 512, 100, True, 1e-3, "mean", (3,)),
     "one-block-three-pairs": (70, 768, 200, False, 0.0, "sum", ()),
+    # four pairs per cluster (H a multiple of 1024, at least 64 column blocks per unit): in the grad_input
+    # pass (17000 / 256 = 67 vocabulary blocks), with two H groups (H = 2048), and in the grad_W pass
+    # (16400 / 256 = 65 token blocks); the other pass of each case runs with two pairs
+    "four-pairs-grad-input": (700, 1024, 17000, True, 1e-3, "mean", (0, 699)),
+    "four-pairs-two-groups": (300, 2048, 16500, True, 1e-4, "mean", (7,)),
+    "four-pairs-grad-W": (16400, 1024, 2100, False, 0.0, "sum", (5, 16399)),
 }
 
 
@@ -466,11 +472,9 @@ def test_flce_full_size_sampled(flce, key):
     assert out["status"] == 0
     assert int(out["n_valid"].item()) == int(exp["n_valid"]) == w.n_valid
     assert_scalar_close(out["loss"].item(), float(exp["loss"]), "loss")
-    # the automatic split tails ran (their row blocks are the last ones; the sample holds tokens and
-    # vocabulary entries among the last 512)
+    # the grad_input pass's automatic split tail ran (its row blocks are the last ones; the sample holds
+    # tokens and vocabulary entries among the last 512, where the grad_W pass's tail is when it splits)
     assert flce.read_vocab_split_units(out["workspace"]) > 0
-    if key == "long":
-        assert flce.read_token_split_units(out["workspace"]) > 0
     rows = torch.from_numpy(exp["rows"]).cuda()
     vr = torch.from_numpy(exp["vocab_rows"]).cuda()
     check_full_size_rows(exp, bf16_to_numpy_f32(out["grad_input"][rows]), out["grad_W"][vr].cpu().numpy(),
@@ -510,6 +514,4 @@ def test_flce_full_size_split_tails(flce, key):
     if a["grad_bias"] is not None:
         assert_grad_close(a["grad_bias"][v0:].cpu().numpy(), b["grad_bias"][v0:].cpu().numpy().astype(np.float64),
                           "grad_bias (split vocabulary rows)")
-    if key == "long":
-        assert ts > 0, "the grad_W pass did not split its last wave"
 
