@@ -536,10 +536,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ce", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other fused workloads")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload with this BT instead (a smaller case of the same shape; not the headline)")
     ap.add_argument("--filter-eps", type=float, default=2.0 ** -12,
                     help="also time the gradient-filtering variant at this threshold (0: skip)")
     args = ap.parse_args()
     w = wl.FUSED_WORKLOADS[args.workload]
+    if args.tokens:
+        # a smaller case of the same shape (for profiler captures): the first N tokens' worth of the workload
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}, BT reduced to {args.tokens}", BT=args.tokens)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     if args.impl == "reference":
@@ -591,7 +597,8 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": (value / world) / PAGES_TOKENS_PER_S[args.workload] if args.workload in PAGES_TOKENS_PER_S else None,
+        "vs_baseline": (value / world) / PAGES_TOKENS_PER_S[args.workload]
+        if args.workload in PAGES_TOKENS_PER_S and not args.tokens else None,
         "vs_baseline_note": "value per GPU / verl tuned _Split_Dlogits_N on an H100 (356 ms, pages' table); context only",
         "dtype": "bf16", "data": "synthetic (seeded; hidden N(0,1), W N(0,0.02), uniform targets, 10% ignored)",
         "config": config_of(w),

@@ -94,8 +94,8 @@ constexpr uint32_t kTmemO = 256;
 // loop the dS block gathers the grad_bias partials.
 template <bool kVocabRows, bool kFilter, int kSlots = 2>
 struct PairCfg {
-  static_assert(kSlots == 2 || (kSlots == 4 && !kFilter), "dS slots: 2, or 4 for the exact passes");
-  static constexpr int kStages = kSlots == 4 ? 3 : (kVocabRows && kFilter) ? 4 : 5;
+  static_assert(kSlots == 2 || ((kSlots == 3 || kSlots == 4) && !kFilter), "dS slots: 2, or 3-4 for the exact passes");
+  static constexpr int kStages = kSlots == 4 ? 3 : kSlots == 3 ? 4 : (kVocabRows && kFilter) ? 4 : 5;
   static constexpr int kStatCols = kVocabRows ? kPN : 1;
   static constexpr int kRing = kFilter ? kFlagRing : 1;
   using Stat = typename std::conditional<kFilter, float4, float2>::type;
@@ -146,6 +146,8 @@ static_assert(pair_smem_bytes<false, true>() <= kSmemBudget, "shared memory budg
 static_assert(pair_smem_bytes<true, true>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
 static_assert(pair_smem_bytes<false, false, 4>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
 static_assert(pair_smem_bytes<true, false, 4>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
+static_assert(pair_smem_bytes<false, false, 3>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
+static_assert(pair_smem_bytes<true, false, 3>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
 static_assert(sizeof(float) * kMaxPairs * 2 * kTileM <= kDsBytes, "the dS block gathers the grad_bias partials");
 
 // Gradient filter: the verdict on half `half` of block j, once the 8 epilogue warps of its owner pair that
@@ -788,9 +790,9 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     }
     float gbias = 0.f;
     bool ok = true;
-    // this warp's writes into each of its slots (half hh's contents go to the slots of parity hh) that had
-    // to wait for the slot's previous content to be consumed
-    int waited[kSlots / 2] = {};
+    // this CTA's writes into each slot, in content order (both halves: with an odd number of slots a slot
+    // holds contents of either half), that had to wait for the slot's previous content to be consumed
+    int waited[kSlots] = {};
     if (filt) {
       // O starts at zero (GEMM2 then always accumulates, whichever halves are skipped): this warp's 32
       // lanes of its 128 of the 256 accumulator columns
@@ -901,12 +903,15 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
       // content 2j + hh goes to slot (2j + hh) mod kSlots.  Unless it is the slot's first content, each pair
       // must be done with the slot's previous content before this content overwrites that pair's copy:
-      // ds_free[slot][pp] completes when pair pp is (phase = this warp's earlier writes into the slot that
-      // waited).  A wait that gives up skips the writes but still reaches the named barrier below.
+      // ds_free[slot][pp] completes when pair pp is (phase = this CTA's earlier writes into the slot that
+      // waited).  A wait that gives up skips the writes; the warp leaves the loop after the send below.
       const int n_ds = 2 * j + hh;
       const int slot = n_ds % kSlots;
       const bool must_wait = n_ds >= kSlots;
-      const uint32_t fpar = must_wait ? static_cast<uint32_t>(waited[slot >> 1]++) & 1u : 0u;
+      const uint32_t fpar = static_cast<uint32_t>(waited[slot]) & 1u;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2)
+        if (2 * j + h2 >= kSlots) ++waited[(2 * j + h2) % kSlots];
       const bool own_free = __all_sync(0xffffffffu, !must_wait || mbar_wait_cluster(&sm.ds_free[slot][pr], fpar, abort));
       ok = ok && own_free;
       if (own_free) {
@@ -1357,6 +1362,8 @@ dgrad_both_kernel(const __grid_constant__ CUtensorMap tm_hidden, const __grid_co
 // too much on shorter units (a grad_W pass over 4096 tokens has 16 blocks per unit).  Measured at
 // BT = 65535, H = 1024, V = 176245: 83.9 ms per step against 91.7 with two pairs.
 constexpr int kFourPairsMinBlocks = 64;
+// dS half-slots per CTA with four pairs
+constexpr int kFourPairSlots = 4;
 
 // Pairs per cluster: 4 when allowed (see above) and the number of 256-wide H chunks divides by 4, else 2
 // when it is even, else 3 when it divides by 3, else 1.
@@ -1509,10 +1516,10 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   const bool filt = p.filter_eps > 0.f;
   const bool four = p.P == 4;   // (exact passes only)
   const size_t smem = filt   ? pair_smem_bytes<kVocabRows, true>()
-                      : four ? pair_smem_bytes<kVocabRows, false, 4>()
+                      : four ? pair_smem_bytes<kVocabRows, false, kFourPairSlots>()
                              : pair_smem_bytes<kVocabRows, false>();
   auto kern = filt   ? dgrad_pair_kernel<kVocabRows, true, 2>
-              : four ? dgrad_pair_kernel<kVocabRows, false, 4>
+              : four ? dgrad_pair_kernel<kVocabRows, false, kFourPairSlots>
                      : dgrad_pair_kernel<kVocabRows, false, 2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -1552,8 +1559,8 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   p.vs_o = a.vs_o;
   p.vs_count = a.vs_count;
   const bool four = p.P == 4;
-  const size_t smem = four ? pair_smem_bytes<false, false, 4>() : pair_smem_bytes<false, false>();
-  auto kern = four ? dgrad_online_kernel<4> : dgrad_online_kernel<2>;
+  const size_t smem = four ? pair_smem_bytes<false, false, kFourPairSlots>() : pair_smem_bytes<false, false>();
+  auto kern = four ? dgrad_online_kernel<kFourPairSlots> : dgrad_online_kernel<2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int rp = row_pairs_of(p);
@@ -1596,9 +1603,9 @@ cudaError_t launch_dgrad_both(const CUtensorMap& hidden_map, const CUtensorMap& 
   const bool filt = a.filter_eps > 0.f;
   const bool four = p_in.P == 4;
   const size_t smem = filt   ? std::max(pair_smem_bytes<false, true>(), pair_smem_bytes<true, true>())
-                      : four ? std::max(pair_smem_bytes<false, false, 4>(), pair_smem_bytes<true, false, 4>())
+                      : four ? std::max(pair_smem_bytes<false, false, kFourPairSlots>(), pair_smem_bytes<true, false, kFourPairSlots>())
                              : std::max(pair_smem_bytes<false, false>(), pair_smem_bytes<true, false>());
-  auto kern = filt ? dgrad_both_kernel<true, 2> : four ? dgrad_both_kernel<false, 4> : dgrad_both_kernel<false, 2>;
+  auto kern = filt ? dgrad_both_kernel<true, 2> : four ? dgrad_both_kernel<false, kFourPairSlots> : dgrad_both_kernel<false, 2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int in_rp = row_pairs_of(p_in), w_rp = row_pairs_of(p_w);

@@ -12,8 +12,9 @@ asserts that every parity wait is unambiguous (the barrier is never two phases a
 one), that no copy of a slot is overwritten before its pair consumed it, that GEMM2 reads the content it
 expects, and that nothing deadlocks.
 
-The kernel uses S = 2 (two pairs or three per cluster) and S = 4 (four pairs); with S even, each slot
-only ever holds one half's contents, so only one warp group of a CTA writes it.  Two planted protocol
+The kernel uses S = 2 (two pairs or three per cluster) and S = 3 or 4 (four pairs); with S odd a slot
+holds contents of either half in turn, so the writer counts its waits per slot in content order over both
+halves.  Random orders are run as well as orders in which one pair's actors are starved.  Two planted protocol
 mistakes must be caught: a release sent to the next block's owner instead of the slot's next writer,
 and a writer that sends to the other pairs without waiting until each of them is done with the slot.
 """
@@ -47,7 +48,7 @@ def g1_share(s, pr, P):
     return s + lead + d, P - 1 - d
 
 
-def run(P, S, nt, nkb, seed, mistake=None):
+def run(P, S, nt, nkb, seed, mistake=None, slow_pair=None):
     rnd = random.Random(seed)
     B = {}
     for p in range(P):
@@ -145,12 +146,19 @@ def run(P, S, nt, nkb, seed, mistake=None):
                 yield
 
     actors = []
+    slow = set()
     for p in range(P):
         actors.append(mma(p))
+        if p == slow_pair:
+            slow.add(actors[-1])
         for c in range(2):
             actors.append(recv(p, c))
+            if p == slow_pair:
+                slow.add(actors[-1])
             for hh in range(2):
                 actors.append(epi(p, c, hh))
+                if p == slow_pair:
+                    slow.add(actors[-1])
     live = list(actors)
     steps = 0
     while live or inflight:
@@ -164,6 +172,8 @@ def run(P, S, nt, nkb, seed, mistake=None):
         if not live:
             continue
         a = rnd.choice(live)
+        if slow_pair is not None and a in slow and rnd.random() < 0.97:
+            continue   # one pair's actors run rarely: the other pairs get as far ahead as the protocol allows
         try:
             next(a)
         except StopIteration:
@@ -171,12 +181,17 @@ def run(P, S, nt, nkb, seed, mistake=None):
     return steps
 
 
-@pytest.mark.parametrize("S", [2, 4])
+@pytest.mark.parametrize("S", [2, 3, 4])
 @pytest.mark.parametrize("P", [1, 2, 3, 4])
 def test_protocol_holds(P, S):
     for nt in range(1, 14):
         for seed in range(20):
             run(P, S, nt, 16, seed * 1000 + nt)
+    # one pair's actors starved, so that the others run as far ahead as the barriers let them
+    for nt in (16, 30):
+        for seed in range(3):
+            for slow in range(P):
+                run(P, S, nt, 16, seed * 7919 + nt, slow_pair=slow)
 
 
 def test_send_without_waiting_for_the_peer_is_caught():
