@@ -38,8 +38,35 @@ KERNELS_PER_STEP = 5  # lse_partial, lse_merge, loss_reduce, dgrad(grad_input), 
 # online flow: bias table, count, grad_input pass with the LSE, loss reduction, four gated classic kernels
 # (launched, exit at once unless the online pass asked for them), grad_W pass; plus the merge of the
 # vocabulary-split clusters when the grad_input pass splits its last wave (and the same for the grad_W
-# pass's token-split clusters)
+# pass's token-split clusters), and one launch of single-pair side clusters per pass that runs them
 KERNELS_PER_STEP_ONLINE = 9
+
+
+def pairs_per_cluster(h_chunks: int, n_blocks: int) -> int:
+    """CTA pairs per cluster of an exact gradient pass, as the library picks them (four when the 256-wide
+    H chunks divide by 4 and a unit runs over at least 64 column blocks, else two, three or one)."""
+    if h_chunks % 4 == 0 and n_blocks >= 64:
+        return 4
+    return 2 if h_chunks % 2 == 0 else 3 if h_chunks % 3 == 0 else 1
+
+
+def pass_tflops(w, passes, queues):
+    """Algorithmic (logits + one GEMM, 4*BT*V*H) and executed TFLOP/s of the two gradient passes of the
+    default flow.  Executed counts the logits once per cluster that covers a row block: h_chunks / P times
+    per row block (P pairs per cluster), and h_chunks times for the row blocks the side clusters took."""
+    h_chunks = -(-w.H // 256)
+    out = {}
+    for name, rows, cols, q in (("dgrad_grad_input_online", w.BT, w.V, queues[0]),
+                                ("dgrad_grad_W", w.V, w.BT, queues[1])):
+        rp = -(-rows // 256)
+        P = pairs_per_cluster(h_chunks, -(-cols // 256))
+        side_rp = (q >> 32) // h_chunks
+        g1 = ((rp - side_rp) * (h_chunks // P) + side_rp * h_chunks) / rp
+        gemm = 2.0 * w.BT * w.V * w.H
+        sec = passes[name] * 1e-3
+        out[name] = {"algorithmic": 2 * gemm / sec / 1e12, "executed": (g1 + 1) * gemm / sec / 1e12,
+                     "logits_computed_per_row_block": g1, "pairs_per_cluster": P, "side_row_blocks": side_rp}
+    return out
 
 
 def load_peaks():
@@ -209,6 +236,11 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
     # vocabulary-split clusters the grad_input pass ran (its merge kernel is one more launch per step)
     split_units = flce.read_vocab_split_units(ws)
     token_split_units = flce.read_token_split_units(ws)
+    # launches of single-pair clusters beside the persistent four-pair clusters (one per pass that used them)
+    side_launches = flce.read_side_launches(ws)
+    # the two passes' work queues (workspace header bytes 40 and 48: main units | side units << 32), for the
+    # executed GEMM1 work of passes that ran side clusters
+    queues = [int(x) for x in ws[40:56].cpu().view(torch.int64).tolist()]
 
     # the same call captured once into a CUDA graph and replayed (what a training loop that captures its
     # step sees: no per-launch host overhead); same buffers, same inputs
@@ -365,7 +397,8 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
         del ws_sort
     return dict(elapsed_ms=elapsed_ms, passes=passes, clocks=clocks, peak_mem=peak_mem, loss=loss, e2e_ms=e2e_ms,
                 e2e_serial_ms=e2e_serial_ms, h2d=h2d, d2h=d2h, workspace_bytes=ws.numel(), filter=filt,
-                split_units=split_units, token_split_units=token_split_units, graph_ms=graph_ms)
+                split_units=split_units, token_split_units=token_split_units, side_launches=side_launches,
+                queues=queues, graph_ms=graph_ms)
 
 
 def bench_workload(w: wl.FusedWorkload, steps: int, warmup: int, local: int, peaks: dict, oracle_rows: int | None):
@@ -610,13 +643,15 @@ def main():
                           "frac_of_sustained": step_tflops / peak_tf, "frac_of_burst": step_tflops / peaks["bf16_tflops"],
                           "convention": "8*BT*V*H per fused forward+backward"},
         "pass_ms": passes,
+        "pass_tflops": pass_tflops(w, passes, r["queues"]) if online else None,
         "gpu_launches": ((KERNELS_PER_STEP_ONLINE + (1 if r["split_units"] else 0)) if online
                          else KERNELS_PER_STEP - 1 if merged else KERNELS_PER_STEP)
-                        * args.steps + (args.steps if r["token_split_units"] else 0),
+                        * args.steps + (args.steps if r["token_split_units"] else 0) + r["side_launches"] * args.steps,
         "graph_replay": {"ms_per_step": r["graph_ms"], "tokens_per_s": world * w.BT / (r["graph_ms"] * 1e-3),
                          "note": "the same call captured once into a CUDA graph, replayed steps times"},
         "vocab_split_clusters": r["split_units"],
         "token_split_clusters": r["token_split_units"],
+        "side_launches_per_step": r["side_launches"],
         "clocks": r["clocks"],
         "e2e": {"value": world * w.BT / (r["e2e_ms"] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],

@@ -338,6 +338,15 @@ def read_token_split_units(workspace) -> int:
     return int(workspace[32:36].cpu().view(torch.int32).item())
 
 
+def read_side_launches(workspace) -> int:
+    """Launches of single-pair clusters that ran beside the persistent four-pair clusters in the last
+    flce_fwd_bwd on this workspace, one per pass that used them (the 32-bit word at byte 56; synchronises
+    the device)."""
+    import torch
+    torch.cuda.synchronize(workspace.device)
+    return int(workspace[56:60].cpu().view(torch.int32).item())
+
+
 def read_device_status(workspace, stream=None) -> int:
     """Status word of a workspace after the call that used it (synchronises the stream)."""
     v = ctypes.c_uint32(0)

@@ -126,6 +126,7 @@ struct PairSmem {
   uint32_t skipf[Cfg::kRing][2][8];   // filter: [block mod ring][half][4 x owner CTA + warp] 1 = all small
   uint32_t tmem_base;
   int abort;
+  int claim;                  // persistent clusters: the unit CTA 0 claimed for the whole cluster (-1: none)
 };
 constexpr size_t kSmemBudget = 232448;
 // The stage ring and the dS block need 1024-byte alignment (128-byte swizzle atoms).  A layout that fits
@@ -424,30 +425,51 @@ __device__ __forceinline__ OnlineRow online_row_finish(const PairParams& p, int 
   return r;
 }
 
+// The shared-memory layout of this CTA (PairSmem), or null when a layout without slack does not start on
+// the 1024-byte boundary it needs (every CTA of a launch sees the same offset).
+template <bool kVocabRows, bool kFilter, int kSlots>
+__device__ __forceinline__ PairSmem<kVocabRows, kFilter, kSlots>* pair_smem_of() {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uintptr_t base = reinterpret_cast<uintptr_t>(smem_raw);
+  if (pair_smem_slack<kVocabRows, kFilter, kSlots>() != 0) {
+    base = (base + 1023) & ~uintptr_t(1023);
+  } else if ((smem_u32(smem_raw) & 1023u) != 0u) {
+    return nullptr;
+  }
+  return reinterpret_cast<PairSmem<kVocabRows, kFilter, kSlots>*>(base);
+}
+
+// TMEM of a dgrad_pair_body call: allocated and freed by it (one unit per CTA), or held by the caller
+// across the units of a persistent CTA.  (Allocating inside the body keeps the one-unit kernels' register
+// allocation as it was.)
+enum : int { kTmemOneUnit = 0, kTmemHeld = 1 };
+
+// The running sum of owner class k (kClasses = 4 in dgrad_pair_body) after blocks 0 .. nt - 1, given the
+// accumulator a0 of the last block's class and a1..a3 of the classes after it: a_i holds class
+// (nt - 1 + i) mod 4.  A class that owns no block holds 0.
+__device__ __forceinline__ float by_class(float a0, float a1, float a2, float a3, int k, int nt) {
+  const int i = (((k - (nt - 1)) % 4) + 4) % 4;
+  return i == 0 ? a0 : i == 1 ? a1 : i == 2 ? a2 : a3;
+}
+
 // kFilter: the gradient-filtering variant (a separate instantiation, so the exact path carries none of
 // its checks).
 // One cluster's work: rows [256 row_pair, +256) (128 per CTA of each pair) and the H chunks of
 // group hgroup (P consecutive 256-wide chunks, one per pair).
 // Columns: blocks [jb, je) of 256 (all of them except for a vocabulary-split unit of the online pass, su >= 0).
-template <bool kVocabRows, bool kFilter, bool kOnline = false, int kSlots = 2>
+// kClasses = 4: a single pair (P = 1) standing in for a cluster of four pairs, whose results it reproduces
+// bit for bit: the per-row sums that four pairs would keep apart (each over the blocks it owns, j mod 4)
+// are kept apart too and combined in the same order (the online pass's softmax sums, grad_bias).
+template <bool kVocabRows, bool kFilter, bool kOnline = false, int kSlots = 2, int kClasses = 1, int kTmem = 0>
 __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols,
                                                 const PairParams& p, uint32_t* __restrict__ status, int row_pair,
                                                 int hgroup, int jb = 0, int je = -1, int su = -1) {
   static_assert(!kOnline || (!kVocabRows && !kFilter), "the online form is a grad_input pass without the filter");
+  static_assert(kClasses == 1 || (kClasses == kMaxPairs && !kFilter), "owner classes: 1, or 4 for the exact passes");
   using Smem = PairSmem<kVocabRows, kFilter, kSlots>;
   constexpr int kStages = Smem::Cfg::kStages;
-  // the classic passes behind an online grad_input pass run only when it asked for them
-  if (p.gate != nullptr && *reinterpret_cast<const volatile uint32_t*>(p.gate) == 0u) return;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uintptr_t smem_base = reinterpret_cast<uintptr_t>(smem_raw);
-  if (pair_smem_slack<kVocabRows, kFilter, kSlots>() != 0) {
-    smem_base = (smem_base + 1023) & ~uintptr_t(1023);
-  } else if ((smem_u32(smem_raw) & 1023u) != 0u) {
-    // (every CTA of the launch sees the same offset, so all of them return here, before any barrier)
-    if (threadIdx.x == 0) atomicOr(status, kStatusInternal);
-    return;
-  }
-  Smem& sm = *reinterpret_cast<Smem*>(smem_base);
+  // (run_units has checked the gate and the layout's alignment and allocated TMEM)
+  Smem& sm = *pair_smem_of<kVocabRows, kFilter, kSlots>();
   const uint32_t rank = cluster_ctarank();
   const int P = p.P;
   const int pr = static_cast<int>(rank >> 1);       // pair index within the cluster
@@ -499,7 +521,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     sm.abort = 0;
     fence_mbarrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (kTmem != kTmemHeld && warp == kMmaWarp) {
     tmem_alloc_pair(&sm.tmem_base, kTmemCols);
     tmem_relinquish_pair();
   }
@@ -512,7 +534,9 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
-  float gbias_out = 0.f;   // grad_W pass: this epilogue thread's grad_bias partial (its row, its half)
+  // grad_W pass: this epilogue thread's grad_bias partial (its row, its half); with kClasses = 4, one per
+  // owner class
+  float gbias_out = 0.f, gbias_c1 = 0.f, gbias_c2 = 0.f, gbias_c3 = 0.f;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------------------ TMA producer
@@ -593,6 +617,14 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         load_stats();
         if (kStepOrder == 0) load_gemm1(kb0, kb1);
         if (kStepOrder == 2) load_gemm1(kbm, kb1);
+      }
+      if (ok) {
+        // every stage's last release (an MMA commit, multicast to both CTAs of the pair) has arrived
+        // before the unit ends, so that a persistent cluster can initialise the barriers for its next unit
+        for (int s = 0; s < kStages && ok; ++s) {
+          ok = mbar_wait(&sm.empty[stage], phase ^ 1u, abort);
+          next();
+        }
       }
       if (!ok) {
         // let copies already issued land before the CTA can finish
@@ -789,6 +821,10 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       rc.y = row;
     }
     float gbias = 0.f;
+    // kClasses = 4: the running sums of the three owner classes other than the current block's; before
+    // block j, on_lsum / on_tsum / gbias hold class j mod 4 and the k-th of these class (j + k) mod 4
+    float cl_l1 = 0.f, cl_l2 = 0.f, cl_l3 = 0.f, cl_t1 = 0.f, cl_t2 = 0.f, cl_t3 = 0.f;
+    float cl_g1 = 0.f, cl_g2 = 0.f, cl_g3 = 0.f;
     bool ok = true;
     // this CTA's writes into each slot, in content order (both halves: with an odd number of slots a slot
     // holds contents of either half), that had to wait for the slot's previous content to be consumed
@@ -805,6 +841,14 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     }
     int u = 0;
     for (int j = pr; j < nt && ok; j += P, ++u) {
+      if (kClasses > 1 && j > 0) {
+        float t = on_lsum;
+        on_lsum = cl_l1, cl_l1 = cl_l2, cl_l2 = cl_l3, cl_l3 = t;
+        t = on_tsum;
+        on_tsum = cl_t1, cl_t1 = cl_t2, cl_t2 = cl_t3, cl_t3 = t;
+        t = gbias;
+        gbias = cl_g1, cl_g1 = cl_g2, cl_g2 = cl_g3, cl_g3 = t;
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full, u & 1, abort))) {
         ok = false;
         break;
@@ -1000,7 +1044,14 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         }
       }
       if (ok) {
-        on_part[pr * 2 + hh] = make_float4(on_lsum, on_zy, on_tsum, 0.f);
+        if (kClasses > 1) {
+          // (the target logit is a maximum: every class may carry it)
+          for (int k = 0; k < kClasses; ++k)
+            on_part[k * 2 + hh] = make_float4(by_class(on_lsum, cl_l1, cl_l2, cl_l3, k, nt), on_zy,
+                                              by_class(on_tsum, cl_t1, cl_t2, cl_t3, k, nt), 0.f);
+        } else {
+          on_part[pr * 2 + hh] = make_float4(on_lsum, on_zy, on_tsum, 0.f);
+        }
         __syncwarp();
         if (lane == 0)
           for (int pp = 0; pp < P; ++pp)
@@ -1009,7 +1060,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
       if (ok) {
         float L = 0.f, zy = -INFINITY, T = 0.f;
-        for (int pp = 0; pp < P; ++pp)
+        for (int pp = 0; pp < (kClasses > 1 ? kClasses : P); ++pp)
           for (int h2 = 0; h2 < 2; ++h2) {
             const float4 v = __ldcg(on_part + pp * 2 + h2);
             L += v.x;
@@ -1110,7 +1161,12 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         }
       }
     }
-    gbias_out = gbias;
+    gbias_out = kClasses > 1 ? by_class(gbias, cl_g1, cl_g2, cl_g3, 0, nt) : gbias;
+    if (kClasses > 1) {
+      gbias_c1 = by_class(gbias, cl_g1, cl_g2, cl_g3, 1, nt);
+      gbias_c2 = by_class(gbias, cl_g1, cl_g2, cl_g3, 2, nt);
+      gbias_c3 = by_class(gbias, cl_g1, cl_g2, cl_g3, 3, nt);
+    }
   }
 
   tc_fence_before();
@@ -1123,6 +1179,12 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     if (warp < kEpiWarps) {
       const int rl = (warp & 3) * 32 + lane;
       st_shared_cluster_f32(mapa_shared(smem_u32(gb_gather + (pr * 2 + (warp >> 2)) * kTileM + rl), q), gbias_out);
+      if (kClasses > 1) {
+        // (P = 1: the gather area is this CTA's own)
+        gb_gather[(2 + (warp >> 2)) * kTileM + rl] = gbias_c1;
+        gb_gather[(4 + (warp >> 2)) * kTileM + rl] = gbias_c2;
+        gb_gather[(6 + (warp >> 2)) * kTileM + rl] = gbias_c3;
+      }
     }
     cluster_sync();
   }
@@ -1131,7 +1193,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     const int row = r0 + rl;
     if (row < p.V) {
       float acc = 0.f;
-      for (int pp = 0; pp < P; ++pp) acc += gb_gather[(pp * 2) * kTileM + rl] + gb_gather[(pp * 2 + 1) * kTileM + rl];
+      for (int pp = 0; pp < (kClasses > 1 ? kClasses : P); ++pp)
+        acc += gb_gather[(pp * 2) * kTileM + rl] + gb_gather[(pp * 2 + 1) * kTileM + rl];
       if (su >= 0) {
         p.vs_gb[static_cast<size_t>(su) * 256 + static_cast<int>(q) * kTileM + rl] = acc;   // for dw_vmerge_kernel
       } else {
@@ -1140,7 +1203,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
     }
   }
-  if (warp == kMmaWarp) {
+  if (kTmem == kTmemOneUnit && warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, kTmemCols);
   }
@@ -1186,23 +1249,132 @@ __device__ __forceinline__ Unit unit_of(const UnitPlan& plan, int c) {
   return u;
 }
 
-// One gradient pass: cluster blockIdx.x / 2P is work unit unit_of(plan, .).
-template <bool kVocabRows, bool kFilter, int kSlots>
+// Work queue of a pass run by persistent clusters (word != null): the main launch's clusters of four
+// pairs take whole units (row pair x H group) from the bottom of the row pairs; a second launch of
+// single-pair clusters (the side launch, on the SMs the main launch leaves idle) takes units of one row
+// pair and one 256-wide H chunk from the top, computing that row pair's logits once per chunk.  One 64-bit
+// word holds both counts (main units claimed | side units claimed << 32), so that a row pair is never
+// split between the two.  The side opens a new row pair only while the main launch has at least `reserve`
+// row pairs left: enough to keep it busy while the side finishes that row pair.
+enum : int { kRoleMain = 1, kRoleSide = 2 };
+struct WorkQueue {
+  unsigned long long* word;   // zeroed before the pass; null: one cluster per unit (blockIdx), no queue
+  uint32_t* side_count;       // side launches that ran (workspace header), or null
+  int role;
+  int row_pairs;
+  int main_groups;            // H groups per row pair of a main unit (h_chunks / 4)
+  int side_groups;            // H chunks per row pair (one per side unit)
+  int reserve;
+};
+
+// The next unit for this launch's role, -1 when there is none left for it, -2 when the compare-and-swap
+// did not settle (the caller flags the status; with a few dozen clusters claiming every few hundred
+// microseconds it always settles at once).
+__device__ __forceinline__ int claim_unit(const WorkQueue& q) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(q.word);
+  for (int tries = 0; tries < (1 << 16); ++tries) {
+    const int a = static_cast<int>(cur & 0xffffffffull);
+    const int b = static_cast<int>(cur >> 32);
+    const int a_rows = (a + q.main_groups - 1) / q.main_groups;   // row pairs the main launch has begun
+    const int b_rows = (b + q.side_groups - 1) / q.side_groups;   // row pairs the side launch has begun
+    unsigned long long next;
+    if (q.role == kRoleMain) {
+      if (a / q.main_groups >= q.row_pairs - b_rows) return -1;
+      next = cur + 1ull;
+    } else {
+      // (a row pair already begun is always finished; a new one only with `reserve` row pairs to spare)
+      if (b % q.side_groups == 0 && (q.row_pairs - 1 - b / q.side_groups) - a_rows < q.reserve) return -1;
+      next = cur + (1ull << 32);
+    }
+    const unsigned long long seen = atomicCAS(q.word, cur, next);
+    if (seen == cur) return q.role == kRoleMain ? a : b;
+    cur = seen;
+  }
+  return -2;
+}
+
+// A CTA's gradient work: TMEM allocated once, then the one unit `fixed` (kQueue false), or (kQueue) the
+// units it claims from the work queue, CTA 0 of the cluster claiming and handing the index to every CTA,
+// until none is left.  The barriers are initialised again for every unit: dgrad_pair_body ends with
+// every arrival on them consumed or ordered before its last cluster barrier.  A unit that gave up on a
+// wait stops the cluster.  (A template flag rather than a run-time one, so that the one-unit kernels keep
+// their register allocation.)
+template <bool kVocabRows, bool kFilter, bool kOnline, int kSlots, int kClasses, bool kQueue>
+__device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols, const PairParams& p,
+                                          uint32_t* __restrict__ status, const Unit& fixed, const UnitPlan& plan,
+                                          const WorkQueue& wq) {
+  // the classic passes behind an online grad_input pass run only when it asked for them
+  if (p.gate != nullptr && *reinterpret_cast<const volatile uint32_t*>(p.gate) == 0u) return;
+  auto* const smp = pair_smem_of<kVocabRows, kFilter, kSlots>();
+  if (smp == nullptr) {
+    if (threadIdx.x == 0) atomicOr(status, kStatusInternal);
+    return;
+  }
+  if constexpr (!kQueue) {
+    // (the body allocates and frees TMEM itself)
+    dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kClasses, kTmemOneUnit>(
+        tm_rows, tm_cols, p, status, fixed.row_pair, fixed.hgroup, fixed.jb, fixed.je, fixed.su);
+  } else {
+    auto& sm = *smp;
+    if ((threadIdx.x >> 5) == kMmaWarp) {
+      tmem_alloc_pair(&sm.tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    }
+    if (wq.role == kRoleMain) {
+      griddep_launch_dependents();   // the side launch may start on the SMs this one leaves free
+    } else if (blockIdx.x == 0 && threadIdx.x == 0 && wq.side_count != nullptr) {
+      atomicAdd(wq.side_count, 1u);
+    }
+    const uint32_t rank = cluster_ctarank();
+    for (;;) {
+      if (rank == 0 && threadIdx.x == 0) {
+        int c = (*reinterpret_cast<volatile uint32_t*>(status) & kStatusTimeout) != 0u ? -1 : claim_unit(wq);
+        if (c == -2) {
+          atomicOr(status, kStatusInternal);
+          c = -1;
+        }
+        for (int r = 0; r < 2 * p.P; ++r)
+          st_shared_cluster_u32(mapa_shared(smem_u32(&sm.claim), static_cast<uint32_t>(r)), static_cast<uint32_t>(c));
+      }
+      cluster_sync();
+      const int c = *reinterpret_cast<volatile int*>(&sm.claim);
+      if (c < 0) break;
+      const Unit u = wq.role == kRoleMain
+                         ? Unit{c / wq.main_groups, c % wq.main_groups, 0, plan.nt, -1}
+                         : Unit{wq.row_pairs - 1 - c / wq.side_groups, c % wq.side_groups, 0, plan.nt, -1};
+      dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kClasses, kTmemHeld>(tm_rows, tm_cols, p, status, u.row_pair,
+                                                                                 u.hgroup, u.jb, u.je, u.su);
+      // every CTA is done with the unit (and has read sm.claim) before the next claim is handed out
+      cluster_sync();
+    }
+    // a side grid completes only after the main grid beside it, so that what follows on the stream sees both
+    if (wq.role == kRoleSide) griddep_wait_primary();
+    // (every CTA of the cluster has passed a cluster barrier after its last TMEM access)
+    if ((threadIdx.x >> 5) == kMmaWarp) {
+      tc_fence_after();
+      tmem_dealloc_pair(sm.tmem_base, kTmemCols);
+    }
+  }
+}
+
+// One gradient pass: without a queue, cluster blockIdx.x / 2P is work unit unit_of(plan, .); with one
+// (kQueue), a persistent cluster of the main or side launch (WorkQueue; the side launch's single pairs with
+// kClasses = 4).
+template <bool kVocabRows, bool kFilter, int kSlots, int kClasses = 1, bool kQueue = false>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
-                  const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan) {
+                  const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan, const WorkQueue wq) {
   const Unit u = unit_of(plan, static_cast<int>(blockIdx.x) / (2 * p.P));
-  dgrad_pair_body<kVocabRows, kFilter, false, kSlots>(tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je,
-                                                      u.su);
+  run_units<kVocabRows, kFilter, false, kSlots, kClasses, kQueue>(tm_rows, tm_cols, p, status, u, plan, wq);
 }
 
 // The grad_input pass without a prior LSE pass: the same cluster layout as dgrad_pair_kernel<false>.
-template <int kSlots>
+template <int kSlots, int kClasses = 1, bool kQueue = false>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_online_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
-                    const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan) {
+                    const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan, const WorkQueue wq) {
   const Unit u = unit_of(plan, static_cast<int>(blockIdx.x) / (2 * p.P));
-  dgrad_pair_body<false, false, true, kSlots>(tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je, u.su);
+  run_units<false, false, true, kSlots, kClasses, kQueue>(tm_rows, tm_cols, p, status, u, plan, wq);
 }
 
 // The vocabulary rows of token-split units of the grad_W pass: grad_W[row] = sum over parts, in order, of
@@ -1348,11 +1520,15 @@ dgrad_both_kernel(const __grid_constant__ CUtensorMap tm_hidden, const __grid_co
                   const PairParams p_in, const PairParams p_w, uint32_t* __restrict__ status, int n_in,
                   int in_row_pairs, int w_row_pairs) {
   const int c = static_cast<int>(blockIdx.x) / (2 * p_in.P);
+  const UnitPlan none{};
+  const WorkQueue no_queue{};
   if (c < n_in) {
-    dgrad_pair_body<false, kFilter, false, kSlots>(tm_hidden, tm_w, p_in, status, c % in_row_pairs, c / in_row_pairs);
+    const Unit u{c % in_row_pairs, c / in_row_pairs, 0, -1, -1};
+    run_units<false, kFilter, false, kSlots, 1, false>(tm_hidden, tm_w, p_in, status, u, none, no_queue);
   } else {
     const int cw = c - n_in;
-    dgrad_pair_body<true, kFilter, false, kSlots>(tm_w, tm_hidden, p_w, status, cw % w_row_pairs, cw / w_row_pairs);
+    const Unit u{cw % w_row_pairs, cw / w_row_pairs, 0, -1, -1};
+    run_units<true, kFilter, false, kSlots, 1, false>(tm_w, tm_hidden, p_w, status, u, none, no_queue);
   }
 }
 
@@ -1506,6 +1682,65 @@ int clusters_of(const UnitPlan& plan, int row_pairs) {
   return plan.n_whole + (row_pairs - plan.rp_tail0) * plan.groups * plan.nsplit;
 }
 
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// A pass with four pairs per cluster, run as persistent clusters of four pairs (one per resident slot)
+// plus, on the SMs those leave idle (8-CTA clusters do not tile every GPC), persistent single-pair clusters
+// sharing its work queue (WorkQueue).  The side launch follows the main one with programmatic stream
+// serialisation: it starts once every main CTA is running, and completes after the main launch.  Taken
+// when the pass has a queue word, the resident count is known and there are at least kCoRunMinWaves waves
+// of main units; otherwise nothing is launched (*launched = false).
+constexpr int kCoRunMinWaves = 3;
+
+template <class MainKernel, class SideKernel>
+cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, size_t smem_side, int res_main,
+                         const CUtensorMap& rows, const CUtensorMap& cols, const PairParams& p, int h_chunks,
+                         int splits_option, const DgPairArgs& a, cudaStream_t stream, bool* launched) {
+  *launched = false;
+  const int rp = row_pairs_of(p);
+  const int main_groups = h_chunks / 4;
+  // (automatic scheduling only: splits_option 1 asks for one cluster per unit, k >= 2 for split units)
+  if (a.work_q == nullptr || splits_option != 0 || p.P != 4 || res_main <= 0 || main_groups < 1 ||
+      rp * main_groups < kCoRunMinWaves * res_main)
+    return cudaSuccess;
+  const int side = (device_sm_count() - 8 * res_main) / 2;
+  if (side < 2) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_main));
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_side))) !=
+      cudaSuccess)
+    return e;
+  const UnitPlan plan = make_plan(rp, main_groups, (p.n_cols + kPN - 1) / kPN, 0, 1, 0, false);
+  // A side unit (one pair: the row pair's logits and one chunk's GEMM2) takes 4 (H + 256) / (H + 1024) times
+  // as long as a main unit (four pairs: the logits once and four chunks' GEMM2) at equal rates per pair; the
+  // side begins a row pair only while the main launch has that many units per main cluster left.
+  const long long num = 4ll * (p.H + kHc) * res_main;
+  const long long den = static_cast<long long>(p.H + 4 * kHc) * main_groups;
+  WorkQueue wq{a.work_q, a.side_count, kRoleMain, rp, main_groups, h_chunks, static_cast<int>((num + den - 1) / den)};
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cm =
+      cluster_config(dim3(8 * std::min(res_main, rp * main_groups), 1, 1), smem_main, 4, stream, attr);
+  if ((e = cudaLaunchKernelEx(&cm, km, rows, cols, p, a.status, plan, wq)) != cudaSuccess) return e;
+  PairParams ps = p;
+  ps.P = 1;
+  WorkQueue wside = wq;
+  wside.role = kRoleSide;
+  cudaLaunchConfig_t cs = cluster_config(dim3(2 * side, 1, 1), smem_side, 1, stream, attr);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cs.numAttrs = 2;
+  if ((e = cudaLaunchKernelEx(&cs, ks, rows, cols, ps, a.status, plan, wside)) != cudaSuccess) return e;
+  *launched = true;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 template <bool kVocabRows>
@@ -1525,6 +1760,15 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   if (e != cudaSuccess) return e;
   const int rp = row_pairs_of(p);
   const int nt = (p.n_cols + kPN - 1) / kPN;
+  if (four && !filt) {
+    static int res4 = 0;
+    if (res4 == 0) res4 = resident_clusters(kern, smem, 4, stream);
+    bool launched = false;
+    e = launch_corun(dgrad_pair_kernel<kVocabRows, false, kFourPairSlots, 1, true>, smem,
+                     dgrad_pair_kernel<kVocabRows, false, 2, kMaxPairs, true>, pair_smem_bytes<kVocabRows, false>(), res4,
+                     rows, cols, p, h_chunks, kVocabRows ? a.token_splits : 0, a, stream, &launched);
+    if (e != cudaSuccess || launched) return e;
+  }
   UnitPlan plan = make_plan(rp, h_chunks / p.P, nt, 0, 1, 0, false);
   if (kVocabRows && a.split_scratch != nullptr) {
     // token-split tail of the grad_W pass: partial rows in the caller's scratch
@@ -1540,7 +1784,7 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * clusters_of(plan, rp), 1, 1), smem, p.P, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, kern, rows, cols, p, a.status, plan);
+  e = cudaLaunchKernelEx(&cfg, kern, rows, cols, p, a.status, plan, WorkQueue{});
   if (e != cudaSuccess) return e;
   if (kVocabRows && plan.nsplit > 1) {
     dw_vmerge_kernel<<<(rp - plan.rp_tail0) * 256, 128, 0, stream>>>(p, plan);
@@ -1566,6 +1810,13 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   const int rp = row_pairs_of(p);
   static int slots_of[kMaxPairs + 1] = {};
   if (slots_of[p.P] == 0) slots_of[p.P] = resident_clusters(kern, smem, p.P, stream);
+  if (four) {
+    bool launched = false;
+    e = launch_corun(dgrad_online_kernel<kFourPairSlots, 1, true>, smem, dgrad_online_kernel<2, kMaxPairs, true>,
+                     pair_smem_bytes<false, false>(), slots_of[4], hidden_map, w_map, p, h_chunks, a.vocab_splits, a,
+                     stream, &launched);
+    if (e != cudaSuccess || launched) return e;
+  }
   // vocabulary-split tail: the accumulators go to the split scratch (16 MiB),
   // or to grad_W when it is larger and holds nothing yet (written only by the grad_W pass, after the merge)
   const size_t per_su = sizeof(float) * 256 * p.P * kHc;
@@ -1580,7 +1831,7 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
       make_plan(rp, h_chunks / p.P, (p.n_cols + kPN - 1) / kPN, slots_of[p.P], a.vocab_splits, su_cap, true);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(dim3(2 * p.P * clusters_of(plan, rp), 1, 1), smem, p.P, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, kern, hidden_map, w_map, p, a.status, plan);
+  e = cudaLaunchKernelEx(&cfg, kern, hidden_map, w_map, p, a.status, plan, WorkQueue{});
   if (e != cudaSuccess) return e;
   if (plan.nsplit > 1) {
     online_vmerge_kernel<<<(rp - plan.rp_tail0) * 256, 128, 0, stream>>>(p, plan);
@@ -1595,8 +1846,10 @@ cudaError_t launch_dgrad_both(const CUtensorMap& hidden_map, const CUtensorMap& 
   const PairParams p_in = make_pair_params<false>(a, &hc_in);
   const PairParams p_w = make_pair_params<true>(a, &hc_w);
   if (p_in.P != p_w.P) {
-    // different cluster shapes: two launches
-    cudaError_t e = launch_dgrad_pair<false>(hidden_map, w_map, a, stream);
+    // different cluster shapes: two launches (the queue word, if any, is the grad_W pass's)
+    DgPairArgs ai = a;
+    ai.work_q = nullptr;
+    cudaError_t e = launch_dgrad_pair<false>(hidden_map, w_map, ai, stream);
     if (e != cudaSuccess) return e;
     return launch_dgrad_pair<true>(w_map, hidden_map, a, stream);
   }

@@ -467,6 +467,8 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   w.fallback = reinterpret_cast<uint32_t*>(p + 24);
   w.vs_count = reinterpret_cast<uint32_t*>(p + 28);
   w.ts_count = reinterpret_cast<uint32_t*>(p + 32);
+  w.work_q = reinterpret_cast<unsigned long long*>(p + 40);
+  w.side_count = reinterpret_cast<uint32_t*>(p + 56);
   size_t off = 256;
   w.part = reinterpret_cast<float2*>(p + off);
   w.part_bytes = align_up(sizeof(float2) * kMaxSplits * btp, 256);

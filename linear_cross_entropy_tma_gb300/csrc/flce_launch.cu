@@ -73,6 +73,8 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
   pa.split_scratch = reinterpret_cast<float*>(ws.part);
   pa.split_scratch_bytes = ws.part_bytes;
   pa.split_count = ws.ts_count;
+  pa.work_q = ws.work_q + 1;     // (the grad_W pass; the gated classic grad_input pass takes none)
+  pa.side_count = ws.side_count;
   if (online) {
     // events: 1 after the bias table and count, 2 after the online grad_input pass, 3 after the loss
     // reduction and the gated classic passes, 4 after the grad_W pass
@@ -102,6 +104,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     po.vs_stat = ws.vs_stat;
     po.vs_o = ws.split_acc;
     po.vs_count = ws.vs_count;
+    po.work_q = ws.work_q;
     if ((e = launch_dgrad_online(tm_h, tm_w, po, stream)) != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
     if ((e = launch_loss_reduce(a, ws, stream)) != cudaSuccess) return e;
@@ -109,6 +112,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     if ((e = launch_lse_passes(a, ws, num_sms, stream, err, err_len, nullptr, ws.fallback)) != cudaSuccess) return e;
     DgPairArgs pg = pa;
     pg.gate = ws.fallback;
+    pg.work_q = nullptr;
     pg.row_redo = ws.row_redo;   // only the rows the online pass left
     if ((e = launch_dgrad_pair<false>(tm_h, tm_w, pg, stream)) != cudaSuccess) return e;
     if ((e = mark(3)) != cudaSuccess) return e;
@@ -141,7 +145,9 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     return mark(4);
   }
   if (a.grad_input != nullptr) {
-    if ((e = launch_dgrad_pair<false>(tm_h128, tm_w128, pa, stream)) != cudaSuccess) return e;
+    DgPairArgs pi = pa;
+    pi.work_q = ws.work_q;   // each pass has its own queue word
+    if ((e = launch_dgrad_pair<false>(tm_h128, tm_w128, pi, stream)) != cudaSuccess) return e;
   }
   if ((e = mark(3)) != cudaSuccess) return e;
   if (want_dw) {

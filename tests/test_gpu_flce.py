@@ -217,6 +217,58 @@ def test_flce_vocab_split_options(flce):
     assert_grad_close(out["grad_bias"].cpu().numpy(), ref["grad_bias"] + gb0, "grad_bias (accumulated)")
 
 
+# Both passes with four pairs per cluster and at least three waves of row pairs (65 token and 66 vocabulary
+# row pairs against 15 resident 8-CTA clusters): persistent four-pair clusters plus single-pair clusters
+# on the SMs they leave idle, which take the last row pairs one 256-wide H chunk at a time.
+PERSISTENT_SHAPE = (16400, 1024, 16700)
+
+
+def test_flce_persistent_with_side_clusters(flce):
+    """Element by element against the oracle; the side launches counted; and bit for bit the same as one
+    cluster per unit (the single pairs keep the four pairs' partial sums apart and add them in order)."""
+    import torch
+    BT, H, V = PERSISTENT_SHAPE
+    d = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(0, BT - 1), seed=41)
+    out = _run(flce, d)
+    assert out["status"] == 0
+    assert flce.read_side_launches(out["workspace"]) == 2
+    assert flce.read_vocab_split_units(out["workspace"]) == 0
+    assert flce.read_token_split_units(out["workspace"]) == 0
+    _check_full(out, d)
+    plain = _run(flce, d, vocab_splits=1, token_splits=1)
+    assert plain["status"] == 0
+    assert flce.read_side_launches(plain["workspace"]) == 0
+    for k in ("grad_input", "grad_W", "grad_bias"):
+        assert torch.equal(out[k], plain[k]), f"{k} differs from one cluster per unit"
+    assert out["loss"].item() == plain["loss"].item()
+
+
+def test_flce_persistent_side_clusters_options(flce):
+    # per-token upstream gradients and losses, entropy (the owner-class sums of the single pairs) and
+    # accumulation, with the side clusters
+    import torch
+    BT, H, V = PERSISTENT_SHAPE
+    d = _synthetic(BT, H, V, True, 1e-3, "none", ignore=(11,), seed=43)
+    rng = np.random.Generator(np.random.PCG64(17))
+    gtok = rng.standard_normal(BT).astype(np.float32)
+    ref = oracle.flce_reference(d["hidden"], d["W"], d["target"], bias=d["bias"], reduction="none", z_loss=1e-3,
+                                grad_loss_per_token=gtok)
+    gi0 = wl.f32_to_bf16_bits((rng.standard_normal((BT, H)) * np.std(ref["grad_input"])).astype(np.float32))
+    gw0 = (rng.standard_normal((V, H)) * np.std(ref["grad_W"])).astype(np.float32)
+    gb0 = (rng.standard_normal(V) * np.std(ref["grad_bias"])).astype(np.float32)
+    acc = {"grad_input": bf16_tensor(gi0), "grad_W": torch.from_numpy(gw0.copy()).cuda(),
+           "grad_bias": torch.from_numpy(gb0.copy()).cuda()}
+    out = _run(flce, d, grad_loss_per_token=torch.from_numpy(gtok).cuda(), want_entropy=True, accumulate=True, out=acc)
+    assert out["status"] == 0
+    assert flce.read_side_launches(out["workspace"]) == 2
+    assert_grad_close(out["loss_per_token"].cpu().numpy(), ref["loss_per_token"], "loss_per_token")
+    assert_grad_close(out["entropy"].cpu().numpy(), ref["entropy"], "entropy")
+    assert_grad_close(bf16_to_numpy_f32(out["grad_input"]),
+                      ref["grad_input"] + (gi0.astype(np.uint32) << 16).view(np.float32), "grad_input (accumulated)")
+    assert_grad_close(out["grad_W"].cpu().numpy(), ref["grad_W"] + gw0, "grad_W (accumulated)")
+    assert_grad_close(out["grad_bias"].cpu().numpy(), ref["grad_bias"] + gb0, "grad_bias (accumulated)")
+
+
 def test_flce_tiny_workload(flce):
     d = wl.make_fused_inputs(wl.TINY)
     out = _run(flce, d)
@@ -357,7 +409,7 @@ def test_flce_online_fallback_vocab_split(flce):
     _check_full(out, d)
 
 
-@pytest.mark.parametrize("shape", [(600, 1024, 9000), (128, 64, 512)])
+@pytest.mark.parametrize("shape", [(600, 1024, 9000), (128, 64, 512), (16400, 1024, 16700)])
 def test_flce_cuda_graph_replay(flce, shape):
     # the call captures into a CUDA graph (no host synchronisation, no allocation inside): a replay gives
     # the eager call's results bit for bit, and replays on new inputs in the same buffers match the oracle
@@ -382,6 +434,9 @@ def test_flce_cuda_graph_replay(flce, shape):
     g.replay()
     torch.cuda.synchronize()
     assert flce.read_device_status(ws) == 0
+    if shape == PERSISTENT_SHAPE:
+        # the single-pair side launches (programmatic dependent launch) are part of the graph
+        assert flce.read_side_launches(ws) == 2
     for k in out:
         assert torch.equal(out[k], eager[k]), f"graph replay differs from the eager call in {k}"
     d2 = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(1, BT - 1), seed=6)
@@ -472,9 +527,13 @@ def test_flce_full_size_sampled(flce, key):
     assert out["status"] == 0
     assert int(out["n_valid"].item()) == int(exp["n_valid"]) == w.n_valid
     assert_scalar_close(out["loss"].item(), float(exp["loss"]), "loss")
-    # the grad_input pass's automatic split tail ran (its row blocks are the last ones; the sample holds
-    # tokens and vocabulary entries among the last 512, where the grad_W pass's tail is when it splits)
-    assert flce.read_vocab_split_units(out["workspace"]) > 0
+    # the grad_input pass's last row blocks ran as an automatic split tail or, where the pass has four pairs
+    # per cluster and enough waves, on the single-pair clusters beside the persistent ones (the sample holds
+    # tokens and vocabulary entries among the last 512, where either form works)
+    side = flce.read_side_launches(out["workspace"])
+    assert flce.read_vocab_split_units(out["workspace"]) > 0 or side > 0
+    if key == "long":
+        assert side == 2, "both passes of the long workload run with single-pair clusters beside"
     rows = torch.from_numpy(exp["rows"]).cuda()
     vr = torch.from_numpy(exp["vocab_rows"]).cuda()
     check_full_size_rows(exp, bf16_to_numpy_f32(out["grad_input"][rows]), out["grad_W"][vr].cpu().numpy(),
@@ -489,20 +548,26 @@ def test_flce_full_size_sampled(flce, key):
 
 @pytest.mark.parametrize("key", ["qwen3", "gemma2", "long"])
 def test_flce_full_size_split_tails(flce, key):
-    """The automatic split tails at the full sizes: every row of the split row pairs (grad_input) and every
-    vocabulary row of the split vocabulary row pairs (grad_W, grad_bias) against the same call with no
+    """The automatic scheduling at the full sizes (split tails, or single-pair clusters beside persistent
+    four-pair clusters): every row of the last row pairs (grad_input) and every vocabulary row of the last
+    vocabulary row pairs (grad_W, grad_bias) against the same call with one cluster per unit and no
     splitting (whose rows the sampled test above checks against the oracle), within the parity bounds."""
     import torch
     d = _full_inputs(key)
     a = _run(flce, d)
     assert a["status"] == 0
-    vs, ts = flce.read_vocab_split_units(a["workspace"]), flce.read_token_split_units(a["workspace"])
-    assert vs > 0, "the grad_input pass did not split its last wave"
+    vs, side = flce.read_vocab_split_units(a["workspace"]), flce.read_side_launches(a["workspace"])
+    assert vs > 0 or side > 0, "the grad_input pass neither split its last wave nor ran side clusters"
     b = _run(flce, d, vocab_splits=1, token_splits=1)
     assert b["status"] == 0
     assert flce.read_vocab_split_units(b["workspace"]) == 0 and flce.read_token_split_units(b["workspace"]) == 0
+    assert flce.read_side_launches(b["workspace"]) == 0
     assert_scalar_close(a["loss"].item(), b["loss"].item(), "loss")
     w = wl.FUSED_WORKLOADS[key]
+    if side > 0:
+        # single-pair clusters reproduce the four-pair clusters bit for bit
+        assert torch.equal(a["grad_input"], b["grad_input"]) and torch.equal(a["grad_W"], b["grad_W"])
+        assert a["loss"].item() == b["loss"].item()
     # the split row pairs are the last ones (at qwen3 all 16, split unevenly); compare the last 4096 rows
     # and the last 1280 vocabulary rows (5 vocabulary row pairs)
     r0 = max(0, w.BT - 4096)
