@@ -38,7 +38,7 @@ KERNELS_PER_STEP = 5  # lse_partial, lse_merge, loss_reduce, dgrad(grad_input), 
 # online flow: bias table, count, grad_input pass with the LSE, loss reduction, four gated classic kernels
 # (launched, exit at once unless the online pass asked for them), grad_W pass; plus the merge of the
 # vocabulary-split clusters when the grad_input pass splits its last wave (and the same for the grad_W
-# pass's token-split clusters), and one launch of single-pair side clusters per pass that runs them
+# pass's token-split clusters), and one launch of side clusters per pass that runs them
 KERNELS_PER_STEP_ONLINE = 9
 
 
@@ -236,8 +236,10 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
     # vocabulary-split clusters the grad_input pass ran (its merge kernel is one more launch per step)
     split_units = flce.read_vocab_split_units(ws)
     token_split_units = flce.read_token_split_units(ws)
-    # launches of single-pair clusters beside the persistent four-pair clusters (one per pass that used them)
+    # launches of side clusters beside the persistent four-pair clusters (one per pass that used them), and
+    # the side clusters that took work (both passes)
     side_launches = flce.read_side_launches(ws)
+    side_clusters = flce.read_side_clusters(ws)
     # the two passes' work queues (workspace header bytes 40 and 48: main units | side units << 32), for the
     # executed GEMM1 work of passes that ran side clusters
     queues = [int(x) for x in ws[40:56].cpu().view(torch.int64).tolist()]
@@ -398,6 +400,7 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
     return dict(elapsed_ms=elapsed_ms, passes=passes, clocks=clocks, peak_mem=peak_mem, loss=loss, e2e_ms=e2e_ms,
                 e2e_serial_ms=e2e_serial_ms, h2d=h2d, d2h=d2h, workspace_bytes=ws.numel(), filter=filt,
                 split_units=split_units, token_split_units=token_split_units, side_launches=side_launches,
+                side_clusters=side_clusters,
                 queues=queues, graph_ms=graph_ms)
 
 
@@ -652,6 +655,7 @@ def main():
         "vocab_split_clusters": r["split_units"],
         "token_split_clusters": r["token_split_units"],
         "side_launches_per_step": r["side_launches"],
+        "side_clusters_with_work_per_step": r["side_clusters"],
         "clocks": r["clocks"],
         "e2e": {"value": world * w.BT / (r["e2e_ms"] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],

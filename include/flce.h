@@ -200,12 +200,13 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        With 0, a pass that runs four pairs per cluster (clusters of 8 CTAs) over at
  *                        least three waves of work units is scheduled instead as persistent 8-CTA
  *                        clusters that take units from a queue in the workspace header, plus a second
- *                        launch of 2-CTA clusters, started by programmatic dependent launch, on the SMs
- *                        the 8-CTA clusters leave idle.  They take single 256-column H chunks of the last
- *                        row blocks (computing those blocks' logits once per chunk) and stop early enough
- *                        to finish with the 8-CTA clusters.  No unit is split then, and results are the
- *                        same up to rounding order.  Each pass that did this adds 1 to the word at byte 56
- *                        of the workspace.
+ *                        launch of 4-CTA clusters (two pairs), started by programmatic dependent launch,
+ *                        on the SMs the 8-CTA clusters leave idle.  They take two 256-column H chunks of
+ *                        the last row blocks at a time (computing those blocks' logits once per two
+ *                        chunks) and stop early enough to finish with the 8-CTA clusters.  No unit is
+ *                        split then, and the results are bit for bit those of one 8-CTA cluster per unit.
+ *                        Each pass that did this adds 1 to the word at byte 56 of the workspace; the word
+ *                        at byte 60 counts the side clusters that took work.
  *   token_splits         the same for the grad_W pass, whose clusters own vocabulary rows and run over
  *                        the tokens: 0 splits the row blocks of its last, partly filled wave into token
  *                        ranges (partial grad_W / grad_bias rows, added in order by a merge kernel), 1
@@ -213,7 +214,7 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        scratch: fewer at small BT).  The classic flow's single launch of both passes
  *                        (separate_lse_pass with grad_input and grad_W) does not split.  The number of
  *                        token-split clusters is the word at byte 32 of the workspace.  0 also allows
- *                        the persistent scheduling with 2-CTA clusters beside the 8-CTA ones described
+ *                        the persistent scheduling with 4-CTA clusters beside the 8-CTA ones described
  *                        under vocab_splits.
  *   debug_stall_us       test-only; 0 in normal use.  When > 0 (at most 1000000, else
  *                        FLCE_ERR_INVALID_ARG), the TMA producer of every CTA of the gradient passes first

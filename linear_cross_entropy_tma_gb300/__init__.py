@@ -14,6 +14,7 @@ from ._lib import (  # noqa: F401
     load,
     read_device_status,
     read_filter_skips,
+    read_side_clusters,
     read_side_launches,
     read_token_split_units,
     read_vocab_split_units,

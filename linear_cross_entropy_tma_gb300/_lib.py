@@ -339,12 +339,20 @@ def read_token_split_units(workspace) -> int:
 
 
 def read_side_launches(workspace) -> int:
-    """Launches of single-pair clusters that ran beside the persistent four-pair clusters in the last
+    """Launches of side clusters (one or two pairs) that ran beside the persistent four-pair clusters in the last
     flce_fwd_bwd on this workspace, one per pass that used them (the 32-bit word at byte 56; synchronises
     the device)."""
     import torch
     torch.cuda.synchronize(workspace.device)
     return int(workspace[56:60].cpu().view(torch.int32).item())
+
+
+def read_side_clusters(workspace) -> int:
+    """Side clusters that took at least one unit in the last flce_fwd_bwd on this workspace, over both
+    passes (the 32-bit word at byte 60; synchronises the device)."""
+    import torch
+    torch.cuda.synchronize(workspace.device)
+    return int(workspace[60:64].cpu().view(torch.int32).item())
 
 
 def read_device_status(workspace, stream=None) -> int:

@@ -444,11 +444,12 @@ __device__ __forceinline__ PairSmem<kVocabRows, kFilter, kSlots>* pair_smem_of()
 // allocation as it was.)
 enum : int { kTmemOneUnit = 0, kTmemHeld = 1 };
 
-// The running sum of owner class k (kClasses = 4 in dgrad_pair_body) after blocks 0 .. nt - 1, given the
-// accumulator a0 of the last block's class and a1..a3 of the classes after it: a_i holds class
-// (nt - 1 + i) mod 4.  A class that owns no block holds 0.
-__device__ __forceinline__ float by_class(float a0, float a1, float a2, float a3, int k, int nt) {
-  const int i = (((k - (nt - 1)) % 4) + 4) % 4;
+// kClasses = 4 in dgrad_pair_body: a pair of a side cluster (P = 1 or 2 pairs) keeps A = 4 / P running
+// sums, one per owner class it meets (its t-th block, j = pr + t P, belongs to class j mod 4 = pr + (t mod
+// A) P), rotating them so that a0 always holds the current block's.  After its n_own blocks, a_i holds
+// slot (n_own - 1 + i) mod A; slot_sum returns slot s.  A slot that met no block holds 0.
+__device__ __forceinline__ float slot_sum(float a0, float a1, float a2, float a3, int s, int n_own, int A) {
+  const int i = (((s - (n_own - 1)) % A) + A) % A;
   return i == 0 ? a0 : i == 1 ? a1 : i == 2 ? a2 : a3;
 }
 
@@ -457,9 +458,9 @@ __device__ __forceinline__ float by_class(float a0, float a1, float a2, float a3
 // One cluster's work: rows [256 row_pair, +256) (128 per CTA of each pair) and the H chunks of
 // group hgroup (P consecutive 256-wide chunks, one per pair).
 // Columns: blocks [jb, je) of 256 (all of them except for a vocabulary-split unit of the online pass, su >= 0).
-// kClasses = 4: a single pair (P = 1) standing in for a cluster of four pairs, whose results it reproduces
-// bit for bit: the per-row sums that four pairs would keep apart (each over the blocks it owns, j mod 4)
-// are kept apart too and combined in the same order (the online pass's softmax sums, grad_bias).
+// kClasses = 4: a cluster of one or two pairs standing in for a cluster of four pairs, whose results it
+// reproduces bit for bit: the per-row sums that four pairs would keep apart (each over the blocks it owns,
+// j mod 4) are kept apart too and combined in the same order (the online pass's softmax sums, grad_bias).
 template <bool kVocabRows, bool kFilter, bool kOnline = false, int kSlots = 2, int kClasses = 1, int kTmem = 0>
 __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols,
                                                 const PairParams& p, uint32_t* __restrict__ status, int row_pair,
@@ -535,8 +536,9 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
   // grad_W pass: this epilogue thread's grad_bias partial (its row, its half); with kClasses = 4, one per
-  // owner class
+  // owner-class slot (slot_sum)
   float gbias_out = 0.f, gbias_c1 = 0.f, gbias_c2 = 0.f, gbias_c3 = 0.f;
+  const int n_slots = kClasses > 1 ? kClasses / P : 1;   // owner classes a pair meets
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------------------ TMA producer
@@ -821,8 +823,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       rc.y = row;
     }
     float gbias = 0.f;
-    // kClasses = 4: the running sums of the three owner classes other than the current block's; before
-    // block j, on_lsum / on_tsum / gbias hold class j mod 4 and the k-th of these class (j + k) mod 4
+    // kClasses = 4: the running sums of the other owner-class slots; before this pair's t-th block,
+    // on_lsum / on_tsum / gbias hold slot t mod n_slots and the k-th of these slot (t + k) mod n_slots
     float cl_l1 = 0.f, cl_l2 = 0.f, cl_l3 = 0.f, cl_t1 = 0.f, cl_t2 = 0.f, cl_t3 = 0.f;
     float cl_g1 = 0.f, cl_g2 = 0.f, cl_g3 = 0.f;
     bool ok = true;
@@ -841,13 +843,22 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     }
     int u = 0;
     for (int j = pr; j < nt && ok; j += P, ++u) {
-      if (kClasses > 1 && j > 0) {
-        float t = on_lsum;
-        on_lsum = cl_l1, cl_l1 = cl_l2, cl_l2 = cl_l3, cl_l3 = t;
-        t = on_tsum;
-        on_tsum = cl_t1, cl_t1 = cl_t2, cl_t2 = cl_t3, cl_t3 = t;
-        t = gbias;
-        gbias = cl_g1, cl_g1 = cl_g2, cl_g2 = cl_g3, cl_g3 = t;
+      if (kClasses > 1 && j > pr) {
+        if (n_slots == 4) {
+          float t = on_lsum;
+          on_lsum = cl_l1, cl_l1 = cl_l2, cl_l2 = cl_l3, cl_l3 = t;
+          t = on_tsum;
+          on_tsum = cl_t1, cl_t1 = cl_t2, cl_t2 = cl_t3, cl_t3 = t;
+          t = gbias;
+          gbias = cl_g1, cl_g1 = cl_g2, cl_g2 = cl_g3, cl_g3 = t;
+        } else {
+          float t = on_lsum;
+          on_lsum = cl_l1, cl_l1 = t;
+          t = on_tsum;
+          on_tsum = cl_t1, cl_t1 = t;
+          t = gbias;
+          gbias = cl_g1, cl_g1 = t;
+        }
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full, u & 1, abort))) {
         ok = false;
@@ -1045,10 +1056,10 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
       if (ok) {
         if (kClasses > 1) {
-          // (the target logit is a maximum: every class may carry it)
-          for (int k = 0; k < kClasses; ++k)
-            on_part[k * 2 + hh] = make_float4(by_class(on_lsum, cl_l1, cl_l2, cl_l3, k, nt), on_zy,
-                                              by_class(on_tsum, cl_t1, cl_t2, cl_t3, k, nt), 0.f);
+          // (the target logit is a maximum: any class may carry it)
+          for (int sl = 0; sl < n_slots; ++sl)
+            on_part[(pr + sl * P) * 2 + hh] = make_float4(slot_sum(on_lsum, cl_l1, cl_l2, cl_l3, sl, u, n_slots), on_zy,
+                                                          slot_sum(on_tsum, cl_t1, cl_t2, cl_t3, sl, u, n_slots), 0.f);
         } else {
           on_part[pr * 2 + hh] = make_float4(on_lsum, on_zy, on_tsum, 0.f);
         }
@@ -1161,11 +1172,11 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         }
       }
     }
-    gbias_out = kClasses > 1 ? by_class(gbias, cl_g1, cl_g2, cl_g3, 0, nt) : gbias;
+    gbias_out = kClasses > 1 ? slot_sum(gbias, cl_g1, cl_g2, cl_g3, 0, u, n_slots) : gbias;
     if (kClasses > 1) {
-      gbias_c1 = by_class(gbias, cl_g1, cl_g2, cl_g3, 1, nt);
-      gbias_c2 = by_class(gbias, cl_g1, cl_g2, cl_g3, 2, nt);
-      gbias_c3 = by_class(gbias, cl_g1, cl_g2, cl_g3, 3, nt);
+      gbias_c1 = slot_sum(gbias, cl_g1, cl_g2, cl_g3, 1, u, n_slots);
+      gbias_c2 = slot_sum(gbias, cl_g1, cl_g2, cl_g3, 2, u, n_slots);
+      gbias_c3 = slot_sum(gbias, cl_g1, cl_g2, cl_g3, 3, u, n_slots);
     }
   }
 
@@ -1180,10 +1191,13 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       const int rl = (warp & 3) * 32 + lane;
       st_shared_cluster_f32(mapa_shared(smem_u32(gb_gather + (pr * 2 + (warp >> 2)) * kTileM + rl), q), gbias_out);
       if (kClasses > 1) {
-        // (P = 1: the gather area is this CTA's own)
-        gb_gather[(2 + (warp >> 2)) * kTileM + rl] = gbias_c1;
-        gb_gather[(4 + (warp >> 2)) * kTileM + rl] = gbias_c2;
-        gb_gather[(6 + (warp >> 2)) * kTileM + rl] = gbias_c3;
+        // the other slots' classes: pr + s P
+        const float gs[3] = {gbias_c1, gbias_c2, gbias_c3};
+#pragma unroll
+        for (int sl = 1; sl < 4; ++sl)
+          if (sl < n_slots)
+            st_shared_cluster_f32(mapa_shared(smem_u32(gb_gather + ((pr + sl * P) * 2 + (warp >> 2)) * kTileM + rl), q),
+                                  gs[sl - 1]);
       }
     }
     cluster_sync();
@@ -1251,15 +1265,17 @@ __device__ __forceinline__ Unit unit_of(const UnitPlan& plan, int c) {
 
 // Work queue of a pass run by persistent clusters (word != null): the main launch's clusters of four
 // pairs take whole units (row pair x H group) from the bottom of the row pairs; a second launch of
-// single-pair clusters (the side launch, on the SMs the main launch leaves idle) takes units of one row
-// pair and one 256-wide H chunk from the top, computing that row pair's logits once per chunk.  One 64-bit
+// side clusters of S = kSidePairs pairs (the side launch, on the SMs the main launch leaves idle) takes
+// units of one row pair and S 256-wide H chunks from the top, computing that row pair's logits once per S
+// chunks.  One 64-bit
 // word holds both counts (main units claimed | side units claimed << 32), so that a row pair is never
 // split between the two.  The side opens a new row pair only while the main launch has at least `reserve`
 // row pairs left: enough to keep it busy while the side finishes that row pair.
 enum : int { kRoleMain = 1, kRoleSide = 2 };
 struct WorkQueue {
   unsigned long long* word;   // zeroed before the pass; null: one cluster per unit (blockIdx), no queue
-  uint32_t* side_count;       // side launches that ran (workspace header), or null
+  uint32_t* side_count;       // [2] side launches that ran, side clusters that took a unit (workspace
+                              // header), or null
   int role;
   int row_pairs;
   int main_groups;            // H groups per row pair of a main unit (h_chunks / 4)
@@ -1326,6 +1342,7 @@ __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUte
       atomicAdd(wq.side_count, 1u);
     }
     const uint32_t rank = cluster_ctarank();
+    bool took = false;
     for (;;) {
       if (rank == 0 && threadIdx.x == 0) {
         int c = (*reinterpret_cast<volatile uint32_t*>(status) & kStatusTimeout) != 0u ? -1 : claim_unit(wq);
@@ -1333,6 +1350,8 @@ __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUte
           atomicOr(status, kStatusInternal);
           c = -1;
         }
+        if (c >= 0 && !took && wq.role == kRoleSide && wq.side_count != nullptr) atomicAdd(wq.side_count + 1, 1u);
+        took = took || c >= 0;
         for (int r = 0; r < 2 * p.P; ++r)
           st_shared_cluster_u32(mapa_shared(smem_u32(&sm.claim), static_cast<uint32_t>(r)), static_cast<uint32_t>(c));
       }
@@ -1358,7 +1377,7 @@ __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUte
 }
 
 // One gradient pass: without a queue, cluster blockIdx.x / 2P is work unit unit_of(plan, .); with one
-// (kQueue), a persistent cluster of the main or side launch (WorkQueue; the side launch's single pairs with
+// (kQueue), a persistent cluster of the main or side launch (WorkQueue; the side launch's pairs with
 // kClasses = 4).
 template <bool kVocabRows, bool kFilter, int kSlots, int kClasses = 1, bool kQueue = false>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1692,17 +1711,26 @@ int device_sm_count() {
 }
 
 // A pass with four pairs per cluster, run as persistent clusters of four pairs (one per resident slot)
-// plus, on the SMs those leave idle (8-CTA clusters do not tile every GPC), persistent single-pair clusters
+// plus, on the SMs those leave idle (8-CTA clusters do not tile every GPC), persistent side clusters
 // sharing its work queue (WorkQueue).  The side launch follows the main one with programmatic stream
 // serialisation: it starts once every main CTA is running, and completes after the main launch.  Taken
 // when the pass has a queue word, the resident count is known and there are at least kCoRunMinWaves waves
 // of main units; otherwise nothing is launched (*launched = false).
 constexpr int kCoRunMinWaves = 3;
+// pairs per side cluster: 1 (2-CTA clusters, a row block's logits once per H chunk) or 2 (4-CTA clusters,
+// once per two chunks).  Measured at the long workload: 78.3-78.8 ms per step with 1, 75.4-75.8 with 2.
+constexpr int kSidePairs = 2;
+// the side launch's reserve (see launch_corun) in quarters of the modelled one, per pass: measured at the
+// long workload, x0.5 / x0.75 / x1 / x1.25 gave 37.8 / 37.8 / 39.9 / 39.9 ms for the grad_input pass and
+// 40.5 / 40.6 / 40.0 / 40.3 ms for the grad_W pass
+constexpr int kReserveQuartersOnline = 2;
+constexpr int kReserveQuartersGradW = 4;
 
 template <class MainKernel, class SideKernel>
 cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, size_t smem_side, int res_main,
                          const CUtensorMap& rows, const CUtensorMap& cols, const PairParams& p, int h_chunks,
-                         int splits_option, const DgPairArgs& a, cudaStream_t stream, bool* launched) {
+                         int splits_option, int reserve_quarters, const DgPairArgs& a, cudaStream_t stream,
+                         bool* launched) {
   *launched = false;
   const int rp = row_pairs_of(p);
   const int main_groups = h_chunks / 4;
@@ -1710,29 +1738,32 @@ cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, size_t 
   if (a.work_q == nullptr || splits_option != 0 || p.P != 4 || res_main <= 0 || main_groups < 1 ||
       rp * main_groups < kCoRunMinWaves * res_main)
     return cudaSuccess;
-  const int side = (device_sm_count() - 8 * res_main) / 2;
-  if (side < 2) return cudaSuccess;
+  const int side = (device_sm_count() - 8 * res_main) / (2 * kSidePairs);   // side clusters
+  if (side * kSidePairs < 2) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_main));
   if (e != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_side))) !=
       cudaSuccess)
     return e;
   const UnitPlan plan = make_plan(rp, main_groups, (p.n_cols + kPN - 1) / kPN, 0, 1, 0, false);
-  // A side unit (one pair: the row pair's logits and one chunk's GEMM2) takes 4 (H + 256) / (H + 1024) times
-  // as long as a main unit (four pairs: the logits once and four chunks' GEMM2) at equal rates per pair; the
-  // side begins a row pair only while the main launch has that many units per main cluster left.
-  const long long num = 4ll * (p.H + kHc) * res_main;
-  const long long den = static_cast<long long>(p.H + 4 * kHc) * main_groups;
-  WorkQueue wq{a.work_q, a.side_count, kRoleMain, rp, main_groups, h_chunks, static_cast<int>((num + den - 1) / den)};
+  // A side unit (S = kSidePairs pairs: the row pair's logits and S chunks' GEMM2) takes
+  // 4 (H + 256 S) / (S (H + 1024)) times as long as a main unit (four pairs: the logits once and four chunks'
+  // GEMM2) at equal rates per pair; the side begins a row pair only while the main launch has that many
+  // units per main cluster left, times reserve_quarters / 4 (measured per pass: the side pairs, with no
+  // hand-over to wait for, run faster per pair than the model says in the grad_input pass).
+  const long long num = static_cast<long long>(reserve_quarters) * (p.H + kSidePairs * kHc) * res_main;
+  const long long den = 4ll * kSidePairs * (p.H + 4 * kHc) * main_groups;
+  WorkQueue wq{a.work_q, a.side_count, kRoleMain, rp, main_groups, h_chunks / kSidePairs,
+               static_cast<int>((num + den - 1) / den)};
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cm =
       cluster_config(dim3(8 * std::min(res_main, rp * main_groups), 1, 1), smem_main, 4, stream, attr);
   if ((e = cudaLaunchKernelEx(&cm, km, rows, cols, p, a.status, plan, wq)) != cudaSuccess) return e;
   PairParams ps = p;
-  ps.P = 1;
+  ps.P = kSidePairs;
   WorkQueue wside = wq;
   wside.role = kRoleSide;
-  cudaLaunchConfig_t cs = cluster_config(dim3(2 * side, 1, 1), smem_side, 1, stream, attr);
+  cudaLaunchConfig_t cs = cluster_config(dim3(2 * kSidePairs * side, 1, 1), smem_side, kSidePairs, stream, attr);
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cs.numAttrs = 2;
@@ -1766,7 +1797,8 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
     bool launched = false;
     e = launch_corun(dgrad_pair_kernel<kVocabRows, false, kFourPairSlots, 1, true>, smem,
                      dgrad_pair_kernel<kVocabRows, false, 2, kMaxPairs, true>, pair_smem_bytes<kVocabRows, false>(), res4,
-                     rows, cols, p, h_chunks, kVocabRows ? a.token_splits : 0, a, stream, &launched);
+                     rows, cols, p, h_chunks, kVocabRows ? a.token_splits : 0, kReserveQuartersGradW, a, stream,
+                     &launched);
     if (e != cudaSuccess || launched) return e;
   }
   UnitPlan plan = make_plan(rp, h_chunks / p.P, nt, 0, 1, 0, false);
@@ -1813,8 +1845,8 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   if (four) {
     bool launched = false;
     e = launch_corun(dgrad_online_kernel<kFourPairSlots, 1, true>, smem, dgrad_online_kernel<2, kMaxPairs, true>,
-                     pair_smem_bytes<false, false>(), slots_of[4], hidden_map, w_map, p, h_chunks, a.vocab_splits, a,
-                     stream, &launched);
+                     pair_smem_bytes<false, false>(), slots_of[4], hidden_map, w_map, p, h_chunks, a.vocab_splits,
+                     kReserveQuartersOnline, a, stream, &launched);
     if (e != cudaSuccess || launched) return e;
   }
   // vocabulary-split tail: the accumulators go to the split scratch (16 MiB),

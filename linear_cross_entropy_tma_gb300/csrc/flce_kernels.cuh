@@ -41,7 +41,8 @@ struct FusedWorkspace {
   uint32_t* vs_count; // header: vocabulary-split clusters of the online grad_input pass
   uint32_t* ts_count; // header: token-split clusters of the grad_W pass
   unsigned long long* work_q;  // header: [2] work queues of the grad_input and grad_W passes (zeroed per call)
-  uint32_t* side_count;        // header: launches of single-pair clusters beside the four-pair clusters
+  uint32_t* side_count;        // header: [2] launches of side clusters beside the four-pair clusters, and
+                               // side clusters that took at least one unit
   uint32_t* zf_neg;  // header: non-zero when the log form of dS does not apply (some valid row has
                      // f u <= 0 with u its upstream gradient, or the gradient scale is <= 0)
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max)); free again by the
@@ -167,8 +168,9 @@ struct DgPairArgs {
   uint32_t* split_count;
   uint32_t debug_stall_us;   // test-only (flce_fwd_bwd_options.debug_stall_us)
   // Shared work queue (a zeroed 64-bit word) for a pass run by persistent clusters of four pairs plus a
-  // second launch of single-pair clusters on the SMs they leave idle, or NULL (one cluster per unit);
-  // side_count: incremented once per launch of single-pair clusters (workspace header)
+  // second launch of smaller side clusters on the SMs they leave idle, or NULL (one cluster per unit);
+  // side_count: [2] incremented once per side launch, and once per side cluster that took a unit
+  // (workspace header)
   unsigned long long* work_q;
   uint32_t* side_count;
 };

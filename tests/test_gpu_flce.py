@@ -218,14 +218,14 @@ def test_flce_vocab_split_options(flce):
 
 
 # Both passes with four pairs per cluster and at least three waves of row pairs (65 token and 66 vocabulary
-# row pairs against 15 resident 8-CTA clusters): persistent four-pair clusters plus single-pair clusters
+# row pairs against 15 resident 8-CTA clusters): persistent four-pair clusters plus side clusters
 # on the SMs they leave idle, which take the last row pairs one 256-wide H chunk at a time.
 PERSISTENT_SHAPE = (16400, 1024, 16700)
 
 
 def test_flce_persistent_with_side_clusters(flce):
     """Element by element against the oracle; the side launches counted; and bit for bit the same as one
-    cluster per unit (the single pairs keep the four pairs' partial sums apart and add them in order)."""
+    cluster per unit (the side pairs keep the four pairs' partial sums apart and add them in order)."""
     import torch
     BT, H, V = PERSISTENT_SHAPE
     d = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(0, BT - 1), seed=41)
@@ -244,7 +244,7 @@ def test_flce_persistent_with_side_clusters(flce):
 
 
 def test_flce_persistent_side_clusters_options(flce):
-    # per-token upstream gradients and losses, entropy (the owner-class sums of the single pairs) and
+    # per-token upstream gradients and losses, entropy (the owner-class sums of the side pairs) and
     # accumulation, with the side clusters
     import torch
     BT, H, V = PERSISTENT_SHAPE
@@ -435,7 +435,7 @@ def test_flce_cuda_graph_replay(flce, shape):
     torch.cuda.synchronize()
     assert flce.read_device_status(ws) == 0
     if shape == PERSISTENT_SHAPE:
-        # the single-pair side launches (programmatic dependent launch) are part of the graph
+        # the side launches (programmatic dependent launch) are part of the graph
         assert flce.read_side_launches(ws) == 2
     for k in out:
         assert torch.equal(out[k], eager[k]), f"graph replay differs from the eager call in {k}"
@@ -528,12 +528,12 @@ def test_flce_full_size_sampled(flce, key):
     assert int(out["n_valid"].item()) == int(exp["n_valid"]) == w.n_valid
     assert_scalar_close(out["loss"].item(), float(exp["loss"]), "loss")
     # the grad_input pass's last row blocks ran as an automatic split tail or, where the pass has four pairs
-    # per cluster and enough waves, on the single-pair clusters beside the persistent ones (the sample holds
+    # per cluster and enough waves, on the side clusters beside the persistent ones (the sample holds
     # tokens and vocabulary entries among the last 512, where either form works)
     side = flce.read_side_launches(out["workspace"])
     assert flce.read_vocab_split_units(out["workspace"]) > 0 or side > 0
     if key == "long":
-        assert side == 2, "both passes of the long workload run with single-pair clusters beside"
+        assert side == 2, "both passes of the long workload run with side clusters beside"
     rows = torch.from_numpy(exp["rows"]).cuda()
     vr = torch.from_numpy(exp["vocab_rows"]).cuda()
     check_full_size_rows(exp, bf16_to_numpy_f32(out["grad_input"][rows]), out["grad_W"][vr].cpu().numpy(),
@@ -548,7 +548,7 @@ def test_flce_full_size_sampled(flce, key):
 
 @pytest.mark.parametrize("key", ["qwen3", "gemma2", "long"])
 def test_flce_full_size_split_tails(flce, key):
-    """The automatic scheduling at the full sizes (split tails, or single-pair clusters beside persistent
+    """The automatic scheduling at the full sizes (split tails, or side clusters beside persistent
     four-pair clusters): every row of the last row pairs (grad_input) and every vocabulary row of the last
     vocabulary row pairs (grad_W, grad_bias) against the same call with one cluster per unit and no
     splitting (whose rows the sampled test above checks against the oracle), within the parity bounds."""
@@ -565,7 +565,7 @@ def test_flce_full_size_split_tails(flce, key):
     assert_scalar_close(a["loss"].item(), b["loss"].item(), "loss")
     w = wl.FUSED_WORKLOADS[key]
     if side > 0:
-        # single-pair clusters reproduce the four-pair clusters bit for bit
+        # side clusters reproduce the four-pair clusters bit for bit
         assert torch.equal(a["grad_input"], b["grad_input"]) and torch.equal(a["grad_W"], b["grad_W"])
         assert a["loss"].item() == b["loss"].item()
     # the split row pairs are the last ones (at qwen3 all 16, split unevenly); compare the last 4096 rows

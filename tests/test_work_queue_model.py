@@ -1,0 +1,104 @@
+"""Randomised model of the work queue shared by the persistent four-pair clusters and the side clusters
+(csrc/flce_bwd.cu, claim_unit / launch_corun), on the CPU.
+
+One 64-bit word holds the main units claimed (low half) and the side units claimed (high half).  A main
+cluster takes unit a (row pair a / main_groups, H group a mod main_groups) while that row pair is below
+every row pair the side has begun; a side cluster takes unit b (row pair R - 1 - b / side_groups, H
+group b mod side_groups), always when it continues a row pair already begun and, for a new row pair, only
+while that row pair lies at least `reserve` row pairs above every row pair the main launch has begun.
+Every update is a compare-and-swap of the whole word.
+
+The model runs main and side claimers in random orders (each claim reads the word, then tries its swap,
+which fails when another claimer swapped in between) and asserts: every (row pair, H chunk) is computed
+exactly once; no row pair is shared between the launches; the side never begins a row pair within
+`reserve` of the main launch's; both launches stop.  Planted mistakes in the rule must be caught.
+"""
+import random
+
+import pytest
+
+
+def claim(word, role, R, mg, sg, reserve, mistake=None):
+    """The next unit for `role` given the word, and the new word; (None, word) when there is none."""
+    a, b = word & 0xFFFFFFFF, word >> 32
+    a_rows = (a + mg - 1) // mg
+    b_rows = (b + sg - 1) // sg
+    if role == "main":
+        limit = R if mistake == "main ignores the side" else R - b_rows
+        if a // mg >= limit:
+            return None, word
+        return a, word + 1
+    opening = b % sg == 0
+    if mistake == "side opens without the reserve":
+        opening = False
+    if opening and (R - 1 - b // sg) - a_rows < reserve:
+        return None, word
+    return b, word + (1 << 32)
+
+
+def run(R, H_chunks, n_main, n_side, reserve, seed, mistake=None):
+    rng = random.Random(seed)
+    mg, sg = H_chunks // 4, H_chunks
+    word = 0
+    done = {}                       # (row pair, chunk) -> launch
+    rows_of = {"main": set(), "side": set()}
+    active = [("main", i) for i in range(n_main)] + [("side", i) for i in range(n_side)]
+    stale = {c: None for c in active}   # word each claimer read before its swap
+    finished = set()
+    steps = 0
+    while len(finished) < len(active):
+        steps += 1
+        assert steps < 10 ** 6, "the claimers did not stop"
+        c = rng.choice([x for x in active if x not in finished])
+        role = c[0]
+        if stale[c] is None:
+            stale[c] = word             # read the word
+            continue
+        seen = stale[c]
+        stale[c] = None
+        unit, new = claim(seen, role, R, mg, sg, reserve, mistake)
+        if unit is None:
+            if seen == word:
+                finished.add(c)         # nothing left for this claimer
+            continue
+        if seen != word:
+            continue                    # the swap failed: read again
+        word = new
+        if role == "main":
+            row, chunks = unit // mg, [4 * (unit % mg) + k for k in range(4)]
+        else:
+            row, chunks = R - 1 - unit // sg, [unit % sg]
+            a_rows = ((word & 0xFFFFFFFF) + mg - 1) // mg
+            if unit % sg == 0:
+                assert row - a_rows >= reserve or mistake, "side began a row pair within the reserve"
+        assert 0 <= row < R, "claimed a row pair outside the pass"
+        rows_of[role].add(row)
+        for k in chunks:
+            assert (row, k) not in done, f"row pair {row} chunk {k} computed twice"
+            done[(row, k)] = role
+    assert not (rows_of["main"] & rows_of["side"]), "a row pair was split between the launches"
+    missing = [(r, k) for r in range(R) for k in range(H_chunks) if (r, k) not in done]
+    assert not missing, f"{len(missing)} (row pair, chunk) units never computed, e.g. {missing[:3]}"
+    return rows_of
+
+
+@pytest.mark.parametrize("R,H_chunks,n_main,n_side,reserve", [
+    (256, 4, 15, 16, 19),     # the long workload's grad_input pass (reserve x0.5)
+    (689, 4, 15, 16, 38),     # its grad_W pass
+    (65, 4, 15, 16, 38),      # the GPU test shape
+    (47, 8, 15, 16, 10),      # two H groups per main unit
+    (40, 4, 3, 1, 1),         # minimal reserve
+    (45, 4, 15, 16, 100),     # a reserve the side can never meet: main does everything
+])
+def test_work_queue_covers_every_unit_once(R, H_chunks, n_main, n_side, reserve):
+    for seed in range(20):
+        rows = run(R, H_chunks, n_main, n_side, reserve, seed)
+        if reserve >= R:
+            assert not rows["side"]
+
+
+@pytest.mark.parametrize("mistake", ["main ignores the side", "side opens without the reserve"])
+def test_work_queue_planted_mistakes_are_caught(mistake):
+    with pytest.raises(AssertionError):
+        for seed in range(20):
+            run(256, 4, 15, 16, 19, seed, mistake)
