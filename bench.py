@@ -356,8 +356,11 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
+    e2e_sampler = ClockSampler(local)
+    e2e_sampler.start()
     e2e_pipelined(e2e_steps, start_ev=a, end_ev=b)
     torch.cuda.synchronize()
+    e2e_clocks = e2e_sampler.stop()
     barrier(world)
     e2e_ms = max_over_ranks(a.elapsed_time(b), world) / e2e_steps
     del h_hidden, h_W, r_gi, r_gw, dev_in, dev_out
@@ -398,6 +401,7 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
                                    "workspace_bytes": ws_sort.numel()}
         del ws_sort
     return dict(elapsed_ms=elapsed_ms, passes=passes, clocks=clocks, peak_mem=peak_mem, loss=loss, e2e_ms=e2e_ms,
+                e2e_clocks=e2e_clocks,
                 e2e_serial_ms=e2e_serial_ms, h2d=h2d, d2h=d2h, workspace_bytes=ws.numel(), filter=filt,
                 split_units=split_units, token_split_units=token_split_units, side_launches=side_launches,
                 side_clusters=side_clusters,
@@ -660,7 +664,7 @@ def main():
         "e2e": {"value": world * w.BT / (r["e2e_ms"] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],
                 "copies": "double-buffered on two copy streams, overlapping the neighbouring steps' compute",
-                "ms_per_step_serial": r["e2e_serial_ms"]},
+                "ms_per_step_serial": r["e2e_serial_ms"], "clocks": r["e2e_clocks"]},
         "memory": {"peak_allocated_bytes": r["peak_mem"], "workspace_bytes": r["workspace_bytes"],
                    "avoided_fp32_logits_bytes": 4 * w.BT * w.V},
         "loss": r["loss"],
