@@ -62,6 +62,12 @@ constexpr int kPN = 256;                      // logits tile columns = K of GEMM
 constexpr int kBK = 64;
 constexpr int kHc = 256;                      // H columns per pair (GEMM2 N)
 constexpr int kMaxPairs = 4;                  // pairs per cluster that share each logits tile
+// Pairs per side cluster (persistent scheduling, launch_corun): beside four-pair main clusters 2 (4-CTA
+// clusters, a row block's logits once per two H chunks; measured at the long workload: 78.3-78.8 ms per
+// step with single pairs, 75.4-75.8 with two).  (A side pair must meet whole owner classes of the main
+// launch: its blocks j = pr + S t fall in classes j mod P, so S divides P; beside two- or three-pair main
+// clusters it would be 1.)
+constexpr int side_pairs_for(int P) { return P == 4 ? 2 : 1; }
 // Gradient filter: ring of per-block skip verdicts.  The owner of block b publishes them once the logits
 // of b are complete, which (in the issue order below) is after every pair finished GEMM2 of block
 // b - P - 2, so a ring of more than P + 2 blocks is never overwritten before every CTA has read it.
@@ -466,7 +472,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
                                                 const PairParams& p, uint32_t* __restrict__ status, int row_pair,
                                                 int hgroup, int jb = 0, int je = -1, int su = -1) {
   static_assert(!kOnline || (!kVocabRows && !kFilter), "the online form is a grad_input pass without the filter");
-  static_assert(kClasses == 1 || (kClasses == kMaxPairs && !kFilter), "owner classes: 1, or 4 for the exact passes");
+  static_assert(kClasses == 1 || (kClasses >= 2 && kClasses <= kMaxPairs && !kFilter),
+                "owner classes: 1, or 2-4 for the exact passes (4 is the one launched)");
   using Smem = PairSmem<kVocabRows, kFilter, kSlots>;
   constexpr int kStages = Smem::Cfg::kStages;
   // (run_units has checked the gate and the layout's alignment and allocated TMEM)
@@ -538,7 +545,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
   // grad_W pass: this epilogue thread's grad_bias partial (its row, its half); with kClasses = 4, one per
   // owner-class slot (slot_sum)
   float gbias_out = 0.f, gbias_c1 = 0.f, gbias_c2 = 0.f, gbias_c3 = 0.f;
-  const int n_slots = kClasses > 1 ? kClasses / P : 1;   // owner classes a pair meets
+  // owner classes a side pair meets (its cluster has side_pairs_for(kClasses) pairs)
+  constexpr int n_slots = kClasses > 1 ? kClasses / side_pairs_for(kClasses) : 1;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------------------ TMA producer
@@ -844,13 +852,20 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     int u = 0;
     for (int j = pr; j < nt && ok; j += P, ++u) {
       if (kClasses > 1 && j > pr) {
-        if (n_slots == 4) {
+        if constexpr (n_slots == 4) {
           float t = on_lsum;
           on_lsum = cl_l1, cl_l1 = cl_l2, cl_l2 = cl_l3, cl_l3 = t;
           t = on_tsum;
           on_tsum = cl_t1, cl_t1 = cl_t2, cl_t2 = cl_t3, cl_t3 = t;
           t = gbias;
           gbias = cl_g1, cl_g1 = cl_g2, cl_g2 = cl_g3, cl_g3 = t;
+        } else if constexpr (n_slots == 3) {
+          float t = on_lsum;
+          on_lsum = cl_l1, cl_l1 = cl_l2, cl_l2 = t;
+          t = on_tsum;
+          on_tsum = cl_t1, cl_t1 = cl_t2, cl_t2 = t;
+          t = gbias;
+          gbias = cl_g1, cl_g1 = cl_g2, cl_g2 = t;
         } else {
           float t = on_lsum;
           on_lsum = cl_l1, cl_l1 = t;
@@ -1265,9 +1280,9 @@ __device__ __forceinline__ Unit unit_of(const UnitPlan& plan, int c) {
 
 // Work queue of a pass run by persistent clusters (word != null): the main launch's clusters of four
 // pairs take whole units (row pair x H group) from the bottom of the row pairs; a second launch of
-// side clusters of S = kSidePairs pairs (the side launch, on the SMs the main launch leaves idle) takes
-// units of one row pair and S 256-wide H chunks from the top, computing that row pair's logits once per S
-// chunks.  One 64-bit
+// side clusters of S pairs (the side launch, on the SMs the main launch leaves idle; S = side_pairs_for(P))
+// takes units of one row pair and S 256-wide H chunks from the top, computing that row pair's logits once
+// per S chunks.  One 64-bit
 // word holds both counts (main units claimed | side units claimed << 32), so that a row pair is never
 // split between the two.  The side opens a new row pair only while the main launch has at least `reserve`
 // row pairs left: enough to keep it busy while the side finishes that row pair.
@@ -1717,9 +1732,6 @@ int device_sm_count() {
 // when the pass has a queue word, the resident count is known and there are at least kCoRunMinWaves waves
 // of main units; otherwise nothing is launched (*launched = false).
 constexpr int kCoRunMinWaves = 3;
-// pairs per side cluster: 1 (2-CTA clusters, a row block's logits once per H chunk) or 2 (4-CTA clusters,
-// once per two chunks).  Measured at the long workload: 78.3-78.8 ms per step with 1, 75.4-75.8 with 2.
-constexpr int kSidePairs = 2;
 // the side launch's reserve (see launch_corun) in quarters of the modelled one, per pass: measured at the
 // long workload, x0.5 / x0.75 / x1 / x1.25 gave 37.8 / 37.8 / 39.9 / 39.9 ms for the grad_input pass and
 // 40.5 / 40.6 / 40.0 / 40.3 ms for the grad_W pass
@@ -1733,37 +1745,42 @@ cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, size_t 
                          bool* launched) {
   *launched = false;
   const int rp = row_pairs_of(p);
-  const int main_groups = h_chunks / 4;
-  // (automatic scheduling only: splits_option 1 asks for one cluster per unit, k >= 2 for split units)
-  if (a.work_q == nullptr || splits_option != 0 || p.P != 4 || res_main <= 0 || main_groups < 1 ||
+  const int P = p.P;
+  const int S = side_pairs_for(P);
+  const int main_groups = h_chunks / P;
+  // (automatic scheduling only: splits_option 1 asks for one cluster per unit, k >= 2 for split units.  Four
+  // pairs only: beside three-pair clusters (gemma2, 14 idle SMs, single-pair side clusters) the grad_W pass
+  // gained 1.5% but the grad_input pass, with four waves of long units, lost 17% against its split tail;
+  // beside two-pair clusters (8 idle SMs) nothing was gained.)
+  if (a.work_q == nullptr || splits_option != 0 || P != 4 || res_main <= 0 || main_groups < 1 ||
       rp * main_groups < kCoRunMinWaves * res_main)
     return cudaSuccess;
-  const int side = (device_sm_count() - 8 * res_main) / (2 * kSidePairs);   // side clusters
-  if (side * kSidePairs < 2) return cudaSuccess;
+  const int side = (device_sm_count() - 2 * P * res_main) / (2 * S);   // side clusters
+  if (side * S < 2) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_main));
   if (e != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_side))) !=
       cudaSuccess)
     return e;
   const UnitPlan plan = make_plan(rp, main_groups, (p.n_cols + kPN - 1) / kPN, 0, 1, 0, false);
-  // A side unit (S = kSidePairs pairs: the row pair's logits and S chunks' GEMM2) takes
-  // 4 (H + 256 S) / (S (H + 1024)) times as long as a main unit (four pairs: the logits once and four chunks'
-  // GEMM2) at equal rates per pair; the side begins a row pair only while the main launch has that many
-  // units per main cluster left, times reserve_quarters / 4 (measured per pass: the side pairs, with no
-  // hand-over to wait for, run faster per pair than the model says in the grad_input pass).
-  const long long num = static_cast<long long>(reserve_quarters) * (p.H + kSidePairs * kHc) * res_main;
-  const long long den = 4ll * kSidePairs * (p.H + 4 * kHc) * main_groups;
-  WorkQueue wq{a.work_q, a.side_count, kRoleMain, rp, main_groups, h_chunks / kSidePairs,
+  // A side unit (S pairs: the row pair's logits and S chunks' GEMM2) takes P (H + 256 S) / (S (H + 256 P))
+  // times as long as a main unit (P pairs: the logits once and P chunks' GEMM2) at equal rates per pair; the
+  // side begins a row pair only while the main launch has that many units per main cluster left, times
+  // reserve_quarters / 4 (measured per pass: the side pairs, with no hand-over to wait for, run faster per
+  // pair than the model says in the grad_input pass).
+  const long long num = static_cast<long long>(reserve_quarters) * P * (p.H + S * kHc) * res_main;
+  const long long den = 4ll * S * (p.H + P * kHc) * main_groups;
+  WorkQueue wq{a.work_q, a.side_count, kRoleMain, rp, main_groups, h_chunks / S,
                static_cast<int>((num + den - 1) / den)};
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cm =
-      cluster_config(dim3(8 * std::min(res_main, rp * main_groups), 1, 1), smem_main, 4, stream, attr);
+      cluster_config(dim3(2 * P * std::min(res_main, rp * main_groups), 1, 1), smem_main, P, stream, attr);
   if ((e = cudaLaunchKernelEx(&cm, km, rows, cols, p, a.status, plan, wq)) != cudaSuccess) return e;
   PairParams ps = p;
-  ps.P = kSidePairs;
+  ps.P = S;
   WorkQueue wside = wq;
   wside.role = kRoleSide;
-  cudaLaunchConfig_t cs = cluster_config(dim3(2 * kSidePairs * side, 1, 1), smem_side, kSidePairs, stream, attr);
+  cudaLaunchConfig_t cs = cluster_config(dim3(2 * S * side, 1, 1), smem_side, S, stream, attr);
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cs.numAttrs = 2;
@@ -1796,9 +1813,9 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
     if (res4 == 0) res4 = resident_clusters(kern, smem, 4, stream);
     bool launched = false;
     e = launch_corun(dgrad_pair_kernel<kVocabRows, false, kFourPairSlots, 1, true>, smem,
-                     dgrad_pair_kernel<kVocabRows, false, 2, kMaxPairs, true>, pair_smem_bytes<kVocabRows, false>(), res4,
-                     rows, cols, p, h_chunks, kVocabRows ? a.token_splits : 0, kReserveQuartersGradW, a, stream,
-                     &launched);
+                     dgrad_pair_kernel<kVocabRows, false, 2, 4, true>, pair_smem_bytes<kVocabRows, false>(), res4, rows,
+                     cols, p, h_chunks, kVocabRows ? a.token_splits : 0,
+                     kVocabRows ? kReserveQuartersGradW : kReserveQuartersOnline, a, stream, &launched);
     if (e != cudaSuccess || launched) return e;
   }
   UnitPlan plan = make_plan(rp, h_chunks / p.P, nt, 0, 1, 0, false);
@@ -1844,7 +1861,7 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   if (slots_of[p.P] == 0) slots_of[p.P] = resident_clusters(kern, smem, p.P, stream);
   if (four) {
     bool launched = false;
-    e = launch_corun(dgrad_online_kernel<kFourPairSlots, 1, true>, smem, dgrad_online_kernel<2, kMaxPairs, true>,
+    e = launch_corun(dgrad_online_kernel<kFourPairSlots, 1, true>, smem, dgrad_online_kernel<2, 4, true>,
                      pair_smem_bytes<false, false>(), slots_of[4], hidden_map, w_map, p, h_chunks, a.vocab_splits,
                      kReserveQuartersOnline, a, stream, &launched);
     if (e != cudaSuccess || launched) return e;

@@ -564,10 +564,16 @@ def test_flce_full_size_split_tails(flce, key):
     assert flce.read_side_launches(b["workspace"]) == 0
     assert_scalar_close(a["loss"].item(), b["loss"].item(), "loss")
     w = wl.FUSED_WORKLOADS[key]
-    if side > 0:
-        # side clusters reproduce the four-pair clusters bit for bit
-        assert torch.equal(a["grad_input"], b["grad_input"]) and torch.equal(a["grad_W"], b["grad_W"])
-        assert a["loss"].item() == b["loss"].item()
+    # a pass that ran persistent with side clusters (no split units) gives the one-cluster-per-unit result
+    # bit for bit; the grad_W pass only when the grad_input pass did not split either (its per-token
+    # statistics, which every grad_W row sums over, carry the split tail's rounding)
+    ts = flce.read_token_split_units(a["workspace"])
+    if side > 0 and vs == 0:
+        assert torch.equal(a["grad_input"], b["grad_input"]) and a["loss"].item() == b["loss"].item()
+        if ts == 0:
+            assert torch.equal(a["grad_W"], b["grad_W"])
+            if a["grad_bias"] is not None:
+                assert torch.equal(a["grad_bias"], b["grad_bias"])
     # the split row pairs are the last ones (at qwen3 all 16, split unevenly); compare the last 4096 rows
     # and the last 1280 vocabulary rows (5 vocabulary row pairs)
     r0 = max(0, w.BT - 4096)

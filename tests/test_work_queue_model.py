@@ -1,11 +1,12 @@
-"""Randomised model of the work queue shared by the persistent four-pair clusters and the side clusters
+"""Randomised model of the work queue shared by the persistent main clusters and the side clusters
 (csrc/flce_bwd.cu, claim_unit / launch_corun), on the CPU.
 
 One 64-bit word holds the main units claimed (low half) and the side units claimed (high half).  A main
-cluster takes unit a (row pair a / main_groups, H group a mod main_groups) while that row pair is below
-every row pair the side has begun; a side cluster takes unit b (row pair R - 1 - b / side_groups, H
-group b mod side_groups), always when it continues a row pair already begun and, for a new row pair, only
-while that row pair lies at least `reserve` row pairs above every row pair the main launch has begun.
+cluster (P pairs) takes unit a (row pair a / main_groups, the P chunks of H group a mod main_groups) while
+that row pair is below every row pair the side has begun; a side cluster (S pairs) takes unit b (row pair
+R - 1 - b / side_groups, the S chunks of group b mod side_groups), always when it continues a row pair
+already begun and, for a new row pair, only while that row pair lies at least `reserve` row pairs above
+every row pair the main launch has begun.
 Every update is a compare-and-swap of the whole word.
 
 The model runs main and side claimers in random orders (each claim reads the word, then tries its swap,
@@ -36,9 +37,10 @@ def claim(word, role, R, mg, sg, reserve, mistake=None):
     return b, word + (1 << 32)
 
 
-def run(R, H_chunks, n_main, n_side, reserve, seed, mistake=None):
+def run(R, H_chunks, n_main, n_side, reserve, seed, mistake=None, P=4, S=1):
+    """P pairs per main cluster (a main unit: P chunks of one row pair), S per side cluster (S chunks)."""
     rng = random.Random(seed)
-    mg, sg = H_chunks // 4, H_chunks
+    mg, sg = H_chunks // P, H_chunks // S
     word = 0
     done = {}                       # (row pair, chunk) -> launch
     rows_of = {"main": set(), "side": set()}
@@ -65,9 +67,9 @@ def run(R, H_chunks, n_main, n_side, reserve, seed, mistake=None):
             continue                    # the swap failed: read again
         word = new
         if role == "main":
-            row, chunks = unit // mg, [4 * (unit % mg) + k for k in range(4)]
+            row, chunks = unit // mg, [P * (unit % mg) + k for k in range(P)]
         else:
-            row, chunks = R - 1 - unit // sg, [unit % sg]
+            row, chunks = R - 1 - unit // sg, [S * (unit % sg) + k for k in range(S)]
             a_rows = ((word & 0xFFFFFFFF) + mg - 1) // mg
             if unit % sg == 0:
                 assert row - a_rows >= reserve or mistake, "side began a row pair within the reserve"
@@ -82,17 +84,19 @@ def run(R, H_chunks, n_main, n_side, reserve, seed, mistake=None):
     return rows_of
 
 
-@pytest.mark.parametrize("R,H_chunks,n_main,n_side,reserve", [
-    (256, 4, 15, 16, 19),     # the long workload's grad_input pass (reserve x0.5)
-    (689, 4, 15, 16, 38),     # its grad_W pass
-    (65, 4, 15, 16, 38),      # the GPU test shape
-    (47, 8, 15, 16, 10),      # two H groups per main unit
-    (40, 4, 3, 1, 1),         # minimal reserve
-    (45, 4, 15, 16, 100),     # a reserve the side can never meet: main does everything
+@pytest.mark.parametrize("R,H_chunks,P,S,n_main,n_side,reserve", [
+    (256, 4, 4, 2, 15, 8, 11),     # the long workload's grad_input pass (two-pair side clusters)
+    (689, 4, 4, 2, 15, 8, 23),     # its grad_W pass
+    (65, 4, 4, 2, 15, 8, 23),      # the GPU test shape
+    (256, 4, 4, 1, 15, 16, 19),    # single-pair side clusters
+    (47, 8, 4, 2, 15, 8, 10),      # two H groups per main unit
+    (1001, 9, 3, 1, 23, 7, 40),    # the rule with three-pair main clusters and single-pair side clusters
+    (40, 4, 4, 2, 3, 1, 1),        # minimal reserve
+    (45, 4, 4, 2, 15, 8, 100),     # a reserve the side can never meet: main does everything
 ])
-def test_work_queue_covers_every_unit_once(R, H_chunks, n_main, n_side, reserve):
+def test_work_queue_covers_every_unit_once(R, H_chunks, P, S, n_main, n_side, reserve):
     for seed in range(20):
-        rows = run(R, H_chunks, n_main, n_side, reserve, seed)
+        rows = run(R, H_chunks, n_main, n_side, reserve, seed, P=P, S=S)
         if reserve >= R:
             assert not rows["side"]
 
@@ -101,4 +105,4 @@ def test_work_queue_covers_every_unit_once(R, H_chunks, n_main, n_side, reserve)
 def test_work_queue_planted_mistakes_are_caught(mistake):
     with pytest.raises(AssertionError):
         for seed in range(20):
-            run(256, 4, 15, 16, 19, seed, mistake)
+            run(256, 4, 15, 8, 11, seed, mistake, P=4, S=2)
