@@ -42,10 +42,11 @@ KERNELS_PER_STEP = 5  # lse_partial, lse_merge, loss_reduce, dgrad(grad_input), 
 KERNELS_PER_STEP_ONLINE = 9
 
 
-def pairs_per_cluster(h_chunks: int, n_blocks: int) -> int:
+def pairs_per_cluster(h_chunks: int, n_blocks: int, side: bool) -> int:
     """CTA pairs per cluster of an exact gradient pass, as the library picks them (four when the 256-wide
-    H chunks divide by 4 and a unit runs over at least 64 column blocks, else two, three or one)."""
-    if h_chunks % 4 == 0 and n_blocks >= 64:
+    H chunks divide by 4 and a unit runs over at least 64 column blocks, or at least 16 when the pass ran
+    with side clusters; else two, three or one)."""
+    if h_chunks % 4 == 0 and (n_blocks >= 64 or (side and n_blocks >= 16)):
         return 4
     return 2 if h_chunks % 2 == 0 else 3 if h_chunks % 3 == 0 else 1
 
@@ -53,15 +54,16 @@ def pairs_per_cluster(h_chunks: int, n_blocks: int) -> int:
 def pass_tflops(w, passes, queues):
     """Algorithmic (logits + one GEMM, 4*BT*V*H) and executed TFLOP/s of the two gradient passes of the
     default flow.  Executed counts the logits once per cluster that covers a row block: h_chunks / P times
-    per row block (P pairs per cluster), and h_chunks times for the row blocks the side clusters took."""
+    per row block (P pairs per cluster), and h_chunks / 2 times for the row blocks the two-pair side
+    clusters took (each of their units covers two H chunks)."""
     h_chunks = -(-w.H // 256)
     out = {}
     for name, rows, cols, q in (("dgrad_grad_input_online", w.BT, w.V, queues[0]),
                                 ("dgrad_grad_W", w.V, w.BT, queues[1])):
         rp = -(-rows // 256)
-        P = pairs_per_cluster(h_chunks, -(-cols // 256))
-        side_rp = (q >> 32) // h_chunks
-        g1 = ((rp - side_rp) * (h_chunks // P) + side_rp * h_chunks) / rp
+        P = pairs_per_cluster(h_chunks, -(-cols // 256), (q >> 32) > 0)
+        side_rp = (q >> 32) // (h_chunks // 2) if P == 4 else 0
+        g1 = ((rp - side_rp) * (h_chunks // P) + side_rp * (h_chunks // 2)) / rp
         gemm = 2.0 * w.BT * w.V * w.H
         sec = passes[name] * 1e-3
         out[name] = {"algorithmic": 2 * gemm / sec / 1e12, "executed": (g1 + 1) * gemm / sec / 1e12,

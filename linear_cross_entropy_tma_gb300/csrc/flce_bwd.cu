@@ -1572,8 +1572,14 @@ dgrad_both_kernel(const __grid_constant__ CUtensorMap tm_hidden, const __grid_co
 // too much on shorter units (a grad_W pass over 4096 tokens has 16 blocks per unit).  Measured at
 // BT = 65535, H = 1024, V = 176245: 83.9 ms per step against 91.7 with two pairs.
 constexpr int kFourPairsMinBlocks = 64;
+// ... or at least this many when the pass runs persistent with side clusters (launch_corun), which take
+// up what the fill costs the shorter units: qwen3's grad_W pass (16 blocks per unit) 2.75 ms with four
+// pairs and side clusters against 2.85 with two pairs.
+constexpr int kFourPairsMinBlocksSide = 16;
 // dS half-slots per CTA with four pairs
 constexpr int kFourPairSlots = 4;
+// Persistent scheduling with side clusters (launch_corun) needs at least this many waves of main units.
+constexpr int kCoRunMinWaves = 3;
 
 // Pairs per cluster: 4 when allowed (see above) and the number of 256-wide H chunks divides by 4, else 2
 // when it is even, else 3 when it divides by 3, else 1.
@@ -1632,6 +1638,16 @@ PairParams make_pair_params(const DgPairArgs& a, int* h_chunks) {
 }
 
 int row_pairs_of(const PairParams& p) { return (p.n_rows + 2 * kTileM - 1) / (2 * kTileM); }
+
+// Whether a pass that make_pair_params gave two pairs (units of kFourPairsMinBlocksSide ..
+// kFourPairsMinBlocks - 1 column blocks) takes four instead: when its H chunks divide by 4 and it will
+// run persistent with side clusters (launch_corun's conditions; res4: resident 8-CTA clusters, 0 unknown).
+bool four_pairs_with_side(const PairParams& p, int h_chunks, int splits_option, const DgPairArgs& a, int res4) {
+  const int n_blocks = (p.n_cols + kPN - 1) / kPN;
+  return p.P == 2 && h_chunks % 4 == 0 && !(p.filter_eps > 0.f) && a.work_q != nullptr && splits_option == 0 &&
+         n_blocks >= kFourPairsMinBlocksSide && res4 > 0 &&
+         row_pairs_of(p) * (h_chunks / 4) >= kCoRunMinWaves * res4;
+}
 
 cudaLaunchConfig_t cluster_config(dim3 grid, size_t smem, int P, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
@@ -1731,7 +1747,6 @@ int device_sm_count() {
 // serialisation: it starts once every main CTA is running, and completes after the main launch.  Taken
 // when the pass has a queue word, the resident count is known and there are at least kCoRunMinWaves waves
 // of main units; otherwise nothing is launched (*launched = false).
-constexpr int kCoRunMinWaves = 3;
 // the side launch's reserve (see launch_corun) in quarters of the modelled one, per pass: measured at the
 // long workload, x0.5 / x0.75 / x1 / x1.25 gave 37.8 / 37.8 / 39.9 / 39.9 ms for the grad_input pass and
 // 40.5 / 40.6 / 40.0 / 40.3 ms for the grad_W pass
@@ -1801,6 +1816,16 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   int h_chunks = 0;
   PairParams p = make_pair_params<kVocabRows>(a, &h_chunks);
   const bool filt = p.filter_eps > 0.f;
+  static int res4 = 0;   // resident 8-CTA clusters of this pass's four-pair kernel
+  if (res4 == 0 && !filt) {
+    auto k4 = dgrad_pair_kernel<kVocabRows, false, kFourPairSlots>;
+    const size_t s4 = pair_smem_bytes<kVocabRows, false, kFourPairSlots>();
+    if (cudaFuncSetAttribute(k4, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s4)) == cudaSuccess)
+      res4 = resident_clusters(k4, s4, 4, stream);
+    else
+      (void)cudaGetLastError();
+  }
+  if (four_pairs_with_side(p, h_chunks, kVocabRows ? a.token_splits : 0, a, res4)) p.P = 4;
   const bool four = p.P == 4;   // (exact passes only)
   const size_t smem = filt   ? pair_smem_bytes<kVocabRows, true>()
                       : four ? pair_smem_bytes<kVocabRows, false, kFourPairSlots>()
@@ -1813,8 +1838,6 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   const int rp = row_pairs_of(p);
   const int nt = (p.n_cols + kPN - 1) / kPN;
   if (four && !filt) {
-    static int res4 = 0;
-    if (res4 == 0) res4 = resident_clusters(kern, smem, 4, stream);
     bool launched = false;
     e = launch_corun(dgrad_pair_kernel<kVocabRows, false, kFourPairSlots, 1, true>, smem,
                      dgrad_pair_kernel<kVocabRows, false, 2, 4, true>, pair_smem_bytes<kVocabRows, false>(), res4, rows,
@@ -1855,13 +1878,22 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   p.vs_stat = a.vs_stat;
   p.vs_o = a.vs_o;
   p.vs_count = a.vs_count;
+  static int slots_of[kMaxPairs + 1] = {};
+  if (slots_of[4] == 0) {
+    auto k4 = dgrad_online_kernel<kFourPairSlots>;
+    const size_t s4 = pair_smem_bytes<false, false, kFourPairSlots>();
+    if (cudaFuncSetAttribute(k4, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s4)) == cudaSuccess)
+      slots_of[4] = resident_clusters(k4, s4, 4, stream);
+    else
+      (void)cudaGetLastError();
+  }
+  if (four_pairs_with_side(p, h_chunks, a.vocab_splits, a, slots_of[4])) p.P = 4;
   const bool four = p.P == 4;
   const size_t smem = four ? pair_smem_bytes<false, false, kFourPairSlots>() : pair_smem_bytes<false, false>();
   auto kern = four ? dgrad_online_kernel<kFourPairSlots> : dgrad_online_kernel<2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int rp = row_pairs_of(p);
-  static int slots_of[kMaxPairs + 1] = {};
   if (slots_of[p.P] == 0) slots_of[p.P] = resident_clusters(kern, smem, p.P, stream);
   if (four) {
     bool launched = false;

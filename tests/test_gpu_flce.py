@@ -243,6 +243,27 @@ def test_flce_persistent_with_side_clusters(flce):
     assert out["loss"].item() == plain["loss"].item()
 
 
+def test_flce_short_units_four_pairs_with_side_clusters(flce):
+    """A grad_W pass of short units (17 token blocks, under the 64 that four pairs otherwise need) with
+    enough vocabulary row pairs (47) runs four pairs per cluster, persistent, with side clusters: against
+    the oracle, and against the same pass with one two-pair cluster per unit (the grad_input pass
+    unsplit in both, so that both grad_W passes read the same statistics)."""
+    import torch
+    BT, H, V = 4100, 1024, 12000
+    d = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(1, BT - 1), seed=47)
+    out = _run(flce, d, vocab_splits=1)
+    assert out["status"] == 0
+    assert flce.read_side_launches(out["workspace"]) == 1, "the grad_W pass did not run with side clusters"
+    _check_full(out, d)
+    plain = _run(flce, d, vocab_splits=1, token_splits=1)
+    assert plain["status"] == 0 and flce.read_side_launches(plain["workspace"]) == 0
+    assert torch.equal(out["grad_input"], plain["grad_input"])
+    # (four pairs against two: the same GEMM1 K order and GEMM2 block order; grad_bias adds the pairs'
+    # partial sums in another grouping, so it is compared within the parity bound)
+    assert torch.equal(out["grad_W"], plain["grad_W"])
+    assert_grad_close(out["grad_bias"].cpu().numpy(), plain["grad_bias"].cpu().numpy().astype(np.float64), "grad_bias")
+
+
 def test_flce_persistent_side_clusters_options(flce):
     # per-token upstream gradients and losses, entropy (the owner-class sums of the side pairs) and
     # accumulation, with the side clusters
