@@ -243,6 +243,23 @@ def test_flce_persistent_with_side_clusters(flce):
     assert out["loss"].item() == plain["loss"].item()
 
 
+def test_flce_persistent_with_side_clusters_sorted_vocab(flce):
+    # the vocabulary sort (its row permutation applied by the grad_W pass's epilogue) with both passes
+    # persistent and side clusters: against the oracle, and bit for bit against the sorted call with one
+    # cluster per unit
+    import torch
+    BT, H, V = PERSISTENT_SHAPE
+    d = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(5,), seed=53)
+    out = _run(flce, d, sort_vocab=True)
+    assert out["status"] == 0
+    assert flce.read_side_launches(out["workspace"]) == 2
+    _check_full(out, d)
+    plain = _run(flce, d, sort_vocab=True, vocab_splits=1, token_splits=1)
+    assert plain["status"] == 0 and flce.read_side_launches(plain["workspace"]) == 0
+    for k in ("grad_input", "grad_W", "grad_bias"):
+        assert torch.equal(out[k], plain[k]), f"{k} differs from one cluster per unit"
+
+
 def test_flce_short_units_four_pairs_with_side_clusters(flce):
     """A grad_W pass of short units (17 token blocks, under the 64 that four pairs otherwise need) with
     enough vocabulary row pairs (47) runs four pairs per cluster, persistent, with side clusters: against
