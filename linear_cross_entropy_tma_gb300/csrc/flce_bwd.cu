@@ -73,12 +73,6 @@ constexpr int side_pairs_for(int P) { return P == 4 ? 2 : 1; }
 // b - P - 2, so a ring of more than P + 2 blocks is never overwritten before every CTA has read it.
 constexpr int kFlagRing = 8;
 static_assert(kFlagRing >= kMaxPairs + 2, "the skip-verdict ring must outlast P + 2 blocks");
-// Order of a step's tensor work: 0 = GEMM2 half 0, half 1, then the GEMM1 share; 1 = the GEMM1 share
-// first; 2 = GEMM2 half 0, half of the share, GEMM2 half 1, the rest of the share.
-constexpr int kStepOrder = 0;
-// dS hand-over to the other pairs: 0 = one lane per warp issues cp.async.bulk copies shared -> peer shared
-// (TMA unit), 1 = every lane stores 16-byte pieces with st.async (load/store path), coalesced.
-constexpr int kDsHandOver = 1;
 constexpr uint32_t kBox = kTileM * kBK * 2;   // 16 KiB: a 128-row x 64-column bf16 box
 constexpr uint32_t kStage = 2 * kBox;
 constexpr uint32_t kHalfBytes = 2 * kBox;     // one 128-column half of a dS block (per CTA)
@@ -590,7 +584,6 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         const bool has_g1 = g.block >= 0 && g.block < nt;
         const int kb0 = has_g1 ? share_begin(g.prog, nkb, P) : 0;
         const int kb1 = has_g1 ? share_begin(g.prog + 1, nkb, P) : 0;
-        const int kbm = kStepOrder == 2 ? (kb0 + kb1) / 2 : kb1;
         auto load_stats = [&]() {
           // grad_W pass: the statistics of the owned block whose last GEMM1 share this step loads, into the
           // single slot once the epilogue has turned the previous owned block into dS (stats are padded to a
@@ -620,13 +613,11 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
             next();
           }
         };
-        if (kStepOrder == 1) load_gemm1(kb0, kb1);
+        // a step's tensor work, in the MMA issuer's order: GEMM2 of half 0 and half 1, then the GEMM1 share
         load_gemm2(s, 0);
-        if (kStepOrder == 2) load_gemm1(kb0, kbm);
         load_gemm2(s, 1);
         load_stats();
-        if (kStepOrder == 0) load_gemm1(kb0, kb1);
-        if (kStepOrder == 2) load_gemm1(kbm, kb1);
+        load_gemm1(kb0, kb1);
       }
       if (ok) {
         // every stage's last release (an MMA commit, multicast to both CTAs of the pair) has arrived
@@ -715,7 +706,6 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         const bool has_g1 = g.block >= 0 && g.block < nt;
         const int kb0 = has_g1 ? share_begin(g.prog, nkb, P) : 0;
         const int kb1 = has_g1 ? share_begin(g.prog + 1, nkb, P) : 0;
-        const int kbm = kStepOrder == 2 ? (kb0 + kb1) / 2 : kb1;
         bool first = true;
         auto gemm1 = [&](int kb_begin, int kb_end) {
           if (!ok || !has_g1) return;
@@ -744,12 +734,9 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
             advance();
           }
         };
-        if (kStepOrder == 1) gemm1(kb0, kb1);
         gemm2(s, 0);
-        if (kStepOrder == 2) gemm1(kb0, kbm);
         gemm2(s, 1);
-        if (kStepOrder == 0) gemm1(kb0, kb1);
-        if (kStepOrder == 2) gemm1(kbm, kb1);
+        gemm1(kb0, kb1);
         if (ok && has_g1 && g.prog == P - 1) {
           mma_commit_mc(&sm.s_full, pair_mask);
           ++u;
@@ -1002,51 +989,31 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       // A verdict wait that gave up sends the data (the kernel is winding down by then).
       bool send = true;
       if (filt && lane == 0) send = filter_verdict(sm, j, hh, abort) != 1;
-      if (kDsHandOver == 1) {
-        // the warp's 32 rows are two contiguous 4 KB runs (one per 64-column box); each lane moves 16-byte
-        // pieces of them, so that every store instruction writes 512 consecutive bytes of the peer's slot
-        send = __shfl_sync(0xffffffffu, send, 0);
-        const uint8_t* const src = sm.ds[slot] + static_cast<uint32_t>(qq) * 4096u;
-        for (int pp = 0; pp < P && ok; ++pp) {
-          if (pp == pr) continue;
-          const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
-          const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[slot]), dst_rank);
-          if (must_wait && !__all_sync(0xffffffffu, mbar_wait_cluster(&sm.ds_free[slot][pp], fpar, abort))) {
-            ok = false;
-            break;
-          }
-          if (send) {
-            const uint32_t dst = mapa_shared(smem_u32(src), dst_rank);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const uint32_t off = static_cast<uint32_t>(i >> 3) * kBox + static_cast<uint32_t>(i & 7) * 512u +
-                                   static_cast<uint32_t>(lane) * 16u;
-              st_async_v4(dst + off, *reinterpret_cast<const uint4*>(src + off), bar);
-            }
-          } else if (lane == 0) {
-            mbar_complete_tx_cluster(bar, 2u * 4096u);
-          }
+      // the warp's 32 rows are two contiguous 4 KB runs (one per 64-column box); each lane moves 16-byte
+      // pieces of them, so that every store instruction writes 512 consecutive bytes of the peer's slot
+      send = __shfl_sync(0xffffffffu, send, 0);
+      const uint8_t* const src = sm.ds[slot] + static_cast<uint32_t>(qq) * 4096u;
+      for (int pp = 0; pp < P && ok; ++pp) {
+        if (pp == pr) continue;
+        const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
+        const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[slot]), dst_rank);
+        if (must_wait && !__all_sync(0xffffffffu, mbar_wait_cluster(&sm.ds_free[slot][pp], fpar, abort))) {
+          ok = false;
+          break;
         }
-      } else if (lane == 0) {
-        // this warp's 32 rows of both 64-column boxes to the other pairs' CTAs with the same rows
-        uint8_t* const src = sm.ds[slot] + static_cast<uint32_t>(qq) * 4096u;
-        for (int pp = 0; pp < P && ok; ++pp) {
-          if (pp == pr) continue;
-          const uint32_t dst_rank = static_cast<uint32_t>(2 * pp) + q;
-          const uint32_t bar = mapa_shared(smem_u32(&sm.rx_full[slot]), dst_rank);
-          if (must_wait && !mbar_wait_cluster(&sm.ds_free[slot][pp], fpar, abort)) {
-            ok = false;
-            break;
+        if (send) {
+          const uint32_t dst = mapa_shared(smem_u32(src), dst_rank);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t off = static_cast<uint32_t>(i >> 3) * kBox + static_cast<uint32_t>(i & 7) * 512u +
+                                 static_cast<uint32_t>(lane) * 16u;
+            st_async_v4(dst + off, *reinterpret_cast<const uint4*>(src + off), bar);
           }
-          if (send) {
-            bulk_copy_to_peer(mapa_shared(smem_u32(src), dst_rank), src, 4096u, bar);
-            bulk_copy_to_peer(mapa_shared(smem_u32(src + kBox), dst_rank), src + kBox, 4096u, bar);
-          } else {
-            mbar_complete_tx_cluster(bar, 2u * 4096u);
-          }
+        } else if (lane == 0) {
+          mbar_complete_tx_cluster(bar, 2u * 4096u);
         }
       }
-      // (lane 0 alone may have given up in the bulk-copy form: every lane takes the same exit)
+      // (every lane takes the same exit)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       // this warp's rows of the slot are written here and on their way to the other pairs: one of the 8

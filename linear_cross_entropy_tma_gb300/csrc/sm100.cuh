@@ -297,16 +297,6 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) 
 }
 __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) { mma_commit_mc(bar, static_cast<uint16_t>(3)); }
 
-// Bulk copy from this CTA's shared memory into another CTA's shared memory of the cluster (both
-// given as offsets: the destination and its mbarrier as shared::cluster addresses); the byte count
-// completes on the destination CTA's mbarrier.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void* src_local, uint32_t bytes,
-                                                  uint32_t bar_cluster) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst_cluster), "r"(smem_u32(src_local)), "r"(bytes), "r"(bar_cluster)
-               : "memory");
-}
-
 // Asynchronous 16-byte store into another CTA's shared memory (a shared::cluster address); its byte count
 // completes on that CTA's mbarrier (also a shared::cluster address).  Issued by any thread, it goes through
 // the SM's load/store path, not the TMA unit.
