@@ -538,7 +538,9 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     d = widened(wl.make_fused_inputs(w))
-    per_step = 64
+    # 512 tokens a step (about 2.5 s of the oracle on 16 cores at the long workload): enough that its fixed
+    # cost per call (the zeroed fp64 grad_W, V x H) is small beside the per-token work, as in cpu_baseline
+    per_step = min(512, max(1, w.BT))
     for k in range(args.warmup):
         time_oracle_tokens(w, d, per_step, offset=(k * per_step) % max(1, w.BT - per_step))
     times = []
