@@ -262,11 +262,12 @@ def test_flce_persistent_with_side_clusters_sorted_vocab(flce):
 
 def test_flce_short_units_four_pairs_with_side_clusters(flce):
     """A grad_W pass of short units (17 token blocks, under the 64 that four pairs otherwise need) with
-    enough vocabulary row pairs (47) runs four pairs per cluster, persistent, with side clusters: against
+    enough vocabulary row pairs (51: three waves of 15, or of 16, resident 8-CTA clusters) runs four pairs
+    per cluster, persistent, with side clusters: against
     the oracle, and against the same pass with one two-pair cluster per unit (the grad_input pass
     unsplit in both, so that both grad_W passes read the same statistics)."""
     import torch
-    BT, H, V = 4100, 1024, 12000
+    BT, H, V = 4100, 1024, 13000
     d = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(1, BT - 1), seed=47)
     out = _run(flce, d, vocab_splits=1)
     assert out["status"] == 0
