@@ -51,23 +51,27 @@ def pairs_per_cluster(h_chunks: int, n_blocks: int, side: bool) -> int:
     return 2 if h_chunks % 2 == 0 else 3 if h_chunks % 3 == 0 else 1
 
 
-def pass_tflops(w, passes, queues):
+def pass_tflops(w, passes, queues, single_units):
     """Algorithmic (logits + one GEMM, 4*BT*V*H) and executed TFLOP/s of the two gradient passes of the
     default flow.  Executed counts the logits once per cluster that covers a row block: h_chunks / P times
-    per row block (P pairs per cluster), and h_chunks / 2 times for the row blocks the two-pair side
-    clusters took (each of their units covers two H chunks)."""
+    per row block (P pairs per cluster), once per side unit (two H chunks) the two-pair side clusters
+    took, and twice per side unit the single-pair clusters took (one chunk at a time)."""
     h_chunks = -(-w.H // 256)
     out = {}
-    for name, rows, cols, q in (("dgrad_grad_input_online", w.BT, w.V, queues[0]),
-                                ("dgrad_grad_W", w.V, w.BT, queues[1])):
+    for name, rows, cols, q, su in (("dgrad_grad_input_online", w.BT, w.V, queues[0], single_units[0]),
+                                    ("dgrad_grad_W", w.V, w.BT, queues[1], single_units[1])):
         rp = -(-rows // 256)
-        P = pairs_per_cluster(h_chunks, -(-cols // 256), (q >> 32) > 0)
-        side_rp = (q >> 32) // (h_chunks // 2) if P == 4 else 0
-        g1 = ((rp - side_rp) * (h_chunks // P) + side_rp * (h_chunks // 2)) / rp
+        side_units = q >> 32
+        P = pairs_per_cluster(h_chunks, -(-cols // 256), side_units > 0)
+        if P != 4:
+            side_units = su = 0
+        side_rp = side_units // (h_chunks // 2)
+        g1 = ((rp - side_rp) * (h_chunks // P) + (side_units - su) + 2 * su) / rp
         gemm = 2.0 * w.BT * w.V * w.H
         sec = passes[name] * 1e-3
         out[name] = {"algorithmic": 2 * gemm / sec / 1e12, "executed": (g1 + 1) * gemm / sec / 1e12,
-                     "logits_computed_per_row_block": g1, "pairs_per_cluster": P, "side_row_blocks": side_rp}
+                     "logits_computed_per_row_block": g1, "pairs_per_cluster": P, "side_row_blocks": side_rp,
+                     "single_pair_units": su}
     return out
 
 
@@ -242,6 +246,11 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
     # the side clusters that took work (both passes)
     side_launches = flce.read_side_launches(ws)
     side_clusters = flce.read_side_clusters(ws)
+    # the same for the single-pair clusters on the SMs where no side cluster finds room, and the units
+    # (row pair, two H chunks) they took per pass
+    single_launches = flce.read_single_launches(ws)
+    single_clusters = flce.read_single_clusters(ws)
+    single_units = flce.read_single_units(ws)
     # the two passes' work queues (workspace header bytes 40 and 48: main units | side units << 32), for the
     # executed GEMM1 work of passes that ran side clusters
     queues = [int(x) for x in ws[40:56].cpu().view(torch.int64).tolist()]
@@ -406,8 +415,8 @@ def bench_fused(w: wl.FusedWorkload, steps: int, warmup: int, world: int, local:
                 e2e_clocks=e2e_clocks,
                 e2e_serial_ms=e2e_serial_ms, h2d=h2d, d2h=d2h, workspace_bytes=ws.numel(), filter=filt,
                 split_units=split_units, token_split_units=token_split_units, side_launches=side_launches,
-                side_clusters=side_clusters,
-                queues=queues, graph_ms=graph_ms)
+                side_clusters=side_clusters, single_launches=single_launches, single_clusters=single_clusters,
+                single_units=single_units, queues=queues, graph_ms=graph_ms)
 
 
 def bench_workload(w: wl.FusedWorkload, steps: int, warmup: int, local: int, peaks: dict, oracle_rows: int | None):
@@ -654,16 +663,19 @@ def main():
                           "frac_of_sustained": step_tflops / peak_tf, "frac_of_burst": step_tflops / peaks["bf16_tflops"],
                           "convention": "8*BT*V*H per fused forward+backward"},
         "pass_ms": passes,
-        "pass_tflops": pass_tflops(w, passes, r["queues"]) if online else None,
+        "pass_tflops": pass_tflops(w, passes, r["queues"], r["single_units"]) if online else None,
         "gpu_launches": ((KERNELS_PER_STEP_ONLINE + (1 if r["split_units"] else 0)) if online
                          else KERNELS_PER_STEP - 1 if merged else KERNELS_PER_STEP)
-                        * args.steps + (args.steps if r["token_split_units"] else 0) + r["side_launches"] * args.steps,
+                        * args.steps + (args.steps if r["token_split_units"] else 0)
+                        + (r["side_launches"] + r["single_launches"]) * args.steps,
         "graph_replay": {"ms_per_step": r["graph_ms"], "tokens_per_s": world * w.BT / (r["graph_ms"] * 1e-3),
                          "note": "the same call captured once into a CUDA graph, replayed steps times"},
         "vocab_split_clusters": r["split_units"],
         "token_split_clusters": r["token_split_units"],
         "side_launches_per_step": r["side_launches"],
         "side_clusters_with_work_per_step": r["side_clusters"],
+        "single_pair_launches_per_step": r["single_launches"],
+        "single_pair_clusters_with_work_per_step": r["single_clusters"],
         "clocks": r["clocks"],
         "e2e": {"value": world * w.BT / (r["e2e_ms"] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"],

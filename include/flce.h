@@ -201,12 +201,17 @@ flce_status flce_fwd_bwd_timed(const uint16_t* hidden, const uint16_t* W, const 
  *                        least three waves of work units is scheduled instead as persistent 8-CTA
  *                        clusters that take units from a queue in the workspace header, plus a second
  *                        launch of 4-CTA clusters (two pairs), started by programmatic dependent launch,
- *                        on the SMs the 8-CTA clusters leave idle.  They take two 256-column H chunks of
- *                        the last row blocks at a time (computing those blocks' logits once per two
- *                        chunks) and stop early enough to finish with the 8-CTA clusters.  No unit is
- *                        split then, and the results are bit for bit those of one 8-CTA cluster per unit.
- *                        Each pass that did this adds 1 to the word at byte 56 of the workspace; the word
- *                        at byte 60 counts the side clusters that took work.
+ *                        on the SMs the 8-CTA clusters leave idle, and (grad_W pass) behind it a third
+ *                        launch of 2-CTA clusters (one pair) on the SMs where no 4-CTA cluster is placed.  Both take two
+ *                        256-column H chunks of the last row blocks at a time (the 4-CTA clusters
+ *                        computing those blocks' logits once per two chunks, the 2-CTA clusters once per
+ *                        chunk, one chunk after the other) and stop early enough to finish with the
+ *                        8-CTA clusters.  No unit is split then, and the results are bit for bit those of
+ *                        one 8-CTA cluster per unit.  Each pass that did this adds 1 to the word at byte
+ *                        56 of the workspace, and 1 to the word at byte 72 when it also launched 2-CTA
+ *                        clusters; the words at bytes 60 and 76 count the 4-CTA and 2-CTA clusters that
+ *                        took work, and those at bytes 64 and 68 the units the 2-CTA clusters took in the
+ *                        grad_input and the grad_W pass.
  *   token_splits         the same for the grad_W pass, whose clusters own vocabulary rows and run over
  *                        the tokens: 0 splits the row blocks of its last, partly filled wave into token
  *                        ranges (partial grad_W / grad_bias rows, added in order by a merge kernel), 1

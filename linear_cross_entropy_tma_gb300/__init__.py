@@ -16,6 +16,9 @@ from ._lib import (  # noqa: F401
     read_filter_skips,
     read_side_clusters,
     read_side_launches,
+    read_single_clusters,
+    read_single_launches,
+    read_single_units,
     read_token_split_units,
     read_vocab_split_units,
     workspace_size,

@@ -339,7 +339,7 @@ def read_token_split_units(workspace) -> int:
 
 
 def read_side_launches(workspace) -> int:
-    """Launches of side clusters (one or two pairs) that ran beside the persistent four-pair clusters in the last
+    """Launches of side clusters (two pairs) that ran beside the persistent four-pair clusters in the last
     flce_fwd_bwd on this workspace, one per pass that used them (the 32-bit word at byte 56; synchronises
     the device)."""
     import torch
@@ -353,6 +353,32 @@ def read_side_clusters(workspace) -> int:
     import torch
     torch.cuda.synchronize(workspace.device)
     return int(workspace[60:64].cpu().view(torch.int32).item())
+
+
+def read_single_launches(workspace) -> int:
+    """Launches of single-pair clusters that ran beside the persistent four-pair and side clusters in the
+    last flce_fwd_bwd on this workspace, one per pass that used them (the 32-bit word at byte 72;
+    synchronises the device)."""
+    import torch
+    torch.cuda.synchronize(workspace.device)
+    return int(workspace[72:76].cpu().view(torch.int32).item())
+
+
+def read_single_clusters(workspace) -> int:
+    """Single-pair clusters that took at least one unit in the last flce_fwd_bwd on this workspace, over
+    both passes (the 32-bit word at byte 76; synchronises the device)."""
+    import torch
+    torch.cuda.synchronize(workspace.device)
+    return int(workspace[76:80].cpu().view(torch.int32).item())
+
+
+def read_single_units(workspace) -> list:
+    """Units (one row pair, two H chunks) the single-pair clusters took in the last flce_fwd_bwd on this
+    workspace: [grad_input pass, grad_W pass] (the 32-bit words at bytes 64 and 68; synchronises the
+    device)."""
+    import torch
+    torch.cuda.synchronize(workspace.device)
+    return [int(x) for x in workspace[64:72].cpu().view(torch.int32).tolist()]
 
 
 def read_device_status(workspace, stream=None) -> int:

@@ -127,6 +127,9 @@ struct PairSmem {
   uint32_t tmem_base;
   int abort;
   int claim;                  // persistent clusters: the unit CTA 0 claimed for the whole cluster (-1: none)
+  // persistent clusters, thread 0 of CTA 0 only (kept here so that nothing stays live across the unit body):
+  // its last claim, the next one-chunk part of it (single-pair clusters), whether the cluster took a unit
+  int q_unit, q_sub, q_took;
 };
 constexpr size_t kSmemBudget = 232448;
 // The stage ring and the dS block need 1024-byte alignment (128-byte swizzle atoms).  A layout that fits
@@ -444,8 +447,8 @@ __device__ __forceinline__ PairSmem<kVocabRows, kFilter, kSlots>* pair_smem_of()
 // allocation as it was.)
 enum : int { kTmemOneUnit = 0, kTmemHeld = 1 };
 
-// kClasses = 4 in dgrad_pair_body: a pair of a side cluster (P = 1 or 2 pairs) keeps A = 4 / P running
-// sums, one per owner class it meets (its t-th block, j = pr + t P, belongs to class j mod 4 = pr + (t mod
+// kOwn = A > 1 in dgrad_pair_body: a pair of a cluster of P = 4 / A pairs keeps A running sums, one per
+// owner class of a four-pair cluster it meets (its t-th block, j = pr + t P, belongs to class j mod 4 = pr + (t mod
 // A) P), rotating them so that a0 always holds the current block's.  After its n_own blocks, a_i holds
 // slot (n_own - 1 + i) mod A; slot_sum returns slot s.  A slot that met no block holds 0.
 __device__ __forceinline__ float slot_sum(float a0, float a1, float a2, float a3, int s, int n_own, int A) {
@@ -458,16 +461,17 @@ __device__ __forceinline__ float slot_sum(float a0, float a1, float a2, float a3
 // One cluster's work: rows [256 row_pair, +256) (128 per CTA of each pair) and the H chunks of
 // group hgroup (P consecutive 256-wide chunks, one per pair).
 // Columns: blocks [jb, je) of 256 (all of them except for a vocabulary-split unit of the online pass, su >= 0).
-// kClasses = 4: a cluster of one or two pairs standing in for a cluster of four pairs, whose results it
-// reproduces bit for bit: the per-row sums that four pairs would keep apart (each over the blocks it owns,
-// j mod 4) are kept apart too and combined in the same order (the online pass's softmax sums, grad_bias).
-template <bool kVocabRows, bool kFilter, bool kOnline = false, int kSlots = 2, int kClasses = 1, int kTmem = 0>
+// kOwn = 2 or 4: a cluster of two pairs or one pair standing in for a cluster of four pairs, whose results
+// it reproduces bit for bit: the per-row sums that four pairs would keep apart (each over the blocks it
+// owns, j mod 4) are kept apart too (kOwn of them per pair) and combined in the same order (the online
+// pass's softmax sums, grad_bias).  kOwn = 1: no owner classes (P pairs, each keeping one sum).
+template <bool kVocabRows, bool kFilter, bool kOnline = false, int kSlots = 2, int kOwn = 1, int kTmem = 0>
 __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols,
                                                 const PairParams& p, uint32_t* __restrict__ status, int row_pair,
                                                 int hgroup, int jb = 0, int je = -1, int su = -1) {
   static_assert(!kOnline || (!kVocabRows && !kFilter), "the online form is a grad_input pass without the filter");
-  static_assert(kClasses == 1 || (kClasses >= 2 && kClasses <= kMaxPairs && !kFilter),
-                "owner classes: 1, or 2-4 for the exact passes (4 is the one launched)");
+  static_assert(kOwn == 1 || ((kOwn == 2 || kOwn == 4) && !kFilter),
+                "owner-class sums per pair: 1, or 2 / 4 (two-pair / single-pair clusters) for the exact passes");
   using Smem = PairSmem<kVocabRows, kFilter, kSlots>;
   constexpr int kStages = Smem::Cfg::kStages;
   // (run_units has checked the gate and the layout's alignment and allocated TMEM)
@@ -536,11 +540,11 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
-  // grad_W pass: this epilogue thread's grad_bias partial (its row, its half); with kClasses = 4, one per
+  // grad_W pass: this epilogue thread's grad_bias partial (its row, its half); with kOwn > 1, one per
   // owner-class slot (slot_sum)
   float gbias_out = 0.f, gbias_c1 = 0.f, gbias_c2 = 0.f, gbias_c3 = 0.f;
-  // owner classes a side pair meets (its cluster has side_pairs_for(kClasses) pairs)
-  constexpr int n_slots = kClasses > 1 ? kClasses / side_pairs_for(kClasses) : 1;
+  // owner classes a pair meets (its cluster has kMaxPairs / kOwn pairs)
+  constexpr int n_slots = kOwn;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------------------ TMA producer
@@ -818,7 +822,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       rc.y = row;
     }
     float gbias = 0.f;
-    // kClasses = 4: the running sums of the other owner-class slots; before this pair's t-th block,
+    // kOwn > 1: the running sums of the other owner-class slots; before this pair's t-th block,
     // on_lsum / on_tsum / gbias hold slot t mod n_slots and the k-th of these slot (t + k) mod n_slots
     float cl_l1 = 0.f, cl_l2 = 0.f, cl_l3 = 0.f, cl_t1 = 0.f, cl_t2 = 0.f, cl_t3 = 0.f;
     float cl_g1 = 0.f, cl_g2 = 0.f, cl_g3 = 0.f;
@@ -838,7 +842,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     }
     int u = 0;
     for (int j = pr; j < nt && ok; j += P, ++u) {
-      if (kClasses > 1 && j > pr) {
+      if (kOwn > 1 && j > pr) {
         if constexpr (n_slots == 4) {
           float t = on_lsum;
           on_lsum = cl_l1, cl_l1 = cl_l2, cl_l2 = cl_l3, cl_l3 = t;
@@ -846,13 +850,6 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
           on_tsum = cl_t1, cl_t1 = cl_t2, cl_t2 = cl_t3, cl_t3 = t;
           t = gbias;
           gbias = cl_g1, cl_g1 = cl_g2, cl_g2 = cl_g3, cl_g3 = t;
-        } else if constexpr (n_slots == 3) {
-          float t = on_lsum;
-          on_lsum = cl_l1, cl_l1 = cl_l2, cl_l2 = t;
-          t = on_tsum;
-          on_tsum = cl_t1, cl_t1 = cl_t2, cl_t2 = t;
-          t = gbias;
-          gbias = cl_g1, cl_g1 = cl_g2, cl_g2 = t;
         } else {
           float t = on_lsum;
           on_lsum = cl_l1, cl_l1 = t;
@@ -1037,7 +1034,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         }
       }
       if (ok) {
-        if (kClasses > 1) {
+        if (kOwn > 1) {
           // (the target logit is a maximum: any class may carry it)
           for (int sl = 0; sl < n_slots; ++sl)
             on_part[(pr + sl * P) * 2 + hh] = make_float4(slot_sum(on_lsum, cl_l1, cl_l2, cl_l3, sl, u, n_slots), on_zy,
@@ -1053,7 +1050,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
       if (ok) {
         float L = 0.f, zy = -INFINITY, T = 0.f;
-        for (int pp = 0; pp < (kClasses > 1 ? kClasses : P); ++pp)
+        for (int pp = 0; pp < (kOwn > 1 ? kMaxPairs : P); ++pp)
           for (int h2 = 0; h2 < 2; ++h2) {
             const float4 v = __ldcg(on_part + pp * 2 + h2);
             L += v.x;
@@ -1154,8 +1151,8 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
         }
       }
     }
-    gbias_out = kClasses > 1 ? slot_sum(gbias, cl_g1, cl_g2, cl_g3, 0, u, n_slots) : gbias;
-    if (kClasses > 1) {
+    gbias_out = kOwn > 1 ? slot_sum(gbias, cl_g1, cl_g2, cl_g3, 0, u, n_slots) : gbias;
+    if (kOwn > 1) {
       gbias_c1 = slot_sum(gbias, cl_g1, cl_g2, cl_g3, 1, u, n_slots);
       gbias_c2 = slot_sum(gbias, cl_g1, cl_g2, cl_g3, 2, u, n_slots);
       gbias_c3 = slot_sum(gbias, cl_g1, cl_g2, cl_g3, 3, u, n_slots);
@@ -1172,7 +1169,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     if (warp < kEpiWarps) {
       const int rl = (warp & 3) * 32 + lane;
       st_shared_cluster_f32(mapa_shared(smem_u32(gb_gather + (pr * 2 + (warp >> 2)) * kTileM + rl), q), gbias_out);
-      if (kClasses > 1) {
+      if (kOwn > 1) {
         // the other slots' classes: pr + s P
         const float gs[3] = {gbias_c1, gbias_c2, gbias_c3};
 #pragma unroll
@@ -1189,7 +1186,7 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
     const int row = r0 + rl;
     if (row < p.V) {
       float acc = 0.f;
-      for (int pp = 0; pp < (kClasses > 1 ? kClasses : P); ++pp)
+      for (int pp = 0; pp < (kOwn > 1 ? kMaxPairs : P); ++pp)
         acc += gb_gather[(pp * 2) * kTileM + rl] + gb_gather[(pp * 2 + 1) * kTileM + rl];
       if (su >= 0) {
         p.vs_gb[static_cast<size_t>(su) * 256 + static_cast<int>(q) * kTileM + rl] = acc;   // for dw_vmerge_kernel
@@ -1249,19 +1246,25 @@ __device__ __forceinline__ Unit unit_of(const UnitPlan& plan, int c) {
 // pairs take whole units (row pair x H group) from the bottom of the row pairs; a second launch of
 // side clusters of S pairs (the side launch, on the SMs the main launch leaves idle; S = side_pairs_for(P))
 // takes units of one row pair and S 256-wide H chunks from the top, computing that row pair's logits once
-// per S chunks.  One 64-bit
-// word holds both counts (main units claimed | side units claimed << 32), so that a row pair is never
-// split between the two.  The side opens a new row pair only while the main launch has at least `reserve`
-// row pairs left: enough to keep it busy while the side finishes that row pair.
-enum : int { kRoleMain = 1, kRoleSide = 2 };
+// per S chunks; a third launch of single-pair clusters (on the SMs where no side cluster finds room) takes
+// the same units as the side launch, from the same count, and runs each as S one-chunk units in turn,
+// computing the logits once per chunk; it takes a unit only with its own reserve to spare, also one that
+// continues a row pair a side cluster began, and stops at the first it cannot take.  One 64-bit word holds both counts (main units claimed | side
+// units claimed << 32), so that a row pair is never split between the main launch and the others.  The
+// side and single-pair clusters open a new row pair only while the main launch has at least `reserve`
+// row pairs left (each launch its own): enough to keep it busy while they finish that row pair.
+enum : int { kRoleMain = 1, kRoleSide = 2, kRoleSingle = 3 };
 struct WorkQueue {
   unsigned long long* word;   // zeroed before the pass; null: one cluster per unit (blockIdx), no queue
   uint32_t* side_count;       // [2] side launches that ran, side clusters that took a unit (workspace
                               // header), or null
+  uint32_t* single_count;     // [2] the same for the single-pair launches, or null
+  uint32_t* single_units;     // this pass's units taken by single-pair clusters, or null
   int role;
   int row_pairs;
   int main_groups;            // H groups per row pair of a main unit (h_chunks / 4)
-  int side_groups;            // H chunks per row pair (one per side unit)
+  int side_groups;            // H groups per row pair of a side unit (h_chunks / S)
+  int side_chunks;            // S: H chunks per side unit
   int reserve;
 };
 
@@ -1280,8 +1283,11 @@ __device__ __forceinline__ int claim_unit(const WorkQueue& q) {
       if (a / q.main_groups >= q.row_pairs - b_rows) return -1;
       next = cur + 1ull;
     } else {
-      // (a row pair already begun is always finished; a new one only with `reserve` row pairs to spare)
-      if (b % q.side_groups == 0 && (q.row_pairs - 1 - b / q.side_groups) - a_rows < q.reserve) return -1;
+      // (side: a row pair already begun is always finished, a new one only with `reserve` row pairs to
+      // spare; single-pair: every unit only with its reserve to spare, which is at least the side's, so
+      // that a side cluster is always there to finish a row pair it began)
+      const bool check = q.role == kRoleSingle || b % q.side_groups == 0;
+      if (check && (q.row_pairs - 1 - b / q.side_groups) - a_rows < q.reserve) return -1;
       next = cur + (1ull << 32);
     }
     const unsigned long long seen = atomicCAS(q.word, cur, next);
@@ -1297,7 +1303,7 @@ __device__ __forceinline__ int claim_unit(const WorkQueue& q) {
 // every arrival on them consumed or ordered before its last cluster barrier.  A unit that gave up on a
 // wait stops the cluster.  (A template flag rather than a run-time one, so that the one-unit kernels keep
 // their register allocation.)
-template <bool kVocabRows, bool kFilter, bool kOnline, int kSlots, int kClasses, bool kQueue>
+template <bool kVocabRows, bool kFilter, bool kOnline, int kSlots, int kOwn, bool kQueue>
 __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols, const PairParams& p,
                                           uint32_t* __restrict__ status, const Unit& fixed, const UnitPlan& plan,
                                           const WorkQueue& wq) {
@@ -1310,7 +1316,7 @@ __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUte
   }
   if constexpr (!kQueue) {
     // (the body allocates and frees TMEM itself)
-    dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kClasses, kTmemOneUnit>(
+    dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kOwn, kTmemOneUnit>(
         tm_rows, tm_cols, p, status, fixed.row_pair, fixed.hgroup, fixed.jb, fixed.je, fixed.su);
   } else {
     auto& sm = *smp;
@@ -1318,38 +1324,53 @@ __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUte
       tmem_alloc_pair(&sm.tmem_base, kTmemCols);
       tmem_relinquish_pair();
     }
-    if (wq.role == kRoleMain) {
-      griddep_launch_dependents();   // the side launch may start on the SMs this one leaves free
-    } else if (blockIdx.x == 0 && threadIdx.x == 0 && wq.side_count != nullptr) {
-      atomicAdd(wq.side_count, 1u);
-    }
+    // the launch behind this one (side behind main, single-pair behind side) may start on the SMs left free
+    griddep_launch_dependents();
+    uint32_t* const counts = wq.role == kRoleSide ? wq.side_count : wq.role == kRoleSingle ? wq.single_count : nullptr;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && counts != nullptr) atomicAdd(counts, 1u);
     const uint32_t rank = cluster_ctarank();
-    bool took = false;
+    // a single-pair cluster runs each side unit it claims as side_chunks one-chunk units in turn (one call
+    // site of the body, so that the register allocation stays that of one unit); CTA 0 hands out
+    // claim x n_sub + part
+    const int n_sub = wq.role == kRoleSingle ? wq.side_chunks : 1;
+    if (rank == 0 && threadIdx.x == 0) {
+      sm.q_sub = 0;
+      sm.q_took = 0;
+    }
     for (;;) {
       if (rank == 0 && threadIdx.x == 0) {
-        int c = (*reinterpret_cast<volatile uint32_t*>(status) & kStatusTimeout) != 0u ? -1 : claim_unit(wq);
-        if (c == -2) {
-          atomicOr(status, kStatusInternal);
-          c = -1;
+        const int sub = sm.q_sub;
+        if (sub == 0) {
+          int cl = (*reinterpret_cast<volatile uint32_t*>(status) & kStatusTimeout) != 0u ? -1 : claim_unit(wq);
+          if (cl == -2) {
+            atomicOr(status, kStatusInternal);
+            cl = -1;
+          }
+          if (cl >= 0 && !sm.q_took && counts != nullptr) atomicAdd(counts + 1, 1u);
+          if (cl >= 0 && wq.role == kRoleSingle && wq.single_units != nullptr) atomicAdd(wq.single_units, 1u);
+          if (cl >= 0) sm.q_took = 1;
+          sm.q_unit = cl;
         }
-        if (c >= 0 && !took && wq.role == kRoleSide && wq.side_count != nullptr) atomicAdd(wq.side_count + 1, 1u);
-        took = took || c >= 0;
+        sm.q_sub = sub + 1 == n_sub ? 0 : sub + 1;
+        const int v = sm.q_unit < 0 ? -1 : sm.q_unit * n_sub + sub;
         for (int r = 0; r < 2 * p.P; ++r)
-          st_shared_cluster_u32(mapa_shared(smem_u32(&sm.claim), static_cast<uint32_t>(r)), static_cast<uint32_t>(c));
+          st_shared_cluster_u32(mapa_shared(smem_u32(&sm.claim), static_cast<uint32_t>(r)), static_cast<uint32_t>(v));
       }
       cluster_sync();
-      const int c = *reinterpret_cast<volatile int*>(&sm.claim);
-      if (c < 0) break;
-      const Unit u = wq.role == kRoleMain
-                         ? Unit{c / wq.main_groups, c % wq.main_groups, 0, plan.nt, -1}
-                         : Unit{wq.row_pairs - 1 - c / wq.side_groups, c % wq.side_groups, 0, plan.nt, -1};
-      dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kClasses, kTmemHeld>(tm_rows, tm_cols, p, status, u.row_pair,
-                                                                                 u.hgroup, u.jb, u.je, u.su);
+      const int v = *reinterpret_cast<volatile int*>(&sm.claim);
+      if (v < 0) break;
+      const int c = v / n_sub;
+      const Unit u = wq.role == kRoleMain ? Unit{c / wq.main_groups, c % wq.main_groups, 0, plan.nt, -1}
+                                          : Unit{wq.row_pairs - 1 - c / wq.side_groups,
+                                                 (c % wq.side_groups) * n_sub + v % n_sub, 0, plan.nt, -1};
+      dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kOwn, kTmemHeld>(tm_rows, tm_cols, p, status, u.row_pair,
+                                                                             u.hgroup, u.jb, u.je, u.su);
       // every CTA is done with the unit (and has read sm.claim) before the next claim is handed out
       cluster_sync();
     }
-    // a side grid completes only after the main grid beside it, so that what follows on the stream sees both
-    if (wq.role == kRoleSide) griddep_wait_primary();
+    // a side grid completes only after the main grid beside it, a single-pair grid only after the side grid
+    // (and so the main grid), so that what follows on the stream sees all of them
+    if (wq.role != kRoleMain) griddep_wait_primary();
     // (every CTA of the cluster has passed a cluster barrier after its last TMEM access)
     if ((threadIdx.x >> 5) == kMmaWarp) {
       tc_fence_after();
@@ -1359,23 +1380,23 @@ __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUte
 }
 
 // One gradient pass: without a queue, cluster blockIdx.x / 2P is work unit unit_of(plan, .); with one
-// (kQueue), a persistent cluster of the main or side launch (WorkQueue; the side launch's pairs with
-// kClasses = 4).
-template <bool kVocabRows, bool kFilter, int kSlots, int kClasses = 1, bool kQueue = false>
+// (kQueue), a persistent cluster of the main, side or single-pair launch (WorkQueue; the side launch's
+// pairs with kOwn = 2, the single-pair launch's with kOwn = 4).
+template <bool kVocabRows, bool kFilter, int kSlots, int kOwn = 1, bool kQueue = false>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_pair_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
                   const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan, const WorkQueue wq) {
   const Unit u = unit_of(plan, static_cast<int>(blockIdx.x) / (2 * p.P));
-  run_units<kVocabRows, kFilter, false, kSlots, kClasses, kQueue>(tm_rows, tm_cols, p, status, u, plan, wq);
+  run_units<kVocabRows, kFilter, false, kSlots, kOwn, kQueue>(tm_rows, tm_cols, p, status, u, plan, wq);
 }
 
 // The grad_input pass without a prior LSE pass: the same cluster layout as dgrad_pair_kernel<false>.
-template <int kSlots, int kClasses = 1, bool kQueue = false>
+template <int kSlots, int kOwn = 1, bool kQueue = false>
 __global__ void __launch_bounds__(kThreads, 1)
 dgrad_online_kernel(const __grid_constant__ CUtensorMap tm_rows, const __grid_constant__ CUtensorMap tm_cols,
                     const PairParams p, uint32_t* __restrict__ status, const UnitPlan plan, const WorkQueue wq) {
   const Unit u = unit_of(plan, static_cast<int>(blockIdx.x) / (2 * p.P));
-  run_units<false, false, true, kSlots, kClasses, kQueue>(tm_rows, tm_cols, p, status, u, plan, wq);
+  run_units<false, false, true, kSlots, kOwn, kQueue>(tm_rows, tm_cols, p, status, u, plan, wq);
 }
 
 // The vocabulary rows of token-split units of the grad_W pass: grad_W[row] = sum over parts, in order, of
@@ -1709,22 +1730,38 @@ int device_sm_count() {
 }
 
 // A pass with four pairs per cluster, run as persistent clusters of four pairs (one per resident slot)
-// plus, on the SMs those leave idle (8-CTA clusters do not tile every GPC), persistent side clusters
-// sharing its work queue (WorkQueue).  The side launch follows the main one with programmatic stream
-// serialisation: it starts once every main CTA is running, and completes after the main launch.  Taken
-// when the pass has a queue word, the resident count is known and there are at least kCoRunMinWaves waves
-// of main units; otherwise nothing is launched (*launched = false).
-// the side launch's reserve (see launch_corun) in quarters of the modelled one, per pass: measured at the
-// long workload, x0.5 / x0.75 / x1 / x1.25 gave 37.8 / 37.8 / 39.9 / 39.9 ms for the grad_input pass and
-// 40.5 / 40.6 / 40.0 / 40.3 ms for the grad_W pass
+// plus, on the SMs those leave idle (8-CTA clusters do not tile every GPC), persistent side clusters of
+// two pairs and single-pair clusters sharing its work queue (WorkQueue).  The side launch follows the main
+// one with programmatic stream serialisation: it starts once every main CTA is running, and completes
+// after the main launch; the single-pair launch follows the side launch in the same way.  Taken when the
+// pass has a queue word, the resident count is known and there are at least kCoRunMinWaves waves of main
+// units; otherwise nothing is launched (*launched = false).
+// The launches' reserves (see launch_corun) in quarters of the modelled ones, per pass.  Side clusters,
+// measured at the long workload: x0.5 / x0.75 / x1 / x1.25 gave 37.8 / 37.8 / 39.9 / 39.9 ms for the
+// grad_input pass and 40.5 / 40.6 / 40.0 / 40.3 ms for the grad_W pass (with single-pair side clusters);
+// with two-pair side clusters x0.25 / x0.5 (grad_input) and x0.75 / x1 / x1.25 (grad_W) were all within
+// 0.2 ms per step.  Single-pair clusters: x0.75 / x1 / x1.5 gave 36.94–36.98 / 36.93–36.98 / 37.64–37.81 ms
+// for the grad_W pass; 0 launches none, as for the grad_input pass, whose single-pair units (two chunks
+// over all the vocabulary blocks, ~12 ms each at the long workload) gained nothing: 36.95–37.27 ms with
+// x1 and x1.5 against 36.76–36.79 without them.
 constexpr int kReserveQuartersOnline = 2;
 constexpr int kReserveQuartersGradW = 4;
+constexpr int kReserveQuartersSingleOnline = 0;
+constexpr int kReserveQuartersSingleGradW = 4;
+// Side clusters that find no room beside the main clusters.  On the 152-SM GB300, 15 resident 8-CTA
+// clusters leave 32 SMs idle; clusters that hold their SMs for a fixed time, launched one behind the other
+// as here, showed room for 6 4-CTA clusters (two more start only once the 8-CTA clusters have finished)
+// and then for 4 2-CTA clusters on the last 8 SMs (two groups of four, in neither of which a 4-CTA cluster
+// is placed).  The single-pair launch starts only once every side CTA runs, so the side launch asks for
+// the ones that fit.  On another layout a side cluster that finds no room delays the single-pair clusters
+// to the end of the pass, where they find nothing left: the results are the same either way.
+constexpr int kSideUnplaced = 2;
 
-template <class MainKernel, class SideKernel>
-cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, size_t smem_side, int res_main,
-                         const CUtensorMap& rows, const CUtensorMap& cols, const PairParams& p, int h_chunks,
-                         int splits_option, int reserve_quarters, const DgPairArgs& a, cudaStream_t stream,
-                         bool* launched) {
+template <class MainKernel, class SideKernel, class SingleKernel>
+cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, SingleKernel kx, size_t smem_side,
+                         int res_main, const CUtensorMap& rows, const CUtensorMap& cols, const PairParams& p,
+                         int h_chunks, int splits_option, int reserve_quarters, int reserve_quarters_single,
+                         const DgPairArgs& a, cudaStream_t stream, bool* launched) {
   *launched = false;
   const int rp = row_pairs_of(p);
   const int P = p.P;
@@ -1735,10 +1772,13 @@ cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, size_t 
   // gained 1.5% but the grad_input pass, with four waves of long units, lost 17% against its split tail;
   // beside two-pair clusters (8 idle SMs) nothing was gained.)
   if (a.work_q == nullptr || splits_option != 0 || P != 4 || res_main <= 0 || main_groups < 1 ||
-      rp * main_groups < kCoRunMinWaves * res_main)
+      h_chunks % S != 0 || rp * main_groups < kCoRunMinWaves * res_main)
     return cudaSuccess;
-  const int side = (device_sm_count() - 2 * P * res_main) / (2 * S);   // side clusters
+  const int idle = device_sm_count() - 2 * P * res_main;
+  int side = idle / (2 * S) - kSideUnplaced;
+  if (side < 1) side = idle / (2 * S);
   if (side * S < 2) return cudaSuccess;
+  const int single = (idle - 2 * S * side) / 2;   // single-pair clusters
   cudaError_t e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_main));
   if (e != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_side))) !=
@@ -1746,18 +1786,26 @@ cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, size_t 
     return e;
   const UnitPlan plan = make_plan(rp, main_groups, (p.n_cols + kPN - 1) / kPN, 0, 1, 0, false);
   // A side unit (S pairs: the row pair's logits and S chunks' GEMM2) takes P (H + 256 S) / (S (H + 256 P))
-  // times as long as a main unit (P pairs: the logits once and P chunks' GEMM2) at equal rates per pair; the
-  // side begins a row pair only while the main launch has that many units per main cluster left, times
-  // reserve_quarters / 4 (measured per pass: the side pairs, with no hand-over to wait for, run faster per
-  // pair than the model says in the grad_input pass).
-  const long long num = static_cast<long long>(reserve_quarters) * P * (p.H + S * kHc) * res_main;
-  const long long den = 4ll * S * (p.H + P * kHc) * main_groups;
-  WorkQueue wq{a.work_q, a.side_count, kRoleMain, rp, main_groups, h_chunks / S,
-               static_cast<int>((num + den - 1) / den)};
+  // times as long as a main unit (P pairs: the logits once and P chunks' GEMM2) at equal rates per pair, and
+  // the same unit on a single pair (S times the logits and one chunk's GEMM2) S P (H + 256) / (H + 256 P)
+  // times; each launch begins a row pair only while the main launch has that many units per main cluster
+  // left, times its reserve quarters / 4 (measured per pass: the side pairs, with no hand-over to wait for,
+  // run faster per pair than the model says in the grad_input pass).
+  auto reserve_of = [&](long long quarters, long long time_num, long long time_den) {
+    const long long num = quarters * time_num * res_main;
+    const long long den = 4ll * time_den * main_groups;
+    return static_cast<int>((num + den - 1) / den);
+  };
+  WorkQueue wq{a.work_q, a.side_count, a.single_count, a.single_units, kRoleMain, rp, main_groups, h_chunks / S, S,
+               reserve_of(reserve_quarters, static_cast<long long>(P) * (p.H + S * kHc),
+                          static_cast<long long>(S) * (p.H + P * kHc))};
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cm =
       cluster_config(dim3(2 * P * std::min(res_main, rp * main_groups), 1, 1), smem_main, P, stream, attr);
   if ((e = cudaLaunchKernelEx(&cm, km, rows, cols, p, a.status, plan, wq)) != cudaSuccess) return e;
+  *launched = true;
+  // the side and single-pair launches are an optimisation: without them the main clusters claim every unit
+  // themselves (a launch that fails leaves the error cleared and the pass correct)
   PairParams ps = p;
   ps.P = S;
   WorkQueue wside = wq;
@@ -1766,13 +1814,28 @@ cudaError_t launch_corun(MainKernel km, size_t smem_main, SideKernel ks, size_t 
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cs.numAttrs = 2;
-  *launched = true;
   if (cudaLaunchKernelEx(&cs, ks, rows, cols, ps, a.status, plan, wside) != cudaSuccess) {
-    // the side launch is an optimisation: without it the main clusters claim every unit themselves
     (void)cudaGetLastError();
     return cudaSuccess;
   }
-  return cudaGetLastError();
+  if (single < 1 || reserve_quarters_single <= 0) return cudaSuccess;
+  if (cudaFuncSetAttribute(kx, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_side)) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return cudaSuccess;
+  }
+  PairParams px = p;
+  px.P = 1;
+  WorkQueue wsingle = wq;
+  wsingle.role = kRoleSingle;
+  wsingle.reserve = std::max(wq.reserve, reserve_of(reserve_quarters_single, static_cast<long long>(S) * P * (p.H + kHc),
+                                                    static_cast<long long>(p.H + P * kHc)));
+  cudaLaunchAttribute attr1[2];
+  cudaLaunchConfig_t cx = cluster_config(dim3(2 * single, 1, 1), smem_side, 1, stream, attr1);
+  attr1[1] = attr[1];
+  cx.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cx, kx, rows, cols, px, a.status, plan, wsingle) != cudaSuccess) (void)cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -1807,9 +1870,10 @@ cudaError_t launch_dgrad_pair(const CUtensorMap& rows, const CUtensorMap& cols, 
   if (four && !filt) {
     bool launched = false;
     e = launch_corun(dgrad_pair_kernel<kVocabRows, false, kFourPairSlots, 1, true>, smem,
-                     dgrad_pair_kernel<kVocabRows, false, 2, 4, true>, pair_smem_bytes<kVocabRows, false>(), res4, rows,
-                     cols, p, h_chunks, kVocabRows ? a.token_splits : 0,
-                     kVocabRows ? kReserveQuartersGradW : kReserveQuartersOnline, a, stream, &launched);
+                     dgrad_pair_kernel<kVocabRows, false, 2, 2, true>, dgrad_pair_kernel<kVocabRows, false, 2, 4, true>,
+                     pair_smem_bytes<kVocabRows, false>(), res4, rows, cols, p, h_chunks,
+                     kVocabRows ? a.token_splits : 0, kVocabRows ? kReserveQuartersGradW : kReserveQuartersOnline,
+                     kVocabRows ? kReserveQuartersSingleGradW : kReserveQuartersSingleOnline, a, stream, &launched);
     if (e != cudaSuccess || launched) return e;
   }
   UnitPlan plan = make_plan(rp, h_chunks / p.P, nt, 0, 1, 0, false);
@@ -1864,9 +1928,10 @@ cudaError_t launch_dgrad_online(const CUtensorMap& hidden_map, const CUtensorMap
   if (slots_of[p.P] == 0) slots_of[p.P] = resident_clusters(kern, smem, p.P, stream);
   if (four) {
     bool launched = false;
-    e = launch_corun(dgrad_online_kernel<kFourPairSlots, 1, true>, smem, dgrad_online_kernel<2, 4, true>,
-                     pair_smem_bytes<false, false>(), slots_of[4], hidden_map, w_map, p, h_chunks, a.vocab_splits,
-                     kReserveQuartersOnline, a, stream, &launched);
+    e = launch_corun(dgrad_online_kernel<kFourPairSlots, 1, true>, smem, dgrad_online_kernel<2, 2, true>,
+                     dgrad_online_kernel<2, 4, true>, pair_smem_bytes<false, false>(), slots_of[4], hidden_map, w_map,
+                     p, h_chunks, a.vocab_splits, kReserveQuartersOnline, kReserveQuartersSingleOnline, a, stream,
+                     &launched);
     if (e != cudaSuccess || launched) return e;
   }
   // vocabulary-split tail: the accumulators go to the split scratch (16 MiB),

@@ -469,6 +469,8 @@ FusedWorkspace carve_workspace(void* base, int64_t BT, int64_t V) {
   w.ts_count = reinterpret_cast<uint32_t*>(p + 32);
   w.work_q = reinterpret_cast<unsigned long long*>(p + 40);
   w.side_count = reinterpret_cast<uint32_t*>(p + 56);
+  w.single_units = reinterpret_cast<uint32_t*>(p + 64);
+  w.single_count = reinterpret_cast<uint32_t*>(p + 72);
   size_t off = 256;
   w.part = reinterpret_cast<float2*>(p + off);
   w.part_bytes = align_up(sizeof(float2) * kMaxSplits * btp, 256);

@@ -43,6 +43,10 @@ struct FusedWorkspace {
   unsigned long long* work_q;  // header: [2] work queues of the grad_input and grad_W passes (zeroed per call)
   uint32_t* side_count;        // header: [2] launches of side clusters beside the four-pair clusters, and
                                // side clusters that took at least one unit
+  uint32_t* single_units;      // header: [2] units the single-pair clusters took in the grad_input and
+                               // grad_W passes
+  uint32_t* single_count;      // header: [2] launches of single-pair clusters, and single-pair clusters
+                               // that took at least one unit
   uint32_t* zf_neg;  // header: non-zero when the log form of dS does not apply (some valid row has
                      // f u <= 0 with u its upstream gradient, or the gradient scale is <= 0)
   float2* part;      // [kMaxSplits][BTp] (max in log2 units, sum of 2^(x - max)); free again by the
@@ -167,12 +171,15 @@ struct DgPairArgs {
   size_t split_scratch_bytes;
   uint32_t* split_count;
   uint32_t debug_stall_us;   // test-only (flce_fwd_bwd_options.debug_stall_us)
-  // Shared work queue (a zeroed 64-bit word) for a pass run by persistent clusters of four pairs plus a
-  // second launch of smaller side clusters on the SMs they leave idle, or NULL (one cluster per unit);
-  // side_count: [2] incremented once per side launch, and once per side cluster that took a unit
-  // (workspace header)
+  // Shared work queue (a zeroed 64-bit word) for a pass run by persistent clusters of four pairs plus
+  // launches of smaller side and single-pair clusters on the SMs they leave idle, or NULL (one cluster
+  // per unit); side_count / single_count: [2] incremented once per side (single-pair) launch, and once
+  // per side (single-pair) cluster that took a unit; single_units: this pass's units taken by single-pair
+  // clusters (workspace header)
   unsigned long long* work_q;
   uint32_t* side_count;
+  uint32_t* single_count;
+  uint32_t* single_units;
 };
 
 // kVocabRows = false: grad_input pass (rows = tokens, reduction over the vocabulary);

@@ -75,6 +75,8 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
   pa.split_count = ws.ts_count;
   pa.work_q = ws.work_q + 1;     // (the grad_W pass; the gated classic grad_input pass takes none)
   pa.side_count = ws.side_count;
+  pa.single_count = ws.single_count;
+  pa.single_units = ws.single_units + 1;
   if (online) {
     // events: 1 after the bias table and count, 2 after the online grad_input pass, 3 after the loss
     // reduction and the gated classic passes, 4 after the grad_W pass
@@ -105,6 +107,7 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
     po.vs_o = ws.split_acc;
     po.vs_count = ws.vs_count;
     po.work_q = ws.work_q;
+    po.single_units = ws.single_units;
     if ((e = launch_dgrad_online(tm_h, tm_w, po, stream)) != cudaSuccess) return e;
     if ((e = mark(2)) != cudaSuccess) return e;
     if ((e = launch_loss_reduce(a, ws, stream)) != cudaSuccess) return e;
@@ -146,7 +149,8 @@ cudaError_t launch_fused(const FusedArgs& args, void* workspace, int num_sms, cu
   }
   if (a.grad_input != nullptr) {
     DgPairArgs pi = pa;
-    pi.work_q = ws.work_q;   // each pass has its own queue word
+    pi.work_q = ws.work_q;   // each pass has its own queue word (and count of single-pair units)
+    pi.single_units = ws.single_units;
     if ((e = launch_dgrad_pair<false>(tm_h128, tm_w128, pi, stream)) != cudaSuccess) return e;
   }
   if ((e = mark(3)) != cudaSuccess) return e;

@@ -262,16 +262,19 @@ def test_flce_persistent_with_side_clusters_sorted_vocab(flce):
 
 def test_flce_short_units_four_pairs_with_side_clusters(flce):
     """A grad_W pass of short units (17 token blocks, under the 64 that four pairs otherwise need) with
-    enough vocabulary row pairs (51: three waves of 15, or of 16, resident 8-CTA clusters) runs four pairs
-    per cluster, persistent, with side clusters: against
-    the oracle, and against the same pass with one two-pair cluster per unit (the grad_input pass
-    unsplit in both, so that both grad_W passes read the same statistics)."""
+    enough vocabulary row pairs (118: more than the 75 above the main clusters' that the single-pair
+    clusters keep in reserve, beside 15 resident 8-CTA clusters) runs four pairs per cluster, persistent,
+    with side and single-pair clusters: against the oracle, and against the same pass with one two-pair
+    cluster per unit (the grad_input pass unsplit in both, so that both grad_W passes read the same
+    statistics)."""
     import torch
-    BT, H, V = 4100, 1024, 13000
+    BT, H, V = 4100, 1024, 30000
     d = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(1, BT - 1), seed=47)
     out = _run(flce, d, vocab_splits=1)
     assert out["status"] == 0
     assert flce.read_side_launches(out["workspace"]) == 1, "the grad_W pass did not run with side clusters"
+    assert flce.read_single_launches(out["workspace"]) == 1
+    assert flce.read_single_units(out["workspace"])[1] > 0, "the single-pair clusters took no unit"
     _check_full(out, d)
     plain = _run(flce, d, vocab_splits=1, token_splits=1)
     assert plain["status"] == 0 and flce.read_side_launches(plain["workspace"]) == 0
@@ -280,6 +283,29 @@ def test_flce_short_units_four_pairs_with_side_clusters(flce):
     # partial sums in another grouping, so it is compared within the parity bound)
     assert torch.equal(out["grad_W"], plain["grad_W"])
     assert_grad_close(out["grad_bias"].cpu().numpy(), plain["grad_bias"].cpu().numpy().astype(np.float64), "grad_bias")
+
+
+def test_flce_single_pair_clusters_grad_W(flce):
+    """The grad_W pass with enough vocabulary row pairs (102) for the single-pair clusters to take units
+    (each a row pair's two H chunks, one at a time, keeping the four pairs' owner-class sums apart): against
+    the oracle element by element, and bit for bit against one four-pair cluster per unit (65 token
+    blocks, so that the one-unit run has four pairs per cluster too).  The grad_input pass runs with side
+    clusters only."""
+    import torch
+    BT, H, V = 16400, 1024, 26000
+    d = _synthetic(BT, H, V, True, 1e-4, "mean", ignore=(2, BT - 2), seed=59)
+    out = _run(flce, d)
+    assert out["status"] == 0
+    assert flce.read_side_launches(out["workspace"]) == 2 and flce.read_single_launches(out["workspace"]) == 1
+    units = flce.read_single_units(out["workspace"])
+    assert units[0] == 0 and units[1] > 0, f"single-pair units per pass: {units}"
+    assert flce.read_single_clusters(out["workspace"]) > 0
+    _check_full(out, d)
+    plain = _run(flce, d, vocab_splits=1, token_splits=1)
+    assert plain["status"] == 0 and flce.read_single_launches(plain["workspace"]) == 0
+    for k in ("grad_input", "grad_W", "grad_bias"):
+        assert torch.equal(out[k], plain[k]), f"{k} differs from one cluster per unit"
+    assert out["loss"].item() == plain["loss"].item()
 
 
 def test_flce_persistent_side_clusters_options(flce):
@@ -573,6 +599,8 @@ def test_flce_full_size_sampled(flce, key):
     assert flce.read_vocab_split_units(out["workspace"]) > 0 or side > 0
     if key == "long":
         assert side == 2, "both passes of the long workload run with side clusters beside"
+        assert flce.read_single_launches(out["workspace"]) == 1, "the grad_W pass launches single-pair clusters"
+        assert flce.read_single_units(out["workspace"])[1] > 0, "the single-pair clusters took no unit"
     rows = torch.from_numpy(exp["rows"]).cuda()
     vr = torch.from_numpy(exp["vocab_rows"]).cuda()
     check_full_size_rows(exp, bf16_to_numpy_f32(out["grad_input"][rows]), out["grad_W"][vr].cpu().numpy(),
