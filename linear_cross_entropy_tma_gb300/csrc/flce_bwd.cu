@@ -442,6 +442,94 @@ __device__ __forceinline__ PairSmem<kVocabRows, kFilter, kSlots>* pair_smem_of()
   return reinterpret_cast<PairSmem<kVocabRows, kFilter, kSlots>*>(base);
 }
 
+// Work queue of a pass run by persistent clusters (word != null): the main launch's clusters of four
+// pairs take whole units (row pair x H group) from the bottom of the row pairs; a second launch of
+// side clusters of S pairs (the side launch, on the SMs the main launch leaves idle; S = side_pairs_for(P))
+// takes units of one row pair and S 256-wide H chunks from the top, computing that row pair's logits once
+// per S chunks; a third launch of single-pair clusters (on the SMs where no side cluster finds room) takes
+// the same units as the side launch, from the same count, and runs each as S one-chunk units in turn,
+// computing the logits once per chunk; it takes a unit only with its own reserve to spare, also one that
+// continues a row pair a side cluster began, and stops at the first it cannot take.  One 64-bit word holds both counts (main units claimed | side
+// units claimed << 32), so that a row pair is never split between the main launch and the others.  The
+// side and single-pair clusters open a new row pair only while the main launch has at least `reserve`
+// row pairs left (each launch its own): enough to keep it busy while they finish that row pair.
+enum : int { kRoleMain = 1, kRoleSide = 2, kRoleSingle = 3 };
+struct WorkQueue {
+  unsigned long long* word;   // zeroed before the pass; null: one cluster per unit (blockIdx), no queue
+  uint32_t* side_count;       // [2] side launches that ran, side clusters that took a unit (workspace
+                              // header), or null
+  uint32_t* single_count;     // [2] the same for the single-pair launches, or null
+  uint32_t* single_units;     // this pass's units taken by single-pair clusters, or null
+  int role;
+  int row_pairs;
+  int main_groups;            // H groups per row pair of a main unit (h_chunks / 4)
+  int side_groups;            // H groups per row pair of a side unit (h_chunks / S)
+  int side_chunks;            // S: H chunks per side unit
+  int reserve;
+};
+
+// The next unit for this launch's role, -1 when there is none left for it, -2 when the compare-and-swap
+// did not settle (the caller flags the status; with a few dozen clusters claiming every few hundred
+// microseconds it always settles at once).
+__device__ __forceinline__ int claim_unit(const WorkQueue& q) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(q.word);
+  for (int tries = 0; tries < (1 << 16); ++tries) {
+    const int a = static_cast<int>(cur & 0xffffffffull);
+    const int b = static_cast<int>(cur >> 32);
+    const int a_rows = (a + q.main_groups - 1) / q.main_groups;   // row pairs the main launch has begun
+    const int b_rows = (b + q.side_groups - 1) / q.side_groups;   // row pairs the side launch has begun
+    unsigned long long next;
+    if (q.role == kRoleMain) {
+      if (a / q.main_groups >= q.row_pairs - b_rows) return -1;
+      next = cur + 1ull;
+    } else {
+      // (side: a row pair already begun is always finished, a new one only with `reserve` row pairs to
+      // spare; single-pair: every unit only with its reserve to spare, which is at least the side's, so
+      // that a side cluster is always there to finish a row pair it began)
+      const bool check = q.role == kRoleSingle || b % q.side_groups == 0;
+      if (check && (q.row_pairs - 1 - b / q.side_groups) - a_rows < q.reserve) return -1;
+      next = cur + (1ull << 32);
+    }
+    const unsigned long long seen = atomicCAS(q.word, cur, next);
+    if (seen == cur) return q.role == kRoleMain ? a : b;
+    cur = seen;
+  }
+  return -2;
+}
+
+// Rank 0's claim of its cluster's next unit, handed to every CTA of the cluster (sm.claim) as
+// claim x n_sub + part, or -1 for none: once by thread 0 before the first unit, then by the MMA issuer of
+// each unit once its last MMA has completed, so that the claim's atomic overlaps the unit's accumulator
+// drain; every CTA reads it after the unit's last cluster barrier.  A single-pair cluster runs each side
+// unit it claims as n_sub = side_chunks one-chunk units in turn.  Nothing more is claimed once the pass's
+// status holds a timeout or (check_abort) a CTA of the cluster gave up on a wait in this unit.  The state
+// (q_unit, q_sub, q_took) lives in rank 0's shared memory, touched by one thread between cluster barriers.
+template <class Smem>
+__device__ __forceinline__ void claim_next(Smem& sm, const WorkQueue& wq, uint32_t* status, int n_ctas,
+                                           bool check_abort) {
+  const int n_sub = wq.role == kRoleSingle ? wq.side_chunks : 1;
+  const int sub = sm.q_sub;
+  if (sub == 0) {
+    bool stop = (*reinterpret_cast<volatile uint32_t*>(status) & kStatusTimeout) != 0u;
+    for (int r = 0; r < n_ctas && check_abort && !stop; ++r)
+      stop = ld_shared_cluster_u32(mapa_shared(smem_u32(&sm.abort), static_cast<uint32_t>(r))) != 0u;
+    int cl = stop ? -1 : claim_unit(wq);
+    if (cl == -2) {
+      atomicOr(status, kStatusInternal);
+      cl = -1;
+    }
+    uint32_t* const counts = wq.role == kRoleSide ? wq.side_count : wq.role == kRoleSingle ? wq.single_count : nullptr;
+    if (cl >= 0 && !sm.q_took && counts != nullptr) atomicAdd(counts + 1, 1u);
+    if (cl >= 0 && wq.role == kRoleSingle && wq.single_units != nullptr) atomicAdd(wq.single_units, 1u);
+    if (cl >= 0) sm.q_took = 1;
+    sm.q_unit = cl;
+  }
+  sm.q_sub = sub + 1 == n_sub ? 0 : sub + 1;
+  const int v = sm.q_unit < 0 ? -1 : sm.q_unit * n_sub + sub;
+  for (int r = 0; r < n_ctas; ++r)
+    st_shared_cluster_u32(mapa_shared(smem_u32(&sm.claim), static_cast<uint32_t>(r)), static_cast<uint32_t>(v));
+}
+
 // TMEM of a dgrad_pair_body call: allocated and freed by it (one unit per CTA), or held by the caller
 // across the units of a persistent CTA.  (Allocating inside the body keeps the one-unit kernels' register
 // allocation as it was.)
@@ -468,7 +556,7 @@ __device__ __forceinline__ float slot_sum(float a0, float a1, float a2, float a3
 template <bool kVocabRows, bool kFilter, bool kOnline = false, int kSlots = 2, int kOwn = 1, int kTmem = 0>
 __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols,
                                                 const PairParams& p, uint32_t* __restrict__ status, int row_pair,
-                                                int hgroup, int jb = 0, int je = -1, int su = -1) {
+                                                int hgroup, int jb, int je, int su, const WorkQueue& wq) {
   static_assert(!kOnline || (!kVocabRows && !kFilter), "the online form is a grad_input pass without the filter");
   static_assert(kOwn == 1 || ((kOwn == 2 || kOwn == 4) && !kFilter),
                 "owner-class sums per pair: 1, or 2 / 4 (two-pair / single-pair clusters) for the exact passes");
@@ -749,6 +837,9 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       if (ok) mma_commit_mc(&sm.o_full, pair_mask);
       mma_commit_mc(&sm.drain, pair_mask);
       mbar_wait_drain(&sm.drain, 0);
+      // persistent cluster of the grad_W pass: the next unit's claim, while the epilogue drains the
+      // accumulator
+      if (kTmem == kTmemHeld && kVocabRows && rank == 0) claim_next(sm, wq, status, 2 * P, true);
     }
   } else if (warp == kRecvWarp) {
     // ---------------------------------------- dS halves of blocks computed by the other pairs
@@ -1242,67 +1333,13 @@ __device__ __forceinline__ Unit unit_of(const UnitPlan& plan, int c) {
   return u;
 }
 
-// Work queue of a pass run by persistent clusters (word != null): the main launch's clusters of four
-// pairs take whole units (row pair x H group) from the bottom of the row pairs; a second launch of
-// side clusters of S pairs (the side launch, on the SMs the main launch leaves idle; S = side_pairs_for(P))
-// takes units of one row pair and S 256-wide H chunks from the top, computing that row pair's logits once
-// per S chunks; a third launch of single-pair clusters (on the SMs where no side cluster finds room) takes
-// the same units as the side launch, from the same count, and runs each as S one-chunk units in turn,
-// computing the logits once per chunk; it takes a unit only with its own reserve to spare, also one that
-// continues a row pair a side cluster began, and stops at the first it cannot take.  One 64-bit word holds both counts (main units claimed | side
-// units claimed << 32), so that a row pair is never split between the main launch and the others.  The
-// side and single-pair clusters open a new row pair only while the main launch has at least `reserve`
-// row pairs left (each launch its own): enough to keep it busy while they finish that row pair.
-enum : int { kRoleMain = 1, kRoleSide = 2, kRoleSingle = 3 };
-struct WorkQueue {
-  unsigned long long* word;   // zeroed before the pass; null: one cluster per unit (blockIdx), no queue
-  uint32_t* side_count;       // [2] side launches that ran, side clusters that took a unit (workspace
-                              // header), or null
-  uint32_t* single_count;     // [2] the same for the single-pair launches, or null
-  uint32_t* single_units;     // this pass's units taken by single-pair clusters, or null
-  int role;
-  int row_pairs;
-  int main_groups;            // H groups per row pair of a main unit (h_chunks / 4)
-  int side_groups;            // H groups per row pair of a side unit (h_chunks / S)
-  int side_chunks;            // S: H chunks per side unit
-  int reserve;
-};
-
-// The next unit for this launch's role, -1 when there is none left for it, -2 when the compare-and-swap
-// did not settle (the caller flags the status; with a few dozen clusters claiming every few hundred
-// microseconds it always settles at once).
-__device__ __forceinline__ int claim_unit(const WorkQueue& q) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(q.word);
-  for (int tries = 0; tries < (1 << 16); ++tries) {
-    const int a = static_cast<int>(cur & 0xffffffffull);
-    const int b = static_cast<int>(cur >> 32);
-    const int a_rows = (a + q.main_groups - 1) / q.main_groups;   // row pairs the main launch has begun
-    const int b_rows = (b + q.side_groups - 1) / q.side_groups;   // row pairs the side launch has begun
-    unsigned long long next;
-    if (q.role == kRoleMain) {
-      if (a / q.main_groups >= q.row_pairs - b_rows) return -1;
-      next = cur + 1ull;
-    } else {
-      // (side: a row pair already begun is always finished, a new one only with `reserve` row pairs to
-      // spare; single-pair: every unit only with its reserve to spare, which is at least the side's, so
-      // that a side cluster is always there to finish a row pair it began)
-      const bool check = q.role == kRoleSingle || b % q.side_groups == 0;
-      if (check && (q.row_pairs - 1 - b / q.side_groups) - a_rows < q.reserve) return -1;
-      next = cur + (1ull << 32);
-    }
-    const unsigned long long seen = atomicCAS(q.word, cur, next);
-    if (seen == cur) return q.role == kRoleMain ? a : b;
-    cur = seen;
-  }
-  return -2;
-}
-
 // A CTA's gradient work: TMEM allocated once, then the one unit `fixed` (kQueue false), or (kQueue) the
-// units it claims from the work queue, CTA 0 of the cluster claiming and handing the index to every CTA,
-// until none is left.  The barriers are initialised again for every unit: dgrad_pair_body ends with
-// every arrival on them consumed or ordered before its last cluster barrier.  A unit that gave up on a
-// wait stops the cluster.  (A template flag rather than a run-time one, so that the one-unit kernels keep
-// their register allocation.)
+// units it claims from the work queue, CTA 0 of the cluster claiming and handing the index to every CTA
+// (claim_next: the first before any unit, each next one during the unit before it), until none is left.
+// The barriers are initialised again for every unit: dgrad_pair_body ends with every arrival on them
+// consumed or ordered before its last cluster barrier, which also orders the next claim before every
+// CTA reads it.  A unit that gave up on a wait stops the cluster.  (A template flag rather than a run-time
+// one, so that the one-unit kernels keep their register allocation.)
 template <bool kVocabRows, bool kFilter, bool kOnline, int kSlots, int kOwn, bool kQueue>
 __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUtensorMap& tm_cols, const PairParams& p,
                                           uint32_t* __restrict__ status, const Unit& fixed, const UnitPlan& plan,
@@ -1317,7 +1354,7 @@ __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUte
   if constexpr (!kQueue) {
     // (the body allocates and frees TMEM itself)
     dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kOwn, kTmemOneUnit>(
-        tm_rows, tm_cols, p, status, fixed.row_pair, fixed.hgroup, fixed.jb, fixed.je, fixed.su);
+        tm_rows, tm_cols, p, status, fixed.row_pair, fixed.hgroup, fixed.jb, fixed.je, fixed.su, wq);
   } else {
     auto& sm = *smp;
     if ((threadIdx.x >> 5) == kMmaWarp) {
@@ -1329,44 +1366,65 @@ __device__ __forceinline__ void run_units(const CUtensorMap& tm_rows, const CUte
     uint32_t* const counts = wq.role == kRoleSide ? wq.side_count : wq.role == kRoleSingle ? wq.single_count : nullptr;
     if (blockIdx.x == 0 && threadIdx.x == 0 && counts != nullptr) atomicAdd(counts, 1u);
     const uint32_t rank = cluster_ctarank();
-    // a single-pair cluster runs each side unit it claims as side_chunks one-chunk units in turn (one call
-    // site of the body, so that the register allocation stays that of one unit); CTA 0 hands out
-    // claim x n_sub + part
     const int n_sub = wq.role == kRoleSingle ? wq.side_chunks : 1;
     if (rank == 0 && threadIdx.x == 0) {
       sm.q_sub = 0;
       sm.q_took = 0;
     }
-    for (;;) {
-      if (rank == 0 && threadIdx.x == 0) {
-        const int sub = sm.q_sub;
-        if (sub == 0) {
-          int cl = (*reinterpret_cast<volatile uint32_t*>(status) & kStatusTimeout) != 0u ? -1 : claim_unit(wq);
-          if (cl == -2) {
-            atomicOr(status, kStatusInternal);
-            cl = -1;
-          }
-          if (cl >= 0 && !sm.q_took && counts != nullptr) atomicAdd(counts + 1, 1u);
-          if (cl >= 0 && wq.role == kRoleSingle && wq.single_units != nullptr) atomicAdd(wq.single_units, 1u);
-          if (cl >= 0) sm.q_took = 1;
-          sm.q_unit = cl;
-        }
-        sm.q_sub = sub + 1 == n_sub ? 0 : sub + 1;
-        const int v = sm.q_unit < 0 ? -1 : sm.q_unit * n_sub + sub;
-        for (int r = 0; r < 2 * p.P; ++r)
-          st_shared_cluster_u32(mapa_shared(smem_u32(&sm.claim), static_cast<uint32_t>(r)), static_cast<uint32_t>(v));
+    // The grad_W pass (units of BT / 256 blocks: short ones at small BT) claims each next unit inside the
+    // unit before it, while the accumulator drains (claim_next in dgrad_pair_body): 2.70 -> 2.64 ms for
+    // qwen3's pass of 16-block units.  The grad_input pass claims between its units, behind one more
+    // cluster barrier: its units are long, and with the claim inside its body, or the claim's code shared
+    // with the grad_W pass, its kernel compiled to one that took 0.1-0.2 ms longer at the long workload.
+    if constexpr (kVocabRows) {
+      if (rank == 0 && threadIdx.x == 0) claim_next(sm, wq, status, 2 * p.P, false);
+      cluster_sync();
+      for (;;) {
+        // (the unit's claim: written by CTA 0 before the cluster barrier above, or before the previous
+        // unit's last one; the next claim is written only after this unit's first cluster barrier)
+        const int v = *reinterpret_cast<volatile int*>(&sm.claim);
+        if (v < 0) break;
+        const int c = v / n_sub;
+        const Unit u = wq.role == kRoleMain ? Unit{c / wq.main_groups, c % wq.main_groups, 0, plan.nt, -1}
+                                            : Unit{wq.row_pairs - 1 - c / wq.side_groups,
+                                                   (c % wq.side_groups) * n_sub + v % n_sub, 0, plan.nt, -1};
+        // (the body ends with a cluster barrier after every access of the unit's barriers, TMEM and
+        // shared memory by the other CTAs, so the next unit may initialise them at once)
+        dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kOwn, kTmemHeld>(
+            tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je, u.su, wq);
       }
-      cluster_sync();
-      const int v = *reinterpret_cast<volatile int*>(&sm.claim);
-      if (v < 0) break;
-      const int c = v / n_sub;
-      const Unit u = wq.role == kRoleMain ? Unit{c / wq.main_groups, c % wq.main_groups, 0, plan.nt, -1}
-                                          : Unit{wq.row_pairs - 1 - c / wq.side_groups,
-                                                 (c % wq.side_groups) * n_sub + v % n_sub, 0, plan.nt, -1};
-      dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kOwn, kTmemHeld>(tm_rows, tm_cols, p, status, u.row_pair,
-                                                                             u.hgroup, u.jb, u.je, u.su);
-      // every CTA is done with the unit (and has read sm.claim) before the next claim is handed out
-      cluster_sync();
+    } else {
+      for (;;) {
+        if (rank == 0 && threadIdx.x == 0) {
+          const int sub = sm.q_sub;
+          if (sub == 0) {
+            int cl = (*reinterpret_cast<volatile uint32_t*>(status) & kStatusTimeout) != 0u ? -1 : claim_unit(wq);
+            if (cl == -2) {
+              atomicOr(status, kStatusInternal);
+              cl = -1;
+            }
+            if (cl >= 0 && !sm.q_took && counts != nullptr) atomicAdd(counts + 1, 1u);
+            if (cl >= 0 && wq.role == kRoleSingle && wq.single_units != nullptr) atomicAdd(wq.single_units, 1u);
+            if (cl >= 0) sm.q_took = 1;
+            sm.q_unit = cl;
+          }
+          sm.q_sub = sub + 1 == n_sub ? 0 : sub + 1;
+          const int v = sm.q_unit < 0 ? -1 : sm.q_unit * n_sub + sub;
+          for (int r = 0; r < 2 * p.P; ++r)
+            st_shared_cluster_u32(mapa_shared(smem_u32(&sm.claim), static_cast<uint32_t>(r)), static_cast<uint32_t>(v));
+        }
+        cluster_sync();
+        const int v = *reinterpret_cast<volatile int*>(&sm.claim);
+        if (v < 0) break;
+        const int c = v / n_sub;
+        const Unit u = wq.role == kRoleMain ? Unit{c / wq.main_groups, c % wq.main_groups, 0, plan.nt, -1}
+                                            : Unit{wq.row_pairs - 1 - c / wq.side_groups,
+                                                   (c % wq.side_groups) * n_sub + v % n_sub, 0, plan.nt, -1};
+        dgrad_pair_body<kVocabRows, kFilter, kOnline, kSlots, kOwn, kTmemHeld>(
+            tm_rows, tm_cols, p, status, u.row_pair, u.hgroup, u.jb, u.je, u.su, wq);
+        // every CTA is done with the unit (and has read sm.claim) before the next claim is handed out
+        cluster_sync();
+      }
     }
     // a side grid completes only after the main grid beside it, a single-pair grid only after the side grid
     // (and so the main grid), so that what follows on the stream sees all of them

@@ -321,6 +321,12 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
 // Programmatic dependent launch: the next launch on the stream that asked for it may start once every CTA
 // of this grid has executed launch_dependents (or exited); wait_primary blocks until the grid it depends on
 // has completed and its memory operations are visible.

@@ -52,3 +52,41 @@ def test_wait_that_gives_up_reports_timeout_and_next_call_is_correct(separate):
     assert_grad_close(bf16_to_numpy_f32(res["grad_input"]), ref["grad_input"], "grad_input")
     assert_grad_close(res["grad_W"].cpu().numpy(), ref["grad_W"], "grad_W")
     assert_grad_close(res["grad_bias"].cpu().numpy(), ref["grad_bias"], "grad_bias")
+
+
+def test_wait_that_gives_up_in_persistent_clusters():
+    """The same in a pass run by persistent clusters: the grad_W pass of this shape (118 vocabulary row
+    pairs of 17 token blocks) runs four-pair clusters with side and single-pair clusters beside them.
+    Every unit's producer stalls, so every cluster gives up in its first unit; the claim of a next unit
+    then sees the abort and the cluster stops.  The call reports the timeout within a fraction of a second,
+    and the next call gives the results of a call before it bit for bit."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for -m gpu tests")
+    import linear_cross_entropy_tma_gb300 as flce
+    flce.load()
+    w = wl.FusedWorkload("timeout-persistent", BT=4100, H=1024, V=30000, bias_std=0.1, ignore_frac=0.05,
+                         z_loss=1e-4, seed=37)
+    d = wl.make_fused_inputs(w)
+    hidden, W = bf16_tensor(d["hidden"]), bf16_tensor(d["W"])
+    target = torch.from_numpy(d["target"]).cuda()
+    bias = torch.from_numpy(d["bias"]).cuda()
+    kw = dict(bias=bias, z_loss=w.z_loss)
+    first = flce.flce_fwd_bwd(hidden, W, target, **kw)
+    torch.cuda.synchronize()
+    ws = first["workspace"]
+    assert flce.read_device_status(ws) == 0
+    assert flce.read_side_launches(ws) == 1 and flce.read_single_launches(ws) == 1
+    res = {k: v for k, v in first.items() if k in ("loss", "n_valid", "grad_input", "grad_W", "grad_bias")}
+    before = {k: v.clone() for k, v in res.items()}
+    t0 = time.perf_counter()
+    flce.flce_fwd_bwd(hidden, W, target, workspace=ws, out=res, debug_stall_us=2000, **kw)
+    st = flce.read_device_status(ws)
+    dt = time.perf_counter() - t0
+    assert st & flce.STATUS_TIMEOUT, f"status {st:#x}: the stalled wait did not report a timeout"
+    assert dt < 1.0, f"the stalled call took {dt:.3f} s"
+    flce.flce_fwd_bwd(hidden, W, target, workspace=ws, out=res, **kw)
+    assert flce.read_device_status(ws) == 0
+    assert flce.read_side_launches(ws) == 1
+    for k, v in before.items():
+        assert torch.equal(res[k], v), f"{k} differs after the stalled call"
