@@ -77,6 +77,9 @@ constexpr uint32_t kBox = kTileM * kBK * 2;   // 16 KiB: a 128-row x 64-column b
 constexpr uint32_t kStage = 2 * kBox;
 constexpr uint32_t kHalfBytes = 2 * kBox;     // one 128-column half of a dS block (per CTA)
 constexpr uint32_t kDsBytes = 2 * kHalfBytes;
+// grad_W drain: each epilogue warp stages 32 rows of 512 bytes in the operand stages and dS slots, 16
+// bytes apart so that the lanes' 16-byte stores meet the fewest bank conflicts
+constexpr uint32_t kDrainRowBytes = 512 + 16;
 constexpr int kEpiWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -153,6 +156,13 @@ static_assert(pair_smem_bytes<true, false, 4>() <= kSmemBudget, "shared memory b
 static_assert(pair_smem_bytes<false, false, 3>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
 static_assert(pair_smem_bytes<true, false, 3>() <= kSmemBudget, "shared memory budget of one CTA exceeded");
 static_assert(sizeof(float) * kMaxPairs * 2 * kTileM <= kDsBytes, "the dS block gathers the grad_bias partials");
+template <bool kVocabRows, bool kFilter, int kSlots>
+constexpr bool drain_fits() {
+  using S = PairSmem<kVocabRows, kFilter, kSlots>;
+  return offsetof(S, ds) == sizeof(S::stage) && sizeof(S::stage) + sizeof(S::ds) >= size_t{kEpiWarps} * 32 * kDrainRowBytes;
+}
+static_assert(drain_fits<true, false, 2>() && drain_fits<true, true, 2>() && drain_fits<true, false, 4>(),
+              "the grad_W drain stages 8 warps x 32 rows in the operand stages and dS slots");
 
 // Gradient filter: the verdict on half `half` of block j, once the 8 epilogue warps of its owner pair that
 // hold the half (4 per CTA) have published theirs: 1 = every pair skips it (no operand stage, no MMA, no
@@ -1159,7 +1169,37 @@ __device__ __forceinline__ void dgrad_pair_body(const CUtensorMap& tm_rows, cons
       }
     }
 
-    if (ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_full, 0, abort))) {
+    const bool o_ready = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_full, 0, abort));
+    if (o_ready && kVocabRows && su < 0) {
+      // grad_W rows: this warp's 32 rows x the 128 columns of half hh, staged in the operand stages and dS
+      // slots (free: every MMA of the pair has completed, every dS sent here has been consumed, and the
+      // producer issues nothing more in this unit), then one bulk copy per row, a bulk reduce-add when
+      // accumulating (old + new, as the register path adds them); the copies have read the stage before
+      // the cluster barrier after which the grad_bias gather reuses it
+      tc_fence_after();
+      const int n_chunks = (hc + 31) / 32;
+      uint8_t* const my_row = &sm.stage[0][0] + (static_cast<size_t>(warp) * 32 + lane) * kDrainRowBytes;
+      for (int c = 4 * hh; c < 4 * hh + 4 && c < n_chunks; ++c) {
+        uint32_t vv[32];
+        tmem_ld_32cols(tmem + (static_cast<uint32_t>(qq * 32) << 16) + kTmemO + 32u * c, vv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int g4 = 0; g4 < 8; ++g4)
+          *reinterpret_cast<uint4*>(my_row + (c - 4 * hh) * 128 + 16 * g4) =
+              make_uint4(vv[4 * g4], vv[4 * g4 + 1], vv[4 * g4 + 2], vv[4 * g4 + 3]);
+      }
+      const int ncols = min(128, hc - 128 * hh);   // this half's columns inside H (a multiple of 8)
+      if (row < p.V && p.grad_W != nullptr && ncols > 0) {
+        fence_proxy_async_smem();
+        const int orow = p.row_perm != nullptr ? p.row_perm[row] : row;
+        float* const out = p.grad_W + static_cast<size_t>(orow) * p.H + h0 + 128 * hh;
+        if (p.accumulate)
+          bulk_add_f32_1d(out, my_row, 4u * static_cast<uint32_t>(ncols));
+        else
+          bulk_store_1d(out, my_row, 4u * static_cast<uint32_t>(ncols));
+        bulk_commit_wait_read();
+      }
+    } else if (o_ready) {
       tc_fence_after();
       const int n_chunks = (hc + 31) / 32;
       for (int c = hh; c < n_chunks; c += 2) {
