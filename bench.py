@@ -85,11 +85,37 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def strip_comments(src: str) -> str:
+    """C/CUDA source without its comments, every run of white space made one space (string and character
+    literals kept), so that a digest of it changes with the code's tokens only."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest(files):
+    """Digest of the kernel sources' code (comments and layout stripped): the key under which
+    profiles/traffic.json stores the DRAM counters taken on that code."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "linear_cross_entropy_tma_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "linear_cross_entropy_tma_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

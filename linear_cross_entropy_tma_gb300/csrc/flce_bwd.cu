@@ -130,8 +130,9 @@ struct PairSmem {
   uint32_t tmem_base;
   int abort;
   int claim;                  // persistent clusters: the unit CTA 0 claimed for the whole cluster (-1: none)
-  // persistent clusters, thread 0 of CTA 0 only (kept here so that nothing stays live across the unit body):
-  // its last claim, the next one-chunk part of it (single-pair clusters), whether the cluster took a unit
+  // persistent clusters, CTA 0 only, one thread at a time between cluster barriers (claim_next; kept here
+  // so that nothing stays live across the unit body): its last claim, the next one-chunk part of it
+  // (single-pair clusters), whether the cluster took a unit
   int q_unit, q_sub, q_took;
 };
 constexpr size_t kSmemBudget = 232448;
@@ -159,7 +160,8 @@ static_assert(sizeof(float) * kMaxPairs * 2 * kTileM <= kDsBytes, "the dS block 
 template <bool kVocabRows, bool kFilter, int kSlots>
 constexpr bool drain_fits() {
   using S = PairSmem<kVocabRows, kFilter, kSlots>;
-  return offsetof(S, ds) == sizeof(S::stage) && sizeof(S::stage) + sizeof(S::ds) >= size_t{kEpiWarps} * 32 * kDrainRowBytes;
+  return offsetof(S, ds) == sizeof(S::stage) &&
+         sizeof(S::stage) + sizeof(S::ds) >= size_t{kEpiWarps} * 32 * kDrainRowBytes;
 }
 static_assert(drain_fits<true, false, 2>() && drain_fits<true, true, 2>() && drain_fits<true, false, 4>(),
               "the grad_W drain stages 8 warps x 32 rows in the operand stages and dS slots");
@@ -458,11 +460,12 @@ __device__ __forceinline__ PairSmem<kVocabRows, kFilter, kSlots>* pair_smem_of()
 // takes units of one row pair and S 256-wide H chunks from the top, computing that row pair's logits once
 // per S chunks; a third launch of single-pair clusters (on the SMs where no side cluster finds room) takes
 // the same units as the side launch, from the same count, and runs each as S one-chunk units in turn,
-// computing the logits once per chunk; it takes a unit only with its own reserve to spare, also one that
-// continues a row pair a side cluster began, and stops at the first it cannot take.  One 64-bit word holds both counts (main units claimed | side
+// computing the logits once per chunk.  One 64-bit word holds both counts (main units claimed | side
 // units claimed << 32), so that a row pair is never split between the main launch and the others.  The
-// side and single-pair clusters open a new row pair only while the main launch has at least `reserve`
-// row pairs left (each launch its own): enough to keep it busy while they finish that row pair.
+// side clusters open a new row pair only while the main launch has at least `reserve` row pairs left:
+// enough to keep it busy while they finish that row pair.  The single-pair clusters take any unit, also
+// one that continues a row pair a side cluster began, only with their own (larger) reserve to spare, and
+// stop at the first they cannot take.
 enum : int { kRoleMain = 1, kRoleSide = 2, kRoleSingle = 3 };
 struct WorkQueue {
   unsigned long long* word;   // zeroed before the pass; null: one cluster per unit (blockIdx), no queue
@@ -546,8 +549,8 @@ __device__ __forceinline__ void claim_next(Smem& sm, const WorkQueue& wq, uint32
 enum : int { kTmemOneUnit = 0, kTmemHeld = 1 };
 
 // kOwn = A > 1 in dgrad_pair_body: a pair of a cluster of P = 4 / A pairs keeps A running sums, one per
-// owner class of a four-pair cluster it meets (its t-th block, j = pr + t P, belongs to class j mod 4 = pr + (t mod
-// A) P), rotating them so that a0 always holds the current block's.  After its n_own blocks, a_i holds
+// owner class of a four-pair cluster it meets (its t-th block, j = pr + t P, belongs to class
+// j mod 4 = pr + (t mod A) P), rotating them so that a0 always holds the current block's.  After its n_own blocks, a_i holds
 // slot (n_own - 1 + i) mod A; slot_sum returns slot s.  A slot that met no block holds 0.
 __device__ __forceinline__ float slot_sum(float a0, float a1, float a2, float a3, int s, int n_own, int A) {
   const int i = (((s - (n_own - 1)) % A) + A) % A;
